@@ -1,0 +1,218 @@
+"""fp64 CPU oracle for exact scaled dot-product attention (test infrastructure).
+
+Only the test-suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product library (the CUDA path in
+``io_aware_exact_09_gb300``) never imports it, and this package never imports
+the product library: the two share no code.
+
+The arithmetic lives in ``fa_oracle.c`` (plain C, fp64, OpenMP over rows);
+this module only builds it with gcc and marshals numpy arrays through ctypes.
+``online.py`` holds the pages' two-block merge identity and ``io_model.py``
+the page-2 traffic/time model.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "fa_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile fa_oracle.c into liboracle.so beside it (gcc, -O3, OpenMP)."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + ".tmp.%d" % os.getpid()
+    cmd = ["gcc", "-O3", "-std=c99", "-fopenmp", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            dp = ctypes.POINTER(ctypes.c_double)
+            ip = ctypes.POINTER(ctypes.c_int32)
+            bp = ctypes.POINTER(ctypes.c_uint8)
+            lp = ctypes.POINTER(ctypes.c_int64)
+            i, dbl = ctypes.c_int, ctypes.c_double
+            common = [i, i, i, i, dbl, i, ip, bp, i]
+            lib.oracle_fwd.argtypes = [dp, dp, dp] + common + [dp, dp, dp]
+            lib.oracle_bwd.argtypes = [dp, dp, dp, dp] + common + [dp, dp, dp, dp, dp]
+            lib.oracle_query_rows.argtypes = [dp, dp, dp, dp] + common + [i, lp, dp, dp, dp]
+            lib.oracle_key_rows.argtypes = [dp, dp, dp, dp] + common + [i, lp, dp, dp]
+            lib.oracle_tile_plan.argtypes = [i, i, i, ip, bp, i, i, i, bp]
+            lib.oracle_num_threads.argtypes = []
+            for f in (lib.oracle_fwd, lib.oracle_bwd, lib.oracle_query_rows,
+                      lib.oracle_key_rows, lib.oracle_tile_plan, lib.oracle_num_threads):
+                f.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _f64(x):
+    a = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    return a
+
+
+def _shapes(*arrays):
+    """Self-attention: every operand is [B, H, N, d] with the same shape."""
+    shp = arrays[0].shape
+    if len(shp) != 4:
+        raise ValueError("expected [B, H, N, d], got %r" % (shp,))
+    for a in arrays[1:]:
+        if a is not None and a.shape != shp:
+            raise ValueError("operand shapes differ: %r vs %r" % (a.shape, shp))
+    return shp
+
+
+def _check_masks(B, N, kl, bm, mask_block):
+    if kl is not None and kl.shape != (B,):
+        raise ValueError("key_len must have shape [B]")
+    if bm is not None:
+        nb = (N + mask_block - 1) // mask_block
+        if bm.shape != (nb, nb):
+            raise ValueError("block_mask must have shape [%d, %d]" % (nb, nb))
+
+
+def _ptr(a, ctype):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def _masks(key_len, block_mask):
+    kl = None if key_len is None else np.ascontiguousarray(np.asarray(key_len, dtype=np.int32))
+    bm = None if block_mask is None else np.ascontiguousarray(np.asarray(block_mask, dtype=np.uint8))
+    return kl, bm
+
+
+def num_threads() -> int:
+    """OpenMP threads the oracle runs with (its `cores`)."""
+    return int(_load().oracle_num_threads())
+
+
+def attention_fwd(Q, K, V, scale, causal=False, key_len=None, block_mask=None,
+                  mask_block=128, return_P=False):
+    """O, LSE (and optionally P) of softmax(scale*QK^T [+mask]) V, fp64.
+
+    Q, K, V: arrays [B, H, N, d].  key_len: int [B] or None.  block_mask:
+    uint8 [ceil(N/mask_block)]^2 or None.
+    """
+    lib = _load()
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    B, H, N, d = _shapes(Q, K, V)
+    kl, bm = _masks(key_len, block_mask)
+    _check_masks(B, N, kl, bm, mask_block)
+    O = np.zeros((B, H, N, d), np.float64)
+    LSE = np.zeros((B, H, N), np.float64)
+    P = np.zeros((B, H, N, N), np.float64) if return_P else None
+    rc = lib.oracle_fwd(_ptr(Q, ctypes.c_double), _ptr(K, ctypes.c_double), _ptr(V, ctypes.c_double),
+                        B, H, N, d, float(scale), int(bool(causal)), _ptr(kl, ctypes.c_int32),
+                        _ptr(bm, ctypes.c_uint8), int(mask_block), _ptr(O, ctypes.c_double),
+                        _ptr(LSE, ctypes.c_double), _ptr(P, ctypes.c_double))
+    if rc != 0:
+        raise RuntimeError("oracle_fwd failed: %d" % rc)
+    return (O, LSE, P) if return_P else (O, LSE)
+
+
+def attention_bwd(Q, K, V, dO, scale, causal=False, key_len=None, block_mask=None, mask_block=128):
+    """O, LSE, dQ, dK, dV for the loss sum(O * dO), fp64 (full materialisation)."""
+    lib = _load()
+    Q, K, V, dO = _f64(Q), _f64(K), _f64(V), _f64(dO)
+    B, H, N, d = _shapes(Q, K, V, dO)
+    kl, bm = _masks(key_len, block_mask)
+    _check_masks(B, N, kl, bm, mask_block)
+    O = np.zeros((B, H, N, d), np.float64)
+    LSE = np.zeros((B, H, N), np.float64)
+    dQ, dK, dV = (np.zeros((B, H, N, d), np.float64) for _ in range(3))
+    c = ctypes.c_double
+    rc = lib.oracle_bwd(_ptr(Q, c), _ptr(K, c), _ptr(V, c), _ptr(dO, c), B, H, N, d, float(scale),
+                        int(bool(causal)), _ptr(kl, ctypes.c_int32), _ptr(bm, ctypes.c_uint8),
+                        int(mask_block), _ptr(O, c), _ptr(LSE, c), _ptr(dQ, c), _ptr(dK, c),
+                        _ptr(dV, c))
+    if rc != 0:
+        raise RuntimeError("oracle_bwd failed: %d" % rc)
+    return O, LSE, dQ, dK, dV
+
+
+def query_rows(Q, K, V, dO, scale, rows, causal=False, key_len=None, block_mask=None,
+               mask_block=128):
+    """O, LSE and dQ for chosen query rows; rows are flat (b*H+h)*N+i indices.
+
+    dO may be None (then dQ is not computed and None is returned for it).
+    """
+    lib = _load()
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    dOa = None if dO is None else _f64(dO)
+    B, H, N, d = _shapes(Q, K, V, dOa)
+    kl, bm = _masks(key_len, block_mask)
+    _check_masks(B, N, kl, bm, mask_block)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    n = rows.size
+    O = np.zeros((n, d), np.float64)
+    LSE = np.zeros((n,), np.float64)
+    dQ = np.zeros((n, d), np.float64) if dOa is not None else None
+    c = ctypes.c_double
+    rc = lib.oracle_query_rows(_ptr(Q, c), _ptr(K, c), _ptr(V, c), _ptr(dOa, c), B, H, N, d,
+                               float(scale), int(bool(causal)), _ptr(kl, ctypes.c_int32),
+                               _ptr(bm, ctypes.c_uint8), int(mask_block), n,
+                               _ptr(rows, ctypes.c_int64), _ptr(O, c), _ptr(LSE, c), _ptr(dQ, c))
+    if rc != 0:
+        raise RuntimeError("oracle_query_rows failed: %d" % rc)
+    return O, LSE, dQ
+
+
+def key_rows(Q, K, V, dO, scale, keys, causal=False, key_len=None, block_mask=None,
+             mask_block=128):
+    """dK and dV for chosen key rows; keys are flat (b*H+h)*N+j indices."""
+    lib = _load()
+    Q, K, V, dO = _f64(Q), _f64(K), _f64(V), _f64(dO)
+    B, H, N, d = _shapes(Q, K, V, dO)
+    kl, bm = _masks(key_len, block_mask)
+    _check_masks(B, N, kl, bm, mask_block)
+    keys = np.ascontiguousarray(np.asarray(keys, dtype=np.int64))
+    n = keys.size
+    dK = np.zeros((n, d), np.float64)
+    dV = np.zeros((n, d), np.float64)
+    c = ctypes.c_double
+    rc = lib.oracle_key_rows(_ptr(Q, c), _ptr(K, c), _ptr(V, c), _ptr(dO, c), B, H, N, d,
+                             float(scale), int(bool(causal)), _ptr(kl, ctypes.c_int32),
+                             _ptr(bm, ctypes.c_uint8), int(mask_block), n,
+                             _ptr(keys, ctypes.c_int64), _ptr(dK, c), _ptr(dV, c))
+    if rc != 0:
+        raise RuntimeError("oracle_key_rows failed: %d" % rc)
+    return dK, dV
+
+
+def tile_plan(B, N, causal=False, key_len=None, block_mask=None, mask_block=128,
+              tile_q=128, tile_k=128):
+    """uint8 [B, Tq, Tk]: 0 skip, 1 full, 2 partial, by brute force over elements."""
+    lib = _load()
+    kl, bm = _masks(key_len, block_mask)
+    _check_masks(B, N, kl, bm, mask_block)
+    Tq = (N + tile_q - 1) // tile_q
+    Tk = (N + tile_k - 1) // tile_k
+    plan = np.zeros((B, Tq, Tk), np.uint8)
+    rc = lib.oracle_tile_plan(B, N, int(bool(causal)), _ptr(kl, ctypes.c_int32),
+                              _ptr(bm, ctypes.c_uint8), int(mask_block), tile_q, tile_k,
+                              _ptr(plan, ctypes.c_uint8))
+    if rc != 0:
+        raise RuntimeError("oracle_tile_plan failed: %d" % rc)
+    return plan
+
+
+from .online import merge_blocks, online_fold  # noqa: E402,F401
+from .io_model import io_model  # noqa: E402,F401
