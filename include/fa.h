@@ -1,0 +1,151 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) exact IO-aware attention library.
+ *
+ * The operation ("FlashAttention: Mathematical Foundations, IO-Aware Tiling,
+ * Online Softmax, and Recomputation Dynamics", section "The GPU Memory
+ * Hierarchy and the Attention Memory Wall"):
+ *
+ *     O = softmax(softmax_scale * Q K^T [+ mask]) V,   Q, K, V of shape (N, d),
+ *
+ * per (batch b, head h).  The forward pass writes only O and one fp32 number
+ * per query row, LSE = m + ln(l) (the row maximum m and normaliser l of the
+ * online softmax folded together; "The Attention Matrix You Never Write
+ * Down", section "Tiling forward, recomputing backward": only the output and
+ * a small per-row normalisation statistic go back to HBM).  The backward
+ * pass rebuilds the score and probability tiles on chip from Q, K and LSE
+ * (same page and section; "Backward Pass and Activation Recomputation" on
+ * the mathematical-foundations page) and produces dQ, dK, dV for the loss
+ * sum(O * dO).  The N x N score matrix is never written to memory.
+ *
+ * Conventions shared by every entry point
+ *   - Tensors are contiguous [B, H, N, d] row-major (d fastest), bf16
+ *     (Q, K, V, O, dO, dQ, dK, dV); LSE is fp32 [B, H, N].
+ *   - Device pointers are owned by the caller and must be 16-byte aligned.
+ *     The library allocates no device memory and keeps no state between
+ *     calls apart from cached kernel attributes.
+ *   - d must be 64 or 128 (else FA_ERR_UNSUPPORTED).  B, H, N >= 0; when
+ *     B*H*N == 0 the call does nothing and returns FA_OK.  Q and K share N
+ *     (self-attention).  softmax_scale must be finite and > 0 (the usual
+ *     value is 1/sqrt(d)).
+ *   - causal != 0 keeps key j for query i iff j <= i (top-left aligned).
+ *   - key_len: NULL, or a DEVICE int32 [B]: key j of batch b is kept iff
+ *     j < key_len[b] (queries are never masked).  Values are read on the
+ *     device; a value outside [0, N] is clamped and flagged in the
+ *     workspace status word (FA_ERR_DEVICE_BAD_KEY_LEN).
+ *   - block_mask: NULL, or a DEVICE uint8 [nb][nb], nb = ceil(N / 128),
+ *     shared by every (b, h): the 128 x 128 block (query block r, key block
+ *     c) is kept iff block_mask[r * nb + c] != 0 ("Attention" chapter of
+ *     learn-kernels.com, block-sparse paragraph: blocks the mask zeroes are
+ *     skipped, never loaded).
+ *   - A query row with no visible key gets O = 0, LSE = -inf and contributes
+ *     nothing to the gradients.
+ *   - stream is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *     asynchronous: they validate, enqueue and return.  Argument errors are
+ *     returned before anything is enqueued.  Errors found on the device (a
+ *     wait that timed out, a bad key_len) are written to the first word of
+ *     the workspace and read back with fa_get_device_status().
+ *   - The workspace must be zero-filled once before its first use (or reset
+ *     with fa_reset_device_status()); the library only ever sets its status
+ *     word, never clears it.
+ *   - No entry point throws or exits; there is no CPU fallback.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARGUMENT = 1,   /* null/misaligned pointer, negative size, bad scale */
+    FA_ERR_UNSUPPORTED = 2,        /* d not in {64, 128}, sizes beyond the 32-bit grid limits */
+    FA_ERR_WORKSPACE = 3,          /* workspace NULL or smaller than the *_workspace_size query */
+    FA_ERR_CUDA = 4,               /* a CUDA runtime call or kernel launch failed */
+    FA_ERR_DEVICE_TIMEOUT = 5,     /* a device-side wait gave up (kernel returned early) */
+    FA_ERR_DEVICE_BAD_KEY_LEN = 6  /* a key_len value was outside [0, N] and was clamped */
+} fa_status;
+
+/* Size of the 128 x 128 tile (and of a block_mask block). */
+int fa_tile_size(void);
+
+/* Bytes of device workspace fa_fwd needs: the status word (256 bytes). */
+size_t fa_fwd_workspace_size(int B, int H, int N, int d);
+
+/* Bytes of device workspace fa_bwd needs: the status word, the fp32 row
+ * dot-products D = rowsum(dO * O) [B, H, N] and the fp32 dQ accumulator
+ * [B, H, N, d], each 256-byte aligned. */
+size_t fa_bwd_workspace_size(int B, int H, int N, int d);
+
+/*
+ * Forward.  Q, K, V: device bf16 [B, H, N, d] (read).  O: device bf16
+ * [B, H, N, d] (written).  LSE: device fp32 [B, H, N] (written, natural log:
+ * P_ij = exp(softmax_scale * q_i.k_j - LSE_i) for visible keys).
+ * One kernel launch.
+ */
+fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H,
+                 int N, int d, float softmax_scale, int causal, const int32_t *key_len,
+                 const uint8_t *block_mask, void *workspace, size_t workspace_bytes,
+                 void *stream);
+
+/*
+ * Backward for the loss sum(O * dO).  Q, K, V, O, dO: device bf16 [B, H, N, d]
+ * (read); LSE: device fp32 [B, H, N] from fa_fwd with the same arguments
+ * (read).  dQ, dK, dV: device bf16 [B, H, N, d] (written).  Three kernel
+ * launches: D = rowsum(dO * O) with the dQ accumulator zeroed; the main
+ * kernel (one CTA per 128-key tile, recomputing S and P tile by tile); the
+ * fp32 -> bf16 conversion of dQ.
+ */
+fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, const float *LSE,
+                 const void *dO, void *dQ, void *dK, void *dV, int B, int H, int N, int d,
+                 float softmax_scale, int causal, const int32_t *key_len,
+                 const uint8_t *block_mask, void *workspace, size_t workspace_bytes,
+                 void *stream);
+
+/*
+ * The tile-skipping decisions the kernels take, exported so that they can be
+ * checked exactly.  plan: device uint8 [B][T][T], T = ceil(N / 128), written
+ * with 0 = skip (every element of the 128 x 128 tile masked; the tile is
+ * never loaded), 1 = full (no element masked), 2 = partial (element masks
+ * applied).  Element set of tile (r, c): query rows i in [128r, 128r+128)
+ * with i < N, key columns j in [128c, 128c+128); j >= N counts as masked.
+ * Computed by the same device function that drives the skipping.
+ */
+fa_status fa_tile_plan(int B, int N, int causal, const int32_t *key_len,
+                       const uint8_t *block_mask, uint8_t *plan, void *workspace,
+                       size_t workspace_bytes, void *stream);
+
+/*
+ * Host-buffer convenience: Q, K, V (and dO unless NULL) are HOST bf16 arrays;
+ * O, LSE (and dQ, dK, dV when dO != NULL) are HOST outputs.  key_len and
+ * block_mask, when given, are HOST arrays too.  The call copies the inputs
+ * into dev_workspace, runs fa_fwd (and fa_bwd), copies the outputs back and
+ * synchronises the stream before returning.  Pinned host memory makes the
+ * copies asynchronous.  dev_workspace: device memory of at least
+ * fa_host_workspace_size() bytes, zero-filled once before first use.
+ */
+size_t fa_host_workspace_size(int B, int H, int N, int d, int with_backward);
+fa_status fa_attention_host(const void *Q, const void *K, const void *V, const void *dO, void *O,
+                            float *LSE, void *dQ, void *dK, void *dV, int B, int H, int N, int d,
+                            float softmax_scale, int causal, const int32_t *key_len,
+                            const uint8_t *block_mask, void *dev_workspace,
+                            size_t dev_workspace_bytes, void *stream);
+
+/* Synchronise stream and return the workspace status word (FA_OK if no
+ * device-side error was recorded). */
+fa_status fa_get_device_status(const void *workspace, void *stream);
+
+/* Enqueue a clear of the workspace status word on stream. */
+fa_status fa_reset_device_status(void *workspace, void *stream);
+
+/* Static string for a status code. */
+const char *fa_status_string(fa_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

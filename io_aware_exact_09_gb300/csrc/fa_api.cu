@@ -1,0 +1,303 @@
+// fa_api.cu -- the C ABI declared in include/fa.h: argument checks, TMA
+// descriptor encoding, kernel launches, the host-buffer convenience path and
+// the device status word.  Host code only; the kernels live in fa_fwd.cu and
+// fa_bwd.cu.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "fa_internal.h"
+
+namespace {
+
+using fa::BwdParams;
+using fa::FwdParams;
+
+constexpr size_t kStatusBytes = 256;
+
+inline size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 3-D bf16 view [BH][N][d] of a contiguous [B, H, N, d] tensor; box of
+// 64 columns x box_rows rows x 1 head, 128-byte swizzle, zero fill outside.
+bool encode_bf16_3d(CUtensorMap *m, const void *ptr, int d, int N, int BH, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Checks shared by fa_fwd / fa_bwd / fa_tile_plan.  Returns FA_OK, or the
+// error to report; *empty is set when there is nothing to compute.
+fa_status check_sizes(int B, int H, int N, int d, bool *empty) {
+    *empty = false;
+    if (B < 0 || H < 0 || N < 0) return FA_ERR_INVALID_ARGUMENT;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if ((int64_t)B * H * N == 0) {
+        *empty = true;
+        return FA_OK;
+    }
+    const int64_t BH = (int64_t)B * H;
+    const int64_t T = ((int64_t)N + 127) / 128;
+    if (BH > INT_MAX || T * BH > INT_MAX) return FA_ERR_UNSUPPORTED;
+    // TMA: global byte strides below 2^40
+    if ((int64_t)N * d * 2 >= (int64_t(1) << 40)) return FA_ERR_UNSUPPORTED;
+    return FA_OK;
+}
+
+bool scale_ok(float s) { return std::isfinite(s) && s > 0.f; }
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+}  // namespace
+
+extern "C" {
+
+int fa_tile_size(void) { return fa::kTile; }
+
+size_t fa_fwd_workspace_size(int B, int H, int N, int d) {
+    (void)B; (void)H; (void)N; (void)d;
+    return kStatusBytes;
+}
+
+size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
+    if (B < 0 || H < 0 || N < 0 || d <= 0) return 0;
+    const size_t rows = (size_t)B * H * N;
+    return kStatusBytes + round256(rows * 4) + round256(rows * (size_t)d * 4);
+}
+
+const char *fa_status_string(fa_status s) {
+    switch (s) {
+        case FA_OK: return "ok";
+        case FA_ERR_INVALID_ARGUMENT: return "invalid argument";
+        case FA_ERR_UNSUPPORTED: return "unsupported configuration";
+        case FA_ERR_WORKSPACE: return "workspace missing or too small";
+        case FA_ERR_CUDA: return "CUDA error";
+        case FA_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+        case FA_ERR_DEVICE_BAD_KEY_LEN: return "key_len value outside [0, N] (clamped)";
+    }
+    return "unknown status";
+}
+
+fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H, int N,
+                 int d, float softmax_scale, int causal, const int32_t *key_len,
+                 const uint8_t *block_mask, void *workspace, size_t workspace_bytes, void *stream) {
+    bool empty = false;
+    fa_status st = check_sizes(B, H, N, d, &empty);
+    if (st != FA_OK) return st;
+    if (!scale_ok(softmax_scale)) return FA_ERR_INVALID_ARGUMENT;
+    if (empty) return FA_OK;
+    if (!Q || !K || !V || !O || !LSE) return FA_ERR_INVALID_ARGUMENT;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(LSE))
+        return FA_ERR_INVALID_ARGUMENT;
+    if (!workspace || !aligned16(workspace) || workspace_bytes < fa_fwd_workspace_size(B, H, N, d))
+        return FA_ERR_WORKSPACE;
+
+    FwdParams p;
+    std::memset(&p, 0, sizeof(p));
+    const int BH = B * H;
+    if (!encode_bf16_3d(&p.tmQ, Q, d, N, BH, 128) || !encode_bf16_3d(&p.tmK, K, d, N, BH, 128) ||
+        !encode_bf16_3d(&p.tmV, V, d, N, BH, 128))
+        return FA_ERR_CUDA;
+    p.O = O;
+    p.LSE = LSE;
+    p.key_len = key_len;
+    p.block_mask = block_mask;
+    p.status = static_cast<unsigned *>(workspace);
+    p.H = H;
+    p.N = N;
+    p.BH = BH;
+    p.Tq = (N + 127) / 128;
+    p.Tk = p.Tq;
+    p.causal = causal ? 1 : 0;
+    p.scale_log2 = softmax_scale * kLog2e;
+    return fa::launch_fwd(d, p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, const float *LSE, const void *dO,
+                 void *dQ, void *dK, void *dV, int B, int H, int N, int d, float softmax_scale, int causal,
+                 const int32_t *key_len, const uint8_t *block_mask, void *workspace, size_t workspace_bytes,
+                 void *stream) {
+    bool empty = false;
+    fa_status st = check_sizes(B, H, N, d, &empty);
+    if (st != FA_OK) return st;
+    if (!scale_ok(softmax_scale)) return FA_ERR_INVALID_ARGUMENT;
+    if (empty) return FA_OK;
+    const void *ptrs[] = {Q, K, V, O, LSE, dO, dQ, dK, dV};
+    for (const void *x : ptrs)
+        if (!x || !aligned16(x)) return FA_ERR_INVALID_ARGUMENT;
+    if (!workspace || !aligned16(workspace) || workspace_bytes < fa_bwd_workspace_size(B, H, N, d))
+        return FA_ERR_WORKSPACE;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int BH = B * H;
+    const int64_t rows = (int64_t)BH * N;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    float *Dvec = reinterpret_cast<float *>(ws + kStatusBytes);
+    float *dQacc = reinterpret_cast<float *>(ws + kStatusBytes + round256((size_t)rows * 4));
+
+    BwdParams p;
+    std::memset(&p, 0, sizeof(p));
+    const int BQ = fa::bwd_query_block(d);
+    if (!encode_bf16_3d(&p.tmQ, Q, d, N, BH, BQ) || !encode_bf16_3d(&p.tmdO, dO, d, N, BH, BQ) ||
+        !encode_bf16_3d(&p.tmK, K, d, N, BH, 128) || !encode_bf16_3d(&p.tmV, V, d, N, BH, 128))
+        return FA_ERR_CUDA;
+    p.LSE = LSE;
+    p.Dvec = Dvec;
+    p.dQacc = dQacc;
+    p.dK = dK;
+    p.dV = dV;
+    p.key_len = key_len;
+    p.block_mask = block_mask;
+    p.status = reinterpret_cast<unsigned *>(ws);
+    p.H = H;
+    p.N = N;
+    p.BH = BH;
+    p.Tk = (N + 127) / 128;
+    p.Tqb = (N + BQ - 1) / BQ;
+    p.causal = causal ? 1 : 0;
+    p.scale_log2 = softmax_scale * kLog2e;
+    p.scale = softmax_scale;
+
+    if (fa::launch_bwd_pre(d, O, dO, Dvec, dQacc, rows, s) != cudaSuccess) return FA_ERR_CUDA;
+    if (fa::launch_bwd_main(d, p, s) != cudaSuccess) return FA_ERR_CUDA;
+    if (fa::launch_bwd_convert(d, dQacc, dQ, rows * d, softmax_scale, s) != cudaSuccess) return FA_ERR_CUDA;
+    return FA_OK;
+}
+
+fa_status fa_tile_plan(int B, int N, int causal, const int32_t *key_len, const uint8_t *block_mask,
+                       uint8_t *plan, void *workspace, size_t workspace_bytes, void *stream) {
+    if (B < 0 || N < 0) return FA_ERR_INVALID_ARGUMENT;
+    if ((int64_t)B * N == 0) return FA_OK;
+    const int64_t T = ((int64_t)N + 127) / 128;
+    if (T * T * B > ((int64_t)1 << 40)) return FA_ERR_UNSUPPORTED;
+    if (!plan) return FA_ERR_INVALID_ARGUMENT;
+    if (!workspace || !aligned16(workspace) || workspace_bytes < kStatusBytes) return FA_ERR_WORKSPACE;
+    return fa::launch_plan(B, N, causal ? 1 : 0, key_len, block_mask, plan, static_cast<unsigned *>(workspace),
+                           static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? FA_OK
+               : FA_ERR_CUDA;
+}
+
+fa_status fa_get_device_status(const void *workspace, void *stream) {
+    if (!workspace) return FA_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned w[2] = {0, 0};
+    if (cudaMemcpyAsync(w, workspace, sizeof(w), cudaMemcpyDeviceToHost, s) != cudaSuccess) return FA_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return FA_ERR_CUDA;
+    return static_cast<fa_status>(w[0]);
+}
+
+fa_status fa_reset_device_status(void *workspace, void *stream) {
+    if (!workspace) return FA_ERR_WORKSPACE;
+    return cudaMemsetAsync(workspace, 0, 8, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK
+                                                                                                 : FA_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------ host-buffer path
+namespace {
+struct HostLayout {
+    size_t attn_ws, q, k, v, o, dO, dQ, dK, dV, lse, klen, bmask, total;
+};
+HostLayout host_layout(int B, int H, int N, int d, int with_bwd) {
+    HostLayout L;
+    const size_t rows = (size_t)B * H * N, t = round256(rows * (size_t)d * 2);
+    const size_t nb = ((size_t)N + 127) / 128;
+    size_t off = 0;
+    L.attn_ws = off;
+    off += round256(with_bwd ? fa_bwd_workspace_size(B, H, N, d) : fa_fwd_workspace_size(B, H, N, d));
+    L.q = off; off += t;
+    L.k = off; off += t;
+    L.v = off; off += t;
+    L.o = off; off += t;
+    L.dO = off; off += with_bwd ? t : 0;
+    L.dQ = off; off += with_bwd ? t : 0;
+    L.dK = off; off += with_bwd ? t : 0;
+    L.dV = off; off += with_bwd ? t : 0;
+    L.lse = off; off += round256(rows * 4);
+    L.klen = off; off += round256((size_t)B * 4);
+    L.bmask = off; off += round256(nb * nb);
+    L.total = off;
+    return L;
+}
+}  // namespace
+
+size_t fa_host_workspace_size(int B, int H, int N, int d, int with_backward) {
+    if (B < 0 || H < 0 || N < 0 || d <= 0) return 0;
+    return host_layout(B, H, N, d, with_backward ? 1 : 0).total;
+}
+
+fa_status fa_attention_host(const void *Q, const void *K, const void *V, const void *dO, void *O, float *LSE,
+                            void *dQ, void *dK, void *dV, int B, int H, int N, int d, float softmax_scale,
+                            int causal, const int32_t *key_len, const uint8_t *block_mask, void *dev_workspace,
+                            size_t dev_workspace_bytes, void *stream) {
+    bool empty = false;
+    fa_status st = check_sizes(B, H, N, d, &empty);
+    if (st != FA_OK) return st;
+    if (!scale_ok(softmax_scale)) return FA_ERR_INVALID_ARGUMENT;
+    if (empty) return FA_OK;
+    const int bwd = dO != nullptr;
+    if (!Q || !K || !V || !O || !LSE || (bwd && (!dQ || !dK || !dV))) return FA_ERR_INVALID_ARGUMENT;
+    const HostLayout L = host_layout(B, H, N, d, bwd);
+    if (!dev_workspace || !aligned16(dev_workspace) || dev_workspace_bytes < L.total) return FA_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t *w = static_cast<uint8_t *>(dev_workspace);
+    const size_t bytes = (size_t)B * H * N * d * 2, lbytes = (size_t)B * H * N * 4;
+    const size_t nb = ((size_t)N + 127) / 128;
+    auto h2d = [&](size_t off, const void *src, size_t n) {
+        return cudaMemcpyAsync(w + off, src, n, cudaMemcpyHostToDevice, s) == cudaSuccess;
+    };
+    auto d2h = [&](void *dst, size_t off, size_t n) {
+        return cudaMemcpyAsync(dst, w + off, n, cudaMemcpyDeviceToHost, s) == cudaSuccess;
+    };
+    if (!h2d(L.q, Q, bytes) || !h2d(L.k, K, bytes) || !h2d(L.v, V, bytes)) return FA_ERR_CUDA;
+    if (bwd && !h2d(L.dO, dO, bytes)) return FA_ERR_CUDA;
+    if (key_len && !h2d(L.klen, key_len, (size_t)B * 4)) return FA_ERR_CUDA;
+    if (block_mask && !h2d(L.bmask, block_mask, nb * nb)) return FA_ERR_CUDA;
+    const int32_t *kl = key_len ? reinterpret_cast<const int32_t *>(w + L.klen) : nullptr;
+    const uint8_t *bm = block_mask ? w + L.bmask : nullptr;
+    const size_t ws_bytes = bwd ? fa_bwd_workspace_size(B, H, N, d) : fa_fwd_workspace_size(B, H, N, d);
+    st = fa_fwd(w + L.q, w + L.k, w + L.v, w + L.o, reinterpret_cast<float *>(w + L.lse), B, H, N, d, softmax_scale,
+                causal, kl, bm, w + L.attn_ws, ws_bytes, stream);
+    if (st != FA_OK) return st;
+    if (bwd) {
+        st = fa_bwd(w + L.q, w + L.k, w + L.v, w + L.o, reinterpret_cast<float *>(w + L.lse), w + L.dO, w + L.dQ,
+                    w + L.dK, w + L.dV, B, H, N, d, softmax_scale, causal, kl, bm, w + L.attn_ws, ws_bytes, stream);
+        if (st != FA_OK) return st;
+    }
+    if (!d2h(O, L.o, bytes) || !d2h(LSE, L.lse, lbytes)) return FA_ERR_CUDA;
+    if (bwd && (!d2h(dQ, L.dQ, bytes) || !d2h(dK, L.dK, bytes) || !d2h(dV, L.dV, bytes))) return FA_ERR_CUDA;
+    return fa_get_device_status(w + L.attn_ws, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,573 @@
+// fa_bwd.cu -- backward kernels: gradients of exact attention by recomputing
+// the score and probability tiles on chip.
+//
+// Method ("The Attention Matrix You Never Write Down", section "Tiling
+// forward, recomputing backward"; "FlashAttention: Mathematical Foundations
+// ...", section "Backward Pass and Activation Recomputation"): the forward
+// kept only O and the per-row statistic LSE; the backward rebuilds each tile
+// P_ij = exp(scale * q_i.k_j - LSE_i) from Q_i, K_j and LSE_i instead of
+// reading a stored N x N matrix.  The gradient formulas themselves are the
+// chain rule through O = P V and the row softmax (the pages give none):
+//     dV = P^T dO,  dP = dO V^T,  D_i = sum_k dO_ik O_ik,
+//     dS = P o (dP - D),  dQ = scale dS K,  dK = scale dS^T Q.
+//
+// Three kernels:
+//   1. fa_bwd_pre:     D = rowsum(dO * O) (fp32) and dQacc = 0      (HBM-bound)
+//   2. fa_bwd_kernel:  one CTA per (128-key tile, b*h); loop over the query
+//      blocks that see the tile:
+//        warp 0  TMA: K_j, V_j once; Q_i, dO_i through a 2-stage ring
+//        warp 1  tcgen05: S^T = K Q^T, dP^T = V dO^T, dV += P^T dO,
+//                dK += dS^T Q (P^T, dS^T read from TMEM), and the dQ
+//                contribution into one of two TMEM buffers
+//        warps 4-7  one key row per thread: P^T = 2^(s*c - LSE*log2 e), masks,
+//                dS^T = P^T o (dP^T - D) -> bf16 into TMEM and into shared
+//                memory (the dQ MMA's operand); drain the previous dQ
+//                contribution into the fp32 accumulator with vector atomics;
+//                at the end dK * scale and dV -> bf16.
+//      d = 64 uses 128-row query blocks and dQ = dS K (TMEM lane = query);
+//      d = 128 uses 64-row query blocks and dQ^T = K^T dS^T (TMEM lane = head
+//      dimension), so that S, dP, dV, dK and two dQ buffers fit in the 512
+//      TMEM columns in both cases.
+//   3. fa_bwd_convert: dQ = bf16(scale * dQacc)                        (HBM-bound)
+#include "fa_internal.h"
+#include "fa_ptx.cuh"
+
+namespace fa {
+
+template <int D>
+struct BwdShape {
+    static constexpr int BQ = (D == 64) ? 128 : 64;       // query rows per inner step
+    static constexpr bool DQ_T = (D == 128);              // dQ^T = K^T dS^T
+    static constexpr int CHUNKS = D / 64;
+    static constexpr int KV_CHUNK = 128 * 128;            // 128 keys x 128 bytes
+    static constexpr int KV_BYTES = CHUNKS * KV_CHUNK;
+    static constexpr int Q_CHUNK = BQ * 128;              // BQ rows x 128 bytes
+    static constexpr int Q_BYTES = CHUNKS * Q_CHUNK;
+    static constexpr int STAGES = 2;
+    static constexpr int DS_BYTES = BQ * 128 * 2;         // BQ queries x 128 keys, bf16
+    static constexpr int OFF_K = 0;
+    static constexpr int OFF_V = OFF_K + KV_BYTES;
+    static constexpr int OFF_Q = OFF_V + KV_BYTES;        // [STAGES]
+    static constexpr int OFF_DO = OFF_Q + STAGES * Q_BYTES;
+    static constexpr int OFF_DS = OFF_DO + STAGES * Q_BYTES;
+    static constexpr int OFF_LSE = OFF_DS + DS_BYTES;     // [2][BQ] fp32 (log2 domain)
+    static constexpr int OFF_DV = OFF_LSE + 2 * BQ * 4;   // [2][BQ] fp32
+    static constexpr int OFF_BAR = OFF_DV + 2 * BQ * 4;
+    static constexpr int B_KV = 0;
+    static constexpr int B_QFULL = 1;                     // [2]
+    static constexpr int B_QEMPTY = 3;                    // [2]
+    static constexpr int B_SFULL = 5;
+    static constexpr int B_DPFULL = 6;
+    static constexpr int B_PFULL = 7;
+    static constexpr int B_DSFULL = 8;
+    static constexpr int B_SDPFREE = 9;
+    static constexpr int B_DQFULL = 10;                   // [2]
+    static constexpr int B_DQFREE = 12;                   // [2]
+    static constexpr int B_ACC = 14;
+    static constexpr int B_FIN = 15;
+    static constexpr int B_LSE = 16;                      // [2] LSE/D block staged (128 arrivals)
+    static constexpr int NBAR = 18;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t TM_S = 0;                   // BQ columns (P^T as bf16 in the first BQ/2)
+    static constexpr uint32_t TM_DP = BQ;                 // BQ columns (dS^T as bf16 in the first BQ/2)
+    static constexpr uint32_t TM_DV = 2 * BQ;             // D columns
+    static constexpr uint32_t TM_DK = 2 * BQ + D;         // D columns
+    static constexpr uint32_t TM_DQ = 2 * BQ + 2 * D;     // 2 x 64 columns
+};
+
+__device__ __forceinline__ void drain_wait_b(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (globaltimer_ns() - t0 > FA_WAIT_TIMEOUT_NS) break;
+}
+
+template <int D>
+__global__ void __launch_bounds__(256, 1) fa_bwd_kernel(const __grid_constant__ BwdParams p) {
+    using S = BwdShape<D>;
+    constexpr int BQ = S::BQ;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *sb = smem_raw + (base - raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    const int kt = (int)(blockIdx.x / p.BH);
+    const int bh = (int)(blockIdx.x % p.BH);
+    const int b = bh / p.H;
+    const int k0 = kt * kTile;
+    const int nb = (p.N + kTile - 1) / kTile;
+
+    auto bar = [&](int i) -> uint32_t { return base + S::OFF_BAR + 8u * (uint32_t)i; };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sb + S::OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sb + S::OFF_MISC + 4);
+    const Guard g{p.status, p.status + 1, abort_flag};
+
+    bool bad = false;
+    const int kvis = key_visible_bound(p.key_len, b, p.N, &bad);
+    if (bad && threadIdx.x == 0 && kt == 0 && (bh % p.H) == 0) record_status(g, kStatusBadKeyLen, 0);
+
+    // class of query block qb (BQ rows) against this key tile
+    auto cls = [&](int qb) -> unsigned {
+        const int qa = qb * BQ;
+        const int on = p.block_mask ? (p.block_mask[(size_t)(qa / kTile) * nb + kt] != 0) : 1;
+        return tile_class(qa, min(BQ, p.N - qa), k0, kTile, kvis, p.causal, on);
+    };
+    auto next_qb = [&](int qb) -> int {
+        for (int x = qb + 1; x < p.Tqb; ++x)
+            if (cls(x) != kTileSkip) return x;
+        return p.Tqb;
+    };
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(S::B_KV), 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar(S::B_QFULL + s), 1);
+            mbar_init(bar(S::B_QEMPTY + s), 1);
+            mbar_init(bar(S::B_DQFULL + s), 1);
+            mbar_init(bar(S::B_DQFREE + s), 128);
+        }
+        mbar_init(bar(S::B_SFULL), 1);
+        mbar_init(bar(S::B_DPFULL), 1);
+        mbar_init(bar(S::B_PFULL), 128);
+        mbar_init(bar(S::B_DSFULL), 128);
+        mbar_init(bar(S::B_SDPFREE), 1);
+        mbar_init(bar(S::B_ACC), 1);
+        mbar_init(bar(S::B_FIN), 1);
+        mbar_init(bar(S::B_LSE), 128);
+        mbar_init(bar(S::B_LSE + 1), 128);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&p.tmQ);
+        tma_prefetch_desc(&p.tmdO);
+        tma_prefetch_desc(&p.tmK);
+        tma_prefetch_desc(&p.tmV);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), S::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int first = next_qb(-1);
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- producer
+        if (lane == 0 && first < p.Tqb) {
+            mbar_arrive_expect_tx(bar(S::B_KV), 2 * S::KV_BYTES);
+            for (int c = 0; c < S::CHUNKS; ++c) {
+                tma_load_3d(base + S::OFF_K + c * S::KV_CHUNK, &p.tmK, bar(S::B_KV), c * 64, k0, bh);
+                tma_load_3d(base + S::OFF_V + c * S::KV_CHUNK, &p.tmV, bar(S::B_KV), c * 64, k0, bh);
+            }
+            int i = 0;
+            bool ok = true;
+            for (int qb = first; qb < p.Tqb; qb = next_qb(qb), ++i) {
+                const int s = i & 1;
+                if (!mbar_wait(bar(S::B_QEMPTY + s), ((uint32_t)(i >> 1) & 1u) ^ 1u, g, 0x111)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(bar(S::B_QFULL + s), 2 * S::Q_BYTES);
+                for (int c = 0; c < S::CHUNKS; ++c) {
+                    tma_load_3d(base + S::OFF_Q + s * S::Q_BYTES + c * S::Q_CHUNK, &p.tmQ,
+                                bar(S::B_QFULL + s), c * 64, qb * BQ, bh);
+                    tma_load_3d(base + S::OFF_DO + s * S::Q_BYTES + c * S::Q_CHUNK, &p.tmdO,
+                                bar(S::B_QFULL + s), c * 64, qb * BQ, bh);
+                }
+            }
+            if (!ok) {
+                drain_wait_b(bar(S::B_KV), 0);
+                for (int j = (i > 2 ? i - 2 : 0); j < i; ++j)
+                    drain_wait_b(bar(S::B_QFULL + (j & 1)), (uint32_t)(j >> 1) & 1u);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t IDESC_S = idesc_bf16(128, BQ, false, false);   // S^T, dP^T
+            constexpr uint32_t IDESC_ACC = idesc_bf16(128, D, false, true);   // dV, dK
+            constexpr uint32_t IDESC_DQ = idesc_bf16(128, 64, true, true);    // dQ or dQ^T
+            bool ok = true;
+            int i = 0;
+            if (first < p.Tqb) {
+                ok = mbar_wait(bar(S::B_KV), 0, g, 0x211);
+                for (int qb = first; ok && qb < p.Tqb; qb = next_qb(qb), ++i) {
+                    const int s = i & 1;
+                    const uint32_t qs = base + S::OFF_Q + s * S::Q_BYTES;
+                    const uint32_t dos = base + S::OFF_DO + s * S::Q_BYTES;
+                    if (!mbar_wait(bar(S::B_QFULL + s), (uint32_t)(i >> 1) & 1u, g, 0x212)) { ok = false; break; }
+                    // S / dP columns are free once dV and dK of the previous step have read them
+                    if (i > 0 && !mbar_wait(bar(S::B_SDPFREE), (uint32_t)(i - 1) & 1u, g, 0x213)) { ok = false; break; }
+                    tc_fence_after();
+                    // S^T = K Q^T and dP^T = V dO^T: M = 128 keys, N = BQ queries, K = D
+#pragma unroll
+                    for (int k = 0; k < D / 16; ++k) {
+                        const uint32_t ko = (k >> 2) * S::KV_CHUNK + (k & 3) * 32;
+                        const uint32_t qo = (k >> 2) * S::Q_CHUNK + (k & 3) * 32;
+                        mma_ss(tmem + S::TM_S, sdesc_sw128(base + S::OFF_K + ko, 16, 1024),
+                               sdesc_sw128(qs + qo, 16, 1024), IDESC_S, k > 0 ? 1u : 0u);
+                    }
+                    mma_commit(bar(S::B_SFULL));
+#pragma unroll
+                    for (int k = 0; k < D / 16; ++k) {
+                        const uint32_t ko = (k >> 2) * S::KV_CHUNK + (k & 3) * 32;
+                        const uint32_t qo = (k >> 2) * S::Q_CHUNK + (k & 3) * 32;
+                        mma_ss(tmem + S::TM_DP, sdesc_sw128(base + S::OFF_V + ko, 16, 1024),
+                               sdesc_sw128(dos + qo, 16, 1024), IDESC_S, k > 0 ? 1u : 0u);
+                    }
+                    mma_commit(bar(S::B_DPFULL));
+                    // dV += P^T dO: A = P^T from TMEM, B = dO (N = D, K = queries, MN-major)
+                    if (!mbar_wait(bar(S::B_PFULL), (uint32_t)i & 1u, g, 0x214)) { ok = false; break; }
+                    tc_fence_after();
+#pragma unroll
+                    for (int k = 0; k < BQ / 16; ++k)
+                        mma_ts(tmem + S::TM_DV, tmem + S::TM_S + 8u * k,
+                               sdesc_sw128(dos + k * 2048, S::Q_CHUNK, 1024), IDESC_ACC,
+                               (i > 0 || k > 0) ? 1u : 0u);
+                    // dK += dS^T Q: A = dS^T from TMEM, B = Q (MN-major)
+                    if (!mbar_wait(bar(S::B_DSFULL), (uint32_t)i & 1u, g, 0x215)) { ok = false; break; }
+                    tc_fence_after();
+#pragma unroll
+                    for (int k = 0; k < BQ / 16; ++k)
+                        mma_ts(tmem + S::TM_DK, tmem + S::TM_DP + 8u * k,
+                               sdesc_sw128(qs + k * 2048, S::Q_CHUNK, 1024), IDESC_ACC,
+                               (i > 0 || k > 0) ? 1u : 0u);
+                    mma_commit(bar(S::B_QEMPTY + s));
+                    mma_commit(bar(S::B_SDPFREE));
+                    // dQ contribution into TMEM buffer i % 2 (drained by the compute warps)
+                    if (i >= 2 &&
+                        !mbar_wait(bar(S::B_DQFREE + s), (uint32_t)((i - 2) >> 1) & 1u, g, 0x216)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t dq_tmem = tmem + S::TM_DQ + 64u * (uint32_t)s;
+                    const uint32_t ds = base + S::OFF_DS;
+                    const uint32_t ks = base + S::OFF_K;
+#pragma unroll
+                    for (int k = 0; k < kTile / 16; ++k) {
+                        if (S::DQ_T)   // dQ^T = K^T dS^T: A = K^T (M = d), B = dS (N = queries)
+                            mma_ss(dq_tmem, sdesc_sw128(ks + k * 2048, S::KV_CHUNK, 1024),
+                                   sdesc_sw128(ds + k * 2048, 128 * 128, 1024), IDESC_DQ, k > 0 ? 1u : 0u);
+                        else           // dQ = dS K: A = dS (M = queries), B = K (N = d)
+                            mma_ss(dq_tmem, sdesc_sw128(ds + k * 2048, 128 * 128, 1024),
+                                   sdesc_sw128(ks + k * 2048, S::KV_CHUNK, 1024), IDESC_DQ, k > 0 ? 1u : 0u);
+                    }
+                    mma_commit(bar(S::B_DQFULL + s));
+                }
+                if (ok) mma_commit(bar(S::B_ACC));
+            }
+            mma_commit(bar(S::B_FIN));
+            drain_wait_b(bar(S::B_FIN), 0);
+        }
+    } else if (warp >= 4) {
+        // ---------------------------------------------------------- compute
+        const int wq = warp & 3;
+        const int r = wq * 32 + lane;           // TMEM lane: key row (S^T, dP^T, dK, dV), query/dim row (dQ)
+        const int tid = threadIdx.x - 128;
+        const int key = k0 + r;
+        const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        const float c2 = p.scale_log2;
+        float *lse_s = reinterpret_cast<float *>(sb + S::OFF_LSE);
+        float *dv_s = reinterpret_cast<float *>(sb + S::OFF_DV);
+        bool ok = true;
+        int i = 0, prev_qb = -1;
+
+        // drain the dQ contribution of step j (query block qb) into dQacc
+        auto drain_dq = [&](int j, int qb) -> bool {
+            if (!mbar_wait_warp(bar(S::B_DQFULL + (j & 1)), (uint32_t)(j >> 1) & 1u, g, 0x411)) return false;
+            tc_fence_after();
+            uint32_t v0[32], v1[32];
+            const uint32_t a = tmem + lane_off + S::TM_DQ + 64u * (uint32_t)(j & 1);
+            tmem_ld32(a, v0);
+            tmem_ld32(a + 32u, v1);
+            tmem_ld_wait(v0);
+            tmem_ld_wait(v1);
+            tc_fence_before();
+            mbar_arrive(bar(S::B_DQFREE + (j & 1)));
+            if (S::DQ_T) {
+                // lane r = head dimension r, column t = query qb*BQ + t
+                float *col = p.dQacc + ((size_t)bh * p.N + (size_t)qb * BQ) * D + r;
+                const int nq = min(BQ, p.N - qb * BQ);
+#pragma unroll 4
+                for (int t = 0; t < 32; ++t)
+                    if (t < nq) atomicAdd(col + (size_t)t * D, __uint_as_float(v0[t]));
+#pragma unroll 4
+                for (int t = 0; t < 32; ++t)
+                    if (t + 32 < nq) atomicAdd(col + (size_t)(t + 32) * D, __uint_as_float(v1[t]));
+            } else {
+                // lane r = query qb*BQ + r, column t = head dimension t
+                const int qrow = qb * BQ + r;
+                if (qrow < p.N) {
+                    float4 *row = reinterpret_cast<float4 *>(p.dQacc + ((size_t)bh * p.N + qrow) * D);
+#pragma unroll
+                    for (int t = 0; t < 8; ++t)
+                        atomicAdd(row + t, make_float4(__uint_as_float(v0[4 * t]), __uint_as_float(v0[4 * t + 1]),
+                                                       __uint_as_float(v0[4 * t + 2]), __uint_as_float(v0[4 * t + 3])));
+#pragma unroll
+                    for (int t = 0; t < 8; ++t)
+                        atomicAdd(row + 8 + t, make_float4(__uint_as_float(v1[4 * t]), __uint_as_float(v1[4 * t + 1]),
+                                                           __uint_as_float(v1[4 * t + 2]), __uint_as_float(v1[4 * t + 3])));
+                }
+            }
+            return true;
+        };
+
+        for (int qb = first; qb < p.Tqb; qb = next_qb(qb), ++i) {
+            const unsigned klass = cls(qb);
+            const int qa = qb * BQ;
+            // LSE (log2 domain; +inf for rows past N or with nothing visible) and D for this block
+            {
+                float *ls = lse_s + (i & 1) * BQ;
+                float *dd = dv_s + (i & 1) * BQ;
+                for (int t = tid; t < 2 * BQ; t += 128) {
+                    const int tt = t % BQ;
+                    const int qq = qa + tt;
+                    if (t < BQ) {
+                        float v = INFINITY;
+                        if (qq < p.N) {
+                            const float L = p.LSE[(size_t)bh * p.N + qq];
+                            v = (L == -INFINITY) ? INFINITY : L * 1.4426950408889634f;
+                        }
+                        ls[tt] = v;
+                    } else {
+                        dd[tt] = (qq < p.N) ? p.Dvec[(size_t)bh * p.N + qq] : 0.f;
+                    }
+                }
+                mbar_arrive(bar(S::B_LSE + (i & 1)));
+                if (!mbar_wait_warp(bar(S::B_LSE + (i & 1)), (uint32_t)(i >> 1) & 1u, g, 0x410)) {
+                    ok = false;
+                    break;
+                }
+            }
+            const float *ls = lse_s + (i & 1) * BQ;
+            const float *dd = dv_s + (i & 1) * BQ;
+
+            // P^T = 2^(s * c - LSE_q * log2 e), masked
+            if (!mbar_wait_warp(bar(S::B_SFULL), (uint32_t)i & 1u, g, 0x412)) { ok = false; break; }
+            tc_fence_after();
+            uint32_t pk[BQ / 2];
+#pragma unroll
+            for (int j = 0; j < BQ / 32; ++j) {
+                uint32_t sr[32];
+                tmem_ld32(tmem + lane_off + S::TM_S + 32u * j, sr);
+                tmem_ld_wait(sr);
+#pragma unroll
+                for (int t = 0; t < 32; t += 2) {
+                    const int qx = qa + 32 * j + t;
+                    float p0 = ex2(fmaf(__uint_as_float(sr[t]), c2, -ls[32 * j + t]));
+                    float p1 = ex2(fmaf(__uint_as_float(sr[t + 1]), c2, -ls[32 * j + t + 1]));
+                    if (klass == kTilePartial) {
+                        if (key >= kvis || (p.causal && key > qx)) p0 = 0.f;
+                        if (key >= kvis || (p.causal && key > qx + 1)) p1 = 0.f;
+                    }
+                    pk[16 * j + t / 2] = pack_bf16x2(p0, p1);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < BQ / 32; ++j) tmem_st16(tmem + lane_off + S::TM_S + 16u * j, pk + 16 * j);
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(bar(S::B_PFULL));
+
+            // dS^T = P^T o (dP^T - D): bf16 into TMEM (for dK) and shared memory (for dQ)
+            if (!mbar_wait_warp(bar(S::B_DPFULL), (uint32_t)i & 1u, g, 0x413)) { ok = false; break; }
+            // the dQ MMA of the previous step must be done reading the shared dS tile
+            if (i > 0 && !mbar_wait_warp(bar(S::B_DQFULL + ((i - 1) & 1)), (uint32_t)((i - 1) >> 1) & 1u, g, 0x414)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint8_t *ds_smem = sb + S::OFF_DS;
+#pragma unroll
+            for (int j = 0; j < BQ / 32; ++j) {
+                uint32_t dp[32];
+                tmem_ld32(tmem + lane_off + S::TM_DP + 32u * j, dp);
+                tmem_ld_wait(dp);
+                uint32_t w[16];
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                    const uint32_t pp = pk[16 * j + t];
+                    const float d0 = bf16lo(pp) * (__uint_as_float(dp[2 * t]) - dd[32 * j + 2 * t]);
+                    const float d1 = bf16hi(pp) * (__uint_as_float(dp[2 * t + 1]) - dd[32 * j + 2 * t + 1]);
+                    w[t] = pack_bf16x2(d0, d1);
+                }
+                tmem_st16(tmem + lane_off + S::TM_DP + 16u * j, w);
+                // shared dS tile, queries contiguous (MN-major, 128-byte swizzle):
+                // [query chunk of 64][key row 0..127][128 bytes]
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int qo = 32 * j + 8 * u;                 // first query of this 16-byte piece
+                    const int grp = (qo & 63) >> 3;
+                    uint8_t *dst = ds_smem + (qo >> 6) * (128 * 128) + r * 128 + ((grp ^ (r & 7)) << 4);
+                    *reinterpret_cast<uint4 *>(dst) = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+                }
+            }
+            tmem_st_wait();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar(S::B_DSFULL));
+
+            // drain the previous step's dQ while the tensor cores work on this one
+            if (i > 0 && !drain_dq(i - 1, prev_qb)) { ok = false; break; }
+            prev_qb = qb;
+        }
+        if (ok && i > 0) ok = drain_dq(i - 1, prev_qb);
+
+        // ---------------------------------------------------------- epilogue: dK, dV
+        if (ok && i > 0) {
+            ok = mbar_wait_warp(bar(S::B_ACC), 0, g, 0x415);
+            tc_fence_after();
+        }
+        if (ok) {
+            // the TMEM loads are warp-collective: every lane loads, only rows < N store
+            __nv_bfloat16 *dkrow = reinterpret_cast<__nv_bfloat16 *>(p.dK) + ((size_t)bh * p.N + key) * D;
+            __nv_bfloat16 *dvrow = reinterpret_cast<__nv_bfloat16 *>(p.dV) + ((size_t)bh * p.N + key) * D;
+#pragma unroll 1
+            for (int j = 0; j < D / 32; ++j) {
+                uint32_t a[32], v[32];
+                if (i > 0) {
+                    tmem_ld32(tmem + lane_off + S::TM_DK + 32u * j, a);
+                    tmem_ld32(tmem + lane_off + S::TM_DV + 32u * j, v);
+                    tmem_ld_wait(a);
+                    tmem_ld_wait(v);
+                } else {
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) a[t] = v[t] = 0u;
+                }
+                uint32_t wk[16], wv[16];
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                    wk[t] = pack_bf16x2(__uint_as_float(a[2 * t]) * p.scale, __uint_as_float(a[2 * t + 1]) * p.scale);
+                    wv[t] = pack_bf16x2(__uint_as_float(v[2 * t]), __uint_as_float(v[2 * t + 1]));
+                }
+                if (key < p.N) {
+                    uint4 *dk4 = reinterpret_cast<uint4 *>(dkrow + 32 * j);
+                    uint4 *dv4 = reinterpret_cast<uint4 *>(dvrow + 32 * j);
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        dk4[t] = make_uint4(wk[4 * t], wk[4 * t + 1], wk[4 * t + 2], wk[4 * t + 3]);
+                        dv4[t] = make_uint4(wv[4 * t], wv[4 * t + 1], wv[4 * t + 2], wv[4 * t + 3]);
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, S::TMEM_COLS);
+}
+
+// D = rowsum(dO * O) in fp32 and dQacc = 0, one warp per row.
+template <int D>
+__global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __nv_bfloat16 *__restrict__ O,
+                                                         const __nv_bfloat16 *__restrict__ dO,
+                                                         float *__restrict__ Dvec, float *__restrict__ dQacc,
+                                                         int64_t rows) {
+    const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    constexpr int PER = D / 32;   // elements per lane: 2 or 4
+    float acc = 0.f;
+    if (PER == 4) {
+        const uint2 o = reinterpret_cast<const uint2 *>(O + row * D)[lane];
+        const uint2 g = reinterpret_cast<const uint2 *>(dO + row * D)[lane];
+        acc = bf16lo(o.x) * bf16lo(g.x) + bf16hi(o.x) * bf16hi(g.x) + bf16lo(o.y) * bf16lo(g.y) +
+              bf16hi(o.y) * bf16hi(g.y);
+        reinterpret_cast<float4 *>(dQacc + row * D)[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+    } else {
+        const uint32_t o = reinterpret_cast<const uint32_t *>(O + row * D)[lane];
+        const uint32_t g = reinterpret_cast<const uint32_t *>(dO + row * D)[lane];
+        acc = bf16lo(o) * bf16lo(g) + bf16hi(o) * bf16hi(g);
+        reinterpret_cast<float2 *>(dQacc + row * D)[lane] = make_float2(0.f, 0.f);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) Dvec[row] = acc;
+}
+
+// dQ = bf16(scale * dQacc), 8 elements per thread.
+__global__ void __launch_bounds__(256) fa_bwd_convert_kernel(const float *__restrict__ acc,
+                                                             __nv_bfloat16 *__restrict__ dQ, int64_t n8,
+                                                             float scale) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const float4 a = reinterpret_cast<const float4 *>(acc)[2 * i];
+        const float4 c = reinterpret_cast<const float4 *>(acc)[2 * i + 1];
+        reinterpret_cast<uint4 *>(dQ)[i] =
+            make_uint4(pack_bf16x2(a.x * scale, a.y * scale), pack_bf16x2(a.z * scale, a.w * scale),
+                       pack_bf16x2(c.x * scale, c.y * scale), pack_bf16x2(c.z * scale, c.w * scale));
+    }
+}
+
+// Tile plan export: the same tile_class the attention kernels skip with.
+__global__ void fa_plan_kernel(int B, int N, int T, int causal, const int32_t *key_len,
+                               const uint8_t *block_mask, uint8_t *plan, unsigned *status) {
+    const int64_t n = (int64_t)B * T * T;
+    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < n;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        const int kt = (int)(idx % T);
+        const int qt = (int)((idx / T) % T);
+        const int b = (int)(idx / ((int64_t)T * T));
+        bool bad = false;
+        const int kvis = key_visible_bound(key_len, b, N, &bad);
+        if (bad && qt == 0 && kt == 0 && atomicCAS(status, 0u, kStatusBadKeyLen) == 0u) atomicExch(status + 1, 0u);
+        const int on = block_mask ? (block_mask[(size_t)qt * T + kt] != 0) : 1;
+        const int q0 = qt * kTile;
+        plan[idx] = (uint8_t)tile_class(q0, min(kTile, N - q0), kt * kTile, kTile, kvis, causal, on);
+    }
+}
+
+int bwd_query_block(int d) { return d == 64 ? BwdShape<64>::BQ : BwdShape<128>::BQ; }
+int bwd_smem_bytes(int d) { return d == 64 ? BwdShape<64>::SMEM_BYTES : BwdShape<128>::SMEM_BYTES; }
+
+template <int D>
+static cudaError_t launch_bwd_main_t(const BwdParams &p, cudaStream_t st) {
+    const int smem = BwdShape<D>::SMEM_BYTES;
+    cudaError_t e = cudaFuncSetAttribute(fa_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    fa_bwd_kernel<D><<<(unsigned)p.Tk * (unsigned)p.BH, 256, smem, st>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_main(int d, const BwdParams &p, cudaStream_t st) {
+    return d == 64 ? launch_bwd_main_t<64>(p, st) : launch_bwd_main_t<128>(p, st);
+}
+
+cudaError_t launch_bwd_pre(int d, const void *O, const void *dO, float *Dvec, float *dQacc, int64_t rows,
+                           cudaStream_t st) {
+    const unsigned grid = (unsigned)((rows + 7) / 8);
+    if (d == 64)
+        fa_bwd_pre_kernel<64><<<grid, 256, 0, st>>>((const __nv_bfloat16 *)O, (const __nv_bfloat16 *)dO, Dvec,
+                                                    dQacc, rows);
+    else
+        fa_bwd_pre_kernel<128><<<grid, 256, 0, st>>>((const __nv_bfloat16 *)O, (const __nv_bfloat16 *)dO, Dvec,
+                                                     dQacc, rows);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_convert(int d, const float *dQacc, void *dQ, int64_t elems, float scale,
+                               cudaStream_t st) {
+    (void)d;
+    const int64_t n8 = elems / 8;
+    int64_t blocks = (n8 + 255) / 256;
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    if (blocks < 1) blocks = 1;
+    fa_bwd_convert_kernel<<<(unsigned)blocks, 256, 0, st>>>(dQacc, (__nv_bfloat16 *)dQ, n8, scale);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_plan(int B, int N, int causal, const int32_t *key_len, const uint8_t *block_mask,
+                        uint8_t *plan, unsigned *status, cudaStream_t st) {
+    const int T = (N + kTile - 1) / kTile;
+    const int64_t n = (int64_t)B * T * T;
+    int64_t blocks = (n + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    if (blocks < 1) blocks = 1;
+    fa_plan_kernel<<<(unsigned)blocks, 256, 0, st>>>(B, N, T, causal, key_len, block_mask, plan, status);
+    return cudaGetLastError();
+}
+
+}  // namespace fa

@@ -1,0 +1,30 @@
+// fa_internal.h -- host-side launchers shared by the API translation unit and
+// the kernel translation units (not part of the public ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "fa_tiles.cuh"
+
+namespace fa {
+
+// Forward: one CTA per (query tile, b*h).
+cudaError_t launch_fwd(int d, const FwdParams &p, cudaStream_t st);
+int fwd_smem_bytes(int d);
+
+// Backward: D = rowsum(dO * O) and dQacc = 0; the main kernel; dQ = bf16(scale * dQacc).
+cudaError_t launch_bwd_pre(int d, const void *O, const void *dO, float *Dvec, float *dQacc,
+                           int64_t rows, cudaStream_t st);
+cudaError_t launch_bwd_main(int d, const BwdParams &p, cudaStream_t st);
+cudaError_t launch_bwd_convert(int d, const float *dQacc, void *dQ, int64_t elems, float scale,
+                               cudaStream_t st);
+int bwd_query_block(int d);
+int bwd_smem_bytes(int d);
+
+// Plan export.
+cudaError_t launch_plan(int B, int N, int causal, const int32_t *key_len,
+                        const uint8_t *block_mask, uint8_t *plan, unsigned *status,
+                        cudaStream_t st);
+
+}  // namespace fa

@@ -1,0 +1,72 @@
+// fa_tiles.cuh -- the tile-skipping rule shared by the forward, backward and
+// plan-export kernels, and the kernel parameter blocks.
+//
+// Block-sparse skipping follows the "Attention" chapter (learn-kernels.com,
+// block-sparse paragraph): a block the mask zeroes is never loaded.  Causal
+// and key-padding masks skip the same way whenever a whole tile is masked.
+#pragma once
+
+#include <cuda.h>
+#include <stdint.h>
+
+namespace fa {
+
+constexpr int kTile = 128;           // query/key tile edge = block_mask block edge
+constexpr unsigned kTileSkip = 0, kTileFull = 1, kTilePartial = 2;
+
+// Class of the tile of query rows [q0, q0 + qn) (all < N) and key columns
+// [k0, k0 + kw) (columns >= N count as masked): skip if every element is
+// masked, full if none is, partial otherwise.
+//   kvis     keys < kvis are visible by length: min(N, key_len[b])
+//   mask_on  the tile's block_mask entry (1 when there is no block mask)
+__host__ __device__ __forceinline__ unsigned tile_class(int q0, int qn, int k0, int kw, int kvis,
+                                                        int causal, int mask_on) {
+    const int q_last = q0 + qn - 1, k_last = k0 + kw - 1;
+    if (!mask_on || qn <= 0) return kTileSkip;
+    if (k0 >= kvis) return kTileSkip;
+    if (causal && k0 > q_last) return kTileSkip;
+    const bool full = (k_last < kvis) && (!causal || k_last <= q0);
+    return full ? kTileFull : kTilePartial;
+}
+
+// Visible-key bound for batch b: min(N, key_len[b]) with key_len clamped to
+// [0, N]; out-of-range values are reported through *bad.
+__device__ __forceinline__ int key_visible_bound(const int32_t *key_len, int b, int N, bool *bad) {
+    if (!key_len) return N;
+    int v = key_len[b];
+    if (v < 0 || v > N) {
+        *bad = true;
+        v = v < 0 ? 0 : N;
+    }
+    return v;
+}
+
+struct FwdParams {
+    CUtensorMap tmQ, tmK, tmV;       // [BH][N][d] bf16, box {64, 128, 1}, 128B swizzle
+    void *O;                         // bf16 [BH][N][d]
+    float *LSE;                      // fp32 [BH][N]
+    const int32_t *key_len;          // device [B] or null
+    const uint8_t *block_mask;       // device [nb][nb] or null
+    unsigned *status;                // workspace words 0 (status) and 1 (detail)
+    int H, N, BH, Tq, Tk;
+    int causal;
+    float scale_log2;                // softmax_scale * log2(e)
+};
+
+struct BwdParams {
+    CUtensorMap tmQ, tmdO;           // box {64, BQ, 1}
+    CUtensorMap tmK, tmV;            // box {64, 128, 1}
+    const float *LSE;                // fp32 [BH][N]
+    const float *Dvec;               // fp32 [BH][N]: rowsum(dO * O)
+    float *dQacc;                    // fp32 [BH][N][d]
+    void *dK, *dV;                   // bf16 [BH][N][d]
+    const int32_t *key_len;
+    const uint8_t *block_mask;
+    unsigned *status;
+    int H, N, BH, Tk, Tqb;           // Tqb = ceil(N / BQ)
+    int causal;
+    float scale_log2;                // softmax_scale * log2(e)
+    float scale;                     // softmax_scale
+};
+
+}  // namespace fa

@@ -1,0 +1,99 @@
+"""The C-ABI library loads without a GPU, exports every symbol include/fa.h
+declares, and rejects bad arguments on the host before anything is launched."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import io_aware_exact_09_gb300 as fa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    fa.build()
+    return fa.lib()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "fa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"\b(fa_[a-z_0-9]+)\s*\(", src)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_functions()
+    assert len(names) >= 11
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(fa.EXPORTED)
+
+
+def test_status_strings_and_sizes(L):
+    assert fa.fa_status_string(0) == "ok"
+    assert "timed out" in fa.fa_status_string(5)
+    assert fa.fa_tile_size() == 128
+    assert fa.fa_fwd_workspace_size(1, 2, 128, 64) == 256
+    # status + D [B,H,N] fp32 + dQacc [B,H,N,d] fp32, 256-byte rounded
+    assert fa.fa_bwd_workspace_size(1, 2, 128, 64) == 256 + 1024 + 65536
+    assert fa.fa_bwd_workspace_size(1, 1, 3, 64) == 256 + 256 + 768
+    assert fa.fa_host_workspace_size(1, 2, 128, 64, 1) > fa.fa_host_workspace_size(1, 2, 128, 64, 0)
+
+
+def _fwd(B=1, H=1, N=128, d=64, scale=0.125, ptr=256, ws=256, wsz=256):
+    return fa.lib().fa_fwd(ptr, ptr, ptr, ptr, ptr, B, H, N, d, scale, 0, None, None, ws, wsz, None)
+
+
+def test_forward_argument_errors(L):
+    assert _fwd(d=96) == 2                 # FA_ERR_UNSUPPORTED
+    assert _fwd(d=256) == 2
+    assert _fwd(B=-1) == 1                 # FA_ERR_INVALID_ARGUMENT
+    assert _fwd(scale=float("nan")) == 1
+    assert _fwd(scale=0.0) == 1
+    assert _fwd(scale=-1.0) == 1
+    assert _fwd(ptr=None) == 1
+    assert _fwd(ptr=258) == 1              # misaligned
+    assert _fwd(ws=None) == 3              # FA_ERR_WORKSPACE
+    assert _fwd(wsz=8) == 3
+    assert _fwd(B=0) == 0                  # empty: nothing to do
+    assert _fwd(N=0) == 0
+
+
+def test_backward_and_plan_argument_errors(L):
+    b = fa.lib().fa_bwd
+    ok_ws = fa.fa_bwd_workspace_size(1, 1, 128, 64)
+    assert b(256, 256, 256, 256, 256, 256, 256, 256, 256, 1, 1, 128, 96, 0.1, 0, None, None, 256, ok_ws,
+             None) == 2
+    assert b(256, 256, 256, 256, 256, 256, None, 256, 256, 1, 1, 128, 64, 0.1, 0, None, None, 256, ok_ws,
+             None) == 1
+    assert b(256, 256, 256, 256, 256, 256, 256, 256, 256, 1, 1, 128, 64, 0.1, 0, None, None, 256, ok_ws - 1,
+             None) == 3
+    assert b(256, 256, 256, 256, 256, 256, 256, 256, 256, 0, 1, 128, 64, 0.1, 0, None, None, None, 0,
+             None) == 0
+    p = fa.lib().fa_tile_plan
+    assert p(-1, 128, 0, None, None, 256, 256, 256, None) == 1
+    assert p(1, 128, 0, None, None, None, 256, 256, None) == 1
+    assert p(1, 128, 0, None, None, 256, None, 256, None) == 3
+    assert p(0, 128, 0, None, None, None, None, 0, None) == 0
+
+
+def test_host_path_argument_errors(L):
+    h = fa.lib().fa_attention_host
+    assert h(256, 256, 256, None, 256, 256, None, None, None, 1, 1, 128, 80, 0.1, 0, None, None, 256, 1 << 30,
+             None) == 2
+    assert h(256, 256, 256, 256, 256, 256, None, 256, 256, 1, 1, 128, 64, 0.1, 0, None, None, 256, 1 << 30,
+             None) == 1  # backward requested without dQ
+    assert h(256, 256, 256, None, 256, 256, None, None, None, 1, 1, 128, 64, 0.1, 0, None, None, 256, 16,
+             None) == 3
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    import importlib
+    mod = importlib.import_module("io_aware_exact_09_gb300")
+    monkeypatch.setattr(mod, "_lib", None)
+    monkeypatch.setattr(mod, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError):
+        mod.lib()

@@ -1,0 +1,117 @@
+"""Parity at the workloads' full sizes, in the launch configuration the
+benchmark times: the CUDA path runs on the whole workload; the oracle checks
+sampled query rows (O, LSE, dQ) and sampled key rows (dK, dV), which it
+computes one by one from the plain definition."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from synthetic import WORKLOADS, make_inputs
+from gpu_common import GRAD_REL_FRO, LSE_MAX_ABS, O_MAX_ABS, O_REL_FRO, f64, oracle_args, rel_fro, run_cuda
+
+pytestmark = pytest.mark.gpu
+
+FULL = ["gpt2m_causal_b8h16n1024d64", "bertl_keypad_b16h16n512d64", "longctx_b1h16n16384d128",
+        "longctx_causal_b1h16n16384d128", "blocksparse_b2h16n8192d64"]
+
+
+def sample_rows(B, H, N, rng, n_heads=2, per_head=24):
+    """Flat (b*H+h)*N+i indices: first and last head plus random ones; in
+    each, the first and last row, the rows around tile edges, random rows."""
+    BH = B * H
+    heads = sorted(set([0, BH - 1] + list(rng.choice(BH, size=min(BH, n_heads), replace=False))))
+    rows = []
+    for bh in heads:
+        pick = {0, N - 1, min(127, N - 1), min(128, N - 1)}
+        pick |= set(int(x) for x in rng.choice(N, size=min(N, per_head), replace=False))
+        rows += [bh * N + i for i in sorted(pick)]
+    return np.array(rows, np.int64), heads
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled(name):
+    w = WORKLOADS[name]
+    case = make_inputs(w)
+    got = run_cuda(case)
+    B, H, N, d = w.B, w.H, w.N, w.d
+    rng = np.random.default_rng(2024)
+    qrows, _ = sample_rows(B, H, N, rng)
+    Q, K, V, dO = (f64(case[k]) for k in ("Q", "K", "V", "dO"))
+    oa = oracle_args(case)
+    O_r, L_r, dQ_r = oracle.query_rows(Q, K, V, dO, case["scale"], qrows, **oa)
+    flat = lambda X: X.reshape(B * H * N, -1)
+    gO, gL, gdQ = flat(got["O"])[qrows], got["LSE"].reshape(-1)[qrows], flat(got["dQ"])[qrows]
+    assert np.all(np.isfinite(gO)) and np.all(np.isfinite(gdQ))
+    assert rel_fro(gO, O_r) <= O_REL_FRO, rel_fro(gO, O_r)
+    assert np.max(np.abs(gO - O_r)) <= O_MAX_ABS
+    fin = np.isfinite(L_r)
+    assert np.max(np.abs(gL[fin] - L_r[fin])) <= LSE_MAX_ABS
+    assert rel_fro(gdQ, dQ_r) <= GRAD_REL_FRO, rel_fro(gdQ, dQ_r)
+    # key rows: dK, dV need every query row of the head, so fewer heads
+    krows, _ = sample_rows(B, H, N, np.random.default_rng(7), n_heads=0, per_head=12)
+    if N * N * d > 2 ** 34:
+        krows = krows[krows < N]          # one head only at the longest lengths
+    dK_r, dV_r = oracle.key_rows(Q, K, V, dO, case["scale"], krows, **oa)
+    gdK, gdV = flat(got["dK"])[krows], flat(got["dV"])[krows]
+    assert rel_fro(gdK, dK_r) <= GRAD_REL_FRO, rel_fro(gdK, dK_r)
+    assert rel_fro(gdV, dV_r) <= GRAD_REL_FRO, rel_fro(gdV, dV_r)
+    # properties that hold at any size, on every row
+    for k in ("O", "dQ", "dK", "dV"):
+        assert np.all(np.isfinite(got[k])), k
+
+
+def test_tile_plan_bit_exact_on_workloads():
+    import io_aware_exact_09_gb300 as fa
+    for name in ("gpt2m_causal_b8h16n1024d64", "bertl_keypad_b16h16n512d64", "blocksparse_b2h16n8192d64",
+                 "longctx_causal_b1h16n16384d128"):
+        w = WORKLOADS[name]
+        case = make_inputs(w, with_dO=False)
+        kl = case["key_len"]
+        bm = case["block_mask"]
+        got = fa.tile_plan(w.B, w.N, w.causal, None if kl is None else kl.cuda(),
+                           None if bm is None else bm.cuda()).cpu().numpy()
+        ref = oracle.tile_plan(w.B, w.N, w.causal, None if kl is None else kl.numpy(),
+                               None if bm is None else bm.numpy())
+        assert np.array_equal(got, ref), name
+
+
+@pytest.mark.parametrize("N", [1, 100, 300, 1000])
+def test_tile_plan_bit_exact_ragged(N):
+    import io_aware_exact_09_gb300 as fa
+    rng = np.random.default_rng(N)
+    T = (N + 127) // 128
+    kl = rng.integers(0, N + 1, size=3).astype(np.int32)
+    bm = (rng.random((T, T)) < 0.6).astype(np.uint8)
+    for causal in (False, True):
+        for use_kl in (False, True):
+            for use_bm in (False, True):
+                got = fa.tile_plan(3, N, causal, torch.from_numpy(kl).cuda() if use_kl else None,
+                                   torch.from_numpy(bm).cuda() if use_bm else None)
+                ref = oracle.tile_plan(3, N, causal, kl if use_kl else None, bm if use_bm else None)
+                assert np.array_equal(got.cpu().numpy(), ref), (N, causal, use_kl, use_bm)
+
+
+def test_host_buffer_path_matches_device_path():
+    import io_aware_exact_09_gb300 as fa
+    w = WORKLOADS["bertl_keypad_b16h16n512d64"]
+    case = make_inputs(w)
+    B, H, N, d = w.B, w.H, w.N, w.d
+    pin = lambda t: t.contiguous().pin_memory()
+    Qh, Kh, Vh, dOh = (pin(case[k]) for k in ("Q", "K", "V", "dO"))
+    O = torch.empty_like(Qh).pin_memory()
+    LSE = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    dQ, dK, dV = (torch.empty_like(Qh).pin_memory() for _ in range(3))
+    kl = case["key_len"].contiguous()
+    need = fa.fa_host_workspace_size(B, H, N, d, 1)
+    ws = fa.workspace(need, "cuda")
+    st = fa.fa_attention_host(Qh, Kh, Vh, dOh, O, LSE, dQ, dK, dV, B, H, N, d, case["scale"], False, kl,
+                              None, ws, ws.numel())
+    assert st == 0, fa.fa_status_string(st)
+    dev = run_cuda(case)
+    assert np.array_equal(O.double().numpy(), dev["O"])
+    assert np.array_equal(LSE.double().numpy(), dev["LSE"])
+    assert np.array_equal(dK.double().numpy(), dev["dK"])
+    assert np.array_equal(dV.double().numpy(), dev["dV"])
+    # dQ goes through fp32 atomics whose order varies: compare within tolerance
+    assert rel_fro(dQ.double().numpy(), dev["dQ"]) < 1e-3

@@ -1,0 +1,116 @@
+"""CUDA path vs the fp64 oracle, element by element, on seeded inputs that
+span several tiles and a ragged tail, every mask kind and the edge cases."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from synthetic import WORKLOADS, make_case, make_inputs
+from gpu_common import (check_forward, check_grads, f64, oracle_args, run_cuda)
+
+pytestmark = pytest.mark.gpu
+
+
+def full_oracle(case):
+    O, LSE, dQ, dK, dV = oracle.attention_bwd(f64(case["Q"]), f64(case["K"]), f64(case["V"]),
+                                              f64(case["dO"]), case["scale"], **oracle_args(case))
+    return dict(O=O, LSE=LSE, dQ=dQ, dK=dK, dV=dV)
+
+
+def compare(case, label):
+    got = run_cuda(case)
+    ref = full_oracle(case)
+    check_forward(got["O"], got["LSE"], ref["O"], ref["LSE"], label)
+    check_grads(got, ref, label)
+
+
+def test_small_workload_exact_config():
+    w = WORKLOADS["small_b1h2n128d64"]
+    compare(make_inputs(w), w.name)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N", [1, 17, 128, 129, 200, 300, 512])
+def test_ragged_lengths_no_mask(d, N):
+    c = make_case(1, 2, N, d, seed=100 + N + d)
+    c["scale"] = 1.0 / d ** 0.5
+    compare(c, "N=%d d=%d" % (N, d))
+
+
+MASKS = {
+    "causal": dict(causal=True),
+    "keylen": dict(key_len=[300, 131]),
+    "sparse": dict(block_mask=[[1, 0, 1], [0, 1, 0], [1, 1, 1]]),
+    "all": dict(causal=True, key_len=[250, 300], block_mask=[[1, 0, 0], [1, 1, 0], [0, 1, 1]]),
+}
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("kind", sorted(MASKS))
+def test_masks_ragged(d, kind):
+    c = make_case(2, 2, 300, d, seed=7 + d, **MASKS[kind])
+    c["scale"] = 1.0 / d ** 0.5
+    compare(c, "%s d=%d" % (kind, d))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_every_mask_combination_n512(d):
+    bm = np.ones((4, 4), np.uint8)
+    bm[0, 1] = bm[2, 0] = bm[3, 1] = bm[1, 3] = 0
+    for causal in (False, True):
+        for kl in (None, [512, 200]):
+            for m in (None, bm):
+                c = make_case(2, 1, 512, d, seed=11, causal=causal, key_len=kl, block_mask=m)
+                c["scale"] = 1.0 / d ** 0.5
+                compare(c, "combo c=%s kl=%s m=%s d=%d" % (causal, kl is not None, m is not None, d))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_fully_masked_rows_and_zero_length(d):
+    # batch 0 has no visible key at all; batch 1 only the first key
+    c = make_case(2, 2, 160, d, seed=3, key_len=[0, 1])
+    c["scale"] = 1.0 / d ** 0.5
+    got = run_cuda(c)
+    ref = full_oracle(c)
+    check_forward(got["O"], got["LSE"], ref["O"], ref["LSE"], "kl0")
+    assert np.all(got["dQ"][0] == 0) and np.all(got["dK"][0] == 0) and np.all(got["dV"][0] == 0)
+    check_grads(got, ref, "kl0")
+    # a block mask that removes every block of one query block-row
+    bm = np.array([[0, 0], [1, 1]], np.uint8)
+    c2 = make_case(1, 2, 256, d, seed=4, block_mask=bm)
+    c2["scale"] = 1.0 / d ** 0.5
+    got2 = run_cuda(c2)
+    ref2 = full_oracle(c2)
+    check_forward(got2["O"], got2["LSE"], ref2["O"], ref2["LSE"], "row-block masked")
+    check_grads(got2, ref2, "row-block masked")
+
+
+def test_large_scores_and_other_scale():
+    # scores of magnitude ~50: exercises the running-maximum rescale
+    c = make_case(1, 2, 384, 64, seed=21, input_scale=3.0)
+    c["scale"] = 0.7
+    compare(c, "large scores")
+
+
+def test_key_len_out_of_range_is_clamped_and_flagged():
+    import io_aware_exact_09_gb300 as fa
+    c = make_case(2, 1, 200, 64, seed=5, key_len=[-3, 500])
+    c["scale"] = 0.125
+    dev = {k: c[k].cuda() for k in ("Q", "K", "V")}
+    kl = c["key_len"].cuda()
+    ws = fa.workspace(256, "cuda")
+    O, LSE = fa.attention_forward(dev["Q"], dev["K"], dev["V"], 0.125, False, kl, None, ws=ws)
+    assert fa.fa_get_device_status(ws) == 6
+    ref_O, ref_L = oracle.attention_fwd(f64(c["Q"]), f64(c["K"]), f64(c["V"]), 0.125, key_len=[0, 200])
+    check_forward(O.double().cpu().numpy(), LSE.double().cpu().numpy(), ref_O, ref_L, "clamped")
+    assert fa.fa_reset_device_status(ws) == 0
+    assert fa.fa_get_device_status(ws) == 0
+
+
+def test_repeat_calls_are_deterministic_forward():
+    import io_aware_exact_09_gb300 as fa
+    c = make_case(1, 4, 1000, 128, seed=9, causal=True)
+    g = {k: c[k].cuda() for k in ("Q", "K", "V")}
+    O1, L1 = fa.attention_forward(g["Q"], g["K"], g["V"], causal=True)
+    O2, L2 = fa.attention_forward(g["Q"], g["K"], g["V"], causal=True)
+    assert torch.equal(O1, O2) and torch.equal(L1, L2)
