@@ -1,0 +1,426 @@
+#!/usr/bin/env python
+"""Benchmark: one step = the whole hot path (forward + backward) of exact
+attention on one seeded synthetic workload, through the C ABI.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0).  ``value`` is forward+backward TFLOP/s
+(algorithmic FLOPs: 4*B*H*N^2*d forward, halved for causal, x3.5 for
+forward+backward; masked pairs are not counted) over all ranks, timed with
+CUDA events on the launching stream, inputs resident in HBM, L2 flushed
+between steps.  ``e2e`` is the same metric through ``fa_attention_host``
+with pinned host buffers (copies inside the timed region).  Under torchrun
+every rank runs its own replica of the workload (weak scaling, no data-path
+collective); the time is the max over ranks.
+
+``--impl reference`` times the fp64 CPU oracle instead, on a bounded sample
+of the same workload, on this machine's host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "longctx_b1h16n16384d128"
+FWD_BWD_FACTOR = 3.5          # forward + backward = forward x (1 + 2.5)
+KERNEL_SOURCES = {"fa_fwd_kernel": "fa_fwd.cu", "fa_bwd_kernel": "fa_bwd.cu"}
+
+
+# ---------------------------------------------------------------- distributed helpers
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(backend):
+    import torch.distributed as dist
+    ws, rank, _ = dist_env()
+    if ws > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return ws, rank
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def reduce_max(x: float, device=None) -> float:
+    """Max of a float over ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_rank_step: float, world: int, step_s: float) -> float:
+    """Aggregate throughput: the units every rank processed / the slowest rank's time."""
+    return flops_per_rank_step * world / step_s / 1e12
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples every 200 ms during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        hi = max(sm)
+        loaded = [s for s in sm if s >= 0.5 * hi] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- peaks / profiles
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def source_digest(fname: str) -> str:
+    h = hashlib.sha256()
+    for f in sorted({fname, "fa_ptx.cuh", "fa_tiles.cuh"}):
+        with open(os.path.join(ROOT, "io_aware_exact_09_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it
+    was taken on the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rows = json.load(f)
+    r = rows.get(kernel, {}).get(workload)
+    if not r or r.get("source_digest") != source_digest(KERNEL_SOURCES[kernel]):
+        return None
+    return r.get("bytes_per_launch")
+
+
+# ---------------------------------------------------------------- CPU oracle baseline
+def _oracle_case(w, n):
+    import torch
+
+    from synthetic import Workload, make_inputs
+    sub = Workload(w.name, 1, 1, n, w.d, w.seed, causal=w.causal, input_scale=w.input_scale,
+                   sparse_density=w.sparse_density)
+    c = make_inputs(sub)
+    kl = [max(1, int(n * 0.625))] if w.key_len_range is not None else None   # mean of U[128,512] / 512
+    Q, K, V, dO = (c[k].to(torch.float64).numpy() for k in ("Q", "K", "V", "dO"))
+    bm = None if c["block_mask"] is None else c["block_mask"].numpy()
+    return Q, K, V, dO, kl, bm
+
+
+def oracle_time(w, n):
+    """One fp64 oracle forward+backward on one head of the workload truncated
+    to its first n tokens: (TFLOP/s, seconds)."""
+    import oracle
+    from synthetic import algorithmic_fwd_flops
+    Q, K, V, dO, kl, bm = _oracle_case(w, n)
+    t0 = time.perf_counter()
+    oracle.attention_bwd(Q, K, V, dO, w.softmax_scale, causal=w.causal, key_len=kl, block_mask=bm)
+    dt = time.perf_counter() - t0
+    fl = FWD_BWD_FACTOR * algorithmic_fwd_flops(1, 1, n, w.d, w.causal, kl, bm)
+    return fl / dt / 1e12, dt
+
+
+def oracle_calibrate(w, budget_s: float):
+    """Largest power-of-two prefix length n (<= N, <= 8192) whose oracle call
+    stays near budget_s."""
+    n = 128
+    while True:
+        _, dt = oracle_time(w, n)
+        if dt * 4.5 > budget_s or 2 * n > min(w.N, 8192):
+            return n
+        n *= 2
+
+
+def oracle_sample(w, budget_s: float, n=None):
+    """Time the fp64 oracle on a bounded sample; returns (TFLOP/s, cores, description)."""
+    import oracle
+    if n is None:
+        n = oracle_calibrate(w, budget_s)
+    tf, dt = oracle_time(w, n)
+    desc = ("fp64 oracle fwd+bwd (materialised S and P), one head of %s truncated to its first %d tokens, "
+            "d=%d, %.2f s per call" % (w.name, n, w.d, dt))
+    return tf, oracle.num_threads(), desc
+
+
+# ---------------------------------------------------------------- reference arm
+def run_reference(args):
+    ws, rank = init_dist("gloo")
+    if rank != 0:
+        return 0
+    from synthetic import WORKLOADS
+    import oracle
+    oracle.build()
+    w = WORKLOADS[args.workload]
+    vals = []
+    desc = cores = None
+    n = oracle_calibrate(w, budget_s=6.0)
+    for i in range(args.warmup + args.steps):
+        tf, cores, desc = oracle_sample(w, 6.0, n)
+        if i >= args.warmup:
+            vals.append(tf)
+    v = statistics.median(vals)
+    line = {"impl": "reference", "metric": "attention fwd+bwd TFLOP/s (bf16)", "value": v, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal},
+            "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc},
+            "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args):
+    import torch
+
+    ws_n, rank = init_dist("nccl")
+    _, _, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import io_aware_exact_09_gb300 as fa
+    from synthetic import WORKLOADS, algorithmic_fwd_flops, make_inputs
+    fa.build()
+    w = WORKLOADS[args.workload]
+    B, H, N, d = w.B, w.H, w.N, w.d
+    case = make_inputs(w)
+    Q, K, V, dO = (case[k].to(dev).contiguous() for k in ("Q", "K", "V", "dO"))
+    kl = None if case["key_len"] is None else case["key_len"].to(dev)
+    bm = None if case["block_mask"] is None else case["block_mask"].contiguous().to(dev)
+    scale = w.softmax_scale
+    O = torch.empty_like(Q)
+    LSE = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
+    wsb = fa.fa_bwd_workspace_size(B, H, N, d)
+    wsf = fa.fa_fwd_workspace_size(B, H, N, d)
+    ws_f = fa.workspace(wsf, dev)
+    ws_b = fa.workspace(wsb, dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    flops_fwd = algorithmic_fwd_flops(B, H, N, d, w.causal,
+                                      None if case["key_len"] is None else case["key_len"].tolist(),
+                                      None if case["block_mask"] is None else case["block_mask"])
+    flops_step = FWD_BWD_FACTOR * flops_fwd
+    flops_main = 2.5 * flops_fwd
+
+    def check(st, where):
+        if st != 0:
+            raise RuntimeError("%s failed: %s" % (where, fa.fa_status_string(st)))
+
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+
+    def step(record):
+        if record:
+            ev[0].record(stream)
+        check(fa.fa_fwd(Q, K, V, O, LSE, B, H, N, d, scale, w.causal, kl, bm, ws_f, wsf, sp), "fa_fwd")
+        if record:
+            ev[1].record(stream)
+        check(fa.fa_bwd_preprocess(O, dO, B, H, N, d, ws_b, wsb, sp), "fa_bwd_preprocess")
+        if record:
+            ev[2].record(stream)
+        check(fa.fa_bwd_main(Q, K, V, LSE, dO, dK, dV, B, H, N, d, scale, w.causal, kl, bm, ws_b, wsb, sp),
+              "fa_bwd_main")
+        if record:
+            ev[3].record(stream)
+        check(fa.fa_bwd_postprocess(dQ, B, H, N, d, scale, ws_b, wsb, sp), "fa_bwd_postprocess")
+        if record:
+            ev[4].record(stream)
+
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)     # 256 MiB > 129 MB L2
+    for _ in range(args.warmup):
+        step(False)
+    torch.cuda.synchronize(dev)
+    for wsx in (ws_f, ws_b):
+        st = fa.fa_get_device_status(wsx, sp)
+        check(st, "device status after warm-up")
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    times = {"step": [], "fwd": [], "pre": [], "main": [], "post": []}
+    barrier()
+    torch.cuda.synchronize(dev)
+    launches = 0
+    for _ in range(args.steps):
+        flush.zero_()                                   # evict L2 between steps (not timed)
+        step(True)
+        launches += 4
+        ev[4].synchronize()
+        times["fwd"].append(ev[0].elapsed_time(ev[1]))
+        times["pre"].append(ev[1].elapsed_time(ev[2]))
+        times["main"].append(ev[2].elapsed_time(ev[3]))
+        times["post"].append(ev[3].elapsed_time(ev[4]))
+        times["step"].append(ev[0].elapsed_time(ev[4]))
+    torch.cuda.synchronize(dev)
+    barrier()
+    clk = clocks.stop()
+    for wsx in (ws_f, ws_b):
+        check(fa.fa_get_device_status(wsx, sp), "device status after timing")
+
+    mean = {k: sum(v) / len(v) for k, v in times.items()}
+    step_ms = reduce_max(mean["step"], dev)
+    value = whole_job_tflops(flops_step, ws_n, step_ms / 1e3)
+    fwd_tf = flops_fwd / (mean["fwd"] / 1e3) / 1e12
+    bwd_tf = 2.5 * flops_fwd / ((mean["pre"] + mean["main"] + mean["post"]) / 1e3) / 1e12
+
+    peaks, peak_src = measured_peaks()
+    peak_tf = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    # dominant kernel of the step
+    dom = "fa_bwd_kernel" if mean["main"] >= mean["fwd"] else "fa_fwd_kernel"
+    dom_ms = mean["main"] if dom == "fa_bwd_kernel" else mean["fwd"]
+    dom_flops = flops_main if dom == "fa_bwd_kernel" else flops_fwd
+    achieved = dom_flops / (dom_ms / 1e3) / 1e12
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
+                "frac": achieved / peak_tf, "traffic": ncu_traffic(dom, w.name),
+                "peak_source": "%s bf16_tflops_sustained (kernel timed inside a continuous step loop)" % peak_src}
+
+    # end-to-end through the host-buffer entry point (pinned memory, copies timed)
+    e2e = None
+    if not args.no_e2e:
+        pin = lambda t: t.contiguous().pin_memory()
+        Qh, Kh, Vh, dOh = (pin(case[k]) for k in ("Q", "K", "V", "dO"))
+        Oh = torch.empty_like(Qh).pin_memory()
+        Lh = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+        dQh, dKh, dVh = (torch.empty_like(Qh).pin_memory() for _ in range(3))
+        klh = None if case["key_len"] is None else case["key_len"].contiguous()
+        bmh = None if case["block_mask"] is None else case["block_mask"].contiguous()
+        hws_n = fa.fa_host_workspace_size(B, H, N, d, 1)
+        del flush
+        hws = fa.workspace(hws_n, dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        et = []
+        n_e2e = max(1, min(args.steps, 5))
+        for i in range(1 + n_e2e):
+            e0.record(stream)
+            check(fa.fa_attention_host(Qh, Kh, Vh, dOh, Oh, Lh, dQh, dKh, dVh, B, H, N, d, scale, w.causal, klh,
+                                       bmh, hws, hws_n, sp), "fa_attention_host")
+            e1.record(stream)
+            e1.synchronize()
+            if i > 0:
+                et.append(e0.elapsed_time(e1))
+            launches += 0
+        e_ms = reduce_max(sum(et) / len(et), dev)
+        nbytes = B * H * N * d * 2
+        e2e = {"value": whole_job_tflops(flops_step, ws_n, e_ms / 1e3), "unit": "TFLOP/s",
+               "h2d_bytes_per_step": 4 * nbytes + (0 if klh is None else 4 * B) + (0 if bmh is None else bmh.numel()),
+               "d2h_bytes_per_step": 4 * nbytes + B * H * N * 4, "ms_per_step": e_ms}
+
+    cpu = None
+    if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
+        tf, cores, desc = oracle_sample(w, budget_s=args.cpu_budget)
+        cpu = {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc}
+
+    if rank == 0:
+        line = {
+            "metric": "attention fwd+bwd TFLOP/s (bf16)", "value": value, "unit": "TFLOP/s", "n_gpus": ws_n,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "B": B, "H": H, "N": N, "d": d, "causal": w.causal,
+                       "key_padding": case["key_len"] is not None, "block_sparse": case["block_mask"] is not None,
+                       "parallelism": "replicas" if ws_n > 1 else "single", "l2": "flushed between steps"},
+            "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
+            "fwd_frac_of_peak": fwd_tf / peak_tf, "bwd_frac_of_peak": bwd_tf / peak_tf,
+            "fwd_bwd_frac_of_peak": value / ws_n / peak_tf,
+            "kernel_ms": {"fa_fwd_kernel": mean["fwd"], "fa_bwd_pre_kernel": mean["pre"],
+                          "fa_bwd_kernel": mean["main"], "fa_bwd_convert_kernel": mean["post"]},
+            "algorithmic_flops_per_step": flops_step,
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
+            "gpu_launches": launches,
+        }
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -106,6 +106,26 @@ fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, con
                  void *stream);
 
 /*
+ * fa_bwd in its three stages, for callers that want to schedule or time them
+ * separately.  Same arguments and preconditions as fa_bwd; the stages must be
+ * enqueued in this order on one stream with the same workspace.
+ *   fa_bwd_preprocess:  D = rowsum(dO * O) (fp32) and dQ accumulator = 0
+ *                       (reads O, dO; writes the workspace).
+ *   fa_bwd_main:        one CTA per 128-key tile: recompute S^T and P^T,
+ *                       dP^T, dS^T; write dK, dV; add dQ contributions into
+ *                       the workspace accumulator.
+ *   fa_bwd_postprocess: dQ = bf16(softmax_scale * accumulator).
+ */
+fa_status fa_bwd_preprocess(const void *O, const void *dO, int B, int H, int N, int d,
+                            void *workspace, size_t workspace_bytes, void *stream);
+fa_status fa_bwd_main(const void *Q, const void *K, const void *V, const float *LSE, const void *dO,
+                      void *dK, void *dV, int B, int H, int N, int d, float softmax_scale,
+                      int causal, const int32_t *key_len, const uint8_t *block_mask,
+                      void *workspace, size_t workspace_bytes, void *stream);
+fa_status fa_bwd_postprocess(void *dQ, int B, int H, int N, int d, float softmax_scale,
+                             const void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * The tile-skipping decisions the kernels take, exported so that they can be
  * checked exactly.  plan: device uint8 [B][T][T], T = ceil(N / 128), written
  * with 0 = skip (every element of the 128 x 128 tile masked; the tile is

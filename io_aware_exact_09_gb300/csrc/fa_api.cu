@@ -144,28 +144,54 @@ fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LS
     return fa::launch_fwd(d, p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, const float *LSE, const void *dO,
-                 void *dQ, void *dK, void *dV, int B, int H, int N, int d, float softmax_scale, int causal,
-                 const int32_t *key_len, const uint8_t *block_mask, void *workspace, size_t workspace_bytes,
-                 void *stream) {
-    bool empty = false;
-    fa_status st = check_sizes(B, H, N, d, &empty);
+namespace {
+struct BwdWs {
+    unsigned *status;
+    float *Dvec, *dQacc;
+};
+BwdWs bwd_ws(void *workspace, int B, int H, int N) {
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const size_t rows = (size_t)B * H * N;
+    return BwdWs{reinterpret_cast<unsigned *>(ws), reinterpret_cast<float *>(ws + kStatusBytes),
+                 reinterpret_cast<float *>(ws + kStatusBytes + round256(rows * 4))};
+}
+fa_status bwd_common_checks(int B, int H, int N, int d, float scale, void *workspace, size_t workspace_bytes,
+                            bool *empty) {
+    fa_status st = check_sizes(B, H, N, d, empty);
     if (st != FA_OK) return st;
-    if (!scale_ok(softmax_scale)) return FA_ERR_INVALID_ARGUMENT;
-    if (empty) return FA_OK;
-    const void *ptrs[] = {Q, K, V, O, LSE, dO, dQ, dK, dV};
-    for (const void *x : ptrs)
-        if (!x || !aligned16(x)) return FA_ERR_INVALID_ARGUMENT;
+    if (!scale_ok(scale)) return FA_ERR_INVALID_ARGUMENT;
+    if (*empty) return FA_OK;
     if (!workspace || !aligned16(workspace) || workspace_bytes < fa_bwd_workspace_size(B, H, N, d))
         return FA_ERR_WORKSPACE;
+    return FA_OK;
+}
+}  // namespace
 
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
+fa_status fa_bwd_preprocess(const void *O, const void *dO, int B, int H, int N, int d, void *workspace,
+                            size_t workspace_bytes, void *stream) {
+    bool empty = false;
+    fa_status st = bwd_common_checks(B, H, N, d, 1.f, workspace, workspace_bytes, &empty);
+    if (st != FA_OK || empty) return st;
+    if (!O || !dO || !aligned16(O) || !aligned16(dO)) return FA_ERR_INVALID_ARGUMENT;
+    const BwdWs w = bwd_ws(workspace, B, H, N);
+    return fa::launch_bwd_pre(d, O, dO, w.Dvec, w.dQacc, (int64_t)B * H * N, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? FA_OK
+               : FA_ERR_CUDA;
+}
+
+fa_status fa_bwd_main(const void *Q, const void *K, const void *V, const float *LSE, const void *dO, void *dK,
+                      void *dV, int B, int H, int N, int d, float softmax_scale, int causal,
+                      const int32_t *key_len, const uint8_t *block_mask, void *workspace,
+                      size_t workspace_bytes, void *stream) {
+    bool empty = false;
+    fa_status st = bwd_common_checks(B, H, N, d, softmax_scale, workspace, workspace_bytes, &empty);
+    if (st != FA_OK || empty) return st;
+    const void *ptrs[] = {Q, K, V, LSE, dO, dK, dV};
+    for (const void *x : ptrs)
+        if (!x || !aligned16(x)) return FA_ERR_INVALID_ARGUMENT;
+    const BwdWs w = bwd_ws(workspace, B, H, N);
     const int BH = B * H;
-    const int64_t rows = (int64_t)BH * N;
-    uint8_t *ws = static_cast<uint8_t *>(workspace);
-    float *Dvec = reinterpret_cast<float *>(ws + kStatusBytes);
-    float *dQacc = reinterpret_cast<float *>(ws + kStatusBytes + round256((size_t)rows * 4));
-
     BwdParams p;
     std::memset(&p, 0, sizeof(p));
     const int BQ = fa::bwd_query_block(d);
@@ -173,13 +199,13 @@ fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, con
         !encode_bf16_3d(&p.tmK, K, d, N, BH, 128) || !encode_bf16_3d(&p.tmV, V, d, N, BH, 128))
         return FA_ERR_CUDA;
     p.LSE = LSE;
-    p.Dvec = Dvec;
-    p.dQacc = dQacc;
+    p.Dvec = w.Dvec;
+    p.dQacc = w.dQacc;
     p.dK = dK;
     p.dV = dV;
     p.key_len = key_len;
     p.block_mask = block_mask;
-    p.status = reinterpret_cast<unsigned *>(ws);
+    p.status = w.status;
     p.H = H;
     p.N = N;
     p.BH = BH;
@@ -188,11 +214,39 @@ fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, con
     p.causal = causal ? 1 : 0;
     p.scale_log2 = softmax_scale * kLog2e;
     p.scale = softmax_scale;
+    return fa::launch_bwd_main(d, p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
 
-    if (fa::launch_bwd_pre(d, O, dO, Dvec, dQacc, rows, s) != cudaSuccess) return FA_ERR_CUDA;
-    if (fa::launch_bwd_main(d, p, s) != cudaSuccess) return FA_ERR_CUDA;
-    if (fa::launch_bwd_convert(d, dQacc, dQ, rows * d, softmax_scale, s) != cudaSuccess) return FA_ERR_CUDA;
-    return FA_OK;
+fa_status fa_bwd_postprocess(void *dQ, int B, int H, int N, int d, float softmax_scale, const void *workspace,
+                             size_t workspace_bytes, void *stream) {
+    bool empty = false;
+    fa_status st =
+        bwd_common_checks(B, H, N, d, softmax_scale, const_cast<void *>(workspace), workspace_bytes, &empty);
+    if (st != FA_OK || empty) return st;
+    if (!dQ || !aligned16(dQ)) return FA_ERR_INVALID_ARGUMENT;
+    const BwdWs w = bwd_ws(const_cast<void *>(workspace), B, H, N);
+    return fa::launch_bwd_convert(d, w.dQacc, dQ, (int64_t)B * H * N * d, softmax_scale,
+                                  static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? FA_OK
+               : FA_ERR_CUDA;
+}
+
+fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, const float *LSE, const void *dO,
+                 void *dQ, void *dK, void *dV, int B, int H, int N, int d, float softmax_scale, int causal,
+                 const int32_t *key_len, const uint8_t *block_mask, void *workspace, size_t workspace_bytes,
+                 void *stream) {
+    bool empty = false;
+    fa_status st = bwd_common_checks(B, H, N, d, softmax_scale, workspace, workspace_bytes, &empty);
+    if (st != FA_OK || empty) return st;
+    const void *ptrs[] = {Q, K, V, O, LSE, dO, dQ, dK, dV};
+    for (const void *x : ptrs)
+        if (!x || !aligned16(x)) return FA_ERR_INVALID_ARGUMENT;
+    st = fa_bwd_preprocess(O, dO, B, H, N, d, workspace, workspace_bytes, stream);
+    if (st != FA_OK) return st;
+    st = fa_bwd_main(Q, K, V, LSE, dO, dK, dV, B, H, N, d, softmax_scale, causal, key_len, block_mask, workspace,
+                     workspace_bytes, stream);
+    if (st != FA_OK) return st;
+    return fa_bwd_postprocess(dQ, B, H, N, d, softmax_scale, workspace, workspace_bytes, stream);
 }
 
 fa_status fa_tile_plan(int B, int N, int causal, const int32_t *key_len, const uint8_t *block_mask,

@@ -86,8 +86,13 @@ def test_fully_masked_rows_and_zero_length(d):
 
 
 def test_large_scores_and_other_scale():
-    # scores of magnitude ~50: exercises the running-maximum rescale
-    c = make_case(1, 2, 384, 64, seed=21, input_scale=3.0)
+    # Q, K scaled by 3 and scale 0.7: scores with standard deviation ~50, so
+    # the running maximum moves often and the softmax is nearly one-hot.  V
+    # stays N(0, 1) so that the absolute bound keeps its meaning (bf16 P
+    # carries a relative rounding of 2^-9 into O).
+    c = make_case(1, 2, 384, 64, seed=21)
+    c["Q"] = (c["Q"].float() * 3).to(torch.bfloat16)
+    c["K"] = (c["K"].float() * 3).to(torch.bfloat16)
     c["scale"] = 0.7
     compare(c, "large scores")
 
