@@ -57,6 +57,20 @@ bool encode_bf16_3d(CUtensorMap *m, const void *ptr, int d, int N, int BH, int b
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D fp32 view [BH][N][d] of the dQ accumulator; box of 32 columns (128
+// bytes) x box_rows rows, 128-byte swizzle (target of the TMA reduce-add).
+bool encode_f32_3d(CUtensorMap *m, const void *ptr, int d, int N, int BH, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)N * d * 4};
+    cuuint32_t box[3] = {32, (cuuint32_t)box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Checks shared by fa_fwd / fa_bwd / fa_tile_plan.  Returns FA_OK, or the
 // error to report; *empty is set when there is nothing to compute.
 fa_status check_sizes(int B, int H, int N, int d, bool *empty) {
@@ -196,7 +210,8 @@ fa_status fa_bwd_main(const void *Q, const void *K, const void *V, const float *
     std::memset(&p, 0, sizeof(p));
     const int BQ = fa::bwd_query_block(d);
     if (!encode_bf16_3d(&p.tmQ, Q, d, N, BH, BQ) || !encode_bf16_3d(&p.tmdO, dO, d, N, BH, BQ) ||
-        !encode_bf16_3d(&p.tmK, K, d, N, BH, 128) || !encode_bf16_3d(&p.tmV, V, d, N, BH, 128))
+        !encode_bf16_3d(&p.tmK, K, d, N, BH, 128) || !encode_bf16_3d(&p.tmV, V, d, N, BH, 128) ||
+        !encode_f32_3d(&p.tmdQ, w.dQacc, d, N, BH, fa::bwd_dq_box_rows(d)))
         return FA_ERR_CUDA;
     p.LSE = LSE;
     p.Dvec = w.Dvec;

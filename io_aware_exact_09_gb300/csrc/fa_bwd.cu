@@ -22,8 +22,9 @@
 //        warps 4-7  one key row per thread: P^T = 2^(s*c - LSE*log2 e), masks,
 //                dS^T = P^T o (dP^T - D) -> bf16 into TMEM and into shared
 //                memory (the dQ MMA's operand); drain the previous dQ
-//                contribution into the fp32 accumulator with vector atomics;
-//                at the end dK * scale and dV -> bf16.
+//                contribution through a swizzled shared tile and a TMA
+//                reduce-add into the fp32 accumulator; at the end
+//                dK * scale and dV -> bf16.
 //      d = 64 uses 128-row query blocks and dQ = dS K (TMEM lane = query);
 //      d = 128 uses 64-row query blocks and dQ^T = K^T dS^T (TMEM lane = head
 //      dimension), so that S, dP, dV, dK and two dQ buffers fit in the 512
@@ -50,7 +51,12 @@ struct BwdShape {
     static constexpr int OFF_Q = OFF_V + KV_BYTES;        // [STAGES]
     static constexpr int OFF_DO = OFF_Q + STAGES * Q_BYTES;
     static constexpr int OFF_DS = OFF_DO + STAGES * Q_BYTES;
-    static constexpr int OFF_LSE = OFF_DS + DS_BYTES;     // [2][BQ] fp32 (log2 domain)
+    // dQ staging for the TMA reduce-add: [D/32 chunks][BQ rows][128 bytes]
+    // fp32, 128-byte swizzled, two buffers
+    static constexpr int STG_BYTES = D * BQ * 4;
+    static constexpr int OFF_DQS = OFF_DS + DS_BYTES;
+    static constexpr int DQ_BOX_ROWS = DQ_T ? BQ : 32;    // rows of one warp's reduce box
+    static constexpr int OFF_LSE = OFF_DQS + 2 * STG_BYTES;  // [2][BQ] fp32 (log2 domain)
     static constexpr int OFF_DV = OFF_LSE + 2 * BQ * 4;   // [2][BQ] fp32
     static constexpr int OFF_BAR = OFF_DV + 2 * BQ * 4;
     static constexpr int B_KV = 0;
@@ -93,8 +99,11 @@ __global__ void __launch_bounds__(256, 1) fa_bwd_kernel(const __grid_constant__ 
     uint8_t *sb = smem_raw + (base - raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    const int kt = (int)(blockIdx.x / p.BH);
-    const int bh = (int)(blockIdx.x % p.BH);
+    // head-major order: the CTAs resident at one time share one head's Q, dO
+    // and dQ accumulator in L2; within a head the causally heaviest key
+    // tiles (lowest index) start first
+    const int kt = (int)(blockIdx.x % p.Tk);
+    const int bh = (int)(blockIdx.x / p.Tk);
     const int b = bh / p.H;
     const int k0 = kt * kTile;
     const int nb = (p.N + kTile - 1) / kTile;
@@ -273,7 +282,9 @@ __global__ void __launch_bounds__(256, 1) fa_bwd_kernel(const __grid_constant__ 
         bool ok = true;
         int i = 0, prev_qb = -1;
 
-        // drain the dQ contribution of step j (query block qb) into dQacc
+        // drain the dQ contribution of step j (query block qb): TMEM -> swizzled
+        // shared staging -> TMA reduce-add into the fp32 accumulator.  Each warp
+        // stages and reduces its own part, so no cross-warp sync is needed.
         auto drain_dq = [&](int j, int qb) -> bool {
             if (!mbar_wait_warp(bar(S::B_DQFULL + (j & 1)), (uint32_t)(j >> 1) & 1u, g, 0x411)) return false;
             tc_fence_after();
@@ -285,30 +296,41 @@ __global__ void __launch_bounds__(256, 1) fa_bwd_kernel(const __grid_constant__ 
             tmem_ld_wait(v1);
             tc_fence_before();
             mbar_arrive(bar(S::B_DQFREE + (j & 1)));
+            uint8_t *stg = sb + S::OFF_DQS + (j & 1) * S::STG_BYTES;
+            // the reduce issued from this buffer two drains ago must have read it
+            if (lane == 0) bulk_wait_group_read<1>();
+            __syncwarp();
             if (S::DQ_T) {
-                // lane r = head dimension r, column t = query qb*BQ + t
-                float *col = p.dQacc + ((size_t)bh * p.N + (size_t)qb * BQ) * D + r;
-                const int nq = min(BQ, p.N - qb * BQ);
-#pragma unroll 4
+                // lane = head dimension 32*wq + lane (chunk wq), column t = query t
+                uint8_t *cb = stg + wq * (BQ * 128) + (lane & 3) * 4;
+                const int grp = lane >> 2;
+#pragma unroll
                 for (int t = 0; t < 32; ++t)
-                    if (t < nq) atomicAdd(col + (size_t)t * D, __uint_as_float(v0[t]));
-#pragma unroll 4
+                    *reinterpret_cast<uint32_t *>(cb + t * 128 + ((grp ^ (t & 7)) << 4)) = v0[t];
+#pragma unroll
                 for (int t = 0; t < 32; ++t)
-                    if (t + 32 < nq) atomicAdd(col + (size_t)(t + 32) * D, __uint_as_float(v1[t]));
+                    *reinterpret_cast<uint32_t *>(cb + (t + 32) * 128 + ((grp ^ (t & 7)) << 4)) = v1[t];
             } else {
-                // lane r = query qb*BQ + r, column t = head dimension t
-                const int qrow = qb * BQ + r;
-                if (qrow < p.N) {
-                    float4 *row = reinterpret_cast<float4 *>(p.dQacc + ((size_t)bh * p.N + qrow) * D);
+                // lane = query row r of the block, columns = head dimensions 0..63
 #pragma unroll
-                    for (int t = 0; t < 8; ++t)
-                        atomicAdd(row + t, make_float4(__uint_as_float(v0[4 * t]), __uint_as_float(v0[4 * t + 1]),
-                                                       __uint_as_float(v0[4 * t + 2]), __uint_as_float(v0[4 * t + 3])));
-#pragma unroll
-                    for (int t = 0; t < 8; ++t)
-                        atomicAdd(row + 8 + t, make_float4(__uint_as_float(v1[4 * t]), __uint_as_float(v1[4 * t + 1]),
-                                                           __uint_as_float(v1[4 * t + 2]), __uint_as_float(v1[4 * t + 3])));
+                for (int gq = 0; gq < 8; ++gq) {
+                    *reinterpret_cast<uint4 *>(stg + r * 128 + ((gq ^ (r & 7)) << 4)) =
+                        make_uint4(v0[4 * gq], v0[4 * gq + 1], v0[4 * gq + 2], v0[4 * gq + 3]);
+                    *reinterpret_cast<uint4 *>(stg + BQ * 128 + r * 128 + ((gq ^ (r & 7)) << 4)) =
+                        make_uint4(v1[4 * gq], v1[4 * gq + 1], v1[4 * gq + 2], v1[4 * gq + 3]);
                 }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                const uint32_t st = smem_u32(stg);
+                if (S::DQ_T) {
+                    tma_reduce_add_3d(&p.tmdQ, st + wq * (BQ * 128), wq * 32, qb * BQ, bh);
+                } else {
+                    tma_reduce_add_3d(&p.tmdQ, st + wq * 32 * 128, 0, qb * BQ + wq * 32, bh);
+                    tma_reduce_add_3d(&p.tmdQ, st + BQ * 128 + wq * 32 * 128, 32, qb * BQ + wq * 32, bh);
+                }
+                bulk_commit_group();
             }
             return true;
         };
@@ -413,6 +435,9 @@ __global__ void __launch_bounds__(256, 1) fa_bwd_kernel(const __grid_constant__ 
             prev_qb = qb;
         }
         if (ok && i > 0) ok = drain_dq(i - 1, prev_qb);
+        // the staged dQ tiles must be fully reduced before shared memory goes away
+        if (lane == 0) bulk_wait_group_all();
+        __syncwarp();
 
         // ---------------------------------------------------------- epilogue: dK, dV
         if (ok && i > 0) {
@@ -521,6 +546,7 @@ __global__ void fa_plan_kernel(int B, int N, int T, int causal, const int32_t *k
 }
 
 int bwd_query_block(int d) { return d == 64 ? BwdShape<64>::BQ : BwdShape<128>::BQ; }
+int bwd_dq_box_rows(int d) { return d == 64 ? BwdShape<64>::DQ_BOX_ROWS : BwdShape<128>::DQ_BOX_ROWS; }
 int bwd_smem_bytes(int d) { return d == 64 ? BwdShape<64>::SMEM_BYTES : BwdShape<128>::SMEM_BYTES; }
 
 template <int D>

@@ -74,10 +74,11 @@ __global__ void __launch_bounds__(256, 1) fa_fwd_kernel(const __grid_constant__ 
     uint8_t *sb = smem_raw + (base - raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // Work item: heaviest query tiles first (they have the most key tiles
-    // under a causal mask), all heads of one query-tile index together.
-    const int qt = p.Tq - 1 - (int)(blockIdx.x / p.BH);
-    const int bh = (int)(blockIdx.x % p.BH);
+    // Work item, head-major: the CTAs resident at one time share one head's K
+    // and V in L2; within a head the causally heaviest query tiles (highest
+    // index, most key tiles) start first.
+    const int qt = p.Tq - 1 - (int)(blockIdx.x % p.Tq);
+    const int bh = (int)(blockIdx.x / p.Tq);
     const int b = bh / p.H;
     const int q0 = qt * kTile;
     const int qn = min(kTile, p.N - q0);

@@ -20,6 +20,7 @@ cudaError_t launch_bwd_main(int d, const BwdParams &p, cudaStream_t st);
 cudaError_t launch_bwd_convert(int d, const float *dQacc, void *dQ, int64_t elems, float scale,
                                cudaStream_t st);
 int bwd_query_block(int d);
+int bwd_dq_box_rows(int d);
 int bwd_smem_bytes(int d);
 
 // Plan export.

@@ -56,6 +56,7 @@ struct FwdParams {
 struct BwdParams {
     CUtensorMap tmQ, tmdO;           // box {64, BQ, 1}
     CUtensorMap tmK, tmV;            // box {64, 128, 1}
+    CUtensorMap tmdQ;                // fp32 [BH][N][d], box {32, 32 or BQ, 1}, 128B swizzle
     const float *LSE;                // fp32 [BH][N]
     const float *Dvec;               // fp32 [BH][N]: rowsum(dO * O)
     float *dQacc;                    // fp32 [BH][N][d]

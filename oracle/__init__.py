@@ -42,7 +42,10 @@ def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
+            # ORACLE_LIB points the tests' mutation check at a deliberately
+            # broken copy of the oracle; normally the library is built here.
+            path = os.environ.get("ORACLE_LIB") or build()
+            lib = ctypes.CDLL(path)
             dp = ctypes.POINTER(ctypes.c_double)
             ip = ctypes.POINTER(ctypes.c_int32)
             bp = ctypes.POINTER(ctypes.c_uint8)

@@ -1,0 +1,48 @@
+"""The pins are strong enough: each plausible mistake planted in a copy of
+the oracle (a dropped term, a wrong sign or index, a transposed operand, an
+off-by-one mask) makes the pin suite fail.  The mutants are compiled from
+the oracle source into a temporary directory; the real oracle is untouched."""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "fa_oracle.c")
+
+MUTANTS = {
+    "dQ without scale": ("dQh[(int64_t)i * d + t] = scale * acc;", "dQh[(int64_t)i * d + t] = acc;"),
+    "dK transposed dS": ("ak += dS[(int64_t)i * N + j] * Qh[(int64_t)i * d + t];",
+                         "ak += dS[(int64_t)j * N + i] * Qh[(int64_t)i * d + t];"),
+    "dS sign of D": ("dS[(int64_t)i * N + j] = p * (dp - Dv[i]);", "dS[(int64_t)i * N + j] = p * (dp + Dv[i]);"),
+    "dV from dS": ("av += P[(int64_t)i * N + j] * dOh[(int64_t)i * d + t];",
+                   "av += dS[(int64_t)i * N + j] * dOh[(int64_t)i * d + t];"),
+    "causal off by one": ("if (causal && j > i) return 0;", "if (causal && j >= i) return 0;"),
+    "key_len off by one": ("if (key_len && j >= key_len[b]) return 0;", "if (key_len && j > key_len[b]) return 0;"),
+    "block mask transposed": ("block_mask[(int64_t)(i / mask_block) * nb + j / mask_block]",
+                              "block_mask[(int64_t)(j / mask_block) * nb + i / mask_block]"),
+    "softmax not normalised": ("for (int j = 0; j < N; j++) s[j] = exp(s[j] - m) / l;",
+                               "for (int j = 0; j < N; j++) s[j] = exp(s[j] - m);"),
+    "LSE drops the max": ("return m + log(l);", "return log(l);"),
+    "score without scale": ("s[j] = scale * acc;", "s[j] = acc;"),
+    "D without dO": ("acc += dOh[(int64_t)i * d + t] * Oh[(int64_t)i * d + t];",
+                     "acc += Oh[(int64_t)i * d + t];"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, name
+    mut = tmp_path / "mutant.c"
+    mut.write_text(src.replace(old, new))
+    lib = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-O1", "-std=c99", "-fopenmp", "-fPIC", "-shared", "-o", str(lib), str(mut), "-lm"],
+                   check=True)
+    env = dict(os.environ, ORACLE_LIB=str(lib), OMP_NUM_THREADS="2")
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, "mutant '%s' survived the pins" % name
