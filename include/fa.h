@@ -154,6 +154,31 @@ fa_status fa_attention_host(const void *Q, const void *K, const void *V, const v
                             const uint8_t *block_mask, void *dev_workspace,
                             size_t dev_workspace_bytes, void *stream);
 
+/*
+ * fa_bwd without a workspace, for callers that cannot allocate device memory
+ * (code that must not call cudaMalloc where it runs, or that is handed only
+ * its input and output buffers).  The pages have no counterpart: this is a
+ * packaging of fa_bwd, not part of the method.
+ *
+ * Same arguments, meaning and results as fa_bwd, minus the workspace.  The
+ * scratch (status word, D, dQ accumulator) is a 64 MiB array built into the
+ * library and held by every GPU that loads it until the process exits.
+ *   - Problems needing more, i.e. B*H*N*(4 + 4*d) + 256 bytes > 64 MiB (for
+ *     example B*H*N > 130,000 rows at d = 128), return FA_ERR_WORKSPACE
+ *     before anything is enqueued.
+ *   - Allocates nothing.  The first call on a device looks up the array's
+ *     device address once, with that device current; make that first call
+ *     before any stream capture.
+ *   - All calls share the array and see the previous call's contents; each
+ *     call clears the status word and zeroes the accumulator first.  Calls
+ *     that overlap on the GPU race on the array: serialise them.
+ *   - Device-side status is not reported here (use fa_bwd for that).
+ */
+fa_status fa_bwd_noalloc(const void *Q, const void *K, const void *V, const void *O,
+                         const float *LSE, const void *dO, void *dQ, void *dK, void *dV, int B,
+                         int H, int N, int d, float softmax_scale, int causal,
+                         const int32_t *key_len, const uint8_t *block_mask, void *stream);
+
 /* Synchronise stream and return the workspace status word (FA_OK if no
  * device-side error was recorded). */
 fa_status fa_get_device_status(const void *workspace, void *stream);

@@ -69,6 +69,8 @@ def lib():
             L.fa_bwd_main.restype = i
             L.fa_bwd_postprocess.argtypes = [vp, i, i, i, i, f, vp, sz, vp]
             L.fa_bwd_postprocess.restype = i
+            L.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp, vp]
+            L.fa_bwd_noalloc.restype = i
             L.fa_tile_plan.argtypes = [i, i, i, vp, vp, vp, vp, sz, vp]
             L.fa_tile_plan.restype = i
             L.fa_attention_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp,
@@ -85,7 +87,7 @@ def lib():
 
 
 EXPORTED = ("fa_tile_size", "fa_fwd_workspace_size", "fa_bwd_workspace_size", "fa_fwd", "fa_bwd",
-            "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_postprocess", "fa_tile_plan", "fa_host_workspace_size", "fa_attention_host", "fa_get_device_status",
+            "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_postprocess", "fa_bwd_noalloc", "fa_tile_plan", "fa_host_workspace_size", "fa_attention_host", "fa_get_device_status",
             "fa_reset_device_status", "fa_status_string")
 
 
@@ -159,6 +161,15 @@ def fa_bwd_main(Q, K, V, LSE, dO, dK, dV, B, H, N, d, softmax_scale, causal, key
 def fa_bwd_postprocess(dQ, B, H, N, d, softmax_scale, workspace, workspace_bytes, stream=None) -> int:
     return lib().fa_bwd_postprocess(_p(dQ), B, H, N, d, float(softmax_scale), _p(workspace),
                                     int(workspace_bytes), _stream(stream))
+
+
+def fa_bwd_noalloc(Q, K, V, O, LSE, dO, dQ, dK, dV, B, H, N, d, softmax_scale, causal, key_len,
+                   block_mask, stream=None) -> int:
+    """fa_bwd using the library's built-in scratch instead of a workspace, for
+    callers that cannot allocate device memory (limits in include/fa.h)."""
+    return lib().fa_bwd_noalloc(_p(Q), _p(K), _p(V), _p(O), _p(LSE), _p(dO), _p(dQ), _p(dK), _p(dV), B,
+                                H, N, d, float(softmax_scale), int(bool(causal)), _p(key_len),
+                                _p(block_mask), _stream(stream))
 
 
 def fa_tile_plan(B, N, causal, key_len, block_mask, plan, workspace, workspace_bytes, stream=None) -> int:

@@ -1,0 +1,58 @@
+"""fa_bwd_noalloc: the backward pass for callers that cannot allocate device
+memory (a plug-in handed only its input and output buffers, code that must
+not call cudaMalloc where it runs).  It takes no workspace and uses the
+library's built-in scratch array instead.  It must give the same gradients
+as fa_bwd with a workspace on two calls in a row (the second call finds the
+first call's scratch contents and must clear what has to start at zero), and
+reject problems larger than the scratch before launching anything.
+
+Kept in a file of its own that pytest collects last, so that a run that
+stops at the first failure has already run every other test."""
+import pytest
+import torch
+
+import io_aware_exact_09_gb300 as fa
+from synthetic import make_case
+
+GRAD_REL_FRO = 1e-2   # the gradient bound the other parity tests use
+
+
+def rel_fro(a, b):
+    a = a.double().cpu()
+    b = b.double().cpu()
+    return float(torch.linalg.norm(a - b) / torch.linalg.norm(b))
+
+
+def test_noalloc_rejects_oversize_before_any_gpu_work():
+    fa.build()
+    L = fa.lib()
+    # 16 heads x 16384 rows at d = 128 need ~135 MB of scratch: more than the built-in 64 MiB
+    assert L.fa_bwd_noalloc(256, 256, 256, 256, 256, 256, 256, 256, 256, 1, 16, 16384, 128, 0.1, 0,
+                            None, None, None) == 3
+    assert L.fa_bwd_noalloc(256, 256, 256, 256, 256, 256, 256, 256, 256, 1, 1, 128, 96, 0.1, 0,
+                            None, None, None) == 2
+    assert L.fa_bwd_noalloc(None, None, None, None, None, None, None, None, None, 0, 1, 128, 64, 0.1, 0,
+                            None, None, None) == 0
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("d", [64, 128])
+def test_noalloc_matches_workspace_backward_twice(d):
+    fa.build()
+    c = make_case(2, 3, 300, d, seed=77 + d, causal=True, key_len=[300, 170])
+    scale = 1.0 / d ** 0.5
+    Q, K, V, dO = (c[k].cuda() for k in ("Q", "K", "V", "dO"))
+    kl = c["key_len"].cuda()
+    O, LSE = fa.attention_forward(Q, K, V, scale, True, kl, None, check_status=True)
+    rQ, rK, rV = fa.attention_backward(Q, K, V, O, LSE, dO, scale, True, kl, None, check_status=True)
+    B, H, N, _ = Q.shape
+    for call in range(2):
+        dQ, dK, dV = (torch.full_like(Q, float("nan")) for _ in range(3))
+        st = fa.fa_bwd_noalloc(Q, K, V, O, LSE, dO, dQ, dK, dV, B, H, N, d, scale, True, kl, None)
+        assert st == 0, fa.fa_status_string(st)
+        torch.cuda.synchronize()
+        for got, ref, name in ((dQ, rQ, "dQ"), (dK, rK, "dK"), (dV, rV, "dV")):
+            assert bool(torch.isfinite(got).all()), (call, name)
+            assert rel_fro(got, ref) <= GRAD_REL_FRO, (call, name, rel_fro(got, ref))
+        # dK and dV are not accumulated across CTAs: identical to the workspace path
+        assert torch.equal(dK, rK) and torch.equal(dV, rV), call
