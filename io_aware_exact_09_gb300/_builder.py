@@ -48,12 +48,41 @@ def _compile(src: str) -> str:
     return obj
 
 
+# Kernels that split registers between warpgroups with setmaxnreg: the
+# split in the source assumes exactly this many registers per thread at
+# launch; a different allocation would make setmaxnreg.inc wait forever, so
+# the build refuses it.
+REGISTER_SPLIT_KERNELS = {"fa_fwd.cu": ("fa_fwd_kernel", 168)}
+
+
+def _check_register_split(src: str) -> None:
+    if src not in REGISTER_SPLIT_KERNELS:
+        return
+    name, want = REGISTER_SPLIT_KERNELS[src]
+    log = open(os.path.join(BUILD, src.replace(".cu", ".ptxas.log"))).read().splitlines()
+    found = 0
+    for i, line in enumerate(log):
+        if "Compiling entry function" in line and name in line:
+            for nxt in log[i + 1:i + 6]:
+                if "Used" in nxt and "registers" in nxt:
+                    regs = int(nxt.split("Used")[1].split("registers")[0])
+                    if regs != want:
+                        raise RuntimeError("%s: ptxas allocated %d registers, the setmaxnreg split needs %d"
+                                           % (name, regs, want))
+                    found += 1
+                    break
+    if found == 0:
+        raise RuntimeError("%s: no ptxas register report found" % name)
+
+
 def build(force: bool = False, verbose: bool = False) -> str:
     if not force and not _stale():
         return LIB
     os.makedirs(BUILD, exist_ok=True)
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(_compile, SOURCES))
+    for src in SOURCES:
+        _check_register_split(src)
     tmp = LIB + ".tmp.%d" % os.getpid()
     cmd = [nvcc()] + ARCH + ["-shared", "-o", tmp] + objs + ["-ldl"]
     r = subprocess.run(cmd, capture_output=True, text=True)

@@ -4,7 +4,7 @@
 // Method ("The Attention Matrix You Never Write Down", section "The
 // running-statistics trick"; "FlashAttention: Mathematical Foundations ...",
 // sections "Incremental Online Updates" and "IO-Aware Tiling Algorithm"):
-// per query row keep the running maximum m and normaliser l; for each new key
+// per query row keep a running maximum m and normaliser l; for each new key
 // tile take m' = max(m, tile max), multiply l and the unnormalised output by
 // exp(m - m'), add the tile's exp(s - m') and exp(s - m') V; divide by l at
 // the end.  The tiling page prints the correction as diag(exp(m - m'))^-1;
@@ -12,18 +12,30 @@
 // diag(l)^-1 normalisation, so the multiply-by-exp(m - m') reading is used.
 // Everything is in base 2: x = s * scale * log2(e), p = 2^(x - m).
 //
+// The reference maximum is only moved when a row's tile maximum exceeds it
+// by more than kRescaleLog2 (2^8): until then l, O and the new p all keep the
+// old reference, which is the same identity with m' replaced by any common
+// reference, so the result is unchanged and p stays <= 2^8.  This skips most
+// O rescales (tcgen05.ld/st of the whole accumulator).
+//
 // GB300 design (not the A100 loop order the tiling page prints; the query
-// tile is the outer loop, as in its "FlashAttention-2" section, so O stays on
-// chip):
-//   - one CTA per (128-row query tile, b*h); heavier causal tiles first;
-//   - warp 0: TMA producer.  Q tile once; K and V tiles through a ring of
-//     shared-memory stages (128-byte swizzle, 64-column boxes);
-//   - warp 1: tcgen05 issuer.  S = Q K^T into one of two TMEM buffers (so the
-//     next tile's S overlaps this tile's softmax), then O += P V with P read
-//     from TMEM (it overwrites the first half of its S buffer as bf16);
-//   - warps 4-7: softmax, one query row per thread (TMEM lane = row), the
-//     O rescale (only when a row's maximum moved), and the epilogue
-//     O / l -> bf16, LSE = (m + log2 l) * ln 2.
+// tile is the outer loop, as in its "FlashAttention-2" section, so O stays
+// on chip):
+//   - one CTA per (pair of 128-row query tiles, b*h), head-major, causally
+//     heaviest pairs first within a head;
+//   - warp 0: TMA producer: both Q tiles once; K and V tiles through a ring
+//     of shared-memory stages (128-byte swizzle, 64-column boxes), over the
+//     union of the key tiles the two query tiles see;
+//   - warp 1: tcgen05 issuer: for each key tile, S_x = Q_x K^T for both query
+//     tiles x into TMEM (one buffer each), then O_x += P_x V with P_x read
+//     from TMEM (bf16, written over the first half of S_x).  The next tile's
+//     S_x is issued one key tile ahead, once P_x has been consumed;
+//   - warps 4-7 and 8-11: softmax of query tile 0 and 1, one row per thread
+//     (TMEM lane = row, warp w reads lane quadrant w % 4), with 216 registers
+//     each (setmaxnreg; warps 0-3 drop to 72).  The whole S row
+//     is loaded with one wait, then max (3-input), 2^(x - m) with packed
+//     f32x2 FMA/add, bf16 pack, store back; then the rare O rescale and, at
+//     the end, the epilogue O / l -> bf16, LSE = (m + log2 l) * ln 2.
 // Skipped tiles (block mask zero, all keys past key_len, above the causal
 // diagonal) are never loaded; partial tiles get element masks.
 #include "fa_internal.h"
@@ -31,22 +43,23 @@
 
 namespace fa {
 
+constexpr float kRescaleLog2 = 8.0f;
+
 template <int D>
 struct FwdShape {
     static constexpr int CHUNKS = D / 64;               // 64-element (128-byte) column chunks
     static constexpr int CHUNK_BYTES = 128 * 128;       // 128 rows x 128 bytes
     static constexpr int TILE_BYTES = CHUNKS * CHUNK_BYTES;
     static constexpr int STAGES = (D == 64) ? 4 : 2;
-    static constexpr int OFF_Q = 0;
-    static constexpr int OFF_K = OFF_Q + TILE_BYTES;
+    static constexpr int OFF_Q = 0;                     // [2] query tiles
+    static constexpr int OFF_K = OFF_Q + 2 * TILE_BYTES;
     static constexpr int OFF_V = OFF_K + STAGES * TILE_BYTES;
     static constexpr int OFF_BAR = OFF_V + STAGES * TILE_BYTES;
-    // barrier indices
     static constexpr int B_QFULL = 0;
     static constexpr int B_KFULL = 1;
     static constexpr int B_VFULL = B_KFULL + STAGES;
     static constexpr int B_KVEMPTY = B_VFULL + STAGES;
-    static constexpr int B_SFULL = B_KVEMPTY + STAGES;   // [2]
+    static constexpr int B_SFULL = B_KVEMPTY + STAGES;   // [2] one per query tile
     static constexpr int B_PFULL = B_SFULL + 2;          // [2]
     static constexpr int B_PVDONE = B_PFULL + 2;         // [2]
     static constexpr int B_FIN = B_PVDONE + 2;
@@ -54,8 +67,16 @@ struct FwdShape {
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem base (4 B), abort flag (4 B)
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1 KB
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t TM_S = 0;                  // S buffers at columns 0 and 128
-    static constexpr uint32_t TM_O = 256;                // O accumulator, D columns
+    static constexpr uint32_t TM_S = 0;                  // S_x at columns 128 x
+    static constexpr uint32_t TM_O = 256;                // O_x at columns 256 + D x
+    static constexpr int THREADS = 384;
+    // register split: launched at 168 per thread (384 x 168 = 64,512);
+    // warpgroup 0 (producer, MMA, two idle warps) keeps 72, the two softmax
+    // warpgroups get 216: 128 x 72 + 256 x 216 = 64,512.
+    static constexpr int LAUNCH_REGS = 168;
+    static constexpr int REGS_CTRL = 72;
+    static constexpr int REGS_SOFTMAX = 216;
+    static_assert(128 * REGS_CTRL + 256 * REGS_SOFTMAX == THREADS * LAUNCH_REGS, "register split");
 };
 
 // Bounded wait used only while draining after an abort (ignores the abort flag).
@@ -66,7 +87,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(256, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
+__global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
     using S = FwdShape<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -75,14 +96,18 @@ __global__ void __launch_bounds__(256, 1) fa_fwd_kernel(const __grid_constant__ 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     // Work item, head-major: the CTAs resident at one time share one head's K
-    // and V in L2; within a head the causally heaviest query tiles (highest
-    // index, most key tiles) start first.
-    const int qt = p.Tq - 1 - (int)(blockIdx.x % p.Tq);
-    const int bh = (int)(blockIdx.x / p.Tq);
+    // and V in L2; within a head the causally heaviest pairs start first.
+    const int Tp = (p.Tq + 1) / 2;
+    const int pq = Tp - 1 - (int)(blockIdx.x % Tp);
+    const int bh = (int)(blockIdx.x / Tp);
     const int b = bh / p.H;
-    const int q0 = qt * kTile;
-    const int qn = min(kTile, p.N - q0);
     const int nb = (p.N + kTile - 1) / kTile;
+    int q0[2], qn[2];
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+        q0[x] = (2 * pq + x) * kTile;
+        qn[x] = max(0, min(kTile, p.N - q0[x]));
+    }
 
     auto bar = [&](int i) -> uint32_t { return base + S::OFF_BAR + 8u * (uint32_t)i; };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sb + S::OFF_MISC);
@@ -91,15 +116,21 @@ __global__ void __launch_bounds__(256, 1) fa_fwd_kernel(const __grid_constant__ 
 
     bool bad = false;
     const int kvis = key_visible_bound(p.key_len, b, p.N, &bad);
-    if (bad && threadIdx.x == 0 && qt == 0 && (bh % p.H) == 0) record_status(g, kStatusBadKeyLen, 0);
+    if (bad && threadIdx.x == 0 && pq == 0 && (bh % p.H) == 0) record_status(g, kStatusBadKeyLen, 0);
 
-    auto cls = [&](int kt) -> unsigned {
-        const int on = p.block_mask ? (p.block_mask[(size_t)qt * nb + kt] != 0) : 1;
-        return tile_class(q0, qn, kt * kTile, kTile, kvis, p.causal, on);
+    // class of key tile kt for query tile x of the pair
+    auto cls = [&](int x, int kt) -> unsigned {
+        if (qn[x] <= 0) return kTileSkip;
+        const int on = p.block_mask ? (p.block_mask[(size_t)(2 * pq + x) * nb + kt] != 0) : 1;
+        return tile_class(q0[x], qn[x], kt * kTile, kTile, kvis, p.causal, on);
     };
-    auto next_tile = [&](int kt) -> int {
-        for (int k = kt + 1; k < p.Tk; ++k)
-            if (cls(k) != kTileSkip) return k;
+    // next key tile after kt seen by query tile x (x = 2: by either)
+    auto next_tile = [&](int x, int kt) -> int {
+        for (int k = kt + 1; k < p.Tk; ++k) {
+            const bool v0 = (x != 1) && cls(0, k) != kTileSkip;
+            const bool v1 = (x != 0) && cls(1, k) != kTileSkip;
+            if (v0 || v1) return k;
+        }
         return p.Tk;
     };
 
@@ -131,134 +162,164 @@ __global__ void __launch_bounds__(256, 1) fa_fwd_kernel(const __grid_constant__ 
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0) {
-        // ---------------------------------------------------------- producer
-        if (lane == 0) {
-            int it = 0;
-            bool ok = true;
-            int kt = next_tile(-1);
-            if (kt < p.Tk) {
-                mbar_arrive_expect_tx(bar(S::B_QFULL), S::TILE_BYTES);
-                for (int c = 0; c < S::CHUNKS; ++c)
-                    tma_load_3d(base + S::OFF_Q + c * S::CHUNK_BYTES, &p.tmQ, bar(S::B_QFULL), c * 64,
-                                q0, bh);
-            }
-            for (; kt < p.Tk; kt = next_tile(kt), ++it) {
-                const int s = it % S::STAGES;
-                const uint32_t ph = (uint32_t)(it / S::STAGES) & 1u;
-                if (!mbar_wait(bar(S::B_KVEMPTY + s), ph ^ 1u, g, 0x101)) {
-                    ok = false;
-                    break;
+    // Register split.  Warpgroup 0 gives registers back once, here, and
+    // keeps 72 to the end; the softmax warpgroups take them, here, and give
+    // them back at the end of their branch, so the shared teardown below runs
+    // with 72 everywhere.  The only setmaxnreg.inc (which blocks until the
+    // pool holds enough) is the softmax one at the start, and the pool is
+    // filled by warpgroup 0's unconditional dec: no inc ever waits on a warp
+    // that is itself waiting.
+    if (warp < 4) {
+        setmaxnreg_dec<S::REGS_CTRL>();
+        if (warp == 0) {
+            // ---------------------------------------------------------- producer
+            if (lane == 0) {
+                int u = 0;
+                bool ok = true;
+                int kt = next_tile(2, -1);
+                if (kt < p.Tk) {
+                    const uint32_t nq = (qn[0] > 0 ? 1u : 0u) + (qn[1] > 0 ? 1u : 0u);
+                    mbar_arrive_expect_tx(bar(S::B_QFULL), nq * S::TILE_BYTES);
+                    for (int x = 0; x < 2; ++x)
+                        if (qn[x] > 0)
+                            for (int c = 0; c < S::CHUNKS; ++c)
+                                tma_load_3d(base + S::OFF_Q + x * S::TILE_BYTES + c * S::CHUNK_BYTES, &p.tmQ,
+                                            bar(S::B_QFULL), c * 64, q0[x], bh);
                 }
-                const uint32_t koff = base + S::OFF_K + s * S::TILE_BYTES;
-                const uint32_t voff = base + S::OFF_V + s * S::TILE_BYTES;
-                mbar_arrive_expect_tx(bar(S::B_KFULL + s), S::TILE_BYTES);
-                for (int c = 0; c < S::CHUNKS; ++c)
-                    tma_load_3d(koff + c * S::CHUNK_BYTES, &p.tmK, bar(S::B_KFULL + s), c * 64,
-                                kt * kTile, bh);
-                mbar_arrive_expect_tx(bar(S::B_VFULL + s), S::TILE_BYTES);
-                for (int c = 0; c < S::CHUNKS; ++c)
-                    tma_load_3d(voff + c * S::CHUNK_BYTES, &p.tmV, bar(S::B_VFULL + s), c * 64,
-                                kt * kTile, bh);
-            }
-            if (!ok) {
-                // gave up: let every copy already issued land before the CTA exits
-                if (next_tile(-1) < p.Tk) drain_wait(bar(S::B_QFULL), 0);
-                for (int i = (it > S::STAGES ? it - S::STAGES : 0); i < it; ++i) {
-                    const int s = i % S::STAGES;
-                    const uint32_t ph = (uint32_t)(i / S::STAGES) & 1u;
-                    drain_wait(bar(S::B_KFULL + s), ph);
-                    drain_wait(bar(S::B_VFULL + s), ph);
-                }
-            }
-        }
-    } else if (warp == 1) {
-        // ---------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
-            constexpr uint32_t IDESC_PV = idesc_bf16(128, D, false, true);
-            int kt = next_tile(-1);
-            bool ok = true;
-            if (kt < p.Tk) {
-                ok = mbar_wait(bar(S::B_QFULL), 0, g, 0x201);
-                // S_i = Q K_i^T into TMEM buffer i % 2
-                auto issue_s = [&](int i) -> bool {
-                    const int s = i % S::STAGES;
-                    if (!mbar_wait(bar(S::B_KFULL + s), (uint32_t)(i / S::STAGES) & 1u, g, 0x202))
-                        return false;
-                    // buffer i%2 last held P_{i-2}: its P.V must have finished
-                    if (i >= 2 &&
-                        !mbar_wait(bar(S::B_PVDONE + (i & 1)), (uint32_t)((i - 2) >> 1) & 1u, g, 0x203))
-                        return false;
-                    tc_fence_after();
-                    const uint32_t d_tmem = tmem + S::TM_S + (uint32_t)(i & 1) * 128u;
-#pragma unroll
-                    for (int k = 0; k < D / 16; ++k) {
-                        const uint32_t qa = base + S::OFF_Q + (k >> 2) * S::CHUNK_BYTES + (k & 3) * 32;
-                        const uint32_t ka = base + S::OFF_K + s * S::TILE_BYTES +
-                                            (k >> 2) * S::CHUNK_BYTES + (k & 3) * 32;
-                        mma_ss(d_tmem, sdesc_sw128(qa, 16, 1024), sdesc_sw128(ka, 16, 1024), IDESC_S,
-                               k > 0 ? 1u : 0u);
-                    }
-                    mma_commit(bar(S::B_SFULL + (i & 1)));
-                    return true;
-                };
-                if (ok) ok = issue_s(0);
-                int it = 0;
-                while (ok && kt < p.Tk) {
-                    const int kt_next = next_tile(kt);
-                    if (kt_next < p.Tk && !(ok = issue_s(it + 1))) break;
-                    const int s = it % S::STAGES;
-                    if (!mbar_wait(bar(S::B_PFULL + (it & 1)), (uint32_t)(it >> 1) & 1u, g, 0x204) ||
-                        !mbar_wait(bar(S::B_VFULL + s), (uint32_t)(it / S::STAGES) & 1u, g, 0x205)) {
+                for (; kt < p.Tk; kt = next_tile(2, kt), ++u) {
+                    const int s = u % S::STAGES;
+                    const uint32_t ph = (uint32_t)(u / S::STAGES) & 1u;
+                    if (!mbar_wait(bar(S::B_KVEMPTY + s), ph ^ 1u, g, 0x101)) {
                         ok = false;
                         break;
                     }
-                    tc_fence_after();
-                    const uint32_t p_tmem = tmem + S::TM_S + (uint32_t)(it & 1) * 128u;
+                    const uint32_t koff = base + S::OFF_K + s * S::TILE_BYTES;
                     const uint32_t voff = base + S::OFF_V + s * S::TILE_BYTES;
-#pragma unroll
-                    for (int k = 0; k < kTile / 16; ++k) {
-                        // A = P (bf16 pairs, 8 columns per 16 keys); B = V, MN-major
-                        mma_ts(tmem + S::TM_O, p_tmem + (uint32_t)k * 8u,
-                               sdesc_sw128(voff + k * 2048, S::CHUNK_BYTES, 1024), IDESC_PV,
-                               (it > 0 || k > 0) ? 1u : 0u);
+                    mbar_arrive_expect_tx(bar(S::B_KFULL + s), S::TILE_BYTES);
+                    for (int c = 0; c < S::CHUNKS; ++c)
+                        tma_load_3d(koff + c * S::CHUNK_BYTES, &p.tmK, bar(S::B_KFULL + s), c * 64, kt * kTile, bh);
+                    mbar_arrive_expect_tx(bar(S::B_VFULL + s), S::TILE_BYTES);
+                    for (int c = 0; c < S::CHUNKS; ++c)
+                        tma_load_3d(voff + c * S::CHUNK_BYTES, &p.tmV, bar(S::B_VFULL + s), c * 64, kt * kTile, bh);
+                }
+                if (!ok) {
+                    // gave up: let every copy already issued land before the CTA exits
+                    if (next_tile(2, -1) < p.Tk) drain_wait(bar(S::B_QFULL), 0);
+                    for (int i = (u > S::STAGES ? u - S::STAGES : 0); i < u; ++i) {
+                        const int s = i % S::STAGES;
+                        const uint32_t ph = (uint32_t)(i / S::STAGES) & 1u;
+                        drain_wait(bar(S::B_KFULL + s), ph);
+                        drain_wait(bar(S::B_VFULL + s), ph);
                     }
-                    mma_commit(bar(S::B_KVEMPTY + s));
-                    mma_commit(bar(S::B_PVDONE + (it & 1)));
-                    kt = kt_next;
-                    ++it;
                 }
             }
-            // every MMA this thread issued must finish before TMEM is freed
-            mma_commit(bar(S::B_FIN));
-            drain_wait(bar(S::B_FIN), 0);
+        } else if (warp == 1) {
+            // ---------------------------------------------------------- MMA issuer
+            if (lane == 0) {
+                constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
+                constexpr uint32_t IDESC_PV = idesc_bf16(128, D, false, true);
+                int kt = next_tile(2, -1);
+                bool ok = true;
+                int nv[2] = {0, 0};      // key tiles processed so far by query tile x
+                // S_x = Q_x K^T for the key tile in stage s (the x-th S buffer)
+                auto issue_s = [&](int x, int s) {
+                    const uint32_t d_tmem = tmem + S::TM_S + 128u * (uint32_t)x;
+    #pragma unroll
+                    for (int k = 0; k < D / 16; ++k) {
+                        const uint32_t qa = base + S::OFF_Q + x * S::TILE_BYTES + (k >> 2) * S::CHUNK_BYTES + (k & 3) * 32;
+                        const uint32_t ka = base + S::OFF_K + s * S::TILE_BYTES + (k >> 2) * S::CHUNK_BYTES + (k & 3) * 32;
+                        mma_ss(d_tmem, sdesc_sw128(qa, 16, 1024), sdesc_sw128(ka, 16, 1024), IDESC_S, k > 0 ? 1u : 0u);
+                    }
+                    mma_commit(bar(S::B_SFULL + x));
+                };
+                if (kt < p.Tk) {
+                    ok = mbar_wait(bar(S::B_QFULL), 0, g, 0x201) && mbar_wait(bar(S::B_KFULL + 0), 0, g, 0x202);
+                    if (ok) {
+                        tc_fence_after();
+                        for (int x = 0; x < 2; ++x)
+                            if (cls(x, kt) != kTileSkip) issue_s(x, 0);
+                    }
+                    int u = 0;
+                    while (ok && kt < p.Tk) {
+                        const int s = u % S::STAGES;
+                        bool vwaited = false;
+                        // O_x += P_x V for both query tiles
+                        for (int x = 0; x < 2 && ok; ++x) {
+                            if (cls(x, kt) == kTileSkip) continue;
+                            if (!mbar_wait(bar(S::B_PFULL + x), (uint32_t)nv[x] & 1u, g, 0x203) ||
+                                (!vwaited && !mbar_wait(bar(S::B_VFULL + s), (uint32_t)(u / S::STAGES) & 1u, g, 0x204))) {
+                                ok = false;
+                                break;
+                            }
+                            vwaited = true;
+                            tc_fence_after();
+                            const uint32_t p_tmem = tmem + S::TM_S + 128u * (uint32_t)x;
+                            const uint32_t o_tmem = tmem + S::TM_O + (uint32_t)(D * x);
+                            const uint32_t voff = base + S::OFF_V + s * S::TILE_BYTES;
+    #pragma unroll
+                            for (int k = 0; k < kTile / 16; ++k)
+                                mma_ts(o_tmem, p_tmem + (uint32_t)k * 8u, sdesc_sw128(voff + k * 2048, S::CHUNK_BYTES, 1024),
+                                       IDESC_PV, (nv[x] > 0 || k > 0) ? 1u : 0u);
+                            mma_commit(bar(S::B_PVDONE + x));
+                            ++nv[x];
+                        }
+                        if (!ok) break;
+                        mma_commit(bar(S::B_KVEMPTY + s));
+                        // the next key tile's S_x, once P_x of this one has been consumed
+                        const int kt_next = next_tile(2, kt);
+                        if (kt_next < p.Tk) {
+                            const int s2 = (u + 1) % S::STAGES;
+                            if (!mbar_wait(bar(S::B_KFULL + s2), (uint32_t)((u + 1) / S::STAGES) & 1u, g, 0x205)) {
+                                ok = false;
+                                break;
+                            }
+                            for (int x = 0; x < 2 && ok; ++x) {
+                                if (cls(x, kt_next) == kTileSkip) continue;
+                                if (nv[x] > 0 && !mbar_wait(bar(S::B_PVDONE + x), (uint32_t)(nv[x] - 1) & 1u, g, 0x206)) {
+                                    ok = false;
+                                    break;
+                                }
+                                tc_fence_after();
+                                issue_s(x, s2);
+                            }
+                        }
+                        kt = kt_next;
+                        ++u;
+                    }
+                }
+                // every MMA this thread issued must finish before TMEM is freed
+                mma_commit(bar(S::B_FIN));
+                drain_wait(bar(S::B_FIN), 0);
+            }
         }
-    } else if (warp >= 4) {
-        // ---------------------------------------------------------- softmax
+    } else {
+        setmaxnreg_inc<S::REGS_SOFTMAX>();
+        // ---------------------------------------------------------- softmax of query tile x
+        const int x = (warp - 4) >> 2;
         const int wq = warp & 3;
         const int r = wq * 32 + lane;
-        const int q = q0 + r;
+        const int q = q0[x] + r;
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        const uint32_t s_tmem = tmem + lane_off + S::TM_S + 128u * (uint32_t)x;
+        const uint32_t o_tmem = tmem + lane_off + S::TM_O + (uint32_t)(D * x);
         const float c2 = p.scale_log2;
-        float m = -INFINITY, l = 0.f;
+        float m_ref = -INFINITY, l = 0.f;
         int it = 0;
         bool ok = true;
-        for (int kt = next_tile(-1); kt < p.Tk; kt = next_tile(kt), ++it) {
-            const unsigned klass = cls(kt);
-            if (!mbar_wait_warp(bar(S::B_SFULL + (it & 1)), (uint32_t)(it >> 1) & 1u, g, 0x401)) {
+        for (int kt = next_tile(x, -1); kt < p.Tk; kt = next_tile(x, kt), ++it) {
+            const bool partial = cls(x, kt) == kTilePartial;
+            const int k0 = kt * kTile;
+            if (!mbar_wait_warp(bar(S::B_SFULL + x), (uint32_t)it & 1u, g, 0x401)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const uint32_t s_tmem = tmem + lane_off + S::TM_S + (uint32_t)(it & 1) * 128u;
             uint32_t sr[4][32];
 #pragma unroll
             for (int j = 0; j < 4; ++j) tmem_ld32(s_tmem + 32u * j, sr[j]);
 #pragma unroll
             for (int j = 0; j < 4; ++j) tmem_ld_wait(sr[j]);
-            if (klass == kTilePartial) {
-                const int k0 = kt * kTile;
+            if (partial) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
 #pragma unroll
@@ -271,56 +332,73 @@ __global__ void __launch_bounds__(256, 1) fa_fwd_kernel(const __grid_constant__ 
 #pragma unroll
             for (int j = 0; j < 4; ++j)
 #pragma unroll
-                for (int t = 0; t < 32; ++t) mx = fmaxf(mx, __uint_as_float(sr[j][t]));
-            const float m_new = fmaxf(m, mx * c2);
-            const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-            const float alpha = ex2(m - m_use);
-            float sum = 0.f;
+                for (int t = 0; t < 32; t += 2) mx = fmax3(mx, __uint_as_float(sr[j][t]), __uint_as_float(sr[j][t + 1]));
+            // move the reference maximum only when the row outgrew it by 2^8
+            const float m_tile = mx * c2;
+            const bool grow = m_tile > m_ref + kRescaleLog2;
+            float alpha = 1.f;
+            const bool rescale = __any_sync(0xffffffffu, grow);
+            if (rescale) {
+                const float m_new = fmaxf(m_ref, m_tile);
+                alpha = (m_new == -INFINITY) ? 1.f : ex2(m_ref - m_new);
+                l *= alpha;
+                m_ref = m_new;
+            }
+            const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+            // p = 2^(s * c - m), bf16 into the first 64 columns of S_x
+            float sum0 = 0.f, sum1 = 0.f;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int t = 0; t < 16; ++t) {
-                    const float a = ex2(fmaf(__uint_as_float(sr[j][2 * t]), c2, -m_use));
-                    const float bb = ex2(fmaf(__uint_as_float(sr[j][2 * t + 1]), c2, -m_use));
-                    sum += a + bb;
+                    float a, bb;
+                    fma2(a, bb, __uint_as_float(sr[j][2 * t]), __uint_as_float(sr[j][2 * t + 1]), c2, c2, -m_use, -m_use);
+                    a = ex2(a);
+                    bb = ex2(bb);
+                    add2(sum0, sum1, a, bb);
                     pk[t] = pack_bf16x2(a, bb);
                 }
-                // P (bf16) overwrites the first 64 columns of this S buffer
                 tmem_st16(s_tmem + 16u * j, pk);
             }
-            l = l * alpha + sum;
-            m = m_new;
+            l += sum0 + sum1;
             tmem_st_wait();
-            if (it > 0) {
-                // O may be rescaled only once the previous P.V has landed
-                if (!mbar_wait_warp(bar(S::B_PVDONE + ((it - 1) & 1)), (uint32_t)((it - 1) >> 1) & 1u, g,
-                                    0x402)) {
+            if (rescale && it > 0) {
+                // O_x may be rescaled only once the previous P_x V has landed
+                if (!mbar_wait_warp(bar(S::B_PVDONE + x), (uint32_t)(it - 1) & 1u, g, 0x402)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                if (__any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll 1
-                    for (int j = 0; j < D / 32; ++j) {
-                        uint32_t o[32];
-                        const uint32_t oa = tmem + lane_off + S::TM_O + 32u * j;
-                        tmem_ld32(oa, o);
-                        tmem_ld_wait(o);
+                // O_x is D columns: D / 32 chunks of 32, loaded up to four at a time
+                constexpr int RC = (D / 32 < 4) ? D / 32 : 4;
 #pragma unroll
-                        for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * alpha);
-                        tmem_st32(oa, o);
+                for (int j0 = 0; j0 < D / 32; j0 += RC) {
+                    uint32_t o[RC][32];
+#pragma unroll
+                    for (int j = 0; j < RC; ++j) tmem_ld32(o_tmem + 32u * (j0 + j), o[j]);
+#pragma unroll
+                    for (int j = 0; j < RC; ++j) tmem_ld_wait(o[j]);
+#pragma unroll
+                    for (int j = 0; j < RC; ++j) {
+#pragma unroll
+                        for (int t = 0; t < 32; t += 2) {
+                            float a, bb;
+                            fma2(a, bb, __uint_as_float(o[j][t]), __uint_as_float(o[j][t + 1]), alpha, alpha, 0.f, 0.f);
+                            o[j][t] = __float_as_uint(a);
+                            o[j][t + 1] = __float_as_uint(bb);
+                        }
+                        tmem_st32(o_tmem + 32u * (j0 + j), o[j]);
                     }
-                    tmem_st_wait();
                 }
+                tmem_st_wait();
             }
             tc_fence_before();
-            mbar_arrive(bar(S::B_PFULL + (it & 1)));
+            mbar_arrive(bar(S::B_PFULL + x));
         }
         // ---------------------------------------------------------- epilogue
         if (ok && it > 0) {
-            ok = mbar_wait_warp(bar(S::B_PVDONE + ((it - 1) & 1)), (uint32_t)((it - 1) >> 1) & 1u, g,
-                                0x403);
+            ok = mbar_wait_warp(bar(S::B_PVDONE + x), (uint32_t)(it - 1) & 1u, g, 0x403);
             tc_fence_after();
         }
         if (ok) {
@@ -330,7 +408,7 @@ __global__ void __launch_bounds__(256, 1) fa_fwd_kernel(const __grid_constant__ 
             for (int j = 0; j < D / 32; ++j) {
                 uint32_t o[32];
                 if (it > 0) {
-                    tmem_ld32(tmem + lane_off + S::TM_O + 32u * j, o);
+                    tmem_ld32(o_tmem + 32u * j, o);
                     tmem_ld_wait(o);
                 } else {
 #pragma unroll
@@ -340,15 +418,17 @@ __global__ void __launch_bounds__(256, 1) fa_fwd_kernel(const __grid_constant__ 
 #pragma unroll
                 for (int t = 0; t < 16; ++t)
                     w[t] = pack_bf16x2(__uint_as_float(o[2 * t]) * inv_l, __uint_as_float(o[2 * t + 1]) * inv_l);
-                if (q < p.N) {
+                if (r < qn[x]) {
                     uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * j);
 #pragma unroll
                     for (int t = 0; t < 4; ++t) dst[t] = make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
                 }
             }
-            if (q < p.N)
-                p.LSE[(size_t)bh * p.N + q] = (l > 0.f) ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+            if (r < qn[x])
+                p.LSE[(size_t)bh * p.N + q] = (l > 0.f) ? (m_ref + log2f(l)) * 0.69314718055994530942f : -INFINITY;
         }
+        __syncwarp();
+        setmaxnreg_dec<S::REGS_CTRL>();
     }
 
     tc_fence_before();
@@ -364,8 +444,8 @@ static cudaError_t launch_fwd_t(const FwdParams &p, cudaStream_t st) {
     const int smem = FwdShape<D>::SMEM_BYTES;
     cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    const unsigned grid = (unsigned)p.Tq * (unsigned)p.BH;
-    fa_fwd_kernel<D><<<grid, 256, smem, st>>>(p);
+    const unsigned grid = (unsigned)((p.Tq + 1) / 2) * (unsigned)p.BH;
+    fa_fwd_kernel<D><<<grid, FwdShape<D>::THREADS, smem, st>>>(p);
     return cudaGetLastError();
 }
 

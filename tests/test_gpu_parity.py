@@ -85,16 +85,19 @@ def test_fully_masked_rows_and_zero_length(d):
     check_grads(got2, ref2, "row-block masked")
 
 
-def test_large_scores_and_other_scale():
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_large_scores_and_other_scale(d, causal):
     # Q, K scaled by 3 and scale 0.7: scores with standard deviation ~50, so
-    # the running maximum moves often and the softmax is nearly one-hot.  V
-    # stays N(0, 1) so that the absolute bound keeps its meaning (bf16 P
-    # carries a relative rounding of 2^-9 into O).
-    c = make_case(1, 2, 384, 64, seed=21)
+    # the running maximum jumps by more than 2^8 on many tiles (every O
+    # rescale path runs, for both query tiles of a CTA) and the softmax is
+    # nearly one-hot.  V stays N(0, 1) so that the absolute bound keeps its
+    # meaning (bf16 P carries a relative rounding of 2^-9 into O).
+    c = make_case(1, 2, 640, d, seed=21 + d, causal=causal)
     c["Q"] = (c["Q"].float() * 3).to(torch.bfloat16)
     c["K"] = (c["K"].float() * 3).to(torch.bfloat16)
     c["scale"] = 0.7
-    compare(c, "large scores")
+    compare(c, "large scores d=%d causal=%s" % (d, causal))
 
 
 def test_key_len_out_of_range_is_clamped_and_flagged():
