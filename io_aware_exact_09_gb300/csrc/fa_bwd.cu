@@ -15,16 +15,19 @@
 //   1. fa_bwd_pre:     D = rowsum(dO * O) (fp32) and dQacc = 0      (HBM-bound)
 //   2. fa_bwd_kernel:  one CTA per (128-key tile, b*h); loop over the query
 //      blocks that see the tile:
-//        warp 0  TMA: K_j, V_j once; Q_i, dO_i through a 2-stage ring
+//        warp 0  TMA: K_j, V_j once; Q_i, dO_i through a 2-stage ring; the
+//                whole warp stages LSE_i and D_i into shared memory with them
 //        warp 1  tcgen05: S^T = K Q^T, dP^T = V dO^T, dV += P^T dO,
 //                dK += dS^T Q (P^T, dS^T read from TMEM), and the dQ
 //                contribution into one of two TMEM buffers
-//        warps 4-7  one key row per thread: P^T = 2^(s*c - LSE*log2 e), masks,
+//        warps 4-7 and 8-11  two compute warpgroups, one key row per thread,
+//                each on half of the query columns (the backward has no row
+//                reduction): P^T = 2^(s*c - LSE*log2 e), masks,
 //                dS^T = P^T o (dP^T - D) -> bf16 into TMEM and into shared
-//                memory (the dQ MMA's operand); drain the previous dQ
-//                contribution through a swizzled shared tile and a TMA
-//                reduce-add into the fp32 accumulator; at the end
-//                dK * scale and dV -> bf16.
+//                memory (the dQ MMA's operand); each drains half of the
+//                previous dQ contribution through a swizzled shared tile and
+//                per-warp TMA reduce-adds into the fp32 accumulator; at the
+//                end each converts half of dK * scale and dV to bf16.
 //      d = 64 uses 128-row query blocks and dQ = dS K (TMEM lane = query);
 //      d = 128 uses 64-row query blocks and dQ^T = K^T dS^T (TMEM lane = head
 //      dimension), so that S, dP, dV, dK and two dQ buffers fit in the 512
@@ -55,7 +58,7 @@ struct BwdShape {
     // fp32, 128-byte swizzled, two buffers
     static constexpr int STG_BYTES = D * BQ * 4;
     static constexpr int OFF_DQS = OFF_DS + DS_BYTES;
-    static constexpr int DQ_BOX_ROWS = DQ_T ? BQ : 32;    // rows of one warp's reduce box
+    static constexpr int DQ_BOX_ROWS = 32;                // one warp's reduce box: 32 x 32 fp32
     static constexpr int OFF_LSE = OFF_DQS + 2 * STG_BYTES;  // [2][BQ] fp32 (log2 domain)
     static constexpr int OFF_DV = OFF_LSE + 2 * BQ * 4;   // [2][BQ] fp32
     static constexpr int OFF_BAR = OFF_DV + 2 * BQ * 4;
@@ -66,18 +69,19 @@ struct BwdShape {
     static constexpr int B_DPFULL = 6;
     static constexpr int B_PFULL = 7;
     static constexpr int B_DSFULL = 8;
-    static constexpr int B_SDPFREE = 9;
+    static constexpr int B_SFREE = 9;                     // dV of a step done: S columns free
     static constexpr int B_DQFULL = 10;                   // [2]
     static constexpr int B_DQFREE = 12;                   // [2]
     static constexpr int B_ACC = 14;
     static constexpr int B_FIN = 15;
-    static constexpr int B_LSE = 16;                      // [2] LSE/D block staged (128 arrivals)
-    static constexpr int NBAR = 18;
+    static constexpr int B_LSE = 16;                      // [2] LSE/D block staged (32 arrivals)
+    static constexpr int B_DPFREE = 18;                   // dK of a step done: dP columns free
+    static constexpr int NBAR = 19;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t TM_S = 0;                   // BQ columns (P^T as bf16 in the first BQ/2)
-    static constexpr uint32_t TM_DP = BQ;                 // BQ columns (dS^T as bf16 in the first BQ/2)
+    static constexpr uint32_t TM_S = 0;                   // BQ columns (P^T as bf16: see packed_col)
+    static constexpr uint32_t TM_DP = BQ;                 // BQ columns (dS^T as bf16: see packed_col)
     static constexpr uint32_t TM_DV = 2 * BQ;             // D columns
     static constexpr uint32_t TM_DK = 2 * BQ + D;         // D columns
     static constexpr uint32_t TM_DQ = 2 * BQ + 2 * D;     // 2 x 64 columns
@@ -90,9 +94,10 @@ __device__ __forceinline__ void drain_wait_b(uint32_t bar, uint32_t parity) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(256, 1) fa_bwd_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(384, 1) fa_bwd_kernel(const __grid_constant__ BwdParams p) {
     using S = BwdShape<D>;
     constexpr int BQ = S::BQ;
+    constexpr int CW = BQ / 2;                  // query columns per compute warpgroup
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -135,23 +140,24 @@ __global__ void __launch_bounds__(256, 1) fa_bwd_kernel(const __grid_constant__ 
             mbar_init(bar(S::B_QFULL + s), 1);
             mbar_init(bar(S::B_QEMPTY + s), 1);
             mbar_init(bar(S::B_DQFULL + s), 1);
-            mbar_init(bar(S::B_DQFREE + s), 128);
+            mbar_init(bar(S::B_DQFREE + s), 256);
+            mbar_init(bar(S::B_LSE + s), 32);
         }
         mbar_init(bar(S::B_SFULL), 1);
         mbar_init(bar(S::B_DPFULL), 1);
-        mbar_init(bar(S::B_PFULL), 128);
-        mbar_init(bar(S::B_DSFULL), 128);
-        mbar_init(bar(S::B_SDPFREE), 1);
+        mbar_init(bar(S::B_PFULL), 256);
+        mbar_init(bar(S::B_DSFULL), 256);
+        mbar_init(bar(S::B_SFREE), 1);
+        mbar_init(bar(S::B_DPFREE), 1);
         mbar_init(bar(S::B_ACC), 1);
         mbar_init(bar(S::B_FIN), 1);
-        mbar_init(bar(S::B_LSE), 128);
-        mbar_init(bar(S::B_LSE + 1), 128);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&p.tmQ);
         tma_prefetch_desc(&p.tmdO);
         tma_prefetch_desc(&p.tmK);
         tma_prefetch_desc(&p.tmV);
+        tma_prefetch_desc(&p.tmdQ);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), S::TMEM_COLS);
@@ -162,32 +168,55 @@ __global__ void __launch_bounds__(256, 1) fa_bwd_kernel(const __grid_constant__ 
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const int first = next_qb(-1);
+    float *lse_s = reinterpret_cast<float *>(sb + S::OFF_LSE);   // [2][BQ], log2 domain
+    float *dv_s = reinterpret_cast<float *>(sb + S::OFF_DV);     // [2][BQ]
 
     if (warp == 0) {
         // ---------------------------------------------------------- producer
-        if (lane == 0 && first < p.Tqb) {
-            mbar_arrive_expect_tx(bar(S::B_KV), 2 * S::KV_BYTES);
-            for (int c = 0; c < S::CHUNKS; ++c) {
-                tma_load_3d(base + S::OFF_K + c * S::KV_CHUNK, &p.tmK, bar(S::B_KV), c * 64, k0, bh);
-                tma_load_3d(base + S::OFF_V + c * S::KV_CHUNK, &p.tmV, bar(S::B_KV), c * 64, k0, bh);
+        // lane 0 issues the TMA copies; the whole warp stages LSE and D of
+        // the same query block into shared memory one stage ahead.
+        if (first < p.Tqb) {
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bar(S::B_KV), 2 * S::KV_BYTES);
+                for (int c = 0; c < S::CHUNKS; ++c) {
+                    tma_load_3d(base + S::OFF_K + c * S::KV_CHUNK, &p.tmK, bar(S::B_KV), c * 64, k0, bh);
+                    tma_load_3d(base + S::OFF_V + c * S::KV_CHUNK, &p.tmV, bar(S::B_KV), c * 64, k0, bh);
+                }
             }
             int i = 0;
             bool ok = true;
             for (int qb = first; qb < p.Tqb; qb = next_qb(qb), ++i) {
                 const int s = i & 1;
-                if (!mbar_wait(bar(S::B_QEMPTY + s), ((uint32_t)(i >> 1) & 1u) ^ 1u, g, 0x111)) {
+                if (!mbar_wait_warp(bar(S::B_QEMPTY + s), ((uint32_t)(i >> 1) & 1u) ^ 1u, g, 0x111)) {
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(bar(S::B_QFULL + s), 2 * S::Q_BYTES);
-                for (int c = 0; c < S::CHUNKS; ++c) {
-                    tma_load_3d(base + S::OFF_Q + s * S::Q_BYTES + c * S::Q_CHUNK, &p.tmQ,
-                                bar(S::B_QFULL + s), c * 64, qb * BQ, bh);
-                    tma_load_3d(base + S::OFF_DO + s * S::Q_BYTES + c * S::Q_CHUNK, &p.tmdO,
-                                bar(S::B_QFULL + s), c * 64, qb * BQ, bh);
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(bar(S::B_QFULL + s), 2 * S::Q_BYTES);
+                    for (int c = 0; c < S::CHUNKS; ++c) {
+                        tma_load_3d(base + S::OFF_Q + s * S::Q_BYTES + c * S::Q_CHUNK, &p.tmQ,
+                                    bar(S::B_QFULL + s), c * 64, qb * BQ, bh);
+                        tma_load_3d(base + S::OFF_DO + s * S::Q_BYTES + c * S::Q_CHUNK, &p.tmdO,
+                                    bar(S::B_QFULL + s), c * 64, qb * BQ, bh);
+                    }
                 }
+                // LSE in the log2 domain (+inf past N or for a row with no
+                // visible key: its P is 0) and D for the block's rows
+                const int qa = qb * BQ;
+                for (int t = lane; t < BQ; t += 32) {
+                    const int qq = qa + t;
+                    float v = INFINITY, dd = 0.f;
+                    if (qq < p.N) {
+                        const float L = p.LSE[(size_t)bh * p.N + qq];
+                        v = (L == -INFINITY) ? INFINITY : L * 1.4426950408889634f;
+                        dd = p.Dvec[(size_t)bh * p.N + qq];
+                    }
+                    lse_s[s * BQ + t] = v;
+                    dv_s[s * BQ + t] = dd;
+                }
+                mbar_arrive(bar(S::B_LSE + s));
             }
-            if (!ok) {
+            if (!ok && lane == 0) {
                 drain_wait_b(bar(S::B_KV), 0);
                 for (int j = (i > 2 ? i - 2 : 0); j < i; ++j)
                     drain_wait_b(bar(S::B_QFULL + (j & 1)), (uint32_t)(j >> 1) & 1u);
@@ -195,64 +224,91 @@ __global__ void __launch_bounds__(256, 1) fa_bwd_kernel(const __grid_constant__ 
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer
+        // Issue order, step i:  dV(i), S(i+1), dK(i), dQ(i), dP(i+1).
+        // S(i+1) only needs dV(i) to have read P(i) from the S columns, and
+        // dP(i+1) only needs dK(i) to have read dS(i) from the dP columns,
+        // so the next step's scores are ready while the compute warps are
+        // still on this step, and the tensor pipe keeps a queue.
         if (lane == 0) {
             constexpr uint32_t IDESC_S = idesc_bf16(128, BQ, false, false);   // S^T, dP^T
             constexpr uint32_t IDESC_ACC = idesc_bf16(128, D, false, true);   // dV, dK
             constexpr uint32_t IDESC_DQ = idesc_bf16(128, 64, true, true);    // dQ or dQ^T
+            const uint32_t ks = base + S::OFF_K, vs = base + S::OFF_V;
+            auto issue_s = [&](int step) {       // S^T = K Q^T: M = 128 keys, N = BQ, K = D
+                const uint32_t qs = base + S::OFF_Q + (step & 1) * S::Q_BYTES;
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t ko = (k >> 2) * S::KV_CHUNK + (k & 3) * 32;
+                    const uint32_t qo = (k >> 2) * S::Q_CHUNK + (k & 3) * 32;
+                    mma_ss(tmem + S::TM_S, sdesc_sw128(ks + ko, 16, 1024), sdesc_sw128(qs + qo, 16, 1024), IDESC_S,
+                           k > 0 ? 1u : 0u);
+                }
+                mma_commit(bar(S::B_SFULL));
+            };
+            auto issue_dp = [&](int step) {      // dP^T = V dO^T
+                const uint32_t dos = base + S::OFF_DO + (step & 1) * S::Q_BYTES;
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t ko = (k >> 2) * S::KV_CHUNK + (k & 3) * 32;
+                    const uint32_t qo = (k >> 2) * S::Q_CHUNK + (k & 3) * 32;
+                    mma_ss(tmem + S::TM_DP, sdesc_sw128(vs + ko, 16, 1024), sdesc_sw128(dos + qo, 16, 1024), IDESC_S,
+                           k > 0 ? 1u : 0u);
+                }
+                mma_commit(bar(S::B_DPFULL));
+            };
+            // P^T and dS^T are stored as bf16 pairs by the two compute
+            // warpgroups, each inside its own half of the columns (so that
+            // neither overwrites fp32 values the other is still reading):
+            // queries [16k, 16k + 16) sit at column (16k / CW) CW + 8 (k mod CW/16).
+            auto packed_col = [](int k) -> uint32_t {
+                constexpr int KW = (BQ / 2) / 16;
+                return (uint32_t)((k / KW) * (BQ / 2) + 8 * (k % KW));
+            };
             bool ok = true;
             int i = 0;
             if (first < p.Tqb) {
-                ok = mbar_wait(bar(S::B_KV), 0, g, 0x211);
-                for (int qb = first; ok && qb < p.Tqb; qb = next_qb(qb), ++i) {
+                ok = mbar_wait(bar(S::B_KV), 0, g, 0x211) && mbar_wait(bar(S::B_QFULL), 0, g, 0x212);
+                if (ok) {
+                    tc_fence_after();
+                    issue_s(0);
+                    issue_dp(0);
+                }
+                for (int qb = first; ok && qb < p.Tqb; ++i) {
                     const int s = i & 1;
                     const uint32_t qs = base + S::OFF_Q + s * S::Q_BYTES;
                     const uint32_t dos = base + S::OFF_DO + s * S::Q_BYTES;
-                    if (!mbar_wait(bar(S::B_QFULL + s), (uint32_t)(i >> 1) & 1u, g, 0x212)) { ok = false; break; }
-                    // S / dP columns are free once dV and dK of the previous step have read them
-                    if (i > 0 && !mbar_wait(bar(S::B_SDPFREE), (uint32_t)(i - 1) & 1u, g, 0x213)) { ok = false; break; }
-                    tc_fence_after();
-                    // S^T = K Q^T and dP^T = V dO^T: M = 128 keys, N = BQ queries, K = D
-#pragma unroll
-                    for (int k = 0; k < D / 16; ++k) {
-                        const uint32_t ko = (k >> 2) * S::KV_CHUNK + (k & 3) * 32;
-                        const uint32_t qo = (k >> 2) * S::Q_CHUNK + (k & 3) * 32;
-                        mma_ss(tmem + S::TM_S, sdesc_sw128(base + S::OFF_K + ko, 16, 1024),
-                               sdesc_sw128(qs + qo, 16, 1024), IDESC_S, k > 0 ? 1u : 0u);
-                    }
-                    mma_commit(bar(S::B_SFULL));
-#pragma unroll
-                    for (int k = 0; k < D / 16; ++k) {
-                        const uint32_t ko = (k >> 2) * S::KV_CHUNK + (k & 3) * 32;
-                        const uint32_t qo = (k >> 2) * S::Q_CHUNK + (k & 3) * 32;
-                        mma_ss(tmem + S::TM_DP, sdesc_sw128(base + S::OFF_V + ko, 16, 1024),
-                               sdesc_sw128(dos + qo, 16, 1024), IDESC_S, k > 0 ? 1u : 0u);
-                    }
-                    mma_commit(bar(S::B_DPFULL));
+                    const int qb_next = next_qb(qb);
+                    const bool more = qb_next < p.Tqb;
                     // dV += P^T dO: A = P^T from TMEM, B = dO (N = D, K = queries, MN-major)
                     if (!mbar_wait(bar(S::B_PFULL), (uint32_t)i & 1u, g, 0x214)) { ok = false; break; }
                     tc_fence_after();
 #pragma unroll
                     for (int k = 0; k < BQ / 16; ++k)
-                        mma_ts(tmem + S::TM_DV, tmem + S::TM_S + 8u * k,
-                               sdesc_sw128(dos + k * 2048, S::Q_CHUNK, 1024), IDESC_ACC,
-                               (i > 0 || k > 0) ? 1u : 0u);
+                        mma_ts(tmem + S::TM_DV, tmem + S::TM_S + packed_col(k), sdesc_sw128(dos + k * 2048, S::Q_CHUNK, 1024),
+                               IDESC_ACC, (i > 0 || k > 0) ? 1u : 0u);
+                    mma_commit(bar(S::B_SFREE));
+                    // S(i+1) once dV(i) has read P(i)
+                    if (more) {
+                        if (!mbar_wait(bar(S::B_QFULL + (s ^ 1)), (uint32_t)((i + 1) >> 1) & 1u, g, 0x217) ||
+                            !mbar_wait(bar(S::B_SFREE), (uint32_t)i & 1u, g, 0x213)) { ok = false; break; }
+                        tc_fence_after();
+                        issue_s(i + 1);
+                    }
                     // dK += dS^T Q: A = dS^T from TMEM, B = Q (MN-major)
                     if (!mbar_wait(bar(S::B_DSFULL), (uint32_t)i & 1u, g, 0x215)) { ok = false; break; }
                     tc_fence_after();
 #pragma unroll
                     for (int k = 0; k < BQ / 16; ++k)
-                        mma_ts(tmem + S::TM_DK, tmem + S::TM_DP + 8u * k,
-                               sdesc_sw128(qs + k * 2048, S::Q_CHUNK, 1024), IDESC_ACC,
-                               (i > 0 || k > 0) ? 1u : 0u);
+                        mma_ts(tmem + S::TM_DK, tmem + S::TM_DP + packed_col(k), sdesc_sw128(qs + k * 2048, S::Q_CHUNK, 1024),
+                               IDESC_ACC, (i > 0 || k > 0) ? 1u : 0u);
+                    mma_commit(bar(S::B_DPFREE));
                     mma_commit(bar(S::B_QEMPTY + s));
-                    mma_commit(bar(S::B_SDPFREE));
                     // dQ contribution into TMEM buffer i % 2 (drained by the compute warps)
                     if (i >= 2 &&
                         !mbar_wait(bar(S::B_DQFREE + s), (uint32_t)((i - 2) >> 1) & 1u, g, 0x216)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t dq_tmem = tmem + S::TM_DQ + 64u * (uint32_t)s;
                     const uint32_t ds = base + S::OFF_DS;
-                    const uint32_t ks = base + S::OFF_K;
 #pragma unroll
                     for (int k = 0; k < kTile / 16; ++k) {
                         if (S::DQ_T)   // dQ^T = K^T dS^T: A = K^T (M = d), B = dS (N = queries)
@@ -263,6 +319,13 @@ __global__ void __launch_bounds__(256, 1) fa_bwd_kernel(const __grid_constant__ 
                                    sdesc_sw128(ks + k * 2048, S::KV_CHUNK, 1024), IDESC_DQ, k > 0 ? 1u : 0u);
                     }
                     mma_commit(bar(S::B_DQFULL + s));
+                    // dP(i+1) once dK(i) has read dS(i)
+                    if (more) {
+                        if (!mbar_wait(bar(S::B_DPFREE), (uint32_t)i & 1u, g, 0x218)) { ok = false; break; }
+                        tc_fence_after();
+                        issue_dp(i + 1);
+                    }
+                    qb = qb_next;
                 }
                 if (ok) mma_commit(bar(S::B_ACC));
             }
@@ -270,66 +333,62 @@ __global__ void __launch_bounds__(256, 1) fa_bwd_kernel(const __grid_constant__ 
             drain_wait_b(bar(S::B_FIN), 0);
         }
     } else if (warp >= 4) {
-        // ---------------------------------------------------------- compute
+        // ---------------------------------------------------------- compute (two warpgroups)
+        // Warpgroup wg handles query columns [wg*CW, wg*CW + CW) of S^T and
+        // dP^T (the backward needs no row reduction, so the halves are
+        // independent), half of the dQ drain and half of the dK/dV columns.
+        const int wg = (warp - 4) >> 2;
         const int wq = warp & 3;
         const int r = wq * 32 + lane;           // TMEM lane: key row (S^T, dP^T, dK, dV), query/dim row (dQ)
-        const int tid = threadIdx.x - 128;
         const int key = k0 + r;
+        const int c0 = wg * CW;
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const float c2 = p.scale_log2;
-        float *lse_s = reinterpret_cast<float *>(sb + S::OFF_LSE);
-        float *dv_s = reinterpret_cast<float *>(sb + S::OFF_DV);
         bool ok = true;
         int i = 0, prev_qb = -1;
 
-        // drain the dQ contribution of step j (query block qb): TMEM -> swizzled
-        // shared staging -> TMA reduce-add into the fp32 accumulator.  Each warp
-        // stages and reduces its own part, so no cross-warp sync is needed.
+        // drain this warpgroup's half of step j's dQ contribution (query
+        // block qb): TMEM -> swizzled shared staging -> per-warp TMA
+        // reduce-add (box 32 x 32) into the fp32 accumulator
         auto drain_dq = [&](int j, int qb) -> bool {
             if (!mbar_wait_warp(bar(S::B_DQFULL + (j & 1)), (uint32_t)(j >> 1) & 1u, g, 0x411)) return false;
             tc_fence_after();
-            uint32_t v0[32], v1[32];
-            const uint32_t a = tmem + lane_off + S::TM_DQ + 64u * (uint32_t)(j & 1);
-            tmem_ld32(a, v0);
-            tmem_ld32(a + 32u, v1);
-            tmem_ld_wait(v0);
-            tmem_ld_wait(v1);
+            uint32_t v[32];
+            tmem_ld32(tmem + lane_off + S::TM_DQ + 64u * (uint32_t)(j & 1) + 32u * wg, v);
+            tmem_ld_wait(v);
             tc_fence_before();
             mbar_arrive(bar(S::B_DQFREE + (j & 1)));
             uint8_t *stg = sb + S::OFF_DQS + (j & 1) * S::STG_BYTES;
             // the reduce issued from this buffer two drains ago must have read it
             if (lane == 0) bulk_wait_group_read<1>();
             __syncwarp();
+            uint32_t box;             // shared address of this warp's 32 x 32 box
+            int cx, cy;               // its coordinates (head dimension, query)
             if (S::DQ_T) {
-                // lane = head dimension 32*wq + lane (chunk wq), column t = query t
-                uint8_t *cb = stg + wq * (BQ * 128) + (lane & 3) * 4;
+                // lane = head dimension 32*wq + lane (chunk wq), column t = query c0 + t
+                uint8_t *cb = stg + wq * (BQ * 128) + c0 * 128 + (lane & 3) * 4;
                 const int grp = lane >> 2;
 #pragma unroll
                 for (int t = 0; t < 32; ++t)
-                    *reinterpret_cast<uint32_t *>(cb + t * 128 + ((grp ^ (t & 7)) << 4)) = v0[t];
-#pragma unroll
-                for (int t = 0; t < 32; ++t)
-                    *reinterpret_cast<uint32_t *>(cb + (t + 32) * 128 + ((grp ^ (t & 7)) << 4)) = v1[t];
+                    *reinterpret_cast<uint32_t *>(cb + t * 128 + ((grp ^ (t & 7)) << 4)) = v[t];
+                box = smem_u32(stg + wq * (BQ * 128) + c0 * 128);
+                cx = wq * 32;
+                cy = qb * BQ + c0;
             } else {
-                // lane = query row r of the block, columns = head dimensions 0..63
+                // lane = query row r of the block, columns = head dimensions 32*wg .. 32*wg + 31
+                uint8_t *cb = stg + wg * (BQ * 128) + r * 128;
 #pragma unroll
-                for (int gq = 0; gq < 8; ++gq) {
-                    *reinterpret_cast<uint4 *>(stg + r * 128 + ((gq ^ (r & 7)) << 4)) =
-                        make_uint4(v0[4 * gq], v0[4 * gq + 1], v0[4 * gq + 2], v0[4 * gq + 3]);
-                    *reinterpret_cast<uint4 *>(stg + BQ * 128 + r * 128 + ((gq ^ (r & 7)) << 4)) =
-                        make_uint4(v1[4 * gq], v1[4 * gq + 1], v1[4 * gq + 2], v1[4 * gq + 3]);
-                }
+                for (int gq = 0; gq < 8; ++gq)
+                    *reinterpret_cast<uint4 *>(cb + ((gq ^ (r & 7)) << 4)) =
+                        make_uint4(v[4 * gq], v[4 * gq + 1], v[4 * gq + 2], v[4 * gq + 3]);
+                box = smem_u32(stg + wg * (BQ * 128) + wq * 32 * 128);
+                cx = wg * 32;
+                cy = qb * BQ + wq * 32;
             }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-                const uint32_t st = smem_u32(stg);
-                if (S::DQ_T) {
-                    tma_reduce_add_3d(&p.tmdQ, st + wq * (BQ * 128), wq * 32, qb * BQ, bh);
-                } else {
-                    tma_reduce_add_3d(&p.tmdQ, st + wq * 32 * 128, 0, qb * BQ + wq * 32, bh);
-                    tma_reduce_add_3d(&p.tmdQ, st + BQ * 128 + wq * 32 * 128, 32, qb * BQ + wq * 32, bh);
-                }
+                tma_reduce_add_3d(&p.tmdQ, box, cx, cy, bh);
                 bulk_commit_group();
             }
             return true;
@@ -338,56 +397,39 @@ __global__ void __launch_bounds__(256, 1) fa_bwd_kernel(const __grid_constant__ 
         for (int qb = first; qb < p.Tqb; qb = next_qb(qb), ++i) {
             const unsigned klass = cls(qb);
             const int qa = qb * BQ;
-            // LSE (log2 domain; +inf for rows past N or with nothing visible) and D for this block
-            {
-                float *ls = lse_s + (i & 1) * BQ;
-                float *dd = dv_s + (i & 1) * BQ;
-                for (int t = tid; t < 2 * BQ; t += 128) {
-                    const int tt = t % BQ;
-                    const int qq = qa + tt;
-                    if (t < BQ) {
-                        float v = INFINITY;
-                        if (qq < p.N) {
-                            const float L = p.LSE[(size_t)bh * p.N + qq];
-                            v = (L == -INFINITY) ? INFINITY : L * 1.4426950408889634f;
-                        }
-                        ls[tt] = v;
-                    } else {
-                        dd[tt] = (qq < p.N) ? p.Dvec[(size_t)bh * p.N + qq] : 0.f;
-                    }
-                }
-                mbar_arrive(bar(S::B_LSE + (i & 1)));
-                if (!mbar_wait_warp(bar(S::B_LSE + (i & 1)), (uint32_t)(i >> 1) & 1u, g, 0x410)) {
-                    ok = false;
-                    break;
-                }
-            }
+            if (!mbar_wait_warp(bar(S::B_LSE + (i & 1)), (uint32_t)(i >> 1) & 1u, g, 0x410)) { ok = false; break; }
             const float *ls = lse_s + (i & 1) * BQ;
             const float *dd = dv_s + (i & 1) * BQ;
 
-            // P^T = 2^(s * c - LSE_q * log2 e), masked
+            // P^T = 2^(s * c - LSE_q * log2 e), masked, for columns c0 .. c0 + CW
             if (!mbar_wait_warp(bar(S::B_SFULL), (uint32_t)i & 1u, g, 0x412)) { ok = false; break; }
             tc_fence_after();
-            uint32_t pk[BQ / 2];
+            uint32_t pk[CW / 2];
+            {
+                uint32_t sr[CW / 32][32];
 #pragma unroll
-            for (int j = 0; j < BQ / 32; ++j) {
-                uint32_t sr[32];
-                tmem_ld32(tmem + lane_off + S::TM_S + 32u * j, sr);
-                tmem_ld_wait(sr);
+                for (int j = 0; j < CW / 32; ++j) tmem_ld32(tmem + lane_off + S::TM_S + c0 + 32u * j, sr[j]);
 #pragma unroll
-                for (int t = 0; t < 32; t += 2) {
-                    const int qx = qa + 32 * j + t;
-                    float p0 = ex2(fmaf(__uint_as_float(sr[t]), c2, -ls[32 * j + t]));
-                    float p1 = ex2(fmaf(__uint_as_float(sr[t + 1]), c2, -ls[32 * j + t + 1]));
-                    if (klass == kTilePartial) {
-                        if (key >= kvis || (p.causal && key > qx)) p0 = 0.f;
-                        if (key >= kvis || (p.causal && key > qx + 1)) p1 = 0.f;
+                for (int j = 0; j < CW / 32; ++j) tmem_ld_wait(sr[j]);
+#pragma unroll
+                for (int j = 0; j < CW / 32; ++j)
+#pragma unroll
+                    for (int t = 0; t < 32; t += 2) {
+                        const int cq = c0 + 32 * j + t;          // query column within the block
+                        const float2 l2 = *reinterpret_cast<const float2 *>(ls + cq);
+                        float p0, p1;
+                        fma2(p0, p1, __uint_as_float(sr[j][t]), __uint_as_float(sr[j][t + 1]), c2, c2, -l2.x, -l2.y);
+                        p0 = ex2(p0);
+                        p1 = ex2(p1);
+                        if (klass == kTilePartial) {
+                            if (key >= kvis || (p.causal && key > qa + cq)) p0 = 0.f;
+                            if (key >= kvis || (p.causal && key > qa + cq + 1)) p1 = 0.f;
+                        }
+                        pk[16 * j + t / 2] = pack_bf16x2(p0, p1);
                     }
-                    pk[16 * j + t / 2] = pack_bf16x2(p0, p1);
-                }
             }
 #pragma unroll
-            for (int j = 0; j < BQ / 32; ++j) tmem_st16(tmem + lane_off + S::TM_S + 16u * j, pk + 16 * j);
+            for (int j = 0; j < CW / 32; ++j) tmem_st16(tmem + lane_off + S::TM_S + c0 + 16u * j, pk + 16 * j);
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(bar(S::B_PFULL));
@@ -401,28 +443,34 @@ __global__ void __launch_bounds__(256, 1) fa_bwd_kernel(const __grid_constant__ 
             }
             tc_fence_after();
             uint8_t *ds_smem = sb + S::OFF_DS;
+            {
+                uint32_t dp[CW / 32][32];
 #pragma unroll
-            for (int j = 0; j < BQ / 32; ++j) {
-                uint32_t dp[32];
-                tmem_ld32(tmem + lane_off + S::TM_DP + 32u * j, dp);
-                tmem_ld_wait(dp);
-                uint32_t w[16];
+                for (int j = 0; j < CW / 32; ++j) tmem_ld32(tmem + lane_off + S::TM_DP + c0 + 32u * j, dp[j]);
 #pragma unroll
-                for (int t = 0; t < 16; ++t) {
-                    const uint32_t pp = pk[16 * j + t];
-                    const float d0 = bf16lo(pp) * (__uint_as_float(dp[2 * t]) - dd[32 * j + 2 * t]);
-                    const float d1 = bf16hi(pp) * (__uint_as_float(dp[2 * t + 1]) - dd[32 * j + 2 * t + 1]);
-                    w[t] = pack_bf16x2(d0, d1);
-                }
-                tmem_st16(tmem + lane_off + S::TM_DP + 16u * j, w);
-                // shared dS tile, queries contiguous (MN-major, 128-byte swizzle):
-                // [query chunk of 64][key row 0..127][128 bytes]
+                for (int j = 0; j < CW / 32; ++j) tmem_ld_wait(dp[j]);
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int qo = 32 * j + 8 * u;                 // first query of this 16-byte piece
-                    const int grp = (qo & 63) >> 3;
-                    uint8_t *dst = ds_smem + (qo >> 6) * (128 * 128) + r * 128 + ((grp ^ (r & 7)) << 4);
-                    *reinterpret_cast<uint4 *>(dst) = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+                for (int j = 0; j < CW / 32; ++j) {
+                    uint32_t w[16];
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) {
+                        const int cq = c0 + 32 * j + 2 * t;
+                        const uint32_t pp = pk[16 * j + t];
+                        const float2 d2 = *reinterpret_cast<const float2 *>(dd + cq);
+                        const float d0 = __uint_as_float(dp[j][2 * t]) - d2.x;
+                        const float d1 = __uint_as_float(dp[j][2 * t + 1]) - d2.y;
+                        w[t] = pack_bf16x2(bf16lo(pp) * d0, bf16hi(pp) * d1);
+                    }
+                    tmem_st16(tmem + lane_off + S::TM_DP + c0 + 16u * j, w);
+                    // shared dS tile, queries contiguous (MN-major, 128-byte swizzle):
+                    // [query chunk of 64][key row 0..127][128 bytes]
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int qo = c0 + 32 * j + 8 * u;        // first query of this 16-byte piece
+                        const int grp = (qo & 63) >> 3;
+                        uint8_t *dst = ds_smem + (qo >> 6) * (128 * 128) + r * 128 + ((grp ^ (r & 7)) << 4);
+                        *reinterpret_cast<uint4 *>(dst) = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+                    }
                 }
             }
             tmem_st_wait();
@@ -440,6 +488,7 @@ __global__ void __launch_bounds__(256, 1) fa_bwd_kernel(const __grid_constant__ 
         __syncwarp();
 
         // ---------------------------------------------------------- epilogue: dK, dV
+        // warpgroup wg converts head-dimension columns [wg*D/2, wg*D/2 + D/2)
         if (ok && i > 0) {
             ok = mbar_wait_warp(bar(S::B_ACC), 0, g, 0x415);
             tc_fence_after();
@@ -449,7 +498,7 @@ __global__ void __launch_bounds__(256, 1) fa_bwd_kernel(const __grid_constant__ 
             __nv_bfloat16 *dkrow = reinterpret_cast<__nv_bfloat16 *>(p.dK) + ((size_t)bh * p.N + key) * D;
             __nv_bfloat16 *dvrow = reinterpret_cast<__nv_bfloat16 *>(p.dV) + ((size_t)bh * p.N + key) * D;
 #pragma unroll 1
-            for (int j = 0; j < D / 32; ++j) {
+            for (int j = wg * (D / 64); j < (wg + 1) * (D / 64); ++j) {
                 uint32_t a[32], v[32];
                 if (i > 0) {
                     tmem_ld32(tmem + lane_off + S::TM_DK + 32u * j, a);
@@ -554,7 +603,7 @@ static cudaError_t launch_bwd_main_t(const BwdParams &p, cudaStream_t st) {
     const int smem = BwdShape<D>::SMEM_BYTES;
     cudaError_t e = cudaFuncSetAttribute(fa_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    fa_bwd_kernel<D><<<(unsigned)p.Tk * (unsigned)p.BH, 256, smem, st>>>(p);
+    fa_bwd_kernel<D><<<(unsigned)p.Tk * (unsigned)p.BH, 384, smem, st>>>(p);
     return cudaGetLastError();
 }
 

@@ -122,3 +122,18 @@ def test_repeat_calls_are_deterministic_forward():
     O1, L1 = fa.attention_forward(g["Q"], g["K"], g["V"], causal=True)
     O2, L2 = fa.attention_forward(g["Q"], g["K"], g["V"], causal=True)
     assert torch.equal(O1, O2) and torch.equal(L1, L2)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_repeat_calls_are_deterministic_backward(d):
+    # dK and dV are accumulated inside one CTA (no atomics): repeated calls
+    # must agree bit for bit; a race between the compute warps shows up here
+    import io_aware_exact_09_gb300 as fa
+    c = make_case(3, 2, 700, d, seed=19, causal=True, key_len=[700, 333, 129])
+    g = {k: c[k].cuda() for k in ("Q", "K", "V", "dO")}
+    kl = c["key_len"].cuda()
+    O, L = fa.attention_forward(g["Q"], g["K"], g["V"], causal=True, key_len=kl)
+    first = fa.attention_backward(g["Q"], g["K"], g["V"], O, L, g["dO"], causal=True, key_len=kl)
+    for _ in range(4):
+        again = fa.attention_backward(g["Q"], g["K"], g["V"], O, L, g["dO"], causal=True, key_len=kl)
+        assert torch.equal(first[1], again[1]) and torch.equal(first[2], again[2])
