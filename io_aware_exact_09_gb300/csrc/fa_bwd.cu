@@ -128,7 +128,15 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_kernel(const __grid_constant__ 
         const int on = p.block_mask ? (p.block_mask[(size_t)(qa / kTile) * nb + kt] != 0) : 1;
         return tile_class(qa, min(BQ, p.N - qa), k0, kTile, kvis, p.causal, on);
     };
+    // Without a block mask the query blocks that see this key tile are
+    // exactly [qb_start, Tqb) (none when the tile lies past key_len): under
+    // the causal mask the first block whose last row reaches k0.
+    const int qb_start = (k0 >= kvis) ? p.Tqb : (p.causal ? k0 / BQ : 0);
     auto next_qb = [&](int qb) -> int {
+        if (!p.block_mask) {
+            const int nq = qb < qb_start ? qb_start : qb + 1;
+            return nq < p.Tqb ? nq : p.Tqb;
+        }
         for (int x = qb + 1; x < p.Tqb; ++x)
             if (cls(x) != kTileSkip) return x;
         return p.Tqb;
@@ -233,27 +241,30 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_kernel(const __grid_constant__ 
             constexpr uint32_t IDESC_S = idesc_bf16(128, BQ, false, false);   // S^T, dP^T
             constexpr uint32_t IDESC_ACC = idesc_bf16(128, D, false, true);   // dV, dK
             constexpr uint32_t IDESC_DQ = idesc_bf16(128, 64, true, true);    // dQ or dQ^T
-            const uint32_t ks = base + S::OFF_K, vs = base + S::OFF_V;
+            // shared-memory descriptors built once; per MMA only the start
+            // address moves (sdesc_add)
+            const uint64_t dK_kmaj = sdesc_sw128(base + S::OFF_K, 16, 1024);          // K as A, K-major
+            const uint64_t dV_kmaj = sdesc_sw128(base + S::OFF_V, 16, 1024);          // V as A, K-major
+            const uint64_t dQ_kmaj = sdesc_sw128(base + S::OFF_Q, 16, 1024);          // Q as B, K-major
+            const uint64_t ddO_kmaj = sdesc_sw128(base + S::OFF_DO, 16, 1024);        // dO as B, K-major
+            const uint64_t dQ_mn = sdesc_sw128(base + S::OFF_Q, S::Q_CHUNK, 1024);    // Q as B, MN-major
+            const uint64_t ddO_mn = sdesc_sw128(base + S::OFF_DO, S::Q_CHUNK, 1024);  // dO as B, MN-major
+            const uint64_t dK_mn = sdesc_sw128(base + S::OFF_K, S::KV_CHUNK, 1024);   // K (A or B), MN-major
+            const uint64_t ddS_mn = sdesc_sw128(base + S::OFF_DS, 128 * 128, 1024);   // dS (A or B), MN-major
             auto issue_s = [&](int step) {       // S^T = K Q^T: M = 128 keys, N = BQ, K = D
-                const uint32_t qs = base + S::OFF_Q + (step & 1) * S::Q_BYTES;
+                const uint64_t qd = sdesc_add(dQ_kmaj, (uint32_t)((step & 1) * S::Q_BYTES));
 #pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t ko = (k >> 2) * S::KV_CHUNK + (k & 3) * 32;
-                    const uint32_t qo = (k >> 2) * S::Q_CHUNK + (k & 3) * 32;
-                    mma_ss(tmem + S::TM_S, sdesc_sw128(ks + ko, 16, 1024), sdesc_sw128(qs + qo, 16, 1024), IDESC_S,
-                           k > 0 ? 1u : 0u);
-                }
+                for (int k = 0; k < D / 16; ++k)
+                    mma_ss(tmem + S::TM_S, sdesc_add(dK_kmaj, (k >> 2) * S::KV_CHUNK + (k & 3) * 32),
+                           sdesc_add(qd, (k >> 2) * S::Q_CHUNK + (k & 3) * 32), IDESC_S, k > 0 ? 1u : 0u);
                 mma_commit(bar(S::B_SFULL));
             };
             auto issue_dp = [&](int step) {      // dP^T = V dO^T
-                const uint32_t dos = base + S::OFF_DO + (step & 1) * S::Q_BYTES;
+                const uint64_t dd = sdesc_add(ddO_kmaj, (uint32_t)((step & 1) * S::Q_BYTES));
 #pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t ko = (k >> 2) * S::KV_CHUNK + (k & 3) * 32;
-                    const uint32_t qo = (k >> 2) * S::Q_CHUNK + (k & 3) * 32;
-                    mma_ss(tmem + S::TM_DP, sdesc_sw128(vs + ko, 16, 1024), sdesc_sw128(dos + qo, 16, 1024), IDESC_S,
-                           k > 0 ? 1u : 0u);
-                }
+                for (int k = 0; k < D / 16; ++k)
+                    mma_ss(tmem + S::TM_DP, sdesc_add(dV_kmaj, (k >> 2) * S::KV_CHUNK + (k & 3) * 32),
+                           sdesc_add(dd, (k >> 2) * S::Q_CHUNK + (k & 3) * 32), IDESC_S, k > 0 ? 1u : 0u);
                 mma_commit(bar(S::B_DPFULL));
             };
             // P^T and dS^T are stored as bf16 pairs by the two compute
@@ -275,8 +286,9 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_kernel(const __grid_constant__ 
                 }
                 for (int qb = first; ok && qb < p.Tqb; ++i) {
                     const int s = i & 1;
-                    const uint32_t qs = base + S::OFF_Q + s * S::Q_BYTES;
-                    const uint32_t dos = base + S::OFF_DO + s * S::Q_BYTES;
+                    const uint64_t q_mn = sdesc_add(dQ_mn, (uint32_t)(s * S::Q_BYTES));
+                    const uint64_t do_mn = sdesc_add(ddO_mn, (uint32_t)(s * S::Q_BYTES));
+                    const uint32_t acc0 = i > 0 ? 1u : 0u;
                     const int qb_next = next_qb(qb);
                     const bool more = qb_next < p.Tqb;
                     // dV += P^T dO: A = P^T from TMEM, B = dO (N = D, K = queries, MN-major)
@@ -284,8 +296,8 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_kernel(const __grid_constant__ 
                     tc_fence_after();
 #pragma unroll
                     for (int k = 0; k < BQ / 16; ++k)
-                        mma_ts(tmem + S::TM_DV, tmem + S::TM_S + packed_col(k), sdesc_sw128(dos + k * 2048, S::Q_CHUNK, 1024),
-                               IDESC_ACC, (i > 0 || k > 0) ? 1u : 0u);
+                        mma_ts(tmem + S::TM_DV, tmem + S::TM_S + packed_col(k), sdesc_add(do_mn, (uint32_t)k * 2048u),
+                               IDESC_ACC, k > 0 ? 1u : acc0);
                     mma_commit(bar(S::B_SFREE));
                     // S(i+1) once dV(i) has read P(i)
                     if (more) {
@@ -299,8 +311,8 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_kernel(const __grid_constant__ 
                     tc_fence_after();
 #pragma unroll
                     for (int k = 0; k < BQ / 16; ++k)
-                        mma_ts(tmem + S::TM_DK, tmem + S::TM_DP + packed_col(k), sdesc_sw128(qs + k * 2048, S::Q_CHUNK, 1024),
-                               IDESC_ACC, (i > 0 || k > 0) ? 1u : 0u);
+                        mma_ts(tmem + S::TM_DK, tmem + S::TM_DP + packed_col(k), sdesc_add(q_mn, (uint32_t)k * 2048u),
+                               IDESC_ACC, k > 0 ? 1u : acc0);
                     mma_commit(bar(S::B_DPFREE));
                     mma_commit(bar(S::B_QEMPTY + s));
                     // dQ contribution into TMEM buffer i % 2 (drained by the compute warps)
@@ -308,15 +320,14 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_kernel(const __grid_constant__ 
                         !mbar_wait(bar(S::B_DQFREE + s), (uint32_t)((i - 2) >> 1) & 1u, g, 0x216)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t dq_tmem = tmem + S::TM_DQ + 64u * (uint32_t)s;
-                    const uint32_t ds = base + S::OFF_DS;
 #pragma unroll
                     for (int k = 0; k < kTile / 16; ++k) {
+                        const uint64_t kk = sdesc_add(dK_mn, (uint32_t)k * 2048u);
+                        const uint64_t dd = sdesc_add(ddS_mn, (uint32_t)k * 2048u);
                         if (S::DQ_T)   // dQ^T = K^T dS^T: A = K^T (M = d), B = dS (N = queries)
-                            mma_ss(dq_tmem, sdesc_sw128(ks + k * 2048, S::KV_CHUNK, 1024),
-                                   sdesc_sw128(ds + k * 2048, 128 * 128, 1024), IDESC_DQ, k > 0 ? 1u : 0u);
+                            mma_ss(dq_tmem, kk, dd, IDESC_DQ, k > 0 ? 1u : 0u);
                         else           // dQ = dS K: A = dS (M = queries), B = K (N = d)
-                            mma_ss(dq_tmem, sdesc_sw128(ds + k * 2048, 128 * 128, 1024),
-                                   sdesc_sw128(ks + k * 2048, S::KV_CHUNK, 1024), IDESC_DQ, k > 0 ? 1u : 0u);
+                            mma_ss(dq_tmem, dd, kk, IDESC_DQ, k > 0 ? 1u : 0u);
                     }
                     mma_commit(bar(S::B_DQFULL + s));
                     // dP(i+1) once dK(i) has read dS(i)

@@ -31,8 +31,8 @@
 //     from TMEM (bf16, written over the first half of S_x).  The next tile's
 //     S_x is issued one key tile ahead, once P_x has been consumed;
 //   - warps 4-7 and 8-11: softmax of query tile 0 and 1, one row per thread
-//     (TMEM lane = row, warp w reads lane quadrant w % 4), with 216 registers
-//     each (setmaxnreg; warps 0-3 drop to 72).  The whole S row
+//     (TMEM lane = row, warp w reads lane quadrant w % 4), with 208 registers
+//     each (setmaxnreg; warps 0-3 drop to 88).  The whole S row
 //     is loaded with one wait, then max (3-input), 2^(x - m) with packed
 //     f32x2 FMA/add, bf16 pack, store back; then the rare O rescale and, at
 //     the end, the epilogue O / l -> bf16, LSE = (m + log2 l) * ln 2.
@@ -71,11 +71,11 @@ struct FwdShape {
     static constexpr uint32_t TM_O = 256;                // O_x at columns 256 + D x
     static constexpr int THREADS = 384;
     // register split: launched at 168 per thread (384 x 168 = 64,512);
-    // warpgroup 0 (producer, MMA, two idle warps) keeps 72, the two softmax
-    // warpgroups get 216: 128 x 72 + 256 x 216 = 64,512.
+    // warpgroup 0 (producer, MMA, two idle warps) keeps 88, the two softmax
+    // warpgroups get 208: 128 x 88 + 256 x 208 = 64,512.
     static constexpr int LAUNCH_REGS = 168;
-    static constexpr int REGS_CTRL = 72;
-    static constexpr int REGS_SOFTMAX = 216;
+    static constexpr int REGS_CTRL = 88;
+    static constexpr int REGS_SOFTMAX = 208;
     static_assert(128 * REGS_CTRL + 256 * REGS_SOFTMAX == THREADS * LAUNCH_REGS, "register split");
 };
 
@@ -118,6 +118,17 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
     const int kvis = key_visible_bound(p.key_len, b, p.N, &bad);
     if (bad && threadIdx.x == 0 && pq == 0 && (bh % p.H) == 0) record_status(g, kStatusBadKeyLen, 0);
 
+    // Without a block mask the key tiles query tile x sees are exactly
+    // [0, kend[x]): keys below key_len and, under the causal mask, not past
+    // its last row.  (tile_class below takes the same decision per tile.)
+    int kend[2];
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+        int lim = kvis;
+        if (p.causal) lim = min(lim, q0[x] + qn[x]);
+        kend[x] = qn[x] > 0 ? (lim + kTile - 1) / kTile : 0;
+    }
+    const int kend_union = max(kend[0], kend[1]);
     // class of key tile kt for query tile x of the pair
     auto cls = [&](int x, int kt) -> unsigned {
         if (qn[x] <= 0) return kTileSkip;
@@ -126,6 +137,10 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
     };
     // next key tile after kt seen by query tile x (x = 2: by either)
     auto next_tile = [&](int x, int kt) -> int {
+        if (!p.block_mask) {
+            const int lim = x == 2 ? kend_union : kend[x];
+            return kt + 1 < lim ? kt + 1 : p.Tk;
+        }
         for (int k = kt + 1; k < p.Tk; ++k) {
             const bool v0 = (x != 1) && cls(0, k) != kTileSkip;
             const bool v1 = (x != 0) && cls(1, k) != kTileSkip;
@@ -163,9 +178,9 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
     const uint32_t tmem = *tmem_slot;
 
     // Register split.  Warpgroup 0 gives registers back once, here, and
-    // keeps 72 to the end; the softmax warpgroups take them, here, and give
+    // keeps 88 to the end; the softmax warpgroups take them, here, and give
     // them back at the end of their branch, so the shared teardown below runs
-    // with 72 everywhere.  The only setmaxnreg.inc (which blocks until the
+    // with 88 everywhere.  The only setmaxnreg.inc (which blocks until the
     // pool holds enough) is the softmax one at the start, and the pool is
     // filled by warpgroup 0's unconditional dec: no inc ever waits on a warp
     // that is itself waiting.
@@ -221,14 +236,21 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                 int kt = next_tile(2, -1);
                 bool ok = true;
                 int nv[2] = {0, 0};      // key tiles processed so far by query tile x
+                // shared-memory descriptors built once; per MMA only the start
+                // address moves (K-major: 32 bytes per 16-wide K step inside a
+                // 128-byte row, then the next 64-column chunk; MN-major V: 16 rows)
+                const uint64_t dq0 = sdesc_sw128(base + S::OFF_Q, 16, 1024);
+                const uint64_t dk0 = sdesc_sw128(base + S::OFF_K, 16, 1024);
+                const uint64_t dv0 = sdesc_sw128(base + S::OFF_V, S::CHUNK_BYTES, 1024);
                 // S_x = Q_x K^T for the key tile in stage s (the x-th S buffer)
                 auto issue_s = [&](int x, int s) {
                     const uint32_t d_tmem = tmem + S::TM_S + 128u * (uint32_t)x;
-    #pragma unroll
+                    const uint64_t qd = sdesc_add(dq0, (uint32_t)(x * S::TILE_BYTES));
+                    const uint64_t kd = sdesc_add(dk0, (uint32_t)(s * S::TILE_BYTES));
+#pragma unroll
                     for (int k = 0; k < D / 16; ++k) {
-                        const uint32_t qa = base + S::OFF_Q + x * S::TILE_BYTES + (k >> 2) * S::CHUNK_BYTES + (k & 3) * 32;
-                        const uint32_t ka = base + S::OFF_K + s * S::TILE_BYTES + (k >> 2) * S::CHUNK_BYTES + (k & 3) * 32;
-                        mma_ss(d_tmem, sdesc_sw128(qa, 16, 1024), sdesc_sw128(ka, 16, 1024), IDESC_S, k > 0 ? 1u : 0u);
+                        const uint32_t off = (k >> 2) * S::CHUNK_BYTES + (k & 3) * 32;
+                        mma_ss(d_tmem, sdesc_add(qd, off), sdesc_add(kd, off), IDESC_S, k > 0 ? 1u : 0u);
                     }
                     mma_commit(bar(S::B_SFULL + x));
                 };
@@ -255,11 +277,12 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                             tc_fence_after();
                             const uint32_t p_tmem = tmem + S::TM_S + 128u * (uint32_t)x;
                             const uint32_t o_tmem = tmem + S::TM_O + (uint32_t)(D * x);
-                            const uint32_t voff = base + S::OFF_V + s * S::TILE_BYTES;
-    #pragma unroll
+                            const uint64_t vd = sdesc_add(dv0, (uint32_t)(s * S::TILE_BYTES));
+                            const uint32_t acc0 = nv[x] > 0 ? 1u : 0u;
+#pragma unroll
                             for (int k = 0; k < kTile / 16; ++k)
-                                mma_ts(o_tmem, p_tmem + (uint32_t)k * 8u, sdesc_sw128(voff + k * 2048, S::CHUNK_BYTES, 1024),
-                                       IDESC_PV, (nv[x] > 0 || k > 0) ? 1u : 0u);
+                                mma_ts(o_tmem, p_tmem + (uint32_t)k * 8u, sdesc_add(vd, (uint32_t)k * 2048u), IDESC_PV,
+                                       k > 0 ? 1u : acc0);
                             mma_commit(bar(S::B_PVDONE + x));
                             ++nv[x];
                         }
@@ -328,11 +351,21 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                         if (key >= kvis || (p.causal && key > q)) sr[j][t] = __float_as_uint(-INFINITY);
                     }
             }
-            float mx = -INFINITY;
+            // row maximum as eight independent 3-input chains, then a tree:
+            // one warp per sub-partition runs this, so the latency of a single
+            // 64-deep chain would sit on the critical path
+            float pm[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) pm[u] = -INFINITY;
 #pragma unroll
             for (int j = 0; j < 4; ++j)
 #pragma unroll
-                for (int t = 0; t < 32; t += 2) mx = fmax3(mx, __uint_as_float(sr[j][t]), __uint_as_float(sr[j][t + 1]));
+                for (int t = 0; t < 32; t += 4) {
+                    const int u = (j * 8 + t / 4) & 7;
+                    pm[u] = fmax3(pm[u], __uint_as_float(sr[j][t]), __uint_as_float(sr[j][t + 1]));
+                    pm[u] = fmax3(pm[u], __uint_as_float(sr[j][t + 2]), __uint_as_float(sr[j][t + 3]));
+                }
+            const float mx = fmaxf(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], fmax3(pm[5], pm[6], pm[7])));
             // move the reference maximum only when the row outgrew it by 2^8
             const float m_tile = mx * c2;
             const bool grow = m_tile > m_ref + kRescaleLog2;
@@ -345,8 +378,11 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                 m_ref = m_new;
             }
             const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-            // p = 2^(s * c - m), bf16 into the first 64 columns of S_x
-            float sum0 = 0.f, sum1 = 0.f;
+            // p = 2^(s * c - m), bf16 into the first 64 columns of S_x; the row
+            // sum in four independent packed accumulators
+            float ps[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) ps[u] = 0.f;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 uint32_t pk[16];
@@ -356,12 +392,13 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                     fma2(a, bb, __uint_as_float(sr[j][2 * t]), __uint_as_float(sr[j][2 * t + 1]), c2, c2, -m_use, -m_use);
                     a = ex2(a);
                     bb = ex2(bb);
-                    add2(sum0, sum1, a, bb);
+                    const int u = 2 * (t & 3);
+                    add2(ps[u], ps[u + 1], a, bb);
                     pk[t] = pack_bf16x2(a, bb);
                 }
                 tmem_st16(s_tmem + 16u * j, pk);
             }
-            l += sum0 + sum1;
+            l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
             tmem_st_wait();
             if (rescale && it > 0) {
                 // O_x may be rescaled only once the previous P_x V has landed

@@ -207,6 +207,10 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
            ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
+// The same descriptor with its start address moved by `bytes` (a multiple of
+// 16; shared addresses stay below 2^18, so the 14-bit field cannot carry).
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
+
 // 32 lanes x 32 columns of 32-bit words: thread t of warp w reads TMEM lane
 // 32*(w%4)+t, columns col..col+31 of taddr.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
