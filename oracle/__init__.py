@@ -57,6 +57,8 @@ def _load():
             lib.oracle_query_rows.argtypes = [dp, dp, dp, dp] + common + [i, lp, dp, dp, dp]
             lib.oracle_key_rows.argtypes = [dp, dp, dp, dp] + common + [i, lp, dp, dp]
             lib.oracle_tile_plan.argtypes = [i, i, i, ip, bp, i, i, i, bp]
+            lib.oracle_decode.argtypes = [dp, dp, dp, i, i, i, i, i, dbl, i, ip, dp, dp]
+            lib.oracle_decode.restype = ctypes.c_int
             lib.oracle_num_threads.argtypes = []
             for f in (lib.oracle_fwd, lib.oracle_bwd, lib.oracle_query_rows,
                       lib.oracle_key_rows, lib.oracle_tile_plan, lib.oracle_num_threads):
@@ -215,6 +217,31 @@ def tile_plan(B, N, causal=False, key_len=None, block_mask=None, mask_block=128,
     if rc != 0:
         raise RuntimeError("oracle_tile_plan failed: %d" % rc)
     return plan
+
+
+def attention_decode(Q, K, V, scale, causal=False, kv_len=None):
+    """O, LSE of Nq query rows against Nk cached keys (fp64).
+
+    Q: [B, H, Nq, d]; K, V: [B, H, Nk, d]; kv_len: int [B] or None.  With
+    causal, query i sees keys j <= kv_len[b] - Nq + i (the queries are the
+    last Nq positions)."""
+    lib = _load()
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    if Q.ndim != 4 or K.shape != V.shape or K.ndim != 4 or Q.shape[:2] != K.shape[:2] or Q.shape[3] != K.shape[3]:
+        raise ValueError("expected Q [B, H, Nq, d] and K, V [B, H, Nk, d]")
+    B, H, Nq, d = Q.shape
+    Nk = K.shape[2]
+    kl = None if kv_len is None else np.ascontiguousarray(np.asarray(kv_len, dtype=np.int32))
+    if kl is not None and kl.shape != (B,):
+        raise ValueError("kv_len must have shape [B]")
+    O = np.zeros((B, H, Nq, d), np.float64)
+    LSE = np.zeros((B, H, Nq), np.float64)
+    c = ctypes.c_double
+    rc = lib.oracle_decode(_ptr(Q, c), _ptr(K, c), _ptr(V, c), B, H, Nq, Nk, d, float(scale),
+                           int(bool(causal)), _ptr(kl, ctypes.c_int32), _ptr(O, c), _ptr(LSE, c))
+    if rc != 0:
+        raise RuntimeError("oracle_decode failed: %d" % rc)
+    return O, LSE
 
 
 from .online import merge_blocks, online_fold  # noqa: E402,F401

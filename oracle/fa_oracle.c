@@ -41,6 +41,15 @@
  *  - A query row with no visible key has O = 0, LSE = -inf, a zero P row and
  *    contributes no gradient (the pages are silent; this is the reading).
  *
+ * Decode shapes (oracle_decode): Nq query rows against Nk cached keys per
+ * (b, h).  Key j is visible to query i iff j < kv_len[b] (all Nk when kv_len
+ * is NULL) and, with the causal flag, j <= kv_len[b] - Nq + i: the queries
+ * are the last Nq positions of the sequence (bottom-right alignment; equal
+ * to the square causal mask when Nq = Nk = kv_len).  The pages describe the
+ * decode kernel only as the same IO-aware framing applied to one new token
+ * per step ("Attention" chapter, decoding paragraph); this is the plain
+ * definition of that step.
+ *
  * Layout: every tensor is contiguous [B, H, N, d] (d fastest); LSE is
  * [B, H, N]; P (optional) is [B, H, N, N].  All functions return 0 on
  * success and a negative number on a bad argument or allocation failure.
@@ -409,4 +418,43 @@ int oracle_tile_plan(int B, int N, int causal, const int32_t *key_len, const uin
                 plan[((int64_t)b * Tq + ti) * Tk + tj] = c;
             }
     return 0;
+}
+
+/*
+ * Decode: Q [B, H, Nq, d], K and V [B, H, Nk, d] -> O [B, H, Nq, d] and
+ * LSE [B, H, Nq].  Each query row: masked scores, three-pass safe softmax,
+ * O = P V, LSE = m + ln l.
+ */
+int oracle_decode(const double *Q, const double *K, const double *V, int B, int H, int Nq, int Nk,
+                  int d, double scale, int causal, const int32_t *kv_len, double *O, double *LSE)
+{
+    if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || d <= 0) return -1;
+    int err = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : err)
+    for (int64_t r = 0; r < (int64_t)B * H * Nq; r++) {
+        const int64_t bh = r / Nq;
+        const int i = (int)(r % Nq);
+        const int b = (int)(bh / H);
+        const int len = kv_len ? kv_len[b] : Nk;
+        double *s = (double *)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+        if (!s) { err |= 1; continue; }
+        const double *q = Q + r * d;
+        const double *Kh = K + bh * (int64_t)Nk * d, *Vh = V + bh * (int64_t)Nk * d;
+        for (int j = 0; j < Nk; j++) {
+            int vis = j < len;
+            if (causal && j > len - Nq + i) vis = 0;
+            if (!vis) { s[j] = -INFINITY; continue; }
+            double acc = 0.0;
+            for (int t = 0; t < d; t++) acc += q[t] * Kh[(int64_t)j * d + t];
+            s[j] = scale * acc;
+        }
+        LSE[r] = safe_softmax_row(s, Nk);
+        double *o = O + r * d;
+        for (int t = 0; t < d; t++) o[t] = 0.0;
+        for (int j = 0; j < Nk; j++)
+            if (s[j] != 0.0)
+                for (int t = 0; t < d; t++) o[t] += s[j] * Vh[(int64_t)j * d + t];
+        free(s);
+    }
+    return err ? -2 : 0;
 }

@@ -383,3 +383,56 @@ def test_tile_plan_block_mask_counts():
     assert int((plan[0] != 0).sum()) == 614
     assert int((plan[0] == 2).sum()) == 0               # N divisible by 128: no partial tiles
     assert np.array_equal(plan[0] != 0, bm.astype(bool))
+
+
+# ---------------------------------------------------------------- decode shapes
+
+def test_decode_equals_square_oracle_when_shapes_agree():
+    # Nq = Nk: key padding by kv_len is the square key_len mask, and the
+    # bottom-right causal alignment coincides with the top-left one
+    B, H, N, d = 2, 2, 24, 8
+    Q, K, V = rnd((B, H, N, d), 50), rnd((B, H, N, d), 51), rnd((B, H, N, d), 52)
+    O, L = oracle.attention_fwd(Q, K, V, 0.3, key_len=[24, 10])
+    Od, Ld = oracle.attention_decode(Q, K, V, 0.3, kv_len=[24, 10])
+    np.testing.assert_allclose(Od, O, atol=1e-12, rtol=0)
+    np.testing.assert_allclose(Ld, L, atol=1e-12, rtol=0)
+    O, L = oracle.attention_fwd(Q, K, V, 0.3, causal=True)
+    Od, Ld = oracle.attention_decode(Q, K, V, 0.3, causal=True)
+    np.testing.assert_allclose(Od, O, atol=1e-12, rtol=0)
+    np.testing.assert_allclose(Ld, L, atol=1e-12, rtol=0)
+
+
+def test_decode_matches_library_sdpa_with_explicit_mask():
+    B, H, Nq, Nk, d = 2, 3, 5, 37, 8
+    Q, K, V = rnd((B, H, Nq, d), 53), rnd((B, H, Nk, d), 54), rnd((B, H, Nk, d), 55)
+    kl = [37, 20]
+    for causal in (False, True):
+        O, L = oracle.attention_decode(Q, K, V, 0.4, causal=causal, kv_len=kl)
+        for b in range(B):
+            i = np.arange(Nq)[:, None]
+            j = np.arange(Nk)[None, :]
+            vis = j < kl[b]
+            if causal:
+                vis = vis & (j <= kl[b] - Nq + i)
+            m = torch.from_numpy(vis)
+            ref = torch.nn.functional.scaled_dot_product_attention(
+                torch.from_numpy(Q[b]), torch.from_numpy(K[b]), torch.from_numpy(V[b]), attn_mask=m, scale=0.4)
+            s = 0.4 * torch.from_numpy(Q[b]) @ torch.from_numpy(K[b]).transpose(-1, -2)
+            lref = torch.logsumexp(s.masked_fill(~m, -math.inf), dim=-1)
+            np.testing.assert_allclose(O[b], ref.numpy(), atol=1e-12, rtol=0)
+            np.testing.assert_allclose(L[b], lref.numpy(), atol=1e-12, rtol=0)
+
+
+def test_decode_split_keys_merge_to_the_whole():
+    # the split-KV decode reading: partial (O, LSE) over key ranges merge by
+    # the "Incremental Online Updates" rule into the full result
+    B, H, Nq, Nk, d = 1, 2, 3, 50, 8
+    Q, K, V = rnd((B, H, Nq, d), 56), rnd((B, H, Nk, d), 57, 2.0), rnd((B, H, Nk, d), 58)
+    O, L = oracle.attention_decode(Q, K, V, 0.5)
+    acc = None
+    for a, b in ((0, 7), (7, 30), (30, 50)):
+        Op, Lp = oracle.attention_decode(Q, K[:, :, a:b], V[:, :, a:b], 0.5)
+        st = (Lp, np.ones_like(Lp), Op)
+        acc = st if acc is None else merge_blocks(*acc, *st)
+    np.testing.assert_allclose(acc[2], O, atol=1e-12, rtol=0)
+    np.testing.assert_allclose(acc[0] + np.log(acc[1]), L, atol=1e-12, rtol=0)
