@@ -25,7 +25,10 @@ MUTANTS = {
     "softmax not normalised": ("for (int j = 0; j < N; j++) s[j] = exp(s[j] - m) / l;",
                                "for (int j = 0; j < N; j++) s[j] = exp(s[j] - m);"),
     "LSE drops the max": ("return m + log(l);", "return log(l);"),
-    "score without scale": ("s[j] = scale * acc;", "s[j] = acc;"),
+    "score without scale": ("        for (int t = 0; t < d; t++) acc += q[t] * k[t];\n        s[j] = scale * acc;",
+                            "        for (int t = 0; t < d; t++) acc += q[t] * k[t];\n        s[j] = acc;"),
+    "decode score without scale": ("acc += q[t] * Kh[(int64_t)j * d + t];\n            s[j] = scale * acc;",
+                                   "acc += q[t] * Kh[(int64_t)j * d + t];\n            s[j] = acc;"),
     "decode causal offset": ("if (causal && j > len - Nq + i) vis = 0;", "if (causal && j > len - Nq + i + 1) vis = 0;"),
     "decode kv_len off by one": ("int vis = j < len;", "int vis = j <= len;"),
     "D without dO": ("acc += dOh[(int64_t)i * d + t] * Oh[(int64_t)i * d + t];",
