@@ -126,6 +126,30 @@ fa_status fa_bwd_postprocess(void *dQ, int B, int H, int N, int d, float softmax
                              const void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Decode-time attention ("Attention" chapter of learn-kernels.com, decoding
+ * paragraph: the same IO-aware framing applied to the small, frequent
+ * product of a few new tokens against a growing key/value cache).
+ *   Q: device bf16 [B, H, Nq, d], the newest Nq tokens; K, V: device bf16
+ *   [B, H, Nk, d], the cache; O: device bf16 [B, H, Nq, d]; LSE: device fp32
+ *   [B, H, Nq] (natural log).  kv_len: NULL or device int32 [B], the valid
+ *   cache length of each batch (key j visible iff j < kv_len[b]; values
+ *   outside [0, Nk] are clamped and flagged).  causal != 0: the queries are
+ *   the last Nq positions, query i sees key j iff j <= kv_len[b] - Nq + i
+ *   (bottom-right alignment).  num_splits: how many CTAs share the key tiles
+ *   of one (query tile, b, h); <= 0 picks enough for two waves of the GPU
+ *   (at most 64).  Each split writes a normalised fp32 partial output and its
+ *   log-sum-exp into the workspace; a second kernel merges them with the
+ *   block-merge identity ("FlashAttention: Mathematical Foundations ...",
+ *   section "Incremental Online Updates").  Two kernel launches.
+ * fa_decode_workspace_size: bytes for the status word and the partials,
+ * for the same num_splits argument.
+ */
+size_t fa_decode_workspace_size(int B, int H, int Nq, int Nk, int d, int num_splits);
+fa_status fa_decode(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H,
+                    int Nq, int Nk, int d, float softmax_scale, int causal, const int32_t *kv_len,
+                    int num_splits, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * The tile-skipping decisions the kernels take, exported so that they can be
  * checked exactly.  plan: device uint8 [B][T][T], T = ceil(N / 128), written
  * with 0 = skip (every element of the 128 x 128 tile masked; the tile is

@@ -71,6 +71,10 @@ def lib():
             L.fa_bwd_postprocess.restype = i
             L.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp, vp]
             L.fa_bwd_noalloc.restype = i
+            L.fa_decode_workspace_size.argtypes = [i, i, i, i, i, i]
+            L.fa_decode_workspace_size.restype = sz
+            L.fa_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, i, vp, sz, vp]
+            L.fa_decode.restype = i
             L.fa_tile_plan.argtypes = [i, i, i, vp, vp, vp, vp, sz, vp]
             L.fa_tile_plan.restype = i
             L.fa_attention_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp,
@@ -87,7 +91,7 @@ def lib():
 
 
 EXPORTED = ("fa_tile_size", "fa_fwd_workspace_size", "fa_bwd_workspace_size", "fa_fwd", "fa_bwd",
-            "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_postprocess", "fa_bwd_noalloc", "fa_tile_plan", "fa_host_workspace_size", "fa_attention_host", "fa_get_device_status",
+            "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_postprocess", "fa_bwd_noalloc", "fa_decode_workspace_size", "fa_decode", "fa_tile_plan", "fa_host_workspace_size", "fa_attention_host", "fa_get_device_status",
             "fa_reset_device_status", "fa_status_string")
 
 
@@ -170,6 +174,17 @@ def fa_bwd_noalloc(Q, K, V, O, LSE, dO, dQ, dK, dV, B, H, N, d, softmax_scale, c
     return lib().fa_bwd_noalloc(_p(Q), _p(K), _p(V), _p(O), _p(LSE), _p(dO), _p(dQ), _p(dK), _p(dV), B,
                                 H, N, d, float(softmax_scale), int(bool(causal)), _p(key_len),
                                 _p(block_mask), _stream(stream))
+
+
+def fa_decode_workspace_size(B, H, Nq, Nk, d, num_splits=0) -> int:
+    return lib().fa_decode_workspace_size(B, H, Nq, Nk, d, int(num_splits))
+
+
+def fa_decode(Q, K, V, O, LSE, B, H, Nq, Nk, d, softmax_scale, causal, kv_len, num_splits, workspace,
+              workspace_bytes, stream=None) -> int:
+    return lib().fa_decode(_p(Q), _p(K), _p(V), _p(O), _p(LSE), B, H, Nq, Nk, d, float(softmax_scale),
+                           int(bool(causal)), _p(kv_len), int(num_splits), _p(workspace),
+                           int(workspace_bytes), _stream(stream))
 
 
 def fa_tile_plan(B, N, causal, key_len, block_mask, plan, workspace, workspace_bytes, stream=None) -> int:
@@ -259,3 +274,22 @@ def tile_plan(B, N, causal=False, key_len=None, block_mask=None, device="cuda", 
     _check(fa_tile_plan(B, N, causal, key_len, block_mask, plan, ws, ws.numel(), stream), "fa_tile_plan")
     _check(fa_get_device_status(ws, stream), "fa_tile_plan (device)")
     return plan
+
+
+def attention_decode(Q, K, V, softmax_scale=None, causal=False, kv_len=None, num_splits=0, ws=None,
+                     stream=None, check_status=False):
+    """O, LSE = fa_decode(...): Q [B, H, Nq, d] against the cache K, V [B, H, Nk, d]."""
+    import torch
+    B, H, Nq, d = _dims(Q)
+    Nk = int(K.shape[2])
+    scale = (1.0 / d ** 0.5) if softmax_scale is None else softmax_scale
+    O = torch.empty_like(Q)
+    LSE = torch.empty((B, H, Nq), dtype=torch.float32, device=Q.device)
+    need = fa_decode_workspace_size(B, H, Nq, Nk, d, num_splits)
+    if ws is None:
+        ws = workspace(need, Q.device)
+    _check(fa_decode(Q, K, V, O, LSE, B, H, Nq, Nk, d, scale, causal, kv_len, num_splits, ws, ws.numel(),
+                     stream), "fa_decode")
+    if check_status:
+        _check(fa_get_device_status(ws, stream), "fa_decode (device)")
+    return O, LSE

@@ -5,6 +5,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <climits>
 #include <cmath>
 #include <cstdint>
@@ -17,6 +18,7 @@
 namespace {
 
 using fa::BwdParams;
+using fa::DecParams;
 using fa::FwdParams;
 
 constexpr size_t kStatusBytes = 256;
@@ -262,6 +264,91 @@ fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, con
                      workspace_bytes, stream);
     if (st != FA_OK) return st;
     return fa_bwd_postprocess(dQ, B, H, N, d, softmax_scale, workspace, workspace_bytes, stream);
+}
+
+// ------------------------------------------------------------------ decode (split KV)
+namespace {
+constexpr int kDecodeMaxSplits = 64;
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        n <= 0)
+        return 148;
+    return n;
+}
+
+// splits actually used for a problem: the request (<= 0: enough CTAs for
+// two waves), at most one per key tile and at most kDecodeMaxSplits, then
+// tightened so that no split is empty.
+void decode_splits(int Tq, int BH, int Tk, int requested, int *splits, int *tiles_per_split) {
+    int sp = requested;
+    if (sp <= 0) {
+        const int64_t items = (int64_t)Tq * BH;
+        sp = (int)((2 * (int64_t)sm_count() + items - 1) / items);
+    }
+    sp = std::max(1, std::min(sp, std::min(std::max(Tk, 1), kDecodeMaxSplits)));
+    const int tps = (std::max(Tk, 1) + sp - 1) / sp;
+    *tiles_per_split = tps;
+    *splits = (std::max(Tk, 1) + tps - 1) / tps;
+}
+}  // namespace
+
+size_t fa_decode_workspace_size(int B, int H, int Nq, int Nk, int d, int num_splits) {
+    if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || d <= 0) return 0;
+    const int Tk = (Nk + 127) / 128;
+    const int sp = std::max(1, std::min(num_splits > 0 ? num_splits : kDecodeMaxSplits,
+                                        std::min(std::max(Tk, 1), kDecodeMaxSplits)));
+    const size_t rows = (size_t)B * H * Nq;
+    return kStatusBytes + round256((size_t)sp * rows * (size_t)d * 4) + round256((size_t)sp * rows * 4);
+}
+
+fa_status fa_decode(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H, int Nq, int Nk,
+                    int d, float softmax_scale, int causal, const int32_t *kv_len, int num_splits, void *workspace,
+                    size_t workspace_bytes, void *stream) {
+    if (B < 0 || H < 0 || Nq < 0 || Nk < 0) return FA_ERR_INVALID_ARGUMENT;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (!scale_ok(softmax_scale)) return FA_ERR_INVALID_ARGUMENT;
+    if ((int64_t)B * H * Nq == 0) return FA_OK;
+    const int64_t BH = (int64_t)B * H;
+    const int Tq = (Nq + 127) / 128, Tk = (Nk + 127) / 128;
+    if (BH > INT_MAX || BH * Tq * kDecodeMaxSplits > INT_MAX) return FA_ERR_UNSUPPORTED;
+    if ((int64_t)std::max(Nq, Nk) * d * 2 >= (int64_t(1) << 40)) return FA_ERR_UNSUPPORTED;
+    if (!Q || !O || !LSE || !aligned16(Q) || !aligned16(O) || !aligned16(LSE)) return FA_ERR_INVALID_ARGUMENT;
+    if (Nk > 0 && (!K || !V || !aligned16(K) || !aligned16(V))) return FA_ERR_INVALID_ARGUMENT;
+    if (!workspace || !aligned16(workspace) ||
+        workspace_bytes < fa_decode_workspace_size(B, H, Nq, Nk, d, num_splits))
+        return FA_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int splits = 0, tps = 0;
+    decode_splits(Tq, (int)BH, Tk, num_splits, &splits, &tps);
+    const int64_t rows = BH * Nq;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    float *Opart = reinterpret_cast<float *>(ws + kStatusBytes);
+    float *Lpart = reinterpret_cast<float *>(ws + kStatusBytes + round256((size_t)splits * rows * (size_t)d * 4));
+    if (Nk == 0)   // nothing visible anywhere: the merge of zero splits writes O = 0, LSE = -inf
+        return fa::launch_decode_merge(d, Opart, Lpart, O, LSE, rows, 0, s) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    DecParams p;
+    std::memset(&p, 0, sizeof(p));
+    if (!encode_bf16_3d(&p.tmQ, Q, d, Nq, (int)BH, 128) || !encode_bf16_3d(&p.tmK, K, d, Nk, (int)BH, 128) ||
+        !encode_bf16_3d(&p.tmV, V, d, Nk, (int)BH, 128))
+        return FA_ERR_CUDA;
+    p.Opart = Opart;
+    p.Lpart = Lpart;
+    p.kv_len = kv_len;
+    p.status = reinterpret_cast<unsigned *>(ws);
+    p.H = H;
+    p.Nq = Nq;
+    p.Nk = Nk;
+    p.BH = (int)BH;
+    p.Tq = Tq;
+    p.Tk = Tk;
+    p.splits = splits;
+    p.tiles_per_split = tps;
+    p.causal = causal ? 1 : 0;
+    p.scale_log2 = softmax_scale * kLog2e;
+    if (fa::launch_decode(d, p, s) != cudaSuccess) return FA_ERR_CUDA;
+    return fa::launch_decode_merge(d, Opart, Lpart, O, LSE, rows, splits, s) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 fa_status fa_tile_plan(int B, int N, int causal, const int32_t *key_len, const uint8_t *block_mask,

@@ -23,6 +23,11 @@ int bwd_query_block(int d);
 int bwd_dq_box_rows(int d);
 int bwd_smem_bytes(int d);
 
+// Decode: split-KV partials, then the merge.
+cudaError_t launch_decode(int d, const DecParams &p, cudaStream_t st);
+cudaError_t launch_decode_merge(int d, const float *Opart, const float *Lpart, void *O, float *LSE,
+                                int64_t rows, int splits, cudaStream_t st);
+
 // Plan export.
 cudaError_t launch_plan(int B, int N, int causal, const int32_t *key_len,
                         const uint8_t *block_mask, uint8_t *plan, unsigned *status,

@@ -29,6 +29,18 @@ __host__ __device__ __forceinline__ unsigned tile_class(int q0, int qn, int k0, 
     return full ? kTileFull : kTilePartial;
 }
 
+// tile_class for decode shapes: the queries are the last rows of the
+// sequence, so with the causal mask query i sees key j iff j <= i + shift
+// (shift = kv_len - Nq; 0 gives tile_class).
+__host__ __device__ __forceinline__ unsigned tile_class_shift(int q0, int qn, int k0, int kw, int kvis,
+                                                              int causal, int shift) {
+    const int q_last = q0 + qn - 1, k_last = k0 + kw - 1;
+    if (qn <= 0 || k0 >= kvis) return kTileSkip;
+    if (causal && k0 > q_last + shift) return kTileSkip;
+    const bool full = (k_last < kvis) && (!causal || k_last <= q0 + shift);
+    return full ? kTileFull : kTilePartial;
+}
+
 // Visible-key bound for batch b: min(N, key_len[b]) with key_len clamped to
 // [0, N]; out-of-range values are reported through *bad.
 __device__ __forceinline__ int key_visible_bound(const int32_t *key_len, int b, int N, bool *bad) {
@@ -51,6 +63,18 @@ struct FwdParams {
     int H, N, BH, Tq, Tk;
     int causal;
     float scale_log2;                // softmax_scale * log2(e)
+};
+
+struct DecParams {
+    CUtensorMap tmQ;                 // [BH][Nq][d] bf16, box {64, 128, 1}
+    CUtensorMap tmK, tmV;            // [BH][Nk][d] bf16, box {64, 128, 1}
+    float *Opart;                    // [splits][BH][Nq][d] fp32, each split's normalised output
+    float *Lpart;                    // [splits][BH][Nq] fp32, each split's log-sum-exp (-inf: none visible)
+    const int32_t *kv_len;           // device [B] or null
+    unsigned *status;
+    int H, Nq, Nk, BH, Tq, Tk, splits, tiles_per_split;
+    int causal;
+    float scale_log2;
 };
 
 struct BwdParams {

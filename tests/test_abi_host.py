@@ -97,3 +97,16 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(mod, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError):
         mod.lib()
+
+
+def test_decode_argument_errors(L):
+    dec = fa.lib().fa_decode
+    ws = fa.fa_decode_workspace_size(1, 1, 1, 1000, 128, 0)
+    assert ws > 256
+    assert dec(256, 256, 256, 256, 256, 1, 1, 1, 1000, 96, 0.1, 0, None, 0, 256, ws, None) == 2
+    assert dec(256, 256, 256, 256, 256, 1, 1, -1, 1000, 128, 0.1, 0, None, 0, 256, ws, None) == 1
+    assert dec(None, 256, 256, 256, 256, 1, 1, 1, 1000, 128, 0.1, 0, None, 0, 256, ws, None) == 1
+    assert dec(256, 256, 256, 256, 256, 1, 1, 1, 1000, 128, 0.1, 0, None, 0, 256, ws - 16, None) == 3
+    assert dec(256, 256, 256, 256, 256, 1, 1, 0, 1000, 128, 0.1, 0, None, 0, None, 0, None) == 0
+    # more splits requested than key tiles: the workspace query caps it the same way
+    assert fa.fa_decode_workspace_size(1, 1, 1, 1000, 128, 1000) == fa.fa_decode_workspace_size(1, 1, 1, 1000, 128, 8)
