@@ -15,7 +15,7 @@
 //
 // Kernel 1 (one CTA per (128-row query tile, b*h, split), 256 threads):
 //   warp 0  TMA: the query tile once, K and V tiles of the split through a
-//           2-stage ring;
+//           3-stage (d = 128) / 6-stage (d = 64) ring;
 //   warp 1  tcgen05: S = Q K^T into one of two TMEM buffers, O += P V with P
 //           read from TMEM;
 //   warps 4-7  softmax, one query row per thread, reference maximum moved
@@ -38,7 +38,7 @@ struct DecShape {
     static constexpr int CHUNKS = D / 64;
     static constexpr int CHUNK_BYTES = 128 * 128;
     static constexpr int TILE_BYTES = CHUNKS * CHUNK_BYTES;
-    static constexpr int STAGES = (D == 64) ? 4 : 2;
+    static constexpr int STAGES = (D == 64) ? 6 : 3;   // deep ring: the kernel streams K/V from HBM
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + TILE_BYTES;
     static constexpr int OFF_V = OFF_K + STAGES * TILE_BYTES;
@@ -240,7 +240,18 @@ __global__ void __launch_bounds__(256, 1) fa_decode_kernel(const __grid_constant
         float m_ref = -INFINITY, l = 0.f;
         int it = 0;
         bool ok = true;
+        // a warp whose 32 rows all lie past Nq has nothing to compute: its P
+        // rows only feed output rows that are never stored
+        const bool active = q0 + wq * 32 < p.Nq;
         for (int kt = first; kt < kt_end; kt = next_tile(kt), ++it) {
+            if (!active) {
+                if (!mbar_wait_warp(bar(S::B_SFULL + (it & 1)), (uint32_t)(it >> 1) & 1u, g, 0x521)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive(bar(S::B_PFULL + (it & 1)));
+                continue;
+            }
             const bool partial = cls(kt) == kTilePartial;
             const int k0 = kt * kTile;
             if (!mbar_wait_warp(bar(S::B_SFULL + (it & 1)), (uint32_t)(it >> 1) & 1u, g, 0x521)) {
@@ -329,7 +340,7 @@ __global__ void __launch_bounds__(256, 1) fa_decode_kernel(const __grid_constant
             ok = mbar_wait_warp(bar(S::B_PVDONE + ((it - 1) & 1)), (uint32_t)((it - 1) >> 1) & 1u, g, 0x523);
             tc_fence_after();
         }
-        if (ok) {
+        if (ok && active) {
             const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
             const size_t row = ((size_t)sp * p.BH + bh) * p.Nq + q;
 #pragma unroll 1
