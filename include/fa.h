@@ -136,8 +136,8 @@ fa_status fa_bwd_postprocess(void *dQ, int B, int H, int N, int d, float softmax
  *   outside [0, Nk] are clamped and flagged).  causal != 0: the queries are
  *   the last Nq positions, query i sees key j iff j <= kv_len[b] - Nq + i
  *   (bottom-right alignment).  num_splits: how many CTAs share the key tiles
- *   of one (query tile, b, h); <= 0 picks enough for two waves of the GPU
- *   (at most 64).  Each split writes a normalised fp32 partial output and its
+ *   of one (query tile, b, h); <= 0 picks the most that still fit the GPU's
+ *   SMs in one wave (at least 1, at most 64).  Each split writes a normalised fp32 partial output and its
  *   log-sum-exp into the workspace; a second kernel merges them with the
  *   block-merge identity ("FlashAttention: Mathematical Foundations ...",
  *   section "Incremental Online Updates").  Two kernel launches.

@@ -284,8 +284,11 @@ int sm_count() {
 void decode_splits(int Tq, int BH, int Tk, int requested, int *splits, int *tiles_per_split) {
     int sp = requested;
     if (sp <= 0) {
+        // one CTA fits on an SM (the K/V ring takes most of shared memory) and
+        // the kernel streams K/V from HBM: fill the SMs in one wave, never
+        // start a second, partly empty wave
         const int64_t items = (int64_t)Tq * BH;
-        sp = (int)((2 * (int64_t)sm_count() + items - 1) / items);
+        sp = (int)std::max<int64_t>(1, (int64_t)sm_count() / items);
     }
     sp = std::max(1, std::min(sp, std::min(std::max(Tk, 1), kDecodeMaxSplits)));
     const int tps = (std::max(Tk, 1) + sp - 1) / sp;
