@@ -15,6 +15,12 @@ collective); the time is the max over ranks.
 
 ``--impl reference`` times the fp64 CPU oracle instead, on a bounded sample
 of the same workload, on this machine's host cores.
+
+``--workload decode_...`` measures the split-KV decode path instead: one step
+= one ``fa_decode`` call (a few new query rows per sequence against a
+resident key/value cache); ``value`` is GB/s of algorithmic traffic (Q, the
+visible K and V rows read once, O and LSE written once) against the measured
+HBM copy bandwidth.
 """
 from __future__ import annotations
 
@@ -214,12 +220,206 @@ def oracle_sample(w, budget_s: float, n=None):
     return tf, oracle.num_threads(), desc
 
 
+# ---------------------------------------------------------------- decode
+def decode_bytes(w, kv_len):
+    """Algorithmic bytes of one decode step: Q read, the visible K and V rows
+    read once, O (bf16) and LSE (fp32) written once."""
+    from synthetic import decode_visible_keys
+    rows = w.B * w.H * w.Nq
+    return rows * w.d * 2 + 2 * decode_visible_keys(w, kv_len) * w.d * 2 + rows * w.d * 2 + rows * 4
+
+
+def _oracle_decode_case(w, B, H):
+    import dataclasses
+
+    import torch
+
+    from synthetic import make_decode_inputs
+    sub = dataclasses.replace(w, B=B, H=H)
+    c = make_decode_inputs(sub)
+    Q, K, V = (c[k].to(torch.float64).numpy() for k in ("Q", "K", "V"))
+    kl = None if c["kv_len"] is None else c["kv_len"].tolist()
+    return sub, Q, K, V, kl
+
+
+def oracle_decode_sample(w, budget_s: float, BH=None):
+    """Time the fp64 oracle decode on a bounded sample: the first B' batch
+    entries with H' heads (same recipe, a smaller draw), at most ~2 GB of
+    fp64 cache, called repeatedly for about budget_s.  Returns (GB/s of
+    bf16-equivalent algorithmic bytes, cores, description, (B', H'))."""
+    import oracle
+    if BH is None:
+        per_head = 2 * w.Nk * w.d * 8
+        H = max(1, min(w.H, (2 << 30) // per_head))
+        B = max(1, min(w.B, (2 << 30) // (per_head * H)))
+    else:
+        B, H = BH
+    sub, Q, K, V, kl = _oracle_decode_case(w, B, H)
+    dts = []
+    t_end = time.perf_counter() + budget_s
+    while not dts or time.perf_counter() < t_end:
+        t0 = time.perf_counter()
+        oracle.attention_decode(Q, K, V, w.softmax_scale, causal=w.causal, kv_len=kl)
+        dts.append(time.perf_counter() - t0)
+    dt = sum(dts) / len(dts)
+    what = ("the whole of %s" % w.name if (B, H) == (w.B, w.H) else
+            "the first %d batch entr%s x %d head(s) of %s (same recipe, smaller draw)"
+            % (B, "y" if B == 1 else "ies", H, w.name))
+    desc = "fp64 oracle decode of %s, %d calls, %.3f s per call" % (what, len(dts), dt)
+    return decode_bytes(sub, kl) / dt / 1e9, oracle.num_threads(), desc, (B, H)
+
+
+def run_decode(args, w):
+    import torch
+
+    ws_n, rank = init_dist("nccl")
+    _, _, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import io_aware_exact_09_gb300 as fa
+    from synthetic import make_decode_inputs
+    fa.build()
+    B, H, Nq, Nk, d = w.B, w.H, w.Nq, w.Nk, w.d
+    case = make_decode_inputs(w)
+    Q, K, V = (case[k].to(dev).contiguous() for k in ("Q", "K", "V"))
+    kl = None if case["kv_len"] is None else case["kv_len"].to(dev)
+    kl_list = None if case["kv_len"] is None else case["kv_len"].tolist()
+    O = torch.empty_like(Q)
+    LSE = torch.empty((B, H, Nq), dtype=torch.float32, device=dev)
+    wsn = fa.fa_decode_workspace_size(B, H, Nq, Nk, d, 0)
+    ws = fa.workspace(wsn, dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    nbytes = decode_bytes(w, kl_list)
+
+    def check(st, where):
+        if st != 0:
+            raise RuntimeError("%s failed: %s" % (where, fa.fa_status_string(st)))
+
+    def step():
+        check(fa.fa_decode(Q, K, V, O, LSE, B, H, Nq, Nk, d, w.softmax_scale, w.causal, kl, 0, ws, wsn, sp),
+              "fa_decode")
+
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)     # 256 MiB > 129 MB L2
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    check(fa.fa_get_device_status(ws, sp), "device status after warm-up")
+
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    # one timed step is ~0.1-0.4 ms: repeat it so the clock sampler sees load
+    reps = max(1, int(args.decode_reps))
+    times = []
+    barrier()
+    torch.cuda.synchronize(dev)
+    launches = 0
+    for _ in range(args.steps):
+        for _ in range(reps):
+            flush.zero_()
+            e0.record(stream)
+            step()
+            e1.record(stream)
+            e1.synchronize()
+            times.append(e0.elapsed_time(e1))
+            launches += 2
+    torch.cuda.synchronize(dev)
+    barrier()
+    clk = clocks.stop()
+    check(fa.fa_get_device_status(ws, sp), "device status after timing")
+    ms = reduce_max(sum(times) / len(times), dev)
+    value = nbytes * ws_n / (ms / 1e3) / 1e9
+
+    peaks, peak_src = measured_peaks()
+    peak = float(peaks.get("hbm_gbs"))
+    achieved = nbytes / (ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "kernel": "fa_decode_kernel + fa_decode_merge_kernel (one fa_decode call)",
+                "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": None, "peak_source": "%s hbm_gbs" % peak_src}
+
+    e2e = None
+    if not args.no_e2e:
+        # the cache stays resident (it is the decode state); each step copies
+        # the new queries in and the outputs out through pinned host memory
+        Qh = case["Q"].contiguous().pin_memory()
+        Oh = torch.empty_like(Qh).pin_memory()
+        Lh = torch.empty((B, H, Nq), dtype=torch.float32).pin_memory()
+        Qd = torch.empty_like(Q)
+        et = []
+        for i in range(1 + max(3, min(args.steps, 10))):
+            flush.zero_()
+            e0.record(stream)
+            Qd.copy_(Qh, non_blocking=True)
+            check(fa.fa_decode(Qd, K, V, O, LSE, B, H, Nq, Nk, d, w.softmax_scale, w.causal, kl, 0, ws, wsn, sp),
+                  "fa_decode")
+            Oh.copy_(O, non_blocking=True)
+            Lh.copy_(LSE, non_blocking=True)
+            e1.record(stream)
+            e1.synchronize()
+            if i > 0:
+                et.append(e0.elapsed_time(e1))
+        e_ms = reduce_max(sum(et) / len(et), dev)
+        e2e = {"value": nbytes * ws_n / (e_ms / 1e3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": Qh.numel() * 2, "d2h_bytes_per_step": Oh.numel() * 2 + Lh.numel() * 4,
+               "ms_per_step": e_ms, "note": "key/value cache resident in HBM"}
+
+    cpu = None
+    if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
+        gbs, cores, desc, _ = oracle_decode_sample(w, args.cpu_budget)
+        cpu = {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": desc}
+
+    if rank == 0:
+        line = {
+            "metric": "decode attention GB/s (bf16 K/V cache)", "value": value, "unit": "GB/s", "n_gpus": ws_n,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "B": B, "H": H, "Nq": Nq, "Nk": Nk, "d": d, "causal": w.causal,
+                       "ragged_cache": kl is not None, "splits": "auto",
+                       "parallelism": "replicas" if ws_n > 1 else "single",
+                       "l2": "flushed between steps (cache larger than L2 too)",
+                       "timed_calls": len(times)},
+            "algorithmic_bytes_per_step": nbytes,
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
+            "gpu_launches": launches,
+        }
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 # ---------------------------------------------------------------- reference arm
+def run_reference_decode(args, w):
+    import oracle
+    oracle.build()
+    vals = []
+    desc = cores = None
+    _, _, _, BH = oracle_decode_sample(w, 0.0)
+    for i in range(args.warmup + args.steps):
+        gbs, cores, desc, _ = oracle_decode_sample(w, 3.0, BH)
+        if i >= args.warmup:
+            vals.append(gbs)
+    v = statistics.median(vals)
+    line = {"impl": "reference", "metric": "decode attention GB/s (bf16 K/V cache)", "value": v, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d,
+                       "causal": w.causal},
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": desc},
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_reference(args):
     ws, rank = init_dist("gloo")
     if rank != 0:
         return 0
-    from synthetic import WORKLOADS
+    from synthetic import DECODE_WORKLOADS, WORKLOADS
+    if args.workload in DECODE_WORKLOADS:
+        return run_reference_decode(args, DECODE_WORKLOADS[args.workload])
     import oracle
     oracle.build()
     w = WORKLOADS[args.workload]
@@ -414,11 +614,16 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--decode-reps", type=int, default=20,
+                    help="decode workloads: timed calls per step (each one is well under a millisecond)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    from synthetic import DECODE_WORKLOADS
+    if args.workload in DECODE_WORKLOADS:
+        return run_decode(args, DECODE_WORKLOADS[args.workload])
     return run_ours(args)
 
 

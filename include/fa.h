@@ -137,10 +137,12 @@ fa_status fa_bwd_postprocess(void *dQ, int B, int H, int N, int d, float softmax
  *   the last Nq positions, query i sees key j iff j <= kv_len[b] - Nq + i
  *   (bottom-right alignment).  num_splits: how many CTAs share the key tiles
  *   of one (query tile, b, h); <= 0 picks the most that still fit the GPU's
- *   SMs in one wave (at least 1, at most 64).  Each split writes a normalised fp32 partial output and its
+ *   SMs in one wave, or about three waves when kv_len is given (at least
+ *   1, at most 64).  Each split writes a normalised fp32 partial output and its
  *   log-sum-exp into the workspace; a second kernel merges them with the
  *   block-merge identity ("FlashAttention: Mathematical Foundations ...",
- *   section "Incremental Online Updates").  Two kernel launches.
+ *   section "Incremental Online Updates").  Two kernel launches; with a
+ *   single split, one (it writes O and LSE itself).
  * fa_decode_workspace_size: bytes for the status word and the partials,
  * for the same num_splits argument.
  */

@@ -281,14 +281,18 @@ int sm_count() {
 // splits actually used for a problem: the request (<= 0: enough CTAs for
 // two waves), at most one per key tile and at most kDecodeMaxSplits, then
 // tightened so that no split is empty.
-void decode_splits(int Tq, int BH, int Tk, int requested, int *splits, int *tiles_per_split) {
+void decode_splits(int Tq, int BH, int Tk, bool ragged, int requested, int *splits, int *tiles_per_split) {
     int sp = requested;
     if (sp <= 0) {
         // one CTA fits on an SM (the K/V ring takes most of shared memory) and
-        // the kernel streams K/V from HBM: fill the SMs in one wave, never
-        // start a second, partly empty wave
+        // the kernel streams K/V from HBM: with equal cache lengths fill the
+        // SMs in one wave and never start a second, partly empty one; with
+        // per-batch lengths the longest cache would set the time of a single
+        // wave, so cut the work into about three waves of shorter pieces
+        // (pieces past a batch's length end at once) and let the block
+        // scheduler balance them
         const int64_t items = (int64_t)Tq * BH;
-        sp = (int)std::max<int64_t>(1, (int64_t)sm_count() / items);
+        sp = (int)std::max<int64_t>(1, (ragged ? 3 : 1) * (int64_t)sm_count() / items);
     }
     sp = std::max(1, std::min(sp, std::min(std::max(Tk, 1), kDecodeMaxSplits)));
     const int tps = (std::max(Tk, 1) + sp - 1) / sp;
@@ -324,7 +328,7 @@ fa_status fa_decode(const void *Q, const void *K, const void *V, void *O, float 
         return FA_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     int splits = 0, tps = 0;
-    decode_splits(Tq, (int)BH, Tk, num_splits, &splits, &tps);
+    decode_splits(Tq, (int)BH, Tk, kv_len != nullptr, num_splits, &splits, &tps);
     const int64_t rows = BH * Nq;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     float *Opart = reinterpret_cast<float *>(ws + kStatusBytes);
@@ -338,6 +342,10 @@ fa_status fa_decode(const void *Q, const void *K, const void *V, void *O, float 
         return FA_ERR_CUDA;
     p.Opart = Opart;
     p.Lpart = Lpart;
+    if (splits == 1) {   // the single split is the whole answer: written directly, no merge launch
+        p.O = O;
+        p.LSE = LSE;
+    }
     p.kv_len = kv_len;
     p.status = reinterpret_cast<unsigned *>(ws);
     p.H = H;
@@ -351,6 +359,7 @@ fa_status fa_decode(const void *Q, const void *K, const void *V, void *O, float 
     p.causal = causal ? 1 : 0;
     p.scale_log2 = softmax_scale * kLog2e;
     if (fa::launch_decode(d, p, s) != cudaSuccess) return FA_ERR_CUDA;
+    if (splits == 1) return FA_OK;
     return fa::launch_decode_merge(d, Opart, Lpart, O, LSE, rows, splits, s) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -20,7 +20,8 @@
 //           read from TMEM;
 //   warps 4-7  softmax, one query row per thread, reference maximum moved
 //           only when a row outgrows it by 2^8; epilogue O / l (fp32) and
-//           L_s = (m + log2 l) ln 2.
+//           L_s = (m + log2 l) ln 2 -- or, when there is one split, the final
+//           bf16 O and LSE, and kernel 2 is not launched.
 // It is HBM-bound (each K/V element is read once); query rows past Nq are
 // zero-filled by TMA and never stored.
 // Kernel 2: one warp per (b, h, query row) merges the splits, O -> bf16.
@@ -336,6 +337,7 @@ __global__ void __launch_bounds__(256, 1) fa_decode_kernel(const __grid_constant
             mbar_arrive(bar(S::B_PFULL + (it & 1)));
         }
         // ---------------------------------------------------------- epilogue: this split's partial
+        // (or, with a single split, the final bf16 output and LSE)
         if (ok && it > 0) {
             ok = mbar_wait_warp(bar(S::B_PVDONE + ((it - 1) & 1)), (uint32_t)((it - 1) >> 1) & 1u, g, 0x523);
             tc_fence_after();
@@ -353,7 +355,15 @@ __global__ void __launch_bounds__(256, 1) fa_decode_kernel(const __grid_constant
 #pragma unroll
                     for (int t = 0; t < 32; ++t) o[t] = 0u;
                 }
-                if (r < qn) {
+                if (r < qn && p.O) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.O) + row * D + 32 * j);
+#pragma unroll
+                    for (int t = 0; t < 4; ++t)
+                        dst[t] = make_uint4(pack_bf16x2(__uint_as_float(o[8 * t]) * inv_l, __uint_as_float(o[8 * t + 1]) * inv_l),
+                                            pack_bf16x2(__uint_as_float(o[8 * t + 2]) * inv_l, __uint_as_float(o[8 * t + 3]) * inv_l),
+                                            pack_bf16x2(__uint_as_float(o[8 * t + 4]) * inv_l, __uint_as_float(o[8 * t + 5]) * inv_l),
+                                            pack_bf16x2(__uint_as_float(o[8 * t + 6]) * inv_l, __uint_as_float(o[8 * t + 7]) * inv_l));
+                } else if (r < qn) {
                     float4 *dst = reinterpret_cast<float4 *>(p.Opart + row * D + 32 * j);
 #pragma unroll
                     for (int t = 0; t < 8; ++t)
@@ -361,7 +371,7 @@ __global__ void __launch_bounds__(256, 1) fa_decode_kernel(const __grid_constant
                                              __uint_as_float(o[4 * t + 2]) * inv_l, __uint_as_float(o[4 * t + 3]) * inv_l);
                 }
             }
-            if (r < qn) p.Lpart[row] = (l > 0.f) ? (m_ref + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+            if (r < qn) (p.LSE ? p.LSE : p.Lpart)[row] = (l > 0.f) ? (m_ref + log2f(l)) * 0.69314718055994530942f : -INFINITY;
         }
     }
 

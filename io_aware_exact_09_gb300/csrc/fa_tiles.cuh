@@ -70,6 +70,8 @@ struct DecParams {
     CUtensorMap tmK, tmV;            // [BH][Nk][d] bf16, box {64, 128, 1}
     float *Opart;                    // [splits][BH][Nq][d] fp32, each split's normalised output
     float *Lpart;                    // [splits][BH][Nq] fp32, each split's log-sum-exp (-inf: none visible)
+    void *O;                         // with one split: bf16 [BH][Nq][d] written directly (no merge), else null
+    float *LSE;                      // with one split: fp32 [BH][Nq] natural-log LSE, else null
     const int32_t *kv_len;           // device [B] or null
     unsigned *status;
     int H, Nq, Nk, BH, Tq, Tk, splits, tiles_per_split;

@@ -66,6 +66,63 @@ WORKLOADS = {
 }
 
 
+@dataclass(frozen=True)
+class DecodeWorkload:
+    """Nq new query rows per (b, h) against a key/value cache of Nk rows."""
+    name: str
+    B: int
+    H: int
+    Nq: int
+    Nk: int
+    d: int
+    seed: int
+    causal: bool = False
+    kv_len_range: Optional[tuple] = None       # inclusive (lo, hi) or None (full caches)
+    description: str = ""
+
+    @property
+    def softmax_scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+
+# Decode shapes (the pages give none): one new token per sequence against a
+# 32K cache with 32 heads of d=128, and a speculative-decoding-like step
+# (4 new tokens, causal) over ragged caches of up to 16K with d=64.
+DECODE_WORKLOADS = {
+    "decode_b4h32q1k32768d128": DecodeWorkload("decode_b4h32q1k32768d128", 4, 32, 1, 32768, 128, 1005,
+                                               description="B4 H32, 1 new token, full 32K caches, d=128"),
+    "decode_ragged_b16h8q4k16384d64": DecodeWorkload("decode_ragged_b16h8q4k16384d64", 16, 8, 4, 16384, 64,
+                                                     1006, causal=True, kv_len_range=(1024, 16384),
+                                                     description="B16 H8, 4 new tokens (causal), "
+                                                                 "cache lengths U[1024, 16384], d=64"),
+}
+
+
+def make_decode_inputs(w: DecodeWorkload, B=None, H=None):
+    """Q [B, H, Nq, d], K, V [B, H, Nk, d] (bf16 from fp32 N(0, 1), drawn in
+    that order) and kv_len (int32 [B] or None) from the workload's seed.
+    B and H may be lowered to draw a smaller case with the same recipe and
+    seed (a bounded CPU sample); its values are not a slice of the full draw."""
+    B = w.B if B is None else B
+    H = w.H if H is None else H
+    gen = torch.Generator().manual_seed(w.seed)
+    Q = to_bf16(torch.randn((B, H, w.Nq, w.d), generator=gen, dtype=torch.float32))
+    K = to_bf16(torch.randn((B, H, w.Nk, w.d), generator=gen, dtype=torch.float32))
+    V = to_bf16(torch.randn((B, H, w.Nk, w.d), generator=gen, dtype=torch.float32))
+    kv_len = None
+    if w.kv_len_range is not None:
+        kv_len = draw_key_len(B, w.kv_len_range[0], w.kv_len_range[1], gen)
+    return {"Q": Q, "K": K, "V": V, "kv_len": kv_len, "causal": w.causal, "scale": w.softmax_scale}
+
+
+def decode_visible_keys(w: DecodeWorkload, kv_len=None) -> int:
+    """Number of (b, h, key) cache rows a decode step must read: every row
+    below the batch's cache length (all Nk when there are no lengths)."""
+    if kv_len is None:
+        return w.B * w.H * w.Nk
+    return w.H * sum(min(max(int(x), 0), w.Nk) for x in kv_len)
+
+
 def to_bf16(x: torch.Tensor) -> torch.Tensor:
     """fp32 -> bf16 with round-to-nearest-even (torch's conversion)."""
     return x.to(torch.bfloat16)

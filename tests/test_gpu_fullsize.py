@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import oracle
-from synthetic import WORKLOADS, make_inputs
+from synthetic import DECODE_WORKLOADS, WORKLOADS, make_decode_inputs, make_inputs
 from gpu_common import GRAD_REL_FRO, LSE_MAX_ABS, O_MAX_ABS, O_REL_FRO, f64, oracle_args, rel_fro, run_cuda
 
 pytestmark = pytest.mark.gpu
@@ -115,3 +115,28 @@ def test_host_buffer_path_matches_device_path():
     assert np.array_equal(dV.double().numpy(), dev["dV"])
     # dQ goes through fp32 atomics whose order varies: compare within tolerance
     assert rel_fro(dQ.double().numpy(), dev["dQ"]) < 1e-3
+
+
+@pytest.mark.parametrize("name", sorted(DECODE_WORKLOADS))
+def test_decode_full_size_sampled(name):
+    """Decode workloads at full size with the split count bench.py uses
+    (automatic): sampled (b, h) pairs against the fp64 decode oracle."""
+    import io_aware_exact_09_gb300 as fa
+    w = DECODE_WORKLOADS[name]
+    c = make_decode_inputs(w)
+    kl = None if c["kv_len"] is None else c["kv_len"].cuda()
+    O, L = fa.attention_decode(c["Q"].cuda(), c["K"].cuda(), c["V"].cuda(), w.softmax_scale, w.causal, kl, 0,
+                               check_status=True)
+    torch.cuda.synchronize()
+    O, L = O.double().cpu().numpy(), L.double().cpu().numpy()
+    rng = np.random.default_rng(w.seed)
+    picks = [(0, 0), (w.B - 1, w.H - 1)] + [(int(rng.integers(w.B)), int(rng.integers(w.H))) for _ in range(4)]
+    for b, h in picks:
+        sl = lambda t: t[b:b + 1, h:h + 1].double().numpy()
+        kvb = None if c["kv_len"] is None else [int(c["kv_len"][b])]
+        rO, rL = oracle.attention_decode(sl(c["Q"]), sl(c["K"]), sl(c["V"]), w.softmax_scale, causal=w.causal,
+                                         kv_len=kvb)
+        o, l = O[b:b + 1, h:h + 1], L[b:b + 1, h:h + 1]
+        assert rel_fro(o, rO) <= O_REL_FRO, (name, b, h, rel_fro(o, rO))
+        assert np.max(np.abs(o - rO)) <= O_MAX_ABS, (name, b, h)
+        assert np.max(np.abs(l - rL)) <= LSE_MAX_ABS, (name, b, h)
