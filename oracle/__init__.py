@@ -59,6 +59,13 @@ def _load():
             lib.oracle_tile_plan.argtypes = [i, i, i, ip, bp, i, i, i, bp]
             lib.oracle_decode.argtypes = [dp, dp, dp, i, i, i, i, i, dbl, i, ip, dp, dp]
             lib.oracle_decode.restype = ctypes.c_int
+            lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+            lib.oracle_e4m3_encode.restype = ctypes.c_ubyte
+            lib.oracle_e4m3_decode.argtypes = [ctypes.c_ubyte]
+            lib.oracle_e4m3_decode.restype = ctypes.c_double
+            fp = ctypes.POINTER(ctypes.c_float)
+            lib.oracle_quantize_fp8.argtypes = [fp, i, i, i, i, bp, fp]
+            lib.oracle_quantize_fp8.restype = ctypes.c_int
             lib.oracle_num_threads.argtypes = []
             for f in (lib.oracle_fwd, lib.oracle_bwd, lib.oracle_query_rows,
                       lib.oracle_key_rows, lib.oracle_tile_plan, lib.oracle_num_threads):
@@ -242,6 +249,59 @@ def attention_decode(Q, K, V, scale, causal=False, kv_len=None):
     if rc != 0:
         raise RuntimeError("oracle_decode failed: %d" % rc)
     return O, LSE
+
+
+E4M3_MAX = 448.0
+FP8_BLOCK = 128
+
+
+def e4m3_encode(x):
+    """e4m3 codes (uint8) of fp32 values: nearest, ties to even, saturating."""
+    lib = _load()
+    x = np.asarray(x, dtype=np.float32)
+    out = np.empty(x.shape, np.uint8)
+    flat, of = x.reshape(-1), out.reshape(-1)
+    for k in range(flat.size):
+        of[k] = lib.oracle_e4m3_encode(float(flat[k]))
+    return out
+
+
+def e4m3_table():
+    """fp64 value of each of the 256 e4m3 codes (NaN for the two NaN codes)."""
+    lib = _load()
+    return np.array([lib.oracle_e4m3_decode(c) for c in range(256)], np.float64)
+
+
+def quantize_fp8(X, transpose=False):
+    """Block quantisation of X [B, H, N, d] (bf16 values as fp32/fp64):
+    codes uint8 [B, H, N, d] (with transpose: [B, H, d, Np], Np = ceil(N/16)*16)
+    and scales fp32 [B, H, ceil(N/128)]."""
+    lib = _load()
+    X = np.ascontiguousarray(np.asarray(X, dtype=np.float32))
+    if X.ndim != 4:
+        raise ValueError("expected X [B, H, N, d]")
+    B, H, N, d = X.shape
+    T = (N + FP8_BLOCK - 1) // FP8_BLOCK
+    Np = (N + 15) // 16 * 16
+    codes = np.zeros((B, H, d, Np) if transpose else (B, H, N, d), np.uint8)
+    scales = np.zeros((B, H, T), np.float32)
+    fp = ctypes.POINTER(ctypes.c_float)
+    rc = lib.oracle_quantize_fp8(X.ctypes.data_as(fp), B * H, N, d, int(bool(transpose)),
+                                 codes.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)), scales.ctypes.data_as(fp))
+    if rc != 0:
+        raise RuntimeError("oracle_quantize_fp8 failed: %d" % rc)
+    return codes, scales
+
+
+def dequantize_fp8(codes, scales, N, transpose=False):
+    """fp64 [B, H, N, d] values the codes stand for: e4m3(code) * scale of the
+    code's 128-row block."""
+    codes = np.asarray(codes)
+    vals = e4m3_table()[codes]
+    if transpose:
+        vals = np.swapaxes(vals, 2, 3)[:, :, :N, :]
+    rows = np.arange(N) // FP8_BLOCK
+    return vals * np.asarray(scales, np.float64)[:, :, rows][..., None]
 
 
 from .online import merge_blocks, online_fold  # noqa: E402,F401

@@ -458,3 +458,104 @@ int oracle_decode(const double *Q, const double *K, const double *V, int B, int 
     }
     return err ? -2 : 0;
 }
+
+/*
+ * FP8 block quantisation.  "FlashAttention: Mathematical Foundations ...",
+ * section "Architectural Evolution" (FlashAttention-3 paragraph): the FP8
+ * matmuls are block-quantised with dynamic scaling; "Attention" chapter
+ * (learn-kernels.com), FlashAttention-3 paragraph: block quantisation on the
+ * hardware FP8 format.  The pages fix no format details.  Readings:
+ *   - element format e4m3 without infinities: 1 sign bit, 4 exponent bits
+ *     with bias 7, 3 mantissa bits; exponent field 0 holds the subnormals
+ *     m/8 * 2^-6; the largest finite magnitude is 1.75 * 2^8 = 448 and the
+ *     pattern S.1111.111 is NaN.  Conversion rounds to nearest, ties to
+ *     even, keeps the sign of values that round to zero and saturates
+ *     magnitudes above 448 to 448;
+ *   - a block is 128 consecutive rows (tokens) x all d columns of one
+ *     (b, h); "dynamic" scaling takes its scale from the data: amax / 448 in
+ *     fp32 (1 for an all-zero block);
+ *   - code = e4m3(x / scale), the division in fp32; the codes stand for the
+ *     values code * scale.
+ */
+unsigned char oracle_e4m3_encode(float xf)
+{
+    if (isnan(xf)) return 0x7F;
+    const unsigned char sign = signbit(xf) ? 0x80 : 0x00;
+    double a = fabs((double)xf);
+    if (a == 0.0) return sign;
+    if (isinf(a)) return sign | 0x7E;
+    /* binade of a: a = f * 2^E, f in [0.5, 1), so 2^(E-1) <= a < 2^E;
+     * below 2^-6 every value shares the subnormal spacing 2^-9 */
+    int E;
+    frexp(a, &E);
+    int e = E - 1;
+    if (e < -6) e = -6;
+    const double ulp = ldexp(1.0, e - 3);          /* 3 mantissa bits */
+    const double q = a / ulp;                       /* exact: ulp is a power of two */
+    double r = floor(q);
+    const double frac = q - r;
+    if (frac > 0.5 || (frac == 0.5 && fmod(r, 2.0) != 0.0)) r += 1.0;
+    double v = r * ulp;
+    if (v > 448.0) v = 448.0;
+    if (v == 0.0) return sign;
+    /* encode the representable magnitude v */
+    int E2;
+    frexp(v, &E2);
+    const int field = (E2 - 1) + 7;
+    unsigned mag;
+    if (field <= 0) {
+        mag = (unsigned)(v / ldexp(1.0, -9));       /* subnormal: m * 2^-9 */
+    } else {
+        const double m = (v / ldexp(1.0, E2 - 1) - 1.0) * 8.0;
+        mag = ((unsigned)field << 3) | (unsigned)m;
+    }
+    return (unsigned char)(sign | mag);
+}
+
+double oracle_e4m3_decode(unsigned char c)
+{
+    const int field = (c >> 3) & 0xF, m = c & 7;
+    if (field == 15 && m == 7) return NAN;
+    const double mag = field == 0 ? ldexp((double)m, -9) : ldexp(1.0 + m / 8.0, field - 7);
+    return (c & 0x80) ? -mag : mag;
+}
+
+/*
+ * X: fp32 [BH][N][d] (the bf16 inputs, exactly).  Writes the codes to
+ * codes ([BH][N][d], or with transpose [BH][d][Np], Np = ceil(N / 16) * 16,
+ * code 0 in the columns N..Np-1) and one scale per (bh, 128-row block) to
+ * scales [BH][ceil(N / 128)].
+ */
+int oracle_quantize_fp8(const float *X, int BH, int N, int d, int transpose, unsigned char *codes,
+                        float *scales)
+{
+    if (BH < 0 || N < 0 || d <= 0) return -1;
+    const int T = (N + 127) / 128;
+    const int Np = (N + 15) / 16 * 16;
+    if (transpose)
+        memset(codes, 0, (size_t)BH * d * Np);
+#pragma omp parallel for schedule(static)
+    for (int64_t blk = 0; blk < (int64_t)BH * T; blk++) {
+        const int64_t bh = blk / T;
+        const int t = (int)(blk % T);
+        const int r0 = 128 * t, r1 = r0 + 128 < N ? r0 + 128 : N;
+        float amax = 0.0f;
+        for (int r = r0; r < r1; r++)
+            for (int c = 0; c < d; c++) {
+                const float v = fabsf(X[(bh * N + r) * d + c]);
+                if (v > amax) amax = v;
+            }
+        const float scale = amax > 0.0f ? amax / 448.0f : 1.0f;
+        scales[blk] = scale;
+        for (int r = r0; r < r1; r++)
+            for (int c = 0; c < d; c++) {
+                const float q = X[(bh * N + r) * d + c] / scale;
+                const unsigned char code = oracle_e4m3_encode(q);
+                if (transpose)
+                    codes[(bh * d + c) * Np + r] = code;
+                else
+                    codes[(bh * N + r) * d + c] = code;
+            }
+    }
+    return 0;
+}

@@ -31,6 +31,10 @@ MUTANTS = {
                                    "acc += q[t] * Kh[(int64_t)j * d + t];\n            s[j] = acc;"),
     "decode causal offset": ("if (causal && j > len - Nq + i) vis = 0;", "if (causal && j > len - Nq + i + 1) vis = 0;"),
     "decode kv_len off by one": ("int vis = j < len;", "int vis = j <= len;"),
+    "e4m3 ties away from even": ("(frac == 0.5 && fmod(r, 2.0) != 0.0)", "(frac == 0.5)"),
+    "e4m3 exponent bias 8": ("const int field = (E2 - 1) + 7;", "const int field = (E2 - 1) + 8;"),
+    "fp8 scale for a 240 maximum": ("amax > 0.0f ? amax / 448.0f : 1.0f", "amax > 0.0f ? amax / 240.0f : 1.0f"),
+    "fp8 transposed row stride": ("codes[(bh * d + c) * Np + r] = code;", "codes[(bh * d + c) * N + r] = code;"),
     "D without dO": ("acc += dOh[(int64_t)i * d + t] * Oh[(int64_t)i * d + t];",
                      "acc += Oh[(int64_t)i * d + t];"),
 }
@@ -48,6 +52,7 @@ def test_pins_catch_mutant(name, tmp_path):
                    check=True)
     env = dict(os.environ, ORACLE_LIB=str(lib), OMP_NUM_THREADS="2")
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_fp8_pins.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, "mutant '%s' survived the pins" % name
