@@ -275,7 +275,7 @@ def e4m3_table():
 def quantize_fp8(X, transpose=False):
     """Block quantisation of X [B, H, N, d] (bf16 values as fp32/fp64):
     codes uint8 [B, H, N, d] (with transpose: [B, H, d, Np], Np = ceil(N/16)*16)
-    and scales fp32 [B, H, ceil(N/128)]."""
+    and scales fp32 [B, H, ceil(N/128)] (amax / 448; 0 for an all-zero block)."""
     lib = _load()
     X = np.ascontiguousarray(np.asarray(X, dtype=np.float32))
     if X.ndim != 4:

@@ -473,7 +473,8 @@ int oracle_decode(const double *Q, const double *K, const double *V, int B, int 
  *     magnitudes above 448 to 448;
  *   - a block is 128 consecutive rows (tokens) x all d columns of one
  *     (b, h); "dynamic" scaling takes its scale from the data: amax / 448 in
- *     fp32 (1 for an all-zero block);
+ *     fp32.  An all-zero block has no range to scale: its scale is 0 and its
+ *     codes are 0 (so it never inflates a maximum taken over block scales);
  *   - code = e4m3(x / scale), the division in fp32; the codes stand for the
  *     values code * scale.
  */
@@ -545,12 +546,11 @@ int oracle_quantize_fp8(const float *X, int BH, int N, int d, int transpose, uns
                 const float v = fabsf(X[(bh * N + r) * d + c]);
                 if (v > amax) amax = v;
             }
-        const float scale = amax > 0.0f ? amax / 448.0f : 1.0f;
+        const float scale = amax > 0.0f ? amax / 448.0f : 0.0f;
         scales[blk] = scale;
         for (int r = r0; r < r1; r++)
             for (int c = 0; c < d; c++) {
-                const float q = X[(bh * N + r) * d + c] / scale;
-                const unsigned char code = oracle_e4m3_encode(q);
+                const unsigned char code = scale > 0.0f ? oracle_e4m3_encode(X[(bh * N + r) * d + c] / scale) : 0;
                 if (transpose)
                     codes[(bh * d + c) * Np + r] = code;
                 else

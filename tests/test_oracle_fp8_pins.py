@@ -100,7 +100,8 @@ def test_transposed_layout_and_zero_block():
     assert np.array_equal(st, scales)
     assert np.array_equal(ct[:, :, :, :N], np.swapaxes(codes, 2, 3))
     assert np.all(ct[:, :, :, N:] == 0)
-    assert scales[0, 1, 1] == 1.0 and np.all(codes[0, 1, 128:] == 0)
+    assert scales[0, 1, 1] == 0.0 and np.all(codes[0, 1, 128:] == 0)
+    assert np.all(oracle.dequantize_fp8(codes, scales, N)[0, 1, 128:] == 0.0)
     assert np.array_equal(oracle.dequantize_fp8(ct, st, N, transpose=True), oracle.dequantize_fp8(codes, scales, N))
 
 

@@ -33,7 +33,7 @@ MUTANTS = {
     "decode kv_len off by one": ("int vis = j < len;", "int vis = j <= len;"),
     "e4m3 ties away from even": ("(frac == 0.5 && fmod(r, 2.0) != 0.0)", "(frac == 0.5)"),
     "e4m3 exponent bias 8": ("const int field = (E2 - 1) + 7;", "const int field = (E2 - 1) + 8;"),
-    "fp8 scale for a 240 maximum": ("amax > 0.0f ? amax / 448.0f : 1.0f", "amax > 0.0f ? amax / 240.0f : 1.0f"),
+    "fp8 scale for a 240 maximum": ("amax > 0.0f ? amax / 448.0f : 0.0f", "amax > 0.0f ? amax / 240.0f : 0.0f"),
     "fp8 transposed row stride": ("codes[(bh * d + c) * Np + r] = code;", "codes[(bh * d + c) * N + r] = code;"),
     "D without dO": ("acc += dOh[(int64_t)i * d + t] * Oh[(int64_t)i * d + t];",
                      "acc += Oh[(int64_t)i * d + t];"),
