@@ -92,6 +92,37 @@ fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LS
                  void *stream);
 
 /*
+ * FP8 block quantisation ("FlashAttention: Mathematical Foundations ...",
+ * section "Architectural Evolution", FlashAttention-3 paragraph:
+ * block-quantised FP8 matmuls with dynamic scaling).  X: device bf16
+ * [B, H, N, d] (read).  A block is 128 consecutive rows of one (b, h); its
+ * scale, written to scales (device fp32 [B, H, ceil(N / 128)]), is
+ * amax / 448 (0 for an all-zero block), and each element becomes the e4m3
+ * code of x / scale (fp32 division, nearest-even, saturating to +-448).
+ * X8 (device, written): e4m3 codes [B, H, N, d], or with transpose != 0
+ * [B, H, d, Np], Np = ceil(N / 16) * 16, columns N..Np-1 zero (the layout
+ * fa_fwd_fp8 wants for V).  One kernel launch, no workspace.
+ */
+fa_status fa_quantize_fp8(const void *X, void *X8, float *scales, int B, int H, int N, int d,
+                          int transpose, void *stream);
+
+/*
+ * FP8 forward (d = 128 only; other d: FA_ERR_UNSUPPORTED).  Q8, K8: e4m3
+ * [B, H, N, d]; Vt8: e4m3 [B, H, d, Np] (fa_quantize_fp8 with transpose);
+ * sQ, sK, sV: their block scales [B, H, ceil(N / 128)]; all device, read.
+ * Computes exact attention of the values the codes stand for (code * block
+ * scale) with both products on the FP8 tensor cores; the probabilities are
+ * rounded to e4m3 for the P.V product (this, not the inputs, sets the
+ * accuracy: about 2^-5 relative per probability).  O (bf16), LSE (fp32,
+ * natural log), masks and workspace as fa_fwd.  One kernel launch.
+ */
+fa_status fa_fwd_fp8(const void *Q8, const void *K8, const void *Vt8, const float *sQ,
+                     const float *sK, const float *sV, void *O, float *LSE, int B, int H, int N,
+                     int d, float softmax_scale, int causal, const int32_t *key_len,
+                     const uint8_t *block_mask, void *workspace, size_t workspace_bytes,
+                     void *stream);
+
+/*
  * Backward for the loss sum(O * dO).  Q, K, V, O, dO: device bf16 [B, H, N, d]
  * (read); LSE: device fp32 [B, H, N] from fa_fwd with the same arguments
  * (read).  dQ, dK, dV: device bf16 [B, H, N, d] (written).  Three kernel

@@ -75,6 +75,10 @@ def lib():
             L.fa_decode_workspace_size.restype = sz
             L.fa_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, i, vp, sz, vp]
             L.fa_decode.restype = i
+            L.fa_quantize_fp8.argtypes = [vp, vp, vp, i, i, i, i, i, vp]
+            L.fa_quantize_fp8.restype = i
+            L.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp, vp, sz, vp]
+            L.fa_fwd_fp8.restype = i
             L.fa_tile_plan.argtypes = [i, i, i, vp, vp, vp, vp, sz, vp]
             L.fa_tile_plan.restype = i
             L.fa_attention_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp,
@@ -91,8 +95,10 @@ def lib():
 
 
 EXPORTED = ("fa_tile_size", "fa_fwd_workspace_size", "fa_bwd_workspace_size", "fa_fwd", "fa_bwd",
-            "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_postprocess", "fa_bwd_noalloc", "fa_decode_workspace_size", "fa_decode", "fa_tile_plan", "fa_host_workspace_size", "fa_attention_host", "fa_get_device_status",
-            "fa_reset_device_status", "fa_status_string")
+            "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_postprocess", "fa_bwd_noalloc",
+            "fa_decode_workspace_size", "fa_decode", "fa_quantize_fp8", "fa_fwd_fp8", "fa_tile_plan",
+            "fa_host_workspace_size", "fa_attention_host", "fa_get_device_status", "fa_reset_device_status",
+            "fa_status_string")
 
 
 # ---------------------------------------------------------------- marshalling helpers
@@ -141,6 +147,17 @@ def fa_fwd(Q, K, V, O, LSE, B, H, N, d, softmax_scale, causal, key_len, block_ma
     return lib().fa_fwd(_p(Q), _p(K), _p(V), _p(O), _p(LSE), B, H, N, d, float(softmax_scale),
                         int(bool(causal)), _p(key_len), _p(block_mask), _p(workspace),
                         int(workspace_bytes), _stream(stream))
+
+
+def fa_quantize_fp8(X, X8, scales, B, H, N, d, transpose, stream=None) -> int:
+    return lib().fa_quantize_fp8(_p(X), _p(X8), _p(scales), B, H, N, d, int(bool(transpose)), _stream(stream))
+
+
+def fa_fwd_fp8(Q8, K8, Vt8, sQ, sK, sV, O, LSE, B, H, N, d, softmax_scale, causal, key_len, block_mask,
+               workspace, workspace_bytes, stream=None) -> int:
+    return lib().fa_fwd_fp8(_p(Q8), _p(K8), _p(Vt8), _p(sQ), _p(sK), _p(sV), _p(O), _p(LSE), B, H, N, d,
+                            float(softmax_scale), int(bool(causal)), _p(key_len), _p(block_mask), _p(workspace),
+                            int(workspace_bytes), _stream(stream))
 
 
 def fa_bwd(Q, K, V, O, LSE, dO, dQ, dK, dV, B, H, N, d, softmax_scale, causal, key_len, block_mask,
@@ -242,6 +259,40 @@ def attention_forward(Q, K, V, softmax_scale=None, causal=False, key_len=None, b
                   stream), "fa_fwd")
     if check_status:
         _check(fa_get_device_status(ws, stream), "fa_fwd (device)")
+    return O, LSE
+
+
+def quantize_fp8(X, transpose=False, stream=None):
+    """(codes, scales) = fa_quantize_fp8(X): codes uint8 [B, H, N, d] (transpose:
+    [B, H, d, Np], Np = ceil(N / 16) * 16), scales fp32 [B, H, ceil(N / 128)]."""
+    import torch
+    B, H, N, d = _dims(X)
+    Np = (N + 15) // 16 * 16
+    X8 = torch.empty((B, H, d, Np) if transpose else (B, H, N, d), dtype=torch.uint8, device=X.device)
+    sc = torch.empty((B, H, (N + 127) // 128), dtype=torch.float32, device=X.device)
+    _check(fa_quantize_fp8(X, X8, sc, B, H, N, d, transpose, stream), "fa_quantize_fp8")
+    return X8, sc
+
+
+def attention_forward_fp8(Q, K, V, softmax_scale=None, causal=False, key_len=None, block_mask=None, ws=None,
+                          stream=None, check_status=False):
+    """O, LSE of the FP8 forward on bf16 CUDA tensors [B, H, N, 128]: Q, K and V
+    are block-quantised (fa_quantize_fp8), then fa_fwd_fp8 runs."""
+    import torch
+    B, H, N, d = _dims(Q)
+    scale = (1.0 / d ** 0.5) if softmax_scale is None else softmax_scale
+    Q8, sQ = quantize_fp8(Q, False, stream)
+    K8, sK = quantize_fp8(K, False, stream)
+    Vt8, sV = quantize_fp8(V, True, stream)
+    O = torch.empty_like(Q)
+    LSE = torch.empty((B, H, N), dtype=torch.float32, device=Q.device)
+    need = fa_fwd_workspace_size(B, H, N, d)
+    if ws is None:
+        ws = workspace(need, Q.device)
+    _check(fa_fwd_fp8(Q8, K8, Vt8, sQ, sK, sV, O, LSE, B, H, N, d, scale, causal, key_len, block_mask, ws,
+                      ws.numel(), stream), "fa_fwd_fp8")
+    if check_status:
+        _check(fa_get_device_status(ws, stream), "fa_fwd_fp8 (device)")
     return O, LSE
 
 

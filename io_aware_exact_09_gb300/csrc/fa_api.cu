@@ -59,6 +59,21 @@ bool encode_bf16_3d(CUtensorMap *m, const void *ptr, int d, int N, int BH, int b
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D byte view [outer][rows][inner] of e4m3 codes; box of 128 bytes x
+// box_rows rows, 128-byte swizzle (FP8 Q, K: inner = d = 128; V^T: inner =
+// Np, rows = d).
+bool encode_u8_3d(CUtensorMap *m, const void *ptr, int inner, int rows, int outer, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)rows, (cuuint64_t)outer};
+    cuuint64_t strides[2] = {(cuuint64_t)inner, (cuuint64_t)rows * inner};
+    cuuint32_t box[3] = {128, (cuuint32_t)box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 3-D fp32 view [BH][N][d] of the dQ accumulator; box of 32 columns (128
 // bytes) x box_rows rows, 128-byte swizzle (target of the TMA reduce-add).
 bool encode_f32_3d(CUtensorMap *m, const void *ptr, int d, int N, int BH, int box_rows) {
@@ -158,6 +173,60 @@ fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LS
     p.causal = causal ? 1 : 0;
     p.scale_log2 = softmax_scale * kLog2e;
     return fa::launch_fwd(d, p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_quantize_fp8(const void *X, void *X8, float *scales, int B, int H, int N, int d, int transpose,
+                          void *stream) {
+    bool empty = false;
+    fa_status st = check_sizes(B, H, N, d, &empty);
+    if (st != FA_OK) return st;
+    if (empty) return FA_OK;
+    if (!X || !X8 || !scales || !aligned16(X) || !aligned16(X8) || !aligned16(scales))
+        return FA_ERR_INVALID_ARGUMENT;
+    return fa::launch_quant_fp8(d, X, X8, scales, B * H, N, transpose ? 1 : 0, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? FA_OK
+               : FA_ERR_CUDA;
+}
+
+fa_status fa_fwd_fp8(const void *Q8, const void *K8, const void *Vt8, const float *sQ, const float *sK,
+                     const float *sV, void *O, float *LSE, int B, int H, int N, int d, float softmax_scale,
+                     int causal, const int32_t *key_len, const uint8_t *block_mask, void *workspace,
+                     size_t workspace_bytes, void *stream) {
+    bool empty = false;
+    fa_status st = check_sizes(B, H, N, d, &empty);
+    if (st != FA_OK) return st;
+    if (d != 128) return FA_ERR_UNSUPPORTED;
+    if (!scale_ok(softmax_scale)) return FA_ERR_INVALID_ARGUMENT;
+    if (empty) return FA_OK;
+    if (!Q8 || !K8 || !Vt8 || !sQ || !sK || !sV || !O || !LSE) return FA_ERR_INVALID_ARGUMENT;
+    if (!aligned16(Q8) || !aligned16(K8) || !aligned16(Vt8) || !aligned16(O) || !aligned16(LSE))
+        return FA_ERR_INVALID_ARGUMENT;
+    if (!workspace || !aligned16(workspace) || workspace_bytes < fa_fwd_workspace_size(B, H, N, d))
+        return FA_ERR_WORKSPACE;
+    FwdParams p;
+    std::memset(&p, 0, sizeof(p));
+    const int BH = B * H;
+    const int Np = (N + 15) / 16 * 16;
+    if (!encode_u8_3d(&p.tmQ, Q8, d, N, BH, 128) || !encode_u8_3d(&p.tmK, K8, d, N, BH, 128) ||
+        !encode_u8_3d(&p.tmV, Vt8, Np, d, BH, d))
+        return FA_ERR_CUDA;
+    p.sQ = sQ;
+    p.sK = sK;
+    p.sV = sV;
+    p.O = O;
+    p.LSE = LSE;
+    p.key_len = key_len;
+    p.block_mask = block_mask;
+    p.status = static_cast<unsigned *>(workspace);
+    p.H = H;
+    p.N = N;
+    p.BH = BH;
+    p.Tq = (N + 127) / 128;
+    p.Tk = p.Tq;
+    p.causal = causal ? 1 : 0;
+    p.scale_log2 = softmax_scale * kLog2e;
+    return fa::launch_fwd_fp8(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 namespace {

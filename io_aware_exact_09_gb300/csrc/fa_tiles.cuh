@@ -54,7 +54,9 @@ __device__ __forceinline__ int key_visible_bound(const int32_t *key_len, int b, 
 }
 
 struct FwdParams {
-    CUtensorMap tmQ, tmK, tmV;       // [BH][N][d] bf16, box {64, 128, 1}, 128B swizzle
+    CUtensorMap tmQ, tmK, tmV;       // [BH][N][d] bf16, box {64, 128, 1}, 128B swizzle; FP8: Q, K e4m3
+                                     // [BH][N][d] box {128, 128, 1}, V^T e4m3 [BH][d][Np] box {128, d, 1}
+    const float *sQ, *sK, *sV;       // FP8 only: per-(bh, 128-row block) scales [BH][T]
     void *O;                         // bf16 [BH][N][d]
     float *LSE;                      // fp32 [BH][N]
     const int32_t *key_len;          // device [B] or null

@@ -1,0 +1,135 @@
+"""FP8 forward: the block quantiser (fa_quantize_fp8) is compared byte for
+byte with the oracle's; the FP8 attention (fa_fwd_fp8) against the fp64
+oracle's exact attention of the values the codes stand for.
+
+Tolerance of the FP8 attention.  Its inputs are exact (the oracle reads the
+same codes and scales); what differs is that the kernel rounds every
+probability to e4m3 for the P.V product.  One e4m3 rounding has relative
+error at most 2^-4, and for values spread over a binade its RMS is
+2^-4 * sqrt(E[(2^e/x)^2] / 3) ~= 0.027.  With value rows that are not
+correlated with the rounding errors, the RMS relative error of O is the
+same 0.027, so the O relative-Frobenius bound is twice that, 0.05; the
+worst case of one row (every rounding in the same direction) is
+2^-4 * max|V| (plus the bf16 rounding of O), the max-abs bound.  LSE uses
+the unrounded probabilities: the bf16 bound 1e-3 applies."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_common import LSE_MAX_ABS, f64, rel_fro
+from synthetic import WORKLOADS, make_case, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+FP8_O_REL_FRO = 0.05
+
+
+def fp8_max_abs(Vh):
+    return 2.0 ** -4 * float(np.max(np.abs(Vh))) + 2.0 ** -8
+
+
+def quant_gpu(X, transpose):
+    import io_aware_exact_09_gb300 as fa
+    X8, sc = fa.quantize_fp8(X.cuda().contiguous(), transpose)
+    torch.cuda.synchronize()
+    return X8.cpu().numpy(), sc.cpu().numpy()
+
+
+@pytest.mark.parametrize("shape", [(1, 2, 300, 128), (2, 1, 128, 64), (1, 1, 17, 128), (1, 2, 1000, 128),
+                                   (2, 2, 129, 64)])
+@pytest.mark.parametrize("transpose", [False, True])
+def test_quantize_bit_exact(shape, transpose):
+    B, H, N, d = shape
+    g = torch.Generator().manual_seed(sum(shape) + transpose)
+    X = torch.randn(shape, generator=g)
+    X[0, 0, :min(N, 128)] *= 1e3                      # a block with a wide range
+    if N > 128:
+        X[-1, -1, 128:256] = 0.0                      # an all-zero block
+    X[0, -1, 0, :5] = torch.tensor([-0.0, 1e-30, -1e-30, 3.0, -3.0])
+    X = X.to(torch.bfloat16)
+    codes, sc = quant_gpu(X, transpose)
+    rc, rs = oracle.quantize_fp8(X.float().numpy(), transpose)
+    assert np.array_equal(sc.view(np.uint32), rs.view(np.uint32))
+    assert codes.shape == rc.shape
+    assert np.array_equal(codes, rc), int(np.sum(codes != rc))
+
+
+def run_fp8(case):
+    import io_aware_exact_09_gb300 as fa
+    dev = lambda t: None if t is None else t.cuda().contiguous()
+    O, L = fa.attention_forward_fp8(dev(case["Q"]), dev(case["K"]), dev(case["V"]), case["scale"], case["causal"],
+                                    dev(case["key_len"]), dev(case["block_mask"]), check_status=True)
+    torch.cuda.synchronize()
+    return O.double().cpu().numpy(), L.double().cpu().numpy()
+
+
+def dequantized(case):
+    N = case["Q"].shape[2]
+    out = []
+    for k, tr in (("Q", False), ("K", False), ("V", True)):
+        codes, sc = oracle.quantize_fp8(case[k].float().numpy(), tr)
+        out.append(oracle.dequantize_fp8(codes, sc, N, tr))
+    return out
+
+
+def check_fp8(O, L, rO, rL, Vh, label):
+    fin = np.isfinite(rL)
+    assert np.all(L[~fin] == -np.inf) and np.all(O[~fin] == 0), label
+    assert np.all(np.isfinite(O)), label
+    e = rel_fro(O, rO)
+    assert e <= FP8_O_REL_FRO, (label, "O rel", e)
+    assert np.max(np.abs(O - rO)) <= fp8_max_abs(Vh), (label, "O abs", np.max(np.abs(O - rO)))
+    assert np.max(np.abs(L[fin] - rL[fin])) <= LSE_MAX_ABS, (label, "LSE")
+    return e
+
+
+@pytest.mark.parametrize("N", [128, 200, 512, 1000])
+@pytest.mark.parametrize("mask", ["none", "causal", "key_len", "block"])
+def test_fwd_fp8_matches_oracle(N, mask):
+    kw = {}
+    if mask == "causal":
+        kw["causal"] = True
+    elif mask == "key_len":
+        kw["key_len"] = [max(1, N // 3), N]
+    elif mask == "block":
+        nb = (N + 127) // 128
+        bm = (np.random.default_rng(N).random((nb, nb)) < 0.5).astype(np.uint8)
+        np.fill_diagonal(bm, 1)
+        kw["block_mask"] = bm
+    case = make_case(2, 2, N, 128, seed=N + len(mask), **kw)
+    O, L = run_fp8(case)
+    Qh, Kh, Vh = dequantized(case)
+    kl = None if case["key_len"] is None else case["key_len"].numpy()
+    bm = None if case["block_mask"] is None else case["block_mask"].numpy()
+    rO, rL = oracle.attention_fwd(Qh, Kh, Vh, case["scale"], causal=case["causal"], key_len=kl, block_mask=bm)
+    check_fp8(O, L, rO, rL, Vh, (N, mask))
+
+
+def test_fwd_fp8_rejects_d64_and_bad_args():
+    import io_aware_exact_09_gb300 as fa
+    x = torch.zeros((1, 1, 128, 64), dtype=torch.uint8, device="cuda")
+    s = torch.zeros((1, 1, 1), device="cuda")
+    O = torch.zeros((1, 1, 128, 64), dtype=torch.bfloat16, device="cuda")
+    L = torch.zeros((1, 1, 128), device="cuda")
+    ws = fa.workspace(fa.fa_fwd_workspace_size(1, 1, 128, 64), "cuda")
+    assert fa.fa_fwd_fp8(x, x, x, s, s, s, O, L, 1, 1, 128, 64, 0.125, 0, None, None, ws, ws.numel()) == 2
+    assert fa.fa_fwd_fp8(None, x, x, s, s, s, O, L, 1, 1, 128, 128, 0.125, 0, None, None, ws, ws.numel()) == 1
+
+
+def test_fwd_fp8_full_size_sampled_rows():
+    """The long-context shape (B=1, H=16, N=16384, d=128) in the launch
+    configuration bench.py times: sampled query rows of two heads."""
+    w = WORKLOADS["longctx_b1h16n16384d128"]
+    case = make_inputs(w, with_dO=False)
+    O, L = run_fp8(case)
+    Qh, Kh, Vh = dequantized(case)
+    B, H, N, d = w.B, w.H, w.N, w.d
+    rng = np.random.default_rng(5)
+    rows = []
+    for h in (0, H - 1):
+        rows += [h * N + r for r in sorted(rng.choice(N, 24, replace=False))]
+    rows = np.array(rows, np.int64)
+    rO, rL, _ = oracle.query_rows(Qh, Kh, Vh, np.zeros_like(Qh), case["scale"], rows)
+    flat = lambda X: X.reshape(B * H * N, -1)
+    check_fp8(flat(O)[rows], L.reshape(-1)[rows], rO, rL, Vh, "full size")
