@@ -16,6 +16,12 @@ collective); the time is the max over ranks.
 ``--impl reference`` times the fp64 CPU oracle instead, on a bounded sample
 of the same workload, on this machine's host cores.
 
+``--fp8`` measures the FP8 forward instead: one step = the block
+quantisation of Q, K and V (``fa_quantize_fp8``, three launches) and
+``fa_fwd_fp8``; ``value`` is forward TFLOP/s over the step, the roofline is
+the FP8 forward kernel against the dense-FP8 peak (the measured sustained
+bf16 figure x 2, the nominal fp8 : bf16 ratio).
+
 ``--workload decode_...`` measures the split-KV decode path instead: one step
 = one ``fa_decode`` call (a few new query rows per sequence against a
 resident key/value cache); ``value`` is GB/s of algorithmic traffic (Q, the
@@ -41,7 +47,8 @@ if ROOT not in sys.path:
 
 DEFAULT_WORKLOAD = "longctx_b1h16n16384d128"
 FWD_BWD_FACTOR = 3.5          # forward + backward = forward x (1 + 2.5)
-KERNEL_SOURCES = {"fa_fwd_kernel": "fa_fwd.cu", "fa_bwd_kernel": "fa_bwd.cu"}
+KERNEL_SOURCES = {"fa_fwd_kernel": "fa_fwd.cu", "fa_bwd_kernel": "fa_bwd.cu", "fa_fwd_kernel_fp8": "fa_fwd.cu",
+                  "fa_decode_kernel": "fa_decode.cu"}
 
 
 # ---------------------------------------------------------------- distributed helpers
@@ -338,7 +345,7 @@ def run_decode(args, w):
     achieved = nbytes / (ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "kernel": "fa_decode_kernel + fa_decode_merge_kernel (one fa_decode call)",
                 "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": None, "peak_source": "%s hbm_gbs" % peak_src}
+                "traffic": ncu_traffic("fa_decode_kernel", w.name), "peak_source": "%s hbm_gbs" % peak_src}
 
     e2e = None
     if not args.no_e2e:
@@ -384,6 +391,133 @@ def run_decode(args, w):
             "algorithmic_bytes_per_step": nbytes,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
             "gpu_launches": launches,
+        }
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- FP8 forward
+def run_fp8(args):
+    import torch
+
+    ws_n, rank = init_dist("nccl")
+    _, _, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import io_aware_exact_09_gb300 as fa
+    from synthetic import WORKLOADS, algorithmic_fwd_flops, make_inputs
+    fa.build()
+    w = WORKLOADS[args.workload]
+    B, H, N, d = w.B, w.H, w.N, w.d
+    if d != 128:
+        raise SystemExit("the FP8 forward needs d = 128")
+    case = make_inputs(w, with_dO=False)
+    Q, K, V = (case[k].to(dev).contiguous() for k in ("Q", "K", "V"))
+    kl = None if case["key_len"] is None else case["key_len"].to(dev)
+    bm = None if case["block_mask"] is None else case["block_mask"].contiguous().to(dev)
+    T, Np = (N + 127) // 128, (N + 15) // 16 * 16
+    Q8 = torch.empty((B, H, N, d), dtype=torch.uint8, device=dev)
+    K8 = torch.empty_like(Q8)
+    Vt8 = torch.empty((B, H, d, Np), dtype=torch.uint8, device=dev)
+    sQ, sK, sV = (torch.empty((B, H, T), dtype=torch.float32, device=dev) for _ in range(3))
+    O = torch.empty_like(Q)
+    LSE = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    wsn = fa.fa_fwd_workspace_size(B, H, N, d)
+    ws = fa.workspace(wsn, dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    flops = algorithmic_fwd_flops(B, H, N, d, w.causal,
+                                  None if case["key_len"] is None else case["key_len"].tolist(),
+                                  None if case["block_mask"] is None else case["block_mask"])
+
+    def check(st, where):
+        if st != 0:
+            raise RuntimeError("%s failed: %s" % (where, fa.fa_status_string(st)))
+
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+
+    def step(record):
+        if record:
+            ev[0].record(stream)
+        check(fa.fa_quantize_fp8(Q, Q8, sQ, B, H, N, d, False, sp), "fa_quantize_fp8 Q")
+        check(fa.fa_quantize_fp8(K, K8, sK, B, H, N, d, False, sp), "fa_quantize_fp8 K")
+        check(fa.fa_quantize_fp8(V, Vt8, sV, B, H, N, d, True, sp), "fa_quantize_fp8 V")
+        if record:
+            ev[1].record(stream)
+        check(fa.fa_fwd_fp8(Q8, K8, Vt8, sQ, sK, sV, O, LSE, B, H, N, d, w.softmax_scale, w.causal, kl, bm, ws, wsn,
+                            sp), "fa_fwd_fp8")
+        if record:
+            ev[2].record(stream)
+
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        step(False)
+    torch.cuda.synchronize(dev)
+    check(fa.fa_get_device_status(ws, sp), "device status after warm-up")
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    tq, tf_, tstep = [], [], []
+    barrier()
+    torch.cuda.synchronize(dev)
+    launches = 0
+    for _ in range(args.steps):
+        flush.zero_()
+        step(True)
+        launches += 4
+        ev[2].synchronize()
+        tq.append(ev[0].elapsed_time(ev[1]))
+        tf_.append(ev[1].elapsed_time(ev[2]))
+        tstep.append(ev[0].elapsed_time(ev[2]))
+    torch.cuda.synchronize(dev)
+    barrier()
+    clk = clocks.stop()
+    check(fa.fa_get_device_status(ws, sp), "device status after timing")
+    mq, mf, ms = (sum(x) / len(x) for x in (tq, tf_, tstep))
+    step_ms = reduce_max(ms, dev)
+    value = whole_job_tflops(flops, ws_n, step_ms / 1e3)
+    peaks, peak_src = measured_peaks()
+    peak8 = 2.0 * float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    achieved = flops / (mf / 1e3) / 1e12
+    roofline = {"bound": "tensor", "kernel": "fa_fwd_kernel<128, fp8>", "achieved": achieved, "peak": peak8,
+                "unit": "TFLOP/s", "frac": achieved / peak8, "traffic": ncu_traffic("fa_fwd_kernel_fp8", w.name),
+                "peak_source": "%s bf16_tflops_sustained x 2 (nominal dense fp8 : bf16 ratio 4.5 : 2.25)" % peak_src}
+    e2e = None
+    if not args.no_e2e:
+        # the user's call from host memory: bf16 Q, K, V in, O and LSE out
+        pin = lambda t: t.contiguous().pin_memory()
+        Qh, Kh, Vh = (pin(case[k]) for k in ("Q", "K", "V"))
+        Oh = torch.empty_like(Qh).pin_memory()
+        Lh = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        et = []
+        for i in range(1 + max(1, min(args.steps, 5))):
+            e0.record(stream)
+            Q.copy_(Qh, non_blocking=True)
+            K.copy_(Kh, non_blocking=True)
+            V.copy_(Vh, non_blocking=True)
+            step(False)
+            Oh.copy_(O, non_blocking=True)
+            Lh.copy_(LSE, non_blocking=True)
+            e1.record(stream)
+            e1.synchronize()
+            if i > 0:
+                et.append(e0.elapsed_time(e1))
+        e_ms = reduce_max(sum(et) / len(et), dev)
+        nb = B * H * N * d * 2
+        e2e = {"value": whole_job_tflops(flops, ws_n, e_ms / 1e3), "unit": "TFLOP/s",
+               "h2d_bytes_per_step": 3 * nb, "d2h_bytes_per_step": nb + B * H * N * 4, "ms_per_step": e_ms}
+    if rank == 0:
+        line = {
+            "metric": "attention fwd TFLOP/s (fp8 e4m3, block-quantised)", "value": value, "unit": "TFLOP/s",
+            "n_gpus": ws_n, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp8-e4m3", "data": "synthetic",
+            "config": {"workload": w.name, "B": B, "H": H, "N": N, "d": d, "causal": w.causal, "path": "fp8 forward",
+                       "parallelism": "replicas" if ws_n > 1 else "single", "l2": "flushed between steps"},
+            "kernel_ms": {"fa_quant_fp8_kernel x3": mq, "fa_fwd_kernel<128, fp8>": mf},
+            "fwd_kernel_tflops": achieved, "algorithmic_flops_per_step": flops,
+            "roofline": roofline, "cpu_baseline": None, "e2e": e2e, "clocks": clk, "gpu_launches": launches,
         }
         print(json.dumps(line), flush=True)
     return 0
@@ -614,6 +748,7 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--fp8", action="store_true", help="measure the FP8 forward (d = 128 workloads)")
     ap.add_argument("--decode-reps", type=int, default=20,
                     help="decode workloads: timed calls per step (each one is well under a millisecond)")
     args = ap.parse_args(argv)
@@ -624,6 +759,8 @@ def main(argv=None):
     from synthetic import DECODE_WORKLOADS
     if args.workload in DECODE_WORKLOADS:
         return run_decode(args, DECODE_WORKLOADS[args.workload])
+    if args.fp8:
+        return run_fp8(args)
     return run_ours(args)
 
 

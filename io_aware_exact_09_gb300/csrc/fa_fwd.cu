@@ -38,18 +38,6 @@
 //     the end, the epilogue O / l -> bf16, LSE = (m + log2 l) * ln 2.
 // Skipped tiles (block mask zero, all keys past key_len, above the causal
 // diagonal) are never loaded; partial tiles get element masks.
-//
-// FP8 instantiation (d = 128; "FlashAttention: Mathematical Foundations
-// ...", section "Architectural Evolution", FlashAttention-3 paragraph:
-// block-quantised FP8 matmuls with dynamic scaling): Q, K and V^T arrive as
-// e4m3 codes with one fp32 scale per 128-row block (fa_quant.cu).  Both
-// products are kind::f8f6f4 MMAs (32 elements of K per instruction).  The
-// score of the (query block i, key block j) tile is
-// scale * sQ_i * sK_j * (q8 . k8), so the softmax multiplier c becomes
-// c * sQ_i * sK_j per tile.  P is quantised to e4m3 for the P.V product; V's
-// block scale sV_j is folded into it as P * (sV_j / max_j sV_j) (at most 1,
-// so P stays <= 2^8 < 448) and the head's max_j sV_j multiplies O in the
-// epilogue; l sums the unquantised p.
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
 
@@ -57,13 +45,12 @@ namespace fa {
 
 constexpr float kRescaleLog2 = 8.0f;
 
-template <int D, bool F8 = false>
+template <int D>
 struct FwdShape {
-    static_assert(!F8 || D == 128, "FP8 forward: d = 128");
-    static constexpr int CHUNKS = F8 ? 1 : D / 64;      // 128-byte column chunks (64 bf16 / 128 e4m3)
+    static constexpr int CHUNKS = D / 64;               // 64-element (128-byte) column chunks
     static constexpr int CHUNK_BYTES = 128 * 128;       // 128 rows x 128 bytes
     static constexpr int TILE_BYTES = CHUNKS * CHUNK_BYTES;
-    static constexpr int STAGES = (F8 || D == 64) ? 4 : 2;
+    static constexpr int STAGES = (D == 64) ? 4 : 2;
     static constexpr int OFF_Q = 0;                     // [2] query tiles
     static constexpr int OFF_K = OFF_Q + 2 * TILE_BYTES;
     static constexpr int OFF_V = OFF_K + STAGES * TILE_BYTES;
@@ -99,9 +86,9 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
         if (globaltimer_ns() - t0 > FA_WAIT_TIMEOUT_NS) break;
 }
 
-template <int D, bool F8>
+template <int D>
 __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
-    using S = FwdShape<D, F8>;
+    using S = FwdShape<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -227,14 +214,8 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                     for (int c = 0; c < S::CHUNKS; ++c)
                         tma_load_3d(koff + c * S::CHUNK_BYTES, &p.tmK, bar(S::B_KFULL + s), c * 64, kt * kTile, bh);
                     mbar_arrive_expect_tx(bar(S::B_VFULL + s), S::TILE_BYTES);
-                    if constexpr (F8) {
-                        // V^T: d rows x 128 keys
-                        tma_load_3d(voff, &p.tmV, bar(S::B_VFULL + s), kt * kTile, 0, bh);
-                    } else {
-                        for (int c = 0; c < S::CHUNKS; ++c)
-                            tma_load_3d(voff + c * S::CHUNK_BYTES, &p.tmV, bar(S::B_VFULL + s), c * 64, kt * kTile,
-                                        bh);
-                    }
+                    for (int c = 0; c < S::CHUNKS; ++c)
+                        tma_load_3d(voff + c * S::CHUNK_BYTES, &p.tmV, bar(S::B_VFULL + s), c * 64, kt * kTile, bh);
                 }
                 if (!ok) {
                     // gave up: let every copy already issued land before the CTA exits
@@ -250,31 +231,26 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
         } else if (warp == 1) {
             // ---------------------------------------------------------- MMA issuer
             if (lane == 0) {
-                constexpr uint32_t IDESC_S = F8 ? idesc_e4m3(128, 128) : idesc_bf16(128, 128, false, false);
-                constexpr uint32_t IDESC_PV = F8 ? idesc_e4m3(128, D) : idesc_bf16(128, D, false, true);
-                constexpr int KSTEP = F8 ? 32 : 16;   // K elements per MMA: 32 bytes either way
+                constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
+                constexpr uint32_t IDESC_PV = idesc_bf16(128, D, false, true);
                 int kt = next_tile(2, -1);
                 bool ok = true;
                 int nv[2] = {0, 0};      // key tiles processed so far by query tile x
                 // shared-memory descriptors built once; per MMA only the start
-                // address moves (K-major: 32 bytes per K step inside a 128-byte
-                // row, then the next chunk; MN-major bf16 V: 16 rows; FP8 V^T is
-                // K-major like K)
+                // address moves (K-major: 32 bytes per 16-wide K step inside a
+                // 128-byte row, then the next 64-column chunk; MN-major V: 16 rows)
                 const uint64_t dq0 = sdesc_sw128(base + S::OFF_Q, 16, 1024);
                 const uint64_t dk0 = sdesc_sw128(base + S::OFF_K, 16, 1024);
-                const uint64_t dv0 = sdesc_sw128(base + S::OFF_V, F8 ? 16u : (uint32_t)S::CHUNK_BYTES, 1024);
+                const uint64_t dv0 = sdesc_sw128(base + S::OFF_V, S::CHUNK_BYTES, 1024);
                 // S_x = Q_x K^T for the key tile in stage s (the x-th S buffer)
                 auto issue_s = [&](int x, int s) {
                     const uint32_t d_tmem = tmem + S::TM_S + 128u * (uint32_t)x;
                     const uint64_t qd = sdesc_add(dq0, (uint32_t)(x * S::TILE_BYTES));
                     const uint64_t kd = sdesc_add(dk0, (uint32_t)(s * S::TILE_BYTES));
 #pragma unroll
-                    for (int k = 0; k < D / KSTEP; ++k) {
+                    for (int k = 0; k < D / 16; ++k) {
                         const uint32_t off = (k >> 2) * S::CHUNK_BYTES + (k & 3) * 32;
-                        if constexpr (F8)
-                            mma_ss_f8(d_tmem, sdesc_add(qd, off), sdesc_add(kd, off), IDESC_S, k > 0 ? 1u : 0u);
-                        else
-                            mma_ss(d_tmem, sdesc_add(qd, off), sdesc_add(kd, off), IDESC_S, k > 0 ? 1u : 0u);
+                        mma_ss(d_tmem, sdesc_add(qd, off), sdesc_add(kd, off), IDESC_S, k > 0 ? 1u : 0u);
                     }
                     mma_commit(bar(S::B_SFULL + x));
                 };
@@ -304,15 +280,9 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                             const uint64_t vd = sdesc_add(dv0, (uint32_t)(s * S::TILE_BYTES));
                             const uint32_t acc0 = nv[x] > 0 ? 1u : 0u;
 #pragma unroll
-                            for (int k = 0; k < kTile / KSTEP; ++k) {
-                                // P: 8 TMEM columns per K step (2 bf16 or 4 e4m3 per column)
-                                if constexpr (F8)
-                                    mma_ts_f8(o_tmem, p_tmem + (uint32_t)k * 8u, sdesc_add(vd, (uint32_t)k * 32u),
-                                              IDESC_PV, k > 0 ? 1u : acc0);
-                                else
-                                    mma_ts(o_tmem, p_tmem + (uint32_t)k * 8u, sdesc_add(vd, (uint32_t)k * 2048u),
-                                           IDESC_PV, k > 0 ? 1u : acc0);
-                            }
+                            for (int k = 0; k < kTile / 16; ++k)
+                                mma_ts(o_tmem, p_tmem + (uint32_t)k * 8u, sdesc_add(vd, (uint32_t)k * 2048u), IDESC_PV,
+                                       k > 0 ? 1u : acc0);
                             mma_commit(bar(S::B_PVDONE + x));
                             ++nv[x];
                         }
@@ -357,29 +327,11 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
         const uint32_t o_tmem = tmem + lane_off + S::TM_O + (uint32_t)(D * x);
         const float c2 = p.scale_log2;
         float m_ref = -INFINITY, l = 0.f;
-        // FP8: the query block's scale and the head's largest V block scale
-        float sq = 1.f, sv_max = 1.f, inv_sv_max = 1.f;
-        if constexpr (F8) {
-            if (qn[x] > 0) sq = p.sQ[(size_t)bh * p.Tq + 2 * pq + x];
-            float mv = 0.f;
-            for (int k = lane; k < p.Tk; k += 32) mv = fmaxf(mv, p.sV[(size_t)bh * p.Tk + k]);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, o));
-            sv_max = mv;
-            inv_sv_max = mv > 0.f ? 1.f / mv : 0.f;
-        }
         int it = 0;
         bool ok = true;
         for (int kt = next_tile(x, -1); kt < p.Tk; kt = next_tile(x, kt), ++it) {
             const bool partial = cls(x, kt) == kTilePartial;
             const int k0 = kt * kTile;
-            // FP8: this tile's softmax multiplier and V-scale ratio (loaded
-            // before the wait so that their latency hides behind it)
-            float ct = c2, rt = 1.f;
-            if constexpr (F8) {
-                ct = c2 * sq * p.sK[(size_t)bh * p.Tk + kt];
-                rt = p.sV[(size_t)bh * p.Tk + kt] * inv_sv_max;
-            }
             if (!mbar_wait_warp(bar(S::B_SFULL + x), (uint32_t)it & 1u, g, 0x401)) {
                 ok = false;
                 break;
@@ -415,7 +367,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                 }
             const float mx = fmaxf(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], fmax3(pm[5], pm[6], pm[7])));
             // move the reference maximum only when the row outgrew it by 2^8
-            const float m_tile = mx * ct;
+            const float m_tile = mx * c2;
             const bool grow = m_tile > m_ref + kRescaleLog2;
             float alpha = 1.f;
             const bool rescale = __any_sync(0xffffffffu, grow);
@@ -426,50 +378,25 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                 m_ref = m_new;
             }
             const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-            // p = 2^(s * c - m), bf16 into the first 64 columns of S_x (FP8:
-            // p * rt as e4m3 into the first 32); the row sum in four
-            // independent packed accumulators
+            // p = 2^(s * c - m), bf16 into the first 64 columns of S_x; the row
+            // sum in four independent packed accumulators
             float ps[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) ps[u] = 0.f;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                if constexpr (F8) {
-                    uint32_t pk[8];
+                uint32_t pk[16];
 #pragma unroll
-                    for (int t = 0; t < 8; ++t) {
-                        float a0, a1, a2, a3;
-                        fma2(a0, a1, __uint_as_float(sr[j][4 * t]), __uint_as_float(sr[j][4 * t + 1]), ct, ct, -m_use,
-                             -m_use);
-                        fma2(a2, a3, __uint_as_float(sr[j][4 * t + 2]), __uint_as_float(sr[j][4 * t + 3]), ct, ct,
-                             -m_use, -m_use);
-                        a0 = ex2(a0);
-                        a1 = ex2(a1);
-                        a2 = ex2(a2);
-                        a3 = ex2(a3);
-                        add2(ps[2 * (t & 3)], ps[2 * (t & 3) + 1], a0, a1);
-                        add2(ps[2 * ((t + 2) & 3)], ps[2 * ((t + 2) & 3) + 1], a2, a3);
-                        float b0, b1, b2, b3;
-                        fma2(b0, b1, a0, a1, rt, rt, 0.f, 0.f);
-                        fma2(b2, b3, a2, a3, rt, rt, 0.f, 0.f);
-                        pk[t] = pack_e4m3x4(b0, b1, b2, b3);
-                    }
-                    tmem_st8(s_tmem + 8u * j, pk);
-                } else {
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int t = 0; t < 16; ++t) {
-                        float a, bb;
-                        fma2(a, bb, __uint_as_float(sr[j][2 * t]), __uint_as_float(sr[j][2 * t + 1]), ct, ct, -m_use,
-                             -m_use);
-                        a = ex2(a);
-                        bb = ex2(bb);
-                        const int u = 2 * (t & 3);
-                        add2(ps[u], ps[u + 1], a, bb);
-                        pk[t] = pack_bf16x2(a, bb);
-                    }
-                    tmem_st16(s_tmem + 16u * j, pk);
+                for (int t = 0; t < 16; ++t) {
+                    float a, bb;
+                    fma2(a, bb, __uint_as_float(sr[j][2 * t]), __uint_as_float(sr[j][2 * t + 1]), c2, c2, -m_use, -m_use);
+                    a = ex2(a);
+                    bb = ex2(bb);
+                    const int u = 2 * (t & 3);
+                    add2(ps[u], ps[u + 1], a, bb);
+                    pk[t] = pack_bf16x2(a, bb);
                 }
+                tmem_st16(s_tmem + 16u * j, pk);
             }
             l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
             tmem_st_wait();
@@ -512,8 +439,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
             tc_fence_after();
         }
         if (ok) {
-            // FP8: O also carries the head's largest V block scale
-            const float inv_l = (l > 0.f) ? sv_max / l : 0.f;
+            const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
             __nv_bfloat16 *orow = reinterpret_cast<__nv_bfloat16 *>(p.O) + ((size_t)bh * p.N + q) * D;
 #pragma unroll 1
             for (int j = 0; j < D / 32; ++j) {
@@ -550,21 +476,18 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
 
 int fwd_smem_bytes(int d) { return d == 64 ? FwdShape<64>::SMEM_BYTES : FwdShape<128>::SMEM_BYTES; }
 
-template <int D, bool F8>
+template <int D>
 static cudaError_t launch_fwd_t(const FwdParams &p, cudaStream_t st) {
-    using S = FwdShape<D, F8>;
-    const int smem = S::SMEM_BYTES;
-    cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    const int smem = FwdShape<D>::SMEM_BYTES;
+    cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)((p.Tq + 1) / 2) * (unsigned)p.BH;
-    fa_fwd_kernel<D, F8><<<grid, S::THREADS, smem, st>>>(p);
+    fa_fwd_kernel<D><<<grid, FwdShape<D>::THREADS, smem, st>>>(p);
     return cudaGetLastError();
 }
 
 cudaError_t launch_fwd(int d, const FwdParams &p, cudaStream_t st) {
-    return d == 64 ? launch_fwd_t<64, false>(p, st) : launch_fwd_t<128, false>(p, st);
+    return d == 64 ? launch_fwd_t<64>(p, st) : launch_fwd_t<128>(p, st);
 }
-
-cudaError_t launch_fwd_fp8(const FwdParams &p, cudaStream_t st) { return launch_fwd_t<128, true>(p, st); }
 
 }  // namespace fa

@@ -1,0 +1,507 @@
+// fa_fwd_fp8.cu -- FP8 forward (d = 128): exact attention of block-quantised
+// e4m3 Q, K, V with both products on the FP8 tensor cores.
+//
+// "FlashAttention: Mathematical Foundations ...", section "Architectural
+// Evolution" (FlashAttention-3 paragraph): block-quantised FP8 matmuls with
+// dynamic scaling.  Q, K and V^T arrive as e4m3 codes with one fp32 scale per
+// 128-row block (fa_quant.cu).  The score of the (query block i, key block
+// j) tile is scale * sQ_i * sK_j * (q8 . k8): the softmax multiplier becomes
+// c * sQ_i * sK_j per tile.  The online softmax is the forward kernel's
+// ("The Attention Matrix You Never Write Down", "The running-statistics
+// trick"; base 2; reference maximum moved only when a row outgrows it by
+// 2^8).  P is rounded to e4m3 for the P.V product; V's block scale sV_j is
+// folded into it as P * (sV_j / max_j sV_j) (at most 1, so P stays <= 2^8,
+// inside e4m3's range; the factor goes into the exponent) and the head's
+// max_j sV_j multiplies O in the epilogue; l sums the unrounded p.
+//
+// What differs from the bf16 forward: with e4m3 operands the two MMAs of a
+// tile take half as long, so the per-tile chain S -> softmax -> P -> P.V
+// would leave the tensor pipe idle most of the time if P overwrote S in
+// TMEM (the next S could only start once P.V had read P).  Here P goes to
+// shared memory instead (16 KB per tile in e4m3, double-buffered per query
+// tile), and the softmax warps release S as soon as they have loaded it into
+// registers, so the next tile's S = Q K^T runs while they compute:
+//   - one CTA per (pair of 128-row query tiles, b*h), head-major;
+//   - warp 0: TMA of both Q tiles once, K and V^T tiles through a 3-stage
+//     ring;
+//   - warp 1: tcgen05 issuer.  Per key tile i: S_x(i+1) = Q_x K(i+1)^T as
+//     soon as softmax x has loaded S_x(i) (SFREE), then O_x += P_x(i) V(i)
+//     (A = P_x from shared memory, B = V^T, both K-major) once P_x(i) is
+//     written (PFULL);
+//   - warps 4-7 and 8-11: softmax of query tile 0 and 1, one row per
+//     thread; P rows go to shared memory in the 128-byte-swizzled K-major
+//     layout the MMA reads.
+#include "fa_internal.h"
+#include "fa_ptx.cuh"
+
+namespace fa {
+
+namespace {
+
+constexpr float kRescaleLog2F8 = 8.0f;
+
+struct F8Shape {
+    static constexpr int D = 128;
+    static constexpr int TILE_BYTES = 128 * 128;            // 128 rows x 128 bytes (e4m3)
+    static constexpr int STAGES = 3;
+    static constexpr int OFF_Q = 0;                         // [2] query tiles
+    static constexpr int OFF_K = OFF_Q + 2 * TILE_BYTES;    // [STAGES]
+    static constexpr int OFF_V = OFF_K + STAGES * TILE_BYTES;
+    static constexpr int OFF_P = OFF_V + STAGES * TILE_BYTES;  // [2 query tiles][2 buffers]
+    static constexpr int OFF_BAR = OFF_P + 4 * TILE_BYTES;
+    static constexpr int B_QFULL = 0;
+    static constexpr int B_KFULL = 1;
+    static constexpr int B_VFULL = B_KFULL + STAGES;
+    static constexpr int B_KVEMPTY = B_VFULL + STAGES;
+    static constexpr int B_SFULL = B_KVEMPTY + STAGES;      // [2] per query tile
+    static constexpr int B_SFREE = B_SFULL + 2;             // [2]
+    static constexpr int B_PFULL = B_SFREE + 2;             // [2]
+    static constexpr int B_PVDONE = B_PFULL + 2;            // [2]
+    static constexpr int B_PFREE = B_PVDONE + 2;            // [2][2] per query tile and P buffer
+    static constexpr int B_FIN = B_PFREE + 4;
+    static constexpr int NBAR = B_FIN + 1;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t TM_S = 0;                     // S_x at columns 128 x
+    static constexpr uint32_t TM_O = 256;                   // O_x at columns 256 + 128 x
+    static constexpr int THREADS = 384;
+    static constexpr int LAUNCH_REGS = 168;
+    static constexpr int REGS_CTRL = 88;
+    static constexpr int REGS_SOFTMAX = 208;
+    static_assert(128 * REGS_CTRL + 256 * REGS_SOFTMAX == THREADS * LAUNCH_REGS, "register split");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+};
+
+__device__ __forceinline__ void f8_drain_wait(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (globaltimer_ns() - t0 > FA_WAIT_TIMEOUT_NS) break;
+}
+
+__global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constant__ FwdParams p) {
+    using S = F8Shape;
+    constexpr int D = S::D;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *sb = smem_raw + (base - raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    const int Tp = (p.Tq + 1) / 2;
+    const int pq = Tp - 1 - (int)(blockIdx.x % Tp);
+    const int bh = (int)(blockIdx.x / Tp);
+    const int b = bh / p.H;
+    const int nb = (p.N + kTile - 1) / kTile;
+    int q0[2], qn[2];
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+        q0[x] = (2 * pq + x) * kTile;
+        qn[x] = max(0, min(kTile, p.N - q0[x]));
+    }
+
+    auto bar = [&](int i) -> uint32_t { return base + S::OFF_BAR + 8u * (uint32_t)i; };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sb + S::OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sb + S::OFF_MISC + 4);
+    const Guard g{p.status, p.status + 1, abort_flag};
+
+    bool bad = false;
+    const int kvis = key_visible_bound(p.key_len, b, p.N, &bad);
+    if (bad && threadIdx.x == 0 && pq == 0 && (bh % p.H) == 0) record_status(g, kStatusBadKeyLen, 0);
+
+    int kend[2];
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+        int lim = kvis;
+        if (p.causal) lim = min(lim, q0[x] + qn[x]);
+        kend[x] = qn[x] > 0 ? (lim + kTile - 1) / kTile : 0;
+    }
+    const int kend_union = max(kend[0], kend[1]);
+    auto cls = [&](int x, int kt) -> unsigned {
+        if (qn[x] <= 0) return kTileSkip;
+        const int on = p.block_mask ? (p.block_mask[(size_t)(2 * pq + x) * nb + kt] != 0) : 1;
+        return tile_class(q0[x], qn[x], kt * kTile, kTile, kvis, p.causal, on);
+    };
+    auto next_tile = [&](int x, int kt) -> int {
+        if (!p.block_mask) {
+            const int lim = x == 2 ? kend_union : kend[x];
+            return kt + 1 < lim ? kt + 1 : p.Tk;
+        }
+        for (int k = kt + 1; k < p.Tk; ++k) {
+            const bool v0 = (x != 1) && cls(0, k) != kTileSkip;
+            const bool v1 = (x != 0) && cls(1, k) != kTileSkip;
+            if (v0 || v1) return k;
+        }
+        return p.Tk;
+    };
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(S::B_QFULL), 1);
+        for (int s = 0; s < S::STAGES; ++s) {
+            mbar_init(bar(S::B_KFULL + s), 1);
+            mbar_init(bar(S::B_VFULL + s), 1);
+            mbar_init(bar(S::B_KVEMPTY + s), 1);
+        }
+        for (int j = 0; j < 2; ++j) {
+            mbar_init(bar(S::B_SFULL + j), 1);
+            mbar_init(bar(S::B_SFREE + j), 128);
+            mbar_init(bar(S::B_PFULL + j), 128);
+            mbar_init(bar(S::B_PVDONE + j), 1);
+        }
+        for (int j = 0; j < 4; ++j) mbar_init(bar(S::B_PFREE + j), 1);
+        mbar_init(bar(S::B_FIN), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&p.tmQ);
+        tma_prefetch_desc(&p.tmK);
+        tma_prefetch_desc(&p.tmV);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), S::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp < 4) {
+        setmaxnreg_dec<S::REGS_CTRL>();
+        if (warp == 0) {
+            // ---------------------------------------------------------- producer
+            if (lane == 0) {
+                int u = 0;
+                bool ok = true;
+                int kt = next_tile(2, -1);
+                if (kt < p.Tk) {
+                    const uint32_t nq = (qn[0] > 0 ? 1u : 0u) + (qn[1] > 0 ? 1u : 0u);
+                    mbar_arrive_expect_tx(bar(S::B_QFULL), nq * S::TILE_BYTES);
+                    for (int x = 0; x < 2; ++x)
+                        if (qn[x] > 0)
+                            tma_load_3d(base + S::OFF_Q + x * S::TILE_BYTES, &p.tmQ, bar(S::B_QFULL), 0, q0[x], bh);
+                }
+                for (; kt < p.Tk; kt = next_tile(2, kt), ++u) {
+                    const int s = u % S::STAGES;
+                    const uint32_t ph = (uint32_t)(u / S::STAGES) & 1u;
+                    if (!mbar_wait(bar(S::B_KVEMPTY + s), ph ^ 1u, g, 0x111)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(bar(S::B_KFULL + s), S::TILE_BYTES);
+                    tma_load_3d(base + S::OFF_K + s * S::TILE_BYTES, &p.tmK, bar(S::B_KFULL + s), 0, kt * kTile, bh);
+                    mbar_arrive_expect_tx(bar(S::B_VFULL + s), S::TILE_BYTES);
+                    tma_load_3d(base + S::OFF_V + s * S::TILE_BYTES, &p.tmV, bar(S::B_VFULL + s), kt * kTile, 0, bh);
+                }
+                if (!ok) {
+                    if (next_tile(2, -1) < p.Tk) f8_drain_wait(bar(S::B_QFULL), 0);
+                    for (int i = (u > S::STAGES ? u - S::STAGES : 0); i < u; ++i) {
+                        const int s = i % S::STAGES;
+                        const uint32_t ph = (uint32_t)(i / S::STAGES) & 1u;
+                        f8_drain_wait(bar(S::B_KFULL + s), ph);
+                        f8_drain_wait(bar(S::B_VFULL + s), ph);
+                    }
+                }
+            }
+        } else if (warp == 1) {
+            // ---------------------------------------------------------- MMA issuer
+            if (lane == 0) {
+                constexpr uint32_t IDESC_S = idesc_e4m3(128, 128);
+                constexpr uint32_t IDESC_PV = idesc_e4m3(128, D);
+                // all operands K-major, 128-byte rows: 32 bytes (32 e4m3) per K step
+                const uint64_t dq0 = sdesc_sw128(base + S::OFF_Q, 16, 1024);
+                const uint64_t dk0 = sdesc_sw128(base + S::OFF_K, 16, 1024);
+                const uint64_t dv0 = sdesc_sw128(base + S::OFF_V, 16, 1024);
+                const uint64_t dp0 = sdesc_sw128(base + S::OFF_P, 16, 1024);
+                int nv[2] = {0, 0};     // P.V products issued per query tile
+                int ns[2] = {0, 0};     // S products issued per query tile
+                bool ok = true;
+                auto issue_s = [&](int x, int s) {
+                    const uint32_t d_tmem = tmem + S::TM_S + 128u * (uint32_t)x;
+                    const uint64_t qd = sdesc_add(dq0, (uint32_t)(x * S::TILE_BYTES));
+                    const uint64_t kd = sdesc_add(dk0, (uint32_t)(s * S::TILE_BYTES));
+#pragma unroll
+                    for (int k = 0; k < D / 32; ++k)
+                        mma_ss_f8(d_tmem, sdesc_add(qd, 32u * k), sdesc_add(kd, 32u * k), IDESC_S, k > 0 ? 1u : 0u);
+                    mma_commit(bar(S::B_SFULL + x));
+                    ++ns[x];
+                };
+                int kt = next_tile(2, -1);
+                if (kt < p.Tk) {
+                    ok = mbar_wait(bar(S::B_QFULL), 0, g, 0x211) && mbar_wait(bar(S::B_KFULL + 0), 0, g, 0x212);
+                    if (ok) {
+                        tc_fence_after();
+                        for (int x = 0; x < 2; ++x)
+                            if (cls(x, kt) != kTileSkip) issue_s(x, 0);
+                    }
+                }
+                int u = 0;
+                while (ok && kt < p.Tk) {
+                    const int s = u % S::STAGES;
+                    // the next key tile's S_x, as soon as softmax x holds S_x(i)
+                    const int kt_next = next_tile(2, kt);
+                    if (kt_next < p.Tk) {
+                        const int s2 = (u + 1) % S::STAGES;
+                        if (!mbar_wait(bar(S::B_KFULL + s2), (uint32_t)((u + 1) / S::STAGES) & 1u, g, 0x213)) {
+                            ok = false;
+                            break;
+                        }
+                        for (int x = 0; x < 2 && ok; ++x) {
+                            if (cls(x, kt_next) == kTileSkip) continue;
+                            if (ns[x] > 0 && !mbar_wait(bar(S::B_SFREE + x), (uint32_t)(ns[x] - 1) & 1u, g, 0x214)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            issue_s(x, s2);
+                        }
+                        if (!ok) break;
+                    }
+                    // O_x += P_x V for both query tiles
+                    bool vwaited = false;
+                    for (int x = 0; x < 2 && ok; ++x) {
+                        if (cls(x, kt) == kTileSkip) continue;
+                        if (!mbar_wait(bar(S::B_PFULL + x), (uint32_t)nv[x] & 1u, g, 0x215) ||
+                            (!vwaited && !mbar_wait(bar(S::B_VFULL + s), (uint32_t)(u / S::STAGES) & 1u, g, 0x216))) {
+                            ok = false;
+                            break;
+                        }
+                        vwaited = true;
+                        tc_fence_after();
+                        const int pb = nv[x] & 1;
+                        const uint64_t pd = sdesc_add(dp0, (uint32_t)((2 * x + pb) * S::TILE_BYTES));
+                        const uint64_t vd = sdesc_add(dv0, (uint32_t)(s * S::TILE_BYTES));
+                        const uint32_t o_tmem = tmem + S::TM_O + (uint32_t)(D * x);
+                        const uint32_t acc0 = nv[x] > 0 ? 1u : 0u;
+#pragma unroll
+                        for (int k = 0; k < kTile / 32; ++k)
+                            mma_ss_f8(o_tmem, sdesc_add(pd, 32u * k), sdesc_add(vd, 32u * k), IDESC_PV,
+                                      k > 0 ? 1u : acc0);
+                        mma_commit(bar(S::B_PVDONE + x));
+                        mma_commit(bar(S::B_PFREE + 2 * x + pb));
+                        ++nv[x];
+                    }
+                    if (!ok) break;
+                    mma_commit(bar(S::B_KVEMPTY + s));
+                    kt = kt_next;
+                    ++u;
+                }
+                mma_commit(bar(S::B_FIN));
+                f8_drain_wait(bar(S::B_FIN), 0);
+            }
+        }
+    } else {
+        setmaxnreg_inc<S::REGS_SOFTMAX>();
+        // ---------------------------------------------------------- softmax of query tile x
+        const int x = (warp - 4) >> 2;
+        const int wq = warp & 3;
+        const int r = wq * 32 + lane;
+        const int q = q0[x] + r;
+        const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        const uint32_t s_tmem = tmem + lane_off + S::TM_S + 128u * (uint32_t)x;
+        const uint32_t o_tmem = tmem + lane_off + S::TM_O + (uint32_t)(D * x);
+        // this thread's row of the P buffers (128-byte swizzle: 16-byte unit
+        // c of row r sits at unit c ^ (r % 8))
+        uint8_t *prow = sb + S::OFF_P + (2 * x) * S::TILE_BYTES + (r >> 3) * 1024 + (r & 7) * 128;
+        const int sw = r & 7;
+        const float c2 = p.scale_log2;
+        float m_ref = -INFINITY, l = 0.f;
+        float sq = 1.f;
+        if (qn[x] > 0) sq = p.sQ[(size_t)bh * p.Tq + 2 * pq + x];
+        float mv = 0.f;
+        for (int k = lane; k < p.Tk; k += 32) mv = fmaxf(mv, p.sV[(size_t)bh * p.Tk + k]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, o));
+        const float sv_max = mv, inv_sv_max = mv > 0.f ? 1.f / mv : 0.f;
+        int it = 0;
+        bool ok = true;
+        // per-tile block scales, loaded one tile ahead so their latency hides
+        // behind the previous tile's work
+        const float *sKh = p.sK + (size_t)bh * p.Tk, *sVh = p.sV + (size_t)bh * p.Tk;
+        int kt = next_tile(x, -1);
+        float sk_n = 0.f, sv_n = 0.f;
+        if (kt < p.Tk) {
+            sk_n = sKh[kt];
+            sv_n = sVh[kt];
+        }
+        for (; kt < p.Tk; ++it) {
+            const bool partial = cls(x, kt) == kTilePartial;
+            const int k0 = kt * kTile;
+            const int kt_next = next_tile(x, kt);
+            // multiplier of this tile's scores; V-scale ratio rt folded into
+            // the exponent (p * rt = 2^(x - m + log2 rt)), and l takes the
+            // tile's sum back divided by rt.  rt = 0 only for an all-zero V
+            // block, whose codes make P irrelevant: there p itself is stored.
+            const float ct = c2 * sq * sk_n;
+            const float rt = sv_n * inv_sv_max;
+            const float lg = rt > 0.f ? __log2f(rt) : 0.f;
+            const float inv_rt = rt > 0.f ? 1.f / rt : 1.f;
+            if (kt_next < p.Tk) {
+                sk_n = sKh[kt_next];
+                sv_n = sVh[kt_next];
+            }
+            if (!mbar_wait_warp(bar(S::B_SFULL + x), (uint32_t)it & 1u, g, 0x411)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t sr[4][32];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) tmem_ld32(s_tmem + 32u * j, sr[j]);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) tmem_ld_wait(sr[j]);
+            // S_x is in registers: the next tile's S_x may overwrite it
+            tc_fence_before();
+            mbar_arrive(bar(S::B_SFREE + x));
+            if (partial) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) {
+                        const int key = k0 + 32 * j + t;
+                        if (key >= kvis || (p.causal && key > q)) sr[j][t] = __float_as_uint(-INFINITY);
+                    }
+            }
+            float pm[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) pm[u] = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int t = 0; t < 32; t += 4) {
+                    const int u = (j * 8 + t / 4) & 7;
+                    pm[u] = fmax3(pm[u], __uint_as_float(sr[j][t]), __uint_as_float(sr[j][t + 1]));
+                    pm[u] = fmax3(pm[u], __uint_as_float(sr[j][t + 2]), __uint_as_float(sr[j][t + 3]));
+                }
+            const float mx = fmaxf(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], fmax3(pm[5], pm[6], pm[7])));
+            const float m_tile = mx * ct;
+            const bool grow = m_tile > m_ref + kRescaleLog2F8;
+            float alpha = 1.f;
+            const bool rescale = __any_sync(0xffffffffu, grow);
+            if (rescale) {
+                const float m_new = fmaxf(m_ref, m_tile);
+                alpha = (m_new == -INFINITY) ? 1.f : ex2(m_ref - m_new);
+                l *= alpha;
+                m_ref = m_new;
+            }
+            const float m_use = ((m_ref == -INFINITY) ? 0.f : m_ref) - lg;
+            // the P buffer of this tile was last read by the P.V two tiles back
+            const int pb = it & 1;
+            if (it >= 2 &&
+                !mbar_wait_warp(bar(S::B_PFREE + 2 * x + pb), (uint32_t)((it >> 1) - 1) & 1u, g, 0x412)) {
+                ok = false;
+                break;
+            }
+            uint8_t *pdst = prow + pb * S::TILE_BYTES;
+            float ps[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) ps[u] = 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint32_t pk[8];
+#pragma unroll
+                for (int t = 0; t < 8; ++t) {
+                    float a0, a1, a2, a3;
+                    fma2(a0, a1, __uint_as_float(sr[j][4 * t]), __uint_as_float(sr[j][4 * t + 1]), ct, ct, -m_use,
+                         -m_use);
+                    fma2(a2, a3, __uint_as_float(sr[j][4 * t + 2]), __uint_as_float(sr[j][4 * t + 3]), ct, ct, -m_use,
+                         -m_use);
+                    a0 = ex2(a0);
+                    a1 = ex2(a1);
+                    a2 = ex2(a2);
+                    a3 = ex2(a3);
+                    add2(ps[2 * (t & 3)], ps[2 * (t & 3) + 1], a0, a1);
+                    add2(ps[2 * ((t + 2) & 3)], ps[2 * ((t + 2) & 3) + 1], a2, a3);
+                    pk[t] = pack_e4m3x4(a0, a1, a2, a3);
+                }
+                // keys 32j .. 32j+31 are 16-byte units 2j and 2j+1 of the row
+                *reinterpret_cast<uint4 *>(pdst + (((2 * j) ^ sw) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                *reinterpret_cast<uint4 *>(pdst + (((2 * j + 1) ^ sw) << 4)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            }
+            l += (((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]))) * inv_rt;
+            if (rescale && it > 0) {
+                // O_x may be rescaled only once the previous P.V has landed
+                if (!mbar_wait_warp(bar(S::B_PVDONE + x), (uint32_t)(it - 1) & 1u, g, 0x413)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int j0 = 0; j0 < D / 32; j0 += 4) {
+                    uint32_t o[4][32];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) tmem_ld32(o_tmem + 32u * (j0 + j), o[j]);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) tmem_ld_wait(o[j]);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+#pragma unroll
+                        for (int t = 0; t < 32; t += 2) {
+                            float a, bb;
+                            fma2(a, bb, __uint_as_float(o[j][t]), __uint_as_float(o[j][t + 1]), alpha, alpha, 0.f, 0.f);
+                            o[j][t] = __float_as_uint(a);
+                            o[j][t + 1] = __float_as_uint(bb);
+                        }
+                        tmem_st32(o_tmem + 32u * (j0 + j), o[j]);
+                    }
+                }
+                tmem_st_wait();
+            }
+            // P rows (generic-proxy stores) must be visible to the tensor core
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar(S::B_PFULL + x));
+            kt = kt_next;
+        }
+        // ---------------------------------------------------------- epilogue
+        if (ok && it > 0) {
+            ok = mbar_wait_warp(bar(S::B_PVDONE + x), (uint32_t)(it - 1) & 1u, g, 0x414);
+            tc_fence_after();
+        }
+        if (ok) {
+            const float inv_l = (l > 0.f) ? sv_max / l : 0.f;
+            __nv_bfloat16 *orow = reinterpret_cast<__nv_bfloat16 *>(p.O) + ((size_t)bh * p.N + q) * D;
+#pragma unroll 1
+            for (int j = 0; j < D / 32; ++j) {
+                uint32_t o[32];
+                if (it > 0) {
+                    tmem_ld32(o_tmem + 32u * j, o);
+                    tmem_ld_wait(o);
+                } else {
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) o[t] = 0u;
+                }
+                uint32_t w[16];
+#pragma unroll
+                for (int t = 0; t < 16; ++t)
+                    w[t] = pack_bf16x2(__uint_as_float(o[2 * t]) * inv_l, __uint_as_float(o[2 * t + 1]) * inv_l);
+                if (r < qn[x]) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * j);
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) dst[t] = make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
+                }
+            }
+            if (r < qn[x])
+                p.LSE[(size_t)bh * p.N + q] = (l > 0.f) ? (m_ref + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+        }
+        __syncwarp();
+        setmaxnreg_dec<S::REGS_CTRL>();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, S::TMEM_COLS);
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_fp8(const FwdParams &p, cudaStream_t st) {
+    const int smem = F8Shape::SMEM_BYTES;
+    cudaError_t e = cudaFuncSetAttribute(fa_fwd_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    const unsigned grid = (unsigned)((p.Tq + 1) / 2) * (unsigned)p.BH;
+    fa_fwd_fp8_kernel<<<grid, F8Shape::THREADS, smem, st>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace fa

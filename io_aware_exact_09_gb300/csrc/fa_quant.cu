@@ -11,7 +11,8 @@
 //
 // One CTA per (b*h, block): 256 threads load the block with 16-byte loads,
 // reduce amax, and write the codes (row layout: 8 bytes per thread per
-// vector; transposed: through a shared-memory tile, 128-byte rows out).
+// vector; transposed: the block is staged in shared memory and each thread
+// writes 32 consecutive codes of one row of V^T).
 // HBM-bound: 2 bytes read and 1 written per element.
 #include <cuda_bf16.h>
 
@@ -22,15 +23,15 @@ namespace fa {
 
 namespace {
 
-template <int D>
+template <int D, bool TRANSPOSE>
 __global__ void __launch_bounds__(256) fa_quant_fp8_kernel(const __nv_bfloat16 *__restrict__ X,
                                                            uint8_t *__restrict__ Y, float *__restrict__ scales,
-                                                           int N, int T, int Np, int transpose) {
+                                                           int N, int T, int Np) {
     constexpr int VPR = D / 8;                 // 16-byte vectors per row
     constexpr int NV = 128 * VPR / 256;        // vectors per thread
-    constexpr int TS = 128 + 16;               // transposed staging row stride (bytes)
     __shared__ float red[8];
-    __shared__ __align__(16) uint8_t tr[D * TS];
+    // transposed path: the bf16 block, read back column by column
+    __shared__ __align__(16) __nv_bfloat16 blk[TRANSPOSE ? 128 * D : 8];
     const int bh = (int)(blockIdx.x / T), t = (int)(blockIdx.x % T);
     const int r0 = t * 128;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -46,6 +47,7 @@ __global__ void __launch_bounds__(256) fa_quant_fp8_kernel(const __nv_bfloat16 *
         const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) amax = fmaxf(amax, fmaxf(fabsf(bf16lo(w[k])), fabsf(bf16hi(w[k]))));
+        if constexpr (TRANSPOSE) reinterpret_cast<uint4 *>(blk)[idx] = v[i];
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
@@ -56,39 +58,37 @@ __global__ void __launch_bounds__(256) fa_quant_fp8_kernel(const __nv_bfloat16 *
     for (int k = 1; k < 8; ++k) amax = fmaxf(amax, red[k]);
     const float scale = amax > 0.f ? __fdiv_rn(amax, 448.f) : 0.f;
     if (tid == 0) scales[blockIdx.x] = scale;
+    auto q = [&](float x) { return scale > 0.f ? __fdiv_rn(x, scale) : 0.f; };
 
+    if constexpr (!TRANSPOSE) {
 #pragma unroll
-    for (int i = 0; i < NV; ++i) {
-        const int idx = tid + 256 * i, row = idx / VPR, cv = idx % VPR;
-        const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-        float f[8];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            f[2 * k] = scale > 0.f ? __fdiv_rn(bf16lo(w[k]), scale) : 0.f;
-            f[2 * k + 1] = scale > 0.f ? __fdiv_rn(bf16hi(w[k]), scale) : 0.f;
-        }
-        const uint32_t c0 = pack_e4m3x4(f[0], f[1], f[2], f[3]);
-        const uint32_t c1 = pack_e4m3x4(f[4], f[5], f[6], f[7]);
-        if (!transpose) {
+        for (int i = 0; i < NV; ++i) {
+            const int idx = tid + 256 * i, row = idx / VPR, cv = idx % VPR;
+            const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+            const uint32_t c0 = pack_e4m3x4(q(bf16lo(w[0])), q(bf16hi(w[0])), q(bf16lo(w[1])), q(bf16hi(w[1])));
+            const uint32_t c1 = pack_e4m3x4(q(bf16lo(w[2])), q(bf16hi(w[2])), q(bf16lo(w[3])), q(bf16hi(w[3])));
             if (r0 + row < N)
                 *reinterpret_cast<uint2 *>(Y + ((size_t)bh * N + r0 + row) * D + cv * 8) = make_uint2(c0, c1);
-        } else {
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                tr[(cv * 8 + k) * TS + row] = (uint8_t)(c0 >> (8 * k));
-                tr[(cv * 8 + 4 + k) * TS + row] = (uint8_t)(c1 >> (8 * k));
-            }
         }
-    }
-    if (transpose) {
-        __syncthreads();
-        // column c of the block -> 128 bytes of row c of V^T, in 16-byte pieces
-        for (int idx = tid; idx < D * 8; idx += 256) {
-            const int c = idx >> 3, piece = idx & 7;
-            const int col = r0 + piece * 16;
-            if (col < Np)
-                *reinterpret_cast<uint4 *>(Y + ((size_t)bh * D + c) * Np + col) =
-                    *reinterpret_cast<const uint4 *>(tr + c * TS + piece * 16);
+    } else {
+        // task (column c, 32-row segment): 32 codes = 32 contiguous bytes of
+        // row c of V^T; a warp covers 32 consecutive columns, so its shared
+        // reads are 64 contiguous bytes per row
+        constexpr int TASKS = D * 4;
+#pragma unroll 1
+        for (int task = tid; task < TASKS; task += 256) {
+            const int c = task % D, seg = task / D;
+            uint32_t w[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int rr = seg * 32 + 4 * k;
+                w[k] = pack_e4m3x4(q(__bfloat162float(blk[(rr + 0) * D + c])), q(__bfloat162float(blk[(rr + 1) * D + c])),
+                                   q(__bfloat162float(blk[(rr + 2) * D + c])), q(__bfloat162float(blk[(rr + 3) * D + c])));
+            }
+            const int col = r0 + seg * 32;
+            uint8_t *dst = Y + ((size_t)bh * D + c) * Np + col;
+            if (col < Np) *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+            if (col + 16 < Np) *reinterpret_cast<uint4 *>(dst + 16) = make_uint4(w[4], w[5], w[6], w[7]);
         }
     }
 }
@@ -100,12 +100,19 @@ cudaError_t launch_quant_fp8(int d, const void *X, void *Y, float *scales, int B
     const int T = (N + 127) / 128;
     const int Np = (N + 15) / 16 * 16;
     const unsigned grid = (unsigned)BH * (unsigned)T;
-    if (d == 64)
-        fa_quant_fp8_kernel<64><<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16 *>(X),
-                                                      static_cast<uint8_t *>(Y), scales, N, T, Np, transpose);
-    else
-        fa_quant_fp8_kernel<128><<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16 *>(X),
-                                                       static_cast<uint8_t *>(Y), scales, N, T, Np, transpose);
+    const __nv_bfloat16 *x = static_cast<const __nv_bfloat16 *>(X);
+    uint8_t *y = static_cast<uint8_t *>(Y);
+    if (d == 64) {
+        if (transpose)
+            fa_quant_fp8_kernel<64, true><<<grid, 256, 0, st>>>(x, y, scales, N, T, Np);
+        else
+            fa_quant_fp8_kernel<64, false><<<grid, 256, 0, st>>>(x, y, scales, N, T, Np);
+    } else {
+        if (transpose)
+            fa_quant_fp8_kernel<128, true><<<grid, 256, 0, st>>>(x, y, scales, N, T, Np);
+        else
+            fa_quant_fp8_kernel<128, false><<<grid, 256, 0, st>>>(x, y, scales, N, T, Np);
+    }
     return cudaGetLastError();
 }
 
