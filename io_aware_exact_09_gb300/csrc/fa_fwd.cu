@@ -26,10 +26,10 @@
 //   - warp 0: TMA producer: both Q tiles once; K and V tiles through a ring
 //     of shared-memory stages (128-byte swizzle, 64-column boxes), over the
 //     union of the key tiles the two query tiles see;
-//   - warp 1: tcgen05 issuer: for each key tile, S_x = Q_x K^T for both query
-//     tiles x into TMEM (one buffer each), then O_x += P_x V with P_x read
-//     from TMEM (bf16, written over the first half of S_x).  The next tile's
-//     S_x is issued one key tile ahead, once P_x has been consumed;
+//   - warp 1: tcgen05 issuer: for each key tile and query tile x in turn,
+//     O_x += P_x V with P_x read from TMEM (bf16, written over the first half
+//     of S_x), then the next key tile's S_x = Q_x K^T as soon as that P.V
+//     has read P_x, before the other query tile's P.V is waited for;
 //   - warps 4-7 and 8-11: softmax of query tile 0 and 1, one row per thread
 //     (TMEM lane = row, warp w reads lane quadrant w % 4), with 208 registers
 //     each (setmaxnreg; warps 0-3 drop to 88).  The whole S row
@@ -264,40 +264,41 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                     int u = 0;
                     while (ok && kt < p.Tk) {
                         const int s = u % S::STAGES;
-                        bool vwaited = false;
-                        // O_x += P_x V for both query tiles
-                        for (int x = 0; x < 2 && ok; ++x) {
-                            if (cls(x, kt) == kTileSkip) continue;
-                            if (!mbar_wait(bar(S::B_PFULL + x), (uint32_t)nv[x] & 1u, g, 0x203) ||
-                                (!vwaited && !mbar_wait(bar(S::B_VFULL + s), (uint32_t)(u / S::STAGES) & 1u, g, 0x204))) {
-                                ok = false;
-                                break;
-                            }
-                            vwaited = true;
-                            tc_fence_after();
-                            const uint32_t p_tmem = tmem + S::TM_S + 128u * (uint32_t)x;
-                            const uint32_t o_tmem = tmem + S::TM_O + (uint32_t)(D * x);
-                            const uint64_t vd = sdesc_add(dv0, (uint32_t)(s * S::TILE_BYTES));
-                            const uint32_t acc0 = nv[x] > 0 ? 1u : 0u;
-#pragma unroll
-                            for (int k = 0; k < kTile / 16; ++k)
-                                mma_ts(o_tmem, p_tmem + (uint32_t)k * 8u, sdesc_add(vd, (uint32_t)k * 2048u), IDESC_PV,
-                                       k > 0 ? 1u : acc0);
-                            mma_commit(bar(S::B_PVDONE + x));
-                            ++nv[x];
-                        }
-                        if (!ok) break;
-                        mma_commit(bar(S::B_KVEMPTY + s));
-                        // the next key tile's S_x, once P_x of this one has been consumed
                         const int kt_next = next_tile(2, kt);
-                        if (kt_next < p.Tk) {
-                            const int s2 = (u + 1) % S::STAGES;
-                            if (!mbar_wait(bar(S::B_KFULL + s2), (uint32_t)((u + 1) / S::STAGES) & 1u, g, 0x205)) {
-                                ok = false;
-                                break;
+                        const int s2 = (u + 1) % S::STAGES;
+                        bool vwaited = false, kwaited = false;
+                        // per query tile: O_x += P_x V, then at once the next key
+                        // tile's S_x (it overwrites P_x, so it waits for that P.V),
+                        // so that each tile's chain S -> softmax -> P.V -> S moves
+                        // on without waiting for the other tile's P
+                        for (int x = 0; x < 2 && ok; ++x) {
+                            if (cls(x, kt) != kTileSkip) {
+                                if (!mbar_wait(bar(S::B_PFULL + x), (uint32_t)nv[x] & 1u, g, 0x203) ||
+                                    (!vwaited &&
+                                     !mbar_wait(bar(S::B_VFULL + s), (uint32_t)(u / S::STAGES) & 1u, g, 0x204))) {
+                                    ok = false;
+                                    break;
+                                }
+                                vwaited = true;
+                                tc_fence_after();
+                                const uint32_t p_tmem = tmem + S::TM_S + 128u * (uint32_t)x;
+                                const uint32_t o_tmem = tmem + S::TM_O + (uint32_t)(D * x);
+                                const uint64_t vd = sdesc_add(dv0, (uint32_t)(s * S::TILE_BYTES));
+                                const uint32_t acc0 = nv[x] > 0 ? 1u : 0u;
+#pragma unroll
+                                for (int k = 0; k < kTile / 16; ++k)
+                                    mma_ts(o_tmem, p_tmem + (uint32_t)k * 8u, sdesc_add(vd, (uint32_t)k * 2048u),
+                                           IDESC_PV, k > 0 ? 1u : acc0);
+                                mma_commit(bar(S::B_PVDONE + x));
+                                ++nv[x];
                             }
-                            for (int x = 0; x < 2 && ok; ++x) {
-                                if (cls(x, kt_next) == kTileSkip) continue;
+                            if (kt_next < p.Tk && cls(x, kt_next) != kTileSkip) {
+                                if (!kwaited && !mbar_wait(bar(S::B_KFULL + s2), (uint32_t)((u + 1) / S::STAGES) & 1u,
+                                                           g, 0x205)) {
+                                    ok = false;
+                                    break;
+                                }
+                                kwaited = true;
                                 if (nv[x] > 0 && !mbar_wait(bar(S::B_PVDONE + x), (uint32_t)(nv[x] - 1) & 1u, g, 0x206)) {
                                     ok = false;
                                     break;
@@ -306,6 +307,9 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                                 issue_s(x, s2);
                             }
                         }
+                        if (!ok) break;
+                        // K and V of stage s are free once this tile's products are done
+                        mma_commit(bar(S::B_KVEMPTY + s));
                         kt = kt_next;
                         ++u;
                     }
