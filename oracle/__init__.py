@@ -251,6 +251,40 @@ def attention_decode(Q, K, V, scale, causal=False, kv_len=None):
     return O, LSE
 
 
+def attention_varlen(Q, K, V, cu_q, cu_k, scale, causal=False):
+    """Ragged batch (packed sequences), fp64.
+
+    Q: [total_q, H, d], K, V: [total_k, H, d]; sequence b owns query rows
+    cu_q[b]..cu_q[b+1]-1 and key rows cu_k[b]..cu_k[b+1]-1.  Each sequence is
+    attended on its own; its Lq queries are the last Lq positions of its Lk
+    keys, so with causal query i sees key j iff j <= i + Lk - Lq (the decode
+    reading, bottom-right; Lq = Lk gives the square causal mask).  Returns
+    O [total_q, H, d] and LSE [H, total_q].  Each sequence goes through
+    attention_decode on its own slice."""
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    cu_q = np.asarray(cu_q, np.int64)
+    cu_k = np.asarray(cu_k, np.int64)
+    if Q.ndim != 3 or K.ndim != 3 or K.shape != V.shape or Q.shape[1:] != K.shape[1:]:
+        raise ValueError("expected Q [total_q, H, d] and K, V [total_k, H, d]")
+    if cu_q.shape != cu_k.shape or cu_q.ndim != 1 or cu_q[0] != 0 or cu_k[0] != 0 or \
+            cu_q[-1] != Q.shape[0] or cu_k[-1] != K.shape[0] or np.any(np.diff(cu_q) < 0) or np.any(np.diff(cu_k) < 0):
+        raise ValueError("cu_q / cu_k must be [B + 1] offsets from 0 to total, non-decreasing")
+    H, d = Q.shape[1], Q.shape[2]
+    O = np.zeros(Q.shape, np.float64)
+    LSE = np.full((H, Q.shape[0]), -np.inf, np.float64)
+    for b in range(len(cu_q) - 1):
+        q0, q1, k0, k1 = int(cu_q[b]), int(cu_q[b + 1]), int(cu_k[b]), int(cu_k[b + 1])
+        if q1 == q0:
+            continue
+        qb = np.ascontiguousarray(Q[q0:q1].transpose(1, 0, 2))[None]
+        kb = np.ascontiguousarray(K[k0:k1].transpose(1, 0, 2))[None]
+        vb = np.ascontiguousarray(V[k0:k1].transpose(1, 0, 2))[None]
+        ob, lb = attention_decode(qb, kb, vb, scale, causal=causal)
+        O[q0:q1] = ob[0].transpose(1, 0, 2)
+        LSE[:, q0:q1] = lb[0]
+    return O, LSE
+
+
 E4M3_MAX = 448.0
 FP8_BLOCK = 128
 

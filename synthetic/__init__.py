@@ -123,6 +123,75 @@ def decode_visible_keys(w: DecodeWorkload, kv_len=None) -> int:
     return w.H * sum(min(max(int(x), 0), w.Nk) for x in kv_len)
 
 
+@dataclass(frozen=True)
+class VarlenWorkload:
+    """A ragged batch of B packed sequences of H heads: query lengths drawn
+    U{lo..hi}; each sequence's keys are its queries (Lk = Lq) unless
+    k_extra_range adds a cached prefix (Lk = Lq + U{lo..hi})."""
+    name: str
+    B: int
+    H: int
+    d: int
+    seed: int
+    q_len_range: tuple
+    k_extra_range: Optional[tuple] = None
+    causal: bool = True
+    description: str = ""
+
+    @property
+    def softmax_scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+
+# Ragged batches (the pages name the layout, not sizes): a prefill batch of
+# 16 sequences of 256..4096 tokens, and a chunked-prefill batch whose new
+# chunks of 128..1024 tokens attend to cached prefixes of up to 8192 tokens.
+VARLEN_WORKLOADS = {
+    "varlen_prefill_b16h16d128": VarlenWorkload("varlen_prefill_b16h16d128", 16, 16, 128, 1007, (256, 4096),
+                                                description="16 sequences, lengths U{256..4096}, causal, d=128"),
+    "varlen_chunked_b16h16d128": VarlenWorkload("varlen_chunked_b16h16d128", 16, 16, 128, 1008, (128, 1024),
+                                                k_extra_range=(0, 8192),
+                                                description="16 chunks of U{128..1024} new tokens after cached "
+                                                            "prefixes of U{0..8192}, causal, d=128"),
+}
+
+
+def make_varlen_inputs(w: VarlenWorkload):
+    """Lengths first (query lengths, then prefix lengths), then Q [total_q, H, d]
+    and K, V [total_k, H, d] (bf16 from fp32 N(0, 1)); cu_q, cu_k int32 [B + 1]."""
+    gen = torch.Generator().manual_seed(w.seed)
+    lq = torch.randint(w.q_len_range[0], w.q_len_range[1] + 1, (w.B,), generator=gen, dtype=torch.int64)
+    lk = lq.clone()
+    if w.k_extra_range is not None:
+        lk = lk + torch.randint(w.k_extra_range[0], w.k_extra_range[1] + 1, (w.B,), generator=gen,
+                                dtype=torch.int64)
+    cu_q = torch.zeros(w.B + 1, dtype=torch.int32)
+    cu_k = torch.zeros(w.B + 1, dtype=torch.int32)
+    cu_q[1:] = torch.cumsum(lq, 0).to(torch.int32)
+    cu_k[1:] = torch.cumsum(lk, 0).to(torch.int32)
+    tq, tk = int(cu_q[-1]), int(cu_k[-1])
+    Q = to_bf16(torch.randn((tq, w.H, w.d), generator=gen, dtype=torch.float32))
+    K = to_bf16(torch.randn((tk, w.H, w.d), generator=gen, dtype=torch.float32))
+    V = to_bf16(torch.randn((tk, w.H, w.d), generator=gen, dtype=torch.float32))
+    return {"Q": Q, "K": K, "V": V, "cu_q": cu_q, "cu_k": cu_k, "max_q": int(lq.max()), "causal": w.causal,
+            "scale": w.softmax_scale}
+
+
+def varlen_fwd_flops(cu_q, cu_k, H, d, causal) -> float:
+    """4 * d * H * (number of visible (query, key) pairs), causal bottom-right."""
+    pairs = 0
+    for b in range(len(cu_q) - 1):
+        lq = int(cu_q[b + 1]) - int(cu_q[b])
+        lk = int(cu_k[b + 1]) - int(cu_k[b])
+        if not causal:
+            pairs += lq * lk
+        else:
+            sh = lk - lq
+            # query i sees min(lk, max(0, i + sh + 1)) keys
+            pairs += sum(min(lk, max(0, i + sh + 1)) for i in range(lq))
+    return 4.0 * d * H * pairs
+
+
 def to_bf16(x: torch.Tensor) -> torch.Tensor:
     """fp32 -> bf16 with round-to-nearest-even (torch's conversion)."""
     return x.to(torch.bfloat16)

@@ -436,3 +436,58 @@ def test_decode_split_keys_merge_to_the_whole():
         acc = st if acc is None else merge_blocks(*acc, *st)
     np.testing.assert_allclose(acc[2], O, atol=1e-12, rtol=0)
     np.testing.assert_allclose(acc[0] + np.log(acc[1]), L, atol=1e-12, rtol=0)
+
+
+def _packed(lens_q, lens_k, H, d, seed):
+    g = torch.Generator().manual_seed(seed)
+    tq, tk = sum(lens_q), sum(lens_k)
+    Q = torch.randn((tq, H, d), generator=g, dtype=torch.float64).numpy()
+    K = torch.randn((tk, H, d), generator=g, dtype=torch.float64).numpy()
+    V = torch.randn((tk, H, d), generator=g, dtype=torch.float64).numpy()
+    cu_q = np.concatenate([[0], np.cumsum(lens_q)]).astype(np.int32)
+    cu_k = np.concatenate([[0], np.cumsum(lens_k)]).astype(np.int32)
+    return Q, K, V, cu_q, cu_k
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_equals_square_oracle_per_sequence(causal):
+    """Lq = Lk: each packed sequence equals the square oracle on that sequence alone."""
+    lens = [5, 1, 17, 0, 9]
+    H, d = 2, 8
+    Q, K, V, cu_q, cu_k = _packed(lens, lens, H, d, seed=31)
+    O, L = oracle.attention_varlen(Q, K, V, cu_q, cu_k, 0.3, causal=causal)
+    for b, n in enumerate(lens):
+        if n == 0:
+            continue
+        sl = slice(cu_q[b], cu_q[b + 1])
+        tr = lambda X: X[sl].transpose(1, 0, 2)[None]
+        rO, rL = oracle.attention_fwd(tr(Q), tr(K), tr(V), 0.3, causal=causal)
+        assert np.max(np.abs(O[sl].transpose(1, 0, 2) - rO[0])) < 1e-12
+        assert np.max(np.abs(L[:, sl] - rL[0])) < 1e-12
+
+
+def test_varlen_matches_library_sdpa_with_bottom_right_mask():
+    """Lq < Lk (queries are the last positions): torch fp64 SDPA with the
+    bottom-right causal mask written out, sequence by sequence."""
+    lens_q, lens_k = [3, 7, 1], [10, 7, 4]
+    H, d = 3, 16
+    Q, K, V, cu_q, cu_k = _packed(lens_q, lens_k, H, d, seed=32)
+    O, L = oracle.attention_varlen(Q, K, V, cu_q, cu_k, 0.25, causal=True)
+    for b, (lq, lk) in enumerate(zip(lens_q, lens_k)):
+        q = torch.from_numpy(Q[cu_q[b]:cu_q[b + 1]].transpose(1, 0, 2).copy())
+        k = torch.from_numpy(K[cu_k[b]:cu_k[b + 1]].transpose(1, 0, 2).copy())
+        v = torch.from_numpy(V[cu_k[b]:cu_k[b + 1]].transpose(1, 0, 2).copy())
+        i = torch.arange(lq)[:, None]
+        j = torch.arange(lk)[None, :]
+        mask = j <= i + (lk - lq)
+        ref = torch.nn.functional.scaled_dot_product_attention(q, k, v, attn_mask=mask, scale=0.25)
+        got = O[cu_q[b]:cu_q[b + 1]].transpose(1, 0, 2)
+        assert np.max(np.abs(got - ref.numpy())) < 1e-12
+
+
+def test_varlen_rejects_bad_offsets():
+    Q, K, V, cu_q, cu_k = _packed([2, 3], [2, 3], 1, 4, seed=33)
+    with pytest.raises(ValueError):
+        oracle.attention_varlen(Q, K, V, cu_q[::-1], cu_k, 0.5)
+    with pytest.raises(ValueError):
+        oracle.attention_varlen(Q, K, V, cu_q, cu_k[:-1], 0.5)
