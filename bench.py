@@ -22,6 +22,10 @@ quantisation of Q, K and V (``fa_quantize_fp8``, three launches) and
 the FP8 forward kernel against the dense-FP8 peak (the measured sustained
 bf16 figure x 2, the nominal fp8 : bf16 ratio).
 
+``--workload varlen_...`` measures the ragged-batch forward (``fa_fwd_varlen``,
+packed sequences of uneven lengths): ``value`` is forward TFLOP/s over the
+visible (query, key) pairs.
+
 ``--workload decode_...`` measures the split-KV decode path instead: one step
 = one ``fa_decode`` call (a few new query rows per sequence against a
 resident key/value cache); ``value`` is GB/s of algorithmic traffic (Q, the
@@ -523,6 +527,134 @@ def run_fp8(args):
     return 0
 
 
+# ---------------------------------------------------------------- ragged batches
+def oracle_varlen_sample(w, budget_s: float):
+    """The fp64 oracle on sequence 0 of the ragged workload, one head, called
+    repeatedly for about budget_s: (TFLOP/s, cores, description)."""
+    import oracle
+    from synthetic import make_varlen_inputs, varlen_fwd_flops
+    c = make_varlen_inputs(w)
+    cq, ck = c["cu_q"].numpy(), c["cu_k"].numpy()
+    f = lambda X, a, b: X[a:b, 0:1].double().numpy().transpose(1, 0, 2)[None]
+    q, k, v = f(c["Q"], cq[0], cq[1]), f(c["K"], ck[0], ck[1]), f(c["V"], ck[0], ck[1])
+    fl = varlen_fwd_flops([0, cq[1] - cq[0]], [0, ck[1] - ck[0]], 1, w.d, w.causal)
+    dts = []
+    t_end = time.perf_counter() + budget_s
+    while not dts or time.perf_counter() < t_end:
+        t0 = time.perf_counter()
+        oracle.attention_decode(q, k, v, w.softmax_scale, causal=w.causal)
+        dts.append(time.perf_counter() - t0)
+    dt = sum(dts) / len(dts)
+    desc = ("fp64 oracle forward of sequence 0 (%d queries, %d keys), head 0, of %s, %d calls, %.3f s per call"
+            % (cq[1] - cq[0], ck[1] - ck[0], w.name, len(dts), dt))
+    return fl / dt / 1e12, oracle.num_threads(), desc
+
+
+def run_varlen(args, w):
+    import torch
+
+    ws_n, rank = init_dist("nccl")
+    _, _, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import io_aware_exact_09_gb300 as fa
+    from synthetic import make_varlen_inputs, varlen_fwd_flops
+    fa.build()
+    c = make_varlen_inputs(w)
+    Q, K, V = (c[k].to(dev).contiguous() for k in ("Q", "K", "V"))
+    cu_q, cu_k = c["cu_q"].to(dev), c["cu_k"].to(dev)
+    B, H, d = w.B, w.H, w.d
+    tq, tk = int(Q.shape[0]), int(K.shape[0])
+    O = torch.empty_like(Q)
+    LSE = torch.empty((H, tq), dtype=torch.float32, device=dev)
+    wsn = fa.fa_fwd_workspace_size(1, 1, 1, d)
+    ws = fa.workspace(wsn, dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    flops = varlen_fwd_flops(c["cu_q"].tolist(), c["cu_k"].tolist(), H, d, w.causal)
+
+    def check(st, where):
+        if st != 0:
+            raise RuntimeError("%s failed: %s" % (where, fa.fa_status_string(st)))
+
+    def step():
+        check(fa.fa_fwd_varlen(Q, K, V, O, LSE, cu_q, cu_k, B, H, tq, tk, c["max_q"], d, w.softmax_scale, w.causal,
+                               ws, wsn, sp), "fa_fwd_varlen")
+
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    check(fa.fa_get_device_status(ws, sp), "device status after warm-up")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    times = []
+    barrier()
+    torch.cuda.synchronize(dev)
+    for _ in range(args.steps):
+        flush.zero_()
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1))
+    torch.cuda.synchronize(dev)
+    barrier()
+    clk = clocks.stop()
+    check(fa.fa_get_device_status(ws, sp), "device status after timing")
+    ms = reduce_max(sum(times) / len(times), dev)
+    value = whole_job_tflops(flops, ws_n, ms / 1e3)
+    peaks, peak_src = measured_peaks()
+    peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    achieved = flops / (ms / 1e3) / 1e12
+    roofline = {"bound": "tensor", "kernel": "fa_fwd_kernel<%d, varlen>" % d, "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                "peak_source": "%s bf16_tflops_sustained" % peak_src}
+    e2e = None
+    if not args.no_e2e:
+        pin = lambda t: t.contiguous().pin_memory()
+        Qh, Kh, Vh = (pin(c[k]) for k in ("Q", "K", "V"))
+        Oh = torch.empty_like(Qh).pin_memory()
+        Lh = torch.empty((H, tq), dtype=torch.float32).pin_memory()
+        et = []
+        for i in range(1 + max(1, min(args.steps, 5))):
+            e0.record(stream)
+            Q.copy_(Qh, non_blocking=True)
+            K.copy_(Kh, non_blocking=True)
+            V.copy_(Vh, non_blocking=True)
+            step()
+            Oh.copy_(O, non_blocking=True)
+            Lh.copy_(LSE, non_blocking=True)
+            e1.record(stream)
+            e1.synchronize()
+            if i > 0:
+                et.append(e0.elapsed_time(e1))
+        e_ms = reduce_max(sum(et) / len(et), dev)
+        e2e = {"value": whole_job_tflops(flops, ws_n, e_ms / 1e3), "unit": "TFLOP/s",
+               "h2d_bytes_per_step": (tq + 2 * tk) * H * d * 2, "d2h_bytes_per_step": tq * H * d * 2 + H * tq * 4,
+               "ms_per_step": e_ms, "note": "cu_seqlens stay resident"}
+    cpu = None
+    if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
+        tf, cores, desc = oracle_varlen_sample(w, args.cpu_budget)
+        cpu = {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc}
+    if rank == 0:
+        line = {
+            "metric": "attention fwd TFLOP/s (bf16, ragged batch)", "value": value, "unit": "TFLOP/s",
+            "n_gpus": ws_n, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "B": B, "H": H, "d": d, "total_q": tq, "total_k": tk,
+                       "max_seqlen_q": c["max_q"], "causal": w.causal,
+                       "parallelism": "replicas" if ws_n > 1 else "single", "l2": "flushed between steps"},
+            "algorithmic_flops_per_step": flops, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "clocks": clk, "gpu_launches": args.steps,
+        }
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 # ---------------------------------------------------------------- reference arm
 def run_reference_decode(args, w):
     import oracle
@@ -551,9 +683,28 @@ def run_reference(args):
     ws, rank = init_dist("gloo")
     if rank != 0:
         return 0
-    from synthetic import DECODE_WORKLOADS, WORKLOADS
+    from synthetic import DECODE_WORKLOADS, VARLEN_WORKLOADS, WORKLOADS
     if args.workload in DECODE_WORKLOADS:
         return run_reference_decode(args, DECODE_WORKLOADS[args.workload])
+    if args.workload in VARLEN_WORKLOADS:
+        w = VARLEN_WORKLOADS[args.workload]
+        import oracle
+        oracle.build()
+        vals = []
+        for i in range(args.warmup + args.steps):
+            tf, cores, desc = oracle_varlen_sample(w, 3.0)
+            if i >= args.warmup:
+                vals.append(tf)
+        v = statistics.median(vals)
+        print(json.dumps({"impl": "reference", "metric": "attention fwd TFLOP/s (bf16, ragged batch)", "value": v,
+                          "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                          "data": "synthetic", "config": {"workload": w.name, "B": w.B, "H": w.H, "d": w.d},
+                          "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                                           "sample": desc},
+                          "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+                          "gpu_launches": 0}), flush=True)
+        return 0
     import oracle
     oracle.build()
     w = WORKLOADS[args.workload]
@@ -756,9 +907,11 @@ def main(argv=None):
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
-    from synthetic import DECODE_WORKLOADS
+    from synthetic import DECODE_WORKLOADS, VARLEN_WORKLOADS
     if args.workload in DECODE_WORKLOADS:
         return run_decode(args, DECODE_WORKLOADS[args.workload])
+    if args.workload in VARLEN_WORKLOADS:
+        return run_varlen(args, VARLEN_WORKLOADS[args.workload])
     if args.fp8:
         return run_fp8(args)
     return run_ours(args)

@@ -92,6 +92,29 @@ fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LS
                  void *stream);
 
 /*
+ * Forward of a ragged batch ("Attention" chapter, serving paragraph: the
+ * ragged layouts inference engines keep their sequences in): B sequences of
+ * different lengths packed one after another.  Q, O: device bf16
+ * [total_q, H, d]; K, V: device bf16 [total_k, H, d]; LSE: device fp32
+ * [H, total_q] (natural log).  cu_seqlens_q, cu_seqlens_k: device int32
+ * [B + 1], non-decreasing offsets from 0 to total_q / total_k: sequence b
+ * owns query rows cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 and key rows
+ * cu_seqlens_k[b] .. cu_seqlens_k[b+1]-1.  max_seqlen_q (host): at least the
+ * longest query length (it sizes the grid).  Lq queries of a sequence are its
+ * last Lq positions among its Lk keys (a cached prefix when Lk > Lq): with
+ * causal != 0 query i sees key j iff j <= i + Lk - Lq.  A row that sees no
+ * key gets O = 0, LSE = -inf.  Offsets outside [0, total], a negative length
+ * or a query length beyond the grid max_seqlen_q sizes (rounded up to whole
+ * 128-row tiles): that sequence is skipped and FA_ERR_DEVICE_BAD_KEY_LEN is
+ * recorded in the workspace status word.
+ * Workspace: fa_fwd_workspace_size(1, 1, 1, d) bytes.  One kernel launch.
+ */
+fa_status fa_fwd_varlen(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                        const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int B, int H,
+                        int total_q, int total_k, int max_seqlen_q, int d, float softmax_scale,
+                        int causal, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * FP8 block quantisation ("FlashAttention: Mathematical Foundations ...",
  * section "Architectural Evolution", FlashAttention-3 paragraph:
  * block-quantised FP8 matmuls with dynamic scaling).  X: device bf16

@@ -75,6 +75,8 @@ def lib():
             L.fa_decode_workspace_size.restype = sz
             L.fa_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, i, vp, sz, vp]
             L.fa_decode.restype = i
+            L.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, sz, vp]
+            L.fa_fwd_varlen.restype = i
             L.fa_quantize_fp8.argtypes = [vp, vp, vp, i, i, i, i, i, vp]
             L.fa_quantize_fp8.restype = i
             L.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp, vp, sz, vp]
@@ -96,7 +98,8 @@ def lib():
 
 EXPORTED = ("fa_tile_size", "fa_fwd_workspace_size", "fa_bwd_workspace_size", "fa_fwd", "fa_bwd",
             "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_postprocess", "fa_bwd_noalloc",
-            "fa_decode_workspace_size", "fa_decode", "fa_quantize_fp8", "fa_fwd_fp8", "fa_tile_plan",
+            "fa_decode_workspace_size", "fa_decode", "fa_fwd_varlen", "fa_quantize_fp8", "fa_fwd_fp8",
+            "fa_tile_plan",
             "fa_host_workspace_size", "fa_attention_host", "fa_get_device_status", "fa_reset_device_status",
             "fa_status_string")
 
@@ -147,6 +150,32 @@ def fa_fwd(Q, K, V, O, LSE, B, H, N, d, softmax_scale, causal, key_len, block_ma
     return lib().fa_fwd(_p(Q), _p(K), _p(V), _p(O), _p(LSE), B, H, N, d, float(softmax_scale),
                         int(bool(causal)), _p(key_len), _p(block_mask), _p(workspace),
                         int(workspace_bytes), _stream(stream))
+
+
+def fa_fwd_varlen(Q, K, V, O, LSE, cu_seqlens_q, cu_seqlens_k, B, H, total_q, total_k, max_seqlen_q, d,
+                  softmax_scale, causal, workspace, workspace_bytes, stream=None) -> int:
+    return lib().fa_fwd_varlen(_p(Q), _p(K), _p(V), _p(O), _p(LSE), _p(cu_seqlens_q), _p(cu_seqlens_k), B, H,
+                               total_q, total_k, max_seqlen_q, d, float(softmax_scale), int(bool(causal)),
+                               _p(workspace), int(workspace_bytes), _stream(stream))
+
+
+def attention_varlen(Q, K, V, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, softmax_scale=None, causal=False,
+                     ws=None, stream=None, check_status=False):
+    """O [total_q, H, d], LSE [H, total_q] = fa_fwd_varlen(...) on bf16 CUDA tensors."""
+    import torch
+    total_q, H, d = (int(x) for x in Q.shape)
+    total_k = int(K.shape[0])
+    B = int(cu_seqlens_q.numel()) - 1
+    scale = (1.0 / d ** 0.5) if softmax_scale is None else softmax_scale
+    O = torch.empty_like(Q)
+    LSE = torch.empty((H, total_q), dtype=torch.float32, device=Q.device)
+    if ws is None:
+        ws = workspace(fa_fwd_workspace_size(1, 1, 1, d), Q.device)
+    _check(fa_fwd_varlen(Q, K, V, O, LSE, cu_seqlens_q, cu_seqlens_k, B, H, total_q, total_k, max_seqlen_q, d,
+                         scale, causal, ws, ws.numel(), stream), "fa_fwd_varlen")
+    if check_status:
+        _check(fa_get_device_status(ws, stream), "fa_fwd_varlen (device)")
+    return O, LSE
 
 
 def fa_quantize_fp8(X, X8, scales, B, H, N, d, transpose, stream=None) -> int:

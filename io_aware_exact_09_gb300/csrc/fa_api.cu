@@ -59,6 +59,20 @@ bool encode_bf16_3d(CUtensorMap *m, const void *ptr, int d, int N, int BH, int b
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D view [total][H][d] of packed (ragged-batch) bf16 rows: box of 64
+// columns of one head x box_rows rows, 128-byte swizzle.
+bool encode_bf16_thd(CUtensorMap *m, const void *ptr, int d, int H, int total, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)total};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 3-D byte view [outer][rows][inner] of e4m3 codes; box of 128 bytes x
 // box_rows rows, 128-byte swizzle (FP8 Q, K: inner = d = 128; V^T: inner =
 // Np, rows = d).
@@ -173,6 +187,48 @@ fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LS
     p.causal = causal ? 1 : 0;
     p.scale_log2 = softmax_scale * kLog2e;
     return fa::launch_fwd(d, p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_fwd_varlen(const void *Q, const void *K, const void *V, void *O, float *LSE, const int32_t *cu_seqlens_q,
+                        const int32_t *cu_seqlens_k, int B, int H, int total_q, int total_k, int max_seqlen_q, int d,
+                        float softmax_scale, int causal, void *workspace, size_t workspace_bytes, void *stream) {
+    if (B < 0 || H <= 0 || total_q < 0 || total_k < 0 || max_seqlen_q < 0) return FA_ERR_INVALID_ARGUMENT;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (!scale_ok(softmax_scale)) return FA_ERR_INVALID_ARGUMENT;
+    if (B == 0 || total_q == 0 || max_seqlen_q == 0) return FA_OK;
+    const int64_t Tq = ((int64_t)max_seqlen_q + 127) / 128;
+    if ((int64_t)B * H > INT_MAX || (Tq + 1) / 2 * (int64_t)B * H > INT_MAX) return FA_ERR_UNSUPPORTED;
+    if ((int64_t)total_q * H * d * 2 >= (int64_t(1) << 40) || (int64_t)total_k * H * d * 2 >= (int64_t(1) << 40))
+        return FA_ERR_UNSUPPORTED;
+    if (!Q || !O || !LSE || !cu_seqlens_q || !cu_seqlens_k || !aligned16(Q) || !aligned16(O) || !aligned16(LSE))
+        return FA_ERR_INVALID_ARGUMENT;
+    if (total_k > 0 && (!K || !V || !aligned16(K) || !aligned16(V))) return FA_ERR_INVALID_ARGUMENT;
+    if (!workspace || !aligned16(workspace) || workspace_bytes < fa_fwd_workspace_size(1, 1, 1, d))
+        return FA_ERR_WORKSPACE;
+    FwdParams p;
+    std::memset(&p, 0, sizeof(p));
+    // a sequence without keys still needs valid maps: point K, V at Q then
+    // (no key tile is ever loaded for it)
+    const void *Km = total_k > 0 ? K : Q, *Vm = total_k > 0 ? V : Q;
+    const int tk = total_k > 0 ? total_k : total_q;
+    if (!encode_bf16_thd(&p.tmQ, Q, d, H, total_q, 128) || !encode_bf16_thd(&p.tmK, Km, d, H, tk, 128) ||
+        !encode_bf16_thd(&p.tmV, Vm, d, H, tk, 128))
+        return FA_ERR_CUDA;
+    p.O = O;
+    p.LSE = LSE;
+    p.cu_q = cu_seqlens_q;
+    p.cu_k = cu_seqlens_k;
+    p.total_q = total_q;
+    p.total_k = total_k;
+    p.status = static_cast<unsigned *>(workspace);
+    p.H = H;
+    p.N = 0;
+    p.BH = B * H;
+    p.Tq = (int)Tq;
+    p.Tk = 0;
+    p.causal = causal ? 1 : 0;
+    p.scale_log2 = softmax_scale * kLog2e;
+    return fa::launch_fwd_varlen(d, p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 fa_status fa_quantize_fp8(const void *X, void *X8, float *scales, int B, int H, int N, int d, int transpose,

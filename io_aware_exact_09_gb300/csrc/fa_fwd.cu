@@ -38,6 +38,12 @@
 //     the end, the epilogue O / l -> bf16, LSE = (m + log2 l) * ln 2.
 // Skipped tiles (block mask zero, all keys past key_len, above the causal
 // diagonal) are never loaded; partial tiles get element masks.
+//
+// Ragged batches (VARLEN): sequences of different lengths packed one after
+// another, [total][H][d]; the grid covers the longest sequence and CTAs past
+// a shorter one's end have nothing to do.  A sequence's Lq queries are its
+// last positions among its Lk keys (a cached prefix, or Lq = Lk for a plain
+// prefill), so the causal diagonal is shifted by Lk - Lq.
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
 
@@ -86,7 +92,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
         if (globaltimer_ns() - t0 > FA_WAIT_TIMEOUT_NS) break;
 }
 
-template <int D>
+template <int D, bool VARLEN>
 __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
     using S = FwdShape<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -100,22 +106,49 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
     const int Tp = (p.Tq + 1) / 2;
     const int pq = Tp - 1 - (int)(blockIdx.x % Tp);
     const int bh = (int)(blockIdx.x / Tp);
-    const int b = bh / p.H;
+    const int b = bh / p.H, h = bh % p.H;
     const int nb = (p.N + kTile - 1) / kTile;
+    // the sequence this CTA works on: rows [q_start, q_start + Lq) of Q and
+    // [k_start, k_start + Lk) of K, V.  Its queries are its last Lq
+    // positions: under the causal mask query i sees key j iff j <= i + shift
+    // (shift = Lk - Lq; 0 for the square [B, H, N, d] case).
+    int q_start = 0, k_start = 0, Lq = p.N, Lk = p.N, Tk = p.Tk;
+    bool bad_len = false;
+    if constexpr (VARLEN) {
+        q_start = p.cu_q[b];
+        Lq = p.cu_q[b + 1] - q_start;
+        k_start = p.cu_k[b];
+        Lk = p.cu_k[b + 1] - k_start;
+        if (q_start < 0 || Lq < 0 || q_start + Lq > p.total_q || k_start < 0 || Lk < 0 ||
+            k_start + Lk > p.total_k || Lq > p.Tq * kTile) {
+            bad_len = true;
+            Lq = Lk = 0;
+        }
+        Tk = (Lk + kTile - 1) / kTile;
+    }
+    const int shift = Lk - Lq;
     int q0[2], qn[2];
 #pragma unroll
     for (int x = 0; x < 2; ++x) {
         q0[x] = (2 * pq + x) * kTile;
-        qn[x] = max(0, min(kTile, p.N - q0[x]));
+        qn[x] = max(0, min(kTile, Lq - q0[x]));
     }
+    // TMA coordinates of row `row` of a sequence starting at `start`:
+    // [B*H][N][d] view, or the [total][H][d] view of a ragged batch
+    auto tload = [&](uint32_t dst, const CUtensorMap *m, uint32_t mbar, int c, int row, int start) {
+        if constexpr (VARLEN)
+            tma_load_3d(dst, m, mbar, c * 64, h, start + row);
+        else
+            tma_load_3d(dst, m, mbar, c * 64, row, bh);
+    };
 
     auto bar = [&](int i) -> uint32_t { return base + S::OFF_BAR + 8u * (uint32_t)i; };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sb + S::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sb + S::OFF_MISC + 4);
     const Guard g{p.status, p.status + 1, abort_flag};
 
-    bool bad = false;
-    const int kvis = key_visible_bound(p.key_len, b, p.N, &bad);
+    bool bad = bad_len;
+    const int kvis = VARLEN ? Lk : key_visible_bound(p.key_len, b, p.N, &bad);
     if (bad && threadIdx.x == 0 && pq == 0 && (bh % p.H) == 0) record_status(g, kStatusBadKeyLen, 0);
 
     // Without a block mask the key tiles query tile x sees are exactly
@@ -125,13 +158,14 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
 #pragma unroll
     for (int x = 0; x < 2; ++x) {
         int lim = kvis;
-        if (p.causal) lim = min(lim, q0[x] + qn[x]);
-        kend[x] = qn[x] > 0 ? (lim + kTile - 1) / kTile : 0;
+        if (p.causal) lim = min(lim, q0[x] + qn[x] + shift);
+        kend[x] = (qn[x] > 0 && lim > 0) ? (lim + kTile - 1) / kTile : 0;
     }
     const int kend_union = max(kend[0], kend[1]);
     // class of key tile kt for query tile x of the pair
     auto cls = [&](int x, int kt) -> unsigned {
         if (qn[x] <= 0) return kTileSkip;
+        if constexpr (VARLEN) return tile_class_shift(q0[x], qn[x], kt * kTile, kTile, kvis, p.causal, shift);
         const int on = p.block_mask ? (p.block_mask[(size_t)(2 * pq + x) * nb + kt] != 0) : 1;
         return tile_class(q0[x], qn[x], kt * kTile, kTile, kvis, p.causal, on);
     };
@@ -139,14 +173,14 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
     auto next_tile = [&](int x, int kt) -> int {
         if (!p.block_mask) {
             const int lim = x == 2 ? kend_union : kend[x];
-            return kt + 1 < lim ? kt + 1 : p.Tk;
+            return kt + 1 < lim ? kt + 1 : Tk;
         }
-        for (int k = kt + 1; k < p.Tk; ++k) {
+        for (int k = kt + 1; k < Tk; ++k) {
             const bool v0 = (x != 1) && cls(0, k) != kTileSkip;
             const bool v1 = (x != 0) && cls(1, k) != kTileSkip;
             if (v0 || v1) return k;
         }
-        return p.Tk;
+        return Tk;
     };
 
     if (threadIdx.x == 0) {
@@ -192,16 +226,16 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                 int u = 0;
                 bool ok = true;
                 int kt = next_tile(2, -1);
-                if (kt < p.Tk) {
+                if (kt < Tk) {
                     const uint32_t nq = (qn[0] > 0 ? 1u : 0u) + (qn[1] > 0 ? 1u : 0u);
                     mbar_arrive_expect_tx(bar(S::B_QFULL), nq * S::TILE_BYTES);
                     for (int x = 0; x < 2; ++x)
                         if (qn[x] > 0)
                             for (int c = 0; c < S::CHUNKS; ++c)
-                                tma_load_3d(base + S::OFF_Q + x * S::TILE_BYTES + c * S::CHUNK_BYTES, &p.tmQ,
-                                            bar(S::B_QFULL), c * 64, q0[x], bh);
+                                tload(base + S::OFF_Q + x * S::TILE_BYTES + c * S::CHUNK_BYTES, &p.tmQ,
+                                      bar(S::B_QFULL), c, q0[x], q_start);
                 }
-                for (; kt < p.Tk; kt = next_tile(2, kt), ++u) {
+                for (; kt < Tk; kt = next_tile(2, kt), ++u) {
                     const int s = u % S::STAGES;
                     const uint32_t ph = (uint32_t)(u / S::STAGES) & 1u;
                     if (!mbar_wait(bar(S::B_KVEMPTY + s), ph ^ 1u, g, 0x101)) {
@@ -212,14 +246,14 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                     const uint32_t voff = base + S::OFF_V + s * S::TILE_BYTES;
                     mbar_arrive_expect_tx(bar(S::B_KFULL + s), S::TILE_BYTES);
                     for (int c = 0; c < S::CHUNKS; ++c)
-                        tma_load_3d(koff + c * S::CHUNK_BYTES, &p.tmK, bar(S::B_KFULL + s), c * 64, kt * kTile, bh);
+                        tload(koff + c * S::CHUNK_BYTES, &p.tmK, bar(S::B_KFULL + s), c, kt * kTile, k_start);
                     mbar_arrive_expect_tx(bar(S::B_VFULL + s), S::TILE_BYTES);
                     for (int c = 0; c < S::CHUNKS; ++c)
-                        tma_load_3d(voff + c * S::CHUNK_BYTES, &p.tmV, bar(S::B_VFULL + s), c * 64, kt * kTile, bh);
+                        tload(voff + c * S::CHUNK_BYTES, &p.tmV, bar(S::B_VFULL + s), c, kt * kTile, k_start);
                 }
                 if (!ok) {
                     // gave up: let every copy already issued land before the CTA exits
-                    if (next_tile(2, -1) < p.Tk) drain_wait(bar(S::B_QFULL), 0);
+                    if (next_tile(2, -1) < Tk) drain_wait(bar(S::B_QFULL), 0);
                     for (int i = (u > S::STAGES ? u - S::STAGES : 0); i < u; ++i) {
                         const int s = i % S::STAGES;
                         const uint32_t ph = (uint32_t)(i / S::STAGES) & 1u;
@@ -254,7 +288,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                     }
                     mma_commit(bar(S::B_SFULL + x));
                 };
-                if (kt < p.Tk) {
+                if (kt < Tk) {
                     ok = mbar_wait(bar(S::B_QFULL), 0, g, 0x201) && mbar_wait(bar(S::B_KFULL + 0), 0, g, 0x202);
                     if (ok) {
                         tc_fence_after();
@@ -262,7 +296,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                             if (cls(x, kt) != kTileSkip) issue_s(x, 0);
                     }
                     int u = 0;
-                    while (ok && kt < p.Tk) {
+                    while (ok && kt < Tk) {
                         const int s = u % S::STAGES;
                         const int kt_next = next_tile(2, kt);
                         const int s2 = (u + 1) % S::STAGES;
@@ -292,7 +326,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                                 mma_commit(bar(S::B_PVDONE + x));
                                 ++nv[x];
                             }
-                            if (kt_next < p.Tk && cls(x, kt_next) != kTileSkip) {
+                            if (kt_next < Tk && cls(x, kt_next) != kTileSkip) {
                                 if (!kwaited && !mbar_wait(bar(S::B_KFULL + s2), (uint32_t)((u + 1) / S::STAGES) & 1u,
                                                            g, 0x205)) {
                                     ok = false;
@@ -333,7 +367,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
         float m_ref = -INFINITY, l = 0.f;
         int it = 0;
         bool ok = true;
-        for (int kt = next_tile(x, -1); kt < p.Tk; kt = next_tile(x, kt), ++it) {
+        for (int kt = next_tile(x, -1); kt < Tk; kt = next_tile(x, kt), ++it) {
             const bool partial = cls(x, kt) == kTilePartial;
             const int k0 = kt * kTile;
             if (!mbar_wait_warp(bar(S::B_SFULL + x), (uint32_t)it & 1u, g, 0x401)) {
@@ -352,7 +386,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
 #pragma unroll
                     for (int t = 0; t < 32; ++t) {
                         const int key = k0 + 32 * j + t;
-                        if (key >= kvis || (p.causal && key > q)) sr[j][t] = __float_as_uint(-INFINITY);
+                        if (key >= kvis || (p.causal && key > q + shift)) sr[j][t] = __float_as_uint(-INFINITY);
                     }
             }
             // row maximum as eight independent 3-input chains, then a tree:
@@ -444,7 +478,8 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
         }
         if (ok) {
             const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-            __nv_bfloat16 *orow = reinterpret_cast<__nv_bfloat16 *>(p.O) + ((size_t)bh * p.N + q) * D;
+            const size_t orow_idx = VARLEN ? (size_t)(q_start + q) * p.H + h : (size_t)bh * p.N + q;
+            __nv_bfloat16 *orow = reinterpret_cast<__nv_bfloat16 *>(p.O) + orow_idx * D;
 #pragma unroll 1
             for (int j = 0; j < D / 32; ++j) {
                 uint32_t o[32];
@@ -466,7 +501,8 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                 }
             }
             if (r < qn[x])
-                p.LSE[(size_t)bh * p.N + q] = (l > 0.f) ? (m_ref + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+                p.LSE[VARLEN ? (size_t)h * p.total_q + q_start + q : (size_t)bh * p.N + q] =
+                    (l > 0.f) ? (m_ref + log2f(l)) * 0.69314718055994530942f : -INFINITY;
         }
         __syncwarp();
         setmaxnreg_dec<S::REGS_CTRL>();
@@ -480,18 +516,23 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
 
 int fwd_smem_bytes(int d) { return d == 64 ? FwdShape<64>::SMEM_BYTES : FwdShape<128>::SMEM_BYTES; }
 
-template <int D>
+template <int D, bool VARLEN>
 static cudaError_t launch_fwd_t(const FwdParams &p, cudaStream_t st) {
     const int smem = FwdShape<D>::SMEM_BYTES;
-    cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(fa_fwd_kernel<D, VARLEN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)((p.Tq + 1) / 2) * (unsigned)p.BH;
-    fa_fwd_kernel<D><<<grid, FwdShape<D>::THREADS, smem, st>>>(p);
+    fa_fwd_kernel<D, VARLEN><<<grid, FwdShape<D>::THREADS, smem, st>>>(p);
     return cudaGetLastError();
 }
 
 cudaError_t launch_fwd(int d, const FwdParams &p, cudaStream_t st) {
-    return d == 64 ? launch_fwd_t<64>(p, st) : launch_fwd_t<128>(p, st);
+    return d == 64 ? launch_fwd_t<64, false>(p, st) : launch_fwd_t<128, false>(p, st);
+}
+
+cudaError_t launch_fwd_varlen(int d, const FwdParams &p, cudaStream_t st) {
+    return d == 64 ? launch_fwd_t<64, true>(p, st) : launch_fwd_t<128, true>(p, st);
 }
 
 }  // namespace fa

@@ -12,6 +12,8 @@ namespace fa {
 // Forward: one CTA per (query tile, b*h).
 cudaError_t launch_fwd(int d, const FwdParams &p, cudaStream_t st);
 int fwd_smem_bytes(int d);
+// Ragged batches: packed [total][H][d] sequences (cu_q, cu_k offsets).
+cudaError_t launch_fwd_varlen(int d, const FwdParams &p, cudaStream_t st);
 // FP8 forward (d = 128): e4m3 Q, K, V^T with per-block scales.
 cudaError_t launch_fwd_fp8(const FwdParams &p, cudaStream_t st);
 // FP8 block quantisation of one bf16 tensor [BH][N][d] (V: transposed).

@@ -57,6 +57,11 @@ struct FwdParams {
     CUtensorMap tmQ, tmK, tmV;       // [BH][N][d] bf16, box {64, 128, 1}, 128B swizzle; FP8: Q, K e4m3
                                      // [BH][N][d] box {128, 128, 1}, V^T e4m3 [BH][d][Np] box {128, d, 1}
     const float *sQ, *sK, *sV;       // FP8 only: per-(bh, 128-row block) scales [BH][T]
+    // ragged batches only: sequence b owns query rows cu_q[b]..cu_q[b+1]-1 of
+    // Q, O [total_q][H][d] and key rows cu_k[b]..cu_k[b+1]-1 of K, V
+    // [total_k][H][d]; LSE is [H][total_q]; the maps view [total][H][d]
+    const int32_t *cu_q, *cu_k;
+    int total_q, total_k;
     void *O;                         // bf16 [BH][N][d]
     float *LSE;                      // fp32 [BH][N]
     const int32_t *key_len;          // device [B] or null
