@@ -22,6 +22,10 @@ quantisation of Q, K and V (``fa_quantize_fp8``, three launches) and
 the FP8 forward kernel against the dense-FP8 peak (the measured sustained
 bf16 figure x 2, the nominal fp8 : bf16 ratio).
 
+``--tile-sweep`` times the forward at each tile shape ``fa_fwd_tiles`` offers
+(query rows per CTA 128 / 256 x key rows per tile 64 / 128) on the workload
+and prints one line with a ``sweep`` list (forward TFLOP/s per shape).
+
 ``--workload varlen_...`` measures the ragged-batch forward (``fa_fwd_varlen``,
 packed sequences of uneven lengths): ``value`` is forward TFLOP/s over the
 visible (query, key) pairs.
@@ -527,6 +531,75 @@ def run_fp8(args):
     return 0
 
 
+# ---------------------------------------------------------------- tile-size sweep
+def run_tile_sweep(args):
+    import torch
+
+    ws_n, rank = init_dist("nccl")
+    _, _, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import io_aware_exact_09_gb300 as fa
+    from synthetic import WORKLOADS, algorithmic_fwd_flops, make_inputs
+    fa.build()
+    w = WORKLOADS[args.workload]
+    B, H, N, d = w.B, w.H, w.N, w.d
+    case = make_inputs(w, with_dO=False)
+    Q, K, V = (case[k].to(dev).contiguous() for k in ("Q", "K", "V"))
+    kl = None if case["key_len"] is None else case["key_len"].to(dev)
+    bm = None if case["block_mask"] is None else case["block_mask"].contiguous().to(dev)
+    O = torch.empty_like(Q)
+    LSE = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    wsn = fa.fa_fwd_workspace_size(B, H, N, d)
+    ws = fa.workspace(wsn, dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    flops = algorithmic_fwd_flops(B, H, N, d, w.causal,
+                                  None if case["key_len"] is None else case["key_len"].tolist(),
+                                  None if case["block_mask"] is None else case["block_mask"])
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    out = []
+    launches = 0
+    for bq, bk in ((256, 128), (256, 64), (128, 128), (128, 64)):
+        def step():
+            st = fa.fa_fwd_tiles(Q, K, V, O, LSE, B, H, N, d, w.softmax_scale, w.causal, kl, bm, bq, bk, ws, wsn, sp)
+            if st != 0:
+                raise RuntimeError("fa_fwd_tiles failed: %s" % fa.fa_status_string(st))
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize(dev)
+        ts = []
+        for _ in range(args.steps):
+            flush.zero_()
+            e0.record(stream)
+            step()
+            e1.record(stream)
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1))
+            launches += 1
+        ms = reduce_max(sum(ts) / len(ts), dev)
+        out.append({"block_q": bq, "block_k": bk, "ms": ms, "tflops": whole_job_tflops(flops, ws_n, ms / 1e3)})
+    if fa.fa_get_device_status(ws, sp) != 0:
+        raise RuntimeError("device status after the sweep")
+    peaks, peak_src = measured_peaks()
+    peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    best = max(out, key=lambda r: r["tflops"])
+    if rank == 0:
+        print(json.dumps({
+            "metric": "attention fwd TFLOP/s (bf16) per tile shape", "value": best["tflops"], "unit": "TFLOP/s",
+            "n_gpus": ws_n, "steps": args.steps, "warmup": args.warmup, "ms_per_step": best["ms"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "B": B, "H": H, "N": N, "d": d, "causal": w.causal,
+                       "l2": "flushed between steps"},
+            "sweep": out,
+            "roofline": {"bound": "tensor", "kernel": "fa_fwd_kernel (best shape)", "achieved": best["tflops"] / ws_n,
+                         "peak": peak, "unit": "TFLOP/s", "frac": best["tflops"] / ws_n / peak, "traffic": None,
+                         "peak_source": "%s bf16_tflops_sustained" % peak_src},
+            "cpu_baseline": None, "e2e": None, "gpu_launches": launches}), flush=True)
+    return 0
+
+
 # ---------------------------------------------------------------- ragged batches
 def oracle_varlen_sample(w, budget_s: float):
     """The fp64 oracle on sequence 0 of the ragged workload, one head, called
@@ -900,6 +973,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--fp8", action="store_true", help="measure the FP8 forward (d = 128 workloads)")
+    ap.add_argument("--tile-sweep", action="store_true", help="time the forward at each tile shape")
     ap.add_argument("--decode-reps", type=int, default=20,
                     help="decode workloads: timed calls per step (each one is well under a millisecond)")
     args = ap.parse_args(argv)
@@ -914,6 +988,8 @@ def main(argv=None):
         return run_varlen(args, VARLEN_WORKLOADS[args.workload])
     if args.fp8:
         return run_fp8(args)
+    if args.tile_sweep:
+        return run_tile_sweep(args)
     return run_ours(args)
 
 

@@ -92,6 +92,22 @@ fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LS
                  void *stream);
 
 /*
+ * The forward with a chosen tile shape, for the block-size sweep
+ * ("Attention" chapter, FlashAttention paragraph: widening the block
+ * shrinks HBM traffic and runtime up to a point).  block_q: query rows per
+ * CTA, 128 or 256 (fa_fwd uses 256: two 128-row tiles); block_k: key rows per
+ * tile, 64 or 128 (fa_fwd: 128).  Other values: FA_ERR_UNSUPPORTED (a 256-key
+ * tile does not fit: its S rows need 256 of the 512 TMEM columns per query
+ * tile, and at d = 128 one K plus one V tile take 128 KB of shared memory).
+ * Arguments, results and masks otherwise as fa_fwd; the block_mask keeps its
+ * 128 x 128 granularity.  One kernel launch.
+ */
+fa_status fa_fwd_tiles(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H,
+                       int N, int d, float softmax_scale, int causal, const int32_t *key_len,
+                       const uint8_t *block_mask, int block_q, int block_k, void *workspace,
+                       size_t workspace_bytes, void *stream);
+
+/*
  * Forward of a ragged batch ("Attention" chapter, serving paragraph: the
  * ragged layouts inference engines keep their sequences in): B sequences of
  * different lengths packed one after another.  Q, O: device bf16

@@ -75,6 +75,8 @@ def lib():
             L.fa_decode_workspace_size.restype = sz
             L.fa_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, i, vp, sz, vp]
             L.fa_decode.restype = i
+            L.fa_fwd_tiles.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp, i, i, vp, sz, vp]
+            L.fa_fwd_tiles.restype = i
             L.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, sz, vp]
             L.fa_fwd_varlen.restype = i
             L.fa_quantize_fp8.argtypes = [vp, vp, vp, i, i, i, i, i, vp]
@@ -98,7 +100,7 @@ def lib():
 
 EXPORTED = ("fa_tile_size", "fa_fwd_workspace_size", "fa_bwd_workspace_size", "fa_fwd", "fa_bwd",
             "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_postprocess", "fa_bwd_noalloc",
-            "fa_decode_workspace_size", "fa_decode", "fa_fwd_varlen", "fa_quantize_fp8", "fa_fwd_fp8",
+            "fa_decode_workspace_size", "fa_decode", "fa_fwd_tiles", "fa_fwd_varlen", "fa_quantize_fp8", "fa_fwd_fp8",
             "fa_tile_plan",
             "fa_host_workspace_size", "fa_attention_host", "fa_get_device_status", "fa_reset_device_status",
             "fa_status_string")
@@ -150,6 +152,13 @@ def fa_fwd(Q, K, V, O, LSE, B, H, N, d, softmax_scale, causal, key_len, block_ma
     return lib().fa_fwd(_p(Q), _p(K), _p(V), _p(O), _p(LSE), B, H, N, d, float(softmax_scale),
                         int(bool(causal)), _p(key_len), _p(block_mask), _p(workspace),
                         int(workspace_bytes), _stream(stream))
+
+
+def fa_fwd_tiles(Q, K, V, O, LSE, B, H, N, d, softmax_scale, causal, key_len, block_mask, block_q, block_k,
+                 workspace, workspace_bytes, stream=None) -> int:
+    return lib().fa_fwd_tiles(_p(Q), _p(K), _p(V), _p(O), _p(LSE), B, H, N, d, float(softmax_scale),
+                              int(bool(causal)), _p(key_len), _p(block_mask), int(block_q), int(block_k),
+                              _p(workspace), int(workspace_bytes), _stream(stream))
 
 
 def fa_fwd_varlen(Q, K, V, O, LSE, cu_seqlens_q, cu_seqlens_k, B, H, total_q, total_k, max_seqlen_q, d,

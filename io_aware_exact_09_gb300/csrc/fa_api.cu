@@ -189,6 +189,44 @@ fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LS
     return fa::launch_fwd(d, p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+fa_status fa_fwd_tiles(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H, int N, int d,
+                       float softmax_scale, int causal, const int32_t *key_len, const uint8_t *block_mask, int block_q,
+                       int block_k, void *workspace, size_t workspace_bytes, void *stream) {
+    if (block_q != 128 && block_q != 256) return FA_ERR_UNSUPPORTED;
+    if (block_k != 64 && block_k != 128) return FA_ERR_UNSUPPORTED;
+    bool empty = false;
+    fa_status st = check_sizes(B, H, N, d, &empty);
+    if (st != FA_OK) return st;
+    if (!scale_ok(softmax_scale)) return FA_ERR_INVALID_ARGUMENT;
+    if (empty) return FA_OK;
+    if (!Q || !K || !V || !O || !LSE) return FA_ERR_INVALID_ARGUMENT;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(LSE))
+        return FA_ERR_INVALID_ARGUMENT;
+    if (!workspace || !aligned16(workspace) || workspace_bytes < fa_fwd_workspace_size(B, H, N, d))
+        return FA_ERR_WORKSPACE;
+    FwdParams p;
+    std::memset(&p, 0, sizeof(p));
+    const int BH = B * H;
+    if (!encode_bf16_3d(&p.tmQ, Q, d, N, BH, 128) || !encode_bf16_3d(&p.tmK, K, d, N, BH, block_k) ||
+        !encode_bf16_3d(&p.tmV, V, d, N, BH, block_k))
+        return FA_ERR_CUDA;
+    p.O = O;
+    p.LSE = LSE;
+    p.key_len = key_len;
+    p.block_mask = block_mask;
+    p.status = static_cast<unsigned *>(workspace);
+    p.H = H;
+    p.N = N;
+    p.BH = BH;
+    p.Tq = (N + 127) / 128;
+    p.Tk = (N + block_k - 1) / block_k;
+    p.qpc = block_q / 128;
+    p.causal = causal ? 1 : 0;
+    p.scale_log2 = softmax_scale * kLog2e;
+    return fa::launch_fwd_tiles(d, block_k, p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK
+                                                                                                  : FA_ERR_CUDA;
+}
+
 fa_status fa_fwd_varlen(const void *Q, const void *K, const void *V, void *O, float *LSE, const int32_t *cu_seqlens_q,
                         const int32_t *cu_seqlens_k, int B, int H, int total_q, int total_k, int max_seqlen_q, int d,
                         float softmax_scale, int causal, void *workspace, size_t workspace_bytes, void *stream) {

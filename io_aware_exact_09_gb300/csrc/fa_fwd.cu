@@ -51,16 +51,20 @@ namespace fa {
 
 constexpr float kRescaleLog2 = 8.0f;
 
-template <int D>
+template <int D, int BC = 128>
 struct FwdShape {
+    static_assert(BC == 64 || BC == 128, "key tile width");
+    static constexpr int KC = BC / 32;                  // 32-column chunks of an S row
     static constexpr int CHUNKS = D / 64;               // 64-element (128-byte) column chunks
-    static constexpr int CHUNK_BYTES = 128 * 128;       // 128 rows x 128 bytes
+    static constexpr int CHUNK_BYTES = 128 * 128;       // 128 query rows x 128 bytes
     static constexpr int TILE_BYTES = CHUNKS * CHUNK_BYTES;
-    static constexpr int STAGES = (D == 64) ? 4 : 2;
+    static constexpr int KV_CHUNK_BYTES = BC * 128;     // BC key rows x 128 bytes
+    static constexpr int KV_TILE_BYTES = CHUNKS * KV_CHUNK_BYTES;
+    static constexpr int STAGES = (D == 64 || BC == 64) ? 4 : 2;
     static constexpr int OFF_Q = 0;                     // [2] query tiles
     static constexpr int OFF_K = OFF_Q + 2 * TILE_BYTES;
-    static constexpr int OFF_V = OFF_K + STAGES * TILE_BYTES;
-    static constexpr int OFF_BAR = OFF_V + STAGES * TILE_BYTES;
+    static constexpr int OFF_V = OFF_K + STAGES * KV_TILE_BYTES;
+    static constexpr int OFF_BAR = OFF_V + STAGES * KV_TILE_BYTES;
     static constexpr int B_QFULL = 0;
     static constexpr int B_KFULL = 1;
     static constexpr int B_VFULL = B_KFULL + STAGES;
@@ -92,9 +96,9 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
         if (globaltimer_ns() - t0 > FA_WAIT_TIMEOUT_NS) break;
 }
 
-template <int D, bool VARLEN>
+template <int D, bool VARLEN, int BC, int QPC>
 __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
-    using S = FwdShape<D>;
+    using S = FwdShape<D, BC>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -103,7 +107,8 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
 
     // Work item, head-major: the CTAs resident at one time share one head's K
     // and V in L2; within a head the causally heaviest pairs start first.
-    const int Tp = (p.Tq + 1) / 2;
+    constexpr int qpc = QPC;                         // query tiles per CTA (1 or 2)
+    const int Tp = (p.Tq + qpc - 1) / qpc;
     const int pq = Tp - 1 - (int)(blockIdx.x % Tp);
     const int bh = (int)(blockIdx.x / Tp);
     const int b = bh / p.H, h = bh % p.H;
@@ -124,14 +129,14 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
             bad_len = true;
             Lq = Lk = 0;
         }
-        Tk = (Lk + kTile - 1) / kTile;
+        Tk = (Lk + BC - 1) / BC;
     }
     const int shift = Lk - Lq;
     int q0[2], qn[2];
 #pragma unroll
     for (int x = 0; x < 2; ++x) {
-        q0[x] = (2 * pq + x) * kTile;
-        qn[x] = max(0, min(kTile, Lq - q0[x]));
+        q0[x] = (qpc * pq + x) * kTile;
+        qn[x] = x < qpc ? max(0, min(kTile, Lq - q0[x])) : 0;
     }
     // TMA coordinates of row `row` of a sequence starting at `start`:
     // [B*H][N][d] view, or the [total][H][d] view of a ragged batch
@@ -159,15 +164,17 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
     for (int x = 0; x < 2; ++x) {
         int lim = kvis;
         if (p.causal) lim = min(lim, q0[x] + qn[x] + shift);
-        kend[x] = (qn[x] > 0 && lim > 0) ? (lim + kTile - 1) / kTile : 0;
+        kend[x] = (qn[x] > 0 && lim > 0) ? (lim + BC - 1) / BC : 0;
     }
     const int kend_union = max(kend[0], kend[1]);
     // class of key tile kt for query tile x of the pair
     auto cls = [&](int x, int kt) -> unsigned {
         if (qn[x] <= 0) return kTileSkip;
-        if constexpr (VARLEN) return tile_class_shift(q0[x], qn[x], kt * kTile, kTile, kvis, p.causal, shift);
-        const int on = p.block_mask ? (p.block_mask[(size_t)(2 * pq + x) * nb + kt] != 0) : 1;
-        return tile_class(q0[x], qn[x], kt * kTile, kTile, kvis, p.causal, on);
+        if constexpr (VARLEN) return tile_class_shift(q0[x], qn[x], kt * BC, BC, kvis, p.causal, shift);
+        // a key tile of BC <= 128 columns lies inside one 128-wide mask block
+        const int on =
+            p.block_mask ? (p.block_mask[(size_t)(QPC * pq + x) * nb + (BC == kTile ? kt : kt / (kTile / BC))] != 0) : 1;
+        return tile_class(q0[x], qn[x], kt * BC, BC, kvis, p.causal, on);
     };
     // next key tile after kt seen by query tile x (x = 2: by either)
     auto next_tile = [&](int x, int kt) -> int {
@@ -242,14 +249,14 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                         ok = false;
                         break;
                     }
-                    const uint32_t koff = base + S::OFF_K + s * S::TILE_BYTES;
-                    const uint32_t voff = base + S::OFF_V + s * S::TILE_BYTES;
-                    mbar_arrive_expect_tx(bar(S::B_KFULL + s), S::TILE_BYTES);
+                    const uint32_t koff = base + S::OFF_K + s * S::KV_TILE_BYTES;
+                    const uint32_t voff = base + S::OFF_V + s * S::KV_TILE_BYTES;
+                    mbar_arrive_expect_tx(bar(S::B_KFULL + s), S::KV_TILE_BYTES);
                     for (int c = 0; c < S::CHUNKS; ++c)
-                        tload(koff + c * S::CHUNK_BYTES, &p.tmK, bar(S::B_KFULL + s), c, kt * kTile, k_start);
-                    mbar_arrive_expect_tx(bar(S::B_VFULL + s), S::TILE_BYTES);
+                        tload(koff + c * S::KV_CHUNK_BYTES, &p.tmK, bar(S::B_KFULL + s), c, kt * BC, k_start);
+                    mbar_arrive_expect_tx(bar(S::B_VFULL + s), S::KV_TILE_BYTES);
                     for (int c = 0; c < S::CHUNKS; ++c)
-                        tload(voff + c * S::CHUNK_BYTES, &p.tmV, bar(S::B_VFULL + s), c, kt * kTile, k_start);
+                        tload(voff + c * S::KV_CHUNK_BYTES, &p.tmV, bar(S::B_VFULL + s), c, kt * BC, k_start);
                 }
                 if (!ok) {
                     // gave up: let every copy already issued land before the CTA exits
@@ -265,7 +272,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
         } else if (warp == 1) {
             // ---------------------------------------------------------- MMA issuer
             if (lane == 0) {
-                constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
+                constexpr uint32_t IDESC_S = idesc_bf16(128, BC, false, false);
                 constexpr uint32_t IDESC_PV = idesc_bf16(128, D, false, true);
                 int kt = next_tile(2, -1);
                 bool ok = true;
@@ -275,16 +282,17 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                 // 128-byte row, then the next 64-column chunk; MN-major V: 16 rows)
                 const uint64_t dq0 = sdesc_sw128(base + S::OFF_Q, 16, 1024);
                 const uint64_t dk0 = sdesc_sw128(base + S::OFF_K, 16, 1024);
-                const uint64_t dv0 = sdesc_sw128(base + S::OFF_V, S::CHUNK_BYTES, 1024);
+                const uint64_t dv0 = sdesc_sw128(base + S::OFF_V, S::KV_CHUNK_BYTES, 1024);
                 // S_x = Q_x K^T for the key tile in stage s (the x-th S buffer)
                 auto issue_s = [&](int x, int s) {
                     const uint32_t d_tmem = tmem + S::TM_S + 128u * (uint32_t)x;
                     const uint64_t qd = sdesc_add(dq0, (uint32_t)(x * S::TILE_BYTES));
-                    const uint64_t kd = sdesc_add(dk0, (uint32_t)(s * S::TILE_BYTES));
+                    const uint64_t kd = sdesc_add(dk0, (uint32_t)(s * S::KV_TILE_BYTES));
 #pragma unroll
                     for (int k = 0; k < D / 16; ++k) {
                         const uint32_t off = (k >> 2) * S::CHUNK_BYTES + (k & 3) * 32;
-                        mma_ss(d_tmem, sdesc_add(qd, off), sdesc_add(kd, off), IDESC_S, k > 0 ? 1u : 0u);
+                        const uint32_t koff = (k >> 2) * S::KV_CHUNK_BYTES + (k & 3) * 32;
+                        mma_ss(d_tmem, sdesc_add(qd, off), sdesc_add(kd, koff), IDESC_S, k > 0 ? 1u : 0u);
                     }
                     mma_commit(bar(S::B_SFULL + x));
                 };
@@ -317,10 +325,10 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                                 tc_fence_after();
                                 const uint32_t p_tmem = tmem + S::TM_S + 128u * (uint32_t)x;
                                 const uint32_t o_tmem = tmem + S::TM_O + (uint32_t)(D * x);
-                                const uint64_t vd = sdesc_add(dv0, (uint32_t)(s * S::TILE_BYTES));
+                                const uint64_t vd = sdesc_add(dv0, (uint32_t)(s * S::KV_TILE_BYTES));
                                 const uint32_t acc0 = nv[x] > 0 ? 1u : 0u;
 #pragma unroll
-                                for (int k = 0; k < kTile / 16; ++k)
+                                for (int k = 0; k < BC / 16; ++k)
                                     mma_ts(o_tmem, p_tmem + (uint32_t)k * 8u, sdesc_add(vd, (uint32_t)k * 2048u),
                                            IDESC_PV, k > 0 ? 1u : acc0);
                                 mma_commit(bar(S::B_PVDONE + x));
@@ -369,20 +377,20 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
         bool ok = true;
         for (int kt = next_tile(x, -1); kt < Tk; kt = next_tile(x, kt), ++it) {
             const bool partial = cls(x, kt) == kTilePartial;
-            const int k0 = kt * kTile;
+            const int k0 = kt * BC;
             if (!mbar_wait_warp(bar(S::B_SFULL + x), (uint32_t)it & 1u, g, 0x401)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            uint32_t sr[4][32];
+            uint32_t sr[S::KC][32];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) tmem_ld32(s_tmem + 32u * j, sr[j]);
+            for (int j = 0; j < S::KC; ++j) tmem_ld32(s_tmem + 32u * j, sr[j]);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) tmem_ld_wait(sr[j]);
+            for (int j = 0; j < S::KC; ++j) tmem_ld_wait(sr[j]);
             if (partial) {
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
+                for (int j = 0; j < S::KC; ++j)
 #pragma unroll
                     for (int t = 0; t < 32; ++t) {
                         const int key = k0 + 32 * j + t;
@@ -396,7 +404,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
 #pragma unroll
             for (int u = 0; u < 8; ++u) pm[u] = -INFINITY;
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
+            for (int j = 0; j < S::KC; ++j)
 #pragma unroll
                 for (int t = 0; t < 32; t += 4) {
                     const int u = (j * 8 + t / 4) & 7;
@@ -422,7 +430,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
 #pragma unroll
             for (int u = 0; u < 8; ++u) ps[u] = 0.f;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < S::KC; ++j) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int t = 0; t < 16; ++t) {
@@ -516,23 +524,35 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
 
 int fwd_smem_bytes(int d) { return d == 64 ? FwdShape<64>::SMEM_BYTES : FwdShape<128>::SMEM_BYTES; }
 
-template <int D, bool VARLEN>
+template <int D, bool VARLEN, int BC, int QPC>
 static cudaError_t launch_fwd_t(const FwdParams &p, cudaStream_t st) {
-    const int smem = FwdShape<D>::SMEM_BYTES;
-    cudaError_t e =
-        cudaFuncSetAttribute(fa_fwd_kernel<D, VARLEN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    using S = FwdShape<D, BC>;
+    const int smem = S::SMEM_BYTES;
+    cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D, VARLEN, BC, QPC>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    const unsigned grid = (unsigned)((p.Tq + 1) / 2) * (unsigned)p.BH;
-    fa_fwd_kernel<D, VARLEN><<<grid, FwdShape<D>::THREADS, smem, st>>>(p);
+    const unsigned grid = (unsigned)((p.Tq + QPC - 1) / QPC) * (unsigned)p.BH;
+    fa_fwd_kernel<D, VARLEN, BC, QPC><<<grid, S::THREADS, smem, st>>>(p);
     return cudaGetLastError();
 }
 
 cudaError_t launch_fwd(int d, const FwdParams &p, cudaStream_t st) {
-    return d == 64 ? launch_fwd_t<64, false>(p, st) : launch_fwd_t<128, false>(p, st);
+    return d == 64 ? launch_fwd_t<64, false, 128, 2>(p, st) : launch_fwd_t<128, false, 128, 2>(p, st);
 }
 
 cudaError_t launch_fwd_varlen(int d, const FwdParams &p, cudaStream_t st) {
-    return d == 64 ? launch_fwd_t<64, true>(p, st) : launch_fwd_t<128, true>(p, st);
+    return d == 64 ? launch_fwd_t<64, true, 128, 2>(p, st) : launch_fwd_t<128, true, 128, 2>(p, st);
+}
+
+template <int D>
+static cudaError_t launch_fwd_tiles_d(int block_k, const FwdParams &p, cudaStream_t st) {
+    if (p.qpc == 1)
+        return block_k == 64 ? launch_fwd_t<D, false, 64, 1>(p, st) : launch_fwd_t<D, false, 128, 1>(p, st);
+    return block_k == 64 ? launch_fwd_t<D, false, 64, 2>(p, st) : launch_fwd_t<D, false, 128, 2>(p, st);
+}
+
+cudaError_t launch_fwd_tiles(int d, int block_k, const FwdParams &p, cudaStream_t st) {
+    return d == 64 ? launch_fwd_tiles_d<64>(block_k, p, st) : launch_fwd_tiles_d<128>(block_k, p, st);
 }
 
 }  // namespace fa

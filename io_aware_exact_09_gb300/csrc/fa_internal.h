@@ -12,6 +12,9 @@ namespace fa {
 // Forward: one CTA per (query tile, b*h).
 cudaError_t launch_fwd(int d, const FwdParams &p, cudaStream_t st);
 int fwd_smem_bytes(int d);
+// Forward with a chosen key-tile width (64 or 128); p.qpc sets the query
+// tiles per CTA.
+cudaError_t launch_fwd_tiles(int d, int block_k, const FwdParams &p, cudaStream_t st);
 // Ragged batches: packed [total][H][d] sequences (cu_q, cu_k offsets).
 cudaError_t launch_fwd_varlen(int d, const FwdParams &p, cudaStream_t st);
 // FP8 forward (d = 128): e4m3 Q, K, V^T with per-block scales.

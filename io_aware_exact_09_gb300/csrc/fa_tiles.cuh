@@ -62,6 +62,7 @@ struct FwdParams {
     // [total_k][H][d]; LSE is [H][total_q]; the maps view [total][H][d]
     const int32_t *cu_q, *cu_k;
     int total_q, total_k;
+    int qpc;                         // fa_fwd_tiles only: query tiles per CTA (1 or 2)
     void *O;                         // bf16 [BH][N][d]
     float *LSE;                      // fp32 [BH][N]
     const int32_t *key_len;          // device [B] or null

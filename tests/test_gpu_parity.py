@@ -6,7 +6,7 @@ import torch
 
 import oracle
 from synthetic import WORKLOADS, make_case, make_inputs
-from gpu_common import (check_forward, check_grads, f64, oracle_args, run_cuda)
+from gpu_common import (check_forward, check_grads, f64, oracle_args, run_cuda, to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -137,3 +137,38 @@ def test_repeat_calls_are_deterministic_backward(d):
     for _ in range(4):
         again = fa.attention_backward(g["Q"], g["K"], g["V"], O, L, g["dO"], causal=True, key_len=kl)
         assert torch.equal(first[1], again[1]) and torch.equal(first[2], again[2])
+
+
+@pytest.mark.parametrize("block_q,block_k", [(256, 64), (128, 128), (128, 64)])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("kw", [dict(), dict(causal=True), dict(key_len=[77, 300]), "block"])
+def test_forward_other_tile_shapes_match_oracle(block_q, block_k, d, kw):
+    """fa_fwd_tiles (the block-size sweep's tile shapes) gives the same
+    attention as the oracle, masks included."""
+    import io_aware_exact_09_gb300 as fa
+    N = 300
+    if kw == "block":
+        nb = (N + 127) // 128
+        bm = (np.random.default_rng(3).random((nb, nb)) < 0.6).astype(np.uint8)
+        np.fill_diagonal(bm, 1)
+        kw = dict(block_mask=bm)
+    case = make_case(2, 2, N, d, seed=block_q + block_k, **kw)
+    g = to_dev(case)
+    O = torch.empty_like(g["Q"])
+    L = torch.empty((2, 2, N), device="cuda")
+    ws = fa.workspace(fa.fa_fwd_workspace_size(2, 2, N, d), "cuda")
+    st = fa.fa_fwd_tiles(g["Q"], g["K"], g["V"], O, L, 2, 2, N, d, case["scale"], case["causal"], g["key_len"],
+                         g["block_mask"], block_q, block_k, ws, ws.numel())
+    assert st == 0 and fa.fa_get_device_status(ws) == 0
+    torch.cuda.synchronize()
+    rO, rL = oracle.attention_fwd(f64(case["Q"]), f64(case["K"]), f64(case["V"]), case["scale"], **oracle_args(case))
+    check_forward(O.double().cpu().numpy(), L.double().cpu().numpy(), rO, rL, (block_q, block_k, str(kw)))
+
+
+def test_forward_tile_shape_arguments():
+    import io_aware_exact_09_gb300 as fa
+    x = torch.zeros((1, 1, 128, 64), dtype=torch.bfloat16, device="cuda")
+    L = torch.zeros((1, 1, 128), device="cuda")
+    ws = fa.workspace(256, "cuda")
+    assert fa.fa_fwd_tiles(x, x, x, x, L, 1, 1, 128, 64, 0.1, 0, None, None, 256, 256, ws, 256) == 2
+    assert fa.fa_fwd_tiles(x, x, x, x, L, 1, 1, 128, 64, 0.1, 0, None, None, 64, 128, ws, 256) == 2
