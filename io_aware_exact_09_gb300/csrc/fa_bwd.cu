@@ -422,6 +422,17 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_kernel(const __grid_constant__ 
                 for (int j = 0; j < CW / 32; ++j) tmem_ld32(tmem + lane_off + S::TM_S + c0 + 32u * j, sr[j]);
 #pragma unroll
                 for (int j = 0; j < CW / 32; ++j) tmem_ld_wait(sr[j]);
+                if (klass == kTilePartial) {
+                    // masked scores -> -inf, so that their p is exactly 0 (a mask
+                    // test inside the exp loop below made that loop several times slower)
+#pragma unroll
+                    for (int j = 0; j < CW / 32; ++j)
+#pragma unroll
+                        for (int t = 0; t < 32; ++t) {
+                            const int qq = qa + c0 + 32 * j + t;
+                            if (key >= kvis || (p.causal && key > qq)) sr[j][t] = __float_as_uint(-INFINITY);
+                        }
+                }
 #pragma unroll
                 for (int j = 0; j < CW / 32; ++j)
 #pragma unroll
@@ -430,13 +441,7 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_kernel(const __grid_constant__ 
                         const float2 l2 = *reinterpret_cast<const float2 *>(ls + cq);
                         float p0, p1;
                         fma2(p0, p1, __uint_as_float(sr[j][t]), __uint_as_float(sr[j][t + 1]), c2, c2, -l2.x, -l2.y);
-                        p0 = ex2(p0);
-                        p1 = ex2(p1);
-                        if (klass == kTilePartial) {
-                            if (key >= kvis || (p.causal && key > qa + cq)) p0 = 0.f;
-                            if (key >= kvis || (p.causal && key > qa + cq + 1)) p1 = 0.f;
-                        }
-                        pk[16 * j + t / 2] = pack_bf16x2(p0, p1);
+                        pk[16 * j + t / 2] = pack_bf16x2(ex2(p0), ex2(p1));
                     }
             }
 #pragma unroll
@@ -605,9 +610,10 @@ __global__ void fa_plan_kernel(int B, int N, int T, int causal, const int32_t *k
     }
 }
 
-int bwd_query_block(int d) { return d == 64 ? BwdShape<64>::BQ : BwdShape<128>::BQ; }
+// d = 128 runs fa_bwd128_kernel (128-row query blocks)
+int bwd_query_block(int d) { return d == 64 ? BwdShape<64>::BQ : 128; }
 int bwd_dq_box_rows(int d) { return d == 64 ? BwdShape<64>::DQ_BOX_ROWS : BwdShape<128>::DQ_BOX_ROWS; }
-int bwd_smem_bytes(int d) { return d == 64 ? BwdShape<64>::SMEM_BYTES : BwdShape<128>::SMEM_BYTES; }
+int bwd_smem_bytes(int d) { return d == 64 ? BwdShape<64>::SMEM_BYTES : bwd128_smem_bytes(); }
 
 template <int D>
 static cudaError_t launch_bwd_main_t(const BwdParams &p, cudaStream_t st) {
@@ -619,7 +625,7 @@ static cudaError_t launch_bwd_main_t(const BwdParams &p, cudaStream_t st) {
 }
 
 cudaError_t launch_bwd_main(int d, const BwdParams &p, cudaStream_t st) {
-    return d == 64 ? launch_bwd_main_t<64>(p, st) : launch_bwd_main_t<128>(p, st);
+    return d == 64 ? launch_bwd_main_t<64>(p, st) : launch_bwd128_main(p, st);
 }
 
 cudaError_t launch_bwd_pre(int d, const void *O, const void *dO, float *Dvec, float *dQacc, int64_t rows,

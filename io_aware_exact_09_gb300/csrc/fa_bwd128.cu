@@ -1,0 +1,531 @@
+// fa_bwd128.cu -- backward main kernel for d = 128 with 128-row query blocks.
+//
+// The same method as fa_bwd.cu ("The Attention Matrix You Never Write Down",
+// "Tiling forward, recomputing backward"; "FlashAttention: Mathematical
+// Foundations ...", "Backward Pass and Activation Recomputation"): per
+// 128-key tile, for each query block rebuild P^T = exp(scale k.q - LSE),
+//     dV += P^T dO,  dP^T = V dO^T,  dS^T = P^T o (dP^T - D),
+//     dK += dS^T Q,  dQ^T = K^T dS^T (reduce-added into the fp32 accumulator).
+//
+// Why a second kernel: with 64-row query blocks every S^T, dP^T and dQ^T MMA
+// is N = 64, and an N = 64 MMA reads nearly as many shared-memory operand
+// bytes as an N = 128 one for half the work, so the tensor pipe waits on
+// shared memory.  128-row blocks make every MMA N = 128, but S^T, dP^T, dV,
+// dK and dQ^T would need 640 TMEM columns.  They fit in 512 because the
+// blocks alternate two 128-column regions:
+//     block i:  S^T(i) -> region a, dP^T(i) -> region b (a, b swap each block)
+//               P^T(i) (bf16, packed) stays in region a until dV(i) reads it,
+//               dS^T(i) (packed) in region b until dK(i) reads it;
+//               dQ^T(i) -> region a once dV(i) is done;
+//     block i+1: S^T(i+1) -> region b once dK(i) is done,
+//                dP^T(i+1) -> region a once dQ^T(i) has been drained.
+// Shared memory (224 KB): K, V; Q double-buffered, dO single; the dS^T tile
+// (the dQ MMA's B operand); 32 KB of dQ staging.  Each compute warp stages its
+// dQ^T rows in two 4 KB boxes: one in its own slice of the staging area, one
+// in the slice of the dS^T tile that it alone writes (free once dQ^T(i) has
+// been computed; the warp waits for its own reduce reads before writing the
+// next dS^T there).
+//
+// Roles (384 threads): warp 0 TMA producer (and, whole warp, the LSE/D
+// staging); warp 1 tcgen05 issuer; warps 4-7 and 8-11 two compute warpgroups,
+// one key row per thread, warpgroup w on query columns [64w, 64w + 64).
+#include "fa_internal.h"
+#include "fa_ptx.cuh"
+
+namespace fa {
+
+namespace {
+
+struct Bwd128 {
+    static constexpr int BQ = 128;
+    static constexpr int CW = 64;                          // query columns per compute warpgroup
+    static constexpr int CHUNK = 128 * 128;                // 128 rows x 128 bytes (64 bf16 columns)
+    static constexpr int TILE = 2 * CHUNK;                 // 128 rows x 128 bf16
+    static constexpr int OFF_K = 0;
+    static constexpr int OFF_V = OFF_K + TILE;
+    static constexpr int OFF_Q = OFF_V + TILE;             // [2]
+    static constexpr int OFF_DO = OFF_Q + 2 * TILE;
+    static constexpr int OFF_DS = OFF_DO + TILE;           // [query chunk 2][key 128][128 B]
+    static constexpr int OFF_STG = OFF_DS + TILE;          // [8 warps][32 queries][128 B]
+    static constexpr int OFF_LSE = OFF_STG + 8 * 4096;     // [BQ] fp32, log2 domain
+    static constexpr int OFF_DV = OFF_LSE + BQ * 4;        // [BQ] fp32
+    static constexpr int OFF_BAR = OFF_DV + BQ * 4;
+    static constexpr int B_KV = 0;
+    static constexpr int B_QFULL = 1;                      // [2]
+    static constexpr int B_QEMPTY = 3;                     // [2]
+    static constexpr int B_DOFULL = 5;
+    static constexpr int B_DOEMPTY = 6;
+    static constexpr int B_LSE = 7;                        // LSE/D staged (32 arrivals)
+    static constexpr int B_LSEFREE = 8;                    // LSE/D consumed (256)
+    static constexpr int B_SFULL = 9;
+    static constexpr int B_DPFULL = 10;
+    static constexpr int B_PFULL = 11;                     // 256
+    static constexpr int B_DSFULL = 12;                    // 256
+    static constexpr int B_DVDONE = 13;
+    static constexpr int B_DKDONE = 14;
+    static constexpr int B_DQFULL = 15;
+    static constexpr int B_DQFREE = 16;                    // 256
+    static constexpr int B_ACC = 17;
+    static constexpr int B_FIN = 18;
+    static constexpr int NBAR = 19;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t TM_R0 = 0;                   // regions a / b: 128 columns each
+    static constexpr uint32_t TM_DV = 256;
+    static constexpr uint32_t TM_DK = 384;
+    static constexpr int THREADS = 384;
+    static constexpr int LAUNCH_REGS = 168;
+    static constexpr int REGS_CTRL = 136;
+    static constexpr int REGS_COMPUTE = 184;
+    static_assert(128 * REGS_CTRL + 256 * REGS_COMPUTE == THREADS * LAUNCH_REGS, "register split");
+};
+
+__device__ __forceinline__ void b128_drain_wait(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (globaltimer_ns() - t0 > FA_WAIT_TIMEOUT_NS) break;
+}
+
+// P^T / dS^T packed (bf16 pairs) inside a region: queries [16k, 16k + 16)
+// at column 64 (k / 4) + 8 (k mod 4): each warpgroup stays inside its own
+// 64-column half, so neither overwrites fp32 values the other still reads.
+__device__ __forceinline__ uint32_t packed_col128(int k) { return (uint32_t)((k >> 2) * 64 + 8 * (k & 3)); }
+
+__global__ void __launch_bounds__(384, 1) fa_bwd128_kernel(const __grid_constant__ BwdParams p) {
+    using S = Bwd128;
+    constexpr int BQ = S::BQ, CW = S::CW;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *sb = smem_raw + (base - raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    const int kt = (int)(blockIdx.x % p.Tk);
+    const int bh = (int)(blockIdx.x / p.Tk);
+    const int b = bh / p.H;
+    const int k0 = kt * kTile;
+    const int nb = (p.N + kTile - 1) / kTile;
+
+    auto bar = [&](int i) -> uint32_t { return base + S::OFF_BAR + 8u * (uint32_t)i; };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sb + S::OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sb + S::OFF_MISC + 4);
+    const Guard g{p.status, p.status + 1, abort_flag};
+
+    bool bad = false;
+    const int kvis = key_visible_bound(p.key_len, b, p.N, &bad);
+    if (bad && threadIdx.x == 0 && kt == 0 && (bh % p.H) == 0) record_status(g, kStatusBadKeyLen, 0);
+
+    // query block qb (128 rows = one mask block) against this key tile
+    auto cls = [&](int qb) -> unsigned {
+        const int qa = qb * BQ;
+        const int on = p.block_mask ? (p.block_mask[(size_t)qb * nb + kt] != 0) : 1;
+        return tile_class(qa, min(BQ, p.N - qa), k0, kTile, kvis, p.causal, on);
+    };
+    const int qb_start = (k0 >= kvis) ? p.Tqb : (p.causal ? k0 / BQ : 0);
+    auto next_qb = [&](int qb) -> int {
+        if (!p.block_mask) {
+            const int nq = qb < qb_start ? qb_start : qb + 1;
+            return nq < p.Tqb ? nq : p.Tqb;
+        }
+        for (int x = qb + 1; x < p.Tqb; ++x)
+            if (cls(x) != kTileSkip) return x;
+        return p.Tqb;
+    };
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(S::B_KV), 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar(S::B_QFULL + s), 1);
+            mbar_init(bar(S::B_QEMPTY + s), 1);
+        }
+        mbar_init(bar(S::B_DOFULL), 1);
+        mbar_init(bar(S::B_DOEMPTY), 1);
+        mbar_init(bar(S::B_LSE), 32);
+        mbar_init(bar(S::B_LSEFREE), 256);
+        mbar_init(bar(S::B_SFULL), 1);
+        mbar_init(bar(S::B_DPFULL), 1);
+        mbar_init(bar(S::B_PFULL), 256);
+        mbar_init(bar(S::B_DSFULL), 256);
+        mbar_init(bar(S::B_DVDONE), 1);
+        mbar_init(bar(S::B_DKDONE), 1);
+        mbar_init(bar(S::B_DQFULL), 1);
+        mbar_init(bar(S::B_DQFREE), 256);
+        mbar_init(bar(S::B_ACC), 1);
+        mbar_init(bar(S::B_FIN), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&p.tmQ);
+        tma_prefetch_desc(&p.tmdO);
+        tma_prefetch_desc(&p.tmK);
+        tma_prefetch_desc(&p.tmV);
+        tma_prefetch_desc(&p.tmdQ);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), S::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int first = next_qb(-1);
+    float *lse_s = reinterpret_cast<float *>(sb + S::OFF_LSE);   // log2 domain
+    float *dv_s = reinterpret_cast<float *>(sb + S::OFF_DV);
+
+    if (warp < 4) {
+        setmaxnreg_dec<S::REGS_CTRL>();
+        if (warp == 0 && first < p.Tqb) {
+            // ---------------------------------------------------------- producer
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bar(S::B_KV), 2 * S::TILE);
+                for (int c = 0; c < 2; ++c) {
+                    tma_load_3d(base + S::OFF_K + c * S::CHUNK, &p.tmK, bar(S::B_KV), c * 64, k0, bh);
+                    tma_load_3d(base + S::OFF_V + c * S::CHUNK, &p.tmV, bar(S::B_KV), c * 64, k0, bh);
+                }
+            }
+            int i = 0, nl = 0;          // blocks seen, blocks whose Q / dO loads were issued
+            bool ok = true;
+            for (int qb = first; qb < p.Tqb; qb = next_qb(qb), ++i) {
+                const int s = i & 1;
+                // Q(i) into stage s once dK(i - 2) has read it; dO(i) once dV(i - 1) has
+                if (!mbar_wait_warp(bar(S::B_QEMPTY + s), ((uint32_t)(i >> 1) & 1u) ^ 1u, g, 0x121) ||
+                    !mbar_wait_warp(bar(S::B_DOEMPTY), ((uint32_t)i & 1u) ^ 1u, g, 0x122)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(bar(S::B_QFULL + s), S::TILE);
+                    mbar_arrive_expect_tx(bar(S::B_DOFULL), S::TILE);
+                    for (int c = 0; c < 2; ++c) {
+                        tma_load_3d(base + S::OFF_Q + s * S::TILE + c * S::CHUNK, &p.tmQ, bar(S::B_QFULL + s),
+                                    c * 64, qb * BQ, bh);
+                        tma_load_3d(base + S::OFF_DO + c * S::CHUNK, &p.tmdO, bar(S::B_DOFULL), c * 64, qb * BQ,
+                                    bh);
+                    }
+                }
+                nl = i + 1;
+                // LSE (log2 domain; +inf past N or for a row with no visible
+                // key: its P is 0) and D of the block, once the previous
+                // block's are consumed
+                if (!mbar_wait_warp(bar(S::B_LSEFREE), ((uint32_t)i & 1u) ^ 1u, g, 0x123)) {
+                    ok = false;
+                    break;
+                }
+                const int qa = qb * BQ;
+                for (int t = lane; t < BQ; t += 32) {
+                    const int qq = qa + t;
+                    float v = INFINITY, dd = 0.f;
+                    if (qq < p.N) {
+                        const float L = p.LSE[(size_t)bh * p.N + qq];
+                        v = (L == -INFINITY) ? INFINITY : L * 1.4426950408889634f;
+                        dd = p.Dvec[(size_t)bh * p.N + qq];
+                    }
+                    lse_s[t] = v;
+                    dv_s[t] = dd;
+                }
+                mbar_arrive(bar(S::B_LSE));
+            }
+            if (!ok && lane == 0) {
+                // gave up: let every copy already issued land before the CTA exits
+                b128_drain_wait(bar(S::B_KV), 0);
+                for (int j = (nl > 2 ? nl - 2 : 0); j < nl; ++j)
+                    b128_drain_wait(bar(S::B_QFULL + (j & 1)), (uint32_t)(j >> 1) & 1u);
+                if (nl > 0) b128_drain_wait(bar(S::B_DOFULL), (uint32_t)(nl - 1) & 1u);
+            }
+        } else if (warp == 1 && lane == 0) {
+            // ---------------------------------------------------------- MMA issuer
+            // Order per block i: dV(i), dK(i), dQ^T(i), S^T(i+1), dP^T(i+1).
+            constexpr uint32_t IDESC_S = idesc_bf16(128, BQ, false, false);   // S^T, dP^T
+            constexpr uint32_t IDESC_ACC = idesc_bf16(128, 128, false, true); // dV, dK: B MN-major
+            constexpr uint32_t IDESC_DQ = idesc_bf16(128, BQ, true, true);    // dQ^T = K^T dS^T
+            const uint64_t dK_kmaj = sdesc_sw128(base + S::OFF_K, 16, 1024);
+            const uint64_t dV_kmaj = sdesc_sw128(base + S::OFF_V, 16, 1024);
+            const uint64_t dQ_kmaj = sdesc_sw128(base + S::OFF_Q, 16, 1024);
+            const uint64_t ddO_kmaj = sdesc_sw128(base + S::OFF_DO, 16, 1024);
+            const uint64_t dQ_mn = sdesc_sw128(base + S::OFF_Q, S::CHUNK, 1024);
+            const uint64_t ddO_mn = sdesc_sw128(base + S::OFF_DO, S::CHUNK, 1024);
+            const uint64_t dK_mn = sdesc_sw128(base + S::OFF_K, S::CHUNK, 1024);
+            const uint64_t ddS_mn = sdesc_sw128(base + S::OFF_DS, S::CHUNK, 1024);
+            auto region = [&](int r) -> uint32_t { return tmem + S::TM_R0 + 128u * (uint32_t)r; };
+            // S^T(i) = K Q^T into region (i & 1)
+            auto issue_s = [&](int i) {
+                const uint64_t qd = sdesc_add(dQ_kmaj, (uint32_t)((i & 1) * S::TILE));
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint32_t off = (k >> 2) * S::CHUNK + (k & 3) * 32;
+                    mma_ss(region(i & 1), sdesc_add(dK_kmaj, off), sdesc_add(qd, off), IDESC_S, k > 0 ? 1u : 0u);
+                }
+                mma_commit(bar(S::B_SFULL));
+            };
+            // dP^T(i) = V dO^T into region (i & 1) ^ 1
+            auto issue_dp = [&](int i) {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint32_t off = (k >> 2) * S::CHUNK + (k & 3) * 32;
+                    mma_ss(region((i & 1) ^ 1), sdesc_add(dV_kmaj, off), sdesc_add(ddO_kmaj, off), IDESC_S,
+                           k > 0 ? 1u : 0u);
+                }
+                mma_commit(bar(S::B_DPFULL));
+            };
+            bool ok = true;
+            int i = 0;
+            if (first < p.Tqb) {
+                ok = mbar_wait(bar(S::B_KV), 0, g, 0x221) && mbar_wait(bar(S::B_QFULL), 0, g, 0x222) &&
+                     mbar_wait(bar(S::B_DOFULL), 0, g, 0x223);
+                if (ok) {
+                    tc_fence_after();
+                    issue_s(0);
+                    issue_dp(0);
+                }
+                for (int qb = first; ok && qb < p.Tqb; ++i) {
+                    const int s = i & 1;
+                    const uint32_t ra = region(s), rb = region(s ^ 1);
+                    const uint32_t acc0 = i > 0 ? 1u : 0u;
+                    const int qb_next = next_qb(qb);
+                    // dV += P^T dO: A = P^T (region a, packed), B = dO (MN-major)
+                    if (!mbar_wait(bar(S::B_PFULL), (uint32_t)i & 1u, g, 0x224)) { ok = false; break; }
+                    tc_fence_after();
+#pragma unroll
+                    for (int k = 0; k < BQ / 16; ++k)
+                        mma_ts(tmem + S::TM_DV, ra + packed_col128(k), sdesc_add(ddO_mn, (uint32_t)k * 2048u),
+                               IDESC_ACC, k > 0 ? 1u : acc0);
+                    mma_commit(bar(S::B_DVDONE));
+                    mma_commit(bar(S::B_DOEMPTY));
+                    // dK += dS^T Q: A = dS^T (region b, packed), B = Q (MN-major)
+                    if (!mbar_wait(bar(S::B_DSFULL), (uint32_t)i & 1u, g, 0x225)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint64_t q_mn = sdesc_add(dQ_mn, (uint32_t)(s * S::TILE));
+#pragma unroll
+                    for (int k = 0; k < BQ / 16; ++k)
+                        mma_ts(tmem + S::TM_DK, rb + packed_col128(k), sdesc_add(q_mn, (uint32_t)k * 2048u),
+                               IDESC_ACC, k > 0 ? 1u : acc0);
+                    mma_commit(bar(S::B_DKDONE));
+                    mma_commit(bar(S::B_QEMPTY + s));
+                    // dQ^T = K^T dS^T into region a, once dV has read P^T there
+                    if (!mbar_wait(bar(S::B_DVDONE), (uint32_t)i & 1u, g, 0x226)) { ok = false; break; }
+                    tc_fence_after();
+#pragma unroll
+                    for (int k = 0; k < kTile / 16; ++k)
+                        mma_ss(ra, sdesc_add(dK_mn, (uint32_t)k * 2048u), sdesc_add(ddS_mn, (uint32_t)k * 2048u),
+                               IDESC_DQ, k > 0 ? 1u : 0u);
+                    mma_commit(bar(S::B_DQFULL));
+                    if (qb_next < p.Tqb) {
+                        // S^T(i+1) into region b once dK has read dS^T there
+                        if (!mbar_wait(bar(S::B_QFULL + (s ^ 1)), (uint32_t)((i + 1) >> 1) & 1u, g, 0x227) ||
+                            !mbar_wait(bar(S::B_DKDONE), (uint32_t)i & 1u, g, 0x228)) { ok = false; break; }
+                        tc_fence_after();
+                        issue_s(i + 1);
+                        // dP^T(i+1) into region a once dQ^T(i) has been drained
+                        if (!mbar_wait(bar(S::B_DOFULL), (uint32_t)(i + 1) & 1u, g, 0x229) ||
+                            !mbar_wait(bar(S::B_DQFREE), (uint32_t)i & 1u, g, 0x22a)) { ok = false; break; }
+                        tc_fence_after();
+                        issue_dp(i + 1);
+                    }
+                    qb = qb_next;
+                }
+                if (ok) mma_commit(bar(S::B_ACC));
+            }
+            mma_commit(bar(S::B_FIN));
+            b128_drain_wait(bar(S::B_FIN), 0);
+        }
+    } else {
+        setmaxnreg_inc<S::REGS_COMPUTE>();
+        // ---------------------------------------------------------- compute (two warpgroups)
+        const int wg = (warp - 4) >> 2;
+        const int wq = warp & 3;
+        const int r = wq * 32 + lane;           // TMEM lane: key row (S^T, dP^T, dK, dV), head dim (dQ^T)
+        const int key = k0 + r;
+        const int c0 = wg * CW;
+        const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        const float c2 = p.scale_log2;
+        // this warp's dQ staging boxes (32 queries x 32 fp32, 128-byte swizzle):
+        // one in the staging area, one in the rows of the dS^T tile it writes
+        uint8_t *stg0 = sb + S::OFF_STG + (wg * 4 + wq) * 4096;
+        uint8_t *stg1 = sb + S::OFF_DS + wg * S::CHUNK + wq * 32 * 128;
+        bool ok = true;
+        int i = 0;
+
+        for (int qb = first; qb < p.Tqb; qb = next_qb(qb), ++i) {
+            const unsigned klass = cls(qb);
+            const int qa = qb * BQ;
+            const uint32_t ra = tmem + lane_off + S::TM_R0 + 128u * (uint32_t)(i & 1);
+            const uint32_t rb = tmem + lane_off + S::TM_R0 + 128u * (uint32_t)((i & 1) ^ 1);
+            if (!mbar_wait_warp(bar(S::B_LSE), (uint32_t)i & 1u, g, 0x421)) { ok = false; break; }
+
+            // P^T = 2^(s * c - LSE_q * log2 e), masked, for columns c0 .. c0 + 63.
+            // The block's LSE values go to registers before the wait: shared-memory
+            // loads inside the loop would queue behind the MMAs' operand reads.
+            if (!mbar_wait_warp(bar(S::B_SFULL), (uint32_t)i & 1u, g, 0x422)) { ok = false; break; }
+            tc_fence_after();
+            uint32_t pk[CW / 2];
+            {
+                uint32_t sr[2][32];
+                tmem_ld32(ra + c0, sr[0]);
+                tmem_ld32(ra + c0 + 32, sr[1]);
+                tmem_ld_wait(sr[0]);
+                tmem_ld_wait(sr[1]);
+                if (klass == kTilePartial) {
+                    // masked scores -> -inf, so that their p is exactly 0 (a mask
+                    // test inside the exp loop below made that loop several times slower)
+#pragma unroll
+                    for (int j = 0; j < 2; ++j)
+#pragma unroll
+                        for (int t = 0; t < 32; ++t) {
+                            const int qq = qa + c0 + 32 * j + t;
+                            if (key >= kvis || (p.causal && key > qq)) sr[j][t] = __float_as_uint(-INFINITY);
+                        }
+                }
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+#pragma unroll
+                    for (int t = 0; t < 32; t += 2) {
+                        const float2 l2 = *reinterpret_cast<const float2 *>(lse_s + c0 + 32 * j + t);
+                        const float lx = -l2.x, ly = -l2.y;
+                        float p0, p1;
+                        fma2(p0, p1, __uint_as_float(sr[j][t]), __uint_as_float(sr[j][t + 1]), c2, c2, lx, ly);
+                        pk[16 * j + t / 2] = pack_bf16x2(ex2(p0), ex2(p1));
+                    }
+            }
+            tmem_st16(ra + c0, pk);
+            tmem_st16(ra + c0 + 16, pk + 16);
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(bar(S::B_PFULL));
+
+            // dS^T = P^T o (dP^T - D): bf16 into region b (for dK) and the shared dS^T tile (for dQ);
+            // D to registers before the wait, as LSE above
+            if (!mbar_wait_warp(bar(S::B_DPFULL), (uint32_t)i & 1u, g, 0x423)) { ok = false; break; }
+            // this warp's rows of the dS^T tile hold its previous dQ staging box:
+            // its reduce must have read them
+            if (lane == 0) bulk_wait_group_read<0>();
+            __syncwarp();
+            tc_fence_after();
+            {
+                uint32_t dp[2][32];
+                tmem_ld32(rb + c0, dp[0]);
+                tmem_ld32(rb + c0 + 32, dp[1]);
+                tmem_ld_wait(dp[0]);
+                tmem_ld_wait(dp[1]);
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    uint32_t w[16];
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) {
+                        const uint32_t pp = pk[16 * j + t];
+                        const float2 d2 = *reinterpret_cast<const float2 *>(dv_s + c0 + 32 * j + 2 * t);
+                        const float dx = d2.x, dy = d2.y;
+                        const float d0 = __uint_as_float(dp[j][2 * t]) - dx;
+                        const float d1 = __uint_as_float(dp[j][2 * t + 1]) - dy;
+                        w[t] = pack_bf16x2(bf16lo(pp) * d0, bf16hi(pp) * d1);
+                    }
+                    tmem_st16(rb + c0 + 16u * j, w);
+                    // shared dS^T tile, queries contiguous (MN-major, 128-byte swizzle):
+                    // [query chunk of 64][key row 0..127][128 bytes]; this warpgroup's
+                    // 64 queries are chunk wg
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int qo = 32 * j + 8 * u;              // first query of this 16-byte piece, in the chunk
+                        uint8_t *dst = sb + S::OFF_DS + wg * S::CHUNK + r * 128 + ((((qo >> 3)) ^ (r & 7)) << 4);
+                        *reinterpret_cast<uint4 *>(dst) = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+                    }
+                }
+            }
+            tmem_st_wait();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar(S::B_DSFULL));
+            mbar_arrive(bar(S::B_LSEFREE));
+
+            // drain dQ^T(i): lane = head dimension 32 wq + lane, 64 query columns
+            if (!mbar_wait_warp(bar(S::B_DQFULL), (uint32_t)i & 1u, g, 0x424)) { ok = false; break; }
+            tc_fence_after();
+            uint32_t v[2][32];
+            tmem_ld32(ra + c0, v[0]);
+            tmem_ld32(ra + c0 + 32, v[1]);
+            tmem_ld_wait(v[0]);
+            tmem_ld_wait(v[1]);
+            tc_fence_before();
+            mbar_arrive(bar(S::B_DQFREE));
+            const int grp = lane >> 2;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint8_t *box = h == 0 ? stg0 : stg1;
+                uint8_t *cb = box + (lane & 3) * 4;
+#pragma unroll
+                for (int t = 0; t < 32; ++t)
+                    *reinterpret_cast<uint32_t *>(cb + t * 128 + ((grp ^ (t & 7)) << 4)) = v[h][t];
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                tma_reduce_add_3d(&p.tmdQ, smem_u32(stg0), wq * 32, qa + c0, bh);
+                tma_reduce_add_3d(&p.tmdQ, smem_u32(stg1), wq * 32, qa + c0 + 32, bh);
+                bulk_commit_group();
+            }
+        }
+        // the staged dQ boxes must be fully reduced before shared memory goes away
+        if (lane == 0) bulk_wait_group_all();
+        __syncwarp();
+
+        // ---------------------------------------------------------- epilogue: dK, dV
+        if (ok && i > 0) {
+            ok = mbar_wait_warp(bar(S::B_ACC), 0, g, 0x425);
+            tc_fence_after();
+        }
+        if (ok) {
+            __nv_bfloat16 *dkrow = reinterpret_cast<__nv_bfloat16 *>(p.dK) + ((size_t)bh * p.N + key) * 128;
+            __nv_bfloat16 *dvrow = reinterpret_cast<__nv_bfloat16 *>(p.dV) + ((size_t)bh * p.N + key) * 128;
+#pragma unroll 1
+            for (int j = wg * 2; j < wg * 2 + 2; ++j) {
+                uint32_t a[32], vv[32];
+                if (i > 0) {
+                    tmem_ld32(tmem + lane_off + S::TM_DK + 32u * j, a);
+                    tmem_ld32(tmem + lane_off + S::TM_DV + 32u * j, vv);
+                    tmem_ld_wait(a);
+                    tmem_ld_wait(vv);
+                } else {
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) a[t] = vv[t] = 0u;
+                }
+                uint32_t wk[16], wv[16];
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                    wk[t] = pack_bf16x2(__uint_as_float(a[2 * t]) * p.scale, __uint_as_float(a[2 * t + 1]) * p.scale);
+                    wv[t] = pack_bf16x2(__uint_as_float(vv[2 * t]), __uint_as_float(vv[2 * t + 1]));
+                }
+                if (key < p.N) {
+                    uint4 *dk4 = reinterpret_cast<uint4 *>(dkrow + 32 * j);
+                    uint4 *dv4 = reinterpret_cast<uint4 *>(dvrow + 32 * j);
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        dk4[t] = make_uint4(wk[4 * t], wk[4 * t + 1], wk[4 * t + 2], wk[4 * t + 3]);
+                        dv4[t] = make_uint4(wv[4 * t], wv[4 * t + 1], wv[4 * t + 2], wv[4 * t + 3]);
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        setmaxnreg_dec<S::REGS_CTRL>();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, S::TMEM_COLS);
+}
+
+}  // namespace
+
+int bwd128_smem_bytes() { return Bwd128::SMEM_BYTES; }
+
+cudaError_t launch_bwd128_main(const BwdParams &p, cudaStream_t st) {
+    const int smem = Bwd128::SMEM_BYTES;
+    cudaError_t e = cudaFuncSetAttribute(fa_bwd128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    fa_bwd128_kernel<<<(unsigned)p.Tk * (unsigned)p.BH, Bwd128::THREADS, smem, st>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace fa

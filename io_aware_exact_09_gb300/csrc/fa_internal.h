@@ -30,6 +30,9 @@ cudaError_t launch_bwd_main(int d, const BwdParams &p, cudaStream_t st);
 cudaError_t launch_bwd_convert(int d, const float *dQacc, void *dQ, int64_t elems, float scale,
                                cudaStream_t st);
 int bwd_query_block(int d);
+// d = 128: the 128-row query block kernel (fa_bwd128.cu).
+cudaError_t launch_bwd128_main(const BwdParams &p, cudaStream_t st);
+int bwd128_smem_bytes();
 int bwd_dq_box_rows(int d);
 int bwd_smem_bytes(int d);
 
