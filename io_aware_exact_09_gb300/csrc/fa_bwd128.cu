@@ -236,7 +236,7 @@ __global__ void __launch_bounds__(384, 1) fa_bwd128_kernel(const __grid_constant
             }
         } else if (warp == 1 && lane == 0) {
             // ---------------------------------------------------------- MMA issuer
-            // Order per block i: dV(i), dK(i), dQ^T(i), S^T(i+1), dP^T(i+1).
+            // Order per block i: dV(i), dQ^T(i), dK(i), S^T(i+1), dP^T(i+1).
             constexpr uint32_t IDESC_S = idesc_bf16(128, BQ, false, false);   // S^T, dP^T
             constexpr uint32_t IDESC_ACC = idesc_bf16(128, 128, false, true); // dV, dK: B MN-major
             constexpr uint32_t IDESC_DQ = idesc_bf16(128, BQ, true, true);    // dQ^T = K^T dS^T
@@ -293,9 +293,18 @@ __global__ void __launch_bounds__(384, 1) fa_bwd128_kernel(const __grid_constant
                                IDESC_ACC, k > 0 ? 1u : acc0);
                     mma_commit(bar(S::B_DVDONE));
                     mma_commit(bar(S::B_DOEMPTY));
-                    // dK += dS^T Q: A = dS^T (region b, packed), B = Q (MN-major)
-                    if (!mbar_wait(bar(S::B_DSFULL), (uint32_t)i & 1u, g, 0x225)) { ok = false; break; }
+                    // dQ^T = K^T dS^T into region a (once dV has read P^T there), first:
+                    // the compute warps drain it before the next block, so it is on
+                    // their critical path; dK follows
+                    if (!mbar_wait(bar(S::B_DSFULL), (uint32_t)i & 1u, g, 0x225) ||
+                        !mbar_wait(bar(S::B_DVDONE), (uint32_t)i & 1u, g, 0x226)) { ok = false; break; }
                     tc_fence_after();
+#pragma unroll
+                    for (int k = 0; k < kTile / 16; ++k)
+                        mma_ss(ra, sdesc_add(dK_mn, (uint32_t)k * 2048u), sdesc_add(ddS_mn, (uint32_t)k * 2048u),
+                               IDESC_DQ, k > 0 ? 1u : 0u);
+                    mma_commit(bar(S::B_DQFULL));
+                    // dK += dS^T Q: A = dS^T (region b, packed), B = Q (MN-major)
                     const uint64_t q_mn = sdesc_add(dQ_mn, (uint32_t)(s * S::TILE));
 #pragma unroll
                     for (int k = 0; k < BQ / 16; ++k)
@@ -303,14 +312,6 @@ __global__ void __launch_bounds__(384, 1) fa_bwd128_kernel(const __grid_constant
                                IDESC_ACC, k > 0 ? 1u : acc0);
                     mma_commit(bar(S::B_DKDONE));
                     mma_commit(bar(S::B_QEMPTY + s));
-                    // dQ^T = K^T dS^T into region a, once dV has read P^T there
-                    if (!mbar_wait(bar(S::B_DVDONE), (uint32_t)i & 1u, g, 0x226)) { ok = false; break; }
-                    tc_fence_after();
-#pragma unroll
-                    for (int k = 0; k < kTile / 16; ++k)
-                        mma_ss(ra, sdesc_add(dK_mn, (uint32_t)k * 2048u), sdesc_add(ddS_mn, (uint32_t)k * 2048u),
-                               IDESC_DQ, k > 0 ? 1u : 0u);
-                    mma_commit(bar(S::B_DQFULL));
                     if (qb_next < p.Tqb) {
                         // S^T(i+1) into region b once dK has read dS^T there
                         if (!mbar_wait(bar(S::B_QFULL + (s ^ 1)), (uint32_t)((i + 1) >> 1) & 1u, g, 0x227) ||
