@@ -58,7 +58,8 @@ struct F8Shape {
     static constexpr int B_PFULL = B_SFREE + 2;             // [2]
     static constexpr int B_PVDONE = B_PFULL + 2;            // [2]
     static constexpr int B_PFREE = B_PVDONE + 2;            // [2][2] per query tile and P buffer
-    static constexpr int B_FIN = B_PFREE + 4;
+    static constexpr int B_OFULL = B_PFREE + 4;             // [2] every product done (single use)
+    static constexpr int B_FIN = B_OFULL + 2;
     static constexpr int NBAR = B_FIN + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
@@ -149,6 +150,8 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
             mbar_init(bar(S::B_PVDONE + j), 1);
         }
         for (int j = 0; j < 4; ++j) mbar_init(bar(S::B_PFREE + j), 1);
+        mbar_init(bar(S::B_OFULL + 0), 1);
+        mbar_init(bar(S::B_OFULL + 1), 1);
         mbar_init(bar(S::B_FIN), 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -284,6 +287,14 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
                     mma_commit(bar(S::B_KVEMPTY + s));
                     kt = kt_next;
                     ++u;
+                }
+                // O_x is final once every product is done.  The softmax warps run
+                // ahead of the P.V products (P lives in shared memory), so they
+                // may reach their epilogue two PVDONE phases early, where a parity
+                // wait cannot tell the phases apart: they wait on this instead.
+                if (ok) {
+                    mma_commit(bar(S::B_OFULL + 0));
+                    mma_commit(bar(S::B_OFULL + 1));
                 }
                 mma_commit(bar(S::B_FIN));
                 f8_drain_wait(bar(S::B_FIN), 0);
@@ -454,7 +465,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
         }
         // ---------------------------------------------------------- epilogue
         if (ok && it > 0) {
-            ok = mbar_wait_warp(bar(S::B_PVDONE + x), (uint32_t)(it - 1) & 1u, g, 0x414);
+            ok = mbar_wait_warp(bar(S::B_OFULL + x), 0u, g, 0x414);
             tc_fence_after();
         }
         if (ok) {
