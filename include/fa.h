@@ -282,6 +282,20 @@ fa_status fa_get_device_status(const void *workspace, void *stream);
 /* Enqueue a clear of the workspace status word on stream. */
 fa_status fa_reset_device_status(void *workspace, void *stream);
 
+/*
+ * Failure-path self-test.  Launches one warp that waits, with the same
+ * bounded wait every kernel here uses for its barriers, on a barrier phase
+ * that nothing completes.  The wait gives up after the kernels' wait limit
+ * (2 s), records FA_ERR_DEVICE_TIMEOUT in the workspace status word (word 1:
+ * the wait site, 0x5e1f) and raises the CTA's abort flag; a second wait
+ * returns at once through that flag; the kernel then exits normally.
+ * workspace: zero-filled device memory of at least 32 bytes; besides the
+ * status words it receives in words 4..6 the outcome of the two waits
+ * (0 = gave up) and 1 if the second wait returned well before the limit.
+ * No GPU fault, trap or hang is involved: the context stays usable.
+ */
+fa_status fa_selftest_wait_timeout(void *workspace, size_t workspace_bytes, void *stream);
+
 /* Static string for a status code. */
 const char *fa_status_string(fa_status s);
 

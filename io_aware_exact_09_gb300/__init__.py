@@ -90,6 +90,8 @@ def lib():
             L.fa_attention_host.restype = i
             L.fa_get_device_status.argtypes = [vp, vp]
             L.fa_get_device_status.restype = i
+            L.fa_selftest_wait_timeout.argtypes = [vp, sz, vp]
+            L.fa_selftest_wait_timeout.restype = i
             L.fa_reset_device_status.argtypes = [vp, vp]
             L.fa_reset_device_status.restype = i
             L.fa_status_string.argtypes = [i]
@@ -103,7 +105,7 @@ EXPORTED = ("fa_tile_size", "fa_fwd_workspace_size", "fa_bwd_workspace_size", "f
             "fa_decode_workspace_size", "fa_decode", "fa_fwd_tiles", "fa_fwd_varlen", "fa_quantize_fp8", "fa_fwd_fp8",
             "fa_tile_plan",
             "fa_host_workspace_size", "fa_attention_host", "fa_get_device_status", "fa_reset_device_status",
-            "fa_status_string")
+            "fa_selftest_wait_timeout", "fa_status_string")
 
 
 # ---------------------------------------------------------------- marshalling helpers
@@ -257,6 +259,10 @@ def fa_attention_host(Q, K, V, dO, O, LSE, dQ, dK, dV, B, H, N, d, softmax_scale
 
 def fa_get_device_status(workspace, stream=None) -> int:
     return lib().fa_get_device_status(_p(workspace), _stream(stream))
+
+
+def fa_selftest_wait_timeout(workspace, workspace_bytes, stream=None) -> int:
+    return lib().fa_selftest_wait_timeout(_p(workspace), int(workspace_bytes), _stream(stream))
 
 
 def fa_reset_device_status(workspace, stream=None) -> int:

@@ -549,6 +549,14 @@ fa_status fa_get_device_status(const void *workspace, void *stream) {
     return static_cast<fa_status>(w[0]);
 }
 
+fa_status fa_selftest_wait_timeout(void *workspace, size_t workspace_bytes, void *stream) {
+    if (!workspace || !aligned16(workspace) || workspace_bytes < 32) return FA_ERR_WORKSPACE;
+    unsigned *w = static_cast<unsigned *>(workspace);
+    // words 0 and 1: status and wait site (as for every kernel); 4..6: the test's own results
+    return fa::launch_selftest_wait(w, w + 4, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK
+                                                                                                : FA_ERR_CUDA;
+}
+
 fa_status fa_reset_device_status(void *workspace, void *stream) {
     if (!workspace) return FA_ERR_WORKSPACE;
     return cudaMemsetAsync(workspace, 0, 8, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK

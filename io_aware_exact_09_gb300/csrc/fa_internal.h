@@ -41,6 +41,9 @@ cudaError_t launch_decode(int d, const DecParams &p, cudaStream_t st);
 cudaError_t launch_decode_merge(int d, const float *Opart, const float *Lpart, void *O, float *LSE,
                                 int64_t rows, int splits, cudaStream_t st);
 
+// Failure-path self-test: a bounded wait on a barrier nothing completes.
+cudaError_t launch_selftest_wait(unsigned *status, unsigned *result, cudaStream_t st);
+
 // Plan export.
 cudaError_t launch_plan(int B, int N, int causal, const int32_t *key_len,
                         const uint8_t *block_mask, uint8_t *plan, unsigned *status,

@@ -110,3 +110,11 @@ def test_decode_argument_errors(L):
     assert dec(256, 256, 256, 256, 256, 1, 1, 0, 1000, 128, 0.1, 0, None, 0, None, 0, None) == 0
     # more splits requested than key tiles: the workspace query caps it the same way
     assert fa.fa_decode_workspace_size(1, 1, 1, 1000, 128, 1000) == fa.fa_decode_workspace_size(1, 1, 1, 1000, 128, 8)
+
+
+def test_selftest_argument_errors(L):
+    # rejected before any launch: no workspace, or too small for its result words
+    st = fa.lib().fa_selftest_wait_timeout
+    assert st(None, 256, None) == 3
+    assert st(256, 16, None) == 3
+    assert st(258, 256, None) == 3
