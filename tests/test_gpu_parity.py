@@ -6,7 +6,7 @@ import torch
 
 import oracle
 from synthetic import WORKLOADS, make_case, make_inputs
-from gpu_common import (check_forward, check_grads, f64, oracle_args, run_cuda, to_dev)
+from gpu_common import (GRAD_REL_FRO, check_forward, check_grads, f64, oracle_args, rel_fro, run_cuda, to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -137,6 +137,32 @@ def test_repeat_calls_are_deterministic_backward(d):
     for _ in range(4):
         again = fa.attention_backward(g["Q"], g["K"], g["V"], O, L, g["dO"], causal=True, key_len=kl)
         assert torch.equal(first[1], again[1]) and torch.equal(first[2], again[2])
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_backward_stages_match_fa_bwd(d):
+    """fa_bwd_preprocess, fa_bwd_main and fa_bwd_postprocess enqueued one by
+    one: dK and dV bit for bit as fa_bwd; dQ (summed by reduce-adds, whose
+    order varies) within the parity bound of the same oracle."""
+    import io_aware_exact_09_gb300 as fa
+    B, H, N = 2, 2, 333
+    c = make_case(B, H, N, d, seed=23 + d, causal=True, key_len=[333, 200],
+                  block_mask=[[1, 0, 1], [1, 1, 0], [0, 1, 1]])
+    g = to_dev(c, "cuda")
+    O, L = fa.attention_forward(g["Q"], g["K"], g["V"], c["scale"], True, g["key_len"], g["block_mask"])
+    ref = fa.attention_backward(g["Q"], g["K"], g["V"], O, L, g["dO"], c["scale"], True, g["key_len"],
+                                g["block_mask"], check_status=True)
+    n = fa.fa_bwd_workspace_size(B, H, N, d)
+    ws = fa.workspace(n, "cuda")
+    dQ, dK, dV = (torch.empty_like(g["Q"]) for _ in range(3))
+    assert fa.fa_bwd_preprocess(O, g["dO"], B, H, N, d, ws, n) == 0
+    assert fa.fa_bwd_main(g["Q"], g["K"], g["V"], L, g["dO"], dK, dV, B, H, N, d, c["scale"], 1, g["key_len"],
+                          g["block_mask"], ws, n) == 0
+    assert fa.fa_bwd_postprocess(dQ, B, H, N, d, c["scale"], ws, n) == 0
+    assert fa.fa_get_device_status(ws) == 0
+    assert torch.equal(dK, ref[1]) and torch.equal(dV, ref[2])
+    rdQ = oracle.attention_bwd(f64(c["Q"]), f64(c["K"]), f64(c["V"]), f64(c["dO"]), c["scale"], **oracle_args(c))[2]
+    assert rel_fro(dQ.double().cpu().numpy(), rdQ) <= GRAD_REL_FRO
 
 
 @pytest.mark.parametrize("block_q,block_k", [(256, 64), (128, 128), (128, 64)])
