@@ -53,7 +53,7 @@ def _compile(src: str) -> str:
 # launch; a different allocation would make setmaxnreg.inc wait forever, so
 # the build refuses it.
 REGISTER_SPLIT_KERNELS = {"fa_fwd.cu": ("fa_fwd_kernel", 168), "fa_fwd_fp8.cu": ("fa_fwd_fp8_kernel", 168),
-                          "fa_bwd128.cu": ("fa_bwd128_kernel", 168)}
+                          "fa_bwd128.cu": ("fa_bwd128_kernel", 128)}
 
 
 def _check_register_split(src: str) -> None:

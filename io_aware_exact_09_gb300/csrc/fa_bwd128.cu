@@ -20,15 +20,18 @@
 //     block i+1: S^T(i+1) -> region b once dK(i) is done,
 //                dP^T(i+1) -> region a once dQ^T(i) has been drained.
 // Shared memory (224 KB): K, V; Q double-buffered, dO single; the dS^T tile
-// (the dQ MMA's B operand); 32 KB of dQ staging.  Each compute warp stages its
-// dQ^T rows in two 4 KB boxes: one in its own slice of the staging area, one
-// in the slice of the dS^T tile that it alone writes (free once dQ^T(i) has
-// been computed; the warp waits for its own reduce reads before writing the
-// next dS^T there).
+// (the dQ MMA's B operand); 32 KB of dQ staging.
 //
-// Roles (384 threads): warp 0 TMA producer (and, whole warp, the LSE/D
+// Roles (512 threads): warp 0 TMA producer (and, whole warp, the LSE/D
 // staging); warp 1 tcgen05 issuer; warps 4-7 and 8-11 two compute warpgroups,
-// one key row per thread, warpgroup w on query columns [64w, 64w + 64).
+// one key row per thread, warpgroup w on query columns [64w, 64w + 64);
+// warps 12-15 the dQ drain, one head-dimension row of dQ^T per thread: TMEM
+// -> swizzled shared staging (two halves of 64 query columns, 8 KB per warp)
+// -> TMA reduce-add into the fp32 accumulator.  The drain has its own
+// warpgroup because on the compute warps it cost ~45 % of every block (a
+// clock64 trace: staging stores queue behind the SS MMAs' operand reads, and
+// the staging area shared with the dS^T tile made them wait for the previous
+// reduce); off their path, the compute chain per block is P -> dS only.
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
 
@@ -46,7 +49,7 @@ struct Bwd128 {
     static constexpr int OFF_Q = OFF_V + TILE;             // [2]
     static constexpr int OFF_DO = OFF_Q + 2 * TILE;
     static constexpr int OFF_DS = OFF_DO + TILE;           // [query chunk 2][key 128][128 B]
-    static constexpr int OFF_STG = OFF_DS + TILE;          // [8 warps][32 queries][128 B]
+    static constexpr int OFF_STG = OFF_DS + TILE;          // [4 drain warps][2 boxes][32 queries][128 B]
     static constexpr int OFF_LSE = OFF_STG + 8 * 4096;     // [BQ] fp32, log2 domain
     static constexpr int OFF_DV = OFF_LSE + BQ * 4;        // [BQ] fp32
     static constexpr int OFF_BAR = OFF_DV + BQ * 4;
@@ -64,7 +67,7 @@ struct Bwd128 {
     static constexpr int B_DVDONE = 13;
     static constexpr int B_DKDONE = 14;
     static constexpr int B_DQFULL = 15;
-    static constexpr int B_DQFREE = 16;                    // 256
+    static constexpr int B_DQFREE = 16;                    // 128 (drain warpgroup)
     static constexpr int B_ACC = 17;
     static constexpr int B_FIN = 18;
     static constexpr int NBAR = 19;
@@ -75,11 +78,13 @@ struct Bwd128 {
     static constexpr uint32_t TM_R0 = 0;                   // regions a / b: 128 columns each
     static constexpr uint32_t TM_DV = 256;
     static constexpr uint32_t TM_DK = 384;
-    static constexpr int THREADS = 384;
-    static constexpr int LAUNCH_REGS = 168;
-    static constexpr int REGS_CTRL = 136;
-    static constexpr int REGS_COMPUTE = 184;
-    static_assert(128 * REGS_CTRL + 256 * REGS_COMPUTE == THREADS * LAUNCH_REGS, "register split");
+    static constexpr int THREADS = 512;
+    static constexpr int LAUNCH_REGS = 128;
+    static constexpr int REGS_CTRL = 112;
+    static constexpr int REGS_COMPUTE = 152;
+    static constexpr int REGS_DRAIN = 96;
+    static_assert(128 * REGS_CTRL + 256 * REGS_COMPUTE + 128 * REGS_DRAIN == THREADS * LAUNCH_REGS,
+                  "register split");
 };
 
 __device__ __forceinline__ void b128_drain_wait(uint32_t bar, uint32_t parity) {
@@ -93,7 +98,7 @@ __device__ __forceinline__ void b128_drain_wait(uint32_t bar, uint32_t parity) {
 // 64-column half, so neither overwrites fp32 values the other still reads.
 __device__ __forceinline__ uint32_t packed_col128(int k) { return (uint32_t)((k >> 2) * 64 + 8 * (k & 3)); }
 
-__global__ void __launch_bounds__(384, 1) fa_bwd128_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant__ BwdParams p) {
     using S = Bwd128;
     constexpr int BQ = S::BQ, CW = S::CW;
     extern __shared__ uint8_t smem_raw[];
@@ -151,7 +156,7 @@ __global__ void __launch_bounds__(384, 1) fa_bwd128_kernel(const __grid_constant
         mbar_init(bar(S::B_DVDONE), 1);
         mbar_init(bar(S::B_DKDONE), 1);
         mbar_init(bar(S::B_DQFULL), 1);
-        mbar_init(bar(S::B_DQFREE), 256);
+        mbar_init(bar(S::B_DQFREE), 128);
         mbar_init(bar(S::B_ACC), 1);
         mbar_init(bar(S::B_FIN), 1);
         *abort_flag = 0;
@@ -294,8 +299,8 @@ __global__ void __launch_bounds__(384, 1) fa_bwd128_kernel(const __grid_constant
                     mma_commit(bar(S::B_DVDONE));
                     mma_commit(bar(S::B_DOEMPTY));
                     // dQ^T = K^T dS^T into region a (once dV has read P^T there), first:
-                    // the compute warps drain it before the next block, so it is on
-                    // their critical path; dK follows
+                    // the sooner it is drained, the sooner dP^T(i+1) can use region a;
+                    // dK follows
                     if (!mbar_wait(bar(S::B_DSFULL), (uint32_t)i & 1u, g, 0x225) ||
                         !mbar_wait(bar(S::B_DVDONE), (uint32_t)i & 1u, g, 0x226)) { ok = false; break; }
                     tc_fence_after();
@@ -331,7 +336,7 @@ __global__ void __launch_bounds__(384, 1) fa_bwd128_kernel(const __grid_constant
             mma_commit(bar(S::B_FIN));
             b128_drain_wait(bar(S::B_FIN), 0);
         }
-    } else {
+    } else if (warp < 12) {
         setmaxnreg_inc<S::REGS_COMPUTE>();
         // ---------------------------------------------------------- compute (two warpgroups)
         const int wg = (warp - 4) >> 2;
@@ -341,10 +346,6 @@ __global__ void __launch_bounds__(384, 1) fa_bwd128_kernel(const __grid_constant
         const int c0 = wg * CW;
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const float c2 = p.scale_log2;
-        // this warp's dQ staging boxes (32 queries x 32 fp32, 128-byte swizzle):
-        // one in the staging area, one in the rows of the dS^T tile it writes
-        uint8_t *stg0 = sb + S::OFF_STG + (wg * 4 + wq) * 4096;
-        uint8_t *stg1 = sb + S::OFF_DS + wg * S::CHUNK + wq * 32 * 128;
         bool ok = true;
         int i = 0;
 
@@ -398,10 +399,6 @@ __global__ void __launch_bounds__(384, 1) fa_bwd128_kernel(const __grid_constant
             // dS^T = P^T o (dP^T - D): bf16 into region b (for dK) and the shared dS^T tile (for dQ);
             // D to registers before the wait, as LSE above
             if (!mbar_wait_warp(bar(S::B_DPFULL), (uint32_t)i & 1u, g, 0x423)) { ok = false; break; }
-            // this warp's rows of the dS^T tile hold its previous dQ staging box:
-            // its reduce must have read them
-            if (lane == 0) bulk_wait_group_read<0>();
-            __syncwarp();
             tc_fence_after();
             {
                 uint32_t dp[2][32];
@@ -438,37 +435,7 @@ __global__ void __launch_bounds__(384, 1) fa_bwd128_kernel(const __grid_constant
             tc_fence_before();
             mbar_arrive(bar(S::B_DSFULL));
             mbar_arrive(bar(S::B_LSEFREE));
-
-            // drain dQ^T(i): lane = head dimension 32 wq + lane, 64 query columns
-            if (!mbar_wait_warp(bar(S::B_DQFULL), (uint32_t)i & 1u, g, 0x424)) { ok = false; break; }
-            tc_fence_after();
-            uint32_t v[2][32];
-            tmem_ld32(ra + c0, v[0]);
-            tmem_ld32(ra + c0 + 32, v[1]);
-            tmem_ld_wait(v[0]);
-            tmem_ld_wait(v[1]);
-            tc_fence_before();
-            mbar_arrive(bar(S::B_DQFREE));
-            const int grp = lane >> 2;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint8_t *box = h == 0 ? stg0 : stg1;
-                uint8_t *cb = box + (lane & 3) * 4;
-#pragma unroll
-                for (int t = 0; t < 32; ++t)
-                    *reinterpret_cast<uint32_t *>(cb + t * 128 + ((grp ^ (t & 7)) << 4)) = v[h][t];
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                tma_reduce_add_3d(&p.tmdQ, smem_u32(stg0), wq * 32, qa + c0, bh);
-                tma_reduce_add_3d(&p.tmdQ, smem_u32(stg1), wq * 32, qa + c0 + 32, bh);
-                bulk_commit_group();
-            }
         }
-        // the staged dQ boxes must be fully reduced before shared memory goes away
-        if (lane == 0) bulk_wait_group_all();
-        __syncwarp();
 
         // ---------------------------------------------------------- epilogue: dK, dV
         if (ok && i > 0) {
@@ -509,6 +476,56 @@ __global__ void __launch_bounds__(384, 1) fa_bwd128_kernel(const __grid_constant
         }
         __syncwarp();
         setmaxnreg_dec<S::REGS_CTRL>();
+    } else {
+        setmaxnreg_dec<S::REGS_DRAIN>();
+        // ---------------------------------------------------------- dQ drain (one warpgroup)
+        // lane = head dimension 32 wq + lane of dQ^T(i); 128 query columns in two
+        // halves through this warp's two staging boxes (32 queries x 32 fp32,
+        // 128-byte swizzle)
+        const int wq = warp & 3;
+        const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        uint8_t *stg = sb + S::OFF_STG + wq * 8192;
+        const int grp = lane >> 2;
+        int i = 0;
+        for (int qb = first; qb < p.Tqb; qb = next_qb(qb), ++i) {
+            const uint32_t ra = tmem + lane_off + S::TM_R0 + 128u * (uint32_t)(i & 1);
+            if (!mbar_wait_warp(bar(S::B_DQFULL), (uint32_t)i & 1u, g, 0x426)) break;
+            tc_fence_after();
+#pragma unroll 1
+            for (int h = 0; h < 2; ++h) {
+                uint32_t v[2][32];
+                tmem_ld32(ra + 64u * h, v[0]);
+                tmem_ld32(ra + 64u * h + 32, v[1]);
+                tmem_ld_wait(v[0]);
+                tmem_ld_wait(v[1]);
+                if (h == 1) {
+                    // all of dQ^T(i) is in registers or staged: region a is free
+                    tc_fence_before();
+                    mbar_arrive(bar(S::B_DQFREE));
+                }
+                // the boxes' previous reduce must have read them
+                if (lane == 0) bulk_wait_group_read<0>();
+                __syncwarp();
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    uint8_t *cb = stg + u * 4096 + (lane & 3) * 4;
+#pragma unroll
+                    for (int t = 0; t < 32; ++t)
+                        *reinterpret_cast<uint32_t *>(cb + t * 128 + ((grp ^ (t & 7)) << 4)) = v[u][t];
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    const int q0 = qb * BQ + 64 * h;
+                    tma_reduce_add_3d(&p.tmdQ, smem_u32(stg), wq * 32, q0, bh);
+                    tma_reduce_add_3d(&p.tmdQ, smem_u32(stg + 4096), wq * 32, q0 + 32, bh);
+                    bulk_commit_group();
+                }
+            }
+        }
+        // the staged boxes must be fully reduced before shared memory goes away
+        if (lane == 0) bulk_wait_group_all();
+        __syncwarp();
     }
 
     tc_fence_before();
