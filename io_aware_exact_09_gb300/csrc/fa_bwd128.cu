@@ -57,15 +57,13 @@ struct Bwd128 {
     static constexpr int B_QFULL = 1;                      // [2]
     static constexpr int B_QEMPTY = 3;                     // [2]
     static constexpr int B_DOFULL = 5;
-    static constexpr int B_DOEMPTY = 6;
     static constexpr int B_LSE = 7;                        // LSE/D staged (32 arrivals)
     static constexpr int B_LSEFREE = 8;                    // LSE/D consumed (256)
     static constexpr int B_SFULL = 9;
     static constexpr int B_DPFULL = 10;
     static constexpr int B_PFULL = 11;                     // 256
     static constexpr int B_DSFULL = 12;                    // 256
-    static constexpr int B_DVDONE = 13;
-    static constexpr int B_DKDONE = 14;
+    static constexpr int B_DVDONE = 13;                    // dV(i) done: dO free, region a readable
     static constexpr int B_DQFULL = 15;
     static constexpr int B_DQFREE = 16;                    // 128 (drain warpgroup)
     static constexpr int B_ACC = 17;
@@ -146,7 +144,6 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
             mbar_init(bar(S::B_QEMPTY + s), 1);
         }
         mbar_init(bar(S::B_DOFULL), 1);
-        mbar_init(bar(S::B_DOEMPTY), 1);
         mbar_init(bar(S::B_LSE), 32);
         mbar_init(bar(S::B_LSEFREE), 256);
         mbar_init(bar(S::B_SFULL), 1);
@@ -154,7 +151,6 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
         mbar_init(bar(S::B_PFULL), 256);
         mbar_init(bar(S::B_DSFULL), 256);
         mbar_init(bar(S::B_DVDONE), 1);
-        mbar_init(bar(S::B_DKDONE), 1);
         mbar_init(bar(S::B_DQFULL), 1);
         mbar_init(bar(S::B_DQFREE), 128);
         mbar_init(bar(S::B_ACC), 1);
@@ -196,7 +192,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
                 const int s = i & 1;
                 // Q(i) into stage s once dK(i - 2) has read it; dO(i) once dV(i - 1) has
                 if (!mbar_wait_warp(bar(S::B_QEMPTY + s), ((uint32_t)(i >> 1) & 1u) ^ 1u, g, 0x121) ||
-                    !mbar_wait_warp(bar(S::B_DOEMPTY), ((uint32_t)i & 1u) ^ 1u, g, 0x122)) {
+                    !mbar_wait_warp(bar(S::B_DVDONE), ((uint32_t)i & 1u) ^ 1u, g, 0x122)) {
                     ok = false;
                     break;
                 }
@@ -297,7 +293,6 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
                         mma_ts(tmem + S::TM_DV, ra + packed_col128(k), sdesc_add(ddO_mn, (uint32_t)k * 2048u),
                                IDESC_ACC, k > 0 ? 1u : acc0);
                     mma_commit(bar(S::B_DVDONE));
-                    mma_commit(bar(S::B_DOEMPTY));
                     // dQ^T = K^T dS^T into region a (once dV has read P^T there), first:
                     // the sooner it is drained, the sooner dP^T(i+1) can use region a;
                     // dK follows
@@ -315,12 +310,11 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
                     for (int k = 0; k < BQ / 16; ++k)
                         mma_ts(tmem + S::TM_DK, rb + packed_col128(k), sdesc_add(q_mn, (uint32_t)k * 2048u),
                                IDESC_ACC, k > 0 ? 1u : acc0);
-                    mma_commit(bar(S::B_DKDONE));
-                    mma_commit(bar(S::B_QEMPTY + s));
+                    mma_commit(bar(S::B_QEMPTY + s));       // dK(i) done
                     if (qb_next < p.Tqb) {
                         // S^T(i+1) into region b once dK has read dS^T there
                         if (!mbar_wait(bar(S::B_QFULL + (s ^ 1)), (uint32_t)((i + 1) >> 1) & 1u, g, 0x227) ||
-                            !mbar_wait(bar(S::B_DKDONE), (uint32_t)i & 1u, g, 0x228)) { ok = false; break; }
+                            !mbar_wait(bar(S::B_QEMPTY + s), (uint32_t)(i >> 1) & 1u, g, 0x228)) { ok = false; break; }
                         tc_fence_after();
                         issue_s(i + 1);
                         // dP^T(i+1) into region a once dQ^T(i) has been drained
@@ -382,12 +376,14 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
 #pragma unroll
                 for (int j = 0; j < 2; ++j)
 #pragma unroll
-                    for (int t = 0; t < 32; t += 2) {
-                        const float2 l2 = *reinterpret_cast<const float2 *>(lse_s + c0 + 32 * j + t);
-                        const float lx = -l2.x, ly = -l2.y;
-                        float p0, p1;
-                        fma2(p0, p1, __uint_as_float(sr[j][t]), __uint_as_float(sr[j][t + 1]), c2, c2, lx, ly);
+                    for (int t = 0; t < 32; t += 4) {
+                        const float4 l4 = *reinterpret_cast<const float4 *>(lse_s + c0 + 32 * j + t);
+                        float p0, p1, p2, p3;
+                        fma2(p0, p1, __uint_as_float(sr[j][t]), __uint_as_float(sr[j][t + 1]), c2, c2, -l4.x, -l4.y);
+                        fma2(p2, p3, __uint_as_float(sr[j][t + 2]), __uint_as_float(sr[j][t + 3]), c2, c2, -l4.z,
+                             -l4.w);
                         pk[16 * j + t / 2] = pack_bf16x2(ex2(p0), ex2(p1));
+                        pk[16 * j + t / 2 + 1] = pack_bf16x2(ex2(p2), ex2(p3));
                     }
             }
             tmem_st16(ra + c0, pk);
@@ -410,13 +406,13 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
                 for (int j = 0; j < 2; ++j) {
                     uint32_t w[16];
 #pragma unroll
-                    for (int t = 0; t < 16; ++t) {
-                        const uint32_t pp = pk[16 * j + t];
-                        const float2 d2 = *reinterpret_cast<const float2 *>(dv_s + c0 + 32 * j + 2 * t);
-                        const float dx = d2.x, dy = d2.y;
-                        const float d0 = __uint_as_float(dp[j][2 * t]) - dx;
-                        const float d1 = __uint_as_float(dp[j][2 * t + 1]) - dy;
-                        w[t] = pack_bf16x2(bf16lo(pp) * d0, bf16hi(pp) * d1);
+                    for (int t = 0; t < 16; t += 2) {
+                        const float4 d4 = *reinterpret_cast<const float4 *>(dv_s + c0 + 32 * j + 2 * t);
+                        const uint32_t pa = pk[16 * j + t], pb = pk[16 * j + t + 1];
+                        w[t] = pack_bf16x2(bf16lo(pa) * (__uint_as_float(dp[j][2 * t]) - d4.x),
+                                           bf16hi(pa) * (__uint_as_float(dp[j][2 * t + 1]) - d4.y));
+                        w[t + 1] = pack_bf16x2(bf16lo(pb) * (__uint_as_float(dp[j][2 * t + 2]) - d4.z),
+                                               bf16hi(pb) * (__uint_as_float(dp[j][2 * t + 3]) - d4.w));
                     }
                     tmem_st16(rb + c0 + 16u * j, w);
                     // shared dS^T tile, queries contiguous (MN-major, 128-byte swizzle):
