@@ -240,8 +240,11 @@ fa_status fa_tile_plan(int B, int N, int causal, const int32_t *key_len,
  * block_mask, when given, are HOST arrays too.  The call copies the inputs
  * into dev_workspace, runs fa_fwd (and fa_bwd), copies the outputs back and
  * synchronises the stream before returning.  Pinned host memory makes the
- * copies asynchronous.  dev_workspace: device memory of at least
- * fa_host_workspace_size() bytes, zero-filled once before first use.
+ * copies asynchronous; the call then spreads them over `stream` and a
+ * private side stream, ordered by events, so that both copy directions run
+ * in parallel and dO's upload and the O/LSE download overlap the kernels.
+ * dev_workspace: device memory of at least fa_host_workspace_size() bytes,
+ * zero-filled once before first use.
  */
 size_t fa_host_workspace_size(int B, int H, int N, int d, int with_backward);
 fa_status fa_attention_host(const void *Q, const void *K, const void *V, const void *dO, void *O,

@@ -596,6 +596,27 @@ size_t fa_host_workspace_size(int B, int H, int N, int d, int with_backward) {
     return host_layout(B, H, N, d, with_backward ? 1 : 0).total;
 }
 
+namespace {
+// A non-blocking side stream and the events that order it against the
+// caller's stream for one fa_attention_host call.  Destroying them right
+// away is safe: CUDA releases a stream or event whose work is still queued
+// once that work completes.
+struct HostSide {
+    cudaStream_t s = nullptr;
+    cudaEvent_t ev[6] = {};
+    bool ok = false;
+    HostSide() {
+        ok = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) == cudaSuccess;
+        for (auto &e : ev) ok = ok && cudaEventCreateWithFlags(&e, cudaEventDisableTiming) == cudaSuccess;
+    }
+    ~HostSide() {
+        for (auto &e : ev)
+            if (e) cudaEventDestroy(e);
+        if (s) cudaStreamDestroy(s);
+    }
+};
+}  // namespace
+
 fa_status fa_attention_host(const void *Q, const void *K, const void *V, const void *dO, void *O, float *LSE,
                             void *dQ, void *dK, void *dV, int B, int H, int N, int d, float softmax_scale,
                             int causal, const int32_t *key_len, const uint8_t *block_mask, void *dev_workspace,
@@ -613,29 +634,47 @@ fa_status fa_attention_host(const void *Q, const void *K, const void *V, const v
     uint8_t *w = static_cast<uint8_t *>(dev_workspace);
     const size_t bytes = (size_t)B * H * N * d * 2, lbytes = (size_t)B * H * N * 4;
     const size_t nb = ((size_t)N + 127) / 128;
-    auto h2d = [&](size_t off, const void *src, size_t n) {
-        return cudaMemcpyAsync(w + off, src, n, cudaMemcpyHostToDevice, s) == cudaSuccess;
+    // Copies go to two streams, so that both copy directions and the kernels
+    // overlap: V and dO upload on a side stream (dO while the forward runs),
+    // O and LSE download there while the backward runs, dQ in parallel with
+    // dK and dV.  The side stream starts after the work already on `stream`
+    // and `stream` waits for it at the end, so the call is one unit on it.
+    HostSide side;
+    if (!side.ok || cudaEventRecord(side.ev[0], s) != cudaSuccess ||
+        cudaStreamWaitEvent(side.s, side.ev[0], 0) != cudaSuccess)
+        return FA_ERR_CUDA;
+    auto h2d = [&](size_t off, const void *src, size_t n, cudaStream_t on) {
+        return cudaMemcpyAsync(w + off, src, n, cudaMemcpyHostToDevice, on) == cudaSuccess;
     };
-    auto d2h = [&](void *dst, size_t off, size_t n) {
-        return cudaMemcpyAsync(dst, w + off, n, cudaMemcpyDeviceToHost, s) == cudaSuccess;
+    auto d2h = [&](void *dst, size_t off, size_t n, cudaStream_t on) {
+        return cudaMemcpyAsync(dst, w + off, n, cudaMemcpyDeviceToHost, on) == cudaSuccess;
     };
-    if (!h2d(L.q, Q, bytes) || !h2d(L.k, K, bytes) || !h2d(L.v, V, bytes)) return FA_ERR_CUDA;
-    if (bwd && !h2d(L.dO, dO, bytes)) return FA_ERR_CUDA;
-    if (key_len && !h2d(L.klen, key_len, (size_t)B * 4)) return FA_ERR_CUDA;
-    if (block_mask && !h2d(L.bmask, block_mask, nb * nb)) return FA_ERR_CUDA;
+    auto handoff = [&](cudaEvent_t e, cudaStream_t from, cudaStream_t to) {
+        return cudaEventRecord(e, from) == cudaSuccess && cudaStreamWaitEvent(to, e, 0) == cudaSuccess;
+    };
+    if (!h2d(L.q, Q, bytes, s) || !h2d(L.k, K, bytes, s) || !h2d(L.v, V, bytes, side.s)) return FA_ERR_CUDA;
+    if (key_len && !h2d(L.klen, key_len, (size_t)B * 4, s)) return FA_ERR_CUDA;
+    if (block_mask && !h2d(L.bmask, block_mask, nb * nb, s)) return FA_ERR_CUDA;
+    if (!handoff(side.ev[1], side.s, s)) return FA_ERR_CUDA;                 // V is in
+    if (bwd && !h2d(L.dO, dO, bytes, side.s)) return FA_ERR_CUDA;
     const int32_t *kl = key_len ? reinterpret_cast<const int32_t *>(w + L.klen) : nullptr;
     const uint8_t *bm = block_mask ? w + L.bmask : nullptr;
     const size_t ws_bytes = bwd ? fa_bwd_workspace_size(B, H, N, d) : fa_fwd_workspace_size(B, H, N, d);
     st = fa_fwd(w + L.q, w + L.k, w + L.v, w + L.o, reinterpret_cast<float *>(w + L.lse), B, H, N, d, softmax_scale,
                 causal, kl, bm, w + L.attn_ws, ws_bytes, stream);
     if (st != FA_OK) return st;
+    if (!handoff(side.ev[2], s, side.s)) return FA_ERR_CUDA;                 // O, LSE are final
+    if (!d2h(O, L.o, bytes, side.s) || !d2h(LSE, L.lse, lbytes, side.s)) return FA_ERR_CUDA;
     if (bwd) {
+        if (!handoff(side.ev[3], side.s, s)) return FA_ERR_CUDA;             // dO is in
         st = fa_bwd(w + L.q, w + L.k, w + L.v, w + L.o, reinterpret_cast<float *>(w + L.lse), w + L.dO, w + L.dQ,
                     w + L.dK, w + L.dV, B, H, N, d, softmax_scale, causal, kl, bm, w + L.attn_ws, ws_bytes, stream);
         if (st != FA_OK) return st;
+        if (!handoff(side.ev[4], s, side.s)) return FA_ERR_CUDA;             // gradients are final
+        if (!d2h(dQ, L.dQ, bytes, side.s) || !d2h(dK, L.dK, bytes, s) || !d2h(dV, L.dV, bytes, s))
+            return FA_ERR_CUDA;
     }
-    if (!d2h(O, L.o, bytes) || !d2h(LSE, L.lse, lbytes)) return FA_ERR_CUDA;
-    if (bwd && (!d2h(dQ, L.dQ, bytes) || !d2h(dK, L.dK, bytes) || !d2h(dV, L.dV, bytes))) return FA_ERR_CUDA;
+    if (!handoff(side.ev[5], side.s, s)) return FA_ERR_CUDA;
     return fa_get_device_status(w + L.attn_ws, stream);
 }
 

@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import oracle
-from synthetic import DECODE_WORKLOADS, WORKLOADS, make_decode_inputs, make_inputs
+from synthetic import DECODE_WORKLOADS, WORKLOADS, make_case, make_decode_inputs, make_inputs
 from gpu_common import GRAD_REL_FRO, LSE_MAX_ABS, O_MAX_ABS, O_REL_FRO, f64, oracle_args, rel_fro, run_cuda
 
 pytestmark = pytest.mark.gpu
@@ -115,6 +115,38 @@ def test_host_buffer_path_matches_device_path():
     assert np.array_equal(dV.double().numpy(), dev["dV"])
     # dQ goes through fp32 atomics whose order varies: compare within tolerance
     assert rel_fro(dQ.double().numpy(), dev["dQ"]) < 1e-3
+
+
+def test_host_buffer_path_orders_its_side_stream():
+    """fa_attention_host spreads its copies over the caller's stream and a side
+    stream.  Work already queued on the caller's stream must finish first: here
+    it zeroes the whole device workspace (slowly, many times), which would
+    wipe the uploaded inputs if a side-stream copy ran ahead of it.  Repeated
+    calls on a non-default stream give the device path's bits each time."""
+    import io_aware_exact_09_gb300 as fa
+    B, H, N, d = 1, 4, 2048, 128
+    case = make_case(B, H, N, d, seed=31)
+    pin = lambda t: t.contiguous().pin_memory()
+    Qh, Kh, Vh, dOh = (pin(case[k]) for k in ("Q", "K", "V", "dO"))
+    dev = run_cuda(case)
+    need = fa.fa_host_workspace_size(B, H, N, d, 1)
+    ws = fa.workspace(need, "cuda")
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            O = torch.empty_like(Qh).pin_memory()
+            LSE = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+            dQ, dK, dV = (torch.empty_like(Qh).pin_memory() for _ in range(3))
+            for _ in range(50):
+                ws.zero_()
+            st = fa.fa_attention_host(Qh, Kh, Vh, dOh, O, LSE, dQ, dK, dV, B, H, N, d, case["scale"], False, None,
+                                      None, ws, ws.numel(), stream)
+            assert st == 0, fa.fa_status_string(st)
+            assert np.array_equal(O.double().numpy(), dev["O"])
+            assert np.array_equal(LSE.double().numpy(), dev["LSE"])
+            assert np.array_equal(dK.double().numpy(), dev["dK"])
+            assert np.array_equal(dV.double().numpy(), dev["dV"])
+            assert rel_fro(dQ.double().numpy(), dev["dQ"]) < 1e-3
 
 
 @pytest.mark.parametrize("name", sorted(DECODE_WORKLOADS))
