@@ -28,11 +28,12 @@
 //                previous dQ contribution through a swizzled shared tile and
 //                per-warp TMA reduce-adds into the fp32 accumulator; at the
 //                end each converts half of dK * scale and dV to bf16.
-//      d = 64 uses 128-row query blocks and dQ = dS K (TMEM lane = query);
-//      d = 128 uses 64-row query blocks and dQ^T = K^T dS^T (TMEM lane = head
-//      dimension), so that S, dP, dV, dK and two dQ buffers fit in the 512
-//      TMEM columns in both cases.
+//      This kernel is the d = 64 one: 128-row query blocks and dQ = dS K
+//      (TMEM lane = query), so that S, dP (128 columns each), dV, dK and two
+//      dQ buffers (64 each) fit in the 512 TMEM columns.  d = 128 has its own
+//      kernel, fa_bwd128.cu.
 //   3. fa_bwd_convert: dQ = bf16(scale * dQacc)                        (HBM-bound)
+// The preprocessing and conversion kernels serve both head dimensions.
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
 
@@ -40,8 +41,8 @@ namespace fa {
 
 template <int D>
 struct BwdShape {
-    static constexpr int BQ = (D == 64) ? 128 : 64;       // query rows per inner step
-    static constexpr bool DQ_T = (D == 128);              // dQ^T = K^T dS^T
+    static_assert(D == 64, "d = 128 has its own kernel (fa_bwd128.cu)");
+    static constexpr int BQ = 128;                        // query rows per inner step
     static constexpr int CHUNKS = D / 64;
     static constexpr int KV_CHUNK = 128 * 128;            // 128 keys x 128 bytes
     static constexpr int KV_BYTES = CHUNKS * KV_CHUNK;
@@ -324,10 +325,8 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_kernel(const __grid_constant__ 
                     for (int k = 0; k < kTile / 16; ++k) {
                         const uint64_t kk = sdesc_add(dK_mn, (uint32_t)k * 2048u);
                         const uint64_t dd = sdesc_add(ddS_mn, (uint32_t)k * 2048u);
-                        if (S::DQ_T)   // dQ^T = K^T dS^T: A = K^T (M = d), B = dS (N = queries)
-                            mma_ss(dq_tmem, kk, dd, IDESC_DQ, k > 0 ? 1u : 0u);
-                        else           // dQ = dS K: A = dS (M = queries), B = K (N = d)
-                            mma_ss(dq_tmem, dd, kk, IDESC_DQ, k > 0 ? 1u : 0u);
+                        // dQ = dS K: A = dS (M = queries), B = K (N = d)
+                        mma_ss(dq_tmem, dd, kk, IDESC_DQ, k > 0 ? 1u : 0u);
                     }
                     mma_commit(bar(S::B_DQFULL + s));
                     // dP(i+1) once dK(i) has read dS(i)
@@ -375,17 +374,7 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_kernel(const __grid_constant__ 
             __syncwarp();
             uint32_t box;             // shared address of this warp's 32 x 32 box
             int cx, cy;               // its coordinates (head dimension, query)
-            if (S::DQ_T) {
-                // lane = head dimension 32*wq + lane (chunk wq), column t = query c0 + t
-                uint8_t *cb = stg + wq * (BQ * 128) + c0 * 128 + (lane & 3) * 4;
-                const int grp = lane >> 2;
-#pragma unroll
-                for (int t = 0; t < 32; ++t)
-                    *reinterpret_cast<uint32_t *>(cb + t * 128 + ((grp ^ (t & 7)) << 4)) = v[t];
-                box = smem_u32(stg + wq * (BQ * 128) + c0 * 128);
-                cx = wq * 32;
-                cy = qb * BQ + c0;
-            } else {
+            {
                 // lane = query row r of the block, columns = head dimensions 32*wg .. 32*wg + 31
                 uint8_t *cb = stg + wg * (BQ * 128) + r * 128;
 #pragma unroll
@@ -612,7 +601,7 @@ __global__ void fa_plan_kernel(int B, int N, int T, int causal, const int32_t *k
 
 // d = 128 runs fa_bwd128_kernel (128-row query blocks)
 int bwd_query_block(int d) { return d == 64 ? BwdShape<64>::BQ : 128; }
-int bwd_dq_box_rows(int d) { return d == 64 ? BwdShape<64>::DQ_BOX_ROWS : BwdShape<128>::DQ_BOX_ROWS; }
+int bwd_dq_box_rows(int) { return BwdShape<64>::DQ_BOX_ROWS; }   // fa_bwd128.cu uses the same 32 x 32 boxes
 int bwd_smem_bytes(int d) { return d == 64 ? BwdShape<64>::SMEM_BYTES : bwd128_smem_bytes(); }
 
 template <int D>
