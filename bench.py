@@ -56,7 +56,8 @@ if ROOT not in sys.path:
 DEFAULT_WORKLOAD = "longctx_b1h16n16384d128"
 FWD_BWD_FACTOR = 3.5          # forward + backward = forward x (1 + 2.5)
 KERNEL_SOURCES = {"fa_fwd_kernel": "fa_fwd.cu", "fa_bwd_kernel": "fa_bwd.cu", "fa_bwd128_kernel": "fa_bwd128.cu",
-                  "fa_fwd_kernel_fp8": "fa_fwd_fp8.cu", "fa_decode_kernel": "fa_decode.cu"}
+                  "fa_fwd_kernel_fp8": "fa_fwd_fp8.cu", "fa_decode_kernel": "fa_decode.cu",
+                  "fa_fwd_kernel_varlen": "fa_fwd.cu"}
 
 
 # ---------------------------------------------------------------- distributed helpers
@@ -684,7 +685,7 @@ def run_varlen(args, w):
     peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
     achieved = flops / (ms / 1e3) / 1e12
     roofline = {"bound": "tensor", "kernel": "fa_fwd_kernel<%d, varlen>" % d, "achieved": achieved, "peak": peak,
-                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": ncu_traffic("fa_fwd_kernel_varlen", w.name),
                 "peak_source": "%s bf16_tflops_sustained" % peak_src}
     e2e = None
     if not args.no_e2e:
