@@ -7,8 +7,9 @@ the product library: the two share no code.
 
 The arithmetic lives in ``fa_oracle.c`` (plain C, fp64, OpenMP over rows);
 this module only builds it with gcc and marshals numpy arrays through ctypes.
-``online.py`` holds the pages' two-block merge identity and ``io_model.py``
-the page-2 traffic/time model.
+``online.py`` holds the pages' two-block merge identity, ``io_model.py``
+the page-2 traffic/time model and ``incoherent.py`` the Hadamard rotation
+of the FP8 forward's incoherent processing.
 """
 from __future__ import annotations
 
@@ -336,6 +337,13 @@ def dequantize_fp8(codes, scales, N, transpose=False):
         vals = np.swapaxes(vals, 2, 3)[:, :, :N, :]
     rows = np.arange(N) // FP8_BLOCK
     return vals * np.asarray(scales, np.float64)[:, :, rows][..., None]
+
+
+def quantize_fp8_rotated(X, signs):
+    """Block quantisation of the incoherently rotated X [B, H, N, d]:
+    quantize_fp8(rotate(X, signs)) (codes [B, H, N, d], scales [B, H, T])."""
+    from .incoherent import rotate
+    return quantize_fp8(rotate(X, signs), False)
 
 
 from .online import merge_blocks, online_fold  # noqa: E402,F401
