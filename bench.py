@@ -20,7 +20,9 @@ of the same workload, on this machine's host cores.
 quantisation of Q, K and V (``fa_quantize_fp8``, three launches) and
 ``fa_fwd_fp8``; ``value`` is forward TFLOP/s over the step, the roofline is
 the FP8 forward kernel against the dense-FP8 peak (the measured sustained
-bf16 figure x 2, the nominal fp8 : bf16 ratio).
+bf16 figure x 2, the nominal fp8 : bf16 ratio).  ``--incoherent`` adds the
+incoherent processing: Q and K go through ``fa_quantize_fp8_rotated`` with a
+seeded random sign vector, and the forward takes softmax_scale / d.
 
 ``--tile-sweep`` times the forward at each tile shape ``fa_fwd_tiles`` offers
 (query rows per CTA 128 / 256 x key rows per tile 64 / 128) on the workload
@@ -432,6 +434,13 @@ def run_fp8(args):
     sQ, sK, sV = (torch.empty((B, H, T), dtype=torch.float32, device=dev) for _ in range(3))
     O = torch.empty_like(Q)
     LSE = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    # incoherent processing: a seeded random sign vector (an input of the method)
+    signs = None
+    scale = w.softmax_scale
+    if args.incoherent:
+        g = torch.Generator().manual_seed(w.seed + 17)
+        signs = torch.where(torch.rand(d, generator=g) < 0.5, -1, 1).to(torch.int8).to(dev)
+        scale = w.softmax_scale / d
     wsn = fa.fa_fwd_workspace_size(B, H, N, d)
     ws = fa.workspace(wsn, dev)
     stream = torch.cuda.current_stream(dev)
@@ -449,12 +458,16 @@ def run_fp8(args):
     def step(record):
         if record:
             ev[0].record(stream)
-        check(fa.fa_quantize_fp8(Q, Q8, sQ, B, H, N, d, False, sp), "fa_quantize_fp8 Q")
-        check(fa.fa_quantize_fp8(K, K8, sK, B, H, N, d, False, sp), "fa_quantize_fp8 K")
+        if signs is None:
+            check(fa.fa_quantize_fp8(Q, Q8, sQ, B, H, N, d, False, sp), "fa_quantize_fp8 Q")
+            check(fa.fa_quantize_fp8(K, K8, sK, B, H, N, d, False, sp), "fa_quantize_fp8 K")
+        else:
+            check(fa.fa_quantize_fp8_rotated(Q, Q8, sQ, signs, B, H, N, d, sp), "fa_quantize_fp8_rotated Q")
+            check(fa.fa_quantize_fp8_rotated(K, K8, sK, signs, B, H, N, d, sp), "fa_quantize_fp8_rotated K")
         check(fa.fa_quantize_fp8(V, Vt8, sV, B, H, N, d, True, sp), "fa_quantize_fp8 V")
         if record:
             ev[1].record(stream)
-        check(fa.fa_fwd_fp8(Q8, K8, Vt8, sQ, sK, sV, O, LSE, B, H, N, d, w.softmax_scale, w.causal, kl, bm, ws, wsn,
+        check(fa.fa_fwd_fp8(Q8, K8, Vt8, sQ, sK, sV, O, LSE, B, H, N, d, scale, w.causal, kl, bm, ws, wsn,
                             sp), "fa_fwd_fp8")
         if record:
             ev[2].record(stream)
@@ -523,6 +536,7 @@ def run_fp8(args):
             "n_gpus": ws_n, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp8-e4m3", "data": "synthetic",
             "config": {"workload": w.name, "B": B, "H": H, "N": N, "d": d, "causal": w.causal, "path": "fp8 forward",
+                       "incoherent_processing": bool(args.incoherent),
                        "parallelism": "replicas" if ws_n > 1 else "single", "l2": "flushed between steps"},
             "kernel_ms": {"fa_quant_fp8_kernel x3": mq, "fa_fwd_kernel<128, fp8>": mf},
             "fwd_kernel_tflops": achieved, "algorithmic_flops_per_step": flops,
@@ -975,6 +989,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--fp8", action="store_true", help="measure the FP8 forward (d = 128 workloads)")
+    ap.add_argument("--incoherent", action="store_true",
+                    help="with --fp8: quantise Q and K with incoherent processing (Hadamard rotation)")
     ap.add_argument("--tile-sweep", action="store_true", help="time the forward at each tile shape")
     ap.add_argument("--decode-reps", type=int, default=20,
                     help="decode workloads: timed calls per step (each one is well under a millisecond)")

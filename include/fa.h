@@ -146,6 +146,24 @@ fa_status fa_quantize_fp8(const void *X, void *X8, float *scales, int B, int H, 
                           int transpose, void *stream);
 
 /*
+ * FP8 block quantisation with incoherent processing (the "Attention" chapter
+ * of learn-kernels.com, FlashAttention-3 paragraph: "block quantization with
+ * incoherent processing"), for Q and K.  Each row x of X (device bf16
+ * [B, H, N, d], read) is first rotated to (x * signs) H: signs is a device
+ * int8 [d] vector of +1 / -1 (16-byte aligned; the caller draws it at
+ * random and uses the same one for Q and K), H the unnormalised d x d
+ * Sylvester-Hadamard matrix, applied as the fast Walsh-Hadamard transform
+ * in fp32 (stages h = 1, 2, ..., d/2, each pair (i, i + h) becoming
+ * (x_i + x_{i+h}, x_i - x_{i+h})).  Then as fa_quantize_fp8 without
+ * transpose: codes X8 [B, H, N, d] and scales [B, H, ceil(N / 128)] of the
+ * rotated values.  Since (Q s H)(K s H)^T = d Q K^T, fa_fwd_fp8 on rotated
+ * Q and K takes softmax_scale / d.  V is quantised unrotated.  One kernel
+ * launch, no workspace.
+ */
+fa_status fa_quantize_fp8_rotated(const void *X, void *X8, float *scales, const int8_t *signs, int B,
+                                  int H, int N, int d, void *stream);
+
+/*
  * FP8 forward (d = 128 only; other d: FA_ERR_UNSUPPORTED).  Q8, K8: e4m3
  * [B, H, N, d]; Vt8: e4m3 [B, H, d, Np] (fa_quantize_fp8 with transpose);
  * sQ, sK, sV: their block scales [B, H, ceil(N / 128)]; all device, read.

@@ -81,6 +81,8 @@ def lib():
             L.fa_fwd_varlen.restype = i
             L.fa_quantize_fp8.argtypes = [vp, vp, vp, i, i, i, i, i, vp]
             L.fa_quantize_fp8.restype = i
+            L.fa_quantize_fp8_rotated.argtypes = [vp, vp, vp, vp, i, i, i, i, vp]
+            L.fa_quantize_fp8_rotated.restype = i
             L.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp, vp, sz, vp]
             L.fa_fwd_fp8.restype = i
             L.fa_tile_plan.argtypes = [i, i, i, vp, vp, vp, vp, sz, vp]
@@ -102,7 +104,7 @@ def lib():
 
 EXPORTED = ("fa_tile_size", "fa_fwd_workspace_size", "fa_bwd_workspace_size", "fa_fwd", "fa_bwd",
             "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_postprocess", "fa_bwd_noalloc",
-            "fa_decode_workspace_size", "fa_decode", "fa_fwd_tiles", "fa_fwd_varlen", "fa_quantize_fp8", "fa_fwd_fp8",
+            "fa_decode_workspace_size", "fa_decode", "fa_fwd_tiles", "fa_fwd_varlen", "fa_quantize_fp8", "fa_quantize_fp8_rotated", "fa_fwd_fp8",
             "fa_tile_plan",
             "fa_host_workspace_size", "fa_attention_host", "fa_get_device_status", "fa_reset_device_status",
             "fa_selftest_wait_timeout", "fa_status_string")
@@ -191,6 +193,10 @@ def attention_varlen(Q, K, V, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, softmax_
 
 def fa_quantize_fp8(X, X8, scales, B, H, N, d, transpose, stream=None) -> int:
     return lib().fa_quantize_fp8(_p(X), _p(X8), _p(scales), B, H, N, d, int(bool(transpose)), _stream(stream))
+
+
+def fa_quantize_fp8_rotated(X, X8, scales, signs, B, H, N, d, stream=None) -> int:
+    return lib().fa_quantize_fp8_rotated(_p(X), _p(X8), _p(scales), _p(signs), B, H, N, d, _stream(stream))
 
 
 def fa_fwd_fp8(Q8, K8, Vt8, sQ, sK, sV, O, LSE, B, H, N, d, softmax_scale, causal, key_len, block_mask,
@@ -306,28 +312,40 @@ def attention_forward(Q, K, V, softmax_scale=None, causal=False, key_len=None, b
     return O, LSE
 
 
-def quantize_fp8(X, transpose=False, stream=None):
+def quantize_fp8(X, transpose=False, stream=None, signs=None):
     """(codes, scales) = fa_quantize_fp8(X): codes uint8 [B, H, N, d] (transpose:
-    [B, H, d, Np], Np = ceil(N / 16) * 16), scales fp32 [B, H, ceil(N / 128)]."""
+    [B, H, d, Np], Np = ceil(N / 16) * 16), scales fp32 [B, H, ceil(N / 128)].
+    With signs (device int8 [d] of +-1), the codes of the incoherently
+    rotated rows (fa_quantize_fp8_rotated; not with transpose)."""
     import torch
     B, H, N, d = _dims(X)
     Np = (N + 15) // 16 * 16
     X8 = torch.empty((B, H, d, Np) if transpose else (B, H, N, d), dtype=torch.uint8, device=X.device)
     sc = torch.empty((B, H, (N + 127) // 128), dtype=torch.float32, device=X.device)
-    _check(fa_quantize_fp8(X, X8, sc, B, H, N, d, transpose, stream), "fa_quantize_fp8")
+    if signs is not None:
+        if transpose:
+            raise ValueError("the rotation applies to Q and K, not to the transposed V")
+        _check(fa_quantize_fp8_rotated(X, X8, sc, signs, B, H, N, d, stream), "fa_quantize_fp8_rotated")
+    else:
+        _check(fa_quantize_fp8(X, X8, sc, B, H, N, d, transpose, stream), "fa_quantize_fp8")
     return X8, sc
 
 
 def attention_forward_fp8(Q, K, V, softmax_scale=None, causal=False, key_len=None, block_mask=None, ws=None,
-                          stream=None, check_status=False):
+                          stream=None, check_status=False, signs=None):
     """O, LSE of the FP8 forward on bf16 CUDA tensors [B, H, N, 128]: Q, K and V
-    are block-quantised (fa_quantize_fp8), then fa_fwd_fp8 runs."""
+    are block-quantised (fa_quantize_fp8), then fa_fwd_fp8 runs.  With signs
+    (device int8 [d] of random +-1), Q and K are quantised with incoherent
+    processing (fa_quantize_fp8_rotated) and the scores' extra factor d is
+    taken out of the softmax scale."""
     import torch
     B, H, N, d = _dims(Q)
     scale = (1.0 / d ** 0.5) if softmax_scale is None else softmax_scale
-    Q8, sQ = quantize_fp8(Q, False, stream)
-    K8, sK = quantize_fp8(K, False, stream)
+    Q8, sQ = quantize_fp8(Q, False, stream, signs)
+    K8, sK = quantize_fp8(K, False, stream, signs)
     Vt8, sV = quantize_fp8(V, True, stream)
+    if signs is not None:
+        scale = scale / d
     O = torch.empty_like(Q)
     LSE = torch.empty((B, H, N), dtype=torch.float32, device=Q.device)
     need = fa_fwd_workspace_size(B, H, N, d)

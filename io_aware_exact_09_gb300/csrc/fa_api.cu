@@ -277,7 +277,21 @@ fa_status fa_quantize_fp8(const void *X, void *X8, float *scales, int B, int H, 
     if (empty) return FA_OK;
     if (!X || !X8 || !scales || !aligned16(X) || !aligned16(X8) || !aligned16(scales))
         return FA_ERR_INVALID_ARGUMENT;
-    return fa::launch_quant_fp8(d, X, X8, scales, B * H, N, transpose ? 1 : 0, static_cast<cudaStream_t>(stream)) ==
+    return fa::launch_quant_fp8(d, X, X8, scales, B * H, N, transpose ? 1 : 0, nullptr,
+                                static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? FA_OK
+               : FA_ERR_CUDA;
+}
+
+fa_status fa_quantize_fp8_rotated(const void *X, void *X8, float *scales, const int8_t *signs, int B, int H, int N,
+                                  int d, void *stream) {
+    bool empty = false;
+    fa_status st = check_sizes(B, H, N, d, &empty);
+    if (st != FA_OK) return st;
+    if (empty) return FA_OK;
+    if (!X || !X8 || !scales || !signs || !aligned16(X) || !aligned16(X8) || !aligned16(scales) || !aligned16(signs))
+        return FA_ERR_INVALID_ARGUMENT;
+    return fa::launch_quant_fp8(d, X, X8, scales, B * H, N, 0, signs, static_cast<cudaStream_t>(stream)) ==
                    cudaSuccess
                ? FA_OK
                : FA_ERR_CUDA;

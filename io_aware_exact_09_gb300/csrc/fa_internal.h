@@ -19,9 +19,10 @@ cudaError_t launch_fwd_tiles(int d, int block_k, const FwdParams &p, cudaStream_
 cudaError_t launch_fwd_varlen(int d, const FwdParams &p, cudaStream_t st);
 // FP8 forward (d = 128): e4m3 Q, K, V^T with per-block scales.
 cudaError_t launch_fwd_fp8(const FwdParams &p, cudaStream_t st);
-// FP8 block quantisation of one bf16 tensor [BH][N][d] (V: transposed).
+// FP8 block quantisation of one bf16 tensor [BH][N][d] (V: transposed);
+// with signs (Q, K only), of the incoherently rotated rows (x * signs) H.
 cudaError_t launch_quant_fp8(int d, const void *X, void *Y, float *scales, int BH, int N, int transpose,
-                             cudaStream_t st);
+                             const int8_t *signs, cudaStream_t st);
 
 // Backward: D = rowsum(dO * O) and dQacc = 0; the main kernel; dQ = bf16(scale * dQacc).
 cudaError_t launch_bwd_pre(int d, const void *O, const void *dO, float *Dvec, float *dQacc,

@@ -14,6 +14,16 @@
 // vector; transposed: the block is staged in shared memory and each thread
 // writes 32 consecutive codes of one row of V^T).
 // HBM-bound: 2 bytes read and 1 written per element.
+//
+// Incoherent processing (same chapter's FlashAttention-3 paragraph: "block
+// quantization with incoherent processing"), for Q and K: before the block
+// amax, each row x becomes (x * s) H, s a caller-given vector of random
+// signs and H the unnormalised d x d Sylvester-Hadamard matrix, so that
+// (Q s H)(K s H)^T = d Q K^T and a few large channels are spread over all d.
+// The fast Walsh-Hadamard transform runs in fp32, stage h = 1, 2, 4, ...,
+// d/2 turning each pair (i, i + h) into (x_i + x_{i+h}, x_i - x_{i+h}): the
+// first three stages inside a thread's 8 values, the rest across the lanes
+// that hold the row (its 16-byte vectors sit in consecutive lanes).
 #include <cuda_bf16.h>
 
 #include "fa_internal.h"
@@ -23,10 +33,11 @@ namespace fa {
 
 namespace {
 
-template <int D, bool TRANSPOSE>
+template <int D, bool TRANSPOSE, bool ROTATE>
 __global__ void __launch_bounds__(256) fa_quant_fp8_kernel(const __nv_bfloat16 *__restrict__ X,
                                                            uint8_t *__restrict__ Y, float *__restrict__ scales,
-                                                           int N, int T, int Np) {
+                                                           const int8_t *__restrict__ signs, int N, int T, int Np) {
+    static_assert(!(ROTATE && TRANSPOSE), "the rotation is for Q and K (row layout)");
     constexpr int VPR = D / 8;                 // 16-byte vectors per row
     constexpr int NV = 128 * VPR / 256;        // vectors per thread
     __shared__ float red[8];
@@ -38,6 +49,8 @@ __global__ void __launch_bounds__(256) fa_quant_fp8_kernel(const __nv_bfloat16 *
     const __nv_bfloat16 *xb = X + ((size_t)bh * N + r0) * D;
 
     uint4 v[NV];
+    // rotated path: the thread's 8 values of each of its rows, in fp32
+    float f[ROTATE ? NV : 1][8];
     float amax = 0.f;
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
@@ -45,8 +58,39 @@ __global__ void __launch_bounds__(256) fa_quant_fp8_kernel(const __nv_bfloat16 *
         v[i] = make_uint4(0u, 0u, 0u, 0u);
         if (r0 + row < N) v[i] = __ldg(reinterpret_cast<const uint4 *>(xb + (size_t)row * D) + cv);
         const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+        if constexpr (ROTATE) {
+            // columns 8 cv .. 8 cv + 7 (cv is the same for all i: 256 is a
+            // multiple of VPR)
+            const uint2 sg = __ldg(reinterpret_cast<const uint2 *>(signs) + cv);
+            const uint32_t sb[2] = {sg.x, sg.y};
 #pragma unroll
-        for (int k = 0; k < 4; ++k) amax = fmaxf(amax, fmaxf(fabsf(bf16lo(w[k])), fabsf(bf16hi(w[k]))));
+            for (int k = 0; k < 8; ++k) {
+                const float x = (k & 1) ? bf16hi(w[k >> 1]) : bf16lo(w[k >> 1]);
+                const int8_t s = (int8_t)((sb[k >> 2] >> (8 * (k & 3))) & 0xFFu);
+                f[i][k] = s < 0 ? -x : x;
+            }
+#pragma unroll
+            for (int h = 1; h < 8; h <<= 1)
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    if (!(k & h)) {
+                        const float a = f[i][k], b = f[i][k + h];
+                        f[i][k] = a + b;
+                        f[i][k + h] = a - b;
+                    }
+#pragma unroll
+            for (int j = 1; j < VPR; j <<= 1)
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const float pv = __shfl_xor_sync(0xffffffffu, f[i][k], j);
+                    f[i][k] = (cv & j) ? pv - f[i][k] : f[i][k] + pv;
+                }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(f[i][k]));
+        } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) amax = fmaxf(amax, fmaxf(fabsf(bf16lo(w[k])), fabsf(bf16hi(w[k]))));
+        }
         if constexpr (TRANSPOSE) reinterpret_cast<uint4 *>(blk)[idx] = v[i];
     }
 #pragma unroll
@@ -65,8 +109,16 @@ __global__ void __launch_bounds__(256) fa_quant_fp8_kernel(const __nv_bfloat16 *
         for (int i = 0; i < NV; ++i) {
             const int idx = tid + 256 * i, row = idx / VPR, cv = idx % VPR;
             const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-            const uint32_t c0 = pack_e4m3x4(q(bf16lo(w[0])), q(bf16hi(w[0])), q(bf16lo(w[1])), q(bf16hi(w[1])));
-            const uint32_t c1 = pack_e4m3x4(q(bf16lo(w[2])), q(bf16hi(w[2])), q(bf16lo(w[3])), q(bf16hi(w[3])));
+            float e[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                if constexpr (ROTATE)
+                    e[k] = f[i][k];
+                else
+                    e[k] = (k & 1) ? bf16hi(w[k >> 1]) : bf16lo(w[k >> 1]);
+            }
+            const uint32_t c0 = pack_e4m3x4(q(e[0]), q(e[1]), q(e[2]), q(e[3]));
+            const uint32_t c1 = pack_e4m3x4(q(e[4]), q(e[5]), q(e[6]), q(e[7]));
             if (r0 + row < N)
                 *reinterpret_cast<uint2 *>(Y + ((size_t)bh * N + r0 + row) * D + cv * 8) = make_uint2(c0, c1);
         }
@@ -96,7 +148,7 @@ __global__ void __launch_bounds__(256) fa_quant_fp8_kernel(const __nv_bfloat16 *
 }  // namespace
 
 cudaError_t launch_quant_fp8(int d, const void *X, void *Y, float *scales, int BH, int N, int transpose,
-                             cudaStream_t st) {
+                             const int8_t *signs, cudaStream_t st) {
     const int T = (N + 127) / 128;
     const int Np = (N + 15) / 16 * 16;
     const unsigned grid = (unsigned)BH * (unsigned)T;
@@ -104,14 +156,18 @@ cudaError_t launch_quant_fp8(int d, const void *X, void *Y, float *scales, int B
     uint8_t *y = static_cast<uint8_t *>(Y);
     if (d == 64) {
         if (transpose)
-            fa_quant_fp8_kernel<64, true><<<grid, 256, 0, st>>>(x, y, scales, N, T, Np);
+            fa_quant_fp8_kernel<64, true, false><<<grid, 256, 0, st>>>(x, y, scales, nullptr, N, T, Np);
+        else if (signs)
+            fa_quant_fp8_kernel<64, false, true><<<grid, 256, 0, st>>>(x, y, scales, signs, N, T, Np);
         else
-            fa_quant_fp8_kernel<64, false><<<grid, 256, 0, st>>>(x, y, scales, N, T, Np);
+            fa_quant_fp8_kernel<64, false, false><<<grid, 256, 0, st>>>(x, y, scales, nullptr, N, T, Np);
     } else {
         if (transpose)
-            fa_quant_fp8_kernel<128, true><<<grid, 256, 0, st>>>(x, y, scales, N, T, Np);
+            fa_quant_fp8_kernel<128, true, false><<<grid, 256, 0, st>>>(x, y, scales, nullptr, N, T, Np);
+        else if (signs)
+            fa_quant_fp8_kernel<128, false, true><<<grid, 256, 0, st>>>(x, y, scales, signs, N, T, Np);
         else
-            fa_quant_fp8_kernel<128, false><<<grid, 256, 0, st>>>(x, y, scales, N, T, Np);
+            fa_quant_fp8_kernel<128, false, false><<<grid, 256, 0, st>>>(x, y, scales, nullptr, N, T, Np);
     }
     return cudaGetLastError();
 }

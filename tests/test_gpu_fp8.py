@@ -150,3 +150,71 @@ def test_fwd_fp8_is_deterministic(causal):
     outs = [run_fp8(case) for _ in range(12)]
     for O, L in outs[1:]:
         assert np.array_equal(O, outs[0][0]) and np.array_equal(L, outs[0][1])
+
+
+# ---------------------------------------------------------------- incoherent processing
+def random_signs(d, seed):
+    return torch.where(torch.rand(d, generator=torch.Generator().manual_seed(seed)) < 0.5, -1, 1).to(torch.int8)
+
+
+@pytest.mark.parametrize("shape", [(1, 2, 300, 128), (2, 1, 128, 64), (1, 1, 17, 128), (2, 2, 129, 64)])
+def test_quantize_rotated_bit_exact(shape):
+    import io_aware_exact_09_gb300 as fa
+    B, H, N, d = shape
+    g = torch.Generator().manual_seed(sum(shape) + 7)
+    X = torch.randn(shape, generator=g)
+    X[..., 3] *= 50.0                                 # an outlier channel
+    if N > 128:
+        X[-1, -1, 128:256] = 0.0                      # an all-zero block stays zero after the rotation
+    X = X.to(torch.bfloat16)
+    s = random_signs(d, d + N)
+    X8, sc = fa.quantize_fp8(X.cuda().contiguous(), False, signs=s.cuda())
+    torch.cuda.synchronize()
+    rc, rs = oracle.quantize_fp8_rotated(X.float().numpy(), s.numpy())
+    assert np.array_equal(sc.cpu().numpy().view(np.uint32), rs.view(np.uint32))
+    codes = X8.cpu().numpy()
+    assert np.array_equal(codes, rc), int(np.sum(codes != rc))
+
+
+def rotated_reference(case, s):
+    N, d = case["Q"].shape[2], case["Q"].shape[3]
+    q = oracle.dequantize_fp8(*oracle.quantize_fp8_rotated(case["Q"].float().numpy(), s), N)
+    k = oracle.dequantize_fp8(*oracle.quantize_fp8_rotated(case["K"].float().numpy(), s), N)
+    v = oracle.dequantize_fp8(*oracle.quantize_fp8(case["V"].float().numpy(), True), N, True)
+    return q, k, v, case["scale"] / d
+
+
+@pytest.mark.parametrize("mask", ["none", "causal"])
+def test_fwd_fp8_incoherent_matches_oracle(mask):
+    import io_aware_exact_09_gb300 as fa
+    case = make_case(2, 2, 512, 128, seed=71, causal=(mask == "causal"))
+    s = random_signs(128, 72)
+    O, L = fa.attention_forward_fp8(case["Q"].cuda().contiguous(), case["K"].cuda().contiguous(),
+                                    case["V"].cuda().contiguous(), case["scale"], case["causal"],
+                                    check_status=True, signs=s.cuda())
+    torch.cuda.synchronize()
+    q, k, v, sc = rotated_reference(case, s.numpy())
+    rO, rL = oracle.attention_fwd(q, k, v, sc, causal=case["causal"])
+    check_fp8(O.double().cpu().numpy(), L.double().cpu().numpy(), rO, rL, v, mask)
+
+
+def test_incoherent_processing_lowers_fp8_error_with_outliers():
+    """The effect the rotation exists for, through the kernels: with a few
+    large channels in Q and K, the FP8 output is closer to the exact
+    attention of the bf16 inputs with the rotation than without."""
+    import io_aware_exact_09_gb300 as fa
+    g = torch.Generator().manual_seed(73)
+    B, H, N, d = 1, 4, 1024, 128
+    Q, K, V = (torch.randn((B, H, N, d), generator=g) for _ in range(3))
+    ch = torch.randperm(d, generator=g)[:4]
+    Q[..., ch] *= 40.0
+    K[..., ch] *= 40.0
+    Q, K, V = (t.to(torch.bfloat16) for t in (Q, K, V))
+    scale = 1.0 / (d ** 0.5 * 40.0)
+    rO, _ = oracle.attention_fwd(f64(Q), f64(K), f64(V), scale)
+    dev = lambda t: t.cuda().contiguous()
+    err = {}
+    for name, s in (("plain", None), ("rotated", random_signs(d, 74).cuda())):
+        O, _ = fa.attention_forward_fp8(dev(Q), dev(K), dev(V), scale, False, check_status=True, signs=s)
+        err[name] = float(np.linalg.norm(O.double().cpu().numpy() - rO) / np.linalg.norm(rO))
+    assert err["plain"] / err["rotated"] > 1.5, err
