@@ -55,9 +55,11 @@ struct F8Shape {
     static constexpr int B_KVEMPTY = B_VFULL + STAGES;
     static constexpr int B_SFULL = B_KVEMPTY + STAGES;      // [2] per query tile
     static constexpr int B_SFREE = B_SFULL + 2;             // [2]
-    static constexpr int B_PFULL = B_SFREE + 2;             // [2]
-    static constexpr int B_PVDONE = B_PFULL + 2;            // [2]
-    static constexpr int B_PFREE = B_PVDONE + 2;            // [2][2] per query tile and P buffer
+    // P_x is written ahead of the P.V products, so its ready barrier is kept
+    // per P buffer: a softmax warp refills a buffer only after the product
+    // that read it, so the issuer is never two phases behind on one barrier
+    static constexpr int B_PFULL = B_SFREE + 2;             // [2][2] per query tile and P buffer
+    static constexpr int B_PFREE = B_PFULL + 4;             // [2][2]
     static constexpr int B_OFULL = B_PFREE + 4;             // [2] every product done (single use)
     static constexpr int B_FIN = B_OFULL + 2;
     static constexpr int NBAR = B_FIN + 1;
@@ -68,8 +70,8 @@ struct F8Shape {
     static constexpr uint32_t TM_O = 256;                   // O_x at columns 256 + 128 x
     static constexpr int THREADS = 384;
     static constexpr int LAUNCH_REGS = 168;
-    static constexpr int REGS_CTRL = 88;
-    static constexpr int REGS_SOFTMAX = 208;
+    static constexpr int REGS_CTRL = 104;
+    static constexpr int REGS_SOFTMAX = 200;
     static_assert(128 * REGS_CTRL + 256 * REGS_SOFTMAX == THREADS * LAUNCH_REGS, "register split");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 };
@@ -118,14 +120,20 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
         kend[x] = qn[x] > 0 ? (lim + kTile - 1) / kTile : 0;
     }
     const int kend_union = max(kend[0], kend[1]);
+    // per-query-tile values by selection, so that the arrays stay in registers
+    auto q0_of = [&](int x) { return x ? q0[1] : q0[0]; };
+    auto qn_of = [&](int x) { return x ? qn[1] : qn[0]; };
+    auto kend_of = [&](int x) { return x ? kend[1] : kend[0]; };
     auto cls = [&](int x, int kt) -> unsigned {
-        if (qn[x] <= 0) return kTileSkip;
+        if (qn_of(x) <= 0) return kTileSkip;
         const int on = p.block_mask ? (p.block_mask[(size_t)(2 * pq + x) * nb + kt] != 0) : 1;
-        return tile_class(q0[x], qn[x], kt * kTile, kTile, kvis, p.causal, on);
+        return tile_class(q0_of(x), qn_of(x), kt * kTile, kTile, kvis, p.causal, on);
     };
+    // without a block mask the visible tiles of query tile x are 0 .. kend[x]-1
+    auto skip = [&](int x, int kt) -> bool { return p.block_mask ? cls(x, kt) == kTileSkip : kt >= kend_of(x); };
     auto next_tile = [&](int x, int kt) -> int {
         if (!p.block_mask) {
-            const int lim = x == 2 ? kend_union : kend[x];
+            const int lim = x == 2 ? kend_union : kend_of(x);
             return kt + 1 < lim ? kt + 1 : p.Tk;
         }
         for (int k = kt + 1; k < p.Tk; ++k) {
@@ -146,10 +154,11 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
         for (int j = 0; j < 2; ++j) {
             mbar_init(bar(S::B_SFULL + j), 1);
             mbar_init(bar(S::B_SFREE + j), 128);
-            mbar_init(bar(S::B_PFULL + j), 128);
-            mbar_init(bar(S::B_PVDONE + j), 1);
         }
-        for (int j = 0; j < 4; ++j) mbar_init(bar(S::B_PFREE + j), 1);
+        for (int j = 0; j < 4; ++j) {
+            mbar_init(bar(S::B_PFULL + j), 128);
+            mbar_init(bar(S::B_PFREE + j), 1);
+        }
         mbar_init(bar(S::B_OFULL + 0), 1);
         mbar_init(bar(S::B_OFULL + 1), 1);
         mbar_init(bar(S::B_FIN), 1);
@@ -179,6 +188,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
                 if (kt < p.Tk) {
                     const uint32_t nq = (qn[0] > 0 ? 1u : 0u) + (qn[1] > 0 ? 1u : 0u);
                     mbar_arrive_expect_tx(bar(S::B_QFULL), nq * S::TILE_BYTES);
+#pragma unroll
                     for (int x = 0; x < 2; ++x)
                         if (qn[x] > 0)
                             tma_load_3d(base + S::OFF_Q + x * S::TILE_BYTES, &p.tmQ, bar(S::B_QFULL), 0, q0[x], bh);
@@ -233,8 +243,9 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
                     ok = mbar_wait(bar(S::B_QFULL), 0, g, 0x211) && mbar_wait(bar(S::B_KFULL + 0), 0, g, 0x212);
                     if (ok) {
                         tc_fence_after();
+#pragma unroll
                         for (int x = 0; x < 2; ++x)
-                            if (cls(x, kt) != kTileSkip) issue_s(x, 0);
+                            if (!skip(x, kt)) issue_s(x, 0);
                     }
                 }
                 int u = 0;
@@ -248,8 +259,9 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
                             ok = false;
                             break;
                         }
+#pragma unroll
                         for (int x = 0; x < 2 && ok; ++x) {
-                            if (cls(x, kt_next) == kTileSkip) continue;
+                            if (skip(x, kt_next)) continue;
                             if (ns[x] > 0 && !mbar_wait(bar(S::B_SFREE + x), (uint32_t)(ns[x] - 1) & 1u, g, 0x214)) {
                                 ok = false;
                                 break;
@@ -261,9 +273,11 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
                     }
                     // O_x += P_x V for both query tiles
                     bool vwaited = false;
+#pragma unroll
                     for (int x = 0; x < 2 && ok; ++x) {
-                        if (cls(x, kt) == kTileSkip) continue;
-                        if (!mbar_wait(bar(S::B_PFULL + x), (uint32_t)nv[x] & 1u, g, 0x215) ||
+                        if (skip(x, kt)) continue;
+                        if (!mbar_wait(bar(S::B_PFULL + 2 * x + (nv[x] & 1)), (uint32_t)(nv[x] >> 1) & 1u, g,
+                                       0x215) ||
                             (!vwaited && !mbar_wait(bar(S::B_VFULL + s), (uint32_t)(u / S::STAGES) & 1u, g, 0x216))) {
                             ok = false;
                             break;
@@ -279,7 +293,6 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
                         for (int k = 0; k < kTile / 32; ++k)
                             mma_ss_f8(o_tmem, sdesc_add(pd, 32u * k), sdesc_add(vd, 32u * k), IDESC_PV,
                                       k > 0 ? 1u : acc0);
-                        mma_commit(bar(S::B_PVDONE + x));
                         mma_commit(bar(S::B_PFREE + 2 * x + pb));
                         ++nv[x];
                     }
@@ -289,9 +302,9 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
                     ++u;
                 }
                 // O_x is final once every product is done.  The softmax warps run
-                // ahead of the P.V products (P lives in shared memory), so they
-                // may reach their epilogue two PVDONE phases early, where a parity
-                // wait cannot tell the phases apart: they wait on this instead.
+                // ahead of the P.V products (P lives in shared memory) and reach
+                // their epilogue before the last ones land: they wait on this
+                // single-use barrier.
                 if (ok) {
                     mma_commit(bar(S::B_OFULL + 0));
                     mma_commit(bar(S::B_OFULL + 1));
@@ -306,7 +319,8 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
         const int x = (warp - 4) >> 2;
         const int wq = warp & 3;
         const int r = wq * 32 + lane;
-        const int q = q0[x] + r;
+        const int q0x = q0_of(x), qnx = qn_of(x);
+        const int q = q0x + r;
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const uint32_t s_tmem = tmem + lane_off + S::TM_S + 128u * (uint32_t)x;
         const uint32_t o_tmem = tmem + lane_off + S::TM_O + (uint32_t)(D * x);
@@ -317,7 +331,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
         const float c2 = p.scale_log2;
         float m_ref = -INFINITY, l = 0.f;
         float sq = 1.f;
-        if (qn[x] > 0) sq = p.sQ[(size_t)bh * p.Tq + 2 * pq + x];
+        if (qnx > 0) sq = p.sQ[(size_t)bh * p.Tq + 2 * pq + x];
         float mv = 0.f;
         for (int k = lane; k < p.Tk; k += 32) mv = fmaxf(mv, p.sV[(size_t)bh * p.Tk + k]);
 #pragma unroll
@@ -430,8 +444,10 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
             }
             l += (((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]))) * inv_rt;
             if (rescale && it > 0) {
-                // O_x may be rescaled only once the previous P.V has landed
-                if (!mbar_wait_warp(bar(S::B_PVDONE + x), (uint32_t)(it - 1) & 1u, g, 0x413)) {
+                // O_x may be rescaled only once the previous P.V has landed:
+                // that product freed P buffer (it - 1) & 1
+                if (!mbar_wait_warp(bar(S::B_PFREE + 2 * x + ((it - 1) & 1)), (uint32_t)((it - 1) >> 1) & 1u, g,
+                                    0x413)) {
                     ok = false;
                     break;
                 }
@@ -460,7 +476,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
             // P rows (generic-proxy stores) must be visible to the tensor core
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(bar(S::B_PFULL + x));
+            mbar_arrive(bar(S::B_PFULL + 2 * x + pb));
             kt = kt_next;
         }
         // ---------------------------------------------------------- epilogue
@@ -485,13 +501,13 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
 #pragma unroll
                 for (int t = 0; t < 16; ++t)
                     w[t] = pack_bf16x2(__uint_as_float(o[2 * t]) * inv_l, __uint_as_float(o[2 * t + 1]) * inv_l);
-                if (r < qn[x]) {
+                if (r < qnx) {
                     uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * j);
 #pragma unroll
                     for (int t = 0; t < 4; ++t) dst[t] = make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
                 }
             }
-            if (r < qn[x])
+            if (r < qnx)
                 p.LSE[(size_t)bh * p.N + q] = (l > 0.f) ? (m_ref + log2f(l)) * 0.69314718055994530942f : -INFINITY;
         }
         __syncwarp();
