@@ -238,7 +238,7 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_kernel(const __grid_constant__ 
         // dP(i+1) only needs dK(i) to have read dS(i) from the dP columns,
         // so the next step's scores are ready while the compute warps are
         // still on this step, and the tensor pipe keeps a queue.
-        if (lane == 0) {
+        {
             constexpr uint32_t IDESC_S = idesc_bf16(128, BQ, false, false);   // S^T, dP^T
             constexpr uint32_t IDESC_ACC = idesc_bf16(128, D, false, true);   // dV, dK
             constexpr uint32_t IDESC_DQ = idesc_bf16(128, 64, true, true);    // dQ or dQ^T
@@ -256,17 +256,17 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_kernel(const __grid_constant__ 
                 const uint64_t qd = sdesc_add(dQ_kmaj, (uint32_t)((step & 1) * S::Q_BYTES));
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k)
-                    mma_ss(tmem + S::TM_S, sdesc_add(dK_kmaj, (k >> 2) * S::KV_CHUNK + (k & 3) * 32),
+                    mma_ss_elect(tmem + S::TM_S, sdesc_add(dK_kmaj, (k >> 2) * S::KV_CHUNK + (k & 3) * 32),
                            sdesc_add(qd, (k >> 2) * S::Q_CHUNK + (k & 3) * 32), IDESC_S, k > 0 ? 1u : 0u);
-                mma_commit(bar(S::B_SFULL));
+                mma_commit_elect(bar(S::B_SFULL));
             };
             auto issue_dp = [&](int step) {      // dP^T = V dO^T
                 const uint64_t dd = sdesc_add(ddO_kmaj, (uint32_t)((step & 1) * S::Q_BYTES));
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k)
-                    mma_ss(tmem + S::TM_DP, sdesc_add(dV_kmaj, (k >> 2) * S::KV_CHUNK + (k & 3) * 32),
+                    mma_ss_elect(tmem + S::TM_DP, sdesc_add(dV_kmaj, (k >> 2) * S::KV_CHUNK + (k & 3) * 32),
                            sdesc_add(dd, (k >> 2) * S::Q_CHUNK + (k & 3) * 32), IDESC_S, k > 0 ? 1u : 0u);
-                mma_commit(bar(S::B_DPFULL));
+                mma_commit_elect(bar(S::B_DPFULL));
             };
             // P^T and dS^T are stored as bf16 pairs by the two compute
             // warpgroups, each inside its own half of the columns (so that
@@ -279,7 +279,7 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_kernel(const __grid_constant__ 
             bool ok = true;
             int i = 0;
             if (first < p.Tqb) {
-                ok = mbar_wait(bar(S::B_KV), 0, g, 0x211) && mbar_wait(bar(S::B_QFULL), 0, g, 0x212);
+                ok = mbar_wait_warp(bar(S::B_KV), 0, g, 0x211) && mbar_wait_warp(bar(S::B_QFULL), 0, g, 0x212);
                 if (ok) {
                     tc_fence_after();
                     issue_s(0);
@@ -293,32 +293,32 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_kernel(const __grid_constant__ 
                     const int qb_next = next_qb(qb);
                     const bool more = qb_next < p.Tqb;
                     // dV += P^T dO: A = P^T from TMEM, B = dO (N = D, K = queries, MN-major)
-                    if (!mbar_wait(bar(S::B_PFULL), (uint32_t)i & 1u, g, 0x214)) { ok = false; break; }
+                    if (!mbar_wait_warp(bar(S::B_PFULL), (uint32_t)i & 1u, g, 0x214)) { ok = false; break; }
                     tc_fence_after();
 #pragma unroll
                     for (int k = 0; k < BQ / 16; ++k)
-                        mma_ts(tmem + S::TM_DV, tmem + S::TM_S + packed_col(k), sdesc_add(do_mn, (uint32_t)k * 2048u),
+                        mma_ts_elect(tmem + S::TM_DV, tmem + S::TM_S + packed_col(k), sdesc_add(do_mn, (uint32_t)k * 2048u),
                                IDESC_ACC, k > 0 ? 1u : acc0);
-                    mma_commit(bar(S::B_SFREE));
+                    mma_commit_elect(bar(S::B_SFREE));
                     // S(i+1) once dV(i) has read P(i)
                     if (more) {
-                        if (!mbar_wait(bar(S::B_QFULL + (s ^ 1)), (uint32_t)((i + 1) >> 1) & 1u, g, 0x217) ||
-                            !mbar_wait(bar(S::B_SFREE), (uint32_t)i & 1u, g, 0x213)) { ok = false; break; }
+                        if (!mbar_wait_warp(bar(S::B_QFULL + (s ^ 1)), (uint32_t)((i + 1) >> 1) & 1u, g, 0x217) ||
+                            !mbar_wait_warp(bar(S::B_SFREE), (uint32_t)i & 1u, g, 0x213)) { ok = false; break; }
                         tc_fence_after();
                         issue_s(i + 1);
                     }
                     // dK += dS^T Q: A = dS^T from TMEM, B = Q (MN-major)
-                    if (!mbar_wait(bar(S::B_DSFULL), (uint32_t)i & 1u, g, 0x215)) { ok = false; break; }
+                    if (!mbar_wait_warp(bar(S::B_DSFULL), (uint32_t)i & 1u, g, 0x215)) { ok = false; break; }
                     tc_fence_after();
 #pragma unroll
                     for (int k = 0; k < BQ / 16; ++k)
-                        mma_ts(tmem + S::TM_DK, tmem + S::TM_DP + packed_col(k), sdesc_add(q_mn, (uint32_t)k * 2048u),
+                        mma_ts_elect(tmem + S::TM_DK, tmem + S::TM_DP + packed_col(k), sdesc_add(q_mn, (uint32_t)k * 2048u),
                                IDESC_ACC, k > 0 ? 1u : acc0);
-                    mma_commit(bar(S::B_DPFREE));
-                    mma_commit(bar(S::B_QEMPTY + s));
+                    mma_commit_elect(bar(S::B_DPFREE));
+                    mma_commit_elect(bar(S::B_QEMPTY + s));
                     // dQ contribution into TMEM buffer i % 2 (drained by the compute warps)
                     if (i >= 2 &&
-                        !mbar_wait(bar(S::B_DQFREE + s), (uint32_t)((i - 2) >> 1) & 1u, g, 0x216)) { ok = false; break; }
+                        !mbar_wait_warp(bar(S::B_DQFREE + s), (uint32_t)((i - 2) >> 1) & 1u, g, 0x216)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t dq_tmem = tmem + S::TM_DQ + 64u * (uint32_t)s;
 #pragma unroll
@@ -326,20 +326,20 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_kernel(const __grid_constant__ 
                         const uint64_t kk = sdesc_add(dK_mn, (uint32_t)k * 2048u);
                         const uint64_t dd = sdesc_add(ddS_mn, (uint32_t)k * 2048u);
                         // dQ = dS K: A = dS (M = queries), B = K (N = d)
-                        mma_ss(dq_tmem, dd, kk, IDESC_DQ, k > 0 ? 1u : 0u);
+                        mma_ss_elect(dq_tmem, dd, kk, IDESC_DQ, k > 0 ? 1u : 0u);
                     }
-                    mma_commit(bar(S::B_DQFULL + s));
+                    mma_commit_elect(bar(S::B_DQFULL + s));
                     // dP(i+1) once dK(i) has read dS(i)
                     if (more) {
-                        if (!mbar_wait(bar(S::B_DPFREE), (uint32_t)i & 1u, g, 0x218)) { ok = false; break; }
+                        if (!mbar_wait_warp(bar(S::B_DPFREE), (uint32_t)i & 1u, g, 0x218)) { ok = false; break; }
                         tc_fence_after();
                         issue_dp(i + 1);
                     }
                     qb = qb_next;
                 }
-                if (ok) mma_commit(bar(S::B_ACC));
+                if (ok) mma_commit_elect(bar(S::B_ACC));
             }
-            mma_commit(bar(S::B_FIN));
+            mma_commit_elect(bar(S::B_FIN));
             drain_wait_b(bar(S::B_FIN), 0);
         }
     } else if (warp >= 4) {

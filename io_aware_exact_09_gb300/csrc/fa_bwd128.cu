@@ -235,7 +235,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
                     b128_drain_wait(bar(S::B_QFULL + (j & 1)), (uint32_t)(j >> 1) & 1u);
                 if (nl > 0) b128_drain_wait(bar(S::B_DOFULL), (uint32_t)(nl - 1) & 1u);
             }
-        } else if (warp == 1 && lane == 0) {
+        } else if (warp == 1) {
             // ---------------------------------------------------------- MMA issuer
             // Order per block i: dV(i), dQ^T(i), dK(i), S^T(i+1), dP^T(i+1).
             constexpr uint32_t IDESC_S = idesc_bf16(128, BQ, false, false);   // S^T, dP^T
@@ -256,25 +256,25 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     const uint32_t off = (k >> 2) * S::CHUNK + (k & 3) * 32;
-                    mma_ss(region(i & 1), sdesc_add(dK_kmaj, off), sdesc_add(qd, off), IDESC_S, k > 0 ? 1u : 0u);
+                    mma_ss_elect(region(i & 1), sdesc_add(dK_kmaj, off), sdesc_add(qd, off), IDESC_S, k > 0 ? 1u : 0u);
                 }
-                mma_commit(bar(S::B_SFULL));
+                mma_commit_elect(bar(S::B_SFULL));
             };
             // dP^T(i) = V dO^T into region (i & 1) ^ 1
             auto issue_dp = [&](int i) {
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     const uint32_t off = (k >> 2) * S::CHUNK + (k & 3) * 32;
-                    mma_ss(region((i & 1) ^ 1), sdesc_add(dV_kmaj, off), sdesc_add(ddO_kmaj, off), IDESC_S,
+                    mma_ss_elect(region((i & 1) ^ 1), sdesc_add(dV_kmaj, off), sdesc_add(ddO_kmaj, off), IDESC_S,
                            k > 0 ? 1u : 0u);
                 }
-                mma_commit(bar(S::B_DPFULL));
+                mma_commit_elect(bar(S::B_DPFULL));
             };
             bool ok = true;
             int i = 0;
             if (first < p.Tqb) {
-                ok = mbar_wait(bar(S::B_KV), 0, g, 0x221) && mbar_wait(bar(S::B_QFULL), 0, g, 0x222) &&
-                     mbar_wait(bar(S::B_DOFULL), 0, g, 0x223);
+                ok = mbar_wait_warp(bar(S::B_KV), 0, g, 0x221) && mbar_wait_warp(bar(S::B_QFULL), 0, g, 0x222) &&
+                     mbar_wait_warp(bar(S::B_DOFULL), 0, g, 0x223);
                 if (ok) {
                     tc_fence_after();
                     issue_s(0);
@@ -286,48 +286,48 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
                     const uint32_t acc0 = i > 0 ? 1u : 0u;
                     const int qb_next = next_qb(qb);
                     // dV += P^T dO: A = P^T (region a, packed), B = dO (MN-major)
-                    if (!mbar_wait(bar(S::B_PFULL), (uint32_t)i & 1u, g, 0x224)) { ok = false; break; }
+                    if (!mbar_wait_warp(bar(S::B_PFULL), (uint32_t)i & 1u, g, 0x224)) { ok = false; break; }
                     tc_fence_after();
 #pragma unroll
                     for (int k = 0; k < BQ / 16; ++k)
-                        mma_ts(tmem + S::TM_DV, ra + packed_col128(k), sdesc_add(ddO_mn, (uint32_t)k * 2048u),
+                        mma_ts_elect(tmem + S::TM_DV, ra + packed_col128(k), sdesc_add(ddO_mn, (uint32_t)k * 2048u),
                                IDESC_ACC, k > 0 ? 1u : acc0);
-                    mma_commit(bar(S::B_DVDONE));
+                    mma_commit_elect(bar(S::B_DVDONE));
                     // dQ^T = K^T dS^T into region a (once dV has read P^T there), first:
                     // the sooner it is drained, the sooner dP^T(i+1) can use region a;
                     // dK follows
-                    if (!mbar_wait(bar(S::B_DSFULL), (uint32_t)i & 1u, g, 0x225) ||
-                        !mbar_wait(bar(S::B_DVDONE), (uint32_t)i & 1u, g, 0x226)) { ok = false; break; }
+                    if (!mbar_wait_warp(bar(S::B_DSFULL), (uint32_t)i & 1u, g, 0x225) ||
+                        !mbar_wait_warp(bar(S::B_DVDONE), (uint32_t)i & 1u, g, 0x226)) { ok = false; break; }
                     tc_fence_after();
 #pragma unroll
                     for (int k = 0; k < kTile / 16; ++k)
-                        mma_ss(ra, sdesc_add(dK_mn, (uint32_t)k * 2048u), sdesc_add(ddS_mn, (uint32_t)k * 2048u),
+                        mma_ss_elect(ra, sdesc_add(dK_mn, (uint32_t)k * 2048u), sdesc_add(ddS_mn, (uint32_t)k * 2048u),
                                IDESC_DQ, k > 0 ? 1u : 0u);
-                    mma_commit(bar(S::B_DQFULL));
+                    mma_commit_elect(bar(S::B_DQFULL));
                     // dK += dS^T Q: A = dS^T (region b, packed), B = Q (MN-major)
                     const uint64_t q_mn = sdesc_add(dQ_mn, (uint32_t)(s * S::TILE));
 #pragma unroll
                     for (int k = 0; k < BQ / 16; ++k)
-                        mma_ts(tmem + S::TM_DK, rb + packed_col128(k), sdesc_add(q_mn, (uint32_t)k * 2048u),
+                        mma_ts_elect(tmem + S::TM_DK, rb + packed_col128(k), sdesc_add(q_mn, (uint32_t)k * 2048u),
                                IDESC_ACC, k > 0 ? 1u : acc0);
-                    mma_commit(bar(S::B_QEMPTY + s));       // dK(i) done
+                    mma_commit_elect(bar(S::B_QEMPTY + s));       // dK(i) done
                     if (qb_next < p.Tqb) {
                         // S^T(i+1) into region b once dK has read dS^T there
-                        if (!mbar_wait(bar(S::B_QFULL + (s ^ 1)), (uint32_t)((i + 1) >> 1) & 1u, g, 0x227) ||
-                            !mbar_wait(bar(S::B_QEMPTY + s), (uint32_t)(i >> 1) & 1u, g, 0x228)) { ok = false; break; }
+                        if (!mbar_wait_warp(bar(S::B_QFULL + (s ^ 1)), (uint32_t)((i + 1) >> 1) & 1u, g, 0x227) ||
+                            !mbar_wait_warp(bar(S::B_QEMPTY + s), (uint32_t)(i >> 1) & 1u, g, 0x228)) { ok = false; break; }
                         tc_fence_after();
                         issue_s(i + 1);
                         // dP^T(i+1) into region a once dQ^T(i) has been drained
-                        if (!mbar_wait(bar(S::B_DOFULL), (uint32_t)(i + 1) & 1u, g, 0x229) ||
-                            !mbar_wait(bar(S::B_DQFREE), (uint32_t)i & 1u, g, 0x22a)) { ok = false; break; }
+                        if (!mbar_wait_warp(bar(S::B_DOFULL), (uint32_t)(i + 1) & 1u, g, 0x229) ||
+                            !mbar_wait_warp(bar(S::B_DQFREE), (uint32_t)i & 1u, g, 0x22a)) { ok = false; break; }
                         tc_fence_after();
                         issue_dp(i + 1);
                     }
                     qb = qb_next;
                 }
-                if (ok) mma_commit(bar(S::B_ACC));
+                if (ok) mma_commit_elect(bar(S::B_ACC));
             }
-            mma_commit(bar(S::B_FIN));
+            mma_commit_elect(bar(S::B_FIN));
             b128_drain_wait(bar(S::B_FIN), 0);
         }
     } else if (warp < 12) {

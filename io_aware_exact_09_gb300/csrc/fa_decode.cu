@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(256, 1) fa_decode_kernel(const __grid_constant
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer
-        if (lane == 0) {
+        {
             constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
             constexpr uint32_t IDESC_PV = idesc_bf16(128, D, false, true);
             const uint64_t dq0 = sdesc_sw128(base + S::OFF_Q, 16, 1024);
@@ -184,13 +184,13 @@ __global__ void __launch_bounds__(256, 1) fa_decode_kernel(const __grid_constant
             const uint64_t dv0 = sdesc_sw128(base + S::OFF_V, S::CHUNK_BYTES, 1024);
             bool ok = true;
             if (first < kt_end) {
-                ok = mbar_wait(bar(S::B_QFULL), 0, g, 0x511);
+                ok = mbar_wait_warp(bar(S::B_QFULL), 0, g, 0x511);
                 // S_i = Q K_i^T into TMEM buffer i % 2
                 auto issue_s = [&](int i) -> bool {
                     const int s = i % S::STAGES;
-                    if (!mbar_wait(bar(S::B_KFULL + s), (uint32_t)(i / S::STAGES) & 1u, g, 0x512)) return false;
+                    if (!mbar_wait_warp(bar(S::B_KFULL + s), (uint32_t)(i / S::STAGES) & 1u, g, 0x512)) return false;
                     // buffer i % 2 last held P_{i-2}: its P.V must have finished
-                    if (i >= 2 && !mbar_wait(bar(S::B_PVDONE + (i & 1)), (uint32_t)((i - 2) >> 1) & 1u, g, 0x513))
+                    if (i >= 2 && !mbar_wait_warp(bar(S::B_PVDONE + (i & 1)), (uint32_t)((i - 2) >> 1) & 1u, g, 0x513))
                         return false;
                     tc_fence_after();
                     const uint32_t d_tmem = tmem + S::TM_S + (uint32_t)(i & 1) * 128u;
@@ -198,9 +198,9 @@ __global__ void __launch_bounds__(256, 1) fa_decode_kernel(const __grid_constant
 #pragma unroll
                     for (int k = 0; k < D / 16; ++k) {
                         const uint32_t off = (k >> 2) * S::CHUNK_BYTES + (k & 3) * 32;
-                        mma_ss(d_tmem, sdesc_add(dq0, off), sdesc_add(kd, off), IDESC_S, k > 0 ? 1u : 0u);
+                        mma_ss_elect(d_tmem, sdesc_add(dq0, off), sdesc_add(kd, off), IDESC_S, k > 0 ? 1u : 0u);
                     }
-                    mma_commit(bar(S::B_SFULL + (i & 1)));
+                    mma_commit_elect(bar(S::B_SFULL + (i & 1)));
                     return true;
                 };
                 if (ok) ok = issue_s(0);
@@ -209,8 +209,8 @@ __global__ void __launch_bounds__(256, 1) fa_decode_kernel(const __grid_constant
                     const int kt_next = next_tile(kt);
                     if (kt_next < kt_end && !(ok = issue_s(it + 1))) break;
                     const int s = it % S::STAGES;
-                    if (!mbar_wait(bar(S::B_PFULL + (it & 1)), (uint32_t)(it >> 1) & 1u, g, 0x514) ||
-                        !mbar_wait(bar(S::B_VFULL + s), (uint32_t)(it / S::STAGES) & 1u, g, 0x515)) {
+                    if (!mbar_wait_warp(bar(S::B_PFULL + (it & 1)), (uint32_t)(it >> 1) & 1u, g, 0x514) ||
+                        !mbar_wait_warp(bar(S::B_VFULL + s), (uint32_t)(it / S::STAGES) & 1u, g, 0x515)) {
                         ok = false;
                         break;
                     }
@@ -220,14 +220,14 @@ __global__ void __launch_bounds__(256, 1) fa_decode_kernel(const __grid_constant
                     const uint32_t acc0 = it > 0 ? 1u : 0u;
 #pragma unroll
                     for (int k = 0; k < kTile / 16; ++k)
-                        mma_ts(tmem + S::TM_O, p_tmem + (uint32_t)k * 8u, sdesc_add(vd, (uint32_t)k * 2048u), IDESC_PV,
+                        mma_ts_elect(tmem + S::TM_O, p_tmem + (uint32_t)k * 8u, sdesc_add(vd, (uint32_t)k * 2048u), IDESC_PV,
                                k > 0 ? 1u : acc0);
-                    mma_commit(bar(S::B_KVEMPTY + s));
-                    mma_commit(bar(S::B_PVDONE + (it & 1)));
+                    mma_commit_elect(bar(S::B_KVEMPTY + s));
+                    mma_commit_elect(bar(S::B_PVDONE + (it & 1)));
                     kt = kt_next;
                 }
             }
-            mma_commit(bar(S::B_FIN));
+            mma_commit_elect(bar(S::B_FIN));
             dec_drain_wait(bar(S::B_FIN), 0);
         }
     } else if (warp >= 4) {

@@ -271,7 +271,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
             }
         } else if (warp == 1) {
             // ---------------------------------------------------------- MMA issuer
-            if (lane == 0) {
+            {
                 constexpr uint32_t IDESC_S = idesc_bf16(128, BC, false, false);
                 constexpr uint32_t IDESC_PV = idesc_bf16(128, D, false, true);
                 int kt = next_tile(2, -1);
@@ -292,12 +292,12 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                     for (int k = 0; k < D / 16; ++k) {
                         const uint32_t off = (k >> 2) * S::CHUNK_BYTES + (k & 3) * 32;
                         const uint32_t koff = (k >> 2) * S::KV_CHUNK_BYTES + (k & 3) * 32;
-                        mma_ss(d_tmem, sdesc_add(qd, off), sdesc_add(kd, koff), IDESC_S, k > 0 ? 1u : 0u);
+                        mma_ss_elect(d_tmem, sdesc_add(qd, off), sdesc_add(kd, koff), IDESC_S, k > 0 ? 1u : 0u);
                     }
-                    mma_commit(bar(S::B_SFULL + x));
+                    mma_commit_elect(bar(S::B_SFULL + x));
                 };
                 if (kt < Tk) {
-                    ok = mbar_wait(bar(S::B_QFULL), 0, g, 0x201) && mbar_wait(bar(S::B_KFULL + 0), 0, g, 0x202);
+                    ok = mbar_wait_warp(bar(S::B_QFULL), 0, g, 0x201) && mbar_wait_warp(bar(S::B_KFULL + 0), 0, g, 0x202);
                     if (ok) {
                         tc_fence_after();
                         for (int x = 0; x < 2; ++x)
@@ -315,9 +315,9 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                         // on without waiting for the other tile's P
                         for (int x = 0; x < 2 && ok; ++x) {
                             if (cls(x, kt) != kTileSkip) {
-                                if (!mbar_wait(bar(S::B_PFULL + x), (uint32_t)nv[x] & 1u, g, 0x203) ||
+                                if (!mbar_wait_warp(bar(S::B_PFULL + x), (uint32_t)nv[x] & 1u, g, 0x203) ||
                                     (!vwaited &&
-                                     !mbar_wait(bar(S::B_VFULL + s), (uint32_t)(u / S::STAGES) & 1u, g, 0x204))) {
+                                     !mbar_wait_warp(bar(S::B_VFULL + s), (uint32_t)(u / S::STAGES) & 1u, g, 0x204))) {
                                     ok = false;
                                     break;
                                 }
@@ -329,19 +329,19 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                                 const uint32_t acc0 = nv[x] > 0 ? 1u : 0u;
 #pragma unroll
                                 for (int k = 0; k < BC / 16; ++k)
-                                    mma_ts(o_tmem, p_tmem + (uint32_t)k * 8u, sdesc_add(vd, (uint32_t)k * 2048u),
+                                    mma_ts_elect(o_tmem, p_tmem + (uint32_t)k * 8u, sdesc_add(vd, (uint32_t)k * 2048u),
                                            IDESC_PV, k > 0 ? 1u : acc0);
-                                mma_commit(bar(S::B_PVDONE + x));
+                                mma_commit_elect(bar(S::B_PVDONE + x));
                                 ++nv[x];
                             }
                             if (kt_next < Tk && cls(x, kt_next) != kTileSkip) {
-                                if (!kwaited && !mbar_wait(bar(S::B_KFULL + s2), (uint32_t)((u + 1) / S::STAGES) & 1u,
+                                if (!kwaited && !mbar_wait_warp(bar(S::B_KFULL + s2), (uint32_t)((u + 1) / S::STAGES) & 1u,
                                                            g, 0x205)) {
                                     ok = false;
                                     break;
                                 }
                                 kwaited = true;
-                                if (nv[x] > 0 && !mbar_wait(bar(S::B_PVDONE + x), (uint32_t)(nv[x] - 1) & 1u, g, 0x206)) {
+                                if (nv[x] > 0 && !mbar_wait_warp(bar(S::B_PVDONE + x), (uint32_t)(nv[x] - 1) & 1u, g, 0x206)) {
                                     ok = false;
                                     break;
                                 }
@@ -351,13 +351,13 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                         }
                         if (!ok) break;
                         // K and V of stage s are free once this tile's products are done
-                        mma_commit(bar(S::B_KVEMPTY + s));
+                        mma_commit_elect(bar(S::B_KVEMPTY + s));
                         kt = kt_next;
                         ++u;
                     }
                 }
                 // every MMA this thread issued must finish before TMEM is freed
-                mma_commit(bar(S::B_FIN));
+                mma_commit_elect(bar(S::B_FIN));
                 drain_wait(bar(S::B_FIN), 0);
             }
         }

@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
             }
         } else if (warp == 1) {
             // ---------------------------------------------------------- MMA issuer
-            if (lane == 0) {
+            {
                 constexpr uint32_t IDESC_S = idesc_e4m3(128, 128);
                 constexpr uint32_t IDESC_PV = idesc_e4m3(128, D);
                 // all operands K-major, 128-byte rows: 32 bytes (32 e4m3) per K step
@@ -234,13 +234,13 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
                     const uint64_t kd = sdesc_add(dk0, (uint32_t)(s * S::TILE_BYTES));
 #pragma unroll
                     for (int k = 0; k < D / 32; ++k)
-                        mma_ss_f8(d_tmem, sdesc_add(qd, 32u * k), sdesc_add(kd, 32u * k), IDESC_S, k > 0 ? 1u : 0u);
-                    mma_commit(bar(S::B_SFULL + x));
+                        mma_ss_f8_elect(d_tmem, sdesc_add(qd, 32u * k), sdesc_add(kd, 32u * k), IDESC_S, k > 0 ? 1u : 0u);
+                    mma_commit_elect(bar(S::B_SFULL + x));
                     ++ns[x];
                 };
                 int kt = next_tile(2, -1);
                 if (kt < p.Tk) {
-                    ok = mbar_wait(bar(S::B_QFULL), 0, g, 0x211) && mbar_wait(bar(S::B_KFULL + 0), 0, g, 0x212);
+                    ok = mbar_wait_warp(bar(S::B_QFULL), 0, g, 0x211) && mbar_wait_warp(bar(S::B_KFULL + 0), 0, g, 0x212);
                     if (ok) {
                         tc_fence_after();
 #pragma unroll
@@ -255,14 +255,14 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
                     const int kt_next = next_tile(2, kt);
                     if (kt_next < p.Tk) {
                         const int s2 = (u + 1) % S::STAGES;
-                        if (!mbar_wait(bar(S::B_KFULL + s2), (uint32_t)((u + 1) / S::STAGES) & 1u, g, 0x213)) {
+                        if (!mbar_wait_warp(bar(S::B_KFULL + s2), (uint32_t)((u + 1) / S::STAGES) & 1u, g, 0x213)) {
                             ok = false;
                             break;
                         }
 #pragma unroll
                         for (int x = 0; x < 2 && ok; ++x) {
                             if (skip(x, kt_next)) continue;
-                            if (ns[x] > 0 && !mbar_wait(bar(S::B_SFREE + x), (uint32_t)(ns[x] - 1) & 1u, g, 0x214)) {
+                            if (ns[x] > 0 && !mbar_wait_warp(bar(S::B_SFREE + x), (uint32_t)(ns[x] - 1) & 1u, g, 0x214)) {
                                 ok = false;
                                 break;
                             }
@@ -276,9 +276,9 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
 #pragma unroll
                     for (int x = 0; x < 2 && ok; ++x) {
                         if (skip(x, kt)) continue;
-                        if (!mbar_wait(bar(S::B_PFULL + 2 * x + (nv[x] & 1)), (uint32_t)(nv[x] >> 1) & 1u, g,
+                        if (!mbar_wait_warp(bar(S::B_PFULL + 2 * x + (nv[x] & 1)), (uint32_t)(nv[x] >> 1) & 1u, g,
                                        0x215) ||
-                            (!vwaited && !mbar_wait(bar(S::B_VFULL + s), (uint32_t)(u / S::STAGES) & 1u, g, 0x216))) {
+                            (!vwaited && !mbar_wait_warp(bar(S::B_VFULL + s), (uint32_t)(u / S::STAGES) & 1u, g, 0x216))) {
                             ok = false;
                             break;
                         }
@@ -291,13 +291,13 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
                         const uint32_t acc0 = nv[x] > 0 ? 1u : 0u;
 #pragma unroll
                         for (int k = 0; k < kTile / 32; ++k)
-                            mma_ss_f8(o_tmem, sdesc_add(pd, 32u * k), sdesc_add(vd, 32u * k), IDESC_PV,
+                            mma_ss_f8_elect(o_tmem, sdesc_add(pd, 32u * k), sdesc_add(vd, 32u * k), IDESC_PV,
                                       k > 0 ? 1u : acc0);
-                        mma_commit(bar(S::B_PFREE + 2 * x + pb));
+                        mma_commit_elect(bar(S::B_PFREE + 2 * x + pb));
                         ++nv[x];
                     }
                     if (!ok) break;
-                    mma_commit(bar(S::B_KVEMPTY + s));
+                    mma_commit_elect(bar(S::B_KVEMPTY + s));
                     kt = kt_next;
                     ++u;
                 }
@@ -306,10 +306,10 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
                 // their epilogue before the last ones land: they wait on this
                 // single-use barrier.
                 if (ok) {
-                    mma_commit(bar(S::B_OFULL + 0));
-                    mma_commit(bar(S::B_OFULL + 1));
+                    mma_commit_elect(bar(S::B_OFULL + 0));
+                    mma_commit_elect(bar(S::B_OFULL + 1));
                 }
-                mma_commit(bar(S::B_FIN));
+                mma_commit_elect(bar(S::B_FIN));
                 f8_drain_wait(bar(S::B_FIN), 0);
             }
         }
