@@ -142,26 +142,26 @@ __global__ void __launch_bounds__(256, 1) fa_decode_kernel(const __grid_constant
 
     if (warp == 0) {
         // ---------------------------------------------------------- producer
-        if (lane == 0 && first < kt_end) {
+        if (first < kt_end) {
             int it = 0;
             bool ok = true;
-            mbar_arrive_expect_tx(bar(S::B_QFULL), S::TILE_BYTES);
+            mbar_arrive_expect_tx_elect(bar(S::B_QFULL), S::TILE_BYTES);
             for (int c = 0; c < S::CHUNKS; ++c)
-                tma_load_3d(base + S::OFF_Q + c * S::CHUNK_BYTES, &p.tmQ, bar(S::B_QFULL), c * 64, q0, bh);
+                tma_load_3d_elect(base + S::OFF_Q + c * S::CHUNK_BYTES, &p.tmQ, bar(S::B_QFULL), c * 64, q0, bh);
             for (int kt = first; kt < kt_end; kt = next_tile(kt), ++it) {
                 const int s = it % S::STAGES;
                 const uint32_t ph = (uint32_t)(it / S::STAGES) & 1u;
-                if (!mbar_wait(bar(S::B_KVEMPTY + s), ph ^ 1u, g, 0x501)) {
+                if (!mbar_wait_warp(bar(S::B_KVEMPTY + s), ph ^ 1u, g, 0x501)) {
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(bar(S::B_KFULL + s), S::TILE_BYTES);
+                mbar_arrive_expect_tx_elect(bar(S::B_KFULL + s), S::TILE_BYTES);
                 for (int c = 0; c < S::CHUNKS; ++c)
-                    tma_load_3d(base + S::OFF_K + s * S::TILE_BYTES + c * S::CHUNK_BYTES, &p.tmK, bar(S::B_KFULL + s),
+                    tma_load_3d_elect(base + S::OFF_K + s * S::TILE_BYTES + c * S::CHUNK_BYTES, &p.tmK, bar(S::B_KFULL + s),
                                 c * 64, kt * kTile, bh);
-                mbar_arrive_expect_tx(bar(S::B_VFULL + s), S::TILE_BYTES);
+                mbar_arrive_expect_tx_elect(bar(S::B_VFULL + s), S::TILE_BYTES);
                 for (int c = 0; c < S::CHUNKS; ++c)
-                    tma_load_3d(base + S::OFF_V + s * S::TILE_BYTES + c * S::CHUNK_BYTES, &p.tmV, bar(S::B_VFULL + s),
+                    tma_load_3d_elect(base + S::OFF_V + s * S::TILE_BYTES + c * S::CHUNK_BYTES, &p.tmV, bar(S::B_VFULL + s),
                                 c * 64, kt * kTile, bh);
             }
             if (!ok) {

@@ -84,8 +84,8 @@ struct FwdShape {
     // warpgroup 0 (producer, MMA, two idle warps) keeps 88, the two softmax
     // warpgroups get 208: 128 x 88 + 256 x 208 = 64,512.
     static constexpr int LAUNCH_REGS = 168;
-    static constexpr int REGS_CTRL = 88;
-    static constexpr int REGS_SOFTMAX = 208;
+    static constexpr int REGS_CTRL = 104;
+    static constexpr int REGS_SOFTMAX = 200;
     static_assert(128 * REGS_CTRL + 256 * REGS_SOFTMAX == THREADS * LAUNCH_REGS, "register split");
 };
 
@@ -140,11 +140,12 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
     }
     // TMA coordinates of row `row` of a sequence starting at `start`:
     // [B*H][N][d] view, or the [total][H][d] view of a ragged batch
+    // warp-collective (the producer warp calls it with uniform arguments)
     auto tload = [&](uint32_t dst, const CUtensorMap *m, uint32_t mbar, int c, int row, int start) {
         if constexpr (VARLEN)
-            tma_load_3d(dst, m, mbar, c * 64, h, start + row);
+            tma_load_3d_elect(dst, m, mbar, c * 64, h, start + row);
         else
-            tma_load_3d(dst, m, mbar, c * 64, row, bh);
+            tma_load_3d_elect(dst, m, mbar, c * 64, row, bh);
     };
 
     auto bar = [&](int i) -> uint32_t { return base + S::OFF_BAR + 8u * (uint32_t)i; };
@@ -167,19 +168,23 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
         kend[x] = (qn[x] > 0 && lim > 0) ? (lim + BC - 1) / BC : 0;
     }
     const int kend_union = max(kend[0], kend[1]);
+    // per-query-tile values by selection, so that the arrays stay in registers
+    auto q0_of = [&](int x) { return x ? q0[1] : q0[0]; };
+    auto qn_of = [&](int x) { return x ? qn[1] : qn[0]; };
+    auto kend_of = [&](int x) { return x ? kend[1] : kend[0]; };
     // class of key tile kt for query tile x of the pair
     auto cls = [&](int x, int kt) -> unsigned {
-        if (qn[x] <= 0) return kTileSkip;
-        if constexpr (VARLEN) return tile_class_shift(q0[x], qn[x], kt * BC, BC, kvis, p.causal, shift);
+        if (qn_of(x) <= 0) return kTileSkip;
+        if constexpr (VARLEN) return tile_class_shift(q0_of(x), qn_of(x), kt * BC, BC, kvis, p.causal, shift);
         // a key tile of BC <= 128 columns lies inside one 128-wide mask block
         const int on =
             p.block_mask ? (p.block_mask[(size_t)(QPC * pq + x) * nb + (BC == kTile ? kt : kt / (kTile / BC))] != 0) : 1;
-        return tile_class(q0[x], qn[x], kt * BC, BC, kvis, p.causal, on);
+        return tile_class(q0_of(x), qn_of(x), kt * BC, BC, kvis, p.causal, on);
     };
     // next key tile after kt seen by query tile x (x = 2: by either)
     auto next_tile = [&](int x, int kt) -> int {
         if (!p.block_mask) {
-            const int lim = x == 2 ? kend_union : kend[x];
+            const int lim = x == 2 ? kend_union : kend_of(x);
             return kt + 1 < lim ? kt + 1 : Tk;
         }
         for (int k = kt + 1; k < Tk; ++k) {
@@ -229,13 +234,14 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
         setmaxnreg_dec<S::REGS_CTRL>();
         if (warp == 0) {
             // ---------------------------------------------------------- producer
-            if (lane == 0) {
+            {
                 int u = 0;
                 bool ok = true;
                 int kt = next_tile(2, -1);
                 if (kt < Tk) {
                     const uint32_t nq = (qn[0] > 0 ? 1u : 0u) + (qn[1] > 0 ? 1u : 0u);
-                    mbar_arrive_expect_tx(bar(S::B_QFULL), nq * S::TILE_BYTES);
+                    mbar_arrive_expect_tx_elect(bar(S::B_QFULL), nq * S::TILE_BYTES);
+                    #pragma unroll
                     for (int x = 0; x < 2; ++x)
                         if (qn[x] > 0)
                             for (int c = 0; c < S::CHUNKS; ++c)
@@ -245,16 +251,16 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                 for (; kt < Tk; kt = next_tile(2, kt), ++u) {
                     const int s = u % S::STAGES;
                     const uint32_t ph = (uint32_t)(u / S::STAGES) & 1u;
-                    if (!mbar_wait(bar(S::B_KVEMPTY + s), ph ^ 1u, g, 0x101)) {
+                    if (!mbar_wait_warp(bar(S::B_KVEMPTY + s), ph ^ 1u, g, 0x101)) {
                         ok = false;
                         break;
                     }
                     const uint32_t koff = base + S::OFF_K + s * S::KV_TILE_BYTES;
                     const uint32_t voff = base + S::OFF_V + s * S::KV_TILE_BYTES;
-                    mbar_arrive_expect_tx(bar(S::B_KFULL + s), S::KV_TILE_BYTES);
+                    mbar_arrive_expect_tx_elect(bar(S::B_KFULL + s), S::KV_TILE_BYTES);
                     for (int c = 0; c < S::CHUNKS; ++c)
                         tload(koff + c * S::KV_CHUNK_BYTES, &p.tmK, bar(S::B_KFULL + s), c, kt * BC, k_start);
-                    mbar_arrive_expect_tx(bar(S::B_VFULL + s), S::KV_TILE_BYTES);
+                    mbar_arrive_expect_tx_elect(bar(S::B_VFULL + s), S::KV_TILE_BYTES);
                     for (int c = 0; c < S::CHUNKS; ++c)
                         tload(voff + c * S::KV_CHUNK_BYTES, &p.tmV, bar(S::B_VFULL + s), c, kt * BC, k_start);
                 }
@@ -300,6 +306,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                     ok = mbar_wait_warp(bar(S::B_QFULL), 0, g, 0x201) && mbar_wait_warp(bar(S::B_KFULL + 0), 0, g, 0x202);
                     if (ok) {
                         tc_fence_after();
+                        #pragma unroll
                         for (int x = 0; x < 2; ++x)
                             if (cls(x, kt) != kTileSkip) issue_s(x, 0);
                     }
@@ -313,6 +320,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                         // tile's S_x (it overwrites P_x, so it waits for that P.V),
                         // so that each tile's chain S -> softmax -> P.V -> S moves
                         // on without waiting for the other tile's P
+                        #pragma unroll
                         for (int x = 0; x < 2 && ok; ++x) {
                             if (cls(x, kt) != kTileSkip) {
                                 if (!mbar_wait_warp(bar(S::B_PFULL + x), (uint32_t)nv[x] & 1u, g, 0x203) ||
@@ -367,7 +375,8 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
         const int x = (warp - 4) >> 2;
         const int wq = warp & 3;
         const int r = wq * 32 + lane;
-        const int q = q0[x] + r;
+        const int q0x = q0_of(x), qnx = qn_of(x);
+        const int q = q0x + r;
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const uint32_t s_tmem = tmem + lane_off + S::TM_S + 128u * (uint32_t)x;
         const uint32_t o_tmem = tmem + lane_off + S::TM_O + (uint32_t)(D * x);
@@ -502,13 +511,13 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
 #pragma unroll
                 for (int t = 0; t < 16; ++t)
                     w[t] = pack_bf16x2(__uint_as_float(o[2 * t]) * inv_l, __uint_as_float(o[2 * t + 1]) * inv_l);
-                if (r < qn[x]) {
+                if (r < qnx) {
                     uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * j);
 #pragma unroll
                     for (int t = 0; t < 4; ++t) dst[t] = make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
                 }
             }
-            if (r < qn[x])
+            if (r < qnx)
                 p.LSE[VARLEN ? (size_t)h * p.total_q + q_start + q : (size_t)bh * p.N + q] =
                     (l > 0.f) ? (m_ref + log2f(l)) * 0.69314718055994530942f : -INFINITY;
         }

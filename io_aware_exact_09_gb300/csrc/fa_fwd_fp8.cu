@@ -181,29 +181,29 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
         setmaxnreg_dec<S::REGS_CTRL>();
         if (warp == 0) {
             // ---------------------------------------------------------- producer
-            if (lane == 0) {
+            {
                 int u = 0;
                 bool ok = true;
                 int kt = next_tile(2, -1);
                 if (kt < p.Tk) {
                     const uint32_t nq = (qn[0] > 0 ? 1u : 0u) + (qn[1] > 0 ? 1u : 0u);
-                    mbar_arrive_expect_tx(bar(S::B_QFULL), nq * S::TILE_BYTES);
+                    mbar_arrive_expect_tx_elect(bar(S::B_QFULL), nq * S::TILE_BYTES);
 #pragma unroll
                     for (int x = 0; x < 2; ++x)
                         if (qn[x] > 0)
-                            tma_load_3d(base + S::OFF_Q + x * S::TILE_BYTES, &p.tmQ, bar(S::B_QFULL), 0, q0[x], bh);
+                            tma_load_3d_elect(base + S::OFF_Q + x * S::TILE_BYTES, &p.tmQ, bar(S::B_QFULL), 0, q0[x], bh);
                 }
                 for (; kt < p.Tk; kt = next_tile(2, kt), ++u) {
                     const int s = u % S::STAGES;
                     const uint32_t ph = (uint32_t)(u / S::STAGES) & 1u;
-                    if (!mbar_wait(bar(S::B_KVEMPTY + s), ph ^ 1u, g, 0x111)) {
+                    if (!mbar_wait_warp(bar(S::B_KVEMPTY + s), ph ^ 1u, g, 0x111)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(bar(S::B_KFULL + s), S::TILE_BYTES);
-                    tma_load_3d(base + S::OFF_K + s * S::TILE_BYTES, &p.tmK, bar(S::B_KFULL + s), 0, kt * kTile, bh);
-                    mbar_arrive_expect_tx(bar(S::B_VFULL + s), S::TILE_BYTES);
-                    tma_load_3d(base + S::OFF_V + s * S::TILE_BYTES, &p.tmV, bar(S::B_VFULL + s), kt * kTile, 0, bh);
+                    mbar_arrive_expect_tx_elect(bar(S::B_KFULL + s), S::TILE_BYTES);
+                    tma_load_3d_elect(base + S::OFF_K + s * S::TILE_BYTES, &p.tmK, bar(S::B_KFULL + s), 0, kt * kTile, bh);
+                    mbar_arrive_expect_tx_elect(bar(S::B_VFULL + s), S::TILE_BYTES);
+                    tma_load_3d_elect(base + S::OFF_V + s * S::TILE_BYTES, &p.tmV, bar(S::B_VFULL + s), kt * kTile, 0, bh);
                 }
                 if (!ok) {
                     if (next_tile(2, -1) < p.Tk) f8_drain_wait(bar(S::B_QFULL), 0);
