@@ -24,10 +24,12 @@
 //   - one CTA per (pair of 128-row query tiles, b*h), head-major;
 //   - warp 0: TMA of both Q tiles once, K and V^T tiles through a 3-stage
 //     ring;
-//   - warp 1: tcgen05 issuer.  Per key tile i: S_x(i+1) = Q_x K(i+1)^T as
-//     soon as softmax x has loaded S_x(i) (SFREE), then O_x += P_x(i) V(i)
-//     (A = P_x from shared memory, B = V^T, both K-major) once P_x(i) is
-//     written (PFULL);
+//   - warps 1 and 2: tcgen05 issuers, one per query tile x, so that one
+//     tile's chain never waits on the other's softmax.  Per key tile i:
+//     S_x(i+1) = Q_x K(i+1)^T as soon as softmax x has loaded S_x(i)
+//     (SFREE), then O_x += P_x(i) V(i) (A = P_x from shared memory, B = V^T,
+//     both K-major) once P_x(i) is written (PFULL).  A K/V stage is free
+//     once both issuers are done with it (two arrivals);
 //   - warps 4-7 and 8-11: softmax of query tile 0 and 1, one row per
 //     thread; P rows go to shared memory in the 128-byte-swizzled K-major
 //     layout the MMA reads.
@@ -61,8 +63,8 @@ struct F8Shape {
     static constexpr int B_PFULL = B_SFREE + 2;             // [2][2] per query tile and P buffer
     static constexpr int B_PFREE = B_PFULL + 4;             // [2][2]
     static constexpr int B_OFULL = B_PFREE + 4;             // [2] every product done (single use)
-    static constexpr int B_FIN = B_OFULL + 2;
-    static constexpr int NBAR = B_FIN + 1;
+    static constexpr int B_FIN = B_OFULL + 2;               // [2] per issuer
+    static constexpr int NBAR = B_FIN + 2;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
     static constexpr uint32_t TMEM_COLS = 512;
@@ -149,7 +151,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
         for (int s = 0; s < S::STAGES; ++s) {
             mbar_init(bar(S::B_KFULL + s), 1);
             mbar_init(bar(S::B_VFULL + s), 1);
-            mbar_init(bar(S::B_KVEMPTY + s), 1);
+            mbar_init(bar(S::B_KVEMPTY + s), 2);
         }
         for (int j = 0; j < 2; ++j) {
             mbar_init(bar(S::B_SFULL + j), 1);
@@ -161,7 +163,8 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
         }
         mbar_init(bar(S::B_OFULL + 0), 1);
         mbar_init(bar(S::B_OFULL + 1), 1);
-        mbar_init(bar(S::B_FIN), 1);
+        mbar_init(bar(S::B_FIN + 0), 1);
+        mbar_init(bar(S::B_FIN + 1), 1);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&p.tmQ);
@@ -215,102 +218,85 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
                     }
                 }
             }
-        } else if (warp == 1) {
-            // ---------------------------------------------------------- MMA issuer
+        } else if (warp == 1 || warp == 2) {
+            // ---------------------------------------------------------- MMA issuer of query tile x
             {
+                const int x = warp - 1;
                 constexpr uint32_t IDESC_S = idesc_e4m3(128, 128);
                 constexpr uint32_t IDESC_PV = idesc_e4m3(128, D);
-                // all operands K-major, 128-byte rows: 32 bytes (32 e4m3) per K step
-                const uint64_t dq0 = sdesc_sw128(base + S::OFF_Q, 16, 1024);
+                const uint64_t dq = sdesc_add(sdesc_sw128(base + S::OFF_Q, 16, 1024), (uint32_t)(x * S::TILE_BYTES));
                 const uint64_t dk0 = sdesc_sw128(base + S::OFF_K, 16, 1024);
                 const uint64_t dv0 = sdesc_sw128(base + S::OFF_V, 16, 1024);
-                const uint64_t dp0 = sdesc_sw128(base + S::OFF_P, 16, 1024);
-                int nv[2] = {0, 0};     // P.V products issued per query tile
-                int ns[2] = {0, 0};     // S products issued per query tile
+                const uint64_t dp = sdesc_add(sdesc_sw128(base + S::OFF_P, 16, 1024), (uint32_t)(2 * x * S::TILE_BYTES));
+                const uint32_t s_tm = tmem + S::TM_S + 128u * (uint32_t)x;
+                const uint32_t o_tm = tmem + S::TM_O + (uint32_t)(D * x);
+                int nv = 0, ns = 0;
                 bool ok = true;
-                auto issue_s = [&](int x, int s) {
-                    const uint32_t d_tmem = tmem + S::TM_S + 128u * (uint32_t)x;
-                    const uint64_t qd = sdesc_add(dq0, (uint32_t)(x * S::TILE_BYTES));
+                auto issue_s = [&](int s) {
                     const uint64_t kd = sdesc_add(dk0, (uint32_t)(s * S::TILE_BYTES));
 #pragma unroll
                     for (int k = 0; k < D / 32; ++k)
-                        mma_ss_f8_elect(d_tmem, sdesc_add(qd, 32u * k), sdesc_add(kd, 32u * k), IDESC_S, k > 0 ? 1u : 0u);
+                        mma_ss_f8_elect(s_tm, sdesc_add(dq, 32u * k), sdesc_add(kd, 32u * k), IDESC_S, k > 0 ? 1u : 0u);
                     mma_commit_elect(bar(S::B_SFULL + x));
-                    ++ns[x];
+                    ++ns;
                 };
                 int kt = next_tile(2, -1);
                 if (kt < p.Tk) {
                     ok = mbar_wait_warp(bar(S::B_QFULL), 0, g, 0x211) && mbar_wait_warp(bar(S::B_KFULL + 0), 0, g, 0x212);
-                    if (ok) {
+                    if (ok && !skip(x, kt)) {
                         tc_fence_after();
-#pragma unroll
-                        for (int x = 0; x < 2; ++x)
-                            if (!skip(x, kt)) issue_s(x, 0);
+                        issue_s(0);
                     }
                 }
                 int u = 0;
                 while (ok && kt < p.Tk) {
                     const int s = u % S::STAGES;
-                    // the next key tile's S_x, as soon as softmax x holds S_x(i)
                     const int kt_next = next_tile(2, kt);
-                    if (kt_next < p.Tk) {
+                    if (kt_next < p.Tk && !skip(x, kt_next)) {
                         const int s2 = (u + 1) % S::STAGES;
-                        if (!mbar_wait_warp(bar(S::B_KFULL + s2), (uint32_t)((u + 1) / S::STAGES) & 1u, g, 0x213)) {
+                        if (!mbar_wait_warp(bar(S::B_KFULL + s2), (uint32_t)((u + 1) / S::STAGES) & 1u, g, 0x213) ||
+                            (ns > 0 && !mbar_wait_warp(bar(S::B_SFREE + x), (uint32_t)(ns - 1) & 1u, g, 0x214))) {
                             ok = false;
                             break;
                         }
-#pragma unroll
-                        for (int x = 0; x < 2 && ok; ++x) {
-                            if (skip(x, kt_next)) continue;
-                            if (ns[x] > 0 && !mbar_wait_warp(bar(S::B_SFREE + x), (uint32_t)(ns[x] - 1) & 1u, g, 0x214)) {
-                                ok = false;
-                                break;
-                            }
-                            tc_fence_after();
-                            issue_s(x, s2);
-                        }
-                        if (!ok) break;
-                    }
-                    // O_x += P_x V for both query tiles
-                    bool vwaited = false;
-#pragma unroll
-                    for (int x = 0; x < 2 && ok; ++x) {
-                        if (skip(x, kt)) continue;
-                        if (!mbar_wait_warp(bar(S::B_PFULL + 2 * x + (nv[x] & 1)), (uint32_t)(nv[x] >> 1) & 1u, g,
-                                       0x215) ||
-                            (!vwaited && !mbar_wait_warp(bar(S::B_VFULL + s), (uint32_t)(u / S::STAGES) & 1u, g, 0x216))) {
-                            ok = false;
-                            break;
-                        }
-                        vwaited = true;
                         tc_fence_after();
-                        const int pb = nv[x] & 1;
-                        const uint64_t pd = sdesc_add(dp0, (uint32_t)((2 * x + pb) * S::TILE_BYTES));
+                        issue_s(s2);
+                    }
+                    if (!skip(x, kt)) {
+                        if (!mbar_wait_warp(bar(S::B_PFULL + 2 * x + (nv & 1)), (uint32_t)(nv >> 1) & 1u, g, 0x215) ||
+                            !mbar_wait_warp(bar(S::B_VFULL + s), (uint32_t)(u / S::STAGES) & 1u, g, 0x216)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const int pb = nv & 1;
+                        const uint64_t pd = sdesc_add(dp, (uint32_t)(pb * S::TILE_BYTES));
                         const uint64_t vd = sdesc_add(dv0, (uint32_t)(s * S::TILE_BYTES));
-                        const uint32_t o_tmem = tmem + S::TM_O + (uint32_t)(D * x);
-                        const uint32_t acc0 = nv[x] > 0 ? 1u : 0u;
+                        const uint32_t acc0 = nv > 0 ? 1u : 0u;
 #pragma unroll
                         for (int k = 0; k < kTile / 32; ++k)
-                            mma_ss_f8_elect(o_tmem, sdesc_add(pd, 32u * k), sdesc_add(vd, 32u * k), IDESC_PV,
-                                      k > 0 ? 1u : acc0);
+                            mma_ss_f8_elect(o_tm, sdesc_add(pd, 32u * k), sdesc_add(vd, 32u * k), IDESC_PV,
+                                            k > 0 ? 1u : acc0);
                         mma_commit_elect(bar(S::B_PFREE + 2 * x + pb));
-                        ++nv[x];
+                        ++nv;
+                        mma_commit_elect(bar(S::B_KVEMPTY + s));
+                    } else {
+                        // no product of this query tile reads the stage: release it, but
+                        // only once the stage holds this use, so that the arrival counts
+                        // towards this use's phase and not an earlier one
+                        if (!mbar_wait_warp(bar(S::B_KFULL + s), (uint32_t)(u / S::STAGES) & 1u, g, 0x217)) {
+                            ok = false;
+                            break;
+                        }
+                        if (lane == 0) mbar_arrive(bar(S::B_KVEMPTY + s));
+                        __syncwarp();
                     }
-                    if (!ok) break;
-                    mma_commit_elect(bar(S::B_KVEMPTY + s));
                     kt = kt_next;
                     ++u;
                 }
-                // O_x is final once every product is done.  The softmax warps run
-                // ahead of the P.V products (P lives in shared memory) and reach
-                // their epilogue before the last ones land: they wait on this
-                // single-use barrier.
-                if (ok) {
-                    mma_commit_elect(bar(S::B_OFULL + 0));
-                    mma_commit_elect(bar(S::B_OFULL + 1));
-                }
-                mma_commit_elect(bar(S::B_FIN));
-                f8_drain_wait(bar(S::B_FIN), 0);
+                if (ok) mma_commit_elect(bar(S::B_OFULL + x));
+                mma_commit_elect(bar(S::B_FIN + x));
+                f8_drain_wait(bar(S::B_FIN + x), 0);
             }
         }
     } else {

@@ -8,9 +8,11 @@ or one more: two more and the wait sleeps through a completed phase; fewer and
 it returns before its phase is done.  Each wait in the model names the phase
 it means, and every poll compares the parity answer with the truth.
 
-The roles follow `fa_fwd_fp8_kernel`: a producer fills a ring of K/V stages; an
-MMA issuer computes, per key tile, the next tile's S_x for both query tiles,
-then O_x += P_x V for both, then releases the stage; two softmax warpgroups
+The roles follow `fa_fwd_fp8_kernel`: a producer fills a ring of K/V stages;
+one MMA issuer per query tile x computes, per key tile, the next tile's S_x,
+then O_x += P_x V, then releases the stage (a stage is free after both
+issuers' releases; an issuer whose query tile skips a key tile releases it
+once the stage holds that tile); two softmax warpgroups
 load S_x, release it, write P_x into one of two shared-memory buffers (after
 the product that last read that buffer), and sometimes rescale O_x (after the
 previous product).  Tensor-core commits and TMA copies complete later, in
@@ -51,44 +53,38 @@ class Barrier:
         return answer
 
 
-def issuer(n_tiles, per_buffer_pfull):
-    """Per key tile u: S of tile u+1 for each query tile that sees it, P.V of
-    tile u, then the stage release.  Query tile x sees tiles 0 .. n_tiles[x]-1."""
+def issuer(x, n_tiles, per_buffer_pfull):
+    """Query tile x's issuer.  It walks the union of the key tiles both query
+    tiles see; query tile x sees tiles 0 .. n_tiles[x]-1."""
     total = max(n_tiles)
-    ns, nv = [0, 0], [0, 0]
+    ns = nv = 0
     yield ("wait", "QFULL", 0, 0)
     yield ("wait", ("KFULL", 0), 0, 0)
-    for x in range(2):
-        if n_tiles[x] > 0:
-            yield ("commit", ("SFULL", x))
-            ns[x] += 1
+    if n_tiles[x] > 0:
+        yield ("commit", ("SFULL", x))
+        ns += 1
     for u in range(total):
         s = u % STAGES
-        if u + 1 < total:
+        if u + 1 < n_tiles[x]:
             k = (u + 1) // STAGES
             yield ("wait", ("KFULL", (u + 1) % STAGES), k & 1, k)
-            for x in range(2):
-                if u + 1 >= n_tiles[x]:
-                    continue
-                yield ("wait", ("SFREE", x), (ns[x] - 1) & 1, ns[x] - 1)
-                yield ("commit", ("SFULL", x))
-                ns[x] += 1
-        vwaited = False
-        for x in range(2):
-            if u >= n_tiles[x]:
-                continue
+            yield ("wait", ("SFREE", x), (ns - 1) & 1, ns - 1)
+            yield ("commit", ("SFULL", x))
+            ns += 1
+        if u < n_tiles[x]:
             if per_buffer_pfull:
-                yield ("wait", ("PFULL", x, nv[x] & 1), (nv[x] >> 1) & 1, nv[x] >> 1)
+                yield ("wait", ("PFULL", x, nv & 1), (nv >> 1) & 1, nv >> 1)
             else:
-                yield ("wait", ("PFULL", x), nv[x] & 1, nv[x])
-            if not vwaited:
-                yield ("wait", ("VFULL", s), (u // STAGES) & 1, u // STAGES)
-                vwaited = True
-            yield ("commit", ("PFREE", x, nv[x] & 1))
-            nv[x] += 1
-        yield ("commit", ("KVEMPTY", s))
-    yield ("commit", ("OFULL", 0))
-    yield ("commit", ("OFULL", 1))
+                yield ("wait", ("PFULL", x), nv & 1, nv)
+            yield ("wait", ("VFULL", s), (u // STAGES) & 1, u // STAGES)
+            yield ("commit", ("PFREE", x, nv & 1))
+            nv += 1
+            yield ("commit", ("KVEMPTY", s))
+        else:
+            yield ("wait", ("KFULL", s), (u // STAGES) & 1, u // STAGES)
+            yield ("arrive", ("KVEMPTY", s))
+    if n_tiles[x] > 0:
+        yield ("commit", ("OFULL", x))
 
 
 def producer(n_tiles):
@@ -123,14 +119,16 @@ def run(seed, n_tiles, per_buffer_pfull, p_rescale=0.3, max_steps=200000):
 
     def bar(name):
         if name not in bars:
-            bars[name] = Barrier()
+            bars[name] = Barrier(2 if name[0] == "KVEMPTY" else 1)   # a stage: both issuers
         return bars[name]
 
-    roles = {"producer": producer(n_tiles), "issuer": issuer(n_tiles, per_buffer_pfull),
+    roles = {"producer": producer(n_tiles), "issuer0": issuer(0, n_tiles, per_buffer_pfull),
+             "issuer1": issuer(1, n_tiles, per_buffer_pfull),
              "softmax0": softmax(0, n_tiles[0], per_buffer_pfull, rng, p_rescale),
              "softmax1": softmax(1, n_tiles[1], per_buffer_pfull, rng, p_rescale)}
     nxt = {r: next(g, None) for r, g in roles.items()}
-    mma, tma = deque(), deque()
+    mma = {"issuer0": deque(), "issuer1": deque()}    # each issuer's commits land in its own order
+    tma = deque()
     # skewed speeds: some roles (and the async engines) run much slower than others
     weight = {r: rng.choice([0.05, 0.3, 1.0, 3.0]) for r in list(roles) + ["mma", "tma"]}
     for _ in range(max_steps):
@@ -146,17 +144,18 @@ def run(seed, n_tiles, per_buffer_pfull, p_rescale=0.3, max_steps=200000):
                     ready.append(r)
             except Alias as e:
                 raise Alias(f"{r} on {op[1]}: {e}") from None
-        if mma:
-            ready.append("mma")
+        for q in mma:
+            if mma[q]:
+                ready.append("mma " + q)
         if tma:
             ready.append("tma")
         if not ready:
             if all(op is None for op in nxt.values()):
                 return
             raise Deadlock({r: op for r, op in nxt.items() if op is not None})
-        r = rng.choices(ready, weights=[weight[q] for q in ready])[0]
-        if r == "mma":
-            bar(mma.popleft()).arrive()
+        r = rng.choices(ready, weights=[weight[q.split()[0]] for q in ready])[0]
+        if r.startswith("mma"):
+            bar(mma[r.split()[1]].popleft()).arrive()
         elif r == "tma":
             bar(tma.popleft()).arrive()
         else:
@@ -164,7 +163,7 @@ def run(seed, n_tiles, per_buffer_pfull, p_rescale=0.3, max_steps=200000):
             if op[0] == "arrive":
                 bar(op[1]).arrive()
             elif op[0] == "commit":
-                mma.append(op[1])
+                mma[r].append(op[1])
             elif op[0] == "tma":
                 tma.append(op[1])
             nxt[r] = next(roles[r], None)
@@ -187,8 +186,8 @@ def test_model_finds_the_alias_of_one_pready_barrier_per_query_tile():
         except Alias as e:
             found.append(str(e))
     assert len(found) > 50
-    # always the issuer, on a P-ready barrier that has run two phases ahead
-    assert all(f.startswith("issuer on ('PFULL'") for f in found), found[:3]
+    # always an issuer, on a P-ready barrier that has run two phases ahead
+    assert all(f.startswith("issuer") and " on ('PFULL'" in f for f in found), found[:3]
     assert all("with" in f and int(f.split("with ")[1].split()[0]) == int(f.split("phase ")[1].split()[0]) + 2
                for f in found)
 
