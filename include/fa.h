@@ -258,9 +258,17 @@ fa_status fa_tile_plan(int B, int N, int causal, const int32_t *key_len,
  * block_mask, when given, are HOST arrays too.  The call copies the inputs
  * into dev_workspace, runs fa_fwd (and fa_bwd), copies the outputs back and
  * synchronises the stream before returning.  Pinned host memory makes the
- * copies asynchronous; the call then spreads them over `stream` and a
- * private side stream, ordered by events, so that both copy directions run
- * in parallel and dO's upload and the O/LSE download overlap the kernels.
+ * copies asynchronous.  Large problems (at least 2^23 elements per tensor,
+ * N a multiple of 4, B*H >= 2) run in up to 8 chunks of whole batches or of
+ * a head range of one batch: each chunk's kernels start once its own inputs
+ * are on the device, on a compute stream of their own so that chunks share
+ * the SMs, and its outputs are copied back while later chunks compute.
+ * Uploads and downloads each have a stream; these streams belong to the
+ * library (one set per device, made on first use) and are ordered after the
+ * work already queued on `stream`, which in turn waits for all of them.
+ * Calls from several host threads enqueue one after the other.  Results are
+ * bit-identical to fa_fwd / fa_bwd on device buffers except dQ (summed by
+ * reduce-adds in a varying order).
  * dev_workspace: device memory of at least fa_host_workspace_size() bytes,
  * zero-filled once before first use.
  */

@@ -579,16 +579,69 @@ fa_status fa_reset_device_status(void *workspace, void *stream) {
 
 // ------------------------------------------------------------------ host-buffer path
 namespace {
+// The host path runs in chunks of (b, h) pairs, so that a chunk's kernels
+// start as soon as its own inputs are on the device and its outputs go back
+// while later chunks still compute: only the first chunk's upload and the
+// last chunk's download stay exposed.  A chunk is either whole batches
+// (b0 .. b0+nb-1, every head) or a head range of one batch, so that key_len
+// applies to it through an offset pointer; its rows are contiguous in every
+// [B,H,N,...] array.
+constexpr int kMaxHostChunks = 8;
+constexpr int kHostChunkTarget = 4;
+// below this many elements per bf16 tensor one launch is cheaper than four
+constexpr size_t kHostChunkMinElems = (size_t)1 << 23;
+
+struct HostChunk {
+    int b0, nb, h0, nh;
+    size_t row0;        // first (b, h, n) row: (b0 * H + h0) * N
+    size_t ws_off;      // this chunk's kernel workspace inside the attention region
+};
+
 struct HostLayout {
     size_t attn_ws, q, k, v, o, dO, dQ, dK, dV, lse, klen, bmask, total;
+    int nchunks;
+    HostChunk chunk[kMaxHostChunks];
 };
+
+int host_chunks(int B, int H, int N, int d, HostChunk *c) {
+    const size_t elems = (size_t)B * H * N * d;
+    // LSE rows are fp32 and the kernels want 16-byte aligned bases: N % 4 == 0
+    // keeps every chunk boundary aligned
+    if (elems < kHostChunkMinElems || N % 4 != 0 || (size_t)B * H < 2) {
+        c[0] = {0, B, 0, H, 0, 0};
+        return 1;
+    }
+    int n = 0;
+    if (B >= kHostChunkTarget) {
+        for (int i = 0; i < kHostChunkTarget; ++i) {
+            const int b0 = (int)((long long)B * i / kHostChunkTarget);
+            const int b1 = (int)((long long)B * (i + 1) / kHostChunkTarget);
+            c[n++] = {b0, b1 - b0, 0, H, 0, 0};
+        }
+    } else {
+        const int g = std::min(H, (kHostChunkTarget + B - 1) / B);
+        for (int b = 0; b < B; ++b)
+            for (int i = 0; i < g; ++i) {
+                const int h0 = (int)((long long)H * i / g), h1 = (int)((long long)H * (i + 1) / g);
+                c[n++] = {b, 1, h0, h1 - h0, 0, 0};
+            }
+    }
+    for (int i = 0; i < n; ++i) c[i].row0 = ((size_t)c[i].b0 * H + c[i].h0) * N;
+    return n;
+}
+
 HostLayout host_layout(int B, int H, int N, int d, int with_bwd) {
     HostLayout L;
     const size_t rows = (size_t)B * H * N, t = round256(rows * (size_t)d * 2);
     const size_t nb = ((size_t)N + 127) / 128;
+    L.nchunks = host_chunks(B, H, N, d, L.chunk);
     size_t off = 0;
     L.attn_ws = off;
-    off += round256(with_bwd ? fa_bwd_workspace_size(B, H, N, d) : fa_fwd_workspace_size(B, H, N, d));
+    for (int i = 0; i < L.nchunks; ++i) {
+        const HostChunk &c = L.chunk[i];
+        L.chunk[i].ws_off = off;
+        off += round256(with_bwd ? fa_bwd_workspace_size(c.nb, c.nh, N, d) : fa_fwd_workspace_size(c.nb, c.nh, N, d));
+    }
     L.q = off; off += t;
     L.k = off; off += t;
     L.v = off; off += t;
@@ -611,24 +664,36 @@ size_t fa_host_workspace_size(int B, int H, int N, int d, int with_backward) {
 }
 
 namespace {
-// A non-blocking side stream and the events that order it against the
-// caller's stream for one fa_attention_host call.  Destroying them right
-// away is safe: CUDA releases a stream or event whose work is still queued
-// once that work completes.
-struct HostSide {
-    cudaStream_t s = nullptr;
-    cudaEvent_t ev[6] = {};
+// Streams and events of the host path, made once per device and kept for
+// the process: an upload stream, a download stream and one compute stream
+// per chunk (so that the chunks' kernels can share the SMs).  A call holds
+// the device's mutex while it enqueues, so concurrent calls from several
+// host threads order their work on these streams one after the other.
+struct HostStreams {
     bool ok = false;
-    HostSide() {
-        ok = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) == cudaSuccess;
-        for (auto &e : ev) ok = ok && cudaEventCreateWithFlags(&e, cudaEventDisableTiming) == cudaSuccess;
-    }
-    ~HostSide() {
-        for (auto &e : ev)
-            if (e) cudaEventDestroy(e);
-        if (s) cudaStreamDestroy(s);
+    cudaStream_t up = nullptr, down = nullptr, comp[kMaxHostChunks] = {};
+    cudaEvent_t start = nullptr, down_done = nullptr, in[kMaxHostChunks] = {}, dO_in[kMaxHostChunks] = {},
+                fwd_done[kMaxHostChunks] = {}, bwd_done[kMaxHostChunks] = {};
+    std::mutex mu;
+    bool init() {
+        auto mk_s = [](cudaStream_t *s) { return cudaStreamCreateWithFlags(s, cudaStreamNonBlocking) == cudaSuccess; };
+        auto mk_e = [](cudaEvent_t *e) { return cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess; };
+        bool good = mk_s(&up) && mk_s(&down) && mk_e(&start) && mk_e(&down_done);
+        for (int i = 0; good && i < kMaxHostChunks; ++i)
+            good = mk_s(&comp[i]) && mk_e(&in[i]) && mk_e(&dO_in[i]) && mk_e(&fwd_done[i]) && mk_e(&bwd_done[i]);
+        return good;
     }
 };
+
+HostStreams *host_streams() {
+    constexpr int kMaxDevices = 64;
+    static HostStreams pool[kMaxDevices];
+    static std::once_flag once[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::call_once(once[dev], [dev] { pool[dev].ok = pool[dev].init(); });
+    return pool[dev].ok ? &pool[dev] : nullptr;
+}
 }  // namespace
 
 fa_status fa_attention_host(const void *Q, const void *K, const void *V, const void *dO, void *O, float *LSE,
@@ -646,50 +711,83 @@ fa_status fa_attention_host(const void *Q, const void *K, const void *V, const v
     if (!dev_workspace || !aligned16(dev_workspace) || dev_workspace_bytes < L.total) return FA_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t *w = static_cast<uint8_t *>(dev_workspace);
-    const size_t bytes = (size_t)B * H * N * d * 2, lbytes = (size_t)B * H * N * 4;
     const size_t nb = ((size_t)N + 127) / 128;
-    // Copies go to two streams, so that both copy directions and the kernels
-    // overlap: V and dO upload on a side stream (dO while the forward runs),
-    // O and LSE download there while the backward runs, dQ in parallel with
-    // dK and dV.  The side stream starts after the work already on `stream`
-    // and `stream` waits for it at the end, so the call is one unit on it.
-    HostSide side;
-    if (!side.ok || cudaEventRecord(side.ev[0], s) != cudaSuccess ||
-        cudaStreamWaitEvent(side.s, side.ev[0], 0) != cudaSuccess)
-        return FA_ERR_CUDA;
-    auto h2d = [&](size_t off, const void *src, size_t n, cudaStream_t on) {
-        return cudaMemcpyAsync(w + off, src, n, cudaMemcpyHostToDevice, on) == cudaSuccess;
-    };
-    auto d2h = [&](void *dst, size_t off, size_t n, cudaStream_t on) {
-        return cudaMemcpyAsync(dst, w + off, n, cudaMemcpyDeviceToHost, on) == cudaSuccess;
-    };
-    auto handoff = [&](cudaEvent_t e, cudaStream_t from, cudaStream_t to) {
-        return cudaEventRecord(e, from) == cudaSuccess && cudaStreamWaitEvent(to, e, 0) == cudaSuccess;
-    };
-    if (!h2d(L.q, Q, bytes, s) || !h2d(L.k, K, bytes, s) || !h2d(L.v, V, bytes, side.s)) return FA_ERR_CUDA;
-    if (key_len && !h2d(L.klen, key_len, (size_t)B * 4, s)) return FA_ERR_CUDA;
-    if (block_mask && !h2d(L.bmask, block_mask, nb * nb, s)) return FA_ERR_CUDA;
-    if (!handoff(side.ev[1], side.s, s)) return FA_ERR_CUDA;                 // V is in
-    if (bwd && !h2d(L.dO, dO, bytes, side.s)) return FA_ERR_CUDA;
-    const int32_t *kl = key_len ? reinterpret_cast<const int32_t *>(w + L.klen) : nullptr;
-    const uint8_t *bm = block_mask ? w + L.bmask : nullptr;
-    const size_t ws_bytes = bwd ? fa_bwd_workspace_size(B, H, N, d) : fa_fwd_workspace_size(B, H, N, d);
-    st = fa_fwd(w + L.q, w + L.k, w + L.v, w + L.o, reinterpret_cast<float *>(w + L.lse), B, H, N, d, softmax_scale,
-                causal, kl, bm, w + L.attn_ws, ws_bytes, stream);
-    if (st != FA_OK) return st;
-    if (!handoff(side.ev[2], s, side.s)) return FA_ERR_CUDA;                 // O, LSE are final
-    if (!d2h(O, L.o, bytes, side.s) || !d2h(LSE, L.lse, lbytes, side.s)) return FA_ERR_CUDA;
-    if (bwd) {
-        if (!handoff(side.ev[3], side.s, s)) return FA_ERR_CUDA;             // dO is in
-        st = fa_bwd(w + L.q, w + L.k, w + L.v, w + L.o, reinterpret_cast<float *>(w + L.lse), w + L.dO, w + L.dQ,
-                    w + L.dK, w + L.dV, B, H, N, d, softmax_scale, causal, kl, bm, w + L.attn_ws, ws_bytes, stream);
-        if (st != FA_OK) return st;
-        if (!handoff(side.ev[4], s, side.s)) return FA_ERR_CUDA;             // gradients are final
-        if (!d2h(dQ, L.dQ, bytes, side.s) || !d2h(dK, L.dK, bytes, s) || !d2h(dV, L.dV, bytes, s))
+    HostStreams *hs = host_streams();
+    if (!hs) return FA_ERR_CUDA;
+    {
+        std::lock_guard<std::mutex> lock(hs->mu);
+        auto after = [](cudaEvent_t e, cudaStream_t from, cudaStream_t to) {
+            return cudaEventRecord(e, from) == cudaSuccess && cudaStreamWaitEvent(to, e, 0) == cudaSuccess;
+        };
+        auto h2d = [&](size_t off, const void *src, size_t n) {
+            return cudaMemcpyAsync(w + off, src, n, cudaMemcpyHostToDevice, hs->up) == cudaSuccess;
+        };
+        auto d2h = [&](void *dst, size_t off, size_t n) {
+            return cudaMemcpyAsync(dst, w + off, n, cudaMemcpyDeviceToHost, hs->down) == cudaSuccess;
+        };
+        // everything starts after the work already on `stream`
+        if (cudaEventRecord(hs->start, s) != cudaSuccess || cudaStreamWaitEvent(hs->up, hs->start, 0) != cudaSuccess ||
+            cudaStreamWaitEvent(hs->down, hs->start, 0) != cudaSuccess)
             return FA_ERR_CUDA;
+        for (int i = 0; i < L.nchunks; ++i)
+            if (cudaStreamWaitEvent(hs->comp[i], hs->start, 0) != cudaSuccess) return FA_ERR_CUDA;
+        // uploads: masks, then each chunk's Q, K, V, then each chunk's dO
+        if (key_len && !h2d(L.klen, key_len, (size_t)B * 4)) return FA_ERR_CUDA;
+        if (block_mask && !h2d(L.bmask, block_mask, nb * nb)) return FA_ERR_CUDA;
+        const size_t row_bytes = (size_t)d * 2;
+        auto cbytes = [&](const HostChunk &c) { return (size_t)c.nb * c.nh * N * row_bytes; };
+        auto at = [](const void *p, size_t off) { return static_cast<const uint8_t *>(p) + off; };
+        for (int i = 0; i < L.nchunks; ++i) {
+            const HostChunk &c = L.chunk[i];
+            const size_t o = c.row0 * row_bytes, n = cbytes(c);
+            if (!h2d(L.q + o, at(Q, o), n) || !h2d(L.k + o, at(K, o), n) || !h2d(L.v + o, at(V, o), n) ||
+                !after(hs->in[i], hs->up, hs->comp[i]))
+                return FA_ERR_CUDA;
+        }
+        if (bwd)
+            for (int i = 0; i < L.nchunks; ++i) {
+                const HostChunk &c = L.chunk[i];
+                const size_t o = c.row0 * row_bytes;
+                if (!h2d(L.dO + o, at(dO, o), cbytes(c)) || !after(hs->dO_in[i], hs->up, hs->comp[i]))
+                    return FA_ERR_CUDA;
+            }
+        // kernels: chunk i on compute stream i
+        for (int i = 0; i < L.nchunks; ++i) {
+            const HostChunk &c = L.chunk[i];
+            const size_t o = c.row0 * row_bytes;
+            const int32_t *kl = key_len ? reinterpret_cast<const int32_t *>(w + L.klen) + c.b0 : nullptr;
+            const uint8_t *bm = block_mask ? w + L.bmask : nullptr;
+            float *lse = reinterpret_cast<float *>(w + L.lse) + c.row0;
+            uint8_t *ws = w + L.attn_ws + c.ws_off;
+            const size_t ws_bytes = bwd ? fa_bwd_workspace_size(c.nb, c.nh, N, d) : fa_fwd_workspace_size(c.nb, c.nh, N, d);
+            st = fa_fwd(w + L.q + o, w + L.k + o, w + L.v + o, w + L.o + o, lse, c.nb, c.nh, N, d, softmax_scale, causal,
+                        kl, bm, ws, ws_bytes, hs->comp[i]);
+            if (st != FA_OK) return st;
+            if (!after(hs->fwd_done[i], hs->comp[i], hs->down)) return FA_ERR_CUDA;
+            if (!d2h(static_cast<uint8_t *>(O) + o, L.o + o, cbytes(c)) ||
+                !d2h(LSE + c.row0, L.lse + c.row0 * 4, (size_t)c.nb * c.nh * N * 4))
+                return FA_ERR_CUDA;
+            if (bwd) {
+                st = fa_bwd(w + L.q + o, w + L.k + o, w + L.v + o, w + L.o + o, lse, w + L.dO + o, w + L.dQ + o,
+                            w + L.dK + o, w + L.dV + o, c.nb, c.nh, N, d, softmax_scale, causal, kl, bm, ws, ws_bytes,
+                            hs->comp[i]);
+                if (st != FA_OK) return st;
+                if (!after(hs->bwd_done[i], hs->comp[i], hs->down)) return FA_ERR_CUDA;
+                if (!d2h(static_cast<uint8_t *>(dQ) + o, L.dQ + o, cbytes(c)) ||
+                    !d2h(static_cast<uint8_t *>(dK) + o, L.dK + o, cbytes(c)) ||
+                    !d2h(static_cast<uint8_t *>(dV) + o, L.dV + o, cbytes(c)))
+                    return FA_ERR_CUDA;
+            }
+        }
+        // the download stream has waited for every chunk's kernels, which waited
+        // for every upload: `stream` resumes after the last download
+        if (!after(hs->down_done, hs->down, s)) return FA_ERR_CUDA;
     }
-    if (!handoff(side.ev[5], side.s, s)) return FA_ERR_CUDA;
-    return fa_get_device_status(w + L.attn_ws, stream);
+    for (int i = 0; i < L.nchunks; ++i) {
+        st = fa_get_device_status(w + L.attn_ws + L.chunk[i].ws_off, stream);
+        if (st != FA_OK) return st;
+    }
+    return FA_OK;
 }
 
 }  // extern "C"

@@ -117,14 +117,44 @@ def test_host_buffer_path_matches_device_path():
     assert rel_fro(dQ.double().numpy(), dev["dQ"]) < 1e-3
 
 
-def test_host_buffer_path_orders_its_side_stream():
-    """fa_attention_host spreads its copies over the caller's stream and a side
-    stream.  Work already queued on the caller's stream must finish first: here
-    it zeroes the whole device workspace (slowly, many times), which would
-    wipe the uploaded inputs if a side-stream copy ran ahead of it.  Repeated
-    calls on a non-default stream give the device path's bits each time."""
+def test_host_buffer_path_chunks_head_ranges_with_key_len():
+    """Large enough to run in chunks; with B = 2 each chunk is a head range of
+    one batch, whose key_len the kernels see through an offset pointer.  The
+    forward and dK, dV are per-head deterministic, so the chunked host path
+    gives the device path's bits; the forward-only call too."""
     import io_aware_exact_09_gb300 as fa
-    B, H, N, d = 1, 4, 2048, 128
+    B, H, N, d = 2, 8, 4096, 128
+    case = make_case(B, H, N, d, seed=37, causal=True, key_len=[4096, 2500])
+    pin = lambda t: t.contiguous().pin_memory()
+    Qh, Kh, Vh, dOh = (pin(case[k]) for k in ("Q", "K", "V", "dO"))
+    kl = case["key_len"].contiguous()
+    dev = run_cuda(case)
+    for with_bwd in (1, 0):
+        O = torch.empty_like(Qh).pin_memory()
+        LSE = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+        dQ, dK, dV = (torch.empty_like(Qh).pin_memory() for _ in range(3))
+        ws = fa.workspace(fa.fa_host_workspace_size(B, H, N, d, with_bwd), "cuda")
+        st = fa.fa_attention_host(Qh, Kh, Vh, dOh if with_bwd else None, O, LSE, dQ if with_bwd else None,
+                                  dK if with_bwd else None, dV if with_bwd else None, B, H, N, d, case["scale"],
+                                  True, kl, None, ws, ws.numel())
+        assert st == 0, fa.fa_status_string(st)
+        assert np.array_equal(O.double().numpy(), dev["O"])
+        assert np.array_equal(LSE.double().numpy(), dev["LSE"])
+        if with_bwd:
+            assert np.array_equal(dK.double().numpy(), dev["dK"])
+            assert np.array_equal(dV.double().numpy(), dev["dV"])
+            assert rel_fro(dQ.double().numpy(), dev["dQ"]) < 1e-3
+
+
+def test_host_buffer_path_orders_its_streams():
+    """fa_attention_host runs on its own upload, download and per-chunk compute
+    streams.  Work already queued on the caller's stream must finish first:
+    here it zeroes the whole device workspace (slowly, many times), which
+    would wipe the uploaded inputs if a copy ran ahead of it.  Repeated calls
+    on a non-default stream give the device path's bits each time (the shape
+    runs in four chunks)."""
+    import io_aware_exact_09_gb300 as fa
+    B, H, N, d = 1, 16, 4096, 128
     case = make_case(B, H, N, d, seed=31)
     pin = lambda t: t.contiguous().pin_memory()
     Qh, Kh, Vh, dOh = (pin(case[k]) for k in ("Q", "K", "V", "dO"))
