@@ -258,7 +258,7 @@ fa_status fa_tile_plan(int B, int N, int causal, const int32_t *key_len,
  * block_mask, when given, are HOST arrays too.  The call copies the inputs
  * into dev_workspace, runs fa_fwd (and fa_bwd), copies the outputs back and
  * synchronises the stream before returning.  Pinned host memory makes the
- * copies asynchronous.  Large problems (at least 2^23 elements per tensor,
+ * copies asynchronous.  Large problems (at least 2^24 elements per tensor,
  * N a multiple of 4, B*H >= 2) run in up to 8 chunks of whole batches or of
  * a head range of one batch: each chunk's kernels start once its own inputs
  * are on the device, on a compute stream of their own so that chunks share

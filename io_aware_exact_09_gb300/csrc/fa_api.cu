@@ -588,8 +588,12 @@ namespace {
 // [B,H,N,...] array.
 constexpr int kMaxHostChunks = 8;
 constexpr int kHostChunkTarget = 4;
-// below this many elements per bf16 tensor one launch is cheaper than four
-constexpr size_t kHostChunkMinElems = (size_t)1 << 23;
+// Below this many elements per bf16 tensor the step is bound by the copies
+// (host <-> device runs at ~200 GB/s per direction; a 2^23-element problem
+// moves ~150 MB for ~0.2 ms of kernels) and one chunk is as fast; four
+// chunks measured better than eight on the long-context shape (more
+// launches, smaller grids).
+constexpr size_t kHostChunkMinElems = (size_t)1 << 24;
 
 struct HostChunk {
     int b0, nb, h0, nh;

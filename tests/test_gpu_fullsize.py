@@ -117,14 +117,16 @@ def test_host_buffer_path_matches_device_path():
     assert rel_fro(dQ.double().numpy(), dev["dQ"]) < 1e-3
 
 
-def test_host_buffer_path_chunks_head_ranges_with_key_len():
-    """Large enough to run in chunks; with B = 2 each chunk is a head range of
-    one batch, whose key_len the kernels see through an offset pointer.  The
-    forward and dK, dV are per-head deterministic, so the chunked host path
-    gives the device path's bits; the forward-only call too."""
+@pytest.mark.parametrize("B,H,N,d,key_len", [(2, 8, 8192, 128, [8192, 2500]),
+                                              (4, 8, 8192, 64, [8192, 300, 5000, 8191])])
+def test_host_buffer_path_in_chunks_with_key_len(B, H, N, d, key_len):
+    """Large enough to run in chunks: with B = 2 each chunk is a head range of
+    one batch, with B = 4 one whole batch; either way the kernels see the
+    chunk's key_len through an offset pointer.  The forward and dK, dV are
+    per-head deterministic, so the chunked host path gives the device path's
+    bits; the forward-only call too."""
     import io_aware_exact_09_gb300 as fa
-    B, H, N, d = 2, 8, 4096, 128
-    case = make_case(B, H, N, d, seed=37, causal=True, key_len=[4096, 2500])
+    case = make_case(B, H, N, d, seed=37, causal=True, key_len=key_len)
     pin = lambda t: t.contiguous().pin_memory()
     Qh, Kh, Vh, dOh = (pin(case[k]) for k in ("Q", "K", "V", "dO"))
     kl = case["key_len"].contiguous()
@@ -154,7 +156,7 @@ def test_host_buffer_path_orders_its_streams():
     on a non-default stream give the device path's bits each time (the shape
     runs in four chunks)."""
     import io_aware_exact_09_gb300 as fa
-    B, H, N, d = 1, 16, 4096, 128
+    B, H, N, d = 1, 16, 8192, 128
     case = make_case(B, H, N, d, seed=31)
     pin = lambda t: t.contiguous().pin_memory()
     Qh, Kh, Vh, dOh = (pin(case[k]) for k in ("Q", "K", "V", "dO"))
