@@ -1,5 +1,6 @@
-"""A model of the FP8 forward kernel's roles and mbarriers, run under random
-schedules, that checks the one rule a parity wait depends on.
+"""Models of the FP8 forward and the d = 128 backward kernels' roles and
+mbarriers, run under random schedules, that check the one rule a parity wait
+depends on.
 
 `mbarrier.try_wait.parity(P)` answers "has the phase of parity P completed?"
 by comparing P with the parity of the phase in progress.  The answer is right
@@ -20,7 +21,11 @@ order, at random times.  The softmax keeps P in shared memory, so it can run a
 tile ahead of the products: the old layout, one P-ready barrier per query
 tile, then lets that barrier get two phases ahead of the issuer.  The test
 checks that the model finds exactly that, and nothing with one P-ready
-barrier per P buffer."""
+barrier per P buffer.
+
+The models check barrier phases only: a wait that guards data rather than a
+phase (the backward producer's wait before it restages LSE and D, say) shows
+up here only if dropping it lets a barrier run two phases ahead."""
 import random
 from collections import deque
 
@@ -113,23 +118,21 @@ def softmax(x, n, per_buffer_pfull, rng, p_rescale):
         yield ("wait", ("OFULL", x), 0, 0)
 
 
-def run(seed, n_tiles, per_buffer_pfull, p_rescale=0.3, max_steps=200000):
-    rng = random.Random(seed)
+def schedule(rng, roles, count, max_steps=400000):
+    """Run the roles (generators of operations) under a random schedule with
+    skewed role speeds.  Commits of one role complete in their issue order;
+    bulk copies complete in any order.  `count(name)` is a barrier's arrival
+    count per phase."""
     bars = {}
 
     def bar(name):
         if name not in bars:
-            bars[name] = Barrier(2 if name[0] == "KVEMPTY" else 1)   # a stage: both issuers
+            bars[name] = Barrier(count(name))
         return bars[name]
 
-    roles = {"producer": producer(n_tiles), "issuer0": issuer(0, n_tiles, per_buffer_pfull),
-             "issuer1": issuer(1, n_tiles, per_buffer_pfull),
-             "softmax0": softmax(0, n_tiles[0], per_buffer_pfull, rng, p_rescale),
-             "softmax1": softmax(1, n_tiles[1], per_buffer_pfull, rng, p_rescale)}
     nxt = {r: next(g, None) for r, g in roles.items()}
-    mma = {"issuer0": deque(), "issuer1": deque()}    # each issuer's commits land in its own order
-    tma = deque()
-    # skewed speeds: some roles (and the async engines) run much slower than others
+    mma = {r: deque() for r in roles}
+    tma = []
     weight = {r: rng.choice([0.05, 0.3, 1.0, 3.0]) for r in list(roles) + ["mma", "tma"]}
     for _ in range(max_steps):
         ready = []
@@ -144,9 +147,7 @@ def run(seed, n_tiles, per_buffer_pfull, p_rescale=0.3, max_steps=200000):
                     ready.append(r)
             except Alias as e:
                 raise Alias(f"{r} on {op[1]}: {e}") from None
-        for q in mma:
-            if mma[q]:
-                ready.append("mma " + q)
+        ready += ["mma " + q for q in mma if mma[q]]
         if tma:
             ready.append("tma")
         if not ready:
@@ -157,7 +158,7 @@ def run(seed, n_tiles, per_buffer_pfull, p_rescale=0.3, max_steps=200000):
         if r.startswith("mma"):
             bar(mma[r.split()[1]].popleft()).arrive()
         elif r == "tma":
-            bar(tma.popleft()).arrive()
+            bar(tma.pop(rng.randrange(len(tma)))).arrive()
         else:
             op = nxt[r]
             if op[0] == "arrive":
@@ -168,6 +169,85 @@ def run(seed, n_tiles, per_buffer_pfull, p_rescale=0.3, max_steps=200000):
                 tma.append(op[1])
             nxt[r] = next(roles[r], None)
     raise AssertionError("model did not finish")
+
+
+def run(seed, n_tiles, per_buffer_pfull, p_rescale=0.3):
+    rng = random.Random(seed)
+    roles = {"producer": producer(n_tiles), "issuer0": issuer(0, n_tiles, per_buffer_pfull),
+             "issuer1": issuer(1, n_tiles, per_buffer_pfull),
+             "softmax0": softmax(0, n_tiles[0], per_buffer_pfull, rng, p_rescale),
+             "softmax1": softmax(1, n_tiles[1], per_buffer_pfull, rng, p_rescale)}
+    schedule(rng, roles, lambda name: 2 if name[0] == "KVEMPTY" else 1)   # a stage: both issuers
+
+
+# ---------------------------------------------------------------- d = 128 backward
+# The roles of `fa_bwd128_kernel` for one key tile and n query blocks: a
+# producer (K, V once; per block Q into one of two stages, dO into one slot,
+# LSE and D staged in shared memory), the MMA issuer (per block dV, dQ^T, dK,
+# then the next block's S^T and dP^T), the compute warpgroups (P^T, dS^T)
+# and the dQ drain warpgroup.  The phase each wait means is the block index
+# (or half of it for the two Q stages).
+
+def bwd_producer(n):
+    yield ("tma", "KV")
+    for i in range(n):
+        s = i & 1
+        yield ("wait", ("QEMPTY", s), ((i >> 1) & 1) ^ 1, (i >> 1) - 1)     # dK(i-2) read Q stage s
+        yield ("wait", "DVDONE", (i & 1) ^ 1, i - 1)                        # dV(i-1) read dO
+        yield ("tma", ("QFULL", s))
+        yield ("tma", "DOFULL")
+        yield ("wait", "LSEFREE", (i & 1) ^ 1, i - 1)                       # block i-1's LSE, D consumed
+        yield ("arrive", "LSE")
+
+
+def bwd_issuer(n):
+    if n:
+        yield ("wait", "KV", 0, 0)
+        yield ("wait", ("QFULL", 0), 0, 0)
+        yield ("wait", "DOFULL", 0, 0)
+        yield ("commit", "SFULL")
+        yield ("commit", "DPFULL")
+    for i in range(n):
+        s = i & 1
+        yield ("wait", "PFULL", i & 1, i)
+        yield ("commit", "DVDONE")                                          # dV(i)
+        yield ("wait", "DSFULL", i & 1, i)
+        yield ("wait", "DVDONE", i & 1, i)
+        yield ("commit", "DQFULL")                                          # dQ^T(i)
+        yield ("commit", ("QEMPTY", s))                                     # dK(i)
+        if i + 1 < n:
+            yield ("wait", ("QFULL", s ^ 1), ((i + 1) >> 1) & 1, (i + 1) >> 1)
+            yield ("wait", ("QEMPTY", s), (i >> 1) & 1, i >> 1)
+            yield ("commit", "SFULL")                                       # S^T(i+1)
+            yield ("wait", "DOFULL", (i + 1) & 1, i + 1)
+            yield ("wait", "DQFREE", i & 1, i)
+            yield ("commit", "DPFULL")                                      # dP^T(i+1)
+    if n:
+        yield ("commit", "ACC")
+
+
+def bwd_compute(n):
+    for i in range(n):
+        yield ("wait", "LSE", i & 1, i)
+        yield ("wait", "SFULL", i & 1, i)
+        yield ("arrive", "PFULL")
+        yield ("wait", "DPFULL", i & 1, i)
+        yield ("arrive", "DSFULL")
+        yield ("arrive", "LSEFREE")
+    if n:
+        yield ("wait", "ACC", 0, 0)
+
+
+def bwd_drain(n):
+    for i in range(n):
+        yield ("wait", "DQFULL", i & 1, i)
+        yield ("arrive", "DQFREE")
+
+
+def run_bwd128(seed, n):
+    rng = random.Random(seed)
+    roles = {"producer": bwd_producer(n), "issuer": bwd_issuer(n), "compute": bwd_compute(n), "drain": bwd_drain(n)}
+    schedule(rng, roles, lambda name: 1)
 
 
 TILE_COUNTS = [(1, 1), (2, 2), (3, 3), (7, 7), (12, 12), (3, 5), (5, 6), (0, 4), (8, 1)]
@@ -190,6 +270,28 @@ def test_model_finds_the_alias_of_one_pready_barrier_per_query_tile():
     assert all(f.startswith("issuer") and " on ('PFULL'" in f for f in found), found[:3]
     assert all("with" in f and int(f.split("with ")[1].split()[0]) == int(f.split("phase ")[1].split()[0]) + 2
                for f in found)
+
+
+def test_bwd128_protocol_never_aliases():
+    for i in range(600):
+        run_bwd128(seed=i, n=(1, 2, 3, 4, 5, 9, 16)[i % 7])
+
+
+def test_bwd128_model_finds_a_dropped_drain_wait():
+    """Without its wait for the dQ drain, the issuer can complete the next
+    block's dQ^T while the drain still waits for the previous one."""
+    def issuer_without_dqfree_wait(n):
+        return (op for op in bwd_issuer(n) if not (op[0] == "wait" and op[1] == "DQFREE"))
+    found = []
+    for i in range(300):
+        n = (2, 5, 9, 16)[i % 4]
+        roles = {"producer": bwd_producer(n), "issuer": issuer_without_dqfree_wait(n), "compute": bwd_compute(n),
+                 "drain": bwd_drain(n)}
+        try:
+            schedule(random.Random(i), roles, lambda name: 1)
+        except Alias as e:
+            found.append(str(e))
+    assert found and all(f.startswith("drain on DQFULL") for f in found), found[:3]
 
 
 def test_model_checker_catches_a_waiter_that_runs_ahead():
