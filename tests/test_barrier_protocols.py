@@ -1,6 +1,6 @@
-"""Models of the FP8 forward and the d = 128 backward kernels' roles and
-mbarriers, run under random schedules, that check the one rule a parity wait
-depends on.
+"""Models of the forward (bf16 and FP8), split-KV decode and d = 128
+backward kernels' roles and mbarriers, run under random schedules, that check
+the one rule a parity wait depends on.
 
 `mbarrier.try_wait.parity(P)` answers "has the phase of parity P completed?"
 by comparing P with the parity of the phase in progress.  The answer is right
@@ -250,6 +250,125 @@ def run_bwd128(seed, n):
     schedule(rng, roles, lambda name: 1)
 
 
+# ---------------------------------------------------------------- bf16 forward
+# `fa_fwd_kernel`: P overwrites S in TMEM, so one issuer alternates the query
+# tiles: per key tile and query tile x, O_x += P_x V once P_x is written, then
+# the next tile's S_x once that product has read P_x.
+
+def fwd_producer(n_tiles, stages):
+    total = max(n_tiles)
+    if total:
+        yield ("tma", "QFULL")
+    for u in range(total):
+        s, k = u % stages, u // stages
+        yield ("wait", ("KVEMPTY", s), (k & 1) ^ 1, k - 1)
+        yield ("tma", ("KFULL", s))
+        yield ("tma", ("VFULL", s))
+
+
+def fwd_issuer(n_tiles, stages):
+    total = max(n_tiles)
+    nv = [0, 0]
+    if not total:
+        return
+    yield ("wait", "QFULL", 0, 0)
+    yield ("wait", ("KFULL", 0), 0, 0)
+    for x in range(2):
+        if n_tiles[x] > 0:
+            yield ("commit", ("SFULL", x))
+    for u in range(total):
+        s, s2 = u % stages, (u + 1) % stages
+        vwaited = kwaited = False
+        for x in range(2):
+            if u < n_tiles[x]:
+                yield ("wait", ("PFULL", x), nv[x] & 1, nv[x])
+                if not vwaited:
+                    yield ("wait", ("VFULL", s), (u // stages) & 1, u // stages)
+                    vwaited = True
+                yield ("commit", ("PVDONE", x))
+                nv[x] += 1
+            if u + 1 < n_tiles[x]:
+                if not kwaited:
+                    k = (u + 1) // stages
+                    yield ("wait", ("KFULL", s2), k & 1, k)
+                    kwaited = True
+                yield ("wait", ("PVDONE", x), (nv[x] - 1) & 1, nv[x] - 1)
+                yield ("commit", ("SFULL", x))
+        yield ("commit", ("KVEMPTY", s))
+
+
+def fwd_softmax(x, n, rng, p_rescale):
+    for it in range(n):
+        yield ("wait", ("SFULL", x), it & 1, it)
+        if it > 0 and rng.random() < p_rescale:
+            yield ("wait", ("PVDONE", x), (it - 1) & 1, it - 1)
+        yield ("arrive", ("PFULL", x))
+    if n:
+        yield ("wait", ("PVDONE", x), (n - 1) & 1, n - 1)
+
+
+def run_fwd(seed, n_tiles, stages, p_rescale=0.3):
+    rng = random.Random(seed)
+    roles = {"producer": fwd_producer(n_tiles, stages), "issuer": fwd_issuer(n_tiles, stages),
+             "softmax0": fwd_softmax(0, n_tiles[0], rng, p_rescale),
+             "softmax1": fwd_softmax(1, n_tiles[1], rng, p_rescale)}
+    schedule(rng, roles, lambda name: 1)
+
+
+# ---------------------------------------------------------------- split-KV decode
+# `fa_decode_kernel`: one query tile, S and P in two TMEM buffers (tile i in
+# buffer i % 2), so the issuer runs one S ahead of the softmax.
+
+def dec_producer(n, stages):
+    if n:
+        yield ("tma", "QFULL")
+    for it in range(n):
+        s, k = it % stages, it // stages
+        yield ("wait", ("KVEMPTY", s), (k & 1) ^ 1, k - 1)
+        yield ("tma", ("KFULL", s))
+        yield ("tma", ("VFULL", s))
+
+
+def dec_issuer(n, stages):
+    if not n:
+        return
+    yield ("wait", "QFULL", 0, 0)
+
+    def issue_s(i):
+        k = i // stages
+        yield ("wait", ("KFULL", i % stages), k & 1, k)
+        if i >= 2:
+            yield ("wait", ("PVDONE", i & 1), ((i - 2) >> 1) & 1, (i - 2) >> 1)
+        yield ("commit", ("SFULL", i & 1))
+
+    yield from issue_s(0)
+    for it in range(n):
+        if it + 1 < n:
+            yield from issue_s(it + 1)
+        s = it % stages
+        yield ("wait", ("PFULL", it & 1), (it >> 1) & 1, it >> 1)
+        yield ("wait", ("VFULL", s), (it // stages) & 1, it // stages)
+        yield ("commit", ("KVEMPTY", s))
+        yield ("commit", ("PVDONE", it & 1))
+
+
+def dec_softmax(n, rng, p_rescale):
+    for it in range(n):
+        yield ("wait", ("SFULL", it & 1), (it >> 1) & 1, it >> 1)
+        if it > 0 and rng.random() < p_rescale:
+            yield ("wait", ("PVDONE", (it - 1) & 1), ((it - 1) >> 1) & 1, (it - 1) >> 1)
+        yield ("arrive", ("PFULL", it & 1))
+    if n:
+        yield ("wait", ("PVDONE", (n - 1) & 1), ((n - 1) >> 1) & 1, (n - 1) >> 1)
+
+
+def run_decode(seed, n, stages, p_rescale=0.3):
+    rng = random.Random(seed)
+    roles = {"producer": dec_producer(n, stages), "issuer": dec_issuer(n, stages),
+             "softmax": dec_softmax(n, rng, p_rescale)}
+    schedule(rng, roles, lambda name: 1)
+
+
 TILE_COUNTS = [(1, 1), (2, 2), (3, 3), (7, 7), (12, 12), (3, 5), (5, 6), (0, 4), (8, 1)]
 
 
@@ -270,6 +389,66 @@ def test_model_finds_the_alias_of_one_pready_barrier_per_query_tile():
     assert all(f.startswith("issuer") and " on ('PFULL'" in f for f in found), found[:3]
     assert all("with" in f and int(f.split("with ")[1].split()[0]) == int(f.split("phase ")[1].split()[0]) + 2
                for f in found)
+
+
+def test_bf16_forward_protocol_never_aliases():
+    for i in range(600):
+        run_fwd(seed=i, n_tiles=TILE_COUNTS[i % len(TILE_COUNTS)], stages=(2, 4)[i % 2])
+
+
+def test_forward_model_finds_s_issued_before_p_is_awaited():
+    """Issuing the next S_x before waiting for P_x (with P kept elsewhere, as
+    the FP8 kernel does) lets a softmax warpgroup finish two tiles before
+    the issuer's wait: the P-ready barrier runs two phases ahead."""
+    def issuer_s_first(n_tiles, stages):
+        total = max(n_tiles)
+        nv, ns = [0, 0], [0, 0]
+        if not total:
+            return
+        yield ("wait", "QFULL", 0, 0)
+        yield ("wait", ("KFULL", 0), 0, 0)
+        for x in range(2):
+            if n_tiles[x] > 0:
+                yield ("commit", ("SFULL", x))
+                ns[x] += 1
+        for u in range(total):
+            s, s2 = u % stages, (u + 1) % stages
+            for x in range(2):
+                if u + 1 < n_tiles[x]:
+                    k = (u + 1) // stages
+                    yield ("wait", ("KFULL", s2), k & 1, k)
+                    yield ("wait", ("SFREE", x), (ns[x] - 1) & 1, ns[x] - 1)
+                    yield ("commit", ("SFULL", x))
+                    ns[x] += 1
+            for x in range(2):
+                if u < n_tiles[x]:
+                    yield ("wait", ("PFULL", x), nv[x] & 1, nv[x])
+                    yield ("wait", ("VFULL", s), (u // stages) & 1, u // stages)
+                    yield ("commit", ("PVDONE", x))
+                    nv[x] += 1
+            yield ("commit", ("KVEMPTY", s))
+
+    def softmax_releasing_s(x, n):
+        for it in range(n):
+            yield ("wait", ("SFULL", x), it & 1, it)
+            yield ("arrive", ("SFREE", x))
+            yield ("arrive", ("PFULL", x))
+
+    found = []
+    for i in range(600):
+        n_tiles, stages = TILE_COUNTS[i % len(TILE_COUNTS)], (2, 4)[i % 2]
+        roles = {"producer": fwd_producer(n_tiles, stages), "issuer": issuer_s_first(n_tiles, stages),
+                 "softmax0": softmax_releasing_s(0, n_tiles[0]), "softmax1": softmax_releasing_s(1, n_tiles[1])}
+        try:
+            schedule(random.Random(i), roles, lambda name: 1)
+        except Alias as e:
+            found.append(str(e))
+    assert found and all(f.startswith("issuer on ('PFULL'") for f in found), found[:3]
+
+
+def test_decode_protocol_never_aliases():
+    for i in range(600):
+        run_decode(seed=i, n=(1, 2, 3, 4, 7, 13, 40)[i % 7], stages=(3, 6)[i % 2])
 
 
 def test_bwd128_protocol_never_aliases():
