@@ -1,5 +1,5 @@
-"""Models of the forward (bf16 and FP8), split-KV decode and d = 128
-backward kernels' roles and mbarriers, run under random schedules, that check
+"""Models of the forward (bf16 and FP8), split-KV decode and backward
+(d = 64 and d = 128) kernels' roles and mbarriers, run under random schedules, that check
 the one rule a parity wait depends on.
 
 `mbarrier.try_wait.parity(P)` answers "has the phase of parity P completed?"
@@ -369,6 +369,73 @@ def run_decode(seed, n, stages, p_rescale=0.3):
     schedule(rng, roles, lambda name: 1)
 
 
+# ---------------------------------------------------------------- d = 64 backward
+# `fa_bwd_kernel<64>`: Q and dO double-buffered together, LSE/D per stage, S
+# and dP in their own TMEM columns, dQ into two TMEM buffers that the compute
+# warpgroups drain one block later (after the next block's dS).
+
+def bwd64_producer(n):
+    yield ("tma", "KV")
+    for i in range(n):
+        s = i & 1
+        yield ("wait", ("QEMPTY", s), ((i >> 1) & 1) ^ 1, (i >> 1) - 1)
+        yield ("tma", ("QFULL", s))
+        yield ("arrive", ("LSE", s))
+
+
+def bwd64_issuer(n):
+    if not n:
+        return
+    yield ("wait", "KV", 0, 0)
+    yield ("wait", ("QFULL", 0), 0, 0)
+    yield ("commit", "SFULL")
+    yield ("commit", "DPFULL")
+    for i in range(n):
+        s, more = i & 1, i + 1 < n
+        yield ("wait", "PFULL", i & 1, i)
+        yield ("commit", "SFREE")                                           # dV(i) read P
+        if more:
+            yield ("wait", ("QFULL", s ^ 1), ((i + 1) >> 1) & 1, (i + 1) >> 1)
+            yield ("wait", "SFREE", i & 1, i)
+            yield ("commit", "SFULL")                                       # S(i+1)
+        yield ("wait", "DSFULL", i & 1, i)
+        yield ("commit", "DPFREE")                                          # dK(i) read dS
+        yield ("commit", ("QEMPTY", s))
+        if i >= 2:
+            yield ("wait", ("DQFREE", s), ((i - 2) >> 1) & 1, (i - 2) >> 1)
+        yield ("commit", ("DQFULL", s))                                     # dQ(i)
+        if more:
+            yield ("wait", "DPFREE", i & 1, i)
+            yield ("commit", "DPFULL")                                      # dP(i+1)
+    yield ("commit", "ACC")
+
+
+def bwd64_compute(n):
+    def drain(j):
+        yield ("wait", ("DQFULL", j & 1), (j >> 1) & 1, j >> 1)
+        yield ("arrive", ("DQFREE", j & 1))
+
+    for i in range(n):
+        yield ("wait", ("LSE", i & 1), (i >> 1) & 1, i >> 1)
+        yield ("wait", "SFULL", i & 1, i)
+        yield ("arrive", "PFULL")
+        yield ("wait", "DPFULL", i & 1, i)
+        if i > 0:
+            yield ("wait", ("DQFULL", (i - 1) & 1), ((i - 1) >> 1) & 1, (i - 1) >> 1)
+        yield ("arrive", "DSFULL")
+        if i > 0:
+            yield from drain(i - 1)
+    if n:
+        yield from drain(n - 1)
+        yield ("wait", "ACC", 0, 0)
+
+
+def run_bwd64(seed, n):
+    rng = random.Random(seed)
+    roles = {"producer": bwd64_producer(n), "issuer": bwd64_issuer(n), "compute": bwd64_compute(n)}
+    schedule(rng, roles, lambda name: 1)
+
+
 TILE_COUNTS = [(1, 1), (2, 2), (3, 3), (7, 7), (12, 12), (3, 5), (5, 6), (0, 4), (8, 1)]
 
 
@@ -449,6 +516,11 @@ def test_forward_model_finds_s_issued_before_p_is_awaited():
 def test_decode_protocol_never_aliases():
     for i in range(600):
         run_decode(seed=i, n=(1, 2, 3, 4, 7, 13, 40)[i % 7], stages=(3, 6)[i % 2])
+
+
+def test_bwd64_protocol_never_aliases():
+    for i in range(600):
+        run_bwd64(seed=i, n=(1, 2, 3, 4, 5, 9, 16)[i % 7])
 
 
 def test_bwd128_protocol_never_aliases():
