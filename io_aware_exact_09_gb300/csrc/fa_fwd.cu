@@ -156,6 +156,10 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
     bool bad = bad_len;
     const int kvis = VARLEN ? Lk : key_visible_bound(p.key_len, b, p.N, &bad);
     if (bad && threadIdx.x == 0 && pq == 0 && (bh % p.H) == 0) record_status(g, kStatusBadKeyLen, 0);
+    // In a ragged batch the grid covers the longest sequence: a CTA whose
+    // query tiles both lie past its own sequence's end has no row to write and
+    // leaves before any set-up (the whole CTA takes this branch together)
+    if (qn[0] <= 0 && qn[1] <= 0) return;
 
     // Without a block mask the key tiles query tile x sees are exactly
     // [0, kend[x]): keys below key_len and, under the causal mask, not past
