@@ -263,10 +263,10 @@ fa_status fa_tile_plan(int B, int N, int causal, const int32_t *key_len,
  * a head range of one batch: each chunk's kernels start once its own inputs
  * are on the device, on a compute stream of their own so that chunks share
  * the SMs, and its outputs are copied back while later chunks compute.
- * Uploads and downloads each have a stream; these streams belong to the
- * library (one set per device, made on first use) and are ordered after the
- * work already queued on `stream`, which in turn waits for all of them.
- * Calls from several host threads enqueue one after the other.  Results are
+ * Uploads and downloads each have a stream.  These streams and their events
+ * are made for the call and released when it returns (nothing persists);
+ * they are ordered after the work already queued on `stream`, which in turn
+ * waits for all of them.  Results are
  * bit-identical to fa_fwd / fa_bwd on device buffers except dQ (summed by
  * reduce-adds in a varying order).
  * dev_workspace: device memory of at least fa_host_workspace_size() bytes,

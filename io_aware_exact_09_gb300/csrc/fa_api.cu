@@ -668,36 +668,38 @@ size_t fa_host_workspace_size(int B, int H, int N, int d, int with_backward) {
 }
 
 namespace {
-// Streams and events of the host path, made once per device and kept for
-// the process: an upload stream, a download stream and one compute stream
-// per chunk (so that the chunks' kernels can share the SMs).  A call holds
-// the device's mutex while it enqueues, so concurrent calls from several
-// host threads order their work on these streams one after the other.
+// Streams and events of one host-path call: an upload stream, a download
+// stream and one compute stream per chunk (so that the chunks' kernels can
+// share the SMs).  They are made for the call and released when it returns;
+// CUDA frees a stream or event whose queued work is still pending once that
+// work has completed, so nothing outlives the call's own work.
 struct HostStreams {
     bool ok = false;
+    int n = 0;
     cudaStream_t up = nullptr, down = nullptr, comp[kMaxHostChunks] = {};
     cudaEvent_t start = nullptr, down_done = nullptr, in[kMaxHostChunks] = {}, dO_in[kMaxHostChunks] = {},
                 fwd_done[kMaxHostChunks] = {}, bwd_done[kMaxHostChunks] = {};
-    std::mutex mu;
-    bool init() {
+    explicit HostStreams(int nchunks) : n(nchunks) {
         auto mk_s = [](cudaStream_t *s) { return cudaStreamCreateWithFlags(s, cudaStreamNonBlocking) == cudaSuccess; };
         auto mk_e = [](cudaEvent_t *e) { return cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess; };
-        bool good = mk_s(&up) && mk_s(&down) && mk_e(&start) && mk_e(&down_done);
-        for (int i = 0; good && i < kMaxHostChunks; ++i)
-            good = mk_s(&comp[i]) && mk_e(&in[i]) && mk_e(&dO_in[i]) && mk_e(&fwd_done[i]) && mk_e(&bwd_done[i]);
-        return good;
+        ok = mk_s(&up) && mk_s(&down) && mk_e(&start) && mk_e(&down_done);
+        for (int i = 0; ok && i < n; ++i)
+            ok = mk_s(&comp[i]) && mk_e(&in[i]) && mk_e(&dO_in[i]) && mk_e(&fwd_done[i]) && mk_e(&bwd_done[i]);
     }
+    ~HostStreams() {
+        for (cudaEvent_t e : {start, down_done})
+            if (e) cudaEventDestroy(e);
+        for (int i = 0; i < kMaxHostChunks; ++i) {
+            for (cudaEvent_t e : {in[i], dO_in[i], fwd_done[i], bwd_done[i]})
+                if (e) cudaEventDestroy(e);
+            if (comp[i]) cudaStreamDestroy(comp[i]);
+        }
+        if (up) cudaStreamDestroy(up);
+        if (down) cudaStreamDestroy(down);
+    }
+    HostStreams(const HostStreams &) = delete;
+    HostStreams &operator=(const HostStreams &) = delete;
 };
-
-HostStreams *host_streams() {
-    constexpr int kMaxDevices = 64;
-    static HostStreams pool[kMaxDevices];
-    static std::once_flag once[kMaxDevices];
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    std::call_once(once[dev], [dev] { pool[dev].ok = pool[dev].init(); });
-    return pool[dev].ok ? &pool[dev] : nullptr;
-}
 }  // namespace
 
 fa_status fa_attention_host(const void *Q, const void *K, const void *V, const void *dO, void *O, float *LSE,
@@ -716,10 +718,10 @@ fa_status fa_attention_host(const void *Q, const void *K, const void *V, const v
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t *w = static_cast<uint8_t *>(dev_workspace);
     const size_t nb = ((size_t)N + 127) / 128;
-    HostStreams *hs = host_streams();
-    if (!hs) return FA_ERR_CUDA;
+    HostStreams streams(L.nchunks);
+    HostStreams *hs = &streams;
+    if (!hs->ok) return FA_ERR_CUDA;
     {
-        std::lock_guard<std::mutex> lock(hs->mu);
         auto after = [](cudaEvent_t e, cudaStream_t from, cudaStream_t to) {
             return cudaEventRecord(e, from) == cudaSuccess && cudaStreamWaitEvent(to, e, 0) == cudaSuccess;
         };
