@@ -11,18 +11,23 @@ CUDA events on the launching stream, inputs resident in HBM, L2 flushed
 between steps.  ``e2e`` is the same metric through ``fa_attention_host``
 with pinned host buffers (copies inside the timed region).  Under torchrun
 every rank runs its own replica of the workload (weak scaling, no data-path
-collective); the time is the max over ranks.
+collective); the time is the max over ranks.  ``per_config`` holds the
+forward and forward+backward figures of every other configuration (a few
+timed steps each, same loop).  Fractions of peak divide by the measured
+dense-bf16 figure that matches the clock record of the timed region: the
+burst figure when the SMs ran at their maximum clock, else the sustained one.
 
 ``--impl reference`` times the fp64 CPU oracle instead, on a bounded sample
-of the same workload, on this machine's host cores.
+of the same workload (one head truncated to ``--cpu-tokens`` tokens, the
+sample ``cpu_baseline`` times too), on this machine's host cores.
 
 ``--fp8`` measures the FP8 forward instead: one step = the block
 quantisation of Q, K and V (``fa_quantize_fp8``, three launches) and
 ``fa_fwd_fp8``; ``value`` is forward TFLOP/s over the step, the roofline is
-the FP8 forward kernel against the dense-FP8 peak (the measured sustained
-bf16 figure x 2, the nominal fp8 : bf16 ratio).  ``--incoherent`` adds the
+the FP8 forward kernel against the dense-FP8 peak (the measured bf16
+figure chosen as above x 2, the nominal fp8 : bf16 ratio).  ``--incoherent`` adds the
 incoherent processing: Q and K go through ``fa_quantize_fp8_rotated`` with a
-seeded random sign vector, and the forward takes softmax_scale / d.
+seeded random sign vector, and the forward is ``fa_fwd_fp8_rotated``.
 
 ``--tile-sweep`` times the forward at each tile shape ``fa_fwd_tiles`` offers
 (query rows per CTA 128 / 256 x key rows per tile 64 / 128) on the workload
@@ -167,6 +172,22 @@ def measured_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
+def pick_peak(peaks, clk):
+    """Dense-bf16 denominator for a kernel timed in this run.  The burst figure
+    (a short cuBLAS run at the maximum SM clock) when the clock record of the
+    timed region shows the SMs at their maximum clock with no power cap
+    active; the sustained figure (a seconds-long cuBLAS loop, power-capped)
+    otherwise, or when no clock record exists.  Returns (TFLOP/s, label)."""
+    burst = float(peaks.get("bf16_tflops"))
+    sustained = float(peaks.get("bf16_tflops_sustained", burst))
+    sm = clk.get("sm_mhz") if clk else None
+    mx = (clk.get("sm_max_mhz") if clk else None) or peaks.get("sm_max_mhz")
+    capped = bool(clk) and "sw_power_cap" in clk.get("reasons", [])
+    if sm is not None and mx and sm >= 0.95 * float(mx) and not capped:
+        return burst, "bf16_tflops (burst: SM clock at its maximum during the timed region)"
+    return sustained, "bf16_tflops_sustained (SM clock below its maximum or not recorded)"
+
+
 def source_digest(fname: str) -> str:
     h = hashlib.sha256()
     for f in sorted({fname, "fa_ptx.cuh", "fa_tiles.cuh"}):
@@ -175,9 +196,9 @@ def source_digest(fname: str) -> str:
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it
-    was taken on the current kernel source (else None)."""
+def ncu_record(kernel: str, workload: str):
+    """The committed ncu figures of `kernel` on `workload`, if they were taken
+    on the current kernel source (else None)."""
     p = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if not os.path.exists(p):
         return None
@@ -186,7 +207,19 @@ def ncu_traffic(kernel: str, workload: str):
     r = rows.get(kernel, {}).get(workload)
     if not r or r.get("source_digest") != source_digest(KERNEL_SOURCES[kernel]):
         return None
-    return r.get("bytes_per_launch")
+    return r
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch (read + write) from the committed ncu capture, or None."""
+    r = ncu_record(kernel, workload)
+    return None if r is None else r.get("bytes_per_launch")
+
+
+def ncu_tensor_pipe(kernel: str, workload: str):
+    """ncu's sm__pipe_tensor_cycles_active (% of peak) from the committed capture, or None."""
+    r = ncu_record(kernel, workload)
+    return None if r is None else r.get("tensor_pipe_active_pct")
 
 
 # ---------------------------------------------------------------- CPU oracle baseline
@@ -216,26 +249,31 @@ def oracle_time(w, n):
     return fl / dt / 1e12, dt
 
 
-def oracle_calibrate(w, budget_s: float):
-    """Largest power-of-two prefix length n (<= N, <= 8192) whose oracle call
-    stays near budget_s."""
-    n = 128
-    while True:
-        _, dt = oracle_time(w, n)
-        if dt * 4.5 > budget_s or 2 * n > min(w.N, 8192):
-            return n
-        n *= 2
+def oracle_sample_desc(w, n):
+    return ("fp64 oracle fwd+bwd (materialised S and P), one head of %s truncated to its first %d tokens, "
+            "d=%d" % (w.name, n, w.d))
 
 
-def oracle_sample(w, budget_s: float, n=None):
-    """Time the fp64 oracle on a bounded sample; returns (TFLOP/s, cores, description)."""
+def oracle_sample(w, n, budget_s: float = 0.0):
+    """Time the fp64 oracle on the bounded sample of n tokens of one head,
+    calling it repeatedly until about budget_s has passed (at least once).
+    Returns (TFLOP/s, cores, description, seconds per call)."""
     import oracle
-    if n is None:
-        n = oracle_calibrate(w, budget_s)
-    tf, dt = oracle_time(w, n)
-    desc = ("fp64 oracle fwd+bwd (materialised S and P), one head of %s truncated to its first %d tokens, "
-            "d=%d, %.2f s per call" % (w.name, n, w.d, dt))
-    return tf, oracle.num_threads(), desc
+    dts, tfs = [], []
+    t_end = time.perf_counter() + budget_s
+    while not dts or time.perf_counter() < t_end:
+        tf, dt = oracle_time(w, n)
+        tfs.append(tf)
+        dts.append(dt)
+    dt = sum(dts) / len(dts)
+    tf = sum(tfs) / len(tfs)
+    desc = oracle_sample_desc(w, n) + ", %d call(s), %.2f s per call" % (len(dts), dt)
+    return tf, oracle.num_threads(), desc, dt
+
+
+def sample_tokens(w, requested):
+    """Tokens of the CPU sample: the requested count, at most N."""
+    return max(1, min(int(requested), w.N))
 
 
 # ---------------------------------------------------------------- decode
@@ -440,7 +478,6 @@ def run_fp8(args):
     if args.incoherent:
         g = torch.Generator().manual_seed(w.seed + 17)
         signs = torch.where(torch.rand(d, generator=g) < 0.5, -1, 1).to(torch.int8).to(dev)
-        scale = w.softmax_scale / d
     wsn = fa.fa_fwd_workspace_size(B, H, N, d)
     ws = fa.workspace(wsn, dev)
     stream = torch.cuda.current_stream(dev)
@@ -467,8 +504,9 @@ def run_fp8(args):
         check(fa.fa_quantize_fp8(V, Vt8, sV, B, H, N, d, True, sp), "fa_quantize_fp8 V")
         if record:
             ev[1].record(stream)
-        check(fa.fa_fwd_fp8(Q8, K8, Vt8, sQ, sK, sV, O, LSE, B, H, N, d, scale, w.causal, kl, bm, ws, wsn,
-                            sp), "fa_fwd_fp8")
+        fwd = fa.fa_fwd_fp8 if signs is None else fa.fa_fwd_fp8_rotated
+        check(fwd(Q8, K8, Vt8, sQ, sK, sV, O, LSE, B, H, N, d, scale, w.causal, kl, bm, ws, wsn, sp),
+              "fa_fwd_fp8" if signs is None else "fa_fwd_fp8_rotated")
         if record:
             ev[2].record(stream)
 
@@ -500,11 +538,13 @@ def run_fp8(args):
     step_ms = reduce_max(ms, dev)
     value = whole_job_tflops(flops, ws_n, step_ms / 1e3)
     peaks, peak_src = measured_peaks()
-    peak8 = 2.0 * float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    peak16, peak_kind = pick_peak(peaks, clk)
+    peak8 = 2.0 * peak16
     achieved = flops / (mf / 1e3) / 1e12
     roofline = {"bound": "tensor", "kernel": "fa_fwd_kernel<128, fp8>", "achieved": achieved, "peak": peak8,
                 "unit": "TFLOP/s", "frac": achieved / peak8, "traffic": ncu_traffic("fa_fwd_kernel_fp8", w.name),
-                "peak_source": "%s bf16_tflops_sustained x 2 (nominal dense fp8 : bf16 ratio 4.5 : 2.25)" % peak_src}
+                "ncu_tensor_pipe_active_pct": ncu_tensor_pipe("fa_fwd_kernel_fp8", w.name),
+                "peak_source": "%s %s x 2 (nominal dense fp8 : bf16 ratio 4.5 : 2.25)" % (peak_src, peak_kind)}
     e2e = None
     if not args.no_e2e:
         # the user's call from host memory: bf16 Q, K, V in, O and LSE out
@@ -576,6 +616,9 @@ def run_tile_sweep(args):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     out = []
     launches = 0
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
     for bq, bk in ((256, 128), (256, 64), (128, 128), (128, 64)):
         def step():
             st = fa.fa_fwd_tiles(Q, K, V, O, LSE, B, H, N, d, w.softmax_scale, w.causal, kl, bm, bq, bk, ws, wsn, sp)
@@ -595,10 +638,11 @@ def run_tile_sweep(args):
             launches += 1
         ms = reduce_max(sum(ts) / len(ts), dev)
         out.append({"block_q": bq, "block_k": bk, "ms": ms, "tflops": whole_job_tflops(flops, ws_n, ms / 1e3)})
+    clk = clocks.stop()
     if fa.fa_get_device_status(ws, sp) != 0:
         raise RuntimeError("device status after the sweep")
     peaks, peak_src = measured_peaks()
-    peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    peak, peak_kind = pick_peak(peaks, clk)
     best = max(out, key=lambda r: r["tflops"])
     if rank == 0:
         print(json.dumps({
@@ -610,8 +654,8 @@ def run_tile_sweep(args):
             "sweep": out,
             "roofline": {"bound": "tensor", "kernel": "fa_fwd_kernel (best shape)", "achieved": best["tflops"] / ws_n,
                          "peak": peak, "unit": "TFLOP/s", "frac": best["tflops"] / ws_n / peak, "traffic": None,
-                         "peak_source": "%s bf16_tflops_sustained" % peak_src},
-            "cpu_baseline": None, "e2e": None, "gpu_launches": launches}), flush=True)
+                         "peak_source": "%s %s" % (peak_src, peak_kind)},
+            "cpu_baseline": None, "e2e": None, "clocks": clk, "gpu_launches": launches}), flush=True)
     return 0
 
 
@@ -696,11 +740,11 @@ def run_varlen(args, w):
     ms = reduce_max(sum(times) / len(times), dev)
     value = whole_job_tflops(flops, ws_n, ms / 1e3)
     peaks, peak_src = measured_peaks()
-    peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    peak, peak_kind = pick_peak(peaks, clk)
     achieved = flops / (ms / 1e3) / 1e12
     roofline = {"bound": "tensor", "kernel": "fa_fwd_kernel<%d, varlen>" % d, "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak, "traffic": ncu_traffic("fa_fwd_kernel_varlen", w.name),
-                "peak_source": "%s bf16_tflops_sustained" % peak_src}
+                "peak_source": "%s %s" % (peak_src, peak_kind)}
     e2e = None
     if not args.no_e2e:
         pin = lambda t: t.contiguous().pin_memory()
@@ -796,18 +840,21 @@ def run_reference(args):
     import oracle
     oracle.build()
     w = WORKLOADS[args.workload]
-    vals = []
-    desc = cores = None
-    n = oracle_calibrate(w, budget_s=6.0)
+    vals, dts = [], []
+    cores = None
+    n = sample_tokens(w, args.cpu_tokens)
+    # one oracle call on the bounded sample per step (the sample cpu_baseline times too)
     for i in range(args.warmup + args.steps):
-        tf, cores, desc = oracle_sample(w, 6.0, n)
+        tf, cores, _, dt = oracle_sample(w, n)
         if i >= args.warmup:
             vals.append(tf)
+            dts.append(dt)
     v = statistics.median(vals)
+    desc = oracle_sample_desc(w, n) + ", %d call(s), %.2f s per call" % (len(dts), sum(dts) / len(dts))
     line = {"impl": "reference", "metric": "attention fwd+bwd TFLOP/s (bf16)", "value": v, "unit": "TFLOP/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal},
+            "config": workload_config(w, args.gpus),
             "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc},
             "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
@@ -816,6 +863,118 @@ def run_reference(args):
 
 
 # ---------------------------------------------------------------- our arm
+# The configurations the method is evaluated on besides the timed workload:
+# each gets a short forward + backward timing in the same run.
+PER_CONFIG = ("small_b1h2n128d64", "gpt2m_causal_b8h16n1024d64", "bertl_keypad_b16h16n512d64",
+              "longctx_causal_b1h16n16384d128", "blocksparse_b2h16n8192d64")
+
+
+def workload_config(w, n_gpus):
+    """The `config` object of a square workload's line (both arms use it)."""
+    return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+            "key_padding": w.key_len_range is not None, "block_sparse": w.sparse_density is not None,
+            "parallelism": "replicas" if n_gpus > 1 else "single", "l2": "flushed between steps"}
+
+
+class SquareStep:
+    """Device buffers of one square workload and its step: fa_fwd, then the
+    three backward stages, each bracketed by CUDA events on the launching
+    stream."""
+
+    def __init__(self, fa, w, dev):
+        import torch
+        from synthetic import algorithmic_fwd_flops, make_inputs
+        self.fa, self.w = fa, w
+        B, H, N, d = w.B, w.H, w.N, w.d
+        self.case = make_inputs(w)
+        c = self.case
+        self.Q, self.K, self.V, self.dO = (c[k].to(dev).contiguous() for k in ("Q", "K", "V", "dO"))
+        self.kl = None if c["key_len"] is None else c["key_len"].to(dev)
+        self.bm = None if c["block_mask"] is None else c["block_mask"].contiguous().to(dev)
+        self.O = torch.empty_like(self.Q)
+        self.LSE = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        self.dQ, self.dK, self.dV = (torch.empty_like(self.Q) for _ in range(3))
+        self.wsb = fa.fa_bwd_workspace_size(B, H, N, d)
+        self.wsf = fa.fa_fwd_workspace_size(B, H, N, d)
+        self.ws_f = fa.workspace(self.wsf, dev)
+        self.ws_b = fa.workspace(self.wsb, dev)
+        self.stream = torch.cuda.current_stream(dev)
+        self.flops_fwd = algorithmic_fwd_flops(B, H, N, d, w.causal,
+                                               None if c["key_len"] is None else c["key_len"].tolist(),
+                                               None if c["block_mask"] is None else c["block_mask"])
+        self.ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        self.bwd_name = "fa_bwd128_kernel" if d == 128 else "fa_bwd_kernel"
+
+    def _check(self, st, where):
+        if st != 0:
+            raise RuntimeError("%s failed: %s" % (where, self.fa.fa_status_string(st)))
+
+    def run(self, record):
+        fa, w, s, ev = self.fa, self.w, self.stream.cuda_stream, self.ev
+        B, H, N, d = w.B, w.H, w.N, w.d
+        if record:
+            ev[0].record(self.stream)
+        self._check(fa.fa_fwd(self.Q, self.K, self.V, self.O, self.LSE, B, H, N, d, w.softmax_scale, w.causal,
+                              self.kl, self.bm, self.ws_f, self.wsf, s), "fa_fwd")
+        if record:
+            ev[1].record(self.stream)
+        self._check(fa.fa_bwd_preprocess(self.O, self.dO, B, H, N, d, self.ws_b, self.wsb, s), "fa_bwd_preprocess")
+        if record:
+            ev[2].record(self.stream)
+        self._check(fa.fa_bwd_main(self.Q, self.K, self.V, self.LSE, self.dO, self.dK, self.dV, B, H, N, d,
+                                   w.softmax_scale, w.causal, self.kl, self.bm, self.ws_b, self.wsb, s), "fa_bwd_main")
+        if record:
+            ev[3].record(self.stream)
+        self._check(fa.fa_bwd_postprocess(self.dQ, B, H, N, d, w.softmax_scale, self.ws_b, self.wsb, s),
+                    "fa_bwd_postprocess")
+        if record:
+            ev[4].record(self.stream)
+
+    def status(self, where):
+        for wsx in (self.ws_f, self.ws_b):
+            self._check(self.fa.fa_get_device_status(wsx, self.stream.cuda_stream), where)
+
+    def time(self, steps, warmup, flush, on_start=None):
+        """Mean ms per stage over `steps` timed steps (L2 flushed before each,
+        outside the events).  on_start runs after the warm-up, before timing."""
+        import torch
+        for _ in range(warmup):
+            self.run(False)
+        torch.cuda.synchronize()
+        self.status("device status after warm-up")
+        if on_start is not None:
+            on_start()
+        times = {"step": [], "fwd": [], "pre": [], "main": [], "post": []}
+        barrier()
+        torch.cuda.synchronize()
+        for _ in range(steps):
+            flush.zero_()
+            self.run(True)
+            ev = self.ev
+            ev[4].synchronize()
+            times["fwd"].append(ev[0].elapsed_time(ev[1]))
+            times["pre"].append(ev[1].elapsed_time(ev[2]))
+            times["main"].append(ev[2].elapsed_time(ev[3]))
+            times["post"].append(ev[3].elapsed_time(ev[4]))
+            times["step"].append(ev[0].elapsed_time(ev[4]))
+        torch.cuda.synchronize()
+        barrier()
+        return {k: sum(v) / len(v) for k, v in times.items()}
+
+
+def per_config_entry(st, mean, peak):
+    """Forward and forward+backward figures of one configuration."""
+    f = st.flops_fwd
+    bwd_ms = mean["pre"] + mean["main"] + mean["post"]
+    fwd_tf = f / (mean["fwd"] / 1e3) / 1e12
+    bwd_tf = 2.5 * f / (bwd_ms / 1e3) / 1e12
+    step_tf = FWD_BWD_FACTOR * f / (mean["step"] / 1e3) / 1e12
+    return {"fwd_ms": mean["fwd"], "bwd_ms": bwd_ms, "bwd_main_ms": mean["main"], "fwd_bwd_ms": mean["step"],
+            "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf, "fwd_bwd_tflops": step_tf,
+            "fwd_frac_of_peak": fwd_tf / peak, "bwd_frac_of_peak": bwd_tf / peak,
+            "fwd_bwd_frac_of_peak": step_tf / peak, "algorithmic_fwd_flops": f}
+
+
 def run_ours(args):
     import torch
 
@@ -825,101 +984,63 @@ def run_ours(args):
     dev = torch.device("cuda", local)
 
     import io_aware_exact_09_gb300 as fa
-    from synthetic import WORKLOADS, algorithmic_fwd_flops, make_inputs
+    from synthetic import WORKLOADS
     fa.build()
     w = WORKLOADS[args.workload]
     B, H, N, d = w.B, w.H, w.N, w.d
-    case = make_inputs(w)
-    Q, K, V, dO = (case[k].to(dev).contiguous() for k in ("Q", "K", "V", "dO"))
-    kl = None if case["key_len"] is None else case["key_len"].to(dev)
-    bm = None if case["block_mask"] is None else case["block_mask"].contiguous().to(dev)
-    scale = w.softmax_scale
-    O = torch.empty_like(Q)
-    LSE = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-    dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
-    wsb = fa.fa_bwd_workspace_size(B, H, N, d)
-    wsf = fa.fa_fwd_workspace_size(B, H, N, d)
-    ws_f = fa.workspace(wsf, dev)
-    ws_b = fa.workspace(wsb, dev)
-    stream = torch.cuda.current_stream(dev)
-    sp = stream.cuda_stream
-    flops_fwd = algorithmic_fwd_flops(B, H, N, d, w.causal,
-                                      None if case["key_len"] is None else case["key_len"].tolist(),
-                                      None if case["block_mask"] is None else case["block_mask"])
+    st = SquareStep(fa, w, dev)
+    case, scale = st.case, w.softmax_scale
+    flops_fwd = st.flops_fwd
     flops_step = FWD_BWD_FACTOR * flops_fwd
     flops_main = 2.5 * flops_fwd
 
-    def check(st, where):
-        if st != 0:
-            raise RuntimeError("%s failed: %s" % (where, fa.fa_status_string(st)))
-
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
-
-    def step(record):
-        if record:
-            ev[0].record(stream)
-        check(fa.fa_fwd(Q, K, V, O, LSE, B, H, N, d, scale, w.causal, kl, bm, ws_f, wsf, sp), "fa_fwd")
-        if record:
-            ev[1].record(stream)
-        check(fa.fa_bwd_preprocess(O, dO, B, H, N, d, ws_b, wsb, sp), "fa_bwd_preprocess")
-        if record:
-            ev[2].record(stream)
-        check(fa.fa_bwd_main(Q, K, V, LSE, dO, dK, dV, B, H, N, d, scale, w.causal, kl, bm, ws_b, wsb, sp),
-              "fa_bwd_main")
-        if record:
-            ev[3].record(stream)
-        check(fa.fa_bwd_postprocess(dQ, B, H, N, d, scale, ws_b, wsb, sp), "fa_bwd_postprocess")
-        if record:
-            ev[4].record(stream)
+    def check(s, where):
+        if s != 0:
+            raise RuntimeError("%s failed: %s" % (where, fa.fa_status_string(s)))
 
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)     # 256 MiB > 129 MB L2
-    for _ in range(args.warmup):
-        step(False)
-    torch.cuda.synchronize(dev)
-    for wsx in (ws_f, ws_b):
-        st = fa.fa_get_device_status(wsx, sp)
-        check(st, "device status after warm-up")
-
     clocks = ClockSampler(local)
-    clocks.start()
-    time.sleep(0.3)
-    times = {"step": [], "fwd": [], "pre": [], "main": [], "post": []}
-    barrier()
-    torch.cuda.synchronize(dev)
-    launches = 0
-    for _ in range(args.steps):
-        flush.zero_()                                   # evict L2 between steps (not timed)
-        step(True)
-        launches += 4
-        ev[4].synchronize()
-        times["fwd"].append(ev[0].elapsed_time(ev[1]))
-        times["pre"].append(ev[1].elapsed_time(ev[2]))
-        times["main"].append(ev[2].elapsed_time(ev[3]))
-        times["post"].append(ev[3].elapsed_time(ev[4]))
-        times["step"].append(ev[0].elapsed_time(ev[4]))
-    torch.cuda.synchronize(dev)
-    barrier()
-    clk = clocks.stop()
-    for wsx in (ws_f, ws_b):
-        check(fa.fa_get_device_status(wsx, sp), "device status after timing")
 
-    mean = {k: sum(v) / len(v) for k, v in times.items()}
+    def start_clocks():
+        clocks.start()
+        time.sleep(0.3)
+
+    mean = st.time(args.steps, args.warmup, flush, on_start=start_clocks)
+    clk = clocks.stop()
+    st.status("device status after timing")
+    launches = 4 * args.steps
+
     step_ms = reduce_max(mean["step"], dev)
     value = whole_job_tflops(flops_step, ws_n, step_ms / 1e3)
     fwd_tf = flops_fwd / (mean["fwd"] / 1e3) / 1e12
     bwd_tf = 2.5 * flops_fwd / ((mean["pre"] + mean["main"] + mean["post"]) / 1e3) / 1e12
 
     peaks, peak_src = measured_peaks()
-    peak_tf = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    peak_tf, peak_kind = pick_peak(peaks, clk)
     # dominant kernel of the step
-    bwd_name = "fa_bwd128_kernel" if d == 128 else "fa_bwd_kernel"     # the d = 128 main kernel has its own file
+    bwd_name = st.bwd_name
     dom = bwd_name if mean["main"] >= mean["fwd"] else "fa_fwd_kernel"
     dom_ms = mean["main"] if dom == bwd_name else mean["fwd"]
     dom_flops = flops_main if dom == bwd_name else flops_fwd
     achieved = dom_flops / (dom_ms / 1e3) / 1e12
     roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
                 "frac": achieved / peak_tf, "traffic": ncu_traffic(dom, w.name),
-                "peak_source": "%s bf16_tflops_sustained (kernel timed inside a continuous step loop)" % peak_src}
+                "ncu_tensor_pipe_active_pct": ncu_tensor_pipe(dom, w.name),
+                "kernel_ms": dom_ms, "algorithmic_flops_per_launch": dom_flops,
+                "peak_source": "%s %s" % (peak_src, peak_kind)}
+
+    # the other configurations, the same timing loop, a few steps each
+    per_config = {}
+    if not args.no_per_config and ws_n == 1:
+        for name in PER_CONFIG:
+            if name == w.name:
+                continue
+            sx = SquareStep(fa, WORKLOADS[name], dev)
+            mx = sx.time(max(3, min(args.steps, 10)), 3, flush)
+            sx.status("device status after timing " + name)
+            per_config[name] = per_config_entry(sx, mx, peak_tf)
+            del sx
+        per_config[w.name] = per_config_entry(st, mean, peak_tf)
 
     # end-to-end through the host-buffer entry point (pinned memory, copies timed)
     e2e = None
@@ -934,6 +1055,8 @@ def run_ours(args):
         hws_n = fa.fa_host_workspace_size(B, H, N, d, 1)
         del flush
         hws = fa.workspace(hws_n, dev)
+        stream = st.stream
+        sp = stream.cuda_stream
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         et = []
         n_e2e = max(1, min(args.steps, 5))
@@ -945,7 +1068,6 @@ def run_ours(args):
             e1.synchronize()
             if i > 0:
                 et.append(e0.elapsed_time(e1))
-            launches += 0
         e_ms = reduce_max(sum(et) / len(et), dev)
         nbytes = B * H * N * d * 2
         e2e = {"value": whole_job_tflops(flops_step, ws_n, e_ms / 1e3), "unit": "TFLOP/s",
@@ -954,7 +1076,7 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
-        tf, cores, desc = oracle_sample(w, budget_s=args.cpu_budget)
+        tf, cores, desc, _ = oracle_sample(w, sample_tokens(w, args.cpu_tokens), budget_s=args.cpu_budget)
         cpu = {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc}
 
     if rank == 0:
@@ -962,16 +1084,14 @@ def run_ours(args):
             "metric": "attention fwd+bwd TFLOP/s (bf16)", "value": value, "unit": "TFLOP/s", "n_gpus": ws_n,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": w.name, "B": B, "H": H, "N": N, "d": d, "causal": w.causal,
-                       "key_padding": case["key_len"] is not None, "block_sparse": case["block_mask"] is not None,
-                       "parallelism": "replicas" if ws_n > 1 else "single", "l2": "flushed between steps"},
+            "config": workload_config(w, ws_n),
             "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
             "fwd_frac_of_peak": fwd_tf / peak_tf, "bwd_frac_of_peak": bwd_tf / peak_tf,
             "fwd_bwd_frac_of_peak": value / ws_n / peak_tf,
             "kernel_ms": {"fa_fwd_kernel": mean["fwd"], "fa_bwd_pre_kernel": mean["pre"],
                           bwd_name: mean["main"], "fa_bwd_convert_kernel": mean["post"]},
             "algorithmic_flops_per_step": flops_step,
-            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
+            "roofline": roofline, "per_config": per_config, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
             "gpu_launches": launches,
         }
         print(json.dumps(line), flush=True)
@@ -987,7 +1107,12 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--cpu-budget", type=float, default=12.0,
+                    help="seconds of repeated oracle calls behind cpu_baseline")
+    ap.add_argument("--cpu-tokens", type=int, default=4096,
+                    help="tokens of the one-head sample the oracle is timed on (both arms)")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the short timings of the other configurations")
     ap.add_argument("--fp8", action="store_true", help="measure the FP8 forward (d = 128 workloads)")
     ap.add_argument("--incoherent", action="store_true",
                     help="with --fp8: quantise Q and K with incoherent processing (Hadamard rotation)")

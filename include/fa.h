@@ -156,9 +156,10 @@ fa_status fa_quantize_fp8(const void *X, void *X8, float *scales, int B, int H, 
  * in fp32 (stages h = 1, 2, ..., d/2, each pair (i, i + h) becoming
  * (x_i + x_{i+h}, x_i - x_{i+h})).  Then as fa_quantize_fp8 without
  * transpose: codes X8 [B, H, N, d] and scales [B, H, ceil(N / 128)] of the
- * rotated values.  Since (Q s H)(K s H)^T = d Q K^T, fa_fwd_fp8 on rotated
- * Q and K takes softmax_scale / d.  V is quantised unrotated.  One kernel
- * launch, no workspace.
+ * rotated values.  Since (Q s H)(K s H)^T = d Q K^T, the forward on
+ * rotated Q and K is fa_fwd_fp8_rotated, which takes the softmax scale of
+ * the unrotated problem and removes the factor d itself.  V is quantised
+ * unrotated.  One kernel launch, no workspace.
  */
 fa_status fa_quantize_fp8_rotated(const void *X, void *X8, float *scales, const int8_t *signs, int B,
                                   int H, int N, int d, void *stream);
@@ -178,6 +179,22 @@ fa_status fa_fwd_fp8(const void *Q8, const void *K8, const void *Vt8, const floa
                      int d, float softmax_scale, int causal, const int32_t *key_len,
                      const uint8_t *block_mask, void *workspace, size_t workspace_bytes,
                      void *stream);
+
+/*
+ * FP8 forward after incoherent processing ("Attention" chapter of
+ * learn-kernels.com, FlashAttention-3 paragraph).  Q8, K8 and sQ, sK come
+ * from fa_quantize_fp8_rotated (the rows of Q and K rotated by diag(signs) H,
+ * with the same signs for both); Vt8, sV from fa_quantize_fp8 with
+ * transpose (V is not rotated).  softmax_scale is the scale of the
+ * unrotated attention (usually 1/sqrt(d)): the rotated scores carry a
+ * factor d ((Q s H)(K s H)^T = d Q K^T), which this call removes by running
+ * fa_fwd_fp8 with softmax_scale / d.  Everything else as fa_fwd_fp8.
+ */
+fa_status fa_fwd_fp8_rotated(const void *Q8, const void *K8, const void *Vt8, const float *sQ,
+                             const float *sK, const float *sV, void *O, float *LSE, int B, int H,
+                             int N, int d, float softmax_scale, int causal, const int32_t *key_len,
+                             const uint8_t *block_mask, void *workspace, size_t workspace_bytes,
+                             void *stream);
 
 /*
  * Backward for the loss sum(O * dO).  Q, K, V, O, dO: device bf16 [B, H, N, d]
@@ -246,7 +263,12 @@ fa_status fa_decode(const void *Q, const void *K, const void *V, void *O, float 
  * never loaded), 1 = full (no element masked), 2 = partial (element masks
  * applied).  Element set of tile (r, c): query rows i in [128r, 128r+128)
  * with i < N, key columns j in [128c, 128c+128); j >= N counts as masked.
- * Computed by the same device function that drives the skipping.
+ * Computed by the same device function the kernels take their full /
+ * partial decisions with, and checked on every tile against the rules the
+ * kernels skip with (without a block mask the forward visits a contiguous
+ * range of key tiles and the backward a contiguous range of query blocks,
+ * each found in O(1)): a tile where either rule disagrees with its class is
+ * written as 3, a value no correct plan contains.
  */
 fa_status fa_tile_plan(int B, int N, int causal, const int32_t *key_len,
                        const uint8_t *block_mask, uint8_t *plan, void *workspace,
@@ -292,8 +314,12 @@ fa_status fa_attention_host(const void *Q, const void *K, const void *V, const v
  *     example B*H*N > 130,000 rows at d = 128), return FA_ERR_WORKSPACE
  *     before anything is enqueued.
  *   - Allocates nothing.  The first call on a device looks up the array's
- *     device address once, with that device current; make that first call
- *     before any stream capture.
+ *     device address, with that device current, and keeps it for the
+ *     device's CUDA context (a context made after cudaDeviceReset gets a
+ *     new lookup); make that first call before any stream capture.
+ *   - Arguments are checked as fa_bwd checks them before the GPU is
+ *     touched: a rejected call enqueues nothing and leaves the array as it
+ *     was.
  *   - All calls share the array and see the previous call's contents; each
  *     call clears the status word and zeroes the accumulator first.  Calls
  *     that overlap on the GPU race on the array: serialise them.

@@ -85,6 +85,8 @@ def lib():
             L.fa_quantize_fp8_rotated.restype = i
             L.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp, vp, sz, vp]
             L.fa_fwd_fp8.restype = i
+            L.fa_fwd_fp8_rotated.argtypes = L.fa_fwd_fp8.argtypes
+            L.fa_fwd_fp8_rotated.restype = i
             L.fa_tile_plan.argtypes = [i, i, i, vp, vp, vp, vp, sz, vp]
             L.fa_tile_plan.restype = i
             L.fa_attention_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp,
@@ -104,7 +106,7 @@ def lib():
 
 EXPORTED = ("fa_tile_size", "fa_fwd_workspace_size", "fa_bwd_workspace_size", "fa_fwd", "fa_bwd",
             "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_postprocess", "fa_bwd_noalloc",
-            "fa_decode_workspace_size", "fa_decode", "fa_fwd_tiles", "fa_fwd_varlen", "fa_quantize_fp8", "fa_quantize_fp8_rotated", "fa_fwd_fp8",
+            "fa_decode_workspace_size", "fa_decode", "fa_fwd_tiles", "fa_fwd_varlen", "fa_quantize_fp8", "fa_quantize_fp8_rotated", "fa_fwd_fp8", "fa_fwd_fp8_rotated",
             "fa_tile_plan",
             "fa_host_workspace_size", "fa_attention_host", "fa_get_device_status", "fa_reset_device_status",
             "fa_selftest_wait_timeout", "fa_status_string")
@@ -204,6 +206,13 @@ def fa_fwd_fp8(Q8, K8, Vt8, sQ, sK, sV, O, LSE, B, H, N, d, softmax_scale, causa
     return lib().fa_fwd_fp8(_p(Q8), _p(K8), _p(Vt8), _p(sQ), _p(sK), _p(sV), _p(O), _p(LSE), B, H, N, d,
                             float(softmax_scale), int(bool(causal)), _p(key_len), _p(block_mask), _p(workspace),
                             int(workspace_bytes), _stream(stream))
+
+
+def fa_fwd_fp8_rotated(Q8, K8, Vt8, sQ, sK, sV, O, LSE, B, H, N, d, softmax_scale, causal, key_len, block_mask,
+                       workspace, workspace_bytes, stream=None) -> int:
+    return lib().fa_fwd_fp8_rotated(_p(Q8), _p(K8), _p(Vt8), _p(sQ), _p(sK), _p(sV), _p(O), _p(LSE), B, H, N, d,
+                                    float(softmax_scale), int(bool(causal)), _p(key_len), _p(block_mask),
+                                    _p(workspace), int(workspace_bytes), _stream(stream))
 
 
 def fa_bwd(Q, K, V, O, LSE, dO, dQ, dK, dV, B, H, N, d, softmax_scale, causal, key_len, block_mask,
@@ -336,23 +345,22 @@ def attention_forward_fp8(Q, K, V, softmax_scale=None, causal=False, key_len=Non
     """O, LSE of the FP8 forward on bf16 CUDA tensors [B, H, N, 128]: Q, K and V
     are block-quantised (fa_quantize_fp8), then fa_fwd_fp8 runs.  With signs
     (device int8 [d] of random +-1), Q and K are quantised with incoherent
-    processing (fa_quantize_fp8_rotated) and the scores' extra factor d is
-    taken out of the softmax scale."""
+    processing (fa_quantize_fp8_rotated) and fa_fwd_fp8_rotated runs (it takes
+    the scores' extra factor d out of the softmax scale)."""
     import torch
     B, H, N, d = _dims(Q)
     scale = (1.0 / d ** 0.5) if softmax_scale is None else softmax_scale
     Q8, sQ = quantize_fp8(Q, False, stream, signs)
     K8, sK = quantize_fp8(K, False, stream, signs)
     Vt8, sV = quantize_fp8(V, True, stream)
-    if signs is not None:
-        scale = scale / d
     O = torch.empty_like(Q)
     LSE = torch.empty((B, H, N), dtype=torch.float32, device=Q.device)
     need = fa_fwd_workspace_size(B, H, N, d)
     if ws is None:
         ws = workspace(need, Q.device)
-    _check(fa_fwd_fp8(Q8, K8, Vt8, sQ, sK, sV, O, LSE, B, H, N, d, scale, causal, key_len, block_mask, ws,
-                      ws.numel(), stream), "fa_fwd_fp8")
+    call, name = (fa_fwd_fp8, "fa_fwd_fp8") if signs is None else (fa_fwd_fp8_rotated, "fa_fwd_fp8_rotated")
+    _check(call(Q8, K8, Vt8, sQ, sK, sV, O, LSE, B, H, N, d, scale, causal, key_len, block_mask, ws,
+                ws.numel(), stream), name)
     if check_status:
         _check(fa_get_device_status(ws, stream), "fa_fwd_fp8 (device)")
     return O, LSE

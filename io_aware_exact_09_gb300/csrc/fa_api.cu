@@ -337,6 +337,17 @@ fa_status fa_fwd_fp8(const void *Q8, const void *K8, const void *Vt8, const floa
     return fa::launch_fwd_fp8(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+fa_status fa_fwd_fp8_rotated(const void *Q8, const void *K8, const void *Vt8, const float *sQ, const float *sK,
+                             const float *sV, void *O, float *LSE, int B, int H, int N, int d, float softmax_scale,
+                             int causal, const int32_t *key_len, const uint8_t *block_mask, void *workspace,
+                             size_t workspace_bytes, void *stream) {
+    if (!scale_ok(softmax_scale)) return FA_ERR_INVALID_ARGUMENT;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    // the rotated scores are d times the unrotated ones: (Q s H)(K s H)^T = d Q K^T
+    return fa_fwd_fp8(Q8, K8, Vt8, sQ, sK, sV, O, LSE, B, H, N, d, softmax_scale / (float)d, causal, key_len,
+                      block_mask, workspace, workspace_bytes, stream);
+}
+
 namespace {
 struct BwdWs {
     unsigned *status;
@@ -721,6 +732,16 @@ fa_status fa_attention_host(const void *Q, const void *K, const void *V, const v
     HostStreams streams(L.nchunks);
     HostStreams *hs = &streams;
     if (!hs->ok) return FA_ERR_CUDA;
+    // An error in the middle of queueing must not return while copies or
+    // kernels already queued still use the caller's buffers: wait for every
+    // side stream first, so that work the caller puts on `stream` afterwards
+    // is ordered after all of this call's work, as on success.
+    auto fail = [hs](fa_status e) -> fa_status {
+        cudaStreamSynchronize(hs->up);
+        cudaStreamSynchronize(hs->down);
+        for (int i = 0; i < hs->n; ++i) cudaStreamSynchronize(hs->comp[i]);
+        return e;
+    };
     {
         auto after = [](cudaEvent_t e, cudaStream_t from, cudaStream_t to) {
             return cudaEventRecord(e, from) == cudaSuccess && cudaStreamWaitEvent(to, e, 0) == cudaSuccess;
@@ -734,12 +755,12 @@ fa_status fa_attention_host(const void *Q, const void *K, const void *V, const v
         // everything starts after the work already on `stream`
         if (cudaEventRecord(hs->start, s) != cudaSuccess || cudaStreamWaitEvent(hs->up, hs->start, 0) != cudaSuccess ||
             cudaStreamWaitEvent(hs->down, hs->start, 0) != cudaSuccess)
-            return FA_ERR_CUDA;
+            return fail(FA_ERR_CUDA);
         for (int i = 0; i < L.nchunks; ++i)
-            if (cudaStreamWaitEvent(hs->comp[i], hs->start, 0) != cudaSuccess) return FA_ERR_CUDA;
+            if (cudaStreamWaitEvent(hs->comp[i], hs->start, 0) != cudaSuccess) return fail(FA_ERR_CUDA);
         // uploads: masks, then each chunk's Q, K, V, then each chunk's dO
-        if (key_len && !h2d(L.klen, key_len, (size_t)B * 4)) return FA_ERR_CUDA;
-        if (block_mask && !h2d(L.bmask, block_mask, nb * nb)) return FA_ERR_CUDA;
+        if (key_len && !h2d(L.klen, key_len, (size_t)B * 4)) return fail(FA_ERR_CUDA);
+        if (block_mask && !h2d(L.bmask, block_mask, nb * nb)) return fail(FA_ERR_CUDA);
         const size_t row_bytes = (size_t)d * 2;
         auto cbytes = [&](const HostChunk &c) { return (size_t)c.nb * c.nh * N * row_bytes; };
         auto at = [](const void *p, size_t off) { return static_cast<const uint8_t *>(p) + off; };
@@ -748,14 +769,14 @@ fa_status fa_attention_host(const void *Q, const void *K, const void *V, const v
             const size_t o = c.row0 * row_bytes, n = cbytes(c);
             if (!h2d(L.q + o, at(Q, o), n) || !h2d(L.k + o, at(K, o), n) || !h2d(L.v + o, at(V, o), n) ||
                 !after(hs->in[i], hs->up, hs->comp[i]))
-                return FA_ERR_CUDA;
+                return fail(FA_ERR_CUDA);
         }
         if (bwd)
             for (int i = 0; i < L.nchunks; ++i) {
                 const HostChunk &c = L.chunk[i];
                 const size_t o = c.row0 * row_bytes;
                 if (!h2d(L.dO + o, at(dO, o), cbytes(c)) || !after(hs->dO_in[i], hs->up, hs->comp[i]))
-                    return FA_ERR_CUDA;
+                    return fail(FA_ERR_CUDA);
             }
         // kernels: chunk i on compute stream i
         for (int i = 0; i < L.nchunks; ++i) {
@@ -768,26 +789,26 @@ fa_status fa_attention_host(const void *Q, const void *K, const void *V, const v
             const size_t ws_bytes = bwd ? fa_bwd_workspace_size(c.nb, c.nh, N, d) : fa_fwd_workspace_size(c.nb, c.nh, N, d);
             st = fa_fwd(w + L.q + o, w + L.k + o, w + L.v + o, w + L.o + o, lse, c.nb, c.nh, N, d, softmax_scale, causal,
                         kl, bm, ws, ws_bytes, hs->comp[i]);
-            if (st != FA_OK) return st;
-            if (!after(hs->fwd_done[i], hs->comp[i], hs->down)) return FA_ERR_CUDA;
+            if (st != FA_OK) return fail(st);
+            if (!after(hs->fwd_done[i], hs->comp[i], hs->down)) return fail(FA_ERR_CUDA);
             if (!d2h(static_cast<uint8_t *>(O) + o, L.o + o, cbytes(c)) ||
                 !d2h(LSE + c.row0, L.lse + c.row0 * 4, (size_t)c.nb * c.nh * N * 4))
-                return FA_ERR_CUDA;
+                return fail(FA_ERR_CUDA);
             if (bwd) {
                 st = fa_bwd(w + L.q + o, w + L.k + o, w + L.v + o, w + L.o + o, lse, w + L.dO + o, w + L.dQ + o,
                             w + L.dK + o, w + L.dV + o, c.nb, c.nh, N, d, softmax_scale, causal, kl, bm, ws, ws_bytes,
                             hs->comp[i]);
-                if (st != FA_OK) return st;
-                if (!after(hs->bwd_done[i], hs->comp[i], hs->down)) return FA_ERR_CUDA;
+                if (st != FA_OK) return fail(st);
+                if (!after(hs->bwd_done[i], hs->comp[i], hs->down)) return fail(FA_ERR_CUDA);
                 if (!d2h(static_cast<uint8_t *>(dQ) + o, L.dQ + o, cbytes(c)) ||
                     !d2h(static_cast<uint8_t *>(dK) + o, L.dK + o, cbytes(c)) ||
                     !d2h(static_cast<uint8_t *>(dV) + o, L.dV + o, cbytes(c)))
-                    return FA_ERR_CUDA;
+                    return fail(FA_ERR_CUDA);
             }
         }
         // the download stream has waited for every chunk's kernels, which waited
         // for every upload: `stream` resumes after the last download
-        if (!after(hs->down_done, hs->down, s)) return FA_ERR_CUDA;
+        if (!after(hs->down_done, hs->down, s)) return fail(FA_ERR_CUDA);
     }
     for (int i = 0; i < L.nchunks; ++i) {
         st = fa_get_device_status(w + L.attn_ws + L.chunk[i].ws_off, stream);

@@ -132,7 +132,7 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_kernel(const __grid_constant__ 
     // Without a block mask the query blocks that see this key tile are
     // exactly [qb_start, Tqb) (none when the tile lies past key_len): under
     // the causal mask the first block whose last row reaches k0.
-    const int qb_start = (k0 >= kvis) ? p.Tqb : (p.causal ? k0 / BQ : 0);
+    const int qb_start = bwd_query_block_begin(k0, kvis, p.causal, 0, BQ, p.Tqb);
     auto next_qb = [&](int qb) -> int {
         if (!p.block_mask) {
             const int nq = qb < qb_start ? qb_start : qb + 1;
@@ -581,7 +581,13 @@ __global__ void __launch_bounds__(256) fa_bwd_convert_kernel(const float *__rest
     }
 }
 
-// Tile plan export: the same tile_class the attention kernels skip with.
+// Tile plan export: the tile_class the attention kernels take their full /
+// partial decisions with, checked against the visit rules the kernels skip
+// tiles with.  With a block mask the kernels visit exactly the tiles whose
+// class is not skip; without one the forward visits the key tiles below
+// fwd_key_tile_end and the backward the query blocks from
+// bwd_query_block_begin.  A tile on which either rule disagrees with its
+// class is exported as kTileRuleMismatch, which no correct plan contains.
 __global__ void fa_plan_kernel(int B, int N, int T, int causal, const int32_t *key_len,
                                const uint8_t *block_mask, uint8_t *plan, unsigned *status) {
     const int64_t n = (int64_t)B * T * T;
@@ -594,8 +600,15 @@ __global__ void fa_plan_kernel(int B, int N, int T, int causal, const int32_t *k
         const int kvis = key_visible_bound(key_len, b, N, &bad);
         if (bad && qt == 0 && kt == 0 && atomicCAS(status, 0u, kStatusBadKeyLen) == 0u) atomicExch(status + 1, 0u);
         const int on = block_mask ? (block_mask[(size_t)qt * T + kt] != 0) : 1;
-        const int q0 = qt * kTile;
-        plan[idx] = (uint8_t)tile_class(q0, min(kTile, N - q0), kt * kTile, kTile, kvis, causal, on);
+        const int q0 = qt * kTile, qn = min(kTile, N - q0);
+        const unsigned c = tile_class(q0, qn, kt * kTile, kTile, kvis, causal, on);
+        bool fwd_visits = c != kTileSkip, bwd_visits = c != kTileSkip;
+        if (!block_mask) {
+            fwd_visits = kt < fwd_key_tile_end(q0, qn, kvis, causal, 0, kTile);
+            bwd_visits = qt >= bwd_query_block_begin(kt * kTile, kvis, causal, 0, kTile, T);
+        }
+        const bool agree = fwd_visits == (c != kTileSkip) && bwd_visits == (c != kTileSkip);
+        plan[idx] = (uint8_t)(agree ? c : kTileRuleMismatch);
     }
 }
 

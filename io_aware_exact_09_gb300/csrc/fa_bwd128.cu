@@ -126,7 +126,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
         const int on = p.block_mask ? (p.block_mask[(size_t)qb * nb + kt] != 0) : 1;
         return tile_class(qa, min(BQ, p.N - qa), k0, kTile, kvis, p.causal, on);
     };
-    const int qb_start = (k0 >= kvis) ? p.Tqb : (p.causal ? k0 / BQ : 0);
+    const int qb_start = bwd_query_block_begin(k0, kvis, p.causal, 0, BQ, p.Tqb);
     auto next_qb = [&](int qb) -> int {
         if (!p.block_mask) {
             const int nq = qb < qb_start ? qb_start : qb + 1;

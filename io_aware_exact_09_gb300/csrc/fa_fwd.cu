@@ -166,11 +166,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
     // its last row.  (tile_class below takes the same decision per tile.)
     int kend[2];
 #pragma unroll
-    for (int x = 0; x < 2; ++x) {
-        int lim = kvis;
-        if (p.causal) lim = min(lim, q0[x] + qn[x] + shift);
-        kend[x] = (qn[x] > 0 && lim > 0) ? (lim + BC - 1) / BC : 0;
-    }
+    for (int x = 0; x < 2; ++x) kend[x] = fwd_key_tile_end(q0[x], qn[x], kvis, p.causal, shift, BC);
     const int kend_union = max(kend[0], kend[1]);
     // per-query-tile values by selection, so that the arrays stay in registers
     auto q0_of = [&](int x) { return x ? q0[1] : q0[0]; };

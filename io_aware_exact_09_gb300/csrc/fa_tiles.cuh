@@ -13,6 +13,8 @@ namespace fa {
 
 constexpr int kTile = 128;           // query/key tile edge = block_mask block edge
 constexpr unsigned kTileSkip = 0, kTileFull = 1, kTilePartial = 2;
+// plan value for a tile whose class disagrees with a kernel's visit rule
+constexpr unsigned kTileRuleMismatch = 3;
 
 // Class of the tile of query rows [q0, q0 + qn) (all < N) and key columns
 // [k0, k0 + kw) (columns >= N count as masked): skip if every element is
@@ -39,6 +41,34 @@ __host__ __device__ __forceinline__ unsigned tile_class_shift(int q0, int qn, in
     if (causal && k0 > q_last + shift) return kTileSkip;
     const bool full = (k_last < kvis) && (!causal || k_last <= q0 + shift);
     return full ? kTileFull : kTilePartial;
+}
+
+// The kernels' own O(1) visit rules when there is no block mask (with a
+// block mask they test tile_class tile by tile).  fa_plan_kernel checks both
+// against tile_class on every tile, so the exported plan shows a wrong rule.
+//
+// Forward: the key tiles of width bc that the query tile [q0, q0 + qn) visits
+// are exactly [0, fwd_key_tile_end): keys below kvis and, under the causal
+// mask, at most the tile's last row + shift.
+__host__ __device__ __forceinline__ int fwd_key_tile_end(int q0, int qn, int kvis, int causal, int shift,
+                                                         int bc) {
+    int lim = kvis;
+    if (causal && q0 + qn + shift < lim) lim = q0 + qn + shift;
+    return (qn > 0 && lim > 0) ? (lim + bc - 1) / bc : 0;
+}
+
+// Backward: the query blocks of bq rows that see the key tile starting at k0
+// are exactly [bwd_query_block_begin, Tqb): none when the tile lies past
+// kvis; under the causal mask, from the first block whose last row reaches
+// k0 (+ shift for a bottom-right diagonal: row i sees key j iff j <= i + shift).
+__host__ __device__ __forceinline__ int bwd_query_block_begin(int k0, int kvis, int causal, int shift, int bq,
+                                                              int Tqb) {
+    if (k0 >= kvis) return Tqb;
+    if (!causal) return 0;
+    const int first_row = k0 - shift;          // the first query row that sees key k0
+    if (first_row <= 0) return 0;
+    const int qb = first_row / bq;
+    return qb < Tqb ? qb : Tqb;
 }
 
 // Visible-key bound for batch b: min(N, key_len[b]) with key_len clamped to

@@ -20,7 +20,7 @@ def free_port():
 def test_reference_arm_two_ranks_prints_one_line():
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
            "--master-addr", "127.0.0.1", "--master-port", str(free_port()),
-           "bench.py", "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "3"]
+           "bench.py", "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "3", "--cpu-tokens", "1024"]
     env = dict(os.environ, OMP_NUM_THREADS="2")
     r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600, env=env)
     assert r.returncode == 0, r.stderr[-2000:]
@@ -31,6 +31,8 @@ def test_reference_arm_two_ranks_prints_one_line():
     assert d["metric"] == "attention fwd+bwd TFLOP/s (bf16)" and d["unit"] == "TFLOP/s"
     assert d["higher_is_better"] is True and d["value"] > 0
     assert d["config"]["workload"] == "longctx_b1h16n16384d128"
+    assert d["config"]["parallelism"] == "replicas" and d["config"]["l2"] == "flushed between steps"
     cpu = d["cpu_baseline"]
+    assert "first 1024 tokens" in cpu["sample"]
     assert cpu["kind"] == "oracle" and cpu["value"] == d["value"] and cpu["cores"] >= 1 and cpu["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}

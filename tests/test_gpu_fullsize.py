@@ -92,6 +92,26 @@ def test_tile_plan_bit_exact_ragged(N):
                 assert np.array_equal(got.cpu().numpy(), ref), (N, causal, use_kl, use_bm)
 
 
+@pytest.mark.parametrize("N", [1, 127, 128, 129, 255, 256, 257, 640, 1000])
+def test_visit_rules_match_tile_classes_at_tile_edges(N):
+    """Without a block mask the forward visits a contiguous range of key tiles
+    and the backward a contiguous range of query blocks, each found in O(1);
+    the exported plan writes 3 wherever either range disagrees with the tile's
+    class.  Key lengths at, just below and just above every tile edge (and 0,
+    1, N), with and without the causal mask: the plan must equal the oracle's
+    brute-force enumeration, so a range one tile too long or too short fails."""
+    import io_aware_exact_09_gb300 as fa
+    edges = {0, 1, N} | {e + o for e in range(0, N + 1, 128) for o in (-1, 0, 1) if 0 <= e + o <= N}
+    kl = np.array(sorted(edges), np.int32)
+    for causal in (False, True):
+        for use_kl in (False, True):
+            B = len(kl) if use_kl else 2
+            got = fa.tile_plan(B, N, causal, torch.from_numpy(kl).cuda() if use_kl else None, None).cpu().numpy()
+            ref = oracle.tile_plan(B, N, causal, kl if use_kl else None, None)
+            assert not np.any(got == 3), (N, causal, use_kl)
+            assert np.array_equal(got, ref), (N, causal, use_kl)
+
+
 def test_host_buffer_path_matches_device_path():
     import io_aware_exact_09_gb300 as fa
     w = WORKLOADS["bertl_keypad_b16h16n512d64"]

@@ -2,16 +2,18 @@
 memory (a plug-in handed only its input and output buffers, code that must
 not call cudaMalloc where it runs).  It takes no workspace and uses the
 library's built-in scratch array instead.  It must give the same gradients
-as fa_bwd with a workspace on two calls in a row (the second call finds the
+as fa_bwd with a workspace, and agree with the fp64 oracle, on two calls in a row (the second call finds the
 first call's scratch contents and must clear what has to start at zero), and
 reject problems larger than the scratch before launching anything.
 
 Kept in a file of its own that pytest collects last, so that a run that
 stops at the first failure has already run every other test."""
+import numpy as np
 import pytest
 import torch
 
 import io_aware_exact_09_gb300 as fa
+import oracle
 from synthetic import make_case
 
 GRAD_REL_FRO = 1e-2   # the gradient bound the other parity tests use
@@ -35,6 +37,23 @@ def test_noalloc_rejects_oversize_before_any_gpu_work():
                             None, None, None) == 0
 
 
+def test_noalloc_rejects_bad_arguments_before_touching_the_gpu():
+    """A NaN or non-positive scale, a null or misaligned pointer: FA_ERR_INVALID_ARGUMENT
+    (1), returned before any CUDA call (here, on a machine without a GPU, a call
+    that reached the CUDA runtime would fail with FA_ERR_CUDA instead), so a
+    rejected call cannot clear the status word of a call still running."""
+    fa.build()
+    L = fa.lib()
+    ok = [256] * 9
+    for scale in (float("nan"), 0.0, -1.0, float("inf")):
+        assert L.fa_bwd_noalloc(*ok, 1, 2, 128, 64, scale, 0, None, None, None) == 1, scale
+    for k in range(9):
+        for bad in (None, 264):
+            args = list(ok)
+            args[k] = bad
+            assert L.fa_bwd_noalloc(*args, 1, 2, 128, 64, 0.125, 0, None, None, None) == 1, (k, bad)
+
+
 @pytest.mark.gpu
 @pytest.mark.parametrize("d", [64, 128])
 def test_noalloc_matches_workspace_backward_twice(d):
@@ -46,6 +65,10 @@ def test_noalloc_matches_workspace_backward_twice(d):
     O, LSE = fa.attention_forward(Q, K, V, scale, True, kl, None, check_status=True)
     rQ, rK, rV = fa.attention_backward(Q, K, V, O, LSE, dO, scale, True, kl, None, check_status=True)
     B, H, N, _ = Q.shape
+    f64 = lambda t: t.to(torch.float64).numpy()
+    _, _, odQ, odK, odV = oracle.attention_bwd(f64(c["Q"]), f64(c["K"]), f64(c["V"]), f64(c["dO"]), scale,
+                                                causal=True, key_len=c["key_len"].numpy())
+    orel = lambda got, ref: float(np.linalg.norm(got.double().cpu().numpy() - ref) / np.linalg.norm(ref))
     for call in range(2):
         dQ, dK, dV = (torch.full_like(Q, float("nan")) for _ in range(3))
         st = fa.fa_bwd_noalloc(Q, K, V, O, LSE, dO, dQ, dK, dV, B, H, N, d, scale, True, kl, None)
@@ -54,5 +77,8 @@ def test_noalloc_matches_workspace_backward_twice(d):
         for got, ref, name in ((dQ, rQ, "dQ"), (dK, rK, "dK"), (dV, rV, "dV")):
             assert bool(torch.isfinite(got).all()), (call, name)
             assert rel_fro(got, ref) <= GRAD_REL_FRO, (call, name, rel_fro(got, ref))
+        # and against the fp64 oracle directly, with the same bound
+        for got, ref, name in ((dQ, odQ, "dQ"), (dK, odK, "dK"), (dV, odV, "dV")):
+            assert orel(got, ref) <= GRAD_REL_FRO, (call, name, "oracle", orel(got, ref))
         # dK and dV are not accumulated across CTAs: identical to the workspace path
         assert torch.equal(dK, rK) and torch.equal(dV, rV), call
