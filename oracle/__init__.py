@@ -60,6 +60,8 @@ def _load():
             lib.oracle_tile_plan.argtypes = [i, i, i, ip, bp, i, i, i, bp]
             lib.oracle_decode.argtypes = [dp, dp, dp, i, i, i, i, i, dbl, i, ip, dp, dp]
             lib.oracle_decode.restype = ctypes.c_int
+            lib.oracle_bwd_rect.argtypes = [dp, dp, dp, dp, i, i, i, i, dbl, i, dp, dp, dp, dp, dp]
+            lib.oracle_bwd_rect.restype = ctypes.c_int
             lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
             lib.oracle_e4m3_encode.restype = ctypes.c_ubyte
             lib.oracle_e4m3_decode.argtypes = [ctypes.c_ubyte]
@@ -284,6 +286,64 @@ def attention_varlen(Q, K, V, cu_q, cu_k, scale, causal=False):
         O[q0:q1] = ob[0].transpose(1, 0, 2)
         LSE[:, q0:q1] = lb[0]
     return O, LSE
+
+
+def attention_bwd_rect(Q, K, V, dO, scale, causal=False):
+    """O, LSE, dQ, dK, dV of Nq query rows against Nk keys (fp64), the queries
+    being the last Nq positions (with causal, query i sees key j iff
+    j <= i + Nk - Nq).  Q, dO: [B, H, Nq, d]; K, V: [B, H, Nk, d]."""
+    lib = _load()
+    Q, K, V, dO = _f64(Q), _f64(K), _f64(V), _f64(dO)
+    if Q.ndim != 4 or K.shape != V.shape or K.ndim != 4 or Q.shape != dO.shape or Q.shape[:2] != K.shape[:2] \
+            or Q.shape[3] != K.shape[3]:
+        raise ValueError("expected Q, dO [B, H, Nq, d] and K, V [B, H, Nk, d]")
+    B, H, Nq, d = Q.shape
+    Nk = K.shape[2]
+    O = np.zeros((B, H, Nq, d), np.float64)
+    LSE = np.zeros((B, H, Nq), np.float64)
+    dQ = np.zeros((B, H, Nq, d), np.float64)
+    dK, dV = np.zeros((B, H, Nk, d), np.float64), np.zeros((B, H, Nk, d), np.float64)
+    c = ctypes.c_double
+    rc = lib.oracle_bwd_rect(_ptr(Q, c), _ptr(K, c), _ptr(V, c), _ptr(dO, c), B * H, Nq, Nk, d, float(scale),
+                             int(bool(causal)), _ptr(O, c), _ptr(LSE, c), _ptr(dQ, c), _ptr(dK, c), _ptr(dV, c))
+    if rc != 0:
+        raise RuntimeError("oracle_bwd_rect failed: %d" % rc)
+    return O, LSE, dQ, dK, dV
+
+
+def attention_varlen_bwd(Q, K, V, dO, cu_q, cu_k, scale, causal=False):
+    """Forward and backward of a ragged batch (packed sequences), fp64.
+
+    Layouts as attention_varlen: Q, dO [total_q, H, d], K, V [total_k, H, d],
+    offsets cu_q, cu_k [B + 1].  Each sequence is attended on its own, its Lq
+    queries being the last Lq of its Lk positions (bottom-right causal).
+    Returns O, dQ [total_q, H, d], LSE [H, total_q] and dK, dV [total_k, H, d];
+    a sequence without queries gets dK = dV = 0 for its keys, one without keys
+    O = dQ = 0 and LSE = -inf.  Each sequence goes through attention_bwd_rect
+    on its own slice."""
+    Q, K, V, dO = _f64(Q), _f64(K), _f64(V), _f64(dO)
+    cu_q = np.asarray(cu_q, np.int64)
+    cu_k = np.asarray(cu_k, np.int64)
+    if Q.ndim != 3 or K.ndim != 3 or K.shape != V.shape or Q.shape != dO.shape or Q.shape[1:] != K.shape[1:]:
+        raise ValueError("expected Q, dO [total_q, H, d] and K, V [total_k, H, d]")
+    if cu_q.shape != cu_k.shape or cu_q.ndim != 1 or cu_q[0] != 0 or cu_k[0] != 0 or \
+            cu_q[-1] != Q.shape[0] or cu_k[-1] != K.shape[0] or np.any(np.diff(cu_q) < 0) or np.any(np.diff(cu_k) < 0):
+        raise ValueError("cu_q / cu_k must be [B + 1] offsets from 0 to total, non-decreasing")
+    H = Q.shape[1]
+    O, dQ = np.zeros(Q.shape, np.float64), np.zeros(Q.shape, np.float64)
+    dK, dV = np.zeros(K.shape, np.float64), np.zeros(K.shape, np.float64)
+    LSE = np.full((H, Q.shape[0]), -np.inf, np.float64)
+    tr = lambda X, a, b: np.ascontiguousarray(X[a:b].transpose(1, 0, 2))[None]
+    for b in range(len(cu_q) - 1):
+        q0, q1, k0, k1 = int(cu_q[b]), int(cu_q[b + 1]), int(cu_k[b]), int(cu_k[b + 1])
+        ob, lb, dqb, dkb, dvb = attention_bwd_rect(tr(Q, q0, q1), tr(K, k0, k1), tr(V, k0, k1), tr(dO, q0, q1),
+                                                   scale, causal=causal)
+        O[q0:q1] = ob[0].transpose(1, 0, 2)
+        dQ[q0:q1] = dqb[0].transpose(1, 0, 2)
+        LSE[:, q0:q1] = lb[0]
+        dK[k0:k1] = dkb[0].transpose(1, 0, 2)
+        dV[k0:k1] = dvb[0].transpose(1, 0, 2)
+    return O, LSE, dQ, dK, dV
 
 
 E4M3_MAX = 448.0

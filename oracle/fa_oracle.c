@@ -460,6 +460,98 @@ int oracle_decode(const double *Q, const double *K, const double *V, int B, int 
 }
 
 /*
+ * Backward of decode-shaped attention: per (b, h), Nq query rows that are the
+ * last Nq positions of a sequence of Nk keys.  Key j is visible to query i
+ * iff j < Nk and, with the causal flag, j <= i + (Nk - Nq) (bottom-right
+ * alignment, as in oracle_decode without kv_len; Nq = Nk gives the square
+ * causal mask).  This is one sequence of a ragged batch ("Attention"
+ * chapter, serving paragraph: ragged layouts); the pages give no backward
+ * formulas, so they are the chain rule of the file header:
+ *   S = scale Q K^T (masked), P = row-softmax(S) (three passes), O = P V,
+ *   D_i = sum_t dO_it O_it,  dS = P o (dO V^T - D 1^T),
+ *   dQ = scale dS K,  dK = scale dS^T Q,  dV = P^T dO.
+ * Q, dO, O, dQ: [BH][Nq][d]; K, V, dK, dV: [BH][Nk][d]; LSE: [BH][Nq].
+ * A query row with no visible key has O = 0, LSE = -inf and a zero gradient.
+ */
+int oracle_bwd_rect(const double *Q, const double *K, const double *V, const double *dO, int BH, int Nq,
+                    int Nk, int d, double scale, int causal, double *O, double *LSE, double *dQ, double *dK,
+                    double *dV)
+{
+    if (BH < 0 || Nq < 0 || Nk < 0 || d <= 0) return -1;
+    const size_t nqk = (size_t)(Nq > 0 ? Nq : 1) * (size_t)(Nk > 0 ? Nk : 1);
+    double *P = (double *)malloc(sizeof(double) * nqk);
+    double *dS = (double *)malloc(sizeof(double) * nqk);
+    double *Dv = (double *)malloc(sizeof(double) * (size_t)(Nq > 0 ? Nq : 1));
+    if (!P || !dS || !Dv) {
+        free(P); free(dS); free(Dv);
+        return -2;
+    }
+    for (int64_t bh = 0; bh < BH; bh++) {
+        const double *Qh = Q + bh * (int64_t)Nq * d, *dOh = dO + bh * (int64_t)Nq * d;
+        const double *Kh = K + bh * (int64_t)Nk * d, *Vh = V + bh * (int64_t)Nk * d;
+        double *Oh = O + bh * (int64_t)Nq * d, *LSEh = LSE + bh * (int64_t)Nq;
+        double *dQh = dQ + bh * (int64_t)Nq * d;
+        double *dKh = dK + bh * (int64_t)Nk * d, *dVh = dV + bh * (int64_t)Nk * d;
+        /* S = scale Q K^T, masked; P = softmax(S) row by row; O = P V */
+#pragma omp parallel for schedule(static)
+        for (int i = 0; i < Nq; i++) {
+            double *p = P + (int64_t)i * Nk;
+            for (int j = 0; j < Nk; j++) {
+                if (causal && j > i + (Nk - Nq)) {
+                    p[j] = -INFINITY;
+                    continue;
+                }
+                double acc = 0.0;
+                for (int t = 0; t < d; t++) acc += Qh[(int64_t)i * d + t] * Kh[(int64_t)j * d + t];
+                p[j] = scale * acc;
+            }
+            LSEh[i] = safe_softmax_row(p, Nk);
+            double *o = Oh + (int64_t)i * d;
+            for (int t = 0; t < d; t++) o[t] = 0.0;
+            for (int j = 0; j < Nk; j++)
+                if (p[j] != 0.0)
+                    for (int t = 0; t < d; t++) o[t] += p[j] * Vh[(int64_t)j * d + t];
+            /* D_i = sum_t dO_it O_it */
+            double Di = 0.0;
+            for (int t = 0; t < d; t++) Di += dOh[(int64_t)i * d + t] * o[t];
+            Dv[i] = Di;
+        }
+        /* dS_ij = P_ij (<dO_i, V_j> - D_i) */
+#pragma omp parallel for schedule(static)
+        for (int i = 0; i < Nq; i++)
+            for (int j = 0; j < Nk; j++) {
+                double dp = 0.0;
+                for (int t = 0; t < d; t++) dp += dOh[(int64_t)i * d + t] * Vh[(int64_t)j * d + t];
+                dS[(int64_t)i * Nk + j] = P[(int64_t)i * Nk + j] * (dp - Dv[i]);
+            }
+        /* dQ = scale dS K */
+#pragma omp parallel for schedule(static)
+        for (int i = 0; i < Nq; i++)
+            for (int t = 0; t < d; t++) {
+                double acc = 0.0;
+                for (int j = 0; j < Nk; j++) acc += dS[(int64_t)i * Nk + j] * Kh[(int64_t)j * d + t];
+                dQh[(int64_t)i * d + t] = scale * acc;
+            }
+        /* dK = scale dS^T Q;  dV = P^T dO */
+#pragma omp parallel for schedule(static)
+        for (int j = 0; j < Nk; j++)
+            for (int t = 0; t < d; t++) {
+                double ak = 0.0, av = 0.0;
+                for (int i = 0; i < Nq; i++) {
+                    ak += dS[(int64_t)i * Nk + j] * Qh[(int64_t)i * d + t];
+                    av += P[(int64_t)i * Nk + j] * dOh[(int64_t)i * d + t];
+                }
+                dKh[(int64_t)j * d + t] = scale * ak;
+                dVh[(int64_t)j * d + t] = av;
+            }
+    }
+    free(P);
+    free(dS);
+    free(Dv);
+    return 0;
+}
+
+/*
  * FP8 block quantisation.  "FlashAttention: Mathematical Foundations ...",
  * section "Architectural Evolution" (FlashAttention-3 paragraph): the FP8
  * matmuls are block-quantised with dynamic scaling; "Attention" chapter

@@ -35,6 +35,11 @@ MUTANTS = {
     "e4m3 exponent bias 8": ("const int field = (E2 - 1) + 7;", "const int field = (E2 - 1) + 8;"),
     "fp8 scale for a 240 maximum": ("amax > 0.0f ? amax / 448.0f : 0.0f", "amax > 0.0f ? amax / 240.0f : 0.0f"),
     "fp8 transposed row stride": ("codes[(bh * d + c) * Np + r] = code;", "codes[(bh * d + c) * N + r] = code;"),
+    "rect backward causal top-left": ("if (causal && j > i + (Nk - Nq)) {", "if (causal && j > i) {"),
+    "rect dV from dS": ("av += P[(int64_t)i * Nk + j] * dOh[(int64_t)i * d + t];",
+                        "av += dS[(int64_t)i * Nk + j] * dOh[(int64_t)i * d + t];"),
+    "rect dK without scale": ("dKh[(int64_t)j * d + t] = scale * ak;\n                dVh[(int64_t)j * d + t] = av;\n            }\n    }",
+                              "dKh[(int64_t)j * d + t] = ak;\n                dVh[(int64_t)j * d + t] = av;\n            }\n    }"),
     "D without dO": ("acc += dOh[(int64_t)i * d + t] * Oh[(int64_t)i * d + t];",
                      "acc += Oh[(int64_t)i * d + t];"),
 }

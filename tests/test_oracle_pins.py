@@ -491,3 +491,88 @@ def test_varlen_rejects_bad_offsets():
         oracle.attention_varlen(Q, K, V, cu_q[::-1], cu_k, 0.5)
     with pytest.raises(ValueError):
         oracle.attention_varlen(Q, K, V, cu_q, cu_k[:-1], 0.5)
+
+
+# ---------------------------------------------------------------- ragged-batch backward
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_bwd_equals_square_oracle_per_sequence(causal):
+    """Lq = Lk: each packed sequence's O, LSE, dQ, dK, dV equal the square
+    oracle (pinned by finite differences and autograd) on that sequence alone."""
+    lens = [5, 1, 17, 0, 9]
+    H, d = 2, 8
+    Q, K, V, cu_q, cu_k = _packed(lens, lens, H, d, seed=41)
+    dO = np.random.default_rng(42).standard_normal(Q.shape)
+    O, L, dQ, dK, dV = oracle.attention_varlen_bwd(Q, K, V, dO, cu_q, cu_k, 0.35, causal=causal)
+    for b, n in enumerate(lens):
+        if n == 0:
+            continue
+        sl = slice(cu_q[b], cu_q[b + 1])
+        tr = lambda X: X[sl].transpose(1, 0, 2)[None]
+        rO, rL, rdQ, rdK, rdV = oracle.attention_bwd(tr(Q), tr(K), tr(V), tr(dO), 0.35, causal=causal)
+        back = lambda X: X[0].transpose(1, 0, 2)
+        for got, ref in ((O[sl], back(rO)), (dQ[sl], back(rdQ)), (dK[sl], back(rdK)), (dV[sl], back(rdV))):
+            assert np.max(np.abs(got - ref)) < 1e-12
+        assert np.max(np.abs(L[:, sl] - rL[0])) < 1e-12
+
+
+def test_varlen_bwd_matches_torch_autograd_bottom_right():
+    """Lq != Lk, causal, bottom-right (queries are the last positions): torch
+    fp64 autograd of softmax with the mask written out, sequence by sequence.
+    Includes a sequence with no queries, one with no keys, and one with
+    Lk < Lq whose first queries see no key (zero output, zero gradient)."""
+    lens_q, lens_k = [3, 7, 1, 0, 4, 5], [10, 7, 4, 3, 0, 2]
+    H, d, scale = 3, 16, 0.3
+    Q, K, V, cu_q, cu_k = _packed(lens_q, lens_k, H, d, seed=43)
+    dO = np.random.default_rng(44).standard_normal(Q.shape)
+    O, L, dQ, dK, dV = oracle.attention_varlen_bwd(Q, K, V, dO, cu_q, cu_k, scale, causal=True)
+    for b, (lq, lk) in enumerate(zip(lens_q, lens_k)):
+        sq, sk = slice(cu_q[b], cu_q[b + 1]), slice(cu_k[b], cu_k[b + 1])
+        t = lambda X, s: torch.from_numpy(X[s].transpose(1, 0, 2).copy()).requires_grad_(True)
+        q, k, v = t(Q, sq), t(K, sk), t(V, sk)
+        g = torch.from_numpy(dO[sq].transpose(1, 0, 2).copy())
+        i = torch.arange(lq)[:, None]
+        j = torch.arange(lk)[None, :]
+        s = (scale * q @ k.transpose(-1, -2)).masked_fill(~(j <= i + (lk - lq)), -math.inf)
+        p = torch.nan_to_num(torch.softmax(s, dim=-1), nan=0.0)
+        o = p @ v
+        if lq and lk:
+            (o * g).sum().backward()
+        grads = [x.grad if x.grad is not None else torch.zeros_like(x) for x in (q, k, v)]
+        back = lambda X: X.detach().numpy().transpose(1, 0, 2)
+        np.testing.assert_allclose(O[sq], back(o), atol=1e-10, rtol=0)
+        np.testing.assert_allclose(dQ[sq], back(grads[0]), atol=1e-10, rtol=0)
+        np.testing.assert_allclose(dK[sk], back(grads[1]), atol=1e-10, rtol=0)
+        np.testing.assert_allclose(dV[sk], back(grads[2]), atol=1e-10, rtol=0)
+        if lq > lk:
+            assert np.all(dQ[sq][: lq - lk] == 0) and np.all(np.isneginf(L[:, sq][:, : lq - lk]))
+
+
+def test_varlen_bwd_matches_central_finite_differences():
+    """Gradients of sum(O * dO) by central differences of the ragged forward
+    (itself pinned against torch's SDPA with the bottom-right mask)."""
+    lens_q, lens_k = [3, 2, 4], [5, 2, 3]
+    H, d, scale = 1, 4, 0.55
+    Q, K, V, cu_q, cu_k = _packed(lens_q, lens_k, H, d, seed=45)
+    dO = np.random.default_rng(46).standard_normal(Q.shape)
+    _, _, dQ, dK, dV = oracle.attention_varlen_bwd(Q, K, V, dO, cu_q, cu_k, scale, causal=True)
+
+    def loss():
+        O, _ = oracle.attention_varlen(Q, K, V, cu_q, cu_k, scale, causal=True)
+        return float(np.sum(O * dO))
+
+    h = 1e-5
+    for name, X, G in (("Q", Q, dQ), ("K", K, dK), ("V", V, dV)):
+        fd = np.zeros_like(X)
+        it = np.nditer(X, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            old = X[idx]
+            X[idx] = old + h
+            lp = loss()
+            X[idx] = old - h
+            lm = loss()
+            X[idx] = old
+            fd[idx] = (lp - lm) / (2 * h)
+        err = np.linalg.norm(fd - G) / max(np.linalg.norm(G), 1e-30)
+        assert err <= 1e-6, (name, err)
