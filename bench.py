@@ -33,9 +33,9 @@ seeded random sign vector, and the forward is ``fa_fwd_fp8_rotated``.
 (query rows per CTA 128 / 256 x key rows per tile 64 / 128) on the workload
 and prints one line with a ``sweep`` list (forward TFLOP/s per shape).
 
-``--workload varlen_...`` measures the ragged-batch forward (``fa_fwd_varlen``,
-packed sequences of uneven lengths): ``value`` is forward TFLOP/s over the
-visible (query, key) pairs.
+``--workload varlen_...`` measures a ragged batch (packed sequences of uneven
+lengths): one step = ``fa_fwd_varlen`` + ``fa_bwd_varlen``; ``value`` is
+forward+backward TFLOP/s over the visible (query, key) pairs.
 
 ``--workload decode_...`` measures the split-KV decode path instead: one step
 = one ``fa_decode`` call (a few new query rows per sequence against a
@@ -661,24 +661,25 @@ def run_tile_sweep(args):
 
 # ---------------------------------------------------------------- ragged batches
 def oracle_varlen_sample(w, budget_s: float):
-    """The fp64 oracle on sequence 0 of the ragged workload, one head, called
-    repeatedly for about budget_s: (TFLOP/s, cores, description)."""
+    """The fp64 oracle forward + backward of sequence 0 of the ragged workload,
+    one head, called repeatedly for about budget_s: (TFLOP/s, cores, description)."""
     import oracle
     from synthetic import make_varlen_inputs, varlen_fwd_flops
     c = make_varlen_inputs(w)
     cq, ck = c["cu_q"].numpy(), c["cu_k"].numpy()
     f = lambda X, a, b: X[a:b, 0:1].double().numpy().transpose(1, 0, 2)[None]
     q, k, v = f(c["Q"], cq[0], cq[1]), f(c["K"], ck[0], ck[1]), f(c["V"], ck[0], ck[1])
-    fl = varlen_fwd_flops([0, cq[1] - cq[0]], [0, ck[1] - ck[0]], 1, w.d, w.causal)
+    g = q * 0.5                       # any fixed dO of the right shape: the work does not depend on its values
+    fl = FWD_BWD_FACTOR * varlen_fwd_flops([0, cq[1] - cq[0]], [0, ck[1] - ck[0]], 1, w.d, w.causal)
     dts = []
     t_end = time.perf_counter() + budget_s
     while not dts or time.perf_counter() < t_end:
         t0 = time.perf_counter()
-        oracle.attention_decode(q, k, v, w.softmax_scale, causal=w.causal)
+        oracle.attention_bwd_rect(q, k, v, g, w.softmax_scale, causal=w.causal)
         dts.append(time.perf_counter() - t0)
     dt = sum(dts) / len(dts)
-    desc = ("fp64 oracle forward of sequence 0 (%d queries, %d keys), head 0, of %s, %d calls, %.3f s per call"
-            % (cq[1] - cq[0], ck[1] - ck[0], w.name, len(dts), dt))
+    desc = ("fp64 oracle forward + backward (materialised S and P) of sequence 0 (%d queries, %d keys), head 0, "
+            "of %s, %d calls, %.3f s per call" % (cq[1] - cq[0], ck[1] - ck[0], w.name, len(dts), dt))
     return fl / dt / 1e12, oracle.num_threads(), desc
 
 
@@ -694,79 +695,110 @@ def run_varlen(args, w):
     from synthetic import make_varlen_inputs, varlen_fwd_flops
     fa.build()
     c = make_varlen_inputs(w)
+    g = torch.Generator().manual_seed(w.seed + 1)
+    dO_h = torch.randn(c["Q"].shape, generator=g).to(torch.bfloat16)
     Q, K, V = (c[k].to(dev).contiguous() for k in ("Q", "K", "V"))
+    dO = dO_h.to(dev)
     cu_q, cu_k = c["cu_q"].to(dev), c["cu_k"].to(dev)
     B, H, d = w.B, w.H, w.d
     tq, tk = int(Q.shape[0]), int(K.shape[0])
+    max_k = int((c["cu_k"][1:] - c["cu_k"][:-1]).max())
     O = torch.empty_like(Q)
     LSE = torch.empty((H, tq), dtype=torch.float32, device=dev)
+    dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
     wsn = fa.fa_fwd_workspace_size(1, 1, 1, d)
     ws = fa.workspace(wsn, dev)
+    wsbn = fa.fa_bwd_varlen_workspace_size(H, tq, d)
+    wsb = fa.workspace(wsbn, dev)
     stream = torch.cuda.current_stream(dev)
     sp = stream.cuda_stream
-    flops = varlen_fwd_flops(c["cu_q"].tolist(), c["cu_k"].tolist(), H, d, w.causal)
+    flops_fwd = varlen_fwd_flops(c["cu_q"].tolist(), c["cu_k"].tolist(), H, d, w.causal)
+    flops = FWD_BWD_FACTOR * flops_fwd
 
     def check(st, where):
         if st != 0:
             raise RuntimeError("%s failed: %s" % (where, fa.fa_status_string(st)))
 
-    def step():
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+
+    def step(record):
+        if record:
+            ev[0].record(stream)
         check(fa.fa_fwd_varlen(Q, K, V, O, LSE, cu_q, cu_k, B, H, tq, tk, c["max_q"], d, w.softmax_scale, w.causal,
                                ws, wsn, sp), "fa_fwd_varlen")
+        if record:
+            ev[1].record(stream)
+        check(fa.fa_bwd_varlen(Q, K, V, O, LSE, dO, dQ, dK, dV, cu_q, cu_k, B, H, tq, tk, max_k, d, w.softmax_scale,
+                               w.causal, wsb, wsbn, sp), "fa_bwd_varlen")
+        if record:
+            ev[2].record(stream)
 
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     for _ in range(args.warmup):
-        step()
+        step(False)
     torch.cuda.synchronize(dev)
     check(fa.fa_get_device_status(ws, sp), "device status after warm-up")
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    check(fa.fa_get_device_status(wsb, sp), "device status after warm-up")
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
-    times = []
+    tf_, tb_, tstep = [], [], []
     barrier()
     torch.cuda.synchronize(dev)
     for _ in range(args.steps):
         flush.zero_()
-        e0.record(stream)
-        step()
-        e1.record(stream)
-        e1.synchronize()
-        times.append(e0.elapsed_time(e1))
+        step(True)
+        ev[2].synchronize()
+        tf_.append(ev[0].elapsed_time(ev[1]))
+        tb_.append(ev[1].elapsed_time(ev[2]))
+        tstep.append(ev[0].elapsed_time(ev[2]))
     torch.cuda.synchronize(dev)
     barrier()
     clk = clocks.stop()
     check(fa.fa_get_device_status(ws, sp), "device status after timing")
-    ms = reduce_max(sum(times) / len(times), dev)
+    check(fa.fa_get_device_status(wsb, sp), "device status after timing")
+    mf, mb, ms = (sum(x) / len(x) for x in (tf_, tb_, tstep))
+    ms = reduce_max(ms, dev)
     value = whole_job_tflops(flops, ws_n, ms / 1e3)
     peaks, peak_src = measured_peaks()
     peak, peak_kind = pick_peak(peaks, clk)
-    achieved = flops / (ms / 1e3) / 1e12
-    roofline = {"bound": "tensor", "kernel": "fa_fwd_kernel<%d, varlen>" % d, "achieved": achieved, "peak": peak,
-                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": ncu_traffic("fa_fwd_kernel_varlen", w.name),
+    fwd_tf = flops_fwd / (mf / 1e3) / 1e12
+    bwd_tf = 2.5 * flops_fwd / (mb / 1e3) / 1e12
+    # the dominant launch sequence of the step is the backward (three kernels)
+    dom_forward = mf >= mb
+    achieved = fwd_tf if dom_forward else bwd_tf
+    roofline = {"bound": "tensor",
+                "kernel": ("fa_fwd_kernel<%d, varlen>" % d) if dom_forward else
+                          ("fa_bwd_varlen (pre + %s<varlen> + convert)" % ("fa_bwd128_kernel" if d == 128 else
+                                                                           "fa_bwd_kernel")),
+                "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": ncu_traffic("fa_fwd_kernel_varlen", w.name) if dom_forward else None,
                 "peak_source": "%s %s" % (peak_src, peak_kind)}
     e2e = None
     if not args.no_e2e:
         pin = lambda t: t.contiguous().pin_memory()
-        Qh, Kh, Vh = (pin(c[k]) for k in ("Q", "K", "V"))
+        Qh, Kh, Vh, dOh = (pin(x) for x in (c["Q"], c["K"], c["V"], dO_h))
         Oh = torch.empty_like(Qh).pin_memory()
         Lh = torch.empty((H, tq), dtype=torch.float32).pin_memory()
+        dQh, dKh, dVh = torch.empty_like(Qh).pin_memory(), torch.empty_like(Kh).pin_memory(), \
+            torch.empty_like(Vh).pin_memory()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         et = []
         for i in range(1 + max(1, min(args.steps, 5))):
             e0.record(stream)
-            Q.copy_(Qh, non_blocking=True)
-            K.copy_(Kh, non_blocking=True)
-            V.copy_(Vh, non_blocking=True)
-            step()
-            Oh.copy_(O, non_blocking=True)
-            Lh.copy_(LSE, non_blocking=True)
+            for dst, src in ((Q, Qh), (K, Kh), (V, Vh), (dO, dOh)):
+                dst.copy_(src, non_blocking=True)
+            step(False)
+            for dst, src in ((Oh, O), (Lh, LSE), (dQh, dQ), (dKh, dK), (dVh, dV)):
+                dst.copy_(src, non_blocking=True)
             e1.record(stream)
             e1.synchronize()
             if i > 0:
                 et.append(e0.elapsed_time(e1))
         e_ms = reduce_max(sum(et) / len(et), dev)
         e2e = {"value": whole_job_tflops(flops, ws_n, e_ms / 1e3), "unit": "TFLOP/s",
-               "h2d_bytes_per_step": (tq + 2 * tk) * H * d * 2, "d2h_bytes_per_step": tq * H * d * 2 + H * tq * 4,
+               "h2d_bytes_per_step": (2 * tq + 2 * tk) * H * d * 2,
+               "d2h_bytes_per_step": (2 * tq + 2 * tk) * H * d * 2 + H * tq * 4,
                "ms_per_step": e_ms, "note": "cu_seqlens stay resident"}
     cpu = None
     if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
@@ -774,14 +806,16 @@ def run_varlen(args, w):
         cpu = {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc}
     if rank == 0:
         line = {
-            "metric": "attention fwd TFLOP/s (bf16, ragged batch)", "value": value, "unit": "TFLOP/s",
+            "metric": "attention fwd+bwd TFLOP/s (bf16, ragged batch)", "value": value, "unit": "TFLOP/s",
             "n_gpus": ws_n, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": w.name, "B": B, "H": H, "d": d, "total_q": tq, "total_k": tk,
-                       "max_seqlen_q": c["max_q"], "causal": w.causal,
+                       "max_seqlen_q": c["max_q"], "max_seqlen_k": max_k, "causal": w.causal,
                        "parallelism": "replicas" if ws_n > 1 else "single", "l2": "flushed between steps"},
+            "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf, "fwd_frac_of_peak": fwd_tf / peak,
+            "bwd_frac_of_peak": bwd_tf / peak, "kernel_ms": {"fa_fwd_varlen": mf, "fa_bwd_varlen": mb},
             "algorithmic_flops_per_step": flops, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "clocks": clk, "gpu_launches": args.steps,
+            "clocks": clk, "gpu_launches": 4 * args.steps,
         }
         print(json.dumps(line), flush=True)
     return 0
@@ -828,7 +862,7 @@ def run_reference(args):
             if i >= args.warmup:
                 vals.append(tf)
         v = statistics.median(vals)
-        print(json.dumps({"impl": "reference", "metric": "attention fwd TFLOP/s (bf16, ragged batch)", "value": v,
+        print(json.dumps({"impl": "reference", "metric": "attention fwd+bwd TFLOP/s (bf16, ragged batch)", "value": v,
                           "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
                           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                           "data": "synthetic", "config": {"workload": w.name, "B": w.B, "H": w.H, "d": w.d},

@@ -44,9 +44,13 @@
  *     returned before anything is enqueued.  Errors found on the device (a
  *     wait that timed out, a bad key_len) are written to the first word of
  *     the workspace and read back with fa_get_device_status().
- *   - The workspace must be zero-filled once before its first use (or reset
- *     with fa_reset_device_status()); the library only ever sets its status
- *     word, never clears it.
+ *   - The workspace must be zero-filled once before its first use.  Word 0
+ *     is the status word, which the library only ever sets, never clears
+ *     (fa_reset_device_status() clears it).  The forward kernels hand out
+ *     their work items from a counter in words 2 and 3, which every launch
+ *     leaves at zero again.  A workspace therefore serves one call at a
+ *     time: calls that may run concurrently (different streams) need
+ *     workspaces of their own.
  *   - No entry point throws or exits; there is no CPU fallback.
  */
 #ifndef FA_GB300_H
@@ -72,7 +76,8 @@ typedef enum {
 /* Size of the 128 x 128 tile (and of a block_mask block). */
 int fa_tile_size(void);
 
-/* Bytes of device workspace fa_fwd needs: the status word (256 bytes). */
+/* Bytes of device workspace fa_fwd needs (256): the status word and the
+ * work-item counter of the persistent forward grid. */
 size_t fa_fwd_workspace_size(int B, int H, int N, int d);
 
 /* Bytes of device workspace fa_bwd needs: the status word, the fp32 row
@@ -84,7 +89,10 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d);
  * Forward.  Q, K, V: device bf16 [B, H, N, d] (read).  O: device bf16
  * [B, H, N, d] (written).  LSE: device fp32 [B, H, N] (written, natural log:
  * P_ij = exp(softmax_scale * q_i.k_j - LSE_i) for visible keys).
- * One kernel launch.
+ * One kernel launch: a persistent grid of at most one CTA per SM taking
+ * (pair of 128-row query tiles, b, h) work items from the workspace
+ * counter.  With a block_mask, N may be at most 2048 * 128 (the key tiles of
+ * a row are listed in shared memory), else FA_ERR_UNSUPPORTED.
  */
 fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H,
                  int N, int d, float softmax_scale, int causal, const int32_t *key_len,
@@ -129,6 +137,31 @@ fa_status fa_fwd_varlen(const void *Q, const void *K, const void *V, void *O, fl
                         const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int B, int H,
                         int total_q, int total_k, int max_seqlen_q, int d, float softmax_scale,
                         int causal, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Backward of a ragged batch (the layout of fa_fwd_varlen) for the loss
+ * sum(O * dO): the gradients of each packed sequence on its own, with the
+ * same bottom-right causal alignment (query i of a sequence sees key j iff
+ * j <= i + Lk - Lq).  Q, O, dO: device bf16 [total_q, H, d] (read); K, V:
+ * device bf16 [total_k, H, d] (read); LSE: device fp32 [H, total_q] from
+ * fa_fwd_varlen with the same arguments (read).  dQ: device bf16
+ * [total_q, H, d]; dK, dV: device bf16 [total_k, H, d] (written; the keys of
+ * a sequence without queries get zero gradients).  cu_seqlens_q,
+ * cu_seqlens_k: device int32 [B + 1] offsets as for fa_fwd_varlen.
+ * max_seqlen_k (host): at least the longest key length (it sizes the grid).
+ * An invalid sequence (offsets outside [0, total], a negative length, a key
+ * length beyond max_seqlen_k rounded up to whole 128-row tiles) is skipped
+ * and FA_ERR_DEVICE_BAD_KEY_LEN recorded in the workspace status word.
+ * Workspace: fa_bwd_varlen_workspace_size(H, total_q, d) bytes (status
+ * word, D = rowsum(dO * O) and the fp32 dQ accumulator, [total_q, H] rows).
+ * Three kernel launches, as fa_bwd.
+ */
+size_t fa_bwd_varlen_workspace_size(int H, int total_q, int d);
+fa_status fa_bwd_varlen(const void *Q, const void *K, const void *V, const void *O, const float *LSE,
+                        const void *dO, void *dQ, void *dK, void *dV, const int32_t *cu_seqlens_q,
+                        const int32_t *cu_seqlens_k, int B, int H, int total_q, int total_k,
+                        int max_seqlen_k, int d, float softmax_scale, int causal, void *workspace,
+                        size_t workspace_bytes, void *stream);
 
 /*
  * FP8 block quantisation ("FlashAttention: Mathematical Foundations ...",

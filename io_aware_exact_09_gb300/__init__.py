@@ -79,6 +79,10 @@ def lib():
             L.fa_fwd_tiles.restype = i
             L.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, sz, vp]
             L.fa_fwd_varlen.restype = i
+            L.fa_bwd_varlen_workspace_size.argtypes = [i, i, i]
+            L.fa_bwd_varlen_workspace_size.restype = sz
+            L.fa_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, sz, vp]
+            L.fa_bwd_varlen.restype = i
             L.fa_quantize_fp8.argtypes = [vp, vp, vp, i, i, i, i, i, vp]
             L.fa_quantize_fp8.restype = i
             L.fa_quantize_fp8_rotated.argtypes = [vp, vp, vp, vp, i, i, i, i, vp]
@@ -106,7 +110,8 @@ def lib():
 
 EXPORTED = ("fa_tile_size", "fa_fwd_workspace_size", "fa_bwd_workspace_size", "fa_fwd", "fa_bwd",
             "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_postprocess", "fa_bwd_noalloc",
-            "fa_decode_workspace_size", "fa_decode", "fa_fwd_tiles", "fa_fwd_varlen", "fa_quantize_fp8", "fa_quantize_fp8_rotated", "fa_fwd_fp8", "fa_fwd_fp8_rotated",
+            "fa_decode_workspace_size", "fa_decode", "fa_fwd_tiles", "fa_fwd_varlen", "fa_bwd_varlen_workspace_size",
+            "fa_bwd_varlen", "fa_quantize_fp8", "fa_quantize_fp8_rotated", "fa_fwd_fp8", "fa_fwd_fp8_rotated",
             "fa_tile_plan",
             "fa_host_workspace_size", "fa_attention_host", "fa_get_device_status", "fa_reset_device_status",
             "fa_selftest_wait_timeout", "fa_status_string")
@@ -191,6 +196,36 @@ def attention_varlen(Q, K, V, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, softmax_
     if check_status:
         _check(fa_get_device_status(ws, stream), "fa_fwd_varlen (device)")
     return O, LSE
+
+
+def fa_bwd_varlen_workspace_size(H, total_q, d) -> int:
+    return lib().fa_bwd_varlen_workspace_size(H, total_q, d)
+
+
+def fa_bwd_varlen(Q, K, V, O, LSE, dO, dQ, dK, dV, cu_seqlens_q, cu_seqlens_k, B, H, total_q, total_k, max_seqlen_k,
+                  d, softmax_scale, causal, workspace, workspace_bytes, stream=None) -> int:
+    return lib().fa_bwd_varlen(_p(Q), _p(K), _p(V), _p(O), _p(LSE), _p(dO), _p(dQ), _p(dK), _p(dV),
+                               _p(cu_seqlens_q), _p(cu_seqlens_k), B, H, total_q, total_k, max_seqlen_k, d,
+                               float(softmax_scale), int(bool(causal)), _p(workspace), int(workspace_bytes),
+                               _stream(stream))
+
+
+def attention_varlen_backward(Q, K, V, O, LSE, dO, cu_seqlens_q, cu_seqlens_k, max_seqlen_k, softmax_scale=None,
+                              causal=False, ws=None, stream=None, check_status=False):
+    """dQ [total_q, H, d], dK, dV [total_k, H, d] = fa_bwd_varlen(...) on bf16 CUDA tensors."""
+    import torch
+    total_q, H, d = (int(x) for x in Q.shape)
+    total_k = int(K.shape[0])
+    B = int(cu_seqlens_q.numel()) - 1
+    scale = (1.0 / d ** 0.5) if softmax_scale is None else softmax_scale
+    dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
+    if ws is None:
+        ws = workspace(fa_bwd_varlen_workspace_size(H, total_q, d), Q.device)
+    _check(fa_bwd_varlen(Q, K, V, O, LSE, dO, dQ, dK, dV, cu_seqlens_q, cu_seqlens_k, B, H, total_q, total_k,
+                         max_seqlen_k, d, scale, causal, ws, ws.numel(), stream), "fa_bwd_varlen")
+    if check_status:
+        _check(fa_get_device_status(ws, stream), "fa_bwd_varlen (device)")
+    return dQ, dK, dV
 
 
 def fa_quantize_fp8(X, X8, scales, B, H, N, d, transpose, stream=None) -> int:

@@ -102,6 +102,20 @@ bool encode_f32_3d(CUtensorMap *m, const void *ptr, int d, int N, int BH, int bo
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D fp32 view [total][H][d] of a ragged batch's dQ accumulator; box of
+// 32 columns of one head x box_rows rows, 128-byte swizzle.
+bool encode_f32_thd(CUtensorMap *m, const void *ptr, int d, int H, int total, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)total};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)H * d * 4};
+    cuuint32_t box[3] = {32, 1, (cuuint32_t)box_rows};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Checks shared by fa_fwd / fa_bwd / fa_tile_plan.  Returns FA_OK, or the
 // error to report; *empty is set when there is nothing to compute.
 fa_status check_sizes(int B, int H, int N, int d, bool *empty) {
@@ -121,6 +135,10 @@ fa_status check_sizes(int B, int H, int N, int d, bool *empty) {
 }
 
 bool scale_ok(float s) { return std::isfinite(s) && s > 0.f; }
+
+// The forward lists an item's key tiles in shared memory under a block mask
+// (at most this many tiles per row).
+constexpr int kFwdMaxMaskedKeyTiles = 2048;
 
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -167,6 +185,7 @@ fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LS
         return FA_ERR_INVALID_ARGUMENT;
     if (!workspace || !aligned16(workspace) || workspace_bytes < fa_fwd_workspace_size(B, H, N, d))
         return FA_ERR_WORKSPACE;
+    if (block_mask && (N + 127) / 128 > kFwdMaxMaskedKeyTiles) return FA_ERR_UNSUPPORTED;
 
     FwdParams p;
     std::memset(&p, 0, sizeof(p));
@@ -204,6 +223,7 @@ fa_status fa_fwd_tiles(const void *Q, const void *K, const void *V, void *O, flo
         return FA_ERR_INVALID_ARGUMENT;
     if (!workspace || !aligned16(workspace) || workspace_bytes < fa_fwd_workspace_size(B, H, N, d))
         return FA_ERR_WORKSPACE;
+    if (block_mask && (N + block_k - 1) / block_k > kFwdMaxMaskedKeyTiles) return FA_ERR_UNSUPPORTED;
     FwdParams p;
     std::memset(&p, 0, sizeof(p));
     const int BH = B * H;
@@ -452,6 +472,79 @@ fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, con
                      workspace_bytes, stream);
     if (st != FA_OK) return st;
     return fa_bwd_postprocess(dQ, B, H, N, d, softmax_scale, workspace, workspace_bytes, stream);
+}
+
+size_t fa_bwd_varlen_workspace_size(int H, int total_q, int d) {
+    if (H < 0 || total_q < 0 || d <= 0) return 0;
+    return fa_bwd_workspace_size(1, H, total_q, d);
+}
+
+fa_status fa_bwd_varlen(const void *Q, const void *K, const void *V, const void *O, const float *LSE, const void *dO,
+                        void *dQ, void *dK, void *dV, const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int B,
+                        int H, int total_q, int total_k, int max_seqlen_k, int d, float softmax_scale, int causal,
+                        void *workspace, size_t workspace_bytes, void *stream) {
+    if (B < 0 || H <= 0 || total_q < 0 || total_k < 0 || max_seqlen_k < 0) return FA_ERR_INVALID_ARGUMENT;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (!scale_ok(softmax_scale)) return FA_ERR_INVALID_ARGUMENT;
+    if (B == 0 || (total_q == 0 && total_k == 0)) return FA_OK;
+    const int64_t Tk = ((int64_t)max_seqlen_k + 127) / 128;
+    if ((int64_t)B * H > INT_MAX || Tk * B * H > INT_MAX) return FA_ERR_UNSUPPORTED;
+    if ((int64_t)total_q * H * d * 4 >= (int64_t(1) << 40) || (int64_t)total_k * H * d * 2 >= (int64_t(1) << 40))
+        return FA_ERR_UNSUPPORTED;
+    if (!cu_seqlens_q || !cu_seqlens_k) return FA_ERR_INVALID_ARGUMENT;
+    if (total_q > 0) {
+        const void *ptrs[] = {Q, O, LSE, dO, dQ};
+        for (const void *x : ptrs)
+            if (!x || !aligned16(x)) return FA_ERR_INVALID_ARGUMENT;
+    }
+    if (total_k > 0) {
+        const void *ptrs[] = {K, V, dK, dV};
+        for (const void *x : ptrs)
+            if (!x || !aligned16(x)) return FA_ERR_INVALID_ARGUMENT;
+    }
+    if (!workspace || !aligned16(workspace) || workspace_bytes < fa_bwd_varlen_workspace_size(H, total_q, d))
+        return FA_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const BwdWs w = bwd_ws(workspace, 1, H, total_q);
+    // D = rowsum(dO * O) and the accumulator zeroed, over the [total_q][H] rows
+    if (total_q > 0 &&
+        fa::launch_bwd_pre(d, O, dO, w.Dvec, w.dQacc, (int64_t)total_q * H, s) != cudaSuccess)
+        return FA_ERR_CUDA;
+    if (total_k > 0 && Tk > 0) {
+        BwdParams p;
+        std::memset(&p, 0, sizeof(p));
+        // without queries the maps still need a valid base: point them at K
+        // (no query block is ever loaded then)
+        const void *Qm = total_q > 0 ? Q : K, *dOm = total_q > 0 ? dO : K;
+        const int tq = total_q > 0 ? total_q : total_k;
+        if (!encode_bf16_thd(&p.tmQ, Qm, d, H, tq, 128) || !encode_bf16_thd(&p.tmdO, dOm, d, H, tq, 128) ||
+            !encode_bf16_thd(&p.tmK, K, d, H, total_k, 128) || !encode_bf16_thd(&p.tmV, V, d, H, total_k, 128) ||
+            !encode_f32_thd(&p.tmdQ, total_q > 0 ? (const void *)w.dQacc : K, d, H, tq, fa::bwd_dq_box_rows(d)))
+            return FA_ERR_CUDA;
+        p.LSE = LSE;
+        p.Dvec = w.Dvec;
+        p.dQacc = w.dQacc;
+        p.dK = dK;
+        p.dV = dV;
+        p.cu_q = cu_seqlens_q;
+        p.cu_k = cu_seqlens_k;
+        p.total_q = total_q;
+        p.total_k = total_k;
+        p.status = w.status;
+        p.H = H;
+        p.N = 0;
+        p.BH = B * H;
+        p.Tk = (int)Tk;
+        p.Tqb = 0;
+        p.causal = causal ? 1 : 0;
+        p.scale_log2 = softmax_scale * kLog2e;
+        p.scale = softmax_scale;
+        if (fa::launch_bwd_main_varlen(d, p, s) != cudaSuccess) return FA_ERR_CUDA;
+    }
+    if (total_q > 0 &&
+        fa::launch_bwd_convert(d, w.dQacc, dQ, (int64_t)total_q * H * d, softmax_scale, s) != cudaSuccess)
+        return FA_ERR_CUDA;
+    return FA_OK;
 }
 
 // ------------------------------------------------------------------ decode (split KV)

@@ -34,6 +34,8 @@
 //      kernel, fa_bwd128.cu.
 //   3. fa_bwd_convert: dQ = bf16(scale * dQacc)                        (HBM-bound)
 // The preprocessing and conversion kernels serve both head dimensions.
+#include <climits>
+
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
 
@@ -94,7 +96,7 @@ __device__ __forceinline__ void drain_wait_b(uint32_t bar, uint32_t parity) {
         if (globaltimer_ns() - t0 > FA_WAIT_TIMEOUT_NS) break;
 }
 
-template <int D>
+template <int D, bool VARLEN>
 __global__ void __launch_bounds__(384, 1) fa_bwd_kernel(const __grid_constant__ BwdParams p) {
     using S = BwdShape<D>;
     constexpr int BQ = S::BQ;
@@ -110,7 +112,7 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_kernel(const __grid_constant__ 
     // tiles (lowest index) start first
     const int kt = (int)(blockIdx.x % p.Tk);
     const int bh = (int)(blockIdx.x / p.Tk);
-    const int b = bh / p.H;
+    const int b = bh / p.H, h = bh % p.H;
     const int k0 = kt * kTile;
     const int nb = (p.N + kTile - 1) / kTile;
 
@@ -119,28 +121,60 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_kernel(const __grid_constant__ 
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sb + S::OFF_MISC + 4);
     const Guard g{p.status, p.status + 1, abort_flag};
 
+    // the sequence: query rows [q_start, q_start + Lq), key rows [k_start,
+    // k_start + Lk); in the square [B, H, N, d] case both are [0, N).  Under
+    // the causal mask query i sees key j iff j <= i + shift (shift = Lk - Lq,
+    // 0 for the square case: a ragged sequence's queries are its last ones).
+    int q_start = 0, k_start = 0, Lq = p.N, Lk = p.N, Tqb = p.Tqb;
     bool bad = false;
-    const int kvis = key_visible_bound(p.key_len, b, p.N, &bad);
-    if (bad && threadIdx.x == 0 && kt == 0 && (bh % p.H) == 0) record_status(g, kStatusBadKeyLen, 0);
+    if constexpr (VARLEN) {
+        varlen_sequence(p.cu_q, p.cu_k, b, p.total_q, p.total_k, INT_MAX, p.Tk * kTile, &q_start, &Lq, &k_start,
+                        &Lk, &bad);
+        Tqb = (Lq + BQ - 1) / BQ;
+    }
+    const int shift = Lk - Lq;
+    const int kvis = VARLEN ? Lk : key_visible_bound(p.key_len, b, p.N, &bad);
+    if (bad && threadIdx.x == 0 && kt == 0 && h == 0) record_status(g, kStatusBadKeyLen, 0);
+    // a ragged batch's grid covers its longest key sequence: a key tile past
+    // this sequence's end has no dK, dV row to write and leaves before any
+    // set-up (the whole CTA takes this branch together)
+    if (VARLEN && k0 >= Lk) return;
 
     // class of query block qb (BQ rows) against this key tile
     auto cls = [&](int qb) -> unsigned {
         const int qa = qb * BQ;
+        if constexpr (VARLEN) return tile_class_shift(qa, min(BQ, Lq - qa), k0, kTile, kvis, p.causal, shift);
         const int on = p.block_mask ? (p.block_mask[(size_t)(qa / kTile) * nb + kt] != 0) : 1;
         return tile_class(qa, min(BQ, p.N - qa), k0, kTile, kvis, p.causal, on);
     };
     // Without a block mask the query blocks that see this key tile are
     // exactly [qb_start, Tqb) (none when the tile lies past key_len): under
-    // the causal mask the first block whose last row reaches k0.
-    const int qb_start = bwd_query_block_begin(k0, kvis, p.causal, 0, BQ, p.Tqb);
+    // the causal mask the first block whose last row reaches k0 - shift.
+    const int qb_start = bwd_query_block_begin(k0, kvis, p.causal, shift, BQ, Tqb);
     auto next_qb = [&](int qb) -> int {
-        if (!p.block_mask) {
+        if (VARLEN || !p.block_mask) {
             const int nq = qb < qb_start ? qb_start : qb + 1;
-            return nq < p.Tqb ? nq : p.Tqb;
+            return nq < Tqb ? nq : Tqb;
         }
-        for (int x = qb + 1; x < p.Tqb; ++x)
+        for (int x = qb + 1; x < Tqb; ++x)
             if (cls(x) != kTileSkip) return x;
-        return p.Tqb;
+        return Tqb;
+    };
+    // TMA coordinates: the [B*H][N][d] view, or the [total][H][d] view of a
+    // ragged batch (warp-collective: the producer warp calls it uniformly)
+    auto tload = [&](uint32_t dst, const CUtensorMap *m, uint32_t mbar, int c, int row, int start) {
+        if constexpr (VARLEN)
+            tma_load_3d_elect(dst, m, mbar, c * 64, h, start + row);
+        else
+            tma_load_3d_elect(dst, m, mbar, c * 64, row, bh);
+    };
+    // index of query row qq of this sequence in LSE ([BH][N] or [H][total_q])
+    // and in D ([BH][N] or [total_q][H])
+    auto lse_index = [&](int qq) -> size_t {
+        return VARLEN ? (size_t)h * p.total_q + q_start + qq : (size_t)bh * p.N + qq;
+    };
+    auto d_index = [&](int qq) -> size_t {
+        return VARLEN ? (size_t)(q_start + qq) * p.H + h : (size_t)bh * p.N + qq;
     };
 
     if (threadIdx.x == 0) {
@@ -182,43 +216,40 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_kernel(const __grid_constant__ 
 
     if (warp == 0) {
         // ---------------------------------------------------------- producer
-        // lane 0 issues the TMA copies; the whole warp stages LSE and D of
-        // the same query block into shared memory one stage ahead.
-        if (first < p.Tqb) {
-            if (lane == 0) {
-                mbar_arrive_expect_tx(bar(S::B_KV), 2 * S::KV_BYTES);
-                for (int c = 0; c < S::CHUNKS; ++c) {
-                    tma_load_3d(base + S::OFF_K + c * S::KV_CHUNK, &p.tmK, bar(S::B_KV), c * 64, k0, bh);
-                    tma_load_3d(base + S::OFF_V + c * S::KV_CHUNK, &p.tmV, bar(S::B_KV), c * 64, k0, bh);
-                }
+        // one elected lane issues the TMA copies; the whole warp stages LSE
+        // and D of the same query block into shared memory one stage ahead.
+        if (first < Tqb) {
+            mbar_arrive_expect_tx_elect(bar(S::B_KV), 2 * S::KV_BYTES);
+            for (int c = 0; c < S::CHUNKS; ++c) {
+                tload(base + S::OFF_K + c * S::KV_CHUNK, &p.tmK, bar(S::B_KV), c, k0, k_start);
+                tload(base + S::OFF_V + c * S::KV_CHUNK, &p.tmV, bar(S::B_KV), c, k0, k_start);
             }
             int i = 0;
             bool ok = true;
-            for (int qb = first; qb < p.Tqb; qb = next_qb(qb), ++i) {
+            for (int qb = first; qb < Tqb; qb = next_qb(qb), ++i) {
                 const int s = i & 1;
                 if (!mbar_wait_warp(bar(S::B_QEMPTY + s), ((uint32_t)(i >> 1) & 1u) ^ 1u, g, 0x111)) {
                     ok = false;
                     break;
                 }
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(bar(S::B_QFULL + s), 2 * S::Q_BYTES);
-                    for (int c = 0; c < S::CHUNKS; ++c) {
-                        tma_load_3d(base + S::OFF_Q + s * S::Q_BYTES + c * S::Q_CHUNK, &p.tmQ,
-                                    bar(S::B_QFULL + s), c * 64, qb * BQ, bh);
-                        tma_load_3d(base + S::OFF_DO + s * S::Q_BYTES + c * S::Q_CHUNK, &p.tmdO,
-                                    bar(S::B_QFULL + s), c * 64, qb * BQ, bh);
-                    }
+                mbar_arrive_expect_tx_elect(bar(S::B_QFULL + s), 2 * S::Q_BYTES);
+                for (int c = 0; c < S::CHUNKS; ++c) {
+                    tload(base + S::OFF_Q + s * S::Q_BYTES + c * S::Q_CHUNK, &p.tmQ, bar(S::B_QFULL + s), c, qb * BQ,
+                          q_start);
+                    tload(base + S::OFF_DO + s * S::Q_BYTES + c * S::Q_CHUNK, &p.tmdO, bar(S::B_QFULL + s), c,
+                          qb * BQ, q_start);
                 }
-                // LSE in the log2 domain (+inf past N or for a row with no
-                // visible key: its P is 0) and D for the block's rows
+                // LSE in the log2 domain (+inf past the sequence's last query
+                // or for a row with no visible key: its P is 0) and D for the
+                // block's rows
                 const int qa = qb * BQ;
                 for (int t = lane; t < BQ; t += 32) {
                     const int qq = qa + t;
                     float v = INFINITY, dd = 0.f;
-                    if (qq < p.N) {
-                        const float L = p.LSE[(size_t)bh * p.N + qq];
+                    if (qq < Lq) {
+                        const float L = p.LSE[lse_index(qq)];
                         v = (L == -INFINITY) ? INFINITY : L * 1.4426950408889634f;
-                        dd = p.Dvec[(size_t)bh * p.N + qq];
+                        dd = p.Dvec[d_index(qq)];
                     }
                     lse_s[s * BQ + t] = v;
                     dv_s[s * BQ + t] = dd;
@@ -278,20 +309,20 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_kernel(const __grid_constant__ 
             };
             bool ok = true;
             int i = 0;
-            if (first < p.Tqb) {
+            if (first < Tqb) {
                 ok = mbar_wait_warp(bar(S::B_KV), 0, g, 0x211) && mbar_wait_warp(bar(S::B_QFULL), 0, g, 0x212);
                 if (ok) {
                     tc_fence_after();
                     issue_s(0);
                     issue_dp(0);
                 }
-                for (int qb = first; ok && qb < p.Tqb; ++i) {
+                for (int qb = first; ok && qb < Tqb; ++i) {
                     const int s = i & 1;
                     const uint64_t q_mn = sdesc_add(dQ_mn, (uint32_t)(s * S::Q_BYTES));
                     const uint64_t do_mn = sdesc_add(ddO_mn, (uint32_t)(s * S::Q_BYTES));
                     const uint32_t acc0 = i > 0 ? 1u : 0u;
                     const int qb_next = next_qb(qb);
-                    const bool more = qb_next < p.Tqb;
+                    const bool more = qb_next < Tqb;
                     // dV += P^T dO: A = P^T from TMEM, B = dO (N = D, K = queries, MN-major)
                     if (!mbar_wait_warp(bar(S::B_PFULL), (uint32_t)i & 1u, g, 0x214)) { ok = false; break; }
                     tc_fence_after();
@@ -388,13 +419,16 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_kernel(const __grid_constant__ 
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-                tma_reduce_add_3d(&p.tmdQ, box, cx, cy, bh);
+                if constexpr (VARLEN)
+                    tma_reduce_add_3d(&p.tmdQ, box, cx, h, q_start + cy);
+                else
+                    tma_reduce_add_3d(&p.tmdQ, box, cx, cy, bh);
                 bulk_commit_group();
             }
             return true;
         };
 
-        for (int qb = first; qb < p.Tqb; qb = next_qb(qb), ++i) {
+        for (int qb = first; qb < Tqb; qb = next_qb(qb), ++i) {
             const unsigned klass = cls(qb);
             const int qa = qb * BQ;
             if (!mbar_wait_warp(bar(S::B_LSE + (i & 1)), (uint32_t)(i >> 1) & 1u, g, 0x410)) { ok = false; break; }
@@ -419,7 +453,7 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_kernel(const __grid_constant__ 
 #pragma unroll
                         for (int t = 0; t < 32; ++t) {
                             const int qq = qa + c0 + 32 * j + t;
-                            if (key >= kvis || (p.causal && key > qq)) sr[j][t] = __float_as_uint(-INFINITY);
+                            if (key >= kvis || (p.causal && key > qq + shift)) sr[j][t] = __float_as_uint(-INFINITY);
                         }
                 }
 #pragma unroll
@@ -500,8 +534,9 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_kernel(const __grid_constant__ 
         }
         if (ok) {
             // the TMEM loads are warp-collective: every lane loads, only rows < N store
-            __nv_bfloat16 *dkrow = reinterpret_cast<__nv_bfloat16 *>(p.dK) + ((size_t)bh * p.N + key) * D;
-            __nv_bfloat16 *dvrow = reinterpret_cast<__nv_bfloat16 *>(p.dV) + ((size_t)bh * p.N + key) * D;
+            const size_t krow = VARLEN ? (size_t)(k_start + key) * p.H + h : (size_t)bh * p.N + key;
+            __nv_bfloat16 *dkrow = reinterpret_cast<__nv_bfloat16 *>(p.dK) + krow * D;
+            __nv_bfloat16 *dvrow = reinterpret_cast<__nv_bfloat16 *>(p.dV) + krow * D;
 #pragma unroll 1
             for (int j = wg * (D / 64); j < (wg + 1) * (D / 64); ++j) {
                 uint32_t a[32], v[32];
@@ -520,7 +555,7 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_kernel(const __grid_constant__ 
                     wk[t] = pack_bf16x2(__uint_as_float(a[2 * t]) * p.scale, __uint_as_float(a[2 * t + 1]) * p.scale);
                     wv[t] = pack_bf16x2(__uint_as_float(v[2 * t]), __uint_as_float(v[2 * t + 1]));
                 }
-                if (key < p.N) {
+                if (key < Lk) {
                     uint4 *dk4 = reinterpret_cast<uint4 *>(dkrow + 32 * j);
                     uint4 *dv4 = reinterpret_cast<uint4 *>(dvrow + 32 * j);
 #pragma unroll
@@ -617,17 +652,22 @@ int bwd_query_block(int d) { return d == 64 ? BwdShape<64>::BQ : 128; }
 int bwd_dq_box_rows(int) { return BwdShape<64>::DQ_BOX_ROWS; }   // fa_bwd128.cu uses the same 32 x 32 boxes
 int bwd_smem_bytes(int d) { return d == 64 ? BwdShape<64>::SMEM_BYTES : bwd128_smem_bytes(); }
 
-template <int D>
+template <int D, bool VARLEN>
 static cudaError_t launch_bwd_main_t(const BwdParams &p, cudaStream_t st) {
     const int smem = BwdShape<D>::SMEM_BYTES;
-    cudaError_t e = cudaFuncSetAttribute(fa_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(fa_bwd_kernel<D, VARLEN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    fa_bwd_kernel<D><<<(unsigned)p.Tk * (unsigned)p.BH, 384, smem, st>>>(p);
+    fa_bwd_kernel<D, VARLEN><<<(unsigned)p.Tk * (unsigned)p.BH, 384, smem, st>>>(p);
     return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_main(int d, const BwdParams &p, cudaStream_t st) {
-    return d == 64 ? launch_bwd_main_t<64>(p, st) : launch_bwd128_main(p, st);
+    return d == 64 ? launch_bwd_main_t<64, false>(p, st) : launch_bwd128_main(p, st);
+}
+
+cudaError_t launch_bwd_main_varlen(int d, const BwdParams &p, cudaStream_t st) {
+    return d == 64 ? launch_bwd_main_t<64, true>(p, st) : launch_bwd128_main_varlen(p, st);
 }
 
 cudaError_t launch_bwd_pre(int d, const void *O, const void *dO, float *Dvec, float *dQacc, int64_t rows,

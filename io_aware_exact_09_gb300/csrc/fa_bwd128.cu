@@ -32,6 +32,8 @@
 // clock64 trace: staging stores queue behind the SS MMAs' operand reads, and
 // the staging area shared with the dS^T tile made them wait for the previous
 // reduce); off their path, the compute chain per block is P -> dS only.
+#include <climits>
+
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
 
@@ -96,6 +98,7 @@ __device__ __forceinline__ void b128_drain_wait(uint32_t bar, uint32_t parity) {
 // 64-column half, so neither overwrites fp32 values the other still reads.
 __device__ __forceinline__ uint32_t packed_col128(int k) { return (uint32_t)((k >> 2) * 64 + 8 * (k & 3)); }
 
+template <bool VARLEN>
 __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant__ BwdParams p) {
     using S = Bwd128;
     constexpr int BQ = S::BQ, CW = S::CW;
@@ -107,7 +110,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
 
     const int kt = (int)(blockIdx.x % p.Tk);
     const int bh = (int)(blockIdx.x / p.Tk);
-    const int b = bh / p.H;
+    const int b = bh / p.H, h = bh % p.H;
     const int k0 = kt * kTile;
     const int nb = (p.N + kTile - 1) / kTile;
 
@@ -116,25 +119,51 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sb + S::OFF_MISC + 4);
     const Guard g{p.status, p.status + 1, abort_flag};
 
+    // the sequence (as in fa_bwd.cu): queries [q_start, q_start + Lq), keys
+    // [k_start, k_start + Lk), bottom-right causal shift Lk - Lq (0 if square)
+    int q_start = 0, k_start = 0, Lq = p.N, Lk = p.N, Tqb = p.Tqb;
     bool bad = false;
-    const int kvis = key_visible_bound(p.key_len, b, p.N, &bad);
-    if (bad && threadIdx.x == 0 && kt == 0 && (bh % p.H) == 0) record_status(g, kStatusBadKeyLen, 0);
+    if constexpr (VARLEN) {
+        varlen_sequence(p.cu_q, p.cu_k, b, p.total_q, p.total_k, INT_MAX, p.Tk * kTile, &q_start, &Lq, &k_start,
+                        &Lk, &bad);
+        Tqb = (Lq + BQ - 1) / BQ;
+    }
+    const int shift = Lk - Lq;
+    const int kvis = VARLEN ? Lk : key_visible_bound(p.key_len, b, p.N, &bad);
+    if (bad && threadIdx.x == 0 && kt == 0 && h == 0) record_status(g, kStatusBadKeyLen, 0);
+    // a key tile past a ragged sequence's end has nothing to write: the whole
+    // CTA leaves before any set-up
+    if (VARLEN && k0 >= Lk) return;
 
     // query block qb (128 rows = one mask block) against this key tile
     auto cls = [&](int qb) -> unsigned {
         const int qa = qb * BQ;
+        if constexpr (VARLEN) return tile_class_shift(qa, min(BQ, Lq - qa), k0, kTile, kvis, p.causal, shift);
         const int on = p.block_mask ? (p.block_mask[(size_t)qb * nb + kt] != 0) : 1;
         return tile_class(qa, min(BQ, p.N - qa), k0, kTile, kvis, p.causal, on);
     };
-    const int qb_start = bwd_query_block_begin(k0, kvis, p.causal, 0, BQ, p.Tqb);
+    const int qb_start = bwd_query_block_begin(k0, kvis, p.causal, shift, BQ, Tqb);
     auto next_qb = [&](int qb) -> int {
-        if (!p.block_mask) {
+        if (VARLEN || !p.block_mask) {
             const int nq = qb < qb_start ? qb_start : qb + 1;
-            return nq < p.Tqb ? nq : p.Tqb;
+            return nq < Tqb ? nq : Tqb;
         }
-        for (int x = qb + 1; x < p.Tqb; ++x)
+        for (int x = qb + 1; x < Tqb; ++x)
             if (cls(x) != kTileSkip) return x;
-        return p.Tqb;
+        return Tqb;
+    };
+    // TMA coordinates: [B*H][N][d] view, or the ragged [total][H][d] view
+    auto tload = [&](uint32_t dst, const CUtensorMap *m, uint32_t mbar, int c, int row, int start) {
+        if constexpr (VARLEN)
+            tma_load_3d(dst, m, mbar, c * 64, h, start + row);
+        else
+            tma_load_3d(dst, m, mbar, c * 64, row, bh);
+    };
+    auto lse_index = [&](int qq) -> size_t {
+        return VARLEN ? (size_t)h * p.total_q + q_start + qq : (size_t)bh * p.N + qq;
+    };
+    auto d_index = [&](int qq) -> size_t {
+        return VARLEN ? (size_t)(q_start + qq) * p.H + h : (size_t)bh * p.N + qq;
     };
 
     if (threadIdx.x == 0) {
@@ -177,18 +206,18 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
 
     if (warp < 4) {
         setmaxnreg_dec<S::REGS_CTRL>();
-        if (warp == 0 && first < p.Tqb) {
+        if (warp == 0 && first < Tqb) {
             // ---------------------------------------------------------- producer
             if (lane == 0) {
                 mbar_arrive_expect_tx(bar(S::B_KV), 2 * S::TILE);
                 for (int c = 0; c < 2; ++c) {
-                    tma_load_3d(base + S::OFF_K + c * S::CHUNK, &p.tmK, bar(S::B_KV), c * 64, k0, bh);
-                    tma_load_3d(base + S::OFF_V + c * S::CHUNK, &p.tmV, bar(S::B_KV), c * 64, k0, bh);
+                    tload(base + S::OFF_K + c * S::CHUNK, &p.tmK, bar(S::B_KV), c, k0, k_start);
+                    tload(base + S::OFF_V + c * S::CHUNK, &p.tmV, bar(S::B_KV), c, k0, k_start);
                 }
             }
             int i = 0, nl = 0;          // blocks seen, blocks whose Q / dO loads were issued
             bool ok = true;
-            for (int qb = first; qb < p.Tqb; qb = next_qb(qb), ++i) {
+            for (int qb = first; qb < Tqb; qb = next_qb(qb), ++i) {
                 const int s = i & 1;
                 // Q(i) into stage s once dK(i - 2) has read it; dO(i) once dV(i - 1) has
                 if (!mbar_wait_warp(bar(S::B_QEMPTY + s), ((uint32_t)(i >> 1) & 1u) ^ 1u, g, 0x121) ||
@@ -200,16 +229,15 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
                     mbar_arrive_expect_tx(bar(S::B_QFULL + s), S::TILE);
                     mbar_arrive_expect_tx(bar(S::B_DOFULL), S::TILE);
                     for (int c = 0; c < 2; ++c) {
-                        tma_load_3d(base + S::OFF_Q + s * S::TILE + c * S::CHUNK, &p.tmQ, bar(S::B_QFULL + s),
-                                    c * 64, qb * BQ, bh);
-                        tma_load_3d(base + S::OFF_DO + c * S::CHUNK, &p.tmdO, bar(S::B_DOFULL), c * 64, qb * BQ,
-                                    bh);
+                        tload(base + S::OFF_Q + s * S::TILE + c * S::CHUNK, &p.tmQ, bar(S::B_QFULL + s), c, qb * BQ,
+                              q_start);
+                        tload(base + S::OFF_DO + c * S::CHUNK, &p.tmdO, bar(S::B_DOFULL), c, qb * BQ, q_start);
                     }
                 }
                 nl = i + 1;
-                // LSE (log2 domain; +inf past N or for a row with no visible
-                // key: its P is 0) and D of the block, once the previous
-                // block's are consumed
+                // LSE (log2 domain; +inf past the sequence's last query or for
+                // a row with no visible key: its P is 0) and D of the block,
+                // once the previous block's are consumed
                 if (!mbar_wait_warp(bar(S::B_LSEFREE), ((uint32_t)i & 1u) ^ 1u, g, 0x123)) {
                     ok = false;
                     break;
@@ -218,10 +246,10 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
                 for (int t = lane; t < BQ; t += 32) {
                     const int qq = qa + t;
                     float v = INFINITY, dd = 0.f;
-                    if (qq < p.N) {
-                        const float L = p.LSE[(size_t)bh * p.N + qq];
+                    if (qq < Lq) {
+                        const float L = p.LSE[lse_index(qq)];
                         v = (L == -INFINITY) ? INFINITY : L * 1.4426950408889634f;
-                        dd = p.Dvec[(size_t)bh * p.N + qq];
+                        dd = p.Dvec[d_index(qq)];
                     }
                     lse_s[t] = v;
                     dv_s[t] = dd;
@@ -272,7 +300,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
             };
             bool ok = true;
             int i = 0;
-            if (first < p.Tqb) {
+            if (first < Tqb) {
                 ok = mbar_wait_warp(bar(S::B_KV), 0, g, 0x221) && mbar_wait_warp(bar(S::B_QFULL), 0, g, 0x222) &&
                      mbar_wait_warp(bar(S::B_DOFULL), 0, g, 0x223);
                 if (ok) {
@@ -280,7 +308,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
                     issue_s(0);
                     issue_dp(0);
                 }
-                for (int qb = first; ok && qb < p.Tqb; ++i) {
+                for (int qb = first; ok && qb < Tqb; ++i) {
                     const int s = i & 1;
                     const uint32_t ra = region(s), rb = region(s ^ 1);
                     const uint32_t acc0 = i > 0 ? 1u : 0u;
@@ -311,7 +339,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
                         mma_ts_elect(tmem + S::TM_DK, rb + packed_col128(k), sdesc_add(q_mn, (uint32_t)k * 2048u),
                                IDESC_ACC, k > 0 ? 1u : acc0);
                     mma_commit_elect(bar(S::B_QEMPTY + s));       // dK(i) done
-                    if (qb_next < p.Tqb) {
+                    if (qb_next < Tqb) {
                         // S^T(i+1) into region b once dK has read dS^T there
                         if (!mbar_wait_warp(bar(S::B_QFULL + (s ^ 1)), (uint32_t)((i + 1) >> 1) & 1u, g, 0x227) ||
                             !mbar_wait_warp(bar(S::B_QEMPTY + s), (uint32_t)(i >> 1) & 1u, g, 0x228)) { ok = false; break; }
@@ -343,7 +371,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
         bool ok = true;
         int i = 0;
 
-        for (int qb = first; qb < p.Tqb; qb = next_qb(qb), ++i) {
+        for (int qb = first; qb < Tqb; qb = next_qb(qb), ++i) {
             const unsigned klass = cls(qb);
             const int qa = qb * BQ;
             const uint32_t ra = tmem + lane_off + S::TM_R0 + 128u * (uint32_t)(i & 1);
@@ -370,7 +398,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
 #pragma unroll
                         for (int t = 0; t < 32; ++t) {
                             const int qq = qa + c0 + 32 * j + t;
-                            if (key >= kvis || (p.causal && key > qq)) sr[j][t] = __float_as_uint(-INFINITY);
+                            if (key >= kvis || (p.causal && key > qq + shift)) sr[j][t] = __float_as_uint(-INFINITY);
                         }
                 }
 #pragma unroll
@@ -439,8 +467,9 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
             tc_fence_after();
         }
         if (ok) {
-            __nv_bfloat16 *dkrow = reinterpret_cast<__nv_bfloat16 *>(p.dK) + ((size_t)bh * p.N + key) * 128;
-            __nv_bfloat16 *dvrow = reinterpret_cast<__nv_bfloat16 *>(p.dV) + ((size_t)bh * p.N + key) * 128;
+            const size_t krow = VARLEN ? (size_t)(k_start + key) * p.H + h : (size_t)bh * p.N + key;
+            __nv_bfloat16 *dkrow = reinterpret_cast<__nv_bfloat16 *>(p.dK) + krow * 128;
+            __nv_bfloat16 *dvrow = reinterpret_cast<__nv_bfloat16 *>(p.dV) + krow * 128;
 #pragma unroll 1
             for (int j = wg * 2; j < wg * 2 + 2; ++j) {
                 uint32_t a[32], vv[32];
@@ -459,7 +488,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
                     wk[t] = pack_bf16x2(__uint_as_float(a[2 * t]) * p.scale, __uint_as_float(a[2 * t + 1]) * p.scale);
                     wv[t] = pack_bf16x2(__uint_as_float(vv[2 * t]), __uint_as_float(vv[2 * t + 1]));
                 }
-                if (key < p.N) {
+                if (key < Lk) {
                     uint4 *dk4 = reinterpret_cast<uint4 *>(dkrow + 32 * j);
                     uint4 *dv4 = reinterpret_cast<uint4 *>(dvrow + 32 * j);
 #pragma unroll
@@ -483,18 +512,18 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
         uint8_t *stg = sb + S::OFF_STG + wq * 8192;
         const int grp = lane >> 2;
         int i = 0;
-        for (int qb = first; qb < p.Tqb; qb = next_qb(qb), ++i) {
+        for (int qb = first; qb < Tqb; qb = next_qb(qb), ++i) {
             const uint32_t ra = tmem + lane_off + S::TM_R0 + 128u * (uint32_t)(i & 1);
             if (!mbar_wait_warp(bar(S::B_DQFULL), (uint32_t)i & 1u, g, 0x426)) break;
             tc_fence_after();
 #pragma unroll 1
-            for (int h = 0; h < 2; ++h) {
+            for (int hf = 0; hf < 2; ++hf) {
                 uint32_t v[2][32];
-                tmem_ld32(ra + 64u * h, v[0]);
-                tmem_ld32(ra + 64u * h + 32, v[1]);
+                tmem_ld32(ra + 64u * hf, v[0]);
+                tmem_ld32(ra + 64u * hf + 32, v[1]);
                 tmem_ld_wait(v[0]);
                 tmem_ld_wait(v[1]);
-                if (h == 1) {
+                if (hf == 1) {
                     // all of dQ^T(i) is in registers or staged: region a is free
                     tc_fence_before();
                     mbar_arrive(bar(S::B_DQFREE));
@@ -512,9 +541,14 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    const int q0 = qb * BQ + 64 * h;
-                    tma_reduce_add_3d(&p.tmdQ, smem_u32(stg), wq * 32, q0, bh);
-                    tma_reduce_add_3d(&p.tmdQ, smem_u32(stg + 4096), wq * 32, q0 + 32, bh);
+                    const int q0 = qb * BQ + 64 * hf;
+                    if constexpr (VARLEN) {
+                        tma_reduce_add_3d(&p.tmdQ, smem_u32(stg), wq * 32, h, q_start + q0);
+                        tma_reduce_add_3d(&p.tmdQ, smem_u32(stg + 4096), wq * 32, h, q_start + q0 + 32);
+                    } else {
+                        tma_reduce_add_3d(&p.tmdQ, smem_u32(stg), wq * 32, q0, bh);
+                        tma_reduce_add_3d(&p.tmdQ, smem_u32(stg + 4096), wq * 32, q0 + 32, bh);
+                    }
                     bulk_commit_group();
                 }
             }
@@ -534,12 +568,18 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
 
 int bwd128_smem_bytes() { return Bwd128::SMEM_BYTES; }
 
-cudaError_t launch_bwd128_main(const BwdParams &p, cudaStream_t st) {
+template <bool VARLEN>
+static cudaError_t launch_bwd128_t(const BwdParams &p, cudaStream_t st) {
     const int smem = Bwd128::SMEM_BYTES;
-    cudaError_t e = cudaFuncSetAttribute(fa_bwd128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(fa_bwd128_kernel<VARLEN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    fa_bwd128_kernel<<<(unsigned)p.Tk * (unsigned)p.BH, Bwd128::THREADS, smem, st>>>(p);
+    fa_bwd128_kernel<VARLEN><<<(unsigned)p.Tk * (unsigned)p.BH, Bwd128::THREADS, smem, st>>>(p);
     return cudaGetLastError();
 }
+
+cudaError_t launch_bwd128_main(const BwdParams &p, cudaStream_t st) { return launch_bwd128_t<false>(p, st); }
+
+cudaError_t launch_bwd128_main_varlen(const BwdParams &p, cudaStream_t st) { return launch_bwd128_t<true>(p, st); }
 
 }  // namespace fa

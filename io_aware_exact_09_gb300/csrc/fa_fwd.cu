@@ -21,11 +21,19 @@
 // GB300 design (not the A100 loop order the tiling page prints; the query
 // tile is the outer loop, as in its "FlashAttention-2" section, so O stays
 // on chip):
-//   - one CTA per (pair of 128-row query tiles, b*h), head-major, causally
-//     heaviest pairs first within a head;
-//   - warp 0: TMA producer: both Q tiles once; K and V tiles through a ring
-//     of shared-memory stages (128-byte swizzle, 64-column boxes), over the
-//     union of the key tiles the two query tiles see;
+//   - a persistent grid, one CTA per SM; a work item is a pair of 128-row
+//     query tiles of one b*h; the CTAs take items from a counter in the
+//     workspace, head-major with the causally heaviest pair of a head first,
+//     so the set-up (barriers, TMEM, register split) is paid once per SM and
+//     the next item's Q load and first S product overlap the current item's
+//     last tile and epilogue;
+//   - warp 0: producer: takes the next item, describes it in a shared
+//     slot for the other roles (under a block mask with the compacted list
+//     of the key tiles the item sees, built once by the whole warp), then
+//     TMA: both Q tiles once the previous item's S products are done with the
+//     Q buffer; K and V tiles through a ring of shared-memory stages
+//     (128-byte swizzle, 64-column boxes), over the union of the key tiles the
+//     two query tiles see;
 //   - warp 1: tcgen05 issuer: for each key tile and query tile x in turn,
 //     O_x += P_x V with P_x read from TMEM (bf16, written over the first half
 //     of S_x), then the next key tile's S_x = Q_x K^T as soon as that P.V
@@ -44,6 +52,9 @@
 // a shorter one's end have nothing to do.  A sequence's Lq queries are its
 // last positions among its Lk keys (a cached prefix, or Lq = Lk for a plain
 // prefill), so the causal diagonal is shifted by Lk - Lq.
+#include <algorithm>
+#include <climits>
+
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
 
@@ -66,28 +77,51 @@ struct FwdShape {
     static constexpr int OFF_V = OFF_K + STAGES * KV_TILE_BYTES;
     static constexpr int OFF_BAR = OFF_V + STAGES * KV_TILE_BYTES;
     static constexpr int B_QFULL = 0;
-    static constexpr int B_KFULL = 1;
+    static constexpr int B_QEMPTY = 1;                   // an item's S products are done: Q free
+    static constexpr int B_KFULL = 2;
     static constexpr int B_VFULL = B_KFULL + STAGES;
     static constexpr int B_KVEMPTY = B_VFULL + STAGES;
     static constexpr int B_SFULL = B_KVEMPTY + STAGES;   // [2] one per query tile
     static constexpr int B_PFULL = B_SFULL + 2;          // [2]
     static constexpr int B_PVDONE = B_PFULL + 2;         // [2]
-    static constexpr int B_FIN = B_PVDONE + 2;
+    static constexpr int B_ITEM = B_PVDONE + 2;          // [2] work-item slot published (32 arrivals)
+    static constexpr int B_ITEMFREE = B_ITEM + 2;        // [2] slot read by every consumer (1 + 8 arrivals)
+    static constexpr int B_FIN = B_ITEMFREE + 2;
     static constexpr int NBAR = B_FIN + 1;
-    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem base (4 B), abort flag (4 B)
+    static constexpr int OFF_SLOT = (OFF_BAR + NBAR * 8 + 127) & ~127;   // [2] FwdItem, 128 bytes each
+    // key-tile list of an item under a block mask: entry = tile | visible to
+    // query tile 0 << 14 | visible to query tile 1 << 15
+    static constexpr int LIST_CAP = 2048;
+    static constexpr int OFF_LIST = OFF_SLOT + 2 * 128;  // [2][LIST_CAP] uint16
+    static constexpr int OFF_MISC = OFF_LIST + 2 * LIST_CAP * 2;   // tmem base (4 B), abort flag (4 B)
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1 KB
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t TM_S = 0;                  // S_x at columns 128 x
     static constexpr uint32_t TM_O = 256;                // O_x at columns 256 + D x
     static constexpr int THREADS = 384;
     // register split: launched at 168 per thread (384 x 168 = 64,512);
-    // warpgroup 0 (producer, MMA, two idle warps) keeps 88, the two softmax
-    // warpgroups get 208: 128 x 88 + 256 x 208 = 64,512.
+    // warpgroup 0 (producer, MMA, two idle warps) keeps 104, the two softmax
+    // warpgroups get 200: 128 x 104 + 256 x 200 = 64,512.
     static constexpr int LAUNCH_REGS = 168;
     static constexpr int REGS_CTRL = 104;
     static constexpr int REGS_SOFTMAX = 200;
     static_assert(128 * REGS_CTRL + 256 * REGS_SOFTMAX == THREADS * LAUNCH_REGS, "register split");
 };
+
+// One work item as the producer publishes it to the other roles.
+struct FwdItem {
+    int item;          // work-item index, or -1: no more work
+    int bh, h;
+    int q_start, k_start;   // first row of the sequence in Q / K (0 unless ragged)
+    int kvis, shift;        // keys < kvis are visible; causal: key j <= query i + shift
+    int q0[2], qn[2];       // query tile x: rows [q0, q0 + qn) of the sequence (qn = 0: none)
+    int kend[2];            // without a list: key tiles [0, kend[x]) are those query tile x sees
+    int count;              // key-tile entries to visit (union of both query tiles)
+    int use_list;           // entries come from the item's key-tile list (block mask)
+    int nq;                 // query tiles with rows
+};
+static_assert(sizeof(FwdItem) <= 128, "item slot");
 
 // Bounded wait used only while draining after an abort (ignores the abort flag).
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
@@ -96,6 +130,13 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
         if (globaltimer_ns() - t0 > FA_WAIT_TIMEOUT_NS) break;
 }
 
+// Persistent grid: one CTA per SM; each CTA takes work items (a pair of
+// 128-row query tiles of one b*h) from a counter in the workspace until none
+// is left.  The items are numbered head-major with the causally heaviest
+// pair of each head first, and handed out in that order, so the CTAs at work
+// at one time share one head's K and V in L2 and the longest items start
+// first.  The counter resets itself: the last CTA to finish taking items sets
+// it back to zero, so the next launch on the same workspace starts from 0.
 template <int D, bool VARLEN, int BC, int QPC>
 __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
     using S = FwdShape<D, BC>;
@@ -105,98 +146,22 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
     uint8_t *sb = smem_raw + (base - raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // Work item, head-major: the CTAs resident at one time share one head's K
-    // and V in L2; within a head the causally heaviest pairs start first.
-    constexpr int qpc = QPC;                         // query tiles per CTA (1 or 2)
+    constexpr int qpc = QPC;                         // query tiles per item (1 or 2)
     const int Tp = (p.Tq + qpc - 1) / qpc;
-    const int pq = Tp - 1 - (int)(blockIdx.x % Tp);
-    const int bh = (int)(blockIdx.x / Tp);
-    const int b = bh / p.H, h = bh % p.H;
+    const int n_items = Tp * p.BH;
     const int nb = (p.N + kTile - 1) / kTile;
-    // the sequence this CTA works on: rows [q_start, q_start + Lq) of Q and
-    // [k_start, k_start + Lk) of K, V.  Its queries are its last Lq
-    // positions: under the causal mask query i sees key j iff j <= i + shift
-    // (shift = Lk - Lq; 0 for the square [B, H, N, d] case).
-    int q_start = 0, k_start = 0, Lq = p.N, Lk = p.N, Tk = p.Tk;
-    bool bad_len = false;
-    if constexpr (VARLEN) {
-        q_start = p.cu_q[b];
-        Lq = p.cu_q[b + 1] - q_start;
-        k_start = p.cu_k[b];
-        Lk = p.cu_k[b + 1] - k_start;
-        if (q_start < 0 || Lq < 0 || q_start + Lq > p.total_q || k_start < 0 || Lk < 0 ||
-            k_start + Lk > p.total_k || Lq > p.Tq * kTile) {
-            bad_len = true;
-            Lq = Lk = 0;
-        }
-        Tk = (Lk + BC - 1) / BC;
-    }
-    const int shift = Lk - Lq;
-    int q0[2], qn[2];
-#pragma unroll
-    for (int x = 0; x < 2; ++x) {
-        q0[x] = (qpc * pq + x) * kTile;
-        qn[x] = x < qpc ? max(0, min(kTile, Lq - q0[x])) : 0;
-    }
-    // TMA coordinates of row `row` of a sequence starting at `start`:
-    // [B*H][N][d] view, or the [total][H][d] view of a ragged batch
-    // warp-collective (the producer warp calls it with uniform arguments)
-    auto tload = [&](uint32_t dst, const CUtensorMap *m, uint32_t mbar, int c, int row, int start) {
-        if constexpr (VARLEN)
-            tma_load_3d_elect(dst, m, mbar, c * 64, h, start + row);
-        else
-            tma_load_3d_elect(dst, m, mbar, c * 64, row, bh);
-    };
 
     auto bar = [&](int i) -> uint32_t { return base + S::OFF_BAR + 8u * (uint32_t)i; };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sb + S::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sb + S::OFF_MISC + 4);
     const Guard g{p.status, p.status + 1, abort_flag};
-
-    bool bad = bad_len;
-    const int kvis = VARLEN ? Lk : key_visible_bound(p.key_len, b, p.N, &bad);
-    if (bad && threadIdx.x == 0 && pq == 0 && (bh % p.H) == 0) record_status(g, kStatusBadKeyLen, 0);
-    // In a ragged batch the grid covers the longest sequence: a CTA whose
-    // query tiles both lie past its own sequence's end has no row to write and
-    // leaves before any set-up (the whole CTA takes this branch together)
-    if (qn[0] <= 0 && qn[1] <= 0) return;
-
-    // Without a block mask the key tiles query tile x sees are exactly
-    // [0, kend[x]): keys below key_len and, under the causal mask, not past
-    // its last row.  (tile_class below takes the same decision per tile.)
-    int kend[2];
-#pragma unroll
-    for (int x = 0; x < 2; ++x) kend[x] = fwd_key_tile_end(q0[x], qn[x], kvis, p.causal, shift, BC);
-    const int kend_union = max(kend[0], kend[1]);
-    // per-query-tile values by selection, so that the arrays stay in registers
-    auto q0_of = [&](int x) { return x ? q0[1] : q0[0]; };
-    auto qn_of = [&](int x) { return x ? qn[1] : qn[0]; };
-    auto kend_of = [&](int x) { return x ? kend[1] : kend[0]; };
-    // class of key tile kt for query tile x of the pair
-    auto cls = [&](int x, int kt) -> unsigned {
-        if (qn_of(x) <= 0) return kTileSkip;
-        if constexpr (VARLEN) return tile_class_shift(q0_of(x), qn_of(x), kt * BC, BC, kvis, p.causal, shift);
-        // a key tile of BC <= 128 columns lies inside one 128-wide mask block
-        const int on =
-            p.block_mask ? (p.block_mask[(size_t)(QPC * pq + x) * nb + (BC == kTile ? kt : kt / (kTile / BC))] != 0) : 1;
-        return tile_class(q0_of(x), qn_of(x), kt * BC, BC, kvis, p.causal, on);
-    };
-    // next key tile after kt seen by query tile x (x = 2: by either)
-    auto next_tile = [&](int x, int kt) -> int {
-        if (!p.block_mask) {
-            const int lim = x == 2 ? kend_union : kend_of(x);
-            return kt + 1 < lim ? kt + 1 : Tk;
-        }
-        for (int k = kt + 1; k < Tk; ++k) {
-            const bool v0 = (x != 1) && cls(0, k) != kTileSkip;
-            const bool v1 = (x != 0) && cls(1, k) != kTileSkip;
-            if (v0 || v1) return k;
-        }
-        return Tk;
-    };
+    FwdItem *slots = reinterpret_cast<FwdItem *>(sb + S::OFF_SLOT);
+    auto list_of = [&](int s) { return reinterpret_cast<uint16_t *>(sb + S::OFF_LIST) + s * S::LIST_CAP; };
+    unsigned *sched = p.status + 2;                  // workspace words 2 (next item) and 3 (CTAs done)
 
     if (threadIdx.x == 0) {
         mbar_init(bar(S::B_QFULL), 1);
+        mbar_init(bar(S::B_QEMPTY), 1);
         for (int s = 0; s < S::STAGES; ++s) {
             mbar_init(bar(S::B_KFULL + s), 1);
             mbar_init(bar(S::B_VFULL + s), 1);
@@ -206,6 +171,8 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
             mbar_init(bar(S::B_SFULL + j), 1);
             mbar_init(bar(S::B_PFULL + j), 128);
             mbar_init(bar(S::B_PVDONE + j), 1);
+            mbar_init(bar(S::B_ITEM + j), 32);
+            mbar_init(bar(S::B_ITEMFREE + j), 9);
         }
         mbar_init(bar(S::B_FIN), 1);
         *abort_flag = 0;
@@ -223,109 +190,242 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    // entry e of an item: its key tile and whether query tile x sees it
+    auto entry_kt = [&](const FwdItem &it, const uint16_t *lst, int e) -> int {
+        return it.use_list ? (int)(lst[e] & 0x3FFFu) : e;
+    };
+    auto entry_vis = [&](const FwdItem &it, const uint16_t *lst, int x, int e) -> bool {
+        if (it.use_list) return (lst[e] >> (14 + x)) & 1u;
+        return e < (x ? it.kend[1] : it.kend[0]);
+    };
+
     // Register split.  Warpgroup 0 gives registers back once, here, and
-    // keeps 88 to the end; the softmax warpgroups take them, here, and give
-    // them back at the end of their branch, so the shared teardown below runs
-    // with 88 everywhere.  The only setmaxnreg.inc (which blocks until the
-    // pool holds enough) is the softmax one at the start, and the pool is
-    // filled by warpgroup 0's unconditional dec: no inc ever waits on a warp
-    // that is itself waiting.
+    // keeps REGS_CTRL to the end; the softmax warpgroups take them, here, and
+    // give them back at the end of their branch, so the shared teardown below
+    // runs with REGS_CTRL everywhere.  The only setmaxnreg.inc (which blocks
+    // until the pool holds enough) is the softmax one at the start, and the
+    // pool is filled by warpgroup 0's unconditional dec: no inc ever waits on
+    // a warp that is itself waiting.
     if (warp < 4) {
         setmaxnreg_dec<S::REGS_CTRL>();
         if (warp == 0) {
-            // ---------------------------------------------------------- producer
-            {
-                int u = 0;
-                bool ok = true;
-                int kt = next_tile(2, -1);
-                if (kt < Tk) {
-                    const uint32_t nq = (qn[0] > 0 ? 1u : 0u) + (qn[1] > 0 ? 1u : 0u);
-                    mbar_arrive_expect_tx_elect(bar(S::B_QFULL), nq * S::TILE_BYTES);
-                    #pragma unroll
-                    for (int x = 0; x < 2; ++x)
-                        if (qn[x] > 0)
-                            for (int c = 0; c < S::CHUNKS; ++c)
-                                tload(base + S::OFF_Q + x * S::TILE_BYTES + c * S::CHUNK_BYTES, &p.tmQ,
-                                      bar(S::B_QFULL), c, q0[x], q_start);
+            // ---------------------------------------------------------- producer (whole warp)
+            // Takes the items, describes each one in a slot for the other
+            // roles (and, under a block mask, lists its key tiles), loads the
+            // item's Q tiles once the previous item's S products are done with
+            // the Q buffer, and streams K and V through the ring.
+            int k = 0, m = 0, u = 0;                 // items published, items with Q loaded, ring uses
+            bool ok = true;
+            for (;; ++k) {
+                const int s = k & 1;
+                if (k >= 2 && !mbar_wait_warp(bar(S::B_ITEMFREE + s), (uint32_t)((k >> 1) - 1) & 1u, g, 0x100)) {
+                    ok = false;
+                    break;
                 }
-                for (; kt < Tk; kt = next_tile(2, kt), ++u) {
-                    const int s = u % S::STAGES;
+                FwdItem it;
+                it.item = -1;
+                for (;;) {
+                    int j = 0;
+                    if (lane == 0) j = (int)atomicAdd(sched, 1u);
+                    j = __shfl_sync(0xffffffffu, j, 0);
+                    if (j >= n_items) break;
+                    // item j: head-major, the causally heaviest pair of the head first
+                    const int pq = Tp - 1 - j % Tp;
+                    const int bh = j / Tp;
+                    const int b = bh / p.H, h = bh % p.H;
+                    int q_start = 0, k_start = 0, Lq = p.N, Lk = p.N;
+                    bool bad = false;
+                    if constexpr (VARLEN)
+                        varlen_sequence(p.cu_q, p.cu_k, b, p.total_q, p.total_k, p.Tq * kTile, INT_MAX, &q_start,
+                                        &Lq, &k_start, &Lk, &bad);
+                    const int kvis = VARLEN ? Lk : key_visible_bound(p.key_len, b, p.N, &bad);
+                    if (bad && lane == 0 && pq == 0 && h == 0) record_status(g, kStatusBadKeyLen, 0);
+                    it.item = j;
+                    it.bh = bh;
+                    it.h = h;
+                    it.q_start = q_start;
+                    it.k_start = k_start;
+                    it.kvis = kvis;
+                    it.shift = Lk - Lq;
+                    it.nq = 0;
+                    for (int x = 0; x < 2; ++x) {
+                        it.q0[x] = (qpc * pq + x) * kTile;
+                        it.qn[x] = x < qpc ? max(0, min(kTile, Lq - it.q0[x])) : 0;
+                        it.kend[x] = fwd_key_tile_end(it.q0[x], it.qn[x], kvis, p.causal, it.shift, BC);
+                        it.nq += it.qn[x] > 0 ? 1 : 0;
+                    }
+                    it.use_list = (!VARLEN && p.block_mask) ? 1 : 0;
+                    it.count = max(it.kend[0], it.kend[1]);
+                    // an item with no query row (past a ragged sequence's end) is not published
+                    if (it.nq > 0) break;
+                    it.item = -1;
+                }
+                uint16_t *lst = list_of(s);
+                if (it.item >= 0 && it.use_list) {
+                    // the key tiles either query tile sees, in order, compacted by the whole warp
+                    const int Tk = p.Tk;
+                    int n = 0;
+                    for (int t0 = 0; t0 < Tk; t0 += 32) {
+                        const int kt = t0 + lane;
+                        bool v[2] = {false, false};
+                        if (kt < Tk)
+                            for (int x = 0; x < 2; ++x) {
+                                if (it.qn[x] <= 0) continue;
+                                const int mb = BC == kTile ? kt : kt / (kTile / BC);
+                                const int on = p.block_mask[(size_t)(it.q0[x] / kTile) * nb + mb] != 0;
+                                v[x] = tile_class(it.q0[x], it.qn[x], kt * BC, BC, it.kvis, p.causal, on) != kTileSkip;
+                            }
+                        const unsigned ball = __ballot_sync(0xffffffffu, v[0] || v[1]);
+                        if (v[0] || v[1])
+                            lst[n + __popc(ball & ((1u << lane) - 1u))] =
+                                (uint16_t)(kt | (v[0] ? 1u << 14 : 0u) | (v[1] ? 1u << 15 : 0u));
+                        n += __popc(ball);
+                    }
+                    it.count = n;
+                }
+                if (lane == 0) slots[s] = it;
+                mbar_arrive(bar(S::B_ITEM + s));    // every lane, after its own list writes
+                if (it.item < 0) break;
+                if (it.count == 0) continue;        // every row sees no key: no loads
+                // Q tiles, once the previous item's S products no longer read the buffer
+                if (m > 0 && !mbar_wait_warp(bar(S::B_QEMPTY), (uint32_t)(m - 1) & 1u, g, 0x101)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx_elect(bar(S::B_QFULL), (uint32_t)it.nq * S::TILE_BYTES);
+                for (int x = 0; x < 2; ++x)
+                    if (it.qn[x] > 0)
+                        for (int c = 0; c < S::CHUNKS; ++c) {
+                            const uint32_t dst = base + S::OFF_Q + x * S::TILE_BYTES + c * S::CHUNK_BYTES;
+                            if constexpr (VARLEN)
+                                tma_load_3d_elect(dst, &p.tmQ, bar(S::B_QFULL), c * 64, it.h, it.q_start + it.q0[x]);
+                            else
+                                tma_load_3d_elect(dst, &p.tmQ, bar(S::B_QFULL), c * 64, it.q0[x], it.bh);
+                        }
+                ++m;
+                for (int e = 0; e < it.count; ++e, ++u) {
+                    const int kt = entry_kt(it, lst, e);
+                    const int st = u % S::STAGES;
                     const uint32_t ph = (uint32_t)(u / S::STAGES) & 1u;
-                    if (!mbar_wait_warp(bar(S::B_KVEMPTY + s), ph ^ 1u, g, 0x101)) {
+                    if (!mbar_wait_warp(bar(S::B_KVEMPTY + st), ph ^ 1u, g, 0x102)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t koff = base + S::OFF_K + s * S::KV_TILE_BYTES;
-                    const uint32_t voff = base + S::OFF_V + s * S::KV_TILE_BYTES;
-                    mbar_arrive_expect_tx_elect(bar(S::B_KFULL + s), S::KV_TILE_BYTES);
-                    for (int c = 0; c < S::CHUNKS; ++c)
-                        tload(koff + c * S::KV_CHUNK_BYTES, &p.tmK, bar(S::B_KFULL + s), c, kt * BC, k_start);
-                    mbar_arrive_expect_tx_elect(bar(S::B_VFULL + s), S::KV_TILE_BYTES);
-                    for (int c = 0; c < S::CHUNKS; ++c)
-                        tload(voff + c * S::KV_CHUNK_BYTES, &p.tmV, bar(S::B_VFULL + s), c, kt * BC, k_start);
-                }
-                if (!ok) {
-                    // gave up: let every copy already issued land before the CTA exits
-                    if (next_tile(2, -1) < Tk) drain_wait(bar(S::B_QFULL), 0);
-                    for (int i = (u > S::STAGES ? u - S::STAGES : 0); i < u; ++i) {
-                        const int s = i % S::STAGES;
-                        const uint32_t ph = (uint32_t)(i / S::STAGES) & 1u;
-                        drain_wait(bar(S::B_KFULL + s), ph);
-                        drain_wait(bar(S::B_VFULL + s), ph);
+                    const uint32_t koff = base + S::OFF_K + st * S::KV_TILE_BYTES;
+                    const uint32_t voff = base + S::OFF_V + st * S::KV_TILE_BYTES;
+                    mbar_arrive_expect_tx_elect(bar(S::B_KFULL + st), S::KV_TILE_BYTES);
+                    for (int c = 0; c < S::CHUNKS; ++c) {
+                        if constexpr (VARLEN)
+                            tma_load_3d_elect(koff + c * S::KV_CHUNK_BYTES, &p.tmK, bar(S::B_KFULL + st), c * 64, it.h,
+                                              it.k_start + kt * BC);
+                        else
+                            tma_load_3d_elect(koff + c * S::KV_CHUNK_BYTES, &p.tmK, bar(S::B_KFULL + st), c * 64,
+                                              kt * BC, it.bh);
                     }
+                    mbar_arrive_expect_tx_elect(bar(S::B_VFULL + st), S::KV_TILE_BYTES);
+                    for (int c = 0; c < S::CHUNKS; ++c) {
+                        if constexpr (VARLEN)
+                            tma_load_3d_elect(voff + c * S::KV_CHUNK_BYTES, &p.tmV, bar(S::B_VFULL + st), c * 64, it.h,
+                                              it.k_start + kt * BC);
+                        else
+                            tma_load_3d_elect(voff + c * S::KV_CHUNK_BYTES, &p.tmV, bar(S::B_VFULL + st), c * 64,
+                                              kt * BC, it.bh);
+                    }
+                }
+                if (!ok) break;
+            }
+            // this CTA takes no more items; the last CTA to get here resets the counter
+            if (lane == 0) {
+                __threadfence();
+                if (atomicAdd(sched + 1, 1u) == gridDim.x - 1) {
+                    atomicExch(sched, 0u);
+                    atomicExch(sched + 1, 0u);
+                }
+            }
+            __syncwarp();
+            if (!ok && lane == 0) {
+                // gave up: let every copy already issued land before the CTA exits
+                if (m > 0) drain_wait(bar(S::B_QFULL), (uint32_t)(m - 1) & 1u);
+                for (int i = (u > S::STAGES ? u - S::STAGES : 0); i < u; ++i) {
+                    const int st = i % S::STAGES;
+                    const uint32_t ph = (uint32_t)(i / S::STAGES) & 1u;
+                    drain_wait(bar(S::B_KFULL + st), ph);
+                    drain_wait(bar(S::B_VFULL + st), ph);
                 }
             }
         } else if (warp == 1) {
-            // ---------------------------------------------------------- MMA issuer
-            {
-                constexpr uint32_t IDESC_S = idesc_bf16(128, BC, false, false);
-                constexpr uint32_t IDESC_PV = idesc_bf16(128, D, false, true);
-                int kt = next_tile(2, -1);
-                bool ok = true;
-                int nv[2] = {0, 0};      // key tiles processed so far by query tile x
-                // shared-memory descriptors built once; per MMA only the start
-                // address moves (K-major: 32 bytes per 16-wide K step inside a
-                // 128-byte row, then the next 64-column chunk; MN-major V: 16 rows)
-                const uint64_t dq0 = sdesc_sw128(base + S::OFF_Q, 16, 1024);
-                const uint64_t dk0 = sdesc_sw128(base + S::OFF_K, 16, 1024);
-                const uint64_t dv0 = sdesc_sw128(base + S::OFF_V, S::KV_CHUNK_BYTES, 1024);
-                // S_x = Q_x K^T for the key tile in stage s (the x-th S buffer)
-                auto issue_s = [&](int x, int s) {
-                    const uint32_t d_tmem = tmem + S::TM_S + 128u * (uint32_t)x;
-                    const uint64_t qd = sdesc_add(dq0, (uint32_t)(x * S::TILE_BYTES));
-                    const uint64_t kd = sdesc_add(dk0, (uint32_t)(s * S::KV_TILE_BYTES));
+            // ---------------------------------------------------------- MMA issuer (whole warp)
+            constexpr uint32_t IDESC_S = idesc_bf16(128, BC, false, false);
+            constexpr uint32_t IDESC_PV = idesc_bf16(128, D, false, true);
+            // shared-memory descriptors built once; per MMA only the start
+            // address moves (K-major: 32 bytes per 16-wide K step inside a
+            // 128-byte row, then the next 64-column chunk; MN-major V: 16 rows)
+            const uint64_t dq0 = sdesc_sw128(base + S::OFF_Q, 16, 1024);
+            const uint64_t dk0 = sdesc_sw128(base + S::OFF_K, 16, 1024);
+            const uint64_t dv0 = sdesc_sw128(base + S::OFF_V, S::KV_CHUNK_BYTES, 1024);
+            // S_x = Q_x K^T for the key tile in stage st (the x-th S buffer)
+            auto issue_s = [&](int x, int st) {
+                const uint32_t d_tmem = tmem + S::TM_S + 128u * (uint32_t)x;
+                const uint64_t qd = sdesc_add(dq0, (uint32_t)(x * S::TILE_BYTES));
+                const uint64_t kd = sdesc_add(dk0, (uint32_t)(st * S::KV_TILE_BYTES));
 #pragma unroll
-                    for (int k = 0; k < D / 16; ++k) {
-                        const uint32_t off = (k >> 2) * S::CHUNK_BYTES + (k & 3) * 32;
-                        const uint32_t koff = (k >> 2) * S::KV_CHUNK_BYTES + (k & 3) * 32;
-                        mma_ss_elect(d_tmem, sdesc_add(qd, off), sdesc_add(kd, koff), IDESC_S, k > 0 ? 1u : 0u);
-                    }
-                    mma_commit_elect(bar(S::B_SFULL + x));
-                };
-                if (kt < Tk) {
-                    ok = mbar_wait_warp(bar(S::B_QFULL), 0, g, 0x201) && mbar_wait_warp(bar(S::B_KFULL + 0), 0, g, 0x202);
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * S::CHUNK_BYTES + (kk & 3) * 32;
+                    const uint32_t koff = (kk >> 2) * S::KV_CHUNK_BYTES + (kk & 3) * 32;
+                    mma_ss_elect(d_tmem, sdesc_add(qd, off), sdesc_add(kd, koff), IDESC_S, kk > 0 ? 1u : 0u);
+                }
+                mma_commit_elect(bar(S::B_SFULL + x));
+            };
+            bool ok = true;
+            int k = 0, m = 0, u = 0;
+            int nv[2] = {0, 0};      // P.V products issued so far for query tile x (all items)
+            for (;; ++k) {
+                const int s = k & 1;
+                if (!mbar_wait_warp(bar(S::B_ITEM + s), (uint32_t)(k >> 1) & 1u, g, 0x200)) {
+                    ok = false;
+                    break;
+                }
+                const FwdItem it = slots[s];
+                const uint16_t *lst = list_of(s);
+                if (it.item < 0) break;
+                if (it.count > 0) {
+                    int nvi[2] = {0, 0};     // this item's P.V products for query tile x
+                    // first entry: S_x for each query tile that sees it, once the
+                    // previous item's last P_x has been read (P_x aliases S_x)
+                    ok = mbar_wait_warp(bar(S::B_QFULL), (uint32_t)m & 1u, g, 0x201) &&
+                         mbar_wait_warp(bar(S::B_KFULL + u % S::STAGES), (uint32_t)(u / S::STAGES) & 1u, g, 0x202);
+                    ++m;
                     if (ok) {
                         tc_fence_after();
-                        #pragma unroll
-                        for (int x = 0; x < 2; ++x)
-                            if (cls(x, kt) != kTileSkip) issue_s(x, 0);
+#pragma unroll
+                        for (int x = 0; x < 2 && ok; ++x)
+                            if (entry_vis(it, lst, x, 0)) {
+                                if (nv[x] > 0 &&
+                                    !mbar_wait_warp(bar(S::B_PVDONE + x), (uint32_t)(nv[x] - 1) & 1u, g, 0x207)) {
+                                    ok = false;
+                                    break;
+                                }
+                                tc_fence_after();
+                                issue_s(x, u % S::STAGES);
+                            }
+                        // the item's S products are all issued: Q is free once they finish
+                        if (ok && it.count == 1) mma_commit_elect(bar(S::B_QEMPTY));
                     }
-                    int u = 0;
-                    while (ok && kt < Tk) {
-                        const int s = u % S::STAGES;
-                        const int kt_next = next_tile(2, kt);
-                        const int s2 = (u + 1) % S::STAGES;
+                    for (int e = 0; ok && e < it.count; ++e, ++u) {
+                        const int st = u % S::STAGES;
+                        const int st2 = (u + 1) % S::STAGES;
+                        const bool more = e + 1 < it.count;
                         bool vwaited = false, kwaited = false;
                         // per query tile: O_x += P_x V, then at once the next key
                         // tile's S_x (it overwrites P_x, so it waits for that P.V),
                         // so that each tile's chain S -> softmax -> P.V -> S moves
                         // on without waiting for the other tile's P
-                        #pragma unroll
+#pragma unroll
                         for (int x = 0; x < 2 && ok; ++x) {
-                            if (cls(x, kt) != kTileSkip) {
+                            if (entry_vis(it, lst, x, e)) {
                                 if (!mbar_wait_warp(bar(S::B_PFULL + x), (uint32_t)nv[x] & 1u, g, 0x203) ||
                                     (!vwaited &&
-                                     !mbar_wait_warp(bar(S::B_VFULL + s), (uint32_t)(u / S::STAGES) & 1u, g, 0x204))) {
+                                     !mbar_wait_warp(bar(S::B_VFULL + st), (uint32_t)(u / S::STAGES) & 1u, g, 0x204))) {
                                     ok = false;
                                     break;
                                 }
@@ -333,41 +433,46 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                                 tc_fence_after();
                                 const uint32_t p_tmem = tmem + S::TM_S + 128u * (uint32_t)x;
                                 const uint32_t o_tmem = tmem + S::TM_O + (uint32_t)(D * x);
-                                const uint64_t vd = sdesc_add(dv0, (uint32_t)(s * S::KV_TILE_BYTES));
-                                const uint32_t acc0 = nv[x] > 0 ? 1u : 0u;
+                                const uint64_t vd = sdesc_add(dv0, (uint32_t)(st * S::KV_TILE_BYTES));
+                                const uint32_t acc0 = nvi[x] > 0 ? 1u : 0u;
 #pragma unroll
-                                for (int k = 0; k < BC / 16; ++k)
-                                    mma_ts_elect(o_tmem, p_tmem + (uint32_t)k * 8u, sdesc_add(vd, (uint32_t)k * 2048u),
-                                           IDESC_PV, k > 0 ? 1u : acc0);
+                                for (int kk = 0; kk < BC / 16; ++kk)
+                                    mma_ts_elect(o_tmem, p_tmem + (uint32_t)kk * 8u, sdesc_add(vd, (uint32_t)kk * 2048u),
+                                                 IDESC_PV, kk > 0 ? 1u : acc0);
                                 mma_commit_elect(bar(S::B_PVDONE + x));
                                 ++nv[x];
+                                ++nvi[x];
                             }
-                            if (kt_next < Tk && cls(x, kt_next) != kTileSkip) {
-                                if (!kwaited && !mbar_wait_warp(bar(S::B_KFULL + s2), (uint32_t)((u + 1) / S::STAGES) & 1u,
-                                                           g, 0x205)) {
+                            if (more && entry_vis(it, lst, x, e + 1)) {
+                                if (!kwaited && !mbar_wait_warp(bar(S::B_KFULL + st2), (uint32_t)((u + 1) / S::STAGES) & 1u,
+                                                                g, 0x205)) {
                                     ok = false;
                                     break;
                                 }
                                 kwaited = true;
-                                if (nv[x] > 0 && !mbar_wait_warp(bar(S::B_PVDONE + x), (uint32_t)(nv[x] - 1) & 1u, g, 0x206)) {
+                                if (nv[x] > 0 &&
+                                    !mbar_wait_warp(bar(S::B_PVDONE + x), (uint32_t)(nv[x] - 1) & 1u, g, 0x206)) {
                                     ok = false;
                                     break;
                                 }
                                 tc_fence_after();
-                                issue_s(x, s2);
+                                issue_s(x, st2);
                             }
                         }
                         if (!ok) break;
-                        // K and V of stage s are free once this tile's products are done
-                        mma_commit_elect(bar(S::B_KVEMPTY + s));
-                        kt = kt_next;
-                        ++u;
+                        // the item's last S products were issued just now: Q is free once they finish
+                        if (e + 2 == it.count) mma_commit_elect(bar(S::B_QEMPTY));
+                        // K and V of stage st are free once this tile's products are done
+                        mma_commit_elect(bar(S::B_KVEMPTY + st));
                     }
                 }
-                // every MMA this thread issued must finish before TMEM is freed
-                mma_commit_elect(bar(S::B_FIN));
-                drain_wait(bar(S::B_FIN), 0);
+                if (!ok) break;
+                // every field of the slot has been read
+                if (lane == 0) mbar_arrive(bar(S::B_ITEMFREE + s));
             }
+            // every MMA this thread issued must finish before TMEM is freed
+            mma_commit_elect(bar(S::B_FIN));
+            drain_wait(bar(S::B_FIN), 0);
         }
     } else {
         setmaxnreg_inc<S::REGS_SOFTMAX>();
@@ -375,151 +480,189 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
         const int x = (warp - 4) >> 2;
         const int wq = warp & 3;
         const int r = wq * 32 + lane;
-        const int q0x = q0_of(x), qnx = qn_of(x);
-        const int q = q0x + r;
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const uint32_t s_tmem = tmem + lane_off + S::TM_S + 128u * (uint32_t)x;
         const uint32_t o_tmem = tmem + lane_off + S::TM_O + (uint32_t)(D * x);
         const float c2 = p.scale_log2;
-        float m_ref = -INFINITY, l = 0.f;
-        int it = 0;
         bool ok = true;
-        for (int kt = next_tile(x, -1); kt < Tk; kt = next_tile(x, kt), ++it) {
-            const bool partial = cls(x, kt) == kTilePartial;
-            const int k0 = kt * BC;
-            if (!mbar_wait_warp(bar(S::B_SFULL + x), (uint32_t)it & 1u, g, 0x401)) {
+        int ns = 0;                                  // S tiles of query tile x so far (all items)
+        for (int k = 0;; ++k) {
+            const int s = k & 1;
+            if (!mbar_wait_warp(bar(S::B_ITEM + s), (uint32_t)(k >> 1) & 1u, g, 0x400)) {
                 ok = false;
                 break;
             }
-            tc_fence_after();
-            uint32_t sr[S::KC][32];
-#pragma unroll
-            for (int j = 0; j < S::KC; ++j) tmem_ld32(s_tmem + 32u * j, sr[j]);
-#pragma unroll
-            for (int j = 0; j < S::KC; ++j) tmem_ld_wait(sr[j]);
-            if (partial) {
-#pragma unroll
-                for (int j = 0; j < S::KC; ++j)
-#pragma unroll
-                    for (int t = 0; t < 32; ++t) {
-                        const int key = k0 + 32 * j + t;
-                        if (key >= kvis || (p.causal && key > q + shift)) sr[j][t] = __float_as_uint(-INFINITY);
-                    }
-            }
-            // row maximum as eight independent 3-input chains, then a tree:
-            // one warp per sub-partition runs this, so the latency of a single
-            // 64-deep chain would sit on the critical path
-            float pm[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) pm[u] = -INFINITY;
-#pragma unroll
-            for (int j = 0; j < S::KC; ++j)
-#pragma unroll
-                for (int t = 0; t < 32; t += 4) {
-                    const int u = (j * 8 + t / 4) & 7;
-                    pm[u] = fmax3(pm[u], __uint_as_float(sr[j][t]), __uint_as_float(sr[j][t + 1]));
-                    pm[u] = fmax3(pm[u], __uint_as_float(sr[j][t + 2]), __uint_as_float(sr[j][t + 3]));
-                }
-            const float mx = fmaxf(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], fmax3(pm[5], pm[6], pm[7])));
-            // move the reference maximum only when the row outgrew it by 2^8
-            const float m_tile = mx * c2;
-            const bool grow = m_tile > m_ref + kRescaleLog2;
-            float alpha = 1.f;
-            const bool rescale = __any_sync(0xffffffffu, grow);
-            if (rescale) {
-                const float m_new = fmaxf(m_ref, m_tile);
-                alpha = (m_new == -INFINITY) ? 1.f : ex2(m_ref - m_new);
-                l *= alpha;
-                m_ref = m_new;
-            }
-            const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-            // p = 2^(s * c - m), bf16 into the first 64 columns of S_x; the row
-            // sum in four independent packed accumulators
-            float ps[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) ps[u] = 0.f;
-#pragma unroll
-            for (int j = 0; j < S::KC; ++j) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int t = 0; t < 16; ++t) {
-                    float a, bb;
-                    fma2(a, bb, __uint_as_float(sr[j][2 * t]), __uint_as_float(sr[j][2 * t + 1]), c2, c2, -m_use, -m_use);
-                    a = ex2(a);
-                    bb = ex2(bb);
-                    const int u = 2 * (t & 3);
-                    add2(ps[u], ps[u + 1], a, bb);
-                    pk[t] = pack_bf16x2(a, bb);
-                }
-                tmem_st16(s_tmem + 16u * j, pk);
-            }
-            l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-            tmem_st_wait();
-            if (rescale && it > 0) {
-                // O_x may be rescaled only once the previous P_x V has landed
-                if (!mbar_wait_warp(bar(S::B_PVDONE + x), (uint32_t)(it - 1) & 1u, g, 0x402)) {
+            const FwdItem &itr = slots[s];
+            const int item = itr.item;
+            if (item < 0) break;
+            const uint16_t *lst = list_of(s);
+            const int q0x = x ? itr.q0[1] : itr.q0[0], qnx = x ? itr.qn[1] : itr.qn[0];
+            const int kvis = itr.kvis, shift = itr.shift, count = itr.count, bh = itr.bh, h = itr.h;
+            const int q_start = itr.q_start;
+            const int use_list = itr.use_list, kendx = x ? itr.kend[1] : itr.kend[0];
+            const int q = q0x + r;
+            float m_ref = -INFINITY, l = 0.f;
+            int it = 0;                              // this item's tiles
+            for (int e = 0; e < count; ++e) {
+                const bool vis = use_list ? ((lst[e] >> (14 + x)) & 1u) : (e < kendx);
+                if (!vis) continue;
+                const int kt = use_list ? (int)(lst[e] & 0x3FFFu) : e;
+                const int k0 = kt * BC;
+                unsigned klass;
+                if constexpr (VARLEN)
+                    klass = tile_class_shift(q0x, qnx, k0, BC, kvis, p.causal, shift);
+                else
+                    klass = tile_class(q0x, qnx, k0, BC, kvis, p.causal, 1);
+                const bool partial = klass == kTilePartial;
+                if (!mbar_wait_warp(bar(S::B_SFULL + x), (uint32_t)ns & 1u, g, 0x401)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                // O_x is D columns: D / 32 chunks of 32, loaded up to four at a time
-                constexpr int RC = (D / 32 < 4) ? D / 32 : 4;
+                uint32_t sr[S::KC][32];
 #pragma unroll
-                for (int j0 = 0; j0 < D / 32; j0 += RC) {
-                    uint32_t o[RC][32];
+                for (int j = 0; j < S::KC; ++j) tmem_ld32(s_tmem + 32u * j, sr[j]);
 #pragma unroll
-                    for (int j = 0; j < RC; ++j) tmem_ld32(o_tmem + 32u * (j0 + j), o[j]);
+                for (int j = 0; j < S::KC; ++j) tmem_ld_wait(sr[j]);
+                if (partial) {
 #pragma unroll
-                    for (int j = 0; j < RC; ++j) tmem_ld_wait(o[j]);
+                    for (int j = 0; j < S::KC; ++j)
 #pragma unroll
-                    for (int j = 0; j < RC; ++j) {
-#pragma unroll
-                        for (int t = 0; t < 32; t += 2) {
-                            float a, bb;
-                            fma2(a, bb, __uint_as_float(o[j][t]), __uint_as_float(o[j][t + 1]), alpha, alpha, 0.f, 0.f);
-                            o[j][t] = __float_as_uint(a);
-                            o[j][t + 1] = __float_as_uint(bb);
+                        for (int t = 0; t < 32; ++t) {
+                            const int key = k0 + 32 * j + t;
+                            if (key >= kvis || (p.causal && key > q + shift)) sr[j][t] = __float_as_uint(-INFINITY);
                         }
-                        tmem_st32(o_tmem + 32u * (j0 + j), o[j]);
+                }
+                // row maximum as eight independent 3-input chains, then a tree:
+                // one warp per sub-partition runs this, so the latency of a single
+                // 64-deep chain would sit on the critical path
+                float pm[8];
+#pragma unroll
+                for (int uu = 0; uu < 8; ++uu) pm[uu] = -INFINITY;
+#pragma unroll
+                for (int j = 0; j < S::KC; ++j)
+#pragma unroll
+                    for (int t = 0; t < 32; t += 4) {
+                        const int uu = (j * 8 + t / 4) & 7;
+                        pm[uu] = fmax3(pm[uu], __uint_as_float(sr[j][t]), __uint_as_float(sr[j][t + 1]));
+                        pm[uu] = fmax3(pm[uu], __uint_as_float(sr[j][t + 2]), __uint_as_float(sr[j][t + 3]));
+                    }
+                const float mx = fmaxf(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], fmax3(pm[5], pm[6], pm[7])));
+                // move the reference maximum only when the row outgrew it by 2^8
+                const float m_tile = mx * c2;
+                const bool grow = m_tile > m_ref + kRescaleLog2;
+                float alpha = 1.f;
+                const bool rescale = __any_sync(0xffffffffu, grow);
+                if (rescale) {
+                    const float m_new = fmaxf(m_ref, m_tile);
+                    alpha = (m_new == -INFINITY) ? 1.f : ex2(m_ref - m_new);
+                    l *= alpha;
+                    m_ref = m_new;
+                }
+                const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+                // p = 2^(s * c - m), bf16 into the first half of S_x's columns;
+                // the row sum in four independent packed accumulators
+                float ps[8];
+#pragma unroll
+                for (int uu = 0; uu < 8; ++uu) ps[uu] = 0.f;
+#pragma unroll
+                for (int j = 0; j < S::KC; ++j) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) {
+                        float a, bb;
+                        fma2(a, bb, __uint_as_float(sr[j][2 * t]), __uint_as_float(sr[j][2 * t + 1]), c2, c2, -m_use,
+                             -m_use);
+                        a = ex2(a);
+                        bb = ex2(bb);
+                        const int uu = 2 * (t & 3);
+                        add2(ps[uu], ps[uu + 1], a, bb);
+                        pk[t] = pack_bf16x2(a, bb);
+                    }
+                    tmem_st16(s_tmem + 16u * j, pk);
+                }
+                l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+                tmem_st_wait();
+                if (rescale && it > 0) {
+                    // O_x may be rescaled only once the previous P_x V has landed
+                    if (!mbar_wait_warp(bar(S::B_PVDONE + x), (uint32_t)(ns - 1) & 1u, g, 0x402)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    // O_x is D columns: D / 32 chunks of 32, loaded up to four at a time
+                    constexpr int RC = (D / 32 < 4) ? D / 32 : 4;
+#pragma unroll
+                    for (int j0 = 0; j0 < D / 32; j0 += RC) {
+                        uint32_t o[RC][32];
+#pragma unroll
+                        for (int j = 0; j < RC; ++j) tmem_ld32(o_tmem + 32u * (j0 + j), o[j]);
+#pragma unroll
+                        for (int j = 0; j < RC; ++j) tmem_ld_wait(o[j]);
+#pragma unroll
+                        for (int j = 0; j < RC; ++j) {
+#pragma unroll
+                            for (int t = 0; t < 32; t += 2) {
+                                float a, bb;
+                                fma2(a, bb, __uint_as_float(o[j][t]), __uint_as_float(o[j][t + 1]), alpha, alpha, 0.f,
+                                     0.f);
+                                o[j][t] = __float_as_uint(a);
+                                o[j][t + 1] = __float_as_uint(bb);
+                            }
+                            tmem_st32(o_tmem + 32u * (j0 + j), o[j]);
+                        }
+                    }
+                    tmem_st_wait();
+                }
+                tc_fence_before();
+                mbar_arrive(bar(S::B_PFULL + x));
+                ++ns;
+                ++it;
+            }
+            if (!ok) break;
+            // ---------------------------------------------------------- epilogue of the item
+            // (the next item's first P.V into O_x is issued only after this
+            // warpgroup's next P arrival, which follows these loads)
+            if (it > 0) {
+                if (!mbar_wait_warp(bar(S::B_PVDONE + x), (uint32_t)(ns - 1) & 1u, g, 0x403)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+            }
+            if (qnx > 0) {
+                const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+                const size_t orow_idx = VARLEN ? (size_t)(q_start + q) * p.H + h : (size_t)bh * p.N + q;
+                __nv_bfloat16 *orow = reinterpret_cast<__nv_bfloat16 *>(p.O) + orow_idx * D;
+#pragma unroll 1
+                for (int j = 0; j < D / 32; ++j) {
+                    uint32_t o[32];
+                    if (it > 0) {
+                        tmem_ld32(o_tmem + 32u * j, o);
+                        tmem_ld_wait(o);
+                    } else {
+#pragma unroll
+                        for (int t = 0; t < 32; ++t) o[t] = 0u;
+                    }
+                    uint32_t w[16];
+#pragma unroll
+                    for (int t = 0; t < 16; ++t)
+                        w[t] = pack_bf16x2(__uint_as_float(o[2 * t]) * inv_l, __uint_as_float(o[2 * t + 1]) * inv_l);
+                    if (r < qnx) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * j);
+#pragma unroll
+                        for (int t = 0; t < 4; ++t)
+                            dst[t] = make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
                     }
                 }
-                tmem_st_wait();
+                if (r < qnx)
+                    p.LSE[VARLEN ? (size_t)h * p.total_q + q_start + q : (size_t)bh * p.N + q] =
+                        (l > 0.f) ? (m_ref + log2f(l)) * 0.69314718055994530942f : -INFINITY;
             }
             tc_fence_before();
-            mbar_arrive(bar(S::B_PFULL + x));
-        }
-        // ---------------------------------------------------------- epilogue
-        if (ok && it > 0) {
-            ok = mbar_wait_warp(bar(S::B_PVDONE + x), (uint32_t)(it - 1) & 1u, g, 0x403);
-            tc_fence_after();
-        }
-        if (ok) {
-            const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-            const size_t orow_idx = VARLEN ? (size_t)(q_start + q) * p.H + h : (size_t)bh * p.N + q;
-            __nv_bfloat16 *orow = reinterpret_cast<__nv_bfloat16 *>(p.O) + orow_idx * D;
-#pragma unroll 1
-            for (int j = 0; j < D / 32; ++j) {
-                uint32_t o[32];
-                if (it > 0) {
-                    tmem_ld32(o_tmem + 32u * j, o);
-                    tmem_ld_wait(o);
-                } else {
-#pragma unroll
-                    for (int t = 0; t < 32; ++t) o[t] = 0u;
-                }
-                uint32_t w[16];
-#pragma unroll
-                for (int t = 0; t < 16; ++t)
-                    w[t] = pack_bf16x2(__uint_as_float(o[2 * t]) * inv_l, __uint_as_float(o[2 * t + 1]) * inv_l);
-                if (r < qnx) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * j);
-#pragma unroll
-                    for (int t = 0; t < 4; ++t) dst[t] = make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
-                }
-            }
-            if (r < qnx)
-                p.LSE[VARLEN ? (size_t)h * p.total_q + q_start + q : (size_t)bh * p.N + q] =
-                    (l > 0.f) ? (m_ref + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+            __syncwarp();
+            // every field of the slot has been read
+            if (lane == 0) mbar_arrive(bar(S::B_ITEMFREE + s));
         }
         __syncwarp();
         setmaxnreg_dec<S::REGS_CTRL>();
@@ -531,6 +674,17 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
     if (warp == 1) tmem_dealloc(tmem, S::TMEM_COLS);
 }
 
+int device_sm_count() {
+    constexpr int kMaxDev = 64;
+    static int cached[kMaxDev] = {};
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (dev >= 0 && dev < kMaxDev && cached[dev] > 0) return cached[dev];
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+    if (dev >= 0 && dev < kMaxDev) cached[dev] = n;
+    return n;
+}
+
 int fwd_smem_bytes(int d) { return d == 64 ? FwdShape<64>::SMEM_BYTES : FwdShape<128>::SMEM_BYTES; }
 
 template <int D, bool VARLEN, int BC, int QPC>
@@ -540,7 +694,10 @@ static cudaError_t launch_fwd_t(const FwdParams &p, cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D, VARLEN, BC, QPC>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    const unsigned grid = (unsigned)((p.Tq + QPC - 1) / QPC) * (unsigned)p.BH;
+    // persistent: one CTA per SM (the shared-memory footprint allows one),
+    // never more CTAs than work items
+    const int64_t items = (int64_t)((p.Tq + QPC - 1) / QPC) * p.BH;
+    const unsigned grid = (unsigned)std::min<int64_t>(items, device_sm_count());
     fa_fwd_kernel<D, VARLEN, BC, QPC><<<grid, S::THREADS, smem, st>>>(p);
     return cudaGetLastError();
 }

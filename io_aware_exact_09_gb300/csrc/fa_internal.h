@@ -9,7 +9,11 @@
 
 namespace fa {
 
-// Forward: one CTA per (query tile, b*h).
+// Multiprocessor count of the current device (cached per device).
+int device_sm_count();
+
+// Forward: a persistent grid of at most one CTA per SM over (query-tile pair,
+// b*h) work items; the workspace's words 2 and 3 hold its item counter.
 cudaError_t launch_fwd(int d, const FwdParams &p, cudaStream_t st);
 int fwd_smem_bytes(int d);
 // Forward with a chosen key-tile width (64 or 128); p.qpc sets the query
@@ -28,11 +32,14 @@ cudaError_t launch_quant_fp8(int d, const void *X, void *Y, float *scales, int B
 cudaError_t launch_bwd_pre(int d, const void *O, const void *dO, float *Dvec, float *dQacc,
                            int64_t rows, cudaStream_t st);
 cudaError_t launch_bwd_main(int d, const BwdParams &p, cudaStream_t st);
+// Ragged batches: packed [total][H][d] sequences (cu_q, cu_k offsets).
+cudaError_t launch_bwd_main_varlen(int d, const BwdParams &p, cudaStream_t st);
 cudaError_t launch_bwd_convert(int d, const float *dQacc, void *dQ, int64_t elems, float scale,
                                cudaStream_t st);
 int bwd_query_block(int d);
 // d = 128: the 128-row query block kernel (fa_bwd128.cu).
 cudaError_t launch_bwd128_main(const BwdParams &p, cudaStream_t st);
+cudaError_t launch_bwd128_main_varlen(const BwdParams &p, cudaStream_t st);
 int bwd128_smem_bytes();
 int bwd_dq_box_rows(int d);
 int bwd_smem_bytes(int d);

@@ -127,11 +127,37 @@ struct BwdParams {
     void *dK, *dV;                   // bf16 [BH][N][d]
     const int32_t *key_len;
     const uint8_t *block_mask;
+    // ragged batches only: sequence b owns query rows cu_q[b]..cu_q[b+1]-1 of
+    // Q, dO, dQ [total_q][H][d] and key rows cu_k[b]..cu_k[b+1]-1 of K, V, dK,
+    // dV [total_k][H][d]; LSE is [H][total_q], D and the dQ accumulator follow
+    // the [total_q][H] row order; the maps view [total][H][d] (box {64, 1, rows},
+    // the accumulator {32, 1, 32})
+    const int32_t *cu_q, *cu_k;
+    int total_q, total_k;
     unsigned *status;
-    int H, N, BH, Tk, Tqb;           // Tqb = ceil(N / BQ)
+    int H, N, BH, Tk, Tqb;           // Tqb = ceil(N / BQ); ragged: Tk covers the longest key sequence
     int causal;
     float scale_log2;                // softmax_scale * log2(e)
     float scale;                     // softmax_scale
 };
+
+// The sequence a CTA of a ragged batch works on: query rows [q_start,
+// q_start + Lq), key rows [k_start, k_start + Lk).  Offsets outside [0, total]
+// or negative lengths, or a key length past the grid's key tiles (max_k_rows),
+// make it invalid: *bad is set and both lengths become 0 (the sequence is
+// skipped).
+__device__ __forceinline__ void varlen_sequence(const int32_t *cu_q, const int32_t *cu_k, int b, int total_q,
+                                                int total_k, int max_q_rows, int max_k_rows, int *q_start,
+                                                int *Lq, int *k_start, int *Lk, bool *bad) {
+    *q_start = cu_q[b];
+    *Lq = cu_q[b + 1] - *q_start;
+    *k_start = cu_k[b];
+    *Lk = cu_k[b + 1] - *k_start;
+    if (*q_start < 0 || *Lq < 0 || *q_start + *Lq > total_q || *k_start < 0 || *Lk < 0 ||
+        *k_start + *Lk > total_k || *Lq > max_q_rows || *Lk > max_k_rows) {
+        *bad = true;
+        *Lq = *Lk = 0;
+    }
+}
 
 }  // namespace fa

@@ -251,68 +251,138 @@ def run_bwd128(seed, n):
 
 
 # ---------------------------------------------------------------- bf16 forward
-# `fa_fwd_kernel`: P overwrites S in TMEM, so one issuer alternates the query
-# tiles: per key tile and query tile x, O_x += P_x V once P_x is written, then
-# the next tile's S_x once that product has read P_x.
+# `fa_fwd_kernel`, persistent: the producer takes work items one after
+# another and publishes each in one of two slots (ITEM), reusing a slot once
+# every consumer has released it (ITEMFREE: the issuer and both softmax
+# warpgroups); it loads an item's Q once the previous item's S products are
+# done (QEMPTY, committed after the item's last S) and streams the item's key
+# tiles through the ring.  An item lists `count` key-tile entries, and query
+# tile x sees entry e iff vis[x][e].  P overwrites S in TMEM, so the issuer
+# alternates the query tiles: per entry and query tile x, O_x += P_x V once
+# P_x is written, then the next entry's S_x once that product has read P_x
+# (also across items: the first S_x of an item waits for the previous item's
+# last P_x V).  Every counter (ring uses, S, P.V, loaded items) runs on across
+# items.
 
-def fwd_producer(n_tiles, stages):
-    total = max(n_tiles)
-    if total:
+def fwd_producer(items, stages, q_empty_wait=True, slot_free_wait=True):
+    m = u = 0
+    for k, it in enumerate(list(items) + [None]):
+        if k >= 2 and slot_free_wait:
+            yield ("wait", ("ITEMFREE", k & 1), ((k >> 1) - 1) & 1, (k >> 1) - 1)
+        yield ("arrive", ("ITEM", k & 1))
+        if it is None:
+            return
+        count, _ = it
+        if not count:
+            continue
+        if m > 0 and q_empty_wait:
+            yield ("wait", "QEMPTY", (m - 1) & 1, m - 1)
         yield ("tma", "QFULL")
-    for u in range(total):
-        s, k = u % stages, u // stages
-        yield ("wait", ("KVEMPTY", s), (k & 1) ^ 1, k - 1)
-        yield ("tma", ("KFULL", s))
-        yield ("tma", ("VFULL", s))
+        m += 1
+        for _ in range(count):
+            s, kk = u % stages, u // stages
+            yield ("wait", ("KVEMPTY", s), (kk & 1) ^ 1, kk - 1)
+            yield ("tma", ("KFULL", s))
+            yield ("tma", ("VFULL", s))
+            u += 1
 
 
-def fwd_issuer(n_tiles, stages):
-    total = max(n_tiles)
+def fwd_issuer(items, stages):
+    m = u = 0
     nv = [0, 0]
-    if not total:
-        return
-    yield ("wait", "QFULL", 0, 0)
-    yield ("wait", ("KFULL", 0), 0, 0)
-    for x in range(2):
-        if n_tiles[x] > 0:
-            yield ("commit", ("SFULL", x))
-    for u in range(total):
-        s, s2 = u % stages, (u + 1) % stages
-        vwaited = kwaited = False
-        for x in range(2):
-            if u < n_tiles[x]:
-                yield ("wait", ("PFULL", x), nv[x] & 1, nv[x])
-                if not vwaited:
-                    yield ("wait", ("VFULL", s), (u // stages) & 1, u // stages)
-                    vwaited = True
-                yield ("commit", ("PVDONE", x))
-                nv[x] += 1
-            if u + 1 < n_tiles[x]:
-                if not kwaited:
-                    k = (u + 1) // stages
-                    yield ("wait", ("KFULL", s2), k & 1, k)
-                    kwaited = True
-                yield ("wait", ("PVDONE", x), (nv[x] - 1) & 1, nv[x] - 1)
-                yield ("commit", ("SFULL", x))
-        yield ("commit", ("KVEMPTY", s))
+    for k, it in enumerate(list(items) + [None]):
+        yield ("wait", ("ITEM", k & 1), (k >> 1) & 1, k >> 1)
+        if it is None:
+            return
+        count, vis = it
+        if count:
+            yield ("wait", "QFULL", m & 1, m)
+            m += 1
+            yield ("wait", ("KFULL", u % stages), (u // stages) & 1, u // stages)
+            for x in range(2):
+                if vis[x][0]:
+                    if nv[x] > 0:
+                        yield ("wait", ("PVDONE", x), (nv[x] - 1) & 1, nv[x] - 1)
+                    yield ("commit", ("SFULL", x))
+            if count == 1:
+                yield ("commit", "QEMPTY")
+            for e in range(count):
+                s, s2 = u % stages, (u + 1) % stages
+                vwaited = kwaited = False
+                for x in range(2):
+                    if vis[x][e]:
+                        yield ("wait", ("PFULL", x), nv[x] & 1, nv[x])
+                        if not vwaited:
+                            yield ("wait", ("VFULL", s), (u // stages) & 1, u // stages)
+                            vwaited = True
+                        yield ("commit", ("PVDONE", x))
+                        nv[x] += 1
+                    if e + 1 < count and vis[x][e + 1]:
+                        if not kwaited:
+                            kk = (u + 1) // stages
+                            yield ("wait", ("KFULL", s2), kk & 1, kk)
+                            kwaited = True
+                        if nv[x] > 0:
+                            yield ("wait", ("PVDONE", x), (nv[x] - 1) & 1, nv[x] - 1)
+                        yield ("commit", ("SFULL", x))
+                if e + 2 == count:
+                    yield ("commit", "QEMPTY")
+                yield ("commit", ("KVEMPTY", s))
+                u += 1
+        yield ("arrive", ("ITEMFREE", k & 1))
 
 
-def fwd_softmax(x, n, rng, p_rescale):
-    for it in range(n):
-        yield ("wait", ("SFULL", x), it & 1, it)
-        if it > 0 and rng.random() < p_rescale:
-            yield ("wait", ("PVDONE", x), (it - 1) & 1, it - 1)
-        yield ("arrive", ("PFULL", x))
-    if n:
-        yield ("wait", ("PVDONE", x), (n - 1) & 1, n - 1)
+def fwd_softmax(x, items, rng, p_rescale):
+    ns = 0
+    for k, it in enumerate(list(items) + [None]):
+        yield ("wait", ("ITEM", k & 1), (k >> 1) & 1, k >> 1)
+        if it is None:
+            return
+        count, vis = it
+        n_item = 0
+        for e in range(count):
+            if not vis[x][e]:
+                continue
+            yield ("wait", ("SFULL", x), ns & 1, ns)
+            if n_item > 0 and rng.random() < p_rescale:
+                yield ("wait", ("PVDONE", x), (ns - 1) & 1, ns - 1)
+            yield ("arrive", ("PFULL", x))
+            ns += 1
+            n_item += 1
+        if n_item:
+            yield ("wait", ("PVDONE", x), (ns - 1) & 1, ns - 1)
+        yield ("arrive", ("ITEMFREE", k & 1))
 
 
-def run_fwd(seed, n_tiles, stages, p_rescale=0.3):
+def fwd_items(rng, n_items):
+    """Random work items: without a block mask query tile x sees the first
+    n_x key tiles (count = max n_x); under one, an arbitrary subset of the
+    listed tiles (each listed tile seen by at least one query tile); the last
+    query tile of an odd count has no rows."""
+    items = []
+    for _ in range(n_items):
+        count = rng.choice([0, 1, 1, 2, 3, 4, 7])
+        two = rng.random() < 0.8
+        if rng.random() < 0.5:
+            n = [rng.randint(0, count), rng.randint(0, count) if two else 0]
+            n[rng.randrange(2) if two else 0] = count
+            vis = [[e < n[x] for e in range(count)] for x in range(2)]
+        else:
+            vis = [[False] * count, [False] * count]
+            for e in range(count):
+                b = rng.choice([1, 2, 3]) if two else 1
+                vis[0][e], vis[1][e] = bool(b & 1), bool(b & 2)
+        items.append((count, vis))
+    return items
+
+
+def run_fwd(seed, stages, n_items=None, p_rescale=0.3, **producer_kw):
     rng = random.Random(seed)
-    roles = {"producer": fwd_producer(n_tiles, stages), "issuer": fwd_issuer(n_tiles, stages),
-             "softmax0": fwd_softmax(0, n_tiles[0], rng, p_rescale),
-             "softmax1": fwd_softmax(1, n_tiles[1], rng, p_rescale)}
-    schedule(rng, roles, lambda name: 1)
+    items = fwd_items(rng, n_items if n_items is not None else rng.randint(1, 7))
+    roles = {"producer": fwd_producer(items, stages, **producer_kw), "issuer": fwd_issuer(items, stages),
+             "softmax0": fwd_softmax(0, items, rng, p_rescale),
+             "softmax1": fwd_softmax(1, items, rng, p_rescale)}
+    schedule(rng, roles, lambda name: 3 if name[0] == "ITEMFREE" else 1)
 
 
 # ---------------------------------------------------------------- split-KV decode
@@ -459,8 +529,32 @@ def test_model_finds_the_alias_of_one_pready_barrier_per_query_tile():
 
 
 def test_bf16_forward_protocol_never_aliases():
-    for i in range(600):
-        run_fwd(seed=i, n_tiles=TILE_COUNTS[i % len(TILE_COUNTS)], stages=(2, 4)[i % 2])
+    for i in range(800):
+        run_fwd(seed=i, stages=(2, 4)[i % 2])
+
+
+def test_forward_model_finds_a_dropped_q_empty_wait():
+    """Loading the next item's Q without waiting for the previous item's S
+    products lets the Q-ready barrier run two phases ahead of the issuer."""
+    found = []
+    for i in range(400):
+        try:
+            run_fwd(seed=i, stages=(2, 4)[i % 2], n_items=6, q_empty_wait=False)
+        except Alias as e:
+            found.append(str(e))
+    assert found and all(" on QFULL" in f for f in found), found[:3]
+
+
+def test_forward_model_finds_a_dropped_slot_free_wait():
+    """Publishing an item into a slot a slow consumer has not yet released
+    lets that slot's barrier run two phases ahead of the consumer."""
+    found = []
+    for i in range(400):
+        try:
+            run_fwd(seed=i, stages=(2, 4)[i % 2], n_items=7, slot_free_wait=False)
+        except Alias as e:
+            found.append(str(e))
+    assert found and all("('ITEM'" in f for f in found), found[:3]
 
 
 def test_forward_model_finds_s_issued_before_p_is_awaited():
@@ -504,7 +598,8 @@ def test_forward_model_finds_s_issued_before_p_is_awaited():
     found = []
     for i in range(600):
         n_tiles, stages = TILE_COUNTS[i % len(TILE_COUNTS)], (2, 4)[i % 2]
-        roles = {"producer": fwd_producer(n_tiles, stages), "issuer": issuer_s_first(n_tiles, stages),
+        one_item = [(max(n_tiles), [[e < n_tiles[x] for e in range(max(n_tiles))] for x in range(2)])]
+        roles = {"producer": fwd_producer(one_item, stages), "issuer": issuer_s_first(n_tiles, stages),
                  "softmax0": softmax_releasing_s(0, n_tiles[0]), "softmax1": softmax_releasing_s(1, n_tiles[1])}
         try:
             schedule(random.Random(i), roles, lambda name: 1)

@@ -125,6 +125,33 @@ def test_repeat_calls_are_deterministic_forward():
 
 
 @pytest.mark.parametrize("d", [64, 128])
+def test_forward_work_counter_resets_and_reuse_is_exact(d):
+    """The persistent forward hands out its work items from a counter in the
+    workspace (words 2 and 3) and every launch leaves it at zero: launches
+    that reuse one workspace, with more items than SMs and with fewer, give
+    bit-identical results and leave the counter at zero each time."""
+    import io_aware_exact_09_gb300 as fa
+    ws = fa.workspace(256, "cuda")
+    for B, H, N in ((4, 16, 1024), (1, 1, 300), (2, 8, 2000)):
+        c = make_case(B, H, N, d, seed=B + N, causal=True)
+        g = {k: c[k].cuda() for k in ("Q", "K", "V")}
+        outs = []
+        for _ in range(3):
+            O, L = fa.attention_forward(g["Q"], g["K"], g["V"], c["scale"], True, ws=ws)
+            torch.cuda.synchronize()
+            assert int(ws[8:16].view(torch.int32).abs().sum()) == 0, (B, H, N)
+            outs.append((O.clone(), L.clone()))
+        assert fa.fa_get_device_status(ws) == 0
+        for O, L in outs[1:]:
+            assert torch.equal(O, outs[0][0]) and torch.equal(L, outs[0][1]), (B, H, N)
+        ref_O, ref_L = oracle.attention_fwd(f64(c["Q"]), f64(c["K"]), f64(c["V"]), c["scale"], causal=True) \
+            if B * H * N <= 2 * 16 * 1024 else (None, None)
+        if ref_O is not None:
+            check_forward(outs[0][0].double().cpu().numpy(), outs[0][1].double().cpu().numpy(), ref_O, ref_L,
+                          "reuse %d" % d)
+
+
+@pytest.mark.parametrize("d", [64, 128])
 def test_repeat_calls_are_deterministic_backward(d):
     # dK and dV are accumulated inside one CTA (no atomics): repeated calls
     # must agree bit for bit; a race between the compute warps shows up here
