@@ -13,7 +13,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libfa_gb300.so")
-SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_fwd_fp8.cu", "fa_bwd.cu", "fa_bwd128.cu", "fa_decode.cu", "fa_quant.cu", "fa_selftest.cu", "fa_noalloc.cu"]
+SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_fwd_fp8.cu", "fa_bwd.cu", "fa_bwd64.cu", "fa_bwd128.cu", "fa_decode.cu", "fa_quant.cu", "fa_selftest.cu", "fa_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
                 "--expt-relaxed-constexpr", "-I", os.path.join(HERE, "..", "include")]
@@ -53,7 +53,7 @@ def _compile(src: str) -> str:
 # launch; a different allocation would make setmaxnreg.inc wait forever, so
 # the build refuses it.
 REGISTER_SPLIT_KERNELS = {"fa_fwd.cu": ("fa_fwd_kernel", 168), "fa_fwd_fp8.cu": ("fa_fwd_fp8_kernel", 168),
-                          "fa_bwd128.cu": ("fa_bwd128_kernel", 128)}
+                          "fa_bwd64.cu": ("fa_bwd64_kernel", 128), "fa_bwd128.cu": ("fa_bwd128_kernel", 128)}
 
 
 def _check_register_split(src: str) -> None:

@@ -414,6 +414,7 @@ fa_status fa_bwd_main(const void *Q, const void *K, const void *V, const float *
     const void *ptrs[] = {Q, K, V, LSE, dO, dK, dV};
     for (const void *x : ptrs)
         if (!x || !aligned16(x)) return FA_ERR_INVALID_ARGUMENT;
+    if (block_mask && (N + 127) / 128 > kFwdMaxMaskedKeyTiles) return FA_ERR_UNSUPPORTED;
     const BwdWs w = bwd_ws(workspace, B, H, N);
     const int BH = B * H;
     BwdParams p;

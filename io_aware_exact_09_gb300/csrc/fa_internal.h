@@ -37,6 +37,11 @@ cudaError_t launch_bwd_main_varlen(int d, const BwdParams &p, cudaStream_t st);
 cudaError_t launch_bwd_convert(int d, const float *dQacc, void *dQ, int64_t elems, float scale,
                                cudaStream_t st);
 int bwd_query_block(int d);
+// d = 64: the persistent kernel (fa_bwd64.cu); the workspace's words 2 and 3
+// hold its item counter.
+cudaError_t launch_bwd64_main(const BwdParams &p, cudaStream_t st);
+cudaError_t launch_bwd64_main_varlen(const BwdParams &p, cudaStream_t st);
+int bwd64_smem_bytes();
 // d = 128: the 128-row query block kernel (fa_bwd128.cu).
 cudaError_t launch_bwd128_main(const BwdParams &p, cudaStream_t st);
 cudaError_t launch_bwd128_main_varlen(const BwdParams &p, cudaStream_t st);

@@ -440,70 +440,122 @@ def run_decode(seed, n, stages, p_rescale=0.3):
 
 
 # ---------------------------------------------------------------- d = 64 backward
-# `fa_bwd_kernel<64>`: Q and dO double-buffered together, LSE/D per stage, S
-# and dP in their own TMEM columns, dQ into two TMEM buffers that the compute
-# warpgroups drain one block later (after the next block's dS).
+# `fa_bwd64_kernel`, persistent: work items (key tiles) published in two
+# slots as in the forward (the issuer, the compute warpgroups and the drain
+# warpgroup release a slot); K and V double-buffered per item (KVFULL /
+# KVFREE, the free commit after the item's products); Q and dO double-buffered
+# together, LSE/D per stage, S and dP in their own TMEM columns, dQ into two
+# TMEM buffers emptied by the drain warpgroup; an item's dK, dV complete at
+# ACC.  Block, stage and item counters run on across items; an item's first
+# S and dP wait for the previous block's dV and dK (SFREE, DPFREE).  The
+# producer's K/V-free wait guards data only (the issuer has waited for a
+# buffer's load before it releases the item slot, so the ready barrier cannot
+# run ahead): dropping it shows in the parity tests, not here.
 
-def bwd64_producer(n):
-    yield ("tma", "KV")
-    for i in range(n):
-        s = i & 1
-        yield ("wait", ("QEMPTY", s), ((i >> 1) & 1) ^ 1, (i >> 1) - 1)
-        yield ("tma", ("QFULL", s))
-        yield ("arrive", ("LSE", s))
-
-
-def bwd64_issuer(n):
-    if not n:
-        return
-    yield ("wait", "KV", 0, 0)
-    yield ("wait", ("QFULL", 0), 0, 0)
-    yield ("commit", "SFULL")
-    yield ("commit", "DPFULL")
-    for i in range(n):
-        s, more = i & 1, i + 1 < n
-        yield ("wait", "PFULL", i & 1, i)
-        yield ("commit", "SFREE")                                           # dV(i) read P
-        if more:
-            yield ("wait", ("QFULL", s ^ 1), ((i + 1) >> 1) & 1, (i + 1) >> 1)
-            yield ("wait", "SFREE", i & 1, i)
-            yield ("commit", "SFULL")                                       # S(i+1)
-        yield ("wait", "DSFULL", i & 1, i)
-        yield ("commit", "DPFREE")                                          # dK(i) read dS
-        yield ("commit", ("QEMPTY", s))
-        if i >= 2:
-            yield ("wait", ("DQFREE", s), ((i - 2) >> 1) & 1, (i - 2) >> 1)
-        yield ("commit", ("DQFULL", s))                                     # dQ(i)
-        if more:
-            yield ("wait", "DPFREE", i & 1, i)
-            yield ("commit", "DPFULL")                                      # dP(i+1)
-    yield ("commit", "ACC")
+def bwd64_producer(items, kv_free_wait=True):
+    i = nkv = 0
+    for k, n in enumerate(list(items) + [None]):
+        if k >= 2:
+            yield ("wait", ("ITEMFREE", k & 1), ((k >> 1) - 1) & 1, (k >> 1) - 1)
+        yield ("arrive", ("ITEM", k & 1))
+        if n is None:
+            return
+        if not n:
+            continue
+        b = nkv & 1
+        if nkv >= 2 and kv_free_wait:
+            yield ("wait", ("KVFREE", b), ((nkv >> 1) - 1) & 1, (nkv >> 1) - 1)
+        yield ("tma", ("KVFULL", b))
+        nkv += 1
+        for _ in range(n):
+            s = i & 1
+            yield ("wait", ("QEMPTY", s), ((i >> 1) & 1) ^ 1, (i >> 1) - 1)
+            yield ("tma", ("QFULL", s))
+            yield ("arrive", ("LSE", s))
+            i += 1
 
 
-def bwd64_compute(n):
-    def drain(j):
-        yield ("wait", ("DQFULL", j & 1), (j >> 1) & 1, j >> 1)
-        yield ("arrive", ("DQFREE", j & 1))
+def bwd64_issuer(items):
+    i = nkv = 0
+    for k, n in enumerate(list(items) + [None]):
+        yield ("wait", ("ITEM", k & 1), (k >> 1) & 1, k >> 1)
+        if n is None:
+            return
+        if n:
+            b = nkv & 1
+            yield ("wait", ("KVFULL", b), (nkv >> 1) & 1, nkv >> 1)
+            nkv += 1
+            yield ("wait", ("QFULL", i & 1), (i >> 1) & 1, i >> 1)
+            if i > 0:
+                yield ("wait", "SFREE", (i - 1) & 1, i - 1)
+            yield ("commit", "SFULL")
+            if i > 0:
+                yield ("wait", "DPFREE", (i - 1) & 1, i - 1)
+            yield ("commit", "DPFULL")
+            for e in range(n):
+                s, more = i & 1, e + 1 < n
+                yield ("wait", "PFULL", i & 1, i)
+                yield ("commit", "SFREE")                                       # dV(i) read P
+                if more:
+                    yield ("wait", ("QFULL", s ^ 1), ((i + 1) >> 1) & 1, (i + 1) >> 1)
+                    yield ("wait", "SFREE", i & 1, i)
+                    yield ("commit", "SFULL")                                   # S(i+1)
+                yield ("wait", "DSFULL", i & 1, i)
+                yield ("commit", "DPFREE")                                      # dK(i) read dS
+                yield ("commit", ("QEMPTY", s))
+                if i >= 2:
+                    yield ("wait", ("DQFREE", s), ((i - 2) >> 1) & 1, (i - 2) >> 1)
+                yield ("commit", ("DQFULL", s))                                 # dQ(i)
+                if more:
+                    yield ("wait", "DPFREE", i & 1, i)
+                    yield ("commit", "DPFULL")                                  # dP(i+1)
+                i += 1
+            yield ("commit", "ACC")
+            yield ("commit", ("KVFREE", b))
+        yield ("arrive", ("ITEMFREE", k & 1))
 
-    for i in range(n):
-        yield ("wait", ("LSE", i & 1), (i >> 1) & 1, i >> 1)
-        yield ("wait", "SFULL", i & 1, i)
-        yield ("arrive", "PFULL")
-        yield ("wait", "DPFULL", i & 1, i)
-        if i > 0:
-            yield ("wait", ("DQFULL", (i - 1) & 1), ((i - 1) >> 1) & 1, (i - 1) >> 1)
-        yield ("arrive", "DSFULL")
-        if i > 0:
-            yield from drain(i - 1)
-    if n:
-        yield from drain(n - 1)
-        yield ("wait", "ACC", 0, 0)
+
+def bwd64_compute(items):
+    i = nacc = 0
+    for k, n in enumerate(list(items) + [None]):
+        yield ("wait", ("ITEM", k & 1), (k >> 1) & 1, k >> 1)
+        if n is None:
+            return
+        for _ in range(n):
+            yield ("wait", ("LSE", i & 1), (i >> 1) & 1, i >> 1)
+            yield ("wait", "SFULL", i & 1, i)
+            yield ("arrive", "PFULL")
+            yield ("wait", "DPFULL", i & 1, i)
+            if i > 0:
+                yield ("wait", ("DQFULL", (i - 1) & 1), ((i - 1) >> 1) & 1, (i - 1) >> 1)
+            yield ("arrive", "DSFULL")
+            i += 1
+        if n:
+            yield ("wait", "ACC", nacc & 1, nacc)
+            nacc += 1
+        yield ("arrive", ("ITEMFREE", k & 1))
 
 
-def run_bwd64(seed, n):
+def bwd64_drain(items):
+    i = 0
+    for k, n in enumerate(list(items) + [None]):
+        yield ("wait", ("ITEM", k & 1), (k >> 1) & 1, k >> 1)
+        if n is None:
+            return
+        for _ in range(n):
+            yield ("wait", ("DQFULL", i & 1), (i >> 1) & 1, i >> 1)
+            yield ("arrive", ("DQFREE", i & 1))
+            i += 1
+        yield ("arrive", ("ITEMFREE", k & 1))
+
+
+def run_bwd64(seed, items=None, **producer_kw):
     rng = random.Random(seed)
-    roles = {"producer": bwd64_producer(n), "issuer": bwd64_issuer(n), "compute": bwd64_compute(n)}
-    schedule(rng, roles, lambda name: 1)
+    if items is None:
+        items = [rng.choice([0, 1, 1, 2, 3, 4, 5, 9]) for _ in range(rng.randint(1, 7))]
+    roles = {"producer": bwd64_producer(items, **producer_kw), "issuer": bwd64_issuer(items),
+             "compute": bwd64_compute(items), "drain": bwd64_drain(items)}
+    schedule(rng, roles, lambda name: 3 if name[0] == "ITEMFREE" else 1)
 
 
 TILE_COUNTS = [(1, 1), (2, 2), (3, 3), (7, 7), (12, 12), (3, 5), (5, 6), (0, 4), (8, 1)]
@@ -614,8 +666,9 @@ def test_decode_protocol_never_aliases():
 
 
 def test_bwd64_protocol_never_aliases():
-    for i in range(600):
-        run_bwd64(seed=i, n=(1, 2, 3, 4, 5, 9, 16)[i % 7])
+    for i in range(800):
+        run_bwd64(seed=i)
+
 
 
 def test_bwd128_protocol_never_aliases():

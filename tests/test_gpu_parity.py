@@ -166,6 +166,31 @@ def test_repeat_calls_are_deterministic_backward(d):
         assert torch.equal(first[1], again[1]) and torch.equal(first[2], again[2])
 
 
+def test_backward_work_counter_resets_and_reuse_is_exact():
+    """The persistent d = 64 backward takes its work items from a counter in
+    the workspace (words 2 and 3) and every launch leaves it at zero: one
+    workspace reused across shapes (more items than SMs and fewer, with and
+    without a block mask) gives dK, dV bit-identical to a fresh workspace and
+    dQ within the parity bound of the oracle."""
+    import io_aware_exact_09_gb300 as fa
+    from gpu_common import GRAD_REL_FRO
+    shapes = ((4, 16, 1024, None), (1, 1, 300, None), (2, 3, 700, [[1, 0, 1, 0, 1, 1]] * 6))
+    ws = fa.workspace(max(fa.fa_bwd_workspace_size(B, H, N, 64) for B, H, N, _ in shapes), "cuda")
+    for B, H, N, bm in shapes:
+        c = make_case(B, H, N, 64, seed=N + H, causal=True, block_mask=bm)
+        g = to_dev(c, "cuda")
+        O, L = fa.attention_forward(g["Q"], g["K"], g["V"], c["scale"], True, None, g["block_mask"])
+        fresh = fa.attention_backward(g["Q"], g["K"], g["V"], O, L, g["dO"], c["scale"], True, None, g["block_mask"])
+        for _ in range(2):
+            dQ, dK, dV = fa.attention_backward(g["Q"], g["K"], g["V"], O, L, g["dO"], c["scale"], True, None,
+                                               g["block_mask"], ws=ws)
+            torch.cuda.synchronize()
+            assert int(ws[8:16].view(torch.int32).abs().sum()) == 0, (B, H, N)
+            assert torch.equal(dK, fresh[1]) and torch.equal(dV, fresh[2]), (B, H, N)
+            assert rel_fro(dQ.double().cpu().numpy(), fresh[0].double().cpu().numpy()) <= GRAD_REL_FRO / 10
+        assert fa.fa_get_device_status(ws) == 0
+
+
 @pytest.mark.parametrize("d", [64, 128])
 def test_backward_stages_match_fa_bwd(d):
     """fa_bwd_preprocess, fa_bwd_main and fa_bwd_postprocess enqueued one by
