@@ -25,8 +25,8 @@
 //   - under a block mask the producer lists an item's query blocks once (a
 //     ballot compaction of the mask column), so no role scans the mask in
 //     global memory block by block.
-// Roles (512 threads): warp 0 producer (items, TMA, LSE/D staging), warp 1
-// tcgen05 issuer, warps 4-11 two compute warpgroups (one key row per thread,
+// Roles (512 threads): warp 0 producer (items, TMA), warp 1 tcgen05 issuer,
+// warp 2 LSE/D stager (a ring of four blocks), warps 4-11 two compute warpgroups (one key row per thread,
 // warpgroup w on query columns [64w, 64w + 64); at the end of an item each
 // converts half of dK * scale and dV to bf16), warps 12-15 the dQ drain
 // (one query row per thread).  TMEM (512 columns): S^T (128), dP^T (128), dV
@@ -53,9 +53,10 @@ struct Bwd64 {
     static constexpr int OFF_DO = OFF_Q + 2 * TILE;        // [2] stages
     static constexpr int OFF_DS = OFF_DO + 2 * TILE;       // [query chunk 2][key 128][128 B]
     static constexpr int OFF_STG = OFF_DS + 2 * TILE;      // [column chunk 2][query 128][128 B] fp32
-    static constexpr int OFF_LSE = OFF_STG + 2 * TILE;     // [2][BQ] fp32 (log2 domain)
-    static constexpr int OFF_DV = OFF_LSE + 2 * BQ * 4;    // [2][BQ] fp32
-    static constexpr int OFF_BAR = OFF_DV + 2 * BQ * 4;
+    static constexpr int LSE_BUFS = 4;                     // LSE/D ring depth (blocks staged ahead)
+    static constexpr int OFF_LSE = OFF_STG + 2 * TILE;     // [LSE_BUFS][BQ] fp32 (log2 domain)
+    static constexpr int OFF_DV = OFF_LSE + LSE_BUFS * BQ * 4;   // [LSE_BUFS][BQ] fp32
+    static constexpr int OFF_BAR = OFF_DV + LSE_BUFS * BQ * 4;
     static constexpr int B_KVFULL = 0;                     // [2] per K/V buffer
     static constexpr int B_KVFREE = 2;                     // [2]
     static constexpr int B_QFULL = 4;                      // [2] per Q/dO stage
@@ -70,10 +71,11 @@ struct Bwd64 {
     static constexpr int B_DQFREE = 16;                    // [2] 128 (drain warpgroup)
     static constexpr int B_ACC = 18;                       // an item's dK, dV complete
     static constexpr int B_FIN = 19;
-    static constexpr int B_LSE = 20;                       // [2] LSE/D block staged (32)
-    static constexpr int B_ITEM = 22;                      // [2] item slot published (32)
-    static constexpr int B_ITEMFREE = 24;                  // [2] slot read by every consumer (1 + 8 + 4)
-    static constexpr int NBAR = 26;
+    static constexpr int B_LSE = 20;                       // [LSE_BUFS] LSE/D block staged (32)
+    static constexpr int B_LSEFREE = 24;                   // [LSE_BUFS] block's LSE/D read (8 compute warps)
+    static constexpr int B_ITEM = 28;                      // [2] item slot published (32)
+    static constexpr int B_ITEMFREE = 30;                  // [2] slot read by every consumer (1 + 1 + 8 + 4)
+    static constexpr int NBAR = 32;
     static constexpr int OFF_SLOT = (OFF_BAR + NBAR * 8 + 127) & ~127;   // [2] item slots, 128 B each
     static constexpr int LIST_CAP = 2048;                  // query blocks listed per item under a block mask
     static constexpr int OFF_LIST = OFF_SLOT + 2 * 128;    // [2][LIST_CAP] uint16
@@ -139,8 +141,8 @@ __global__ void __launch_bounds__(512, 1) fa_bwd64_kernel(const __grid_constant_
     BwdItem *slots = reinterpret_cast<BwdItem *>(sb + S::OFF_SLOT);
     auto list_of = [&](int s) { return reinterpret_cast<uint16_t *>(sb + S::OFF_LIST) + s * S::LIST_CAP; };
     unsigned *sched = p.status + 2;                  // workspace words 2 (next item) and 3 (CTAs done)
-    float *lse_s = reinterpret_cast<float *>(sb + S::OFF_LSE);   // [2][BQ], log2 domain
-    float *dv_s = reinterpret_cast<float *>(sb + S::OFF_DV);     // [2][BQ]
+    float *lse_s = reinterpret_cast<float *>(sb + S::OFF_LSE);   // [LSE_BUFS][BQ], log2 domain
+    float *dv_s = reinterpret_cast<float *>(sb + S::OFF_DV);     // [LSE_BUFS][BQ]
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < 2; ++s) {
@@ -150,9 +152,12 @@ __global__ void __launch_bounds__(512, 1) fa_bwd64_kernel(const __grid_constant_
             mbar_init(bar(S::B_QEMPTY + s), 1);
             mbar_init(bar(S::B_DQFULL + s), 1);
             mbar_init(bar(S::B_DQFREE + s), 128);
-            mbar_init(bar(S::B_LSE + s), 32);
             mbar_init(bar(S::B_ITEM + s), 32);
-            mbar_init(bar(S::B_ITEMFREE + s), 13);
+            mbar_init(bar(S::B_ITEMFREE + s), 14);
+        }
+        for (int s = 0; s < S::LSE_BUFS; ++s) {
+            mbar_init(bar(S::B_LSE + s), 32);
+            mbar_init(bar(S::B_LSEFREE + s), 8);
         }
         mbar_init(bar(S::B_SFULL), 1);
         mbar_init(bar(S::B_DPFULL), 1);
@@ -304,24 +309,6 @@ __global__ void __launch_bounds__(512, 1) fa_bwd64_kernel(const __grid_constant_
                         tma_load_3d_elect(base + S::OFF_DO + st * S::TILE, &p.tmdO, bar(S::B_QFULL + st), 0, qb * BQ,
                                           it.bh);
                     }
-                    // LSE in the log2 domain (+inf past the sequence's last query
-                    // or for a row with no visible key: its P is 0) and D of the block
-                    const int qa = qb * BQ;
-                    for (int t = lane; t < BQ; t += 32) {
-                        const int qq = qa + t;
-                        float v = INFINITY, dd = 0.f;
-                        if (qq < it.Lq) {
-                            const size_t li = VARLEN ? (size_t)it.h * p.total_q + it.q_start + qq
-                                                     : (size_t)it.bh * p.N + qq;
-                            const size_t di = VARLEN ? (size_t)(it.q_start + qq) * p.H + it.h : (size_t)it.bh * p.N + qq;
-                            const float L = p.LSE[li];
-                            v = (L == -INFINITY) ? INFINITY : L * 1.4426950408889634f;
-                            dd = p.Dvec[di];
-                        }
-                        lse_s[st * BQ + t] = v;
-                        dv_s[st * BQ + t] = dd;
-                    }
-                    mbar_arrive(bar(S::B_LSE + st));
                 }
                 if (!ok) break;
             }
@@ -339,6 +326,55 @@ __global__ void __launch_bounds__(512, 1) fa_bwd64_kernel(const __grid_constant_
                 if (nkv > 0) b64_drain_wait(bar(S::B_KVFULL + ((nkv - 1) & 1)), (uint32_t)((nkv - 1) >> 1) & 1u);
                 for (int j = (i > 2 ? i - 2 : 0); j < i; ++j)
                     b64_drain_wait(bar(S::B_QFULL + (j & 1)), (uint32_t)(j >> 1) & 1u);
+            }
+        } else if (warp == 2) {
+            // ---------------------------------------------------------- LSE / D stager (whole warp)
+            // Stages each block's LSE (log2 domain; +inf past the sequence's
+            // last query or for a row with no visible key, so that its P is 0)
+            // and D into a ring of LSE_BUFS buffers, up to LSE_BUFS blocks ahead
+            // of the compute warps and independent of the Q/dO ring: staged by
+            // the producer behind each block's Q/dO slot, these global loads sat
+            // on the compute warps' path.
+            int i = 0;
+            for (int k = 0;; ++k) {
+                const int s = k & 1;
+                if (!mbar_wait_warp(bar(S::B_ITEM + s), (uint32_t)(k >> 1) & 1u, g, 0x1b0)) break;
+                const BwdItem it = slots[s];
+                if (it.item < 0) break;
+                const uint16_t *lst = list_of(s);
+                bool ok = true;
+                for (int e = 0; e < it.count; ++e, ++i) {
+                    const int qb = entry_qb(it, lst, e);
+                    const int lb = i % S::LSE_BUFS;
+                    if (i >= S::LSE_BUFS && !mbar_wait_warp(bar(S::B_LSEFREE + lb),
+                                                            (uint32_t)(i / S::LSE_BUFS - 1) & 1u, g, 0x1b1)) {
+                        ok = false;
+                        break;
+                    }
+                    // all eight loads of this lane first, then the stores
+                    float v[BQ / 32], dd[BQ / 32];
+#pragma unroll
+                    for (int u = 0; u < BQ / 32; ++u) {
+                        const int qq = qb * BQ + u * 32 + lane;
+                        v[u] = INFINITY;
+                        dd[u] = 0.f;
+                        if (qq < it.Lq) {
+                            const size_t li = VARLEN ? (size_t)it.h * p.total_q + it.q_start + qq
+                                                     : (size_t)it.bh * p.N + qq;
+                            const size_t di = VARLEN ? (size_t)(it.q_start + qq) * p.H + it.h : (size_t)it.bh * p.N + qq;
+                            v[u] = p.LSE[li];
+                            dd[u] = p.Dvec[di];
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < BQ / 32; ++u) {
+                        lse_s[lb * BQ + u * 32 + lane] = (v[u] == -INFINITY) ? INFINITY : v[u] * 1.4426950408889634f;
+                        dv_s[lb * BQ + u * 32 + lane] = dd[u];
+                    }
+                    mbar_arrive(bar(S::B_LSE + lb));
+                }
+                if (!ok) break;
+                if (lane == 0) mbar_arrive(bar(S::B_ITEMFREE + s));
             }
         } else if (warp == 1) {
             // ---------------------------------------------------------- MMA issuer (whole warp)
@@ -481,10 +517,13 @@ __global__ void __launch_bounds__(512, 1) fa_bwd64_kernel(const __grid_constant_
                 const int qb = entry_qb(it, lst, e);
                 const unsigned klass = cls(it, qb);
                 const int qa = qb * BQ;
-                const int st = i & 1;
-                if (!mbar_wait_warp(bar(S::B_LSE + st), (uint32_t)(i >> 1) & 1u, g, 0x431)) { ok = false; break; }
-                const float *ls = lse_s + st * BQ;
-                const float *dd = dv_s + st * BQ;
+                const int lb = i % S::LSE_BUFS;
+                if (!mbar_wait_warp(bar(S::B_LSE + lb), (uint32_t)(i / S::LSE_BUFS) & 1u, g, 0x431)) {
+                    ok = false;
+                    break;
+                }
+                const float *ls = lse_s + lb * BQ;
+                const float *dd = dv_s + lb * BQ;
                 // P^T = 2^(s * c - LSE_q * log2 e), masked, for columns c0 .. c0 + CW
                 if (!mbar_wait_warp(bar(S::B_SFULL), (uint32_t)i & 1u, g, 0x432)) { ok = false; break; }
                 tc_fence_after();
@@ -569,6 +608,9 @@ __global__ void __launch_bounds__(512, 1) fa_bwd64_kernel(const __grid_constant_
                 fence_proxy_async_smem();
                 tc_fence_before();
                 mbar_arrive(bar(S::B_DSFULL));
+                // this block's LSE and D have been read
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(S::B_LSEFREE + lb));
             }
             if (!ok) break;
             // ---------------------------------------------------------- epilogue of the item: dK, dV

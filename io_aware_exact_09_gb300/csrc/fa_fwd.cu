@@ -84,7 +84,8 @@ struct FwdShape {
     static constexpr int B_SFULL = B_KVEMPTY + STAGES;   // [2] one per query tile
     static constexpr int B_PFULL = B_SFULL + 2;          // [2]
     static constexpr int B_PVDONE = B_PFULL + 2;         // [2]
-    static constexpr int B_ITEM = B_PVDONE + 2;          // [2] work-item slot published (32 arrivals)
+    static constexpr int B_SFREE = B_PVDONE + 2;         // [2] S_x loaded by its softmax (separate P only)
+    static constexpr int B_ITEM = B_SFREE + 2;           // [2] work-item slot published (32 arrivals)
     static constexpr int B_ITEMFREE = B_ITEM + 2;        // [2] slot read by every consumer (1 + 8 arrivals)
     static constexpr int B_FIN = B_ITEMFREE + 2;
     static constexpr int NBAR = B_FIN + 1;
@@ -97,8 +98,13 @@ struct FwdShape {
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1 KB
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
     static constexpr uint32_t TMEM_COLS = 512;
+    // d = 64 leaves room for P in columns of its own (S_x 128, P_x 64, O_x 64
+    // per query tile: 512 in all), so the next S_x need not wait for P_x V;
+    // at d = 128 P overwrites the first half of S_x
+    static constexpr bool SEP_P = (D == 64);
     static constexpr uint32_t TM_S = 0;                  // S_x at columns 128 x
-    static constexpr uint32_t TM_O = 256;                // O_x at columns 256 + D x
+    static constexpr uint32_t TM_P = SEP_P ? 256 : 0;    // P_x at TM_P + (BC / 2) x (separate), else over S_x
+    static constexpr uint32_t TM_O = SEP_P ? 384 : 256;  // O_x at columns TM_O + D x
     static constexpr int THREADS = 384;
     // register split: launched at 168 per thread (384 x 168 = 64,512);
     // warpgroup 0 (producer, MMA, two idle warps) keeps 104, the two softmax
@@ -171,6 +177,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
             mbar_init(bar(S::B_SFULL + j), 1);
             mbar_init(bar(S::B_PFULL + j), 128);
             mbar_init(bar(S::B_PVDONE + j), 1);
+            mbar_init(bar(S::B_SFREE + j), 128);
             mbar_init(bar(S::B_ITEM + j), 32);
             mbar_init(bar(S::B_ITEMFREE + j), 9);
         }
@@ -379,6 +386,18 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
             bool ok = true;
             int k = 0, m = 0, u = 0;
             int nv[2] = {0, 0};      // P.V products issued so far for query tile x (all items)
+            int ns[2] = {0, 0};      // S products issued so far for query tile x (all items)
+            auto p_tmem_of = [&](int x) -> uint32_t {
+                return S::SEP_P ? tmem + S::TM_P + (uint32_t)(BC / 2 * x) : tmem + S::TM_S + 128u * (uint32_t)x;
+            };
+            // S_x into its columns: with P aliasing S, once the previous P_x V
+            // has read P_x; with P apart, once softmax x has loaded S_x
+            auto s_ready = [&](int x, unsigned site) -> bool {
+                if (ns[x] == 0) return true;
+                if constexpr (S::SEP_P)
+                    return mbar_wait_warp(bar(S::B_SFREE + x), (uint32_t)(ns[x] - 1) & 1u, g, site);
+                return nv[x] == 0 || mbar_wait_warp(bar(S::B_PVDONE + x), (uint32_t)(nv[x] - 1) & 1u, g, site);
+            };
             for (;; ++k) {
                 const int s = k & 1;
                 if (!mbar_wait_warp(bar(S::B_ITEM + s), (uint32_t)(k >> 1) & 1u, g, 0x200)) {
@@ -400,13 +419,13 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
 #pragma unroll
                         for (int x = 0; x < 2 && ok; ++x)
                             if (entry_vis(it, lst, x, 0)) {
-                                if (nv[x] > 0 &&
-                                    !mbar_wait_warp(bar(S::B_PVDONE + x), (uint32_t)(nv[x] - 1) & 1u, g, 0x207)) {
+                                if (!s_ready(x, 0x207)) {
                                     ok = false;
                                     break;
                                 }
                                 tc_fence_after();
                                 issue_s(x, u % S::STAGES);
+                                ++ns[x];
                             }
                         // the item's S products are all issued: Q is free once they finish
                         if (ok && it.count == 1) mma_commit_elect(bar(S::B_QEMPTY));
@@ -416,6 +435,52 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                         const int st2 = (u + 1) % S::STAGES;
                         const bool more = e + 1 < it.count;
                         bool vwaited = false, kwaited = false;
+                        if constexpr (S::SEP_P) {
+                            // both query tiles' next S first (each needs only its
+                            // softmax to have loaded the current S), then this
+                            // entry's P V products as the P tiles arrive
+#pragma unroll
+                            for (int x = 0; x < 2 && ok && more; ++x)
+                                if (entry_vis(it, lst, x, e + 1)) {
+                                    if ((!kwaited && !mbar_wait_warp(bar(S::B_KFULL + st2),
+                                                                     (uint32_t)((u + 1) / S::STAGES) & 1u, g, 0x208)) ||
+                                        !s_ready(x, 0x209)) {
+                                        ok = false;
+                                        break;
+                                    }
+                                    kwaited = true;
+                                    tc_fence_after();
+                                    issue_s(x, st2);
+                                    ++ns[x];
+                                }
+                            if (!ok) break;
+                            if (e + 2 == it.count) mma_commit_elect(bar(S::B_QEMPTY));
+#pragma unroll
+                            for (int x = 0; x < 2 && ok; ++x)
+                                if (entry_vis(it, lst, x, e)) {
+                                    if (!mbar_wait_warp(bar(S::B_PFULL + x), (uint32_t)nv[x] & 1u, g, 0x20a) ||
+                                        (!vwaited && !mbar_wait_warp(bar(S::B_VFULL + st), (uint32_t)(u / S::STAGES) & 1u,
+                                                                     g, 0x20b))) {
+                                        ok = false;
+                                        break;
+                                    }
+                                    vwaited = true;
+                                    tc_fence_after();
+                                    const uint32_t o_tmem = tmem + S::TM_O + (uint32_t)(D * x);
+                                    const uint64_t vd = sdesc_add(dv0, (uint32_t)(st * S::KV_TILE_BYTES));
+                                    const uint32_t acc0 = nvi[x] > 0 ? 1u : 0u;
+#pragma unroll
+                                    for (int kk = 0; kk < BC / 16; ++kk)
+                                        mma_ts_elect(o_tmem, p_tmem_of(x) + (uint32_t)kk * 8u,
+                                                     sdesc_add(vd, (uint32_t)kk * 2048u), IDESC_PV, kk > 0 ? 1u : acc0);
+                                    mma_commit_elect(bar(S::B_PVDONE + x));
+                                    ++nv[x];
+                                    ++nvi[x];
+                                }
+                            if (!ok) break;
+                            mma_commit_elect(bar(S::B_KVEMPTY + st));
+                            continue;
+                        }
                         // per query tile: O_x += P_x V, then at once the next key
                         // tile's S_x (it overwrites P_x, so it waits for that P.V),
                         // so that each tile's chain S -> softmax -> P.V -> S moves
@@ -450,13 +515,13 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                                     break;
                                 }
                                 kwaited = true;
-                                if (nv[x] > 0 &&
-                                    !mbar_wait_warp(bar(S::B_PVDONE + x), (uint32_t)(nv[x] - 1) & 1u, g, 0x206)) {
+                                if (!s_ready(x, 0x206)) {
                                     ok = false;
                                     break;
                                 }
                                 tc_fence_after();
                                 issue_s(x, st2);
+                                ++ns[x];
                             }
                         }
                         if (!ok) break;
@@ -482,6 +547,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
         const int r = wq * 32 + lane;
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const uint32_t s_tmem = tmem + lane_off + S::TM_S + 128u * (uint32_t)x;
+        const uint32_t p_tmem = S::SEP_P ? tmem + lane_off + S::TM_P + (uint32_t)(BC / 2 * x) : s_tmem;
         const uint32_t o_tmem = tmem + lane_off + S::TM_O + (uint32_t)(D * x);
         const float c2 = p.scale_log2;
         bool ok = true;
@@ -524,6 +590,11 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                 for (int j = 0; j < S::KC; ++j) tmem_ld32(s_tmem + 32u * j, sr[j]);
 #pragma unroll
                 for (int j = 0; j < S::KC; ++j) tmem_ld_wait(sr[j]);
+                if constexpr (S::SEP_P) {
+                    // S_x is in registers: the next S_x may overwrite its columns
+                    tc_fence_before();
+                    mbar_arrive(bar(S::B_SFREE + x));
+                }
                 if (partial) {
 #pragma unroll
                     for (int j = 0; j < S::KC; ++j)
@@ -560,14 +631,17 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                     m_ref = m_new;
                 }
                 const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-                // p = 2^(s * c - m), bf16 into the first half of S_x's columns;
-                // the row sum in four independent packed accumulators
+                // p = 2^(s * c - m), bf16; the row sum in four independent
+                // packed accumulators.  With P apart from S, P_x is written only
+                // once the previous P_x V has read it (the first tile of an item
+                // included: the buffer serves every item); with P over S, S_x's
+                // columns are already this tile's.
                 float ps[8];
 #pragma unroll
                 for (int uu = 0; uu < 8; ++uu) ps[uu] = 0.f;
+                uint32_t pk[S::KC][16];
 #pragma unroll
                 for (int j = 0; j < S::KC; ++j) {
-                    uint32_t pk[16];
 #pragma unroll
                     for (int t = 0; t < 16; ++t) {
                         float a, bb;
@@ -577,15 +651,26 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                         bb = ex2(bb);
                         const int uu = 2 * (t & 3);
                         add2(ps[uu], ps[uu + 1], a, bb);
-                        pk[t] = pack_bf16x2(a, bb);
+                        pk[j][t] = pack_bf16x2(a, bb);
                     }
-                    tmem_st16(s_tmem + 16u * j, pk);
+                    if constexpr (!S::SEP_P) tmem_st16(p_tmem + 16u * j, pk[j]);
+                }
+                bool pv_waited = false;
+                if constexpr (S::SEP_P) {
+                    if (ns > 0 && !mbar_wait_warp(bar(S::B_PVDONE + x), (uint32_t)(ns - 1) & 1u, g, 0x404)) {
+                        ok = false;
+                        break;
+                    }
+                    pv_waited = true;
+                    tc_fence_after();
+#pragma unroll
+                    for (int j = 0; j < S::KC; ++j) tmem_st16(p_tmem + 16u * j, pk[j]);
                 }
                 l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
                 tmem_st_wait();
                 if (rescale && it > 0) {
                     // O_x may be rescaled only once the previous P_x V has landed
-                    if (!mbar_wait_warp(bar(S::B_PVDONE + x), (uint32_t)(ns - 1) & 1u, g, 0x402)) {
+                    if (!pv_waited && !mbar_wait_warp(bar(S::B_PVDONE + x), (uint32_t)(ns - 1) & 1u, g, 0x402)) {
                         ok = false;
                         break;
                     }

@@ -287,9 +287,22 @@ def fwd_producer(items, stages, q_empty_wait=True, slot_free_wait=True):
             u += 1
 
 
-def fwd_issuer(items, stages):
+def fwd_issuer(items, stages, sep=False):
+    """sep: P in TMEM columns of its own (d = 64): S_x needs only its softmax
+    to have loaded the previous S_x (SFREE); per entry both next S first, then
+    the P.V products."""
     m = u = 0
     nv = [0, 0]
+    ns = [0, 0]
+
+    def s_ready(x):
+        if ns[x] == 0:
+            return
+        if sep:
+            yield ("wait", ("SFREE", x), (ns[x] - 1) & 1, ns[x] - 1)
+        elif nv[x] > 0:
+            yield ("wait", ("PVDONE", x), (nv[x] - 1) & 1, nv[x] - 1)
+
     for k, it in enumerate(list(items) + [None]):
         yield ("wait", ("ITEM", k & 1), (k >> 1) & 1, k >> 1)
         if it is None:
@@ -301,14 +314,37 @@ def fwd_issuer(items, stages):
             yield ("wait", ("KFULL", u % stages), (u // stages) & 1, u // stages)
             for x in range(2):
                 if vis[x][0]:
-                    if nv[x] > 0:
-                        yield ("wait", ("PVDONE", x), (nv[x] - 1) & 1, nv[x] - 1)
+                    yield from s_ready(x)
                     yield ("commit", ("SFULL", x))
+                    ns[x] += 1
             if count == 1:
                 yield ("commit", "QEMPTY")
             for e in range(count):
                 s, s2 = u % stages, (u + 1) % stages
                 vwaited = kwaited = False
+                if sep:
+                    for x in range(2):
+                        if e + 1 < count and vis[x][e + 1]:
+                            if not kwaited:
+                                kk = (u + 1) // stages
+                                yield ("wait", ("KFULL", s2), kk & 1, kk)
+                                kwaited = True
+                            yield from s_ready(x)
+                            yield ("commit", ("SFULL", x))
+                            ns[x] += 1
+                    if e + 2 == count:
+                        yield ("commit", "QEMPTY")
+                    for x in range(2):
+                        if vis[x][e]:
+                            yield ("wait", ("PFULL", x), nv[x] & 1, nv[x])
+                            if not vwaited:
+                                yield ("wait", ("VFULL", s), (u // stages) & 1, u // stages)
+                                vwaited = True
+                            yield ("commit", ("PVDONE", x))
+                            nv[x] += 1
+                    yield ("commit", ("KVEMPTY", s))
+                    u += 1
+                    continue
                 for x in range(2):
                     if vis[x][e]:
                         yield ("wait", ("PFULL", x), nv[x] & 1, nv[x])
@@ -322,9 +358,9 @@ def fwd_issuer(items, stages):
                             kk = (u + 1) // stages
                             yield ("wait", ("KFULL", s2), kk & 1, kk)
                             kwaited = True
-                        if nv[x] > 0:
-                            yield ("wait", ("PVDONE", x), (nv[x] - 1) & 1, nv[x] - 1)
+                        yield from s_ready(x)
                         yield ("commit", ("SFULL", x))
+                        ns[x] += 1
                 if e + 2 == count:
                     yield ("commit", "QEMPTY")
                 yield ("commit", ("KVEMPTY", s))
@@ -332,7 +368,7 @@ def fwd_issuer(items, stages):
         yield ("arrive", ("ITEMFREE", k & 1))
 
 
-def fwd_softmax(x, items, rng, p_rescale):
+def fwd_softmax(x, items, rng, p_rescale, sep=False):
     ns = 0
     for k, it in enumerate(list(items) + [None]):
         yield ("wait", ("ITEM", k & 1), (k >> 1) & 1, k >> 1)
@@ -344,7 +380,11 @@ def fwd_softmax(x, items, rng, p_rescale):
             if not vis[x][e]:
                 continue
             yield ("wait", ("SFULL", x), ns & 1, ns)
-            if n_item > 0 and rng.random() < p_rescale:
+            if sep:
+                yield ("arrive", ("SFREE", x))
+                if ns > 0:                      # the P buffer: the previous P.V has read it
+                    yield ("wait", ("PVDONE", x), (ns - 1) & 1, ns - 1)
+            elif n_item > 0 and rng.random() < p_rescale:
                 yield ("wait", ("PVDONE", x), (ns - 1) & 1, ns - 1)
             yield ("arrive", ("PFULL", x))
             ns += 1
@@ -376,12 +416,12 @@ def fwd_items(rng, n_items):
     return items
 
 
-def run_fwd(seed, stages, n_items=None, p_rescale=0.3, **producer_kw):
+def run_fwd(seed, stages, n_items=None, p_rescale=0.3, sep=False, **producer_kw):
     rng = random.Random(seed)
     items = fwd_items(rng, n_items if n_items is not None else rng.randint(1, 7))
-    roles = {"producer": fwd_producer(items, stages, **producer_kw), "issuer": fwd_issuer(items, stages),
-             "softmax0": fwd_softmax(0, items, rng, p_rescale),
-             "softmax1": fwd_softmax(1, items, rng, p_rescale)}
+    roles = {"producer": fwd_producer(items, stages, **producer_kw), "issuer": fwd_issuer(items, stages, sep),
+             "softmax0": fwd_softmax(0, items, rng, p_rescale, sep),
+             "softmax1": fwd_softmax(1, items, rng, p_rescale, sep)}
     schedule(rng, roles, lambda name: 3 if name[0] == "ITEMFREE" else 1)
 
 
@@ -471,8 +511,27 @@ def bwd64_producer(items, kv_free_wait=True):
             s = i & 1
             yield ("wait", ("QEMPTY", s), ((i >> 1) & 1) ^ 1, (i >> 1) - 1)
             yield ("tma", ("QFULL", s))
-            yield ("arrive", ("LSE", s))
             i += 1
+
+
+LSE_BUFS = 4
+
+
+def bwd64_stager(items, lse_free_wait=True):
+    """Stages every block's LSE and D into a ring of LSE_BUFS buffers, ahead
+    of the compute warps and independent of the Q/dO ring."""
+    i = 0
+    for k, n in enumerate(list(items) + [None]):
+        yield ("wait", ("ITEM", k & 1), (k >> 1) & 1, k >> 1)
+        if n is None:
+            return
+        for _ in range(n):
+            b = i % LSE_BUFS
+            if i >= LSE_BUFS and lse_free_wait:
+                yield ("wait", ("LSEFREE", b), (i // LSE_BUFS - 1) & 1, i // LSE_BUFS - 1)
+            yield ("arrive", ("LSE", b))
+            i += 1
+        yield ("arrive", ("ITEMFREE", k & 1))
 
 
 def bwd64_issuer(items):
@@ -522,13 +581,15 @@ def bwd64_compute(items):
         if n is None:
             return
         for _ in range(n):
-            yield ("wait", ("LSE", i & 1), (i >> 1) & 1, i >> 1)
+            b = i % LSE_BUFS
+            yield ("wait", ("LSE", b), (i // LSE_BUFS) & 1, i // LSE_BUFS)
             yield ("wait", "SFULL", i & 1, i)
             yield ("arrive", "PFULL")
             yield ("wait", "DPFULL", i & 1, i)
             if i > 0:
                 yield ("wait", ("DQFULL", (i - 1) & 1), ((i - 1) >> 1) & 1, (i - 1) >> 1)
             yield ("arrive", "DSFULL")
+            yield ("arrive", ("LSEFREE", b))
             i += 1
         if n:
             yield ("wait", "ACC", nacc & 1, nacc)
@@ -549,13 +610,13 @@ def bwd64_drain(items):
         yield ("arrive", ("ITEMFREE", k & 1))
 
 
-def run_bwd64(seed, items=None, **producer_kw):
+def run_bwd64(seed, items=None, lse_free_wait=True, **producer_kw):
     rng = random.Random(seed)
     if items is None:
         items = [rng.choice([0, 1, 1, 2, 3, 4, 5, 9]) for _ in range(rng.randint(1, 7))]
-    roles = {"producer": bwd64_producer(items, **producer_kw), "issuer": bwd64_issuer(items),
-             "compute": bwd64_compute(items), "drain": bwd64_drain(items)}
-    schedule(rng, roles, lambda name: 3 if name[0] == "ITEMFREE" else 1)
+    roles = {"producer": bwd64_producer(items, **producer_kw), "stager": bwd64_stager(items, lse_free_wait),
+             "issuer": bwd64_issuer(items), "compute": bwd64_compute(items), "drain": bwd64_drain(items)}
+    schedule(rng, roles, lambda name: 4 if name[0] == "ITEMFREE" else 1)
 
 
 TILE_COUNTS = [(1, 1), (2, 2), (3, 3), (7, 7), (12, 12), (3, 5), (5, 6), (0, 4), (8, 1)]
@@ -583,6 +644,51 @@ def test_model_finds_the_alias_of_one_pready_barrier_per_query_tile():
 def test_bf16_forward_protocol_never_aliases():
     for i in range(800):
         run_fwd(seed=i, stages=(2, 4)[i % 2])
+
+
+def test_bf16_forward_separate_p_protocol_never_aliases():
+    """d = 64: P in TMEM columns of its own, the next S after the softmax has
+    loaded the current one, the P buffer rewritten after the previous P.V."""
+    for i in range(800):
+        run_fwd(seed=i, stages=4, sep=True)
+
+
+def test_separate_p_model_finds_a_dropped_p_buffer_wait():
+    """Writing P_x before the previous P_x V has read it lets the softmax run
+    ahead of the products: some parity wait then meets a barrier two phases
+    away from the one it means."""
+    def softmax_no_pv_wait(x, items):
+        ns = 0
+        for k, it in enumerate(list(items) + [None]):
+            yield ("wait", ("ITEM", k & 1), (k >> 1) & 1, k >> 1)
+            if it is None:
+                return
+            count, vis = it
+            n_item = 0
+            for e in range(count):
+                if vis[x][e]:
+                    yield ("wait", ("SFULL", x), ns & 1, ns)
+                    yield ("arrive", ("SFREE", x))
+                    yield ("arrive", ("PFULL", x))
+                    ns += 1
+                    n_item += 1
+            if n_item:
+                yield ("wait", ("PVDONE", x), (ns - 1) & 1, ns - 1)
+            yield ("arrive", ("ITEMFREE", k & 1))
+
+    found = []
+    for i in range(400):
+        rng = random.Random(i)
+        items = fwd_items(rng, 5)
+        roles = {"producer": fwd_producer(items, 4), "issuer": fwd_issuer(items, 4, True),
+                 "softmax0": softmax_no_pv_wait(0, items), "softmax1": softmax_no_pv_wait(1, items)}
+        try:
+            schedule(rng, roles, lambda name: 3 if name[0] == "ITEMFREE" else 1)
+        except Alias as e:
+            found.append(str(e))
+    # the issuer meets a P-ready barrier two phases ahead, or the softmax,
+    # run ahead, waits for a P.V product two phases before it completes
+    assert found and all("('PFULL'" in f or "('PVDONE'" in f for f in found), found[:3]
 
 
 def test_forward_model_finds_a_dropped_q_empty_wait():
@@ -668,6 +774,18 @@ def test_decode_protocol_never_aliases():
 def test_bwd64_protocol_never_aliases():
     for i in range(800):
         run_bwd64(seed=i)
+
+
+def test_bwd64_model_finds_a_dropped_lse_free_wait():
+    """Staging LSE and D into a buffer the compute warps have not released
+    lets that buffer's ready barrier run two phases ahead of them."""
+    found = []
+    for i in range(400):
+        try:
+            run_bwd64(seed=i, items=[9, 5, 9, 7], lse_free_wait=False)
+        except Alias as e:
+            found.append(str(e))
+    assert found and all("('LSE'" in f for f in found), found[:3]
 
 
 
