@@ -22,8 +22,8 @@
 // Shared memory (224 KB): K, V; Q double-buffered, dO single; the dS^T tile
 // (the dQ MMA's B operand); 32 KB of dQ staging.
 //
-// Roles (512 threads): warp 0 TMA producer (and, whole warp, the LSE/D
-// staging); warp 1 tcgen05 issuer; warps 4-7 and 8-11 two compute warpgroups,
+// Roles (512 threads): warp 0 TMA producer; warp 1 tcgen05 issuer; warp 2
+// the LSE/D stager; warps 4-7 and 8-11 two compute warpgroups,
 // one key row per thread, warpgroup w on query columns [64w, 64w + 64);
 // warps 12-15 the dQ drain, one head-dimension row of dQ^T per thread: TMEM
 // -> swizzled shared staging (two halves of 64 query columns, 8 KB per warp)
@@ -59,8 +59,8 @@ struct Bwd128 {
     static constexpr int B_QFULL = 1;                      // [2]
     static constexpr int B_QEMPTY = 3;                     // [2]
     static constexpr int B_DOFULL = 5;
-    static constexpr int B_LSE = 7;                        // LSE/D staged (32 arrivals)
-    static constexpr int B_LSEFREE = 8;                    // LSE/D consumed (256)
+    static constexpr int B_LSE = 7;                        // LSE of a block staged (32 arrivals)
+    static constexpr int B_LSEFREE = 8;                    // LSE read by the P pass (256)
     static constexpr int B_SFULL = 9;
     static constexpr int B_DPFULL = 10;
     static constexpr int B_PFULL = 11;                     // 256
@@ -70,7 +70,9 @@ struct Bwd128 {
     static constexpr int B_DQFREE = 16;                    // 128 (drain warpgroup)
     static constexpr int B_ACC = 17;
     static constexpr int B_FIN = 18;
-    static constexpr int NBAR = 19;
+    static constexpr int B_D = 19;                         // D of a block staged (32)
+    static constexpr int B_DFREE = 20;                     // D read by the dS pass (256)
+    static constexpr int NBAR = 21;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
@@ -175,6 +177,8 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
         mbar_init(bar(S::B_DOFULL), 1);
         mbar_init(bar(S::B_LSE), 32);
         mbar_init(bar(S::B_LSEFREE), 256);
+        mbar_init(bar(S::B_D), 32);
+        mbar_init(bar(S::B_DFREE), 256);
         mbar_init(bar(S::B_SFULL), 1);
         mbar_init(bar(S::B_DPFULL), 1);
         mbar_init(bar(S::B_PFULL), 256);
@@ -235,26 +239,6 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
                     }
                 }
                 nl = i + 1;
-                // LSE (log2 domain; +inf past the sequence's last query or for
-                // a row with no visible key: its P is 0) and D of the block,
-                // once the previous block's are consumed
-                if (!mbar_wait_warp(bar(S::B_LSEFREE), ((uint32_t)i & 1u) ^ 1u, g, 0x123)) {
-                    ok = false;
-                    break;
-                }
-                const int qa = qb * BQ;
-                for (int t = lane; t < BQ; t += 32) {
-                    const int qq = qa + t;
-                    float v = INFINITY, dd = 0.f;
-                    if (qq < Lq) {
-                        const float L = p.LSE[lse_index(qq)];
-                        v = (L == -INFINITY) ? INFINITY : L * 1.4426950408889634f;
-                        dd = p.Dvec[d_index(qq)];
-                    }
-                    lse_s[t] = v;
-                    dv_s[t] = dd;
-                }
-                mbar_arrive(bar(S::B_LSE));
             }
             if (!ok && lane == 0) {
                 // gave up: let every copy already issued land before the CTA exits
@@ -262,6 +246,44 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
                 for (int j = (nl > 2 ? nl - 2 : 0); j < nl; ++j)
                     b128_drain_wait(bar(S::B_QFULL + (j & 1)), (uint32_t)(j >> 1) & 1u);
                 if (nl > 0) b128_drain_wait(bar(S::B_DOFULL), (uint32_t)(nl - 1) & 1u);
+            }
+        } else if (warp == 2 && first < Tqb) {
+            // ---------------------------------------------------------- LSE / D stager
+            // LSE (log2 domain; +inf past the sequence's last query or for a row
+            // with no visible key, so that its P is 0) and D of each block.  The
+            // next block's values are loaded into registers while the current
+            // block computes; LSE is stored as soon as the P pass has read the
+            // previous block's, D as soon as the dS pass has read the previous
+            // D, so that no global-load latency falls between two blocks (staged
+            // by the producer behind the previous block's release, the compute
+            // warps waited ~3,500 cycles per block for them).
+            float rl[BQ / 32], rd[BQ / 32];
+            auto fetch = [&](int qb) {
+#pragma unroll
+                for (int u = 0; u < BQ / 32; ++u) {
+                    const int qq = qb * BQ + u * 32 + lane;
+                    rl[u] = -INFINITY;
+                    rd[u] = 0.f;
+                    if (qq < Lq) {
+                        rl[u] = p.LSE[lse_index(qq)];
+                        rd[u] = p.Dvec[d_index(qq)];
+                    }
+                }
+            };
+            int i = 0;
+            fetch(first);
+            for (int qb = first; qb < Tqb; ++i) {
+                if (i > 0 && !mbar_wait_warp(bar(S::B_LSEFREE), (uint32_t)(i - 1) & 1u, g, 0x124)) break;
+#pragma unroll
+                for (int u = 0; u < BQ / 32; ++u)
+                    lse_s[u * 32 + lane] = (rl[u] == -INFINITY) ? INFINITY : rl[u] * 1.4426950408889634f;
+                mbar_arrive(bar(S::B_LSE));
+                if (i > 0 && !mbar_wait_warp(bar(S::B_DFREE), (uint32_t)(i - 1) & 1u, g, 0x125)) break;
+#pragma unroll
+                for (int u = 0; u < BQ / 32; ++u) dv_s[u * 32 + lane] = rd[u];
+                mbar_arrive(bar(S::B_D));
+                qb = next_qb(qb);
+                if (qb < Tqb) fetch(qb);
             }
         } else if (warp == 1) {
             // ---------------------------------------------------------- MMA issuer
@@ -419,10 +441,12 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(bar(S::B_PFULL));
+            mbar_arrive(bar(S::B_LSEFREE));           // this block's LSE has been read
 
             // dS^T = P^T o (dP^T - D): bf16 into region b (for dK) and the shared dS^T tile (for dQ);
             // D to registers before the wait, as LSE above
-            if (!mbar_wait_warp(bar(S::B_DPFULL), (uint32_t)i & 1u, g, 0x423)) { ok = false; break; }
+            if (!mbar_wait_warp(bar(S::B_DPFULL), (uint32_t)i & 1u, g, 0x423) ||
+                !mbar_wait_warp(bar(S::B_D), (uint32_t)i & 1u, g, 0x424)) { ok = false; break; }
             tc_fence_after();
             {
                 uint32_t dp[2][32];
@@ -458,7 +482,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(bar(S::B_DSFULL));
-            mbar_arrive(bar(S::B_LSEFREE));
+            mbar_arrive(bar(S::B_DFREE));             // this block's D has been read
         }
 
         // ---------------------------------------------------------- epilogue: dK, dV

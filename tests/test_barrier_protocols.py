@@ -182,8 +182,9 @@ def run(seed, n_tiles, per_buffer_pfull, p_rescale=0.3):
 
 # ---------------------------------------------------------------- d = 128 backward
 # The roles of `fa_bwd128_kernel` for one key tile and n query blocks: a
-# producer (K, V once; per block Q into one of two stages, dO into one slot,
-# LSE and D staged in shared memory), the MMA issuer (per block dV, dQ^T, dK,
+# producer (K, V once; per block Q into one of two stages, dO into one slot),
+# the LSE/D stager (one buffer each, refilled as soon as the P and the dS
+# pass have read them), the MMA issuer (per block dV, dQ^T, dK,
 # then the next block's S^T and dP^T), the compute warpgroups (P^T, dS^T)
 # and the dQ drain warpgroup.  The phase each wait means is the block index
 # (or half of it for the two Q stages).
@@ -196,8 +197,18 @@ def bwd_producer(n):
         yield ("wait", "DVDONE", (i & 1) ^ 1, i - 1)                        # dV(i-1) read dO
         yield ("tma", ("QFULL", s))
         yield ("tma", "DOFULL")
-        yield ("wait", "LSEFREE", (i & 1) ^ 1, i - 1)                       # block i-1's LSE, D consumed
+
+
+def bwd_stager(n):
+    """LSE of block i once the P pass has read block i-1's, D once the dS pass
+    has read block i-1's (one buffer each)."""
+    for i in range(n):
+        if i > 0:
+            yield ("wait", "LSEFREE", (i - 1) & 1, i - 1)
         yield ("arrive", "LSE")
+        if i > 0:
+            yield ("wait", "DFREE", (i - 1) & 1, i - 1)
+        yield ("arrive", "D")
 
 
 def bwd_issuer(n):
@@ -231,9 +242,11 @@ def bwd_compute(n):
         yield ("wait", "LSE", i & 1, i)
         yield ("wait", "SFULL", i & 1, i)
         yield ("arrive", "PFULL")
-        yield ("wait", "DPFULL", i & 1, i)
-        yield ("arrive", "DSFULL")
         yield ("arrive", "LSEFREE")
+        yield ("wait", "DPFULL", i & 1, i)
+        yield ("wait", "D", i & 1, i)
+        yield ("arrive", "DSFULL")
+        yield ("arrive", "DFREE")
     if n:
         yield ("wait", "ACC", 0, 0)
 
@@ -246,7 +259,8 @@ def bwd_drain(n):
 
 def run_bwd128(seed, n):
     rng = random.Random(seed)
-    roles = {"producer": bwd_producer(n), "issuer": bwd_issuer(n), "compute": bwd_compute(n), "drain": bwd_drain(n)}
+    roles = {"producer": bwd_producer(n), "stager": bwd_stager(n), "issuer": bwd_issuer(n),
+             "compute": bwd_compute(n), "drain": bwd_drain(n)}
     schedule(rng, roles, lambda name: 1)
 
 
@@ -802,8 +816,8 @@ def test_bwd128_model_finds_a_dropped_drain_wait():
     found = []
     for i in range(300):
         n = (2, 5, 9, 16)[i % 4]
-        roles = {"producer": bwd_producer(n), "issuer": issuer_without_dqfree_wait(n), "compute": bwd_compute(n),
-                 "drain": bwd_drain(n)}
+        roles = {"producer": bwd_producer(n), "stager": bwd_stager(n), "issuer": issuer_without_dqfree_wait(n),
+                 "compute": bwd_compute(n), "drain": bwd_drain(n)}
         try:
             schedule(random.Random(i), roles, lambda name: 1)
         except Alias as e:
