@@ -287,7 +287,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
             }
         } else if (warp == 1) {
             // ---------------------------------------------------------- MMA issuer
-            // Order per block i: dV(i), dK(i), S^T(i+1), dQ^T(i), dP^T(i+1).
+            // Order per block i: dV(i), dQ^T(i), dK(i), S^T(i+1), dP^T(i+1).
             constexpr uint32_t IDESC_S = idesc_bf16(128, BQ, false, false);   // S^T, dP^T
             constexpr uint32_t IDESC_ACC = idesc_bf16(128, 128, false, true); // dV, dK: B MN-major
             constexpr uint32_t IDESC_DQ = idesc_bf16(128, BQ, true, true);    // dQ^T = K^T dS^T
@@ -343,12 +343,18 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
                         mma_ts_elect(tmem + S::TM_DV, ra + packed_col128(k), sdesc_add(ddO_mn, (uint32_t)k * 2048u),
                                IDESC_ACC, k > 0 ? 1u : acc0);
                     mma_commit_elect(bar(S::B_DVDONE));
-                    // dK += dS^T Q: A = dS^T (region b, packed), B = Q (MN-major); first,
-                    // so that S^T(i+1), which needs region b back, runs before dQ^T(i)
-                    // (the compute warps wait for S^T(i+1); dP^T(i+1) is needed only
-                    // after the P pass)
-                    if (!mbar_wait_warp(bar(S::B_DSFULL), (uint32_t)i & 1u, g, 0x225)) { ok = false; break; }
+                    // dQ^T = K^T dS^T into region a (once dV has read P^T there), first:
+                    // the sooner it is drained, the sooner dP^T(i+1) can use region a;
+                    // dK follows
+                    if (!mbar_wait_warp(bar(S::B_DSFULL), (uint32_t)i & 1u, g, 0x225) ||
+                        !mbar_wait_warp(bar(S::B_DVDONE), (uint32_t)i & 1u, g, 0x226)) { ok = false; break; }
                     tc_fence_after();
+#pragma unroll
+                    for (int k = 0; k < kTile / 16; ++k)
+                        mma_ss_elect(ra, sdesc_add(dK_mn, (uint32_t)k * 2048u), sdesc_add(ddS_mn, (uint32_t)k * 2048u),
+                               IDESC_DQ, k > 0 ? 1u : 0u);
+                    mma_commit_elect(bar(S::B_DQFULL));
+                    // dK += dS^T Q: A = dS^T (region b, packed), B = Q (MN-major)
                     const uint64_t q_mn = sdesc_add(dQ_mn, (uint32_t)(s * S::TILE));
 #pragma unroll
                     for (int k = 0; k < BQ / 16; ++k)
@@ -361,16 +367,6 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
                             !mbar_wait_warp(bar(S::B_QEMPTY + s), (uint32_t)(i >> 1) & 1u, g, 0x228)) { ok = false; break; }
                         tc_fence_after();
                         issue_s(i + 1);
-                    }
-                    // dQ^T = K^T dS^T into region a (once dV has read P^T there)
-                    if (!mbar_wait_warp(bar(S::B_DVDONE), (uint32_t)i & 1u, g, 0x226)) { ok = false; break; }
-                    tc_fence_after();
-#pragma unroll
-                    for (int k = 0; k < kTile / 16; ++k)
-                        mma_ss_elect(ra, sdesc_add(dK_mn, (uint32_t)k * 2048u), sdesc_add(ddS_mn, (uint32_t)k * 2048u),
-                               IDESC_DQ, k > 0 ? 1u : 0u);
-                    mma_commit_elect(bar(S::B_DQFULL));
-                    if (qb_next < Tqb) {
                         // dP^T(i+1) into region a once dQ^T(i) has been drained
                         if (!mbar_wait_warp(bar(S::B_DOFULL), (uint32_t)(i + 1) & 1u, g, 0x229) ||
                             !mbar_wait_warp(bar(S::B_DQFREE), (uint32_t)i & 1u, g, 0x22a)) { ok = false; break; }

@@ -184,8 +184,8 @@ def run(seed, n_tiles, per_buffer_pfull, p_rescale=0.3):
 # The roles of `fa_bwd128_kernel` for one key tile and n query blocks: a
 # producer (K, V once; per block Q into one of two stages, dO into one slot),
 # the LSE/D stager (one buffer each, refilled as soon as the P and the dS
-# pass have read them), the MMA issuer (per block dV, dK, the next block's
-# S^T, dQ^T, then the next block's dP^T), the compute warpgroups (P^T, dS^T)
+# pass have read them), the MMA issuer (per block dV, dQ^T, dK,
+# then the next block's S^T and dP^T), the compute warpgroups (P^T, dS^T)
 # and the dQ drain warpgroup.  The phase each wait means is the block index
 # (or half of it for the two Q stages).
 
@@ -223,14 +223,13 @@ def bwd_issuer(n):
         yield ("wait", "PFULL", i & 1, i)
         yield ("commit", "DVDONE")                                          # dV(i)
         yield ("wait", "DSFULL", i & 1, i)
+        yield ("wait", "DVDONE", i & 1, i)
+        yield ("commit", "DQFULL")                                          # dQ^T(i)
         yield ("commit", ("QEMPTY", s))                                     # dK(i)
         if i + 1 < n:
             yield ("wait", ("QFULL", s ^ 1), ((i + 1) >> 1) & 1, (i + 1) >> 1)
             yield ("wait", ("QEMPTY", s), (i >> 1) & 1, i >> 1)
             yield ("commit", "SFULL")                                       # S^T(i+1)
-        yield ("wait", "DVDONE", i & 1, i)
-        yield ("commit", "DQFULL")                                          # dQ^T(i)
-        if i + 1 < n:
             yield ("wait", "DOFULL", (i + 1) & 1, i + 1)
             yield ("wait", "DQFREE", i & 1, i)
             yield ("commit", "DPFULL")                                      # dP^T(i+1)
