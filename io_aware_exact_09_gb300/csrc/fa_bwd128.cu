@@ -22,8 +22,9 @@
 // Shared memory (224 KB): K, V; Q double-buffered, dO single; the dS^T tile
 // (the dQ MMA's B operand); 32 KB of dQ staging.
 //
-// Roles (512 threads): warp 0 TMA producer; warp 1 tcgen05 issuer; warp 2
-// the LSE/D stager; warps 4-7 and 8-11 two compute warpgroups,
+// Roles (512 threads): warp 0 TMA producer (under the causal mask also the
+// LSE/D staging); warp 1 tcgen05 issuer; warp 2 the LSE/D stager
+// (non-causal); warps 4-7 and 8-11 two compute warpgroups,
 // one key row per thread, warpgroup w on query columns [64w, 64w + 64);
 // warps 12-15 the dQ drain, one head-dimension row of dQ^T per thread: TMEM
 // -> swizzled shared staging (two halves of 64 query columns, 8 KB per warp)
@@ -207,6 +208,40 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
     const int first = next_qb(-1);
     float *lse_s = reinterpret_cast<float *>(sb + S::OFF_LSE);   // log2 domain
     float *dv_s = reinterpret_cast<float *>(sb + S::OFF_DV);
+    // LSE and D of a block, raw, for lane `lane`'s four rows (row >= Lq: LSE
+    // -inf, D 0), and their conversion into the staging buffers: LSE into the
+    // log2 domain, +inf for a row past the sequence's end or with no visible
+    // key (its P is then 0)
+    auto fetch_lse = [&](int qb, float (&rl)[BQ / 32], float (&rd)[BQ / 32]) {
+#pragma unroll
+        for (int u = 0; u < BQ / 32; ++u) {
+            const int qq = qb * BQ + u * 32 + lane;
+            rl[u] = -INFINITY;
+            rd[u] = 0.f;
+            if (qq < Lq) {
+                rl[u] = p.LSE[lse_index(qq)];
+                rd[u] = p.Dvec[d_index(qq)];
+            }
+        }
+    };
+    auto store_lse = [&](const float (&rl)[BQ / 32]) {
+#pragma unroll
+        for (int u = 0; u < BQ / 32; ++u)
+            lse_s[u * 32 + lane] = (rl[u] == -INFINITY) ? INFINITY : rl[u] * 1.4426950408889634f;
+    };
+    auto store_d = [&](const float (&rd)[BQ / 32]) {
+#pragma unroll
+        for (int u = 0; u < BQ / 32; ++u) dv_s[u * 32 + lane] = rd[u];
+    };
+    // Who stages them: without the causal mask a warp of its own (warp 2),
+    // which loads the next block's values while the current one computes and
+    // stores each buffer as soon as its pass has read it; under the causal
+    // mask the producer, behind the previous block's dS pass.  Measured on
+    // the long-context shapes: the stager warp takes the non-causal backward
+    // from 4.95 to 4.74 ms but the causal one from 2.36 to 2.50 ms (same
+    // GPU, several variants of the stager alike), so each mode keeps the
+    // faster one.
+    const bool stager = !p.causal;
 
     if (warp < 4) {
         setmaxnreg_dec<S::REGS_CTRL>();
@@ -239,6 +274,19 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
                     }
                 }
                 nl = i + 1;
+                if (!stager) {
+                    // LSE and D of block i once the dS pass has read block i - 1's
+                    if (!mbar_wait_warp(bar(S::B_DFREE), ((uint32_t)i & 1u) ^ 1u, g, 0x123)) {
+                        ok = false;
+                        break;
+                    }
+                    float rl[BQ / 32], rd[BQ / 32];
+                    fetch_lse(qb, rl, rd);
+                    store_lse(rl);
+                    store_d(rd);
+                    mbar_arrive(bar(S::B_LSE));
+                    mbar_arrive(bar(S::B_D));
+                }
             }
             if (!ok && lane == 0) {
                 // gave up: let every copy already issued land before the CTA exits
@@ -247,43 +295,27 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
                     b128_drain_wait(bar(S::B_QFULL + (j & 1)), (uint32_t)(j >> 1) & 1u);
                 if (nl > 0) b128_drain_wait(bar(S::B_DOFULL), (uint32_t)(nl - 1) & 1u);
             }
-        } else if (warp == 2 && first < Tqb) {
-            // ---------------------------------------------------------- LSE / D stager
-            // LSE (log2 domain; +inf past the sequence's last query or for a row
-            // with no visible key, so that its P is 0) and D of each block.  The
-            // next block's values are loaded into registers while the current
-            // block computes; LSE is stored as soon as the P pass has read the
-            // previous block's, D as soon as the dS pass has read the previous
-            // D, so that no global-load latency falls between two blocks (staged
-            // by the producer behind the previous block's release, the compute
-            // warps waited ~3,500 cycles per block for them).
+        } else if (warp == 2 && stager && first < Tqb) {
+            // ---------------------------------------------------------- LSE / D stager (non-causal)
+            // The next block's values are loaded into registers while the
+            // current block computes; LSE is stored as soon as the P pass has
+            // read the previous block's, D as soon as the dS pass has read the
+            // previous D, so that no global-load latency falls between two
+            // blocks (staged by the producer behind the previous block's
+            // release, the compute warps waited ~3,500 cycles per block for them
+            // on the non-causal long-context shape).
             float rl[BQ / 32], rd[BQ / 32];
-            auto fetch = [&](int qb) {
-#pragma unroll
-                for (int u = 0; u < BQ / 32; ++u) {
-                    const int qq = qb * BQ + u * 32 + lane;
-                    rl[u] = -INFINITY;
-                    rd[u] = 0.f;
-                    if (qq < Lq) {
-                        rl[u] = p.LSE[lse_index(qq)];
-                        rd[u] = p.Dvec[d_index(qq)];
-                    }
-                }
-            };
             int i = 0;
-            fetch(first);
+            fetch_lse(first, rl, rd);
             for (int qb = first; qb < Tqb; ++i) {
                 if (i > 0 && !mbar_wait_warp(bar(S::B_LSEFREE), (uint32_t)(i - 1) & 1u, g, 0x124)) break;
-#pragma unroll
-                for (int u = 0; u < BQ / 32; ++u)
-                    lse_s[u * 32 + lane] = (rl[u] == -INFINITY) ? INFINITY : rl[u] * 1.4426950408889634f;
+                store_lse(rl);
                 mbar_arrive(bar(S::B_LSE));
                 if (i > 0 && !mbar_wait_warp(bar(S::B_DFREE), (uint32_t)(i - 1) & 1u, g, 0x125)) break;
-#pragma unroll
-                for (int u = 0; u < BQ / 32; ++u) dv_s[u * 32 + lane] = rd[u];
+                store_d(rd);
                 mbar_arrive(bar(S::B_D));
                 qb = next_qb(qb);
-                if (qb < Tqb) fetch(qb);
+                if (qb < Tqb) fetch_lse(qb, rl, rd);
             }
         } else if (warp == 1) {
             // ---------------------------------------------------------- MMA issuer

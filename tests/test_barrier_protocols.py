@@ -184,12 +184,15 @@ def run(seed, n_tiles, per_buffer_pfull, p_rescale=0.3):
 # The roles of `fa_bwd128_kernel` for one key tile and n query blocks: a
 # producer (K, V once; per block Q into one of two stages, dO into one slot),
 # the LSE/D stager (one buffer each, refilled as soon as the P and the dS
-# pass have read them), the MMA issuer (per block dV, dQ^T, dK,
+# pass have read them; under the causal mask the producer stages both behind
+# the previous block's dS pass), the MMA issuer (per block dV, dQ^T, dK,
 # then the next block's S^T and dP^T), the compute warpgroups (P^T, dS^T)
 # and the dQ drain warpgroup.  The phase each wait means is the block index
 # (or half of it for the two Q stages).
 
-def bwd_producer(n):
+def bwd_producer(n, stages_lse=False):
+    """stages_lse: the causal mode, where the producer stages LSE and D of
+    block i itself once the dS pass has read block i-1's."""
     yield ("tma", "KV")
     for i in range(n):
         s = i & 1
@@ -197,6 +200,10 @@ def bwd_producer(n):
         yield ("wait", "DVDONE", (i & 1) ^ 1, i - 1)                        # dV(i-1) read dO
         yield ("tma", ("QFULL", s))
         yield ("tma", "DOFULL")
+        if stages_lse:
+            yield ("wait", "DFREE", (i & 1) ^ 1, i - 1)
+            yield ("arrive", "LSE")
+            yield ("arrive", "D")
 
 
 def bwd_stager(n):
@@ -257,10 +264,12 @@ def bwd_drain(n):
         yield ("arrive", "DQFREE")
 
 
-def run_bwd128(seed, n):
+def run_bwd128(seed, n, causal=False):
     rng = random.Random(seed)
-    roles = {"producer": bwd_producer(n), "stager": bwd_stager(n), "issuer": bwd_issuer(n),
+    roles = {"producer": bwd_producer(n, stages_lse=causal), "issuer": bwd_issuer(n),
              "compute": bwd_compute(n), "drain": bwd_drain(n)}
+    if not causal:
+        roles["stager"] = bwd_stager(n)
     schedule(rng, roles, lambda name: 1)
 
 
@@ -805,7 +814,7 @@ def test_bwd64_model_finds_a_dropped_lse_free_wait():
 
 def test_bwd128_protocol_never_aliases():
     for i in range(600):
-        run_bwd128(seed=i, n=(1, 2, 3, 4, 5, 9, 16)[i % 7])
+        run_bwd128(seed=i, n=(1, 2, 3, 4, 5, 9, 16)[i % 7], causal=bool(i & 1))
 
 
 def test_bwd128_model_finds_a_dropped_drain_wait():
