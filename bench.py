@@ -62,7 +62,7 @@ if ROOT not in sys.path:
 
 DEFAULT_WORKLOAD = "longctx_b1h16n16384d128"
 FWD_BWD_FACTOR = 3.5          # forward + backward = forward x (1 + 2.5)
-KERNEL_SOURCES = {"fa_fwd_kernel": "fa_fwd.cu", "fa_bwd_kernel": "fa_bwd.cu", "fa_bwd128_kernel": "fa_bwd128.cu",
+KERNEL_SOURCES = {"fa_fwd_kernel": "fa_fwd.cu", "fa_bwd64_kernel": "fa_bwd64.cu", "fa_bwd128_kernel": "fa_bwd128.cu",
                   "fa_fwd_kernel_fp8": "fa_fwd_fp8.cu", "fa_decode_kernel": "fa_decode.cu",
                   "fa_fwd_kernel_varlen": "fa_fwd.cu"}
 
@@ -770,7 +770,7 @@ def run_varlen(args, w):
     roofline = {"bound": "tensor",
                 "kernel": ("fa_fwd_kernel<%d, varlen>" % d) if dom_forward else
                           ("fa_bwd_varlen (pre + %s<varlen> + convert)" % ("fa_bwd128_kernel" if d == 128 else
-                                                                           "fa_bwd_kernel")),
+                                                                           "fa_bwd64_kernel")),
                 "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                 "traffic": ncu_traffic("fa_fwd_kernel_varlen", w.name) if dom_forward else None,
                 "peak_source": "%s %s" % (peak_src, peak_kind)}
@@ -937,7 +937,7 @@ class SquareStep:
                                                None if c["key_len"] is None else c["key_len"].tolist(),
                                                None if c["block_mask"] is None else c["block_mask"])
         self.ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
-        self.bwd_name = "fa_bwd128_kernel" if d == 128 else "fa_bwd_kernel"
+        self.bwd_name = "fa_bwd128_kernel" if d == 128 else "fa_bwd64_kernel"
 
     def _check(self, st, where):
         if st != 0:
