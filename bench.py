@@ -64,7 +64,7 @@ DEFAULT_WORKLOAD = "longctx_b1h16n16384d128"
 FWD_BWD_FACTOR = 3.5          # forward + backward = forward x (1 + 2.5)
 KERNEL_SOURCES = {"fa_fwd_kernel": "fa_fwd.cu", "fa_bwd64_kernel": "fa_bwd64.cu", "fa_bwd128_kernel": "fa_bwd128.cu",
                   "fa_fwd_kernel_fp8": "fa_fwd_fp8.cu", "fa_decode_kernel": "fa_decode.cu",
-                  "fa_fwd_kernel_varlen": "fa_fwd.cu"}
+                  "fa_fwd_kernel_varlen": "fa_fwd.cu", "fa_bwd_varlen": ("fa_bwd.cu", "fa_bwd128.cu")}
 
 
 # ---------------------------------------------------------------- distributed helpers
@@ -188,9 +188,12 @@ def pick_peak(peaks, clk):
     return sustained, "bf16_tflops_sustained (SM clock below its maximum or not recorded)"
 
 
-def source_digest(fname: str) -> str:
+def source_digest(fname) -> str:
+    """Digest of a kernel's source file(s) (a name or a tuple of names) and the
+    shared device headers."""
     h = hashlib.sha256()
-    for f in sorted({fname, "fa_ptx.cuh", "fa_tiles.cuh"}):
+    files = {fname} if isinstance(fname, str) else set(fname)
+    for f in sorted(files | {"fa_ptx.cuh", "fa_tiles.cuh"}):
         with open(os.path.join(ROOT, "io_aware_exact_09_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -772,7 +775,9 @@ def run_varlen(args, w):
                           ("fa_bwd_varlen (pre + %s<varlen> + convert)" % ("fa_bwd128_kernel" if d == 128 else
                                                                            "fa_bwd64_kernel")),
                 "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": ncu_traffic("fa_fwd_kernel_varlen", w.name) if dom_forward else None,
+                "traffic": ncu_traffic("fa_fwd_kernel_varlen" if dom_forward else "fa_bwd_varlen", w.name),
+                "ncu_tensor_pipe_active_pct": ncu_tensor_pipe("fa_fwd_kernel_varlen" if dom_forward else "fa_bwd_varlen",
+                                                              w.name),
                 "peak_source": "%s %s" % (peak_src, peak_kind)}
     e2e = None
     if not args.no_e2e:
