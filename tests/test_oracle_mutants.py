@@ -12,7 +12,10 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "fa_oracle.c")
 
 MUTANTS = {
-    "dQ without scale": ("dQh[(int64_t)i * d + t] = scale * acc;", "dQh[(int64_t)i * d + t] = acc;"),
+    "dQ without scale": ("acc += dS[(int64_t)i * N + j] * Kh[(int64_t)j * d + t];\n                    dQh[(int64_t)i * d + t] = scale * acc;",
+                         "acc += dS[(int64_t)i * N + j] * Kh[(int64_t)j * d + t];\n                    dQh[(int64_t)i * d + t] = acc;"),
+    "rect dQ without scale": ("acc += dS[(int64_t)i * Nk + j] * Kh[(int64_t)j * d + t];\n                dQh[(int64_t)i * d + t] = scale * acc;",
+                              "acc += dS[(int64_t)i * Nk + j] * Kh[(int64_t)j * d + t];\n                dQh[(int64_t)i * d + t] = acc;"),
     "dK transposed dS": ("ak += dS[(int64_t)i * N + j] * Qh[(int64_t)i * d + t];",
                          "ak += dS[(int64_t)j * N + i] * Qh[(int64_t)i * d + t];"),
     "dS sign of D": ("dS[(int64_t)i * N + j] = p * (dp - Dv[i]);", "dS[(int64_t)i * N + j] = p * (dp + Dv[i]);"),
