@@ -16,7 +16,8 @@
 //     split) is paid once, work items (key tile, b*h) come from a counter in
 //     the workspace (words 2 and 3, left at zero by every launch: the last
 //     CTA to stop taking items resets it), head-major with the causally
-//     heaviest key tile of a head first;
+//     heaviest key tile of a head first, or, when the items differ in length,
+//     spread across heads (key tile 0 of every head first) for a short tail;
 //   - K and V double-buffered: the next item's tiles load while the current
 //     item computes;
 //   - a dQ-drain warpgroup of its own (TMEM -> swizzled staging -> TMA
@@ -218,8 +219,9 @@ __global__ void __launch_bounds__(512, 1) fa_bwd64_kernel(const __grid_constant_
                     if (lane == 0) j = (int)atomicAdd(sched, 1u);
                     j = __shfl_sync(0xffffffffu, j, 0);
                     if (j >= n_items) break;
-                    // item j: head-major, the causally heaviest (lowest) key tile first
-                    const int kt = j % p.Tk, bh = j / p.Tk;
+                    // item j: head-major, the causally heaviest (lowest) key tile first;
+                    // spread: key tile 0 of every head first, then key tile 1
+                    const int kt = p.spread ? j / p.BH : j % p.Tk, bh = p.spread ? j % p.BH : j / p.Tk;
                     const int b = bh / p.H, h = bh % p.H;
                     int q_start = 0, k_start = 0, Lq = p.N, Lk = p.N;
                     bool bad = false;

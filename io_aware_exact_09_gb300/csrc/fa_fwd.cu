@@ -141,7 +141,11 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 // is left.  The items are numbered head-major with the causally heaviest
 // pair of each head first, and handed out in that order, so the CTAs at work
 // at one time share one head's K and V in L2 and the longest items start
-// first.  The counter resets itself: the last CTA to finish taking items sets
+// first.  When the items differ in length (causal, key padding, block mask,
+// ragged) the host asks for the spread order instead: the heaviest pair of
+// every head, then the next, so that the last items handed out are the
+// shortest of all (head-major would start the last head's heaviest pair near
+// the end, where it runs alone).  The counter resets itself: the last CTA to finish taking items sets
 // it back to zero, so the next launch on the same workspace starts from 0.
 template <int D, bool VARLEN, int BC, int QPC>
 __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
@@ -236,9 +240,10 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                     if (lane == 0) j = (int)atomicAdd(sched, 1u);
                     j = __shfl_sync(0xffffffffu, j, 0);
                     if (j >= n_items) break;
-                    // item j: head-major, the causally heaviest pair of the head first
-                    const int pq = Tp - 1 - j % Tp;
-                    const int bh = j / Tp;
+                    // item j: head-major, the causally heaviest pair of the head first;
+                    // spread: the heaviest pair of every head first, then the next
+                    const int pq = Tp - 1 - (p.spread ? j / p.BH : j % Tp);
+                    const int bh = p.spread ? j % p.BH : j / Tp;
                     const int b = bh / p.H, h = bh % p.H;
                     int q_start = 0, k_start = 0, Lq = p.N, Lk = p.N;
                     bool bad = false;

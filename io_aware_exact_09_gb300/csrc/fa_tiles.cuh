@@ -101,6 +101,9 @@ struct FwdParams {
     int H, N, BH, Tq, Tk;
     int causal;
     float scale_log2;                // softmax_scale * log2(e)
+    int spread;                      // persistent grid: items handed out query-tile-pair-major across
+                                     // heads (heaviest pairs of every head first), else head-major;
+                                     // set when the items differ in length
 };
 
 struct DecParams {
@@ -139,6 +142,8 @@ struct BwdParams {
     int causal;
     float scale_log2;                // softmax_scale * log2(e)
     float scale;                     // softmax_scale
+    int spread;                      // d = 64 persistent grid: items handed out key-tile-major across
+                                     // heads (heaviest key tiles of every head first), else head-major
 };
 
 // The sequence a CTA of a ragged batch works on: query rows [q_start,
