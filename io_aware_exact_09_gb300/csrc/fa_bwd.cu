@@ -18,6 +18,7 @@
 //      (d = 128): one key tile per CTA or work item, recomputing S and P
 //      tile by tile, dQ reduce-added into dQacc
 //   3. fa_bwd_convert: dQ = bf16(scale * dQacc)
+#include <algorithm>
 #include <climits>
 
 #include "fa_internal.h"
@@ -25,32 +26,50 @@
 
 namespace fa {
 
-// D = rowsum(dO * O) in fp32 and dQacc = 0, one warp per row.
+// D = rowsum(dO * O) in fp32 and dQacc = 0.  Each thread takes 8 consecutive
+// elements of a row (16-byte loads; D / 8 threads per row, reduced with
+// shuffles inside an aligned group of lanes) and four rows a grid stride
+// apart at once, so that enough bytes are in flight to keep HBM busy.  The
+// loop bound is uniform over the block, so every lane reaches the shuffles.
 template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __nv_bfloat16 *__restrict__ O,
                                                          const __nv_bfloat16 *__restrict__ dO,
                                                          float *__restrict__ Dvec, float *__restrict__ dQacc,
                                                          int64_t rows) {
-    const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (row >= rows) return;
-    constexpr int PER = D / 32;   // elements per lane: 2 or 4
-    float acc = 0.f;
-    if (PER == 4) {
-        const uint2 o = reinterpret_cast<const uint2 *>(O + row * D)[lane];
-        const uint2 g = reinterpret_cast<const uint2 *>(dO + row * D)[lane];
-        acc = bf16lo(o.x) * bf16lo(g.x) + bf16hi(o.x) * bf16hi(g.x) + bf16lo(o.y) * bf16lo(g.y) +
-              bf16hi(o.y) * bf16hi(g.y);
-        reinterpret_cast<float4 *>(dQacc + row * D)[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
-    } else {
-        const uint32_t o = reinterpret_cast<const uint32_t *>(O + row * D)[lane];
-        const uint32_t g = reinterpret_cast<const uint32_t *>(dO + row * D)[lane];
-        acc = bf16lo(o) * bf16lo(g) + bf16hi(o) * bf16hi(g);
-        reinterpret_cast<float2 *>(dQacc + row * D)[lane] = make_float2(0.f, 0.f);
-    }
+    constexpr int TPR = D / 8;                 // threads per row
+    constexpr int RPB = 256 / TPR;             // rows per block and pass
+    constexpr int U = 4;                       // passes in flight per thread
+    const int sub = threadIdx.x % TPR;
+    const int64_t stride = (int64_t)gridDim.x * RPB;
+    for (int64_t b0 = (int64_t)blockIdx.x * RPB; b0 < rows; b0 += stride * U) {
+        uint4 o[U], g[U];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) Dvec[row] = acc;
+        for (int u = 0; u < U; ++u) {
+            const int64_t row = b0 + threadIdx.x / TPR + u * stride;
+            if (row < rows) {
+                o[u] = __ldg(reinterpret_cast<const uint4 *>(O + row * D) + sub);
+                g[u] = __ldg(reinterpret_cast<const uint4 *>(dO + row * D) + sub);
+            } else {
+                o[u] = g[u] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t row = b0 + threadIdx.x / TPR + u * stride;
+            float acc = bf16lo(o[u].x) * bf16lo(g[u].x) + bf16hi(o[u].x) * bf16hi(g[u].x) +
+                        bf16lo(o[u].y) * bf16lo(g[u].y) + bf16hi(o[u].y) * bf16hi(g[u].y) +
+                        bf16lo(o[u].z) * bf16lo(g[u].z) + bf16hi(o[u].z) * bf16hi(g[u].z) +
+                        bf16lo(o[u].w) * bf16lo(g[u].w) + bf16hi(o[u].w) * bf16hi(g[u].w);
+#pragma unroll
+            for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            if (row < rows) {
+                float4 *z = reinterpret_cast<float4 *>(dQacc + row * D) + 2 * sub;
+                z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+                z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (sub == 0) Dvec[row] = acc;
+            }
+        }
+    }
 }
 
 // dQ = bf16(scale * dQacc), 8 elements per thread.
@@ -113,7 +132,10 @@ cudaError_t launch_bwd_main_varlen(int d, const BwdParams &p, cudaStream_t st) {
 
 cudaError_t launch_bwd_pre(int d, const void *O, const void *dO, float *Dvec, float *dQacc, int64_t rows,
                            cudaStream_t st) {
-    const unsigned grid = (unsigned)((rows + 7) / 8);
+    // rows per block and pass: 256 / (d / 8); four passes per thread
+    const int64_t per_block = (int64_t)(256 / (d / 8)) * 4;
+    const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>((rows + per_block - 1) / per_block,
+                                                                           (int64_t)device_sm_count() * 16));
     if (d == 64)
         fa_bwd_pre_kernel<64><<<grid, 256, 0, st>>>((const __nv_bfloat16 *)O, (const __nv_bfloat16 *)dO, Dvec,
                                                     dQacc, rows);
