@@ -142,8 +142,9 @@ struct BwdParams {
     int causal;
     float scale_log2;                // softmax_scale * log2(e)
     float scale;                     // softmax_scale
-    int spread;                      // d = 64 persistent grid: items handed out key-tile-major across
-                                     // heads (heaviest key tiles of every head first), else head-major
+    int spread;                      // d = 64 persistent grid: items (key tile, b*h) taken
+                                     // key-tile-major across heads (key tile 0 of every head first),
+                                     // else head-major; set when the items differ in length
 };
 
 // The sequence a CTA of a ragged batch works on: query rows [q_start,
