@@ -642,16 +642,36 @@ __global__ void __launch_bounds__(512, 1) fa_bwd64_kernel(const __grid_constant_
                     wk[t] = pack_bf16x2(__uint_as_float(a[2 * t]) * p.scale, __uint_as_float(a[2 * t + 1]) * p.scale);
                     wv[t] = pack_bf16x2(__uint_as_float(v[2 * t]), __uint_as_float(v[2 * t + 1]));
                 }
-                if (key < it.Lk) {
-                    const size_t krow = VARLEN ? (size_t)(it.k_start + key) * p.H + it.h : (size_t)it.bh * p.N + key;
-                    uint4 *dk4 = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.dK) + krow * D + 32 * wg);
-                    uint4 *dv4 = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.dV) + krow * D + 32 * wg);
+                // Through this warp's own rows of the dS tile (free: the item's
+                // products are complete, and only this warp writes these rows
+                // again, in its next dS pass): 64 bytes of dK and of dV per row
+                // (128-byte swizzle), then read back so that each store covers
+                // 8 rows x 64 contiguous bytes.  Stored straight from registers,
+                // each store touched 32 rows and the epilogue took ~4,000 cycles.
+                uint8_t *stg = sb + S::OFF_DS + wg * S::TILE + wq * 32 * 128;
 #pragma unroll
-                    for (int t = 0; t < 4; ++t) {
-                        dk4[t] = make_uint4(wk[4 * t], wk[4 * t + 1], wk[4 * t + 2], wk[4 * t + 3]);
-                        dv4[t] = make_uint4(wv[4 * t], wv[4 * t + 1], wv[4 * t + 2], wv[4 * t + 3]);
+                for (int t = 0; t < 4; ++t) {
+                    *reinterpret_cast<uint4 *>(stg + lane * 128 + ((t ^ (lane & 7)) << 4)) =
+                        make_uint4(wk[4 * t], wk[4 * t + 1], wk[4 * t + 2], wk[4 * t + 3]);
+                    *reinterpret_cast<uint4 *>(stg + lane * 128 + (((4 + t) ^ (lane & 7)) << 4)) =
+                        make_uint4(wv[4 * t], wv[4 * t + 1], wv[4 * t + 2], wv[4 * t + 3]);
+                }
+                __syncwarp();
+                const int u = lane & 3;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int rr = 8 * j + (lane >> 2);          // row of this warp's 32
+                    const uint4 kq = *reinterpret_cast<const uint4 *>(stg + rr * 128 + ((u ^ (rr & 7)) << 4));
+                    const uint4 vq = *reinterpret_cast<const uint4 *>(stg + rr * 128 + (((4 + u) ^ (rr & 7)) << 4));
+                    const int keyr = it.kt * kTile + wq * 32 + rr;
+                    if (keyr < it.Lk) {
+                        const size_t krow =
+                            VARLEN ? (size_t)(it.k_start + keyr) * p.H + it.h : (size_t)it.bh * p.N + keyr;
+                        *reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.dK) + krow * D + 32 * wg + 8 * u) = kq;
+                        *reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.dV) + krow * D + 32 * wg + 8 * u) = vq;
                     }
                 }
+                __syncwarp();
             }
             // (the next item's first dV and dK into these columns follow this
             // warpgroup's next P and dS arrivals, which follow these loads)
