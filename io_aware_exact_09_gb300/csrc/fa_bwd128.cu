@@ -101,7 +101,7 @@ __device__ __forceinline__ void b128_drain_wait(uint32_t bar, uint32_t parity) {
 // 64-column half, so neither overwrites fp32 values the other still reads.
 __device__ __forceinline__ uint32_t packed_col128(int k) { return (uint32_t)((k >> 2) * 64 + 8 * (k & 3)); }
 
-template <bool VARLEN>
+template <bool VARLEN, bool STAGER>
 __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant__ BwdParams p) {
     using S = Bwd128;
     constexpr int BQ = S::BQ, CW = S::CW;
@@ -240,8 +240,9 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
     // the long-context shapes: the stager warp takes the non-causal backward
     // from 4.95 to 4.74 ms but the causal one from 2.36 to 2.50 ms (same
     // GPU, several variants of the stager alike), so each mode keeps the
-    // faster one.
-    const bool stager = !p.causal;
+    // faster one.  The mode is a template parameter (STAGER = !causal), so
+    // that each kernel carries only its own staging code.
+    constexpr bool stager = STAGER;
 
     if (warp < 4) {
         setmaxnreg_dec<S::REGS_CTRL>();
@@ -522,35 +523,90 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
             ok = mbar_wait_warp(bar(S::B_ACC), 0, g, 0x425);
             tc_fence_after();
         }
+        if constexpr (!STAGER) {
         if (ok) {
-            const size_t krow = VARLEN ? (size_t)(k_start + key) * p.H + h : (size_t)bh * p.N + key;
-            __nv_bfloat16 *dkrow = reinterpret_cast<__nv_bfloat16 *>(p.dK) + krow * 128;
-            __nv_bfloat16 *dvrow = reinterpret_cast<__nv_bfloat16 *>(p.dV) + krow * 128;
+            // causal mode: dK (* scale) and dV, this warp's 32 rows x 64 columns
+            // (128 bytes) of each through its own 8 KB of the query tiles (free:
+            // every product is complete and no further block is loaded), read
+            // back so that each store covers 4 whole 128-byte rows (stored
+            // straight from registers, every store touched 32 rows: measured
+            // 2-8 % slower on causal shapes; the non-causal kernel, whose speed
+            // changed with its code rather than with this work, keeps that)
+            uint8_t *stg = sb + S::OFF_Q + (warp - 4) * 8192;
 #pragma unroll 1
-            for (int j = wg * 2; j < wg * 2 + 2; ++j) {
+            for (int jh = 0; jh < 2; ++jh) {
                 uint32_t a[32], vv[32];
                 if (i > 0) {
-                    tmem_ld32(tmem + lane_off + S::TM_DK + 32u * j, a);
-                    tmem_ld32(tmem + lane_off + S::TM_DV + 32u * j, vv);
+                    tmem_ld32(tmem + lane_off + S::TM_DK + 32u * (wg * 2 + jh), a);
+                    tmem_ld32(tmem + lane_off + S::TM_DV + 32u * (wg * 2 + jh), vv);
                     tmem_ld_wait(a);
                     tmem_ld_wait(vv);
                 } else {
 #pragma unroll
                     for (int t = 0; t < 32; ++t) a[t] = vv[t] = 0u;
                 }
-                uint32_t wk[16], wv[16];
 #pragma unroll
-                for (int t = 0; t < 16; ++t) {
-                    wk[t] = pack_bf16x2(__uint_as_float(a[2 * t]) * p.scale, __uint_as_float(a[2 * t + 1]) * p.scale);
-                    wv[t] = pack_bf16x2(__uint_as_float(vv[2 * t]), __uint_as_float(vv[2 * t + 1]));
+                for (int t = 0; t < 4; ++t) {
+                    const int off = lane * 128 + (((4 * jh + t) ^ (lane & 7)) << 4);
+                    *reinterpret_cast<uint4 *>(stg + off) = make_uint4(
+                        pack_bf16x2(__uint_as_float(a[8 * t]) * p.scale, __uint_as_float(a[8 * t + 1]) * p.scale),
+                        pack_bf16x2(__uint_as_float(a[8 * t + 2]) * p.scale, __uint_as_float(a[8 * t + 3]) * p.scale),
+                        pack_bf16x2(__uint_as_float(a[8 * t + 4]) * p.scale, __uint_as_float(a[8 * t + 5]) * p.scale),
+                        pack_bf16x2(__uint_as_float(a[8 * t + 6]) * p.scale, __uint_as_float(a[8 * t + 7]) * p.scale));
+                    *reinterpret_cast<uint4 *>(stg + 4096 + off) = make_uint4(
+                        pack_bf16x2(__uint_as_float(vv[8 * t]), __uint_as_float(vv[8 * t + 1])),
+                        pack_bf16x2(__uint_as_float(vv[8 * t + 2]), __uint_as_float(vv[8 * t + 3])),
+                        pack_bf16x2(__uint_as_float(vv[8 * t + 4]), __uint_as_float(vv[8 * t + 5])),
+                        pack_bf16x2(__uint_as_float(vv[8 * t + 6]), __uint_as_float(vv[8 * t + 7])));
                 }
-                if (key < Lk) {
-                    uint4 *dk4 = reinterpret_cast<uint4 *>(dkrow + 32 * j);
-                    uint4 *dv4 = reinterpret_cast<uint4 *>(dvrow + 32 * j);
+            }
+            __syncwarp();
+            const int u = lane & 7;
 #pragma unroll
-                    for (int t = 0; t < 4; ++t) {
-                        dk4[t] = make_uint4(wk[4 * t], wk[4 * t + 1], wk[4 * t + 2], wk[4 * t + 3]);
-                        dv4[t] = make_uint4(wv[4 * t], wv[4 * t + 1], wv[4 * t + 2], wv[4 * t + 3]);
+            for (int jj = 0; jj < 8; ++jj) {
+                const int rr = 4 * jj + (lane >> 3);                // row of this warp's 32
+                const int off = rr * 128 + ((u ^ (rr & 7)) << 4);
+                const uint4 kq = *reinterpret_cast<const uint4 *>(stg + off);
+                const uint4 vq = *reinterpret_cast<const uint4 *>(stg + 4096 + off);
+                const int keyr = k0 + wq * 32 + rr;
+                if (keyr < Lk) {
+                    const size_t krow = VARLEN ? (size_t)(k_start + keyr) * p.H + h : (size_t)bh * p.N + keyr;
+                    *reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.dK) + krow * 128 + 64 * wg + 8 * u) = kq;
+                    *reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.dV) + krow * 128 + 64 * wg + 8 * u) = vq;
+                }
+            }
+        }
+        } else {
+            if (ok) {
+                const size_t krow = VARLEN ? (size_t)(k_start + key) * p.H + h : (size_t)bh * p.N + key;
+                __nv_bfloat16 *dkrow = reinterpret_cast<__nv_bfloat16 *>(p.dK) + krow * 128;
+                __nv_bfloat16 *dvrow = reinterpret_cast<__nv_bfloat16 *>(p.dV) + krow * 128;
+    #pragma unroll 1
+                for (int j = wg * 2; j < wg * 2 + 2; ++j) {
+                    uint32_t a[32], vv[32];
+                    if (i > 0) {
+                        tmem_ld32(tmem + lane_off + S::TM_DK + 32u * j, a);
+                        tmem_ld32(tmem + lane_off + S::TM_DV + 32u * j, vv);
+                        tmem_ld_wait(a);
+                        tmem_ld_wait(vv);
+                    } else {
+    #pragma unroll
+                        for (int t = 0; t < 32; ++t) a[t] = vv[t] = 0u;
+                    }
+                    uint32_t wk[16], wv[16];
+    #pragma unroll
+                    for (int t = 0; t < 16; ++t) {
+                        wk[t] = pack_bf16x2(__uint_as_float(a[2 * t]) * p.scale, __uint_as_float(a[2 * t + 1]) * p.scale);
+                        wv[t] = pack_bf16x2(__uint_as_float(vv[2 * t]), __uint_as_float(vv[2 * t + 1]));
+                    }
+                    if (key < Lk) {
+                        uint4 *dk4 = reinterpret_cast<uint4 *>(dkrow + 32 * j);
+                        uint4 *dv4 = reinterpret_cast<uint4 *>(dvrow + 32 * j);
+    #pragma unroll
+                        for (int t = 0; t < 4; ++t) {
+                            dk4[t] = make_uint4(wk[4 * t], wk[4 * t + 1], wk[4 * t + 2], wk[4 * t + 3]);
+                            dv4[t] = make_uint4(wv[4 * t], wv[4 * t + 1], wv[4 * t + 2], wv[4 * t + 3]);
+                        }
                     }
                 }
             }
@@ -624,18 +680,22 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
 
 int bwd128_smem_bytes() { return Bwd128::SMEM_BYTES; }
 
-template <bool VARLEN>
+template <bool VARLEN, bool STAGER>
 static cudaError_t launch_bwd128_t(const BwdParams &p, cudaStream_t st) {
     const int smem = Bwd128::SMEM_BYTES;
     cudaError_t e =
-        cudaFuncSetAttribute(fa_bwd128_kernel<VARLEN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaFuncSetAttribute(fa_bwd128_kernel<VARLEN, STAGER>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    fa_bwd128_kernel<VARLEN><<<(unsigned)p.Tk * (unsigned)p.BH, Bwd128::THREADS, smem, st>>>(p);
+    fa_bwd128_kernel<VARLEN, STAGER><<<(unsigned)p.Tk * (unsigned)p.BH, Bwd128::THREADS, smem, st>>>(p);
     return cudaGetLastError();
 }
 
-cudaError_t launch_bwd128_main(const BwdParams &p, cudaStream_t st) { return launch_bwd128_t<false>(p, st); }
+cudaError_t launch_bwd128_main(const BwdParams &p, cudaStream_t st) {
+    return p.causal ? launch_bwd128_t<false, false>(p, st) : launch_bwd128_t<false, true>(p, st);
+}
 
-cudaError_t launch_bwd128_main_varlen(const BwdParams &p, cudaStream_t st) { return launch_bwd128_t<true>(p, st); }
+cudaError_t launch_bwd128_main_varlen(const BwdParams &p, cudaStream_t st) {
+    return p.causal ? launch_bwd128_t<true, false>(p, st) : launch_bwd128_t<true, true>(p, st);
+}
 
 }  // namespace fa
