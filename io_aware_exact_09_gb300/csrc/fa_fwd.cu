@@ -147,7 +147,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 // shortest of all (head-major would start the last head's heaviest pair near
 // the end, where it runs alone).  The counter resets itself: the last CTA to finish taking items sets
 // it back to zero, so the next launch on the same workspace starts from 0.
-template <int D, bool VARLEN, int BC, int QPC>
+template <int D, bool VARLEN, int BC, int QPC, bool PLAIN>
 __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
     using S = FwdShape<D, BC>;
     extern __shared__ uint8_t smem_raw[];
@@ -202,11 +202,15 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
     const uint32_t tmem = *tmem_slot;
 
     // entry e of an item: its key tile and whether query tile x sees it
+    // PLAIN: no causal mask, key padding or block mask, N a multiple of the
+    // key tile: every visited tile is full, there is no list, and the kernel
+    // carries none of that code
     auto entry_kt = [&](const FwdItem &it, const uint16_t *lst, int e) -> int {
+        if constexpr (PLAIN) return e;
         return it.use_list ? (int)(lst[e] & 0x3FFFu) : e;
     };
     auto entry_vis = [&](const FwdItem &it, const uint16_t *lst, int x, int e) -> bool {
-        if (it.use_list) return (lst[e] >> (14 + x)) & 1u;
+        if (!PLAIN && it.use_list) return (lst[e] >> (14 + x)) & 1u;
         return e < (x ? it.kend[1] : it.kend[0]);
     };
 
@@ -266,14 +270,14 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                         it.kend[x] = fwd_key_tile_end(it.q0[x], it.qn[x], kvis, p.causal, it.shift, BC);
                         it.nq += it.qn[x] > 0 ? 1 : 0;
                     }
-                    it.use_list = (!VARLEN && p.block_mask) ? 1 : 0;
+                    it.use_list = (!PLAIN && !VARLEN && p.block_mask) ? 1 : 0;
                     it.count = max(it.kend[0], it.kend[1]);
                     // an item with no query row (past a ragged sequence's end) is not published
                     if (it.nq > 0) break;
                     it.item = -1;
                 }
                 uint16_t *lst = list_of(s);
-                if (it.item >= 0 && it.use_list) {
+                if (!PLAIN && it.item >= 0 && it.use_list) {
                     // the key tiles either query tile sees, in order, compacted by the whole warp
                     const int Tk = p.Tk;
                     int n = 0;
@@ -575,16 +579,16 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
             float m_ref = -INFINITY, l = 0.f;
             int it = 0;                              // this item's tiles
             for (int e = 0; e < count; ++e) {
-                const bool vis = use_list ? ((lst[e] >> (14 + x)) & 1u) : (e < kendx);
+                const bool vis = (!PLAIN && use_list) ? ((lst[e] >> (14 + x)) & 1u) : (e < kendx);
                 if (!vis) continue;
-                const int kt = use_list ? (int)(lst[e] & 0x3FFFu) : e;
+                const int kt = (!PLAIN && use_list) ? (int)(lst[e] & 0x3FFFu) : e;
                 const int k0 = kt * BC;
-                unsigned klass;
+                unsigned klass = kTileFull;
                 if constexpr (VARLEN)
                     klass = tile_class_shift(q0x, qnx, k0, BC, kvis, p.causal, shift);
-                else
+                else if constexpr (!PLAIN)
                     klass = tile_class(q0x, qnx, k0, BC, kvis, p.causal, 1);
-                const bool partial = klass == kTilePartial;
+                const bool partial = !PLAIN && klass == kTilePartial;
                 if (!mbar_wait_warp(bar(S::B_SFULL + x), (uint32_t)ns & 1u, g, 0x401)) {
                     ok = false;
                     break;
@@ -777,23 +781,26 @@ int device_sm_count() {
 
 int fwd_smem_bytes(int d) { return d == 64 ? FwdShape<64>::SMEM_BYTES : FwdShape<128>::SMEM_BYTES; }
 
-template <int D, bool VARLEN, int BC, int QPC>
+template <int D, bool VARLEN, int BC, int QPC, bool PLAIN = false>
 static cudaError_t launch_fwd_t(const FwdParams &p, cudaStream_t st) {
     using S = FwdShape<D, BC>;
     const int smem = S::SMEM_BYTES;
-    cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D, VARLEN, BC, QPC>,
+    cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D, VARLEN, BC, QPC, PLAIN>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     // persistent: one CTA per SM (the shared-memory footprint allows one),
     // never more CTAs than work items
     const int64_t items = (int64_t)((p.Tq + QPC - 1) / QPC) * p.BH;
     const unsigned grid = (unsigned)std::min<int64_t>(items, device_sm_count());
-    fa_fwd_kernel<D, VARLEN, BC, QPC><<<grid, S::THREADS, smem, st>>>(p);
+    fa_fwd_kernel<D, VARLEN, BC, QPC, PLAIN><<<grid, S::THREADS, smem, st>>>(p);
     return cudaGetLastError();
 }
 
 cudaError_t launch_fwd(int d, const FwdParams &p, cudaStream_t st) {
-    return d == 64 ? launch_fwd_t<64, false, 128, 2>(p, st) : launch_fwd_t<128, false, 128, 2>(p, st);
+    const bool plain = !p.causal && !p.key_len && !p.block_mask && p.N % 128 == 0;
+    if (d == 64)
+        return plain ? launch_fwd_t<64, false, 128, 2, true>(p, st) : launch_fwd_t<64, false, 128, 2>(p, st);
+    return plain ? launch_fwd_t<128, false, 128, 2, true>(p, st) : launch_fwd_t<128, false, 128, 2>(p, st);
 }
 
 cudaError_t launch_fwd_varlen(int d, const FwdParams &p, cudaStream_t st) {
