@@ -101,7 +101,7 @@ __device__ __forceinline__ void b128_drain_wait(uint32_t bar, uint32_t parity) {
 // 64-column half, so neither overwrites fp32 values the other still reads.
 __device__ __forceinline__ uint32_t packed_col128(int k) { return (uint32_t)((k >> 2) * 64 + 8 * (k & 3)); }
 
-template <bool VARLEN, bool STAGER>
+template <bool VARLEN, bool STAGER, bool PLAIN>
 __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant__ BwdParams p) {
     using S = Bwd128;
     constexpr int BQ = S::BQ, CW = S::CW;
@@ -147,7 +147,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
     };
     const int qb_start = bwd_query_block_begin(k0, kvis, p.causal, shift, BQ, Tqb);
     auto next_qb = [&](int qb) -> int {
-        if (VARLEN || !p.block_mask) {
+        if (PLAIN || VARLEN || !p.block_mask) {
             const int nq = qb < qb_start ? qb_start : qb + 1;
             return nq < Tqb ? nq : Tqb;
         }
@@ -427,7 +427,9 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
         int i = 0;
 
         for (int qb = first; qb < Tqb; qb = next_qb(qb), ++i) {
-            const unsigned klass = cls(qb);
+            // PLAIN: no causal mask, key padding or block mask, N a multiple of
+            // 128: every block is full and the masking code is not compiled
+            const unsigned klass = PLAIN ? kTileFull : cls(qb);
             const int qa = qb * BQ;
             const uint32_t ra = tmem + lane_off + S::TM_R0 + 128u * (uint32_t)(i & 1);
             const uint32_t rb = tmem + lane_off + S::TM_R0 + 128u * (uint32_t)((i & 1) ^ 1);
@@ -445,7 +447,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
                 tmem_ld32(ra + c0 + 32, sr[1]);
                 tmem_ld_wait(sr[0]);
                 tmem_ld_wait(sr[1]);
-                if (klass == kTilePartial) {
+                if (!PLAIN && klass == kTilePartial) {
                     // masked scores -> -inf, so that their p is exactly 0 (a mask
                     // test inside the exp loop below made that loop several times slower)
 #pragma unroll
@@ -680,18 +682,20 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
 
 int bwd128_smem_bytes() { return Bwd128::SMEM_BYTES; }
 
-template <bool VARLEN, bool STAGER>
+template <bool VARLEN, bool STAGER, bool PLAIN = false>
 static cudaError_t launch_bwd128_t(const BwdParams &p, cudaStream_t st) {
     const int smem = Bwd128::SMEM_BYTES;
-    cudaError_t e =
-        cudaFuncSetAttribute(fa_bwd128_kernel<VARLEN, STAGER>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = cudaFuncSetAttribute(fa_bwd128_kernel<VARLEN, STAGER, PLAIN>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    fa_bwd128_kernel<VARLEN, STAGER><<<(unsigned)p.Tk * (unsigned)p.BH, Bwd128::THREADS, smem, st>>>(p);
+    fa_bwd128_kernel<VARLEN, STAGER, PLAIN><<<(unsigned)p.Tk * (unsigned)p.BH, Bwd128::THREADS, smem, st>>>(p);
     return cudaGetLastError();
 }
 
 cudaError_t launch_bwd128_main(const BwdParams &p, cudaStream_t st) {
-    return p.causal ? launch_bwd128_t<false, false>(p, st) : launch_bwd128_t<false, true>(p, st);
+    if (p.causal) return launch_bwd128_t<false, false>(p, st);
+    const bool plain = !p.key_len && !p.block_mask && p.N % 128 == 0;
+    return plain ? launch_bwd128_t<false, true, true>(p, st) : launch_bwd128_t<false, true>(p, st);
 }
 
 cudaError_t launch_bwd128_main_varlen(const BwdParams &p, cudaStream_t st) {
