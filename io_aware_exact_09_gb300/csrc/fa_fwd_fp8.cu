@@ -84,6 +84,7 @@ __device__ __forceinline__ void f8_drain_wait(uint32_t bar, uint32_t parity) {
         if (globaltimer_ns() - t0 > FA_WAIT_TIMEOUT_NS) break;
 }
 
+template <bool PLAIN>
 __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constant__ FwdParams p) {
     using S = F8Shape;
     constexpr int D = S::D;
@@ -126,15 +127,20 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
     auto q0_of = [&](int x) { return x ? q0[1] : q0[0]; };
     auto qn_of = [&](int x) { return x ? qn[1] : qn[0]; };
     auto kend_of = [&](int x) { return x ? kend[1] : kend[0]; };
+    // PLAIN: no causal mask, key padding or block mask, N a multiple of 128:
+    // every visible tile is full and the masking code is not compiled
     auto cls = [&](int x, int kt) -> unsigned {
         if (qn_of(x) <= 0) return kTileSkip;
+        if constexpr (PLAIN) return kTileFull;
         const int on = p.block_mask ? (p.block_mask[(size_t)(2 * pq + x) * nb + kt] != 0) : 1;
         return tile_class(q0_of(x), qn_of(x), kt * kTile, kTile, kvis, p.causal, on);
     };
     // without a block mask the visible tiles of query tile x are 0 .. kend[x]-1
-    auto skip = [&](int x, int kt) -> bool { return p.block_mask ? cls(x, kt) == kTileSkip : kt >= kend_of(x); };
+    auto skip = [&](int x, int kt) -> bool {
+        return (!PLAIN && p.block_mask) ? cls(x, kt) == kTileSkip : kt >= kend_of(x);
+    };
     auto next_tile = [&](int x, int kt) -> int {
-        if (!p.block_mask) {
+        if (PLAIN || !p.block_mask) {
             const int lim = x == 2 ? kend_union : kend_of(x);
             return kt + 1 < lim ? kt + 1 : p.Tk;
         }
@@ -335,7 +341,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
             sv_n = sVh[kt];
         }
         for (; kt < p.Tk; ++it) {
-            const bool partial = cls(x, kt) == kTilePartial;
+            const bool partial = !PLAIN && cls(x, kt) == kTilePartial;
             const int k0 = kt * kTile;
             const int kt_next = next_tile(x, kt);
             // multiplier of this tile's scores; V-scale ratio rt folded into
@@ -510,10 +516,15 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
 
 cudaError_t launch_fwd_fp8(const FwdParams &p, cudaStream_t st) {
     const int smem = F8Shape::SMEM_BYTES;
-    cudaError_t e = cudaFuncSetAttribute(fa_fwd_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    const bool plain = !p.causal && !p.key_len && !p.block_mask && p.N % 128 == 0;
+    cudaError_t e = cudaFuncSetAttribute(plain ? fa_fwd_fp8_kernel<true> : fa_fwd_fp8_kernel<false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)((p.Tq + 1) / 2) * (unsigned)p.BH;
-    fa_fwd_fp8_kernel<<<grid, F8Shape::THREADS, smem, st>>>(p);
+    if (plain)
+        fa_fwd_fp8_kernel<true><<<grid, F8Shape::THREADS, smem, st>>>(p);
+    else
+        fa_fwd_fp8_kernel<false><<<grid, F8Shape::THREADS, smem, st>>>(p);
     return cudaGetLastError();
 }
 
