@@ -605,13 +605,15 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                     mbar_arrive(bar(S::B_SFREE + x));
                 }
                 if (partial) {
+                    // this row sees keys k0 .. k0 + lim - 1 of the tile: one compare
+                    // against a constant per score
+                    int lim = kvis - k0;
+                    if (p.causal) lim = min(lim, q + shift + 1 - k0);
 #pragma unroll
                     for (int j = 0; j < S::KC; ++j)
 #pragma unroll
-                        for (int t = 0; t < 32; ++t) {
-                            const int key = k0 + 32 * j + t;
-                            if (key >= kvis || (p.causal && key > q + shift)) sr[j][t] = __float_as_uint(-INFINITY);
-                        }
+                        for (int t = 0; t < 32; ++t)
+                            if (32 * j + t >= lim) sr[j][t] = __float_as_uint(-INFINITY);
                 }
                 // row maximum as eight independent 3-input chains, then a tree:
                 // one warp per sub-partition runs this, so the latency of a single
