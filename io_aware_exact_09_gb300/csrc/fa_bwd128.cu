@@ -450,13 +450,15 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
                 if (!PLAIN && klass == kTilePartial) {
                     // masked scores -> -inf, so that their p is exactly 0 (a mask
                     // test inside the exp loop below made that loop several times slower)
+                    // this key row sees the columns from lo on (none past the visible
+                    // keys): one compare against a constant per score
+                    int lo = p.causal ? key - shift - qa - c0 : INT_MIN;
+                    if (key >= kvis) lo = INT_MAX;
 #pragma unroll
                     for (int j = 0; j < 2; ++j)
 #pragma unroll
-                        for (int t = 0; t < 32; ++t) {
-                            const int qq = qa + c0 + 32 * j + t;
-                            if (key >= kvis || (p.causal && key > qq + shift)) sr[j][t] = __float_as_uint(-INFINITY);
-                        }
+                        for (int t = 0; t < 32; ++t)
+                            if (32 * j + t < lo) sr[j][t] = __float_as_uint(-INFINITY);
                 }
 #pragma unroll
                 for (int j = 0; j < 2; ++j)

@@ -537,15 +537,16 @@ __global__ void __launch_bounds__(512, 1) fa_bwd64_kernel(const __grid_constant_
 #pragma unroll
                     for (int j = 0; j < CW / 32; ++j) tmem_ld_wait(sr[j]);
                     if (klass == kTilePartial) {
-                        // masked scores -> -inf, so that their p is exactly 0
+                        // masked scores -> -inf, so that their p is exactly 0: this key
+                        // row sees the columns from lo on (none past the visible keys),
+                        // one compare against a constant per score
+                        int lo = p.causal ? key - it.shift - qa - c0 : INT_MIN;
+                        if (key >= it.kvis) lo = INT_MAX;
 #pragma unroll
                         for (int j = 0; j < CW / 32; ++j)
 #pragma unroll
-                            for (int t = 0; t < 32; ++t) {
-                                const int qq = qa + c0 + 32 * j + t;
-                                if (key >= it.kvis || (p.causal && key > qq + it.shift))
-                                    sr[j][t] = __float_as_uint(-INFINITY);
-                            }
+                            for (int t = 0; t < 32; ++t)
+                                if (32 * j + t < lo) sr[j][t] = __float_as_uint(-INFINITY);
                     }
 #pragma unroll
                     for (int j = 0; j < CW / 32; ++j)

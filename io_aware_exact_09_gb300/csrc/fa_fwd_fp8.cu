@@ -370,13 +370,15 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
             tc_fence_before();
             mbar_arrive(bar(S::B_SFREE + x));
             if (partial) {
+                // this row sees keys k0 .. k0 + lim - 1: one compare against a
+                // constant per score
+                int lim = kvis - k0;
+                if (p.causal) lim = min(lim, q + 1 - k0);
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
 #pragma unroll
-                    for (int t = 0; t < 32; ++t) {
-                        const int key = k0 + 32 * j + t;
-                        if (key >= kvis || (p.causal && key > q)) sr[j][t] = __float_as_uint(-INFINITY);
-                    }
+                    for (int t = 0; t < 32; ++t)
+                        if (32 * j + t >= lim) sr[j][t] = __float_as_uint(-INFINITY);
             }
             float pm[8];
 #pragma unroll
