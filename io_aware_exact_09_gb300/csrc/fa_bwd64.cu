@@ -122,7 +122,7 @@ __device__ __forceinline__ void b64_drain_wait(uint32_t bar, uint32_t parity) {
 // its own 64-column half and never overwrites fp32 values the other reads.
 __device__ __forceinline__ uint32_t packed_col64(int k) { return (uint32_t)((k >> 2) * 64 + 8 * (k & 3)); }
 
-template <bool VARLEN>
+template <bool VARLEN, bool LIST>
 __global__ void __launch_bounds__(512, 1) fa_bwd64_kernel(const __grid_constant__ BwdParams p) {
     using S = Bwd64;
     constexpr int BQ = S::BQ, CW = S::CW, D = S::D;
@@ -187,6 +187,9 @@ __global__ void __launch_bounds__(512, 1) fa_bwd64_kernel(const __grid_constant_
 
     // query block of entry e of an item
     auto entry_qb = [&](const BwdItem &it, const uint16_t *lst, int e) -> int {
+        // LIST: a block mask may be given (query-block lists); without one the
+        // kernel carries no list code
+        if constexpr (!LIST) return it.qb_start + e;
         return it.use_list ? (int)lst[e] : it.qb_start + e;
     };
     // class of query block qb against the item's key tile (a listed block is
@@ -245,11 +248,11 @@ __global__ void __launch_bounds__(512, 1) fa_bwd64_kernel(const __grid_constant_
                     it.shift = Lk - Lq;
                     it.qb_start = bwd_query_block_begin(kt * kTile, kvis, p.causal, it.shift, BQ, Tqb);
                     it.count = Tqb - it.qb_start;
-                    it.use_list = (!VARLEN && p.block_mask) ? 1 : 0;
+                    it.use_list = (LIST && !VARLEN && p.block_mask) ? 1 : 0;
                     break;
                 }
                 uint16_t *lst = list_of(s);
-                if (it.item >= 0 && it.use_list) {
+                if (LIST && it.item >= 0 && it.use_list) {
                     // the query blocks that see this key tile, in order, compacted by the whole warp
                     const int Tqb = (it.Lq + BQ - 1) / BQ;
                     int n = 0;
@@ -753,14 +756,14 @@ __global__ void __launch_bounds__(512, 1) fa_bwd64_kernel(const __grid_constant_
     if (warp == 1) tmem_dealloc(tmem, S::TMEM_COLS);
 }
 
-template <bool VARLEN>
+template <bool VARLEN, bool LIST>
 cudaError_t launch_bwd64_t(const BwdParams &p, cudaStream_t st) {
     const int smem = Bwd64::SMEM_BYTES;
-    cudaError_t e = cudaFuncSetAttribute(fa_bwd64_kernel<VARLEN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = cudaFuncSetAttribute(fa_bwd64_kernel<VARLEN, LIST>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int64_t items = (int64_t)p.Tk * p.BH;
     const unsigned grid = (unsigned)std::min<int64_t>(items, device_sm_count());
-    fa_bwd64_kernel<VARLEN><<<grid, Bwd64::THREADS, smem, st>>>(p);
+    fa_bwd64_kernel<VARLEN, LIST><<<grid, Bwd64::THREADS, smem, st>>>(p);
     return cudaGetLastError();
 }
 
@@ -768,8 +771,12 @@ cudaError_t launch_bwd64_t(const BwdParams &p, cudaStream_t st) {
 
 int bwd64_smem_bytes() { return Bwd64::SMEM_BYTES; }
 
-cudaError_t launch_bwd64_main(const BwdParams &p, cudaStream_t st) { return launch_bwd64_t<false>(p, st); }
+cudaError_t launch_bwd64_main(const BwdParams &p, cudaStream_t st) {
+    return p.block_mask ? launch_bwd64_t<false, true>(p, st) : launch_bwd64_t<false, false>(p, st);
+}
 
-cudaError_t launch_bwd64_main_varlen(const BwdParams &p, cudaStream_t st) { return launch_bwd64_t<true>(p, st); }
+cudaError_t launch_bwd64_main_varlen(const BwdParams &p, cudaStream_t st) {
+    return launch_bwd64_t<true, false>(p, st);
+}
 
 }  // namespace fa

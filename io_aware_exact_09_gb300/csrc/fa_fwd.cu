@@ -147,8 +147,13 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 // shortest of all (head-major would start the last head's heaviest pair near
 // the end, where it runs alone).  The counter resets itself: the last CTA to finish taking items sets
 // it back to zero, so the next launch on the same workspace starts from 0.
-template <int D, bool VARLEN, int BC, int QPC, bool PLAIN>
+template <int D, bool VARLEN, int BC, int QPC, int MODE>
 __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
+    // MODE 2 (plain): no causal mask, key padding or block mask, N a multiple
+    // of the key tile: every visited tile is full.  MODE 1: no block mask.
+    // MODE 0: a block mask may be given (key-tile lists).  Each kernel
+    // carries only the code its mode needs.
+    constexpr bool PLAIN = MODE == 2, LIST = MODE == 0;
     using S = FwdShape<D, BC>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -202,15 +207,12 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
     const uint32_t tmem = *tmem_slot;
 
     // entry e of an item: its key tile and whether query tile x sees it
-    // PLAIN: no causal mask, key padding or block mask, N a multiple of the
-    // key tile: every visited tile is full, there is no list, and the kernel
-    // carries none of that code
     auto entry_kt = [&](const FwdItem &it, const uint16_t *lst, int e) -> int {
-        if constexpr (PLAIN) return e;
+        if constexpr (!LIST) return e;
         return it.use_list ? (int)(lst[e] & 0x3FFFu) : e;
     };
     auto entry_vis = [&](const FwdItem &it, const uint16_t *lst, int x, int e) -> bool {
-        if (!PLAIN && it.use_list) return (lst[e] >> (14 + x)) & 1u;
+        if (LIST && it.use_list) return (lst[e] >> (14 + x)) & 1u;
         return e < (x ? it.kend[1] : it.kend[0]);
     };
 
@@ -270,14 +272,14 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                         it.kend[x] = fwd_key_tile_end(it.q0[x], it.qn[x], kvis, p.causal, it.shift, BC);
                         it.nq += it.qn[x] > 0 ? 1 : 0;
                     }
-                    it.use_list = (!PLAIN && !VARLEN && p.block_mask) ? 1 : 0;
+                    it.use_list = (LIST && !VARLEN && p.block_mask) ? 1 : 0;
                     it.count = max(it.kend[0], it.kend[1]);
                     // an item with no query row (past a ragged sequence's end) is not published
                     if (it.nq > 0) break;
                     it.item = -1;
                 }
                 uint16_t *lst = list_of(s);
-                if (!PLAIN && it.item >= 0 && it.use_list) {
+                if (LIST && it.item >= 0 && it.use_list) {
                     // the key tiles either query tile sees, in order, compacted by the whole warp
                     const int Tk = p.Tk;
                     int n = 0;
@@ -579,9 +581,9 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
             float m_ref = -INFINITY, l = 0.f;
             int it = 0;                              // this item's tiles
             for (int e = 0; e < count; ++e) {
-                const bool vis = (!PLAIN && use_list) ? ((lst[e] >> (14 + x)) & 1u) : (e < kendx);
+                const bool vis = (LIST && use_list) ? ((lst[e] >> (14 + x)) & 1u) : (e < kendx);
                 if (!vis) continue;
-                const int kt = (!PLAIN && use_list) ? (int)(lst[e] & 0x3FFFu) : e;
+                const int kt = (LIST && use_list) ? (int)(lst[e] & 0x3FFFu) : e;
                 const int k0 = kt * BC;
                 unsigned klass = kTileFull;
                 if constexpr (VARLEN)
@@ -783,30 +785,32 @@ int device_sm_count() {
 
 int fwd_smem_bytes(int d) { return d == 64 ? FwdShape<64>::SMEM_BYTES : FwdShape<128>::SMEM_BYTES; }
 
-template <int D, bool VARLEN, int BC, int QPC, bool PLAIN = false>
+template <int D, bool VARLEN, int BC, int QPC, int MODE = 0>
 static cudaError_t launch_fwd_t(const FwdParams &p, cudaStream_t st) {
     using S = FwdShape<D, BC>;
     const int smem = S::SMEM_BYTES;
-    cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D, VARLEN, BC, QPC, PLAIN>,
+    cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D, VARLEN, BC, QPC, MODE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     // persistent: one CTA per SM (the shared-memory footprint allows one),
     // never more CTAs than work items
     const int64_t items = (int64_t)((p.Tq + QPC - 1) / QPC) * p.BH;
     const unsigned grid = (unsigned)std::min<int64_t>(items, device_sm_count());
-    fa_fwd_kernel<D, VARLEN, BC, QPC, PLAIN><<<grid, S::THREADS, smem, st>>>(p);
+    fa_fwd_kernel<D, VARLEN, BC, QPC, MODE><<<grid, S::THREADS, smem, st>>>(p);
     return cudaGetLastError();
 }
 
 cudaError_t launch_fwd(int d, const FwdParams &p, cudaStream_t st) {
-    const bool plain = !p.causal && !p.key_len && !p.block_mask && p.N % 128 == 0;
+    const int mode = p.block_mask ? 0 : (!p.causal && !p.key_len && p.N % 128 == 0) ? 2 : 1;
     if (d == 64)
-        return plain ? launch_fwd_t<64, false, 128, 2, true>(p, st) : launch_fwd_t<64, false, 128, 2>(p, st);
-    return plain ? launch_fwd_t<128, false, 128, 2, true>(p, st) : launch_fwd_t<128, false, 128, 2>(p, st);
+        return mode == 2 ? launch_fwd_t<64, false, 128, 2, 2>(p, st)
+             : mode == 1 ? launch_fwd_t<64, false, 128, 2, 1>(p, st) : launch_fwd_t<64, false, 128, 2, 0>(p, st);
+    return mode == 2 ? launch_fwd_t<128, false, 128, 2, 2>(p, st)
+         : mode == 1 ? launch_fwd_t<128, false, 128, 2, 1>(p, st) : launch_fwd_t<128, false, 128, 2, 0>(p, st);
 }
 
 cudaError_t launch_fwd_varlen(int d, const FwdParams &p, cudaStream_t st) {
-    return d == 64 ? launch_fwd_t<64, true, 128, 2>(p, st) : launch_fwd_t<128, true, 128, 2>(p, st);
+    return d == 64 ? launch_fwd_t<64, true, 128, 2, 1>(p, st) : launch_fwd_t<128, true, 128, 2, 1>(p, st);
 }
 
 template <int D>
