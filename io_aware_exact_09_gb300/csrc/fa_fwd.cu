@@ -519,6 +519,9 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                                 ++nv[x];
                                 ++nvi[x];
                             }
+                            // K and V of stage st are free once both P.V products (their last
+                            // readers) are done: released before the last S, not after it
+                            if (x == 1) mma_commit_elect(bar(S::B_KVEMPTY + st));
                             if (more && entry_vis(it, lst, x, e + 1)) {
                                 if (!kwaited && !mbar_wait_warp(bar(S::B_KFULL + st2), (uint32_t)((u + 1) / S::STAGES) & 1u,
                                                                 g, 0x205)) {
@@ -538,8 +541,6 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                         if (!ok) break;
                         // the item's last S products were issued just now: Q is free once they finish
                         if (e + 2 == it.count) mma_commit_elect(bar(S::B_QEMPTY));
-                        // K and V of stage st are free once this tile's products are done
-                        mma_commit_elect(bar(S::B_KVEMPTY + st));
                     }
                 }
                 if (!ok) break;

@@ -376,6 +376,10 @@ def fwd_issuer(items, stages, sep=False):
                             vwaited = True
                         yield ("commit", ("PVDONE", x))
                         nv[x] += 1
+                    if x == 1:
+                        # the stage's last readers (both P.V) are issued: release it
+                        # before the second query tile's next S
+                        yield ("commit", ("KVEMPTY", s))
                     if e + 1 < count and vis[x][e + 1]:
                         if not kwaited:
                             kk = (u + 1) // stages
@@ -386,7 +390,6 @@ def fwd_issuer(items, stages, sep=False):
                         ns[x] += 1
                 if e + 2 == count:
                     yield ("commit", "QEMPTY")
-                yield ("commit", ("KVEMPTY", s))
                 u += 1
         yield ("arrive", ("ITEMFREE", k & 1))
 
