@@ -80,8 +80,11 @@ struct FwdShape {
     static constexpr int B_QEMPTY = 1;                   // an item's S products are done: Q free
     static constexpr int B_KFULL = 2;
     static constexpr int B_VFULL = B_KFULL + STAGES;
-    static constexpr int B_KVEMPTY = B_VFULL + STAGES;
-    static constexpr int B_SFULL = B_KVEMPTY + STAGES;   // [2] one per query tile
+    // a stage's K is free once the S products of its key tile are done, its V
+    // once the P.V products are: released apart, the next K loads a step sooner
+    static constexpr int B_KEMPTY = B_VFULL + STAGES;
+    static constexpr int B_VEMPTY = B_KEMPTY + STAGES;
+    static constexpr int B_SFULL = B_VEMPTY + STAGES;    // [2] one per query tile
     static constexpr int B_PFULL = B_SFULL + 2;          // [2]
     static constexpr int B_PVDONE = B_PFULL + 2;         // [2]
     static constexpr int B_SFREE = B_PVDONE + 2;         // [2] S_x loaded by its softmax (separate P only)
@@ -180,7 +183,8 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
         for (int s = 0; s < S::STAGES; ++s) {
             mbar_init(bar(S::B_KFULL + s), 1);
             mbar_init(bar(S::B_VFULL + s), 1);
-            mbar_init(bar(S::B_KVEMPTY + s), 1);
+            mbar_init(bar(S::B_KEMPTY + s), 1);
+            mbar_init(bar(S::B_VEMPTY + s), 1);
         }
         for (int j = 0; j < 2; ++j) {
             mbar_init(bar(S::B_SFULL + j), 1);
@@ -232,6 +236,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
             // item's Q tiles once the previous item's S products are done with
             // the Q buffer, and streams K and V through the ring.
             int k = 0, m = 0, u = 0;                 // items published, items with Q loaded, ring uses
+            int k_only = -1;                         // a use whose K was loaded but not its V (on giving up)
             bool ok = true;
             for (;; ++k) {
                 const int s = k & 1;
@@ -325,7 +330,9 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                     const int kt = entry_kt(it, lst, e);
                     const int st = u % S::STAGES;
                     const uint32_t ph = (uint32_t)(u / S::STAGES) & 1u;
-                    if (!mbar_wait_warp(bar(S::B_KVEMPTY + st), ph ^ 1u, g, 0x102)) {
+                    // K of stage st once the S products of its previous key tile
+                    // are done, V once that tile's P.V products are
+                    if (!mbar_wait_warp(bar(S::B_KEMPTY + st), ph ^ 1u, g, 0x102)) {
                         ok = false;
                         break;
                     }
@@ -339,6 +346,11 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                         else
                             tma_load_3d_elect(koff + c * S::KV_CHUNK_BYTES, &p.tmK, bar(S::B_KFULL + st), c * 64,
                                               kt * BC, it.bh);
+                    }
+                    if (!mbar_wait_warp(bar(S::B_VEMPTY + st), ph ^ 1u, g, 0x103)) {
+                        k_only = u;                 // this use's K load is on its way, its V not
+                        ok = false;
+                        break;
                     }
                     mbar_arrive_expect_tx_elect(bar(S::B_VFULL + st), S::KV_TILE_BYTES);
                     for (int c = 0; c < S::CHUNKS; ++c) {
@@ -370,6 +382,8 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                     drain_wait(bar(S::B_KFULL + st), ph);
                     drain_wait(bar(S::B_VFULL + st), ph);
                 }
+                if (k_only >= 0)
+                    drain_wait(bar(S::B_KFULL + k_only % S::STAGES), (uint32_t)(k_only / S::STAGES) & 1u);
             }
         } else if (warp == 1) {
             // ---------------------------------------------------------- MMA issuer (whole warp)
@@ -438,6 +452,8 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                                 issue_s(x, u % S::STAGES);
                                 ++ns[x];
                             }
+                        // the first key tile's S products are issued: its K is free once they finish
+                        if (ok) mma_commit_elect(bar(S::B_KEMPTY + u % S::STAGES));
                         // the item's S products are all issued: Q is free once they finish
                         if (ok && it.count == 1) mma_commit_elect(bar(S::B_QEMPTY));
                     }
@@ -465,6 +481,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                                     ++ns[x];
                                 }
                             if (!ok) break;
+                            if (more) mma_commit_elect(bar(S::B_KEMPTY + st2));
                             if (e + 2 == it.count) mma_commit_elect(bar(S::B_QEMPTY));
 #pragma unroll
                             for (int x = 0; x < 2 && ok; ++x)
@@ -489,7 +506,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                                     ++nvi[x];
                                 }
                             if (!ok) break;
-                            mma_commit_elect(bar(S::B_KVEMPTY + st));
+                            mma_commit_elect(bar(S::B_VEMPTY + st));
                             continue;
                         }
                         // per query tile: O_x += P_x V, then at once the next key
@@ -519,9 +536,9 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                                 ++nv[x];
                                 ++nvi[x];
                             }
-                            // K and V of stage st are free once both P.V products (their last
-                            // readers) are done: released before the last S, not after it
-                            if (x == 1) mma_commit_elect(bar(S::B_KVEMPTY + st));
+                            // V of stage st is free once both P.V products (its last readers)
+                            // are done: released before the second query tile's next S
+                            if (x == 1) mma_commit_elect(bar(S::B_VEMPTY + st));
                             if (more && entry_vis(it, lst, x, e + 1)) {
                                 if (!kwaited && !mbar_wait_warp(bar(S::B_KFULL + st2), (uint32_t)((u + 1) / S::STAGES) & 1u,
                                                                 g, 0x205)) {
@@ -539,6 +556,8 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                             }
                         }
                         if (!ok) break;
+                        // the next key tile's S products are issued: its K is free once they finish
+                        if (more) mma_commit_elect(bar(S::B_KEMPTY + st2));
                         // the item's last S products were issued just now: Q is free once they finish
                         if (e + 2 == it.count) mma_commit_elect(bar(S::B_QEMPTY));
                     }

@@ -304,8 +304,11 @@ def fwd_producer(items, stages, q_empty_wait=True, slot_free_wait=True):
         m += 1
         for _ in range(count):
             s, kk = u % stages, u // stages
-            yield ("wait", ("KVEMPTY", s), (kk & 1) ^ 1, kk - 1)
+            # K once the stage's previous key tile's S products are done, V once
+            # its P.V products are
+            yield ("wait", ("KEMPTY", s), (kk & 1) ^ 1, kk - 1)
             yield ("tma", ("KFULL", s))
+            yield ("wait", ("VEMPTY", s), (kk & 1) ^ 1, kk - 1)
             yield ("tma", ("VFULL", s))
             u += 1
 
@@ -340,6 +343,7 @@ def fwd_issuer(items, stages, sep=False):
                     yield from s_ready(x)
                     yield ("commit", ("SFULL", x))
                     ns[x] += 1
+            yield ("commit", ("KEMPTY", u % stages))
             if count == 1:
                 yield ("commit", "QEMPTY")
             for e in range(count):
@@ -355,6 +359,8 @@ def fwd_issuer(items, stages, sep=False):
                             yield from s_ready(x)
                             yield ("commit", ("SFULL", x))
                             ns[x] += 1
+                    if e + 1 < count:
+                        yield ("commit", ("KEMPTY", s2))
                     if e + 2 == count:
                         yield ("commit", "QEMPTY")
                     for x in range(2):
@@ -365,7 +371,7 @@ def fwd_issuer(items, stages, sep=False):
                                 vwaited = True
                             yield ("commit", ("PVDONE", x))
                             nv[x] += 1
-                    yield ("commit", ("KVEMPTY", s))
+                    yield ("commit", ("VEMPTY", s))
                     u += 1
                     continue
                 for x in range(2):
@@ -377,9 +383,9 @@ def fwd_issuer(items, stages, sep=False):
                         yield ("commit", ("PVDONE", x))
                         nv[x] += 1
                     if x == 1:
-                        # the stage's last readers (both P.V) are issued: release it
-                        # before the second query tile's next S
-                        yield ("commit", ("KVEMPTY", s))
+                        # V's last readers (both P.V) are issued: release it before the
+                        # second query tile's next S
+                        yield ("commit", ("VEMPTY", s))
                     if e + 1 < count and vis[x][e + 1]:
                         if not kwaited:
                             kk = (u + 1) // stages
@@ -388,6 +394,8 @@ def fwd_issuer(items, stages, sep=False):
                         yield from s_ready(x)
                         yield ("commit", ("SFULL", x))
                         ns[x] += 1
+                if e + 1 < count:
+                    yield ("commit", ("KEMPTY", s2))
                 if e + 2 == count:
                     yield ("commit", "QEMPTY")
                 u += 1
@@ -756,6 +764,7 @@ def test_forward_model_finds_s_issued_before_p_is_awaited():
             if n_tiles[x] > 0:
                 yield ("commit", ("SFULL", x))
                 ns[x] += 1
+        yield ("commit", ("KEMPTY", 0))
         for u in range(total):
             s, s2 = u % stages, (u + 1) % stages
             for x in range(2):
@@ -765,13 +774,15 @@ def test_forward_model_finds_s_issued_before_p_is_awaited():
                     yield ("wait", ("SFREE", x), (ns[x] - 1) & 1, ns[x] - 1)
                     yield ("commit", ("SFULL", x))
                     ns[x] += 1
+            if u + 1 < total:
+                yield ("commit", ("KEMPTY", s2))
             for x in range(2):
                 if u < n_tiles[x]:
                     yield ("wait", ("PFULL", x), nv[x] & 1, nv[x])
                     yield ("wait", ("VFULL", s), (u // stages) & 1, u // stages)
                     yield ("commit", ("PVDONE", x))
                     nv[x] += 1
-            yield ("commit", ("KVEMPTY", s))
+            yield ("commit", ("VEMPTY", s))
 
     def softmax_releasing_s(x, n):
         for it in range(n):
