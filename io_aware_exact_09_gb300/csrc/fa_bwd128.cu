@@ -255,24 +255,32 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
                     tload(base + S::OFF_V + c * S::CHUNK, &p.tmV, bar(S::B_KV), c, k0, k_start);
                 }
             }
-            int i = 0, nl = 0;          // blocks seen, blocks whose Q / dO loads were issued
+            int i = 0, nq = 0, nl = 0;  // blocks seen, blocks whose Q / dO loads were issued
             bool ok = true;
             for (int qb = first; qb < Tqb; qb = next_qb(qb), ++i) {
                 const int s = i & 1;
-                // Q(i) into stage s once dK(i - 2) has read it; dO(i) once dV(i - 1) has
-                if (!mbar_wait_warp(bar(S::B_QEMPTY + s), ((uint32_t)(i >> 1) & 1u) ^ 1u, g, 0x121) ||
-                    !mbar_wait_warp(bar(S::B_DVDONE), ((uint32_t)i & 1u) ^ 1u, g, 0x122)) {
+                // Q(i) into stage s once dK(i - 2) has read it, then dO(i) once dV(i - 1)
+                // has read the single dO buffer: each load waits for its own buffer only
+                // (Q used to wait for dV(i - 1) too, a block later than its stage was free)
+                if (!mbar_wait_warp(bar(S::B_QEMPTY + s), ((uint32_t)(i >> 1) & 1u) ^ 1u, g, 0x121)) {
                     ok = false;
                     break;
                 }
                 if (lane == 0) {
                     mbar_arrive_expect_tx(bar(S::B_QFULL + s), S::TILE);
-                    mbar_arrive_expect_tx(bar(S::B_DOFULL), S::TILE);
-                    for (int c = 0; c < 2; ++c) {
+                    for (int c = 0; c < 2; ++c)
                         tload(base + S::OFF_Q + s * S::TILE + c * S::CHUNK, &p.tmQ, bar(S::B_QFULL + s), c, qb * BQ,
                               q_start);
+                }
+                nq = i + 1;
+                if (!mbar_wait_warp(bar(S::B_DVDONE), ((uint32_t)i & 1u) ^ 1u, g, 0x122)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(bar(S::B_DOFULL), S::TILE);
+                    for (int c = 0; c < 2; ++c)
                         tload(base + S::OFF_DO + c * S::CHUNK, &p.tmdO, bar(S::B_DOFULL), c, qb * BQ, q_start);
-                    }
                 }
                 nl = i + 1;
                 if (!stager) {
@@ -292,7 +300,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
             if (!ok && lane == 0) {
                 // gave up: let every copy already issued land before the CTA exits
                 b128_drain_wait(bar(S::B_KV), 0);
-                for (int j = (nl > 2 ? nl - 2 : 0); j < nl; ++j)
+                for (int j = (nq > 2 ? nq - 2 : 0); j < nq; ++j)
                     b128_drain_wait(bar(S::B_QFULL + (j & 1)), (uint32_t)(j >> 1) & 1u);
                 if (nl > 0) b128_drain_wait(bar(S::B_DOFULL), (uint32_t)(nl - 1) & 1u);
             }

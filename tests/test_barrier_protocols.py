@@ -197,8 +197,8 @@ def bwd_producer(n, stages_lse=False):
     for i in range(n):
         s = i & 1
         yield ("wait", ("QEMPTY", s), ((i >> 1) & 1) ^ 1, (i >> 1) - 1)     # dK(i-2) read Q stage s
-        yield ("wait", "DVDONE", (i & 1) ^ 1, i - 1)                        # dV(i-1) read dO
         yield ("tma", ("QFULL", s))
+        yield ("wait", "DVDONE", (i & 1) ^ 1, i - 1)                        # dV(i-1) read dO
         yield ("tma", "DOFULL")
         if stages_lse:
             yield ("wait", "DFREE", (i & 1) ^ 1, i - 1)
