@@ -661,18 +661,28 @@ __global__ void __launch_bounds__(512, 1) fa_bwd64_kernel(const __grid_constant_
                         make_uint4(wv[4 * t], wv[4 * t + 1], wv[4 * t + 2], wv[4 * t + 3]);
                 }
                 __syncwarp();
+                // all eight values first, then the stores: interleaved, each shared
+                // load waited behind the previous global store (the compiler cannot
+                // tell the two apart)
                 const int u = lane & 3;
+                uint4 kq[4], vq[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const int rr = 8 * j + (lane >> 2);          // row of this warp's 32
-                    const uint4 kq = *reinterpret_cast<const uint4 *>(stg + rr * 128 + ((u ^ (rr & 7)) << 4));
-                    const uint4 vq = *reinterpret_cast<const uint4 *>(stg + rr * 128 + (((4 + u) ^ (rr & 7)) << 4));
+                    kq[j] = *reinterpret_cast<const uint4 *>(stg + rr * 128 + ((u ^ (rr & 7)) << 4));
+                    vq[j] = *reinterpret_cast<const uint4 *>(stg + rr * 128 + (((4 + u) ^ (rr & 7)) << 4));
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int rr = 8 * j + (lane >> 2);
                     const int keyr = it.kt * kTile + wq * 32 + rr;
                     if (keyr < it.Lk) {
                         const size_t krow =
                             VARLEN ? (size_t)(it.k_start + keyr) * p.H + it.h : (size_t)it.bh * p.N + keyr;
-                        *reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.dK) + krow * D + 32 * wg + 8 * u) = kq;
-                        *reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.dV) + krow * D + 32 * wg + 8 * u) = vq;
+                        *reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.dK) + krow * D + 32 * wg + 8 * u) =
+                            kq[j];
+                        *reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.dV) + krow * D + 32 * wg + 8 * u) =
+                            vq[j];
                     }
                 }
                 __syncwarp();
