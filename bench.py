@@ -729,7 +729,7 @@ def run_varlen(args, w):
             ev[0].record(stream)
         check(fa.fa_fwd_varlen(Q, K, V, O, LSE, cu_q, cu_k, B, H, tq, tk, c["max_q"], d, w.softmax_scale, w.causal,
                                ws, wsn, sp), "fa_fwd_varlen")
-        if record:
+        if record is True:
             ev[1].record(stream)
         check(fa.fa_bwd_varlen(Q, K, V, O, LSE, dO, dQ, dK, dV, cu_q, cu_k, B, H, tq, tk, max_k, d, w.softmax_scale,
                                w.causal, wsb, wsbn, sp), "fa_bwd_varlen")
@@ -754,6 +754,12 @@ def run_varlen(args, w):
         ev[2].synchronize()
         tf_.append(ev[0].elapsed_time(ev[1]))
         tb_.append(ev[1].elapsed_time(ev[2]))
+    # the whole step with events at its ends only (an event between the calls
+    # would keep the backward's first kernel from overlapping the forward's tail)
+    for _ in range(args.steps):
+        flush.zero_()
+        step("ends")
+        ev[2].synchronize()
         tstep.append(ev[0].elapsed_time(ev[2]))
     torch.cuda.synchronize(dev)
     barrier()
@@ -951,20 +957,21 @@ class SquareStep:
             raise RuntimeError("%s failed: %s" % (where, self.fa.fa_status_string(st)))
 
     def run(self, record):
+        """One step; record: False, "ends" (events 0 and 4 only) or True (an event between calls)."""
         fa, w, s, ev = self.fa, self.w, self.stream.cuda_stream, self.ev
         B, H, N, d = w.B, w.H, w.N, w.d
         if record:
             ev[0].record(self.stream)
         self._check(fa.fa_fwd(self.Q, self.K, self.V, self.O, self.LSE, B, H, N, d, w.softmax_scale, w.causal,
                               self.kl, self.bm, self.ws_f, self.wsf, s), "fa_fwd")
-        if record:
+        if record is True:
             ev[1].record(self.stream)
         self._check(fa.fa_bwd_preprocess(self.O, self.dO, B, H, N, d, self.ws_b, self.wsb, s), "fa_bwd_preprocess")
-        if record:
+        if record is True:
             ev[2].record(self.stream)
         self._check(fa.fa_bwd_main(self.Q, self.K, self.V, self.LSE, self.dO, self.dK, self.dV, B, H, N, d,
                                    w.softmax_scale, w.causal, self.kl, self.bm, self.ws_b, self.wsb, s), "fa_bwd_main")
-        if record:
+        if record is True:
             ev[3].record(self.stream)
         self._check(fa.fa_bwd_postprocess(self.dQ, B, H, N, d, w.softmax_scale, self.ws_b, self.wsb, s),
                     "fa_bwd_postprocess")
@@ -976,8 +983,9 @@ class SquareStep:
             self._check(self.fa.fa_get_device_status(wsx, self.stream.cuda_stream), where)
 
     def time(self, steps, warmup, flush, on_start=None):
-        """Mean ms per stage over `steps` timed steps (L2 flushed before each,
-        outside the events).  on_start runs after the warm-up, before timing."""
+        """Mean ms per stage over `steps` timed steps, then of the whole step
+        over `steps` more (L2 flushed before each, outside the events).
+        on_start runs after the warm-up, before timing."""
         import torch
         for _ in range(warmup):
             self.run(False)
@@ -985,7 +993,7 @@ class SquareStep:
         self.status("device status after warm-up")
         if on_start is not None:
             on_start()
-        times = {"step": [], "fwd": [], "pre": [], "main": [], "post": []}
+        times = {"step": [], "step_staged": [], "fwd": [], "pre": [], "main": [], "post": []}
         barrier()
         torch.cuda.synchronize()
         for _ in range(steps):
@@ -997,7 +1005,15 @@ class SquareStep:
             times["pre"].append(ev[1].elapsed_time(ev[2]))
             times["main"].append(ev[2].elapsed_time(ev[3]))
             times["post"].append(ev[3].elapsed_time(ev[4]))
-            times["step"].append(ev[0].elapsed_time(ev[4]))
+            times["step_staged"].append(ev[0].elapsed_time(ev[4]))
+        # the step itself, timed with events at its ends only: an event between
+        # two calls would separate kernels that otherwise overlap (each is
+        # launched to be scheduled while the one before it drains)
+        for _ in range(steps):
+            flush.zero_()
+            self.run("ends")
+            self.ev[4].synchronize()
+            times["step"].append(self.ev[0].elapsed_time(self.ev[4]))
         torch.cuda.synchronize()
         barrier()
         return {k: sum(v) / len(v) for k, v in times.items()}

@@ -36,6 +36,8 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __nv_bfloat16 *__
                                                          const __nv_bfloat16 *__restrict__ dO,
                                                          float *__restrict__ Dvec, float *__restrict__ dQacc,
                                                          int64_t rows) {
+    grid_dep_wait();                                 // the previous kernel in the stream is done
+    grid_dep_launch();
     constexpr int TPR = D / 8;                 // threads per row
     constexpr int RPB = 256 / TPR;             // rows per block and pass
     constexpr int U = 4;                       // passes in flight per thread
@@ -76,6 +78,8 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __nv_bfloat16 *__
 __global__ void __launch_bounds__(256) fa_bwd_convert_kernel(const float *__restrict__ acc,
                                                              __nv_bfloat16 *__restrict__ dQ, int64_t n8,
                                                              float scale) {
+    grid_dep_wait();                                 // the previous kernel in the stream is done
+    grid_dep_launch();
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
          i += (int64_t)gridDim.x * blockDim.x) {
         const float4 a = reinterpret_cast<const float4 *>(acc)[2 * i];
@@ -137,12 +141,11 @@ cudaError_t launch_bwd_pre(int d, const void *O, const void *dO, float *Dvec, fl
     const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>((rows + per_block - 1) / per_block,
                                                                            (int64_t)device_sm_count() * 16));
     if (d == 64)
-        fa_bwd_pre_kernel<64><<<grid, 256, 0, st>>>((const __nv_bfloat16 *)O, (const __nv_bfloat16 *)dO, Dvec,
-                                                    dQacc, rows);
+        return launch_dep(fa_bwd_pre_kernel<64>, grid, 256, 0, st, (const __nv_bfloat16 *)O,
+                          (const __nv_bfloat16 *)dO, Dvec, dQacc, rows);
     else
-        fa_bwd_pre_kernel<128><<<grid, 256, 0, st>>>((const __nv_bfloat16 *)O, (const __nv_bfloat16 *)dO, Dvec,
-                                                     dQacc, rows);
-    return cudaGetLastError();
+        return launch_dep(fa_bwd_pre_kernel<128>, grid, 256, 0, st, (const __nv_bfloat16 *)O,
+                          (const __nv_bfloat16 *)dO, Dvec, dQacc, rows);
 }
 
 cudaError_t launch_bwd_convert(int d, const float *dQacc, void *dQ, int64_t elems, float scale,
@@ -152,8 +155,7 @@ cudaError_t launch_bwd_convert(int d, const float *dQacc, void *dQ, int64_t elem
     int64_t blocks = (n8 + 255) / 256;
     if (blocks > 152 * 16) blocks = 152 * 16;
     if (blocks < 1) blocks = 1;
-    fa_bwd_convert_kernel<<<(unsigned)blocks, 256, 0, st>>>(dQacc, (__nv_bfloat16 *)dQ, n8, scale);
-    return cudaGetLastError();
+    return launch_dep(fa_bwd_convert_kernel, (unsigned)blocks, 256, 0, st, dQacc, (__nv_bfloat16 *)dQ, n8, scale);
 }
 
 cudaError_t launch_plan(int B, int N, int causal, const int32_t *key_len, const uint8_t *block_mask,

@@ -103,6 +103,8 @@ __device__ __forceinline__ uint32_t packed_col128(int k) { return (uint32_t)((k 
 
 template <bool VARLEN, bool STAGER, bool PLAIN>
 __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant__ BwdParams p) {
+    grid_dep_wait();                                 // the previous kernel in the stream is done
+    grid_dep_launch();
     using S = Bwd128;
     constexpr int BQ = S::BQ, CW = S::CW;
     extern __shared__ uint8_t smem_raw[];
@@ -698,8 +700,8 @@ static cudaError_t launch_bwd128_t(const BwdParams &p, cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(fa_bwd128_kernel<VARLEN, STAGER, PLAIN>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    fa_bwd128_kernel<VARLEN, STAGER, PLAIN><<<(unsigned)p.Tk * (unsigned)p.BH, Bwd128::THREADS, smem, st>>>(p);
-    return cudaGetLastError();
+    return launch_dep(fa_bwd128_kernel<VARLEN, STAGER, PLAIN>, (unsigned)p.Tk * (unsigned)p.BH, Bwd128::THREADS,
+                      smem, st, p);
 }
 
 cudaError_t launch_bwd128_main(const BwdParams &p, cudaStream_t st) {

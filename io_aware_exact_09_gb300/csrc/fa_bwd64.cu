@@ -124,6 +124,8 @@ __device__ __forceinline__ uint32_t packed_col64(int k) { return (uint32_t)((k >
 
 template <bool VARLEN, bool LIST>
 __global__ void __launch_bounds__(512, 1) fa_bwd64_kernel(const __grid_constant__ BwdParams p) {
+    grid_dep_wait();                                 // the previous kernel in the stream is done
+    grid_dep_launch();
     using S = Bwd64;
     constexpr int BQ = S::BQ, CW = S::CW, D = S::D;
     extern __shared__ uint8_t smem_raw[];
@@ -773,8 +775,7 @@ cudaError_t launch_bwd64_t(const BwdParams &p, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     const int64_t items = (int64_t)p.Tk * p.BH;
     const unsigned grid = (unsigned)std::min<int64_t>(items, device_sm_count());
-    fa_bwd64_kernel<VARLEN, LIST><<<grid, Bwd64::THREADS, smem, st>>>(p);
-    return cudaGetLastError();
+    return launch_dep(fa_bwd64_kernel<VARLEN, LIST>, grid, Bwd64::THREADS, smem, st, p);
 }
 
 }  // namespace

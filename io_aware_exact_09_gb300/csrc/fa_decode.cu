@@ -70,6 +70,8 @@ __device__ __forceinline__ void dec_drain_wait(uint32_t bar, uint32_t parity) {
 
 template <int D>
 __global__ void __launch_bounds__(256, 1) fa_decode_kernel(const __grid_constant__ DecParams p) {
+    grid_dep_wait();                                 // the previous kernel in the stream is done
+    grid_dep_launch();
     using S = DecShape<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -388,6 +390,8 @@ __global__ void __launch_bounds__(256) fa_decode_merge_kernel(const float *__res
                                                               const float *__restrict__ Lpart,
                                                               __nv_bfloat16 *__restrict__ O, float *__restrict__ LSE,
                                                               int64_t rows, int splits) {
+    grid_dep_wait();                                 // the previous kernel in the stream is done
+    grid_dep_launch();
     const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
@@ -435,8 +439,7 @@ static cudaError_t launch_decode_t(const DecParams &p, cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(fa_decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)p.Tq * (unsigned)p.BH * (unsigned)p.splits;
-    fa_decode_kernel<D><<<grid, 256, smem, st>>>(p);
-    return cudaGetLastError();
+    return launch_dep(fa_decode_kernel<D>, grid, 256, smem, st, p);
 }
 
 cudaError_t launch_decode(int d, const DecParams &p, cudaStream_t st) {
@@ -447,10 +450,11 @@ cudaError_t launch_decode_merge(int d, const float *Opart, const float *Lpart, v
                                 int splits, cudaStream_t st) {
     const unsigned grid = (unsigned)((rows + 7) / 8);
     if (d == 64)
-        fa_decode_merge_kernel<64><<<grid, 256, 0, st>>>(Opart, Lpart, (__nv_bfloat16 *)O, LSE, rows, splits);
+        return launch_dep(fa_decode_merge_kernel<64>, grid, 256, 0, st, Opart, Lpart, (__nv_bfloat16 *)O, LSE, rows,
+                          splits);
     else
-        fa_decode_merge_kernel<128><<<grid, 256, 0, st>>>(Opart, Lpart, (__nv_bfloat16 *)O, LSE, rows, splits);
-    return cudaGetLastError();
+        return launch_dep(fa_decode_merge_kernel<128>, grid, 256, 0, st, Opart, Lpart, (__nv_bfloat16 *)O, LSE, rows,
+                          splits);
 }
 
 }  // namespace fa

@@ -152,6 +152,8 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 // it back to zero, so the next launch on the same workspace starts from 0.
 template <int D, bool VARLEN, int BC, int QPC, int MODE>
 __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
+    grid_dep_wait();                                 // the previous kernel in the stream is done
+    grid_dep_launch();
     // MODE 2 (plain): no causal mask, key padding or block mask, N a multiple
     // of the key tile: every visited tile is full.  MODE 1: no block mask.
     // MODE 0: a block mask may be given (key-tile lists).  Each kernel
@@ -816,8 +818,7 @@ static cudaError_t launch_fwd_t(const FwdParams &p, cudaStream_t st) {
     // never more CTAs than work items
     const int64_t items = (int64_t)((p.Tq + QPC - 1) / QPC) * p.BH;
     const unsigned grid = (unsigned)std::min<int64_t>(items, device_sm_count());
-    fa_fwd_kernel<D, VARLEN, BC, QPC, MODE><<<grid, S::THREADS, smem, st>>>(p);
-    return cudaGetLastError();
+    return launch_dep(fa_fwd_kernel<D, VARLEN, BC, QPC, MODE>, grid, S::THREADS, smem, st, p);
 }
 
 cudaError_t launch_fwd(int d, const FwdParams &p, cudaStream_t st) {

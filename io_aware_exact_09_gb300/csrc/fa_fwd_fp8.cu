@@ -86,6 +86,8 @@ __device__ __forceinline__ void f8_drain_wait(uint32_t bar, uint32_t parity) {
 
 template <bool PLAIN>
 __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constant__ FwdParams p) {
+    grid_dep_wait();                                 // the previous kernel in the stream is done
+    grid_dep_launch();
     using S = F8Shape;
     constexpr int D = S::D;
     extern __shared__ uint8_t smem_raw[];
@@ -524,10 +526,9 @@ cudaError_t launch_fwd_fp8(const FwdParams &p, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)((p.Tq + 1) / 2) * (unsigned)p.BH;
     if (plain)
-        fa_fwd_fp8_kernel<true><<<grid, F8Shape::THREADS, smem, st>>>(p);
+        return launch_dep(fa_fwd_fp8_kernel<true>, grid, F8Shape::THREADS, smem, st, p);
     else
-        fa_fwd_fp8_kernel<false><<<grid, F8Shape::THREADS, smem, st>>>(p);
-    return cudaGetLastError();
+        return launch_dep(fa_fwd_fp8_kernel<false>, grid, F8Shape::THREADS, smem, st, p);
 }
 
 }  // namespace fa

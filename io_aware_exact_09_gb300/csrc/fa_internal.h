@@ -12,6 +12,26 @@ namespace fa {
 // Multiprocessor count of the current device (cached per device).
 int device_sm_count();
 
+// Launch with programmatic stream serialisation: the kernel may be scheduled
+// while the previous kernel in the stream drains, and waits for it on the
+// device (grid_dep_wait() in fa_ptx.cuh, the first statement of every kernel
+// launched this way).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dep(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                              cudaStream_t st, const Args &...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // Forward: a persistent grid of at most one CTA per SM over (query-tile pair,
 // b*h) work items; the workspace's words 2 and 3 hold its item counter.
 cudaError_t launch_fwd(int d, const FwdParams &p, cudaStream_t st);

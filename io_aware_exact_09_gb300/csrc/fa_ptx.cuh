@@ -30,6 +30,20 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     return t;
 }
 
+// ------------------------------------------------------------------ programmatic dependent launch
+// The library launches its kernels with programmatic stream serialisation, so
+// a kernel's CTAs may be scheduled while the previous kernel in the stream is
+// still draining.  Every kernel calls grid_dep_wait() in every thread as its
+// first statement: it returns once the previous kernel has completed and its
+// memory operations are visible (at once outside such a launch).  Since no
+// grid completes before its own wait returned, all earlier work in the stream
+// is complete then too; and a waiting CTA holds no TMEM and touches no global
+// memory.  grid_dep_launch() then lets the next kernel's CTAs be scheduled as
+// this grid's CTAs exit (they need every CTA of this grid to have called it
+// or exited, so this grid never waits for room the next one holds).
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");

@@ -53,6 +53,8 @@ __global__ void __launch_bounds__(256) fa_quant_fp8_kernel(const __nv_bfloat16 *
                                                            uint8_t *__restrict__ Y, float *__restrict__ scales,
                                                            const int8_t *__restrict__ signs, int N, int T, int Np,
                                                            int nblk) {
+    grid_dep_wait();                                 // the previous kernel in the stream is done
+    grid_dep_launch();
     static_assert(!(ROTATE && TRANSPOSE), "the rotation is for Q and K (row layout)");
     using Q = QuantShape<D>;
     constexpr int VPR = Q::VPR, NV = Q::NV;
@@ -202,8 +204,7 @@ cudaError_t launch_quant_t(const __nv_bfloat16 *x, uint8_t *y, float *scales, co
         (e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, smem)) != cudaSuccess)
         return e;
     const int grid = std::max(1, std::min(nblk, sms * std::max(per_sm, 1)));
-    kern<<<grid, 256, smem, st>>>(x, y, scales, signs, N, T, Np, nblk);
-    return cudaGetLastError();
+    return launch_dep(kern, grid, 256, smem, st, x, y, scales, signs, N, T, Np, nblk);
 }
 
 }  // namespace
