@@ -48,7 +48,10 @@
  *     is the status word, which the library only ever sets, never clears
  *     (fa_reset_device_status() clears it).  The forward kernels hand out
  *     their work items from a counter in words 2 and 3, which every launch
- *     leaves at zero again.  A workspace therefore serves one call at a
+ *     leaves at zero again; the d = 128 backward keeps the counters of its
+ *     split key tiles (fa_bwd_workspace_size) in words 8..63, also left at
+ *     zero.  After a call that recorded a device-side timeout, zero-fill
+ *     the workspace again before reusing it.  A workspace therefore serves one call at a
  *     time: calls that may run concurrently (different streams) need
  *     workspaces of their own.
  *   - No entry point throws or exits; there is no CPU fallback.
@@ -67,7 +70,7 @@ typedef enum {
     FA_OK = 0,
     FA_ERR_INVALID_ARGUMENT = 1,   /* null/misaligned pointer, negative size, bad scale */
     FA_ERR_UNSUPPORTED = 2,        /* d not in {64, 128}, sizes beyond the 32-bit grid limits */
-    FA_ERR_WORKSPACE = 3,          /* workspace NULL or smaller than the *_workspace_size query */
+    FA_ERR_WORKSPACE = 3,          /* workspace NULL or smaller than the call needs (*_workspace_size) */
     FA_ERR_CUDA = 4,               /* a CUDA runtime call or kernel launch failed */
     FA_ERR_DEVICE_TIMEOUT = 5,     /* a device-side wait gave up (kernel returned early) */
     FA_ERR_DEVICE_BAD_KEY_LEN = 6  /* a key_len value was outside [0, N] and was clamped */
@@ -80,9 +83,16 @@ int fa_tile_size(void);
  * work-item counter of the persistent forward grid. */
 size_t fa_fwd_workspace_size(int B, int H, int N, int d);
 
-/* Bytes of device workspace fa_bwd needs: the status word, the fp32 row
- * dot-products D = rowsum(dO * O) [B, H, N] and the fp32 dQ accumulator
- * [B, H, N, d], each 256-byte aligned. */
+/* Bytes of device workspace fa_bwd uses: the 256-byte status block, the
+ * fp32 row dot-products D = rowsum(dO * O) [B, H, N] and the fp32 dQ
+ * accumulator [B, H, N, d], each 256-byte aligned; for d = 128 and N > 128
+ * then the split area: 128 KiB per CTA of a split key tile, for
+ * min(256, B * H * ceil(N / 128) * min(4, ceil(N / 128))) of them.  With no
+ * mask and N a multiple of 128 every key tile takes the same time; the main
+ * kernel runs one CTA per SM at a time, and the key tiles past its last full
+ * wave run as 2-4 CTAs each over parts of the query range, whose fp32 dK and
+ * dV meet in that area.  The calls accept a workspace without the split area
+ * (status block, D and accumulator only) and then do not split. */
 size_t fa_bwd_workspace_size(int B, int H, int N, int d);
 
 /*
@@ -234,8 +244,9 @@ fa_status fa_fwd_fp8_rotated(const void *Q8, const void *K8, const void *Vt8, co
  * (read); LSE: device fp32 [B, H, N] from fa_fwd with the same arguments
  * (read).  dQ, dK, dV: device bf16 [B, H, N, d] (written).  Three kernel
  * launches: D = rowsum(dO * O) with the dQ accumulator zeroed; the main
- * kernel (one CTA per 128-key tile, recomputing S and P tile by tile); the
- * fp32 -> bf16 conversion of dQ.
+ * kernel (one CTA per 128-key tile, recomputing S and P tile by tile; the
+ * last wave's tiles split over several CTAs, see fa_bwd_workspace_size);
+ * the fp32 -> bf16 conversion of dQ.
  */
 fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, const float *LSE,
                  const void *dO, void *dQ, void *dK, void *dV, int B, int H, int N, int d,
@@ -341,8 +352,9 @@ fa_status fa_attention_host(const void *Q, const void *K, const void *V, const v
  * packaging of fa_bwd, not part of the method.
  *
  * Same arguments, meaning and results as fa_bwd, minus the workspace.  The
- * scratch (status word, D, dQ accumulator) is a 64 MiB array built into the
- * library and held by every GPU that loads it until the process exits.
+ * scratch (status word, D, dQ accumulator, and the d = 128 split area when
+ * it fits) is a 64 MiB array built into the library and held by every GPU
+ * that loads it until the process exits.
  *   - Problems needing more, i.e. B*H*N*(4 + 4*d) + 256 bytes > 64 MiB (for
  *     example B*H*N > 130,000 rows at d = 128), return FA_ERR_WORKSPACE
  *     before anything is enqueued.

@@ -144,6 +144,30 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 }  // namespace
 
+namespace fa {
+size_t bwd_base_workspace_bytes(int B, int H, int N, int d) {
+    if (B < 0 || H < 0 || N < 0 || d <= 0) return 0;
+    const size_t rows = (size_t)B * H * N;
+    return kStatusBytes + round256(rows * 4) + round256(rows * (size_t)d * 4);
+}
+}  // namespace fa
+
+namespace {
+// d = 128: slots for the split of the last wave's items (fa_bwd128.cu), one
+// fp32 [128 keys][dK 128 | dV 128] slot per part; at most four parts per
+// item, one per query block, kSplitMaxParts in all.  Their counters live in
+// the status block, so this area needs no zero fill.
+constexpr size_t kSplitSlotBytes = 128 * 256 * 4;
+size_t bwd_split_parts(int B, int H, int N, int d) {
+    if (d != 128 || B <= 0 || H <= 0 || N <= 128) return 0;
+    const int64_t T = (N + 127) / 128;
+    const int64_t bh = (int64_t)B * H;
+    const int64_t per = T * std::min<int64_t>(4, T);
+    if (bh >= fa::kSplitMaxParts || per >= fa::kSplitMaxParts) return fa::kSplitMaxParts;
+    return (size_t)std::min<int64_t>(fa::kSplitMaxParts, bh * per);
+}
+}  // namespace
+
 extern "C" {
 
 int fa_tile_size(void) { return fa::kTile; }
@@ -154,9 +178,9 @@ size_t fa_fwd_workspace_size(int B, int H, int N, int d) {
 }
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
-    if (B < 0 || H < 0 || N < 0 || d <= 0) return 0;
-    const size_t rows = (size_t)B * H * N;
-    return kStatusBytes + round256(rows * 4) + round256(rows * (size_t)d * 4);
+    const size_t base = fa::bwd_base_workspace_bytes(B, H, N, d);
+    if (base == 0) return 0;
+    return base + bwd_split_parts(B, H, N, d) * kSplitSlotBytes;
 }
 
 const char *fa_status_string(fa_status s) {
@@ -408,7 +432,7 @@ fa_status bwd_common_checks(int B, int H, int N, int d, float scale, void *works
     if (st != FA_OK) return st;
     if (!scale_ok(scale)) return FA_ERR_INVALID_ARGUMENT;
     if (*empty) return FA_OK;
-    if (!workspace || !aligned16(workspace) || workspace_bytes < fa_bwd_workspace_size(B, H, N, d))
+    if (!workspace || !aligned16(workspace) || workspace_bytes < fa::bwd_base_workspace_bytes(B, H, N, d))
         return FA_ERR_WORKSPACE;
     return FA_OK;
 }
@@ -464,6 +488,14 @@ fa_status fa_bwd_main(const void *Q, const void *K, const void *V, const float *
     p.scale_log2 = softmax_scale * kLog2e;
     p.scale = softmax_scale;
     p.spread = spread_items(causal || key_len || block_mask, 12.0 * BH * N * d, BH);
+    // the split area, when the workspace holds it (the launcher decides whether to split)
+    const size_t base = fa::bwd_base_workspace_bytes(B, H, N, d);
+    const size_t parts = bwd_split_parts(B, H, N, d);
+    if (parts >= 2 && workspace_bytes >= base + parts * kSplitSlotBytes) {
+        p.split_cnt = w.status + 8;
+        p.split_buf = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + base);
+        p.split_cap = (int)parts;
+    }
     return fa::launch_bwd_main(d, p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -501,7 +533,7 @@ fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, con
 
 size_t fa_bwd_varlen_workspace_size(int H, int total_q, int d) {
     if (H < 0 || total_q < 0 || d <= 0) return 0;
-    return fa_bwd_workspace_size(1, H, total_q, d);
+    return fa::bwd_base_workspace_bytes(1, H, total_q, d);
 }
 
 fa_status fa_bwd_varlen(const void *Q, const void *K, const void *V, const void *O, const float *LSE, const void *dO,

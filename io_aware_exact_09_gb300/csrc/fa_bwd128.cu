@@ -33,6 +33,7 @@
 // clock64 trace: staging stores queue behind the SS MMAs' operand reads, and
 // the staging area shared with the dS^T tile made them wait for the previous
 // reduce); off their path, the compute chain per block is P -> dS only.
+#include <algorithm>
 #include <climits>
 
 #include "fa_internal.h"
@@ -113,8 +114,24 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
     uint8_t *sb = smem_raw + (base - raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    const int kt = (int)(blockIdx.x % p.Tk);
-    const int bh = (int)(blockIdx.x / p.Tk);
+    // the item (key tile, b*h) of this CTA; from split_from on (every tile
+    // full), part `part` of an item run as split_f CTAs, each over its own
+    // range of query blocks (the last wave's items, so that it fills the SMs)
+    // (split_part: -1 for a whole item, else the part; *sidx: the split item's
+    // index past split_from.  Recomputed where needed rather than kept live.)
+    auto split_part = [&](int *sidx) -> int {
+        const int j = (int)blockIdx.x - p.split_from;
+        if (!PLAIN || p.split_f < 2 || j < 0) return -1;
+        *sidx = j / p.split_f;
+        return j - *sidx * p.split_f;
+    };
+    int item = (int)blockIdx.x;
+    {
+        int si = 0;
+        if (split_part(&si) >= 0) item = p.split_from + si;
+    }
+    const int kt = item % p.Tk;
+    const int bh = item / p.Tk;
     const int b = bh / p.H, h = bh % p.H;
     const int k0 = kt * kTile;
     const int nb = (p.N + kTile - 1) / kTile;
@@ -133,6 +150,15 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
                         &Lk, &bad);
         Tqb = (Lq + BQ - 1) / BQ;
     }
+    int qb_lo = 0;                      // a part's first query block (its range ends at Tqb)
+    if constexpr (PLAIN) {
+        int si = 0;
+        const int part = split_part(&si);
+        if (part >= 0) {
+            qb_lo = part * Tqb / p.split_f;
+            Tqb = (part + 1) * Tqb / p.split_f;
+        }
+    }
     const int shift = Lk - Lq;
     const int kvis = VARLEN ? Lk : key_visible_bound(p.key_len, b, p.N, &bad);
     if (bad && threadIdx.x == 0 && kt == 0 && h == 0) record_status(g, kStatusBadKeyLen, 0);
@@ -147,7 +173,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
         const int on = p.block_mask ? (p.block_mask[(size_t)qb * nb + kt] != 0) : 1;
         return tile_class(qa, min(BQ, p.N - qa), k0, kTile, kvis, p.causal, on);
     };
-    const int qb_start = bwd_query_block_begin(k0, kvis, p.causal, shift, BQ, Tqb);
+    const int qb_start = PLAIN ? qb_lo : bwd_query_block_begin(k0, kvis, p.causal, shift, BQ, Tqb);
     auto next_qb = [&](int qb) -> int {
         if (PLAIN || VARLEN || !p.block_mask) {
             const int nq = qb < qb_start ? qb_start : qb + 1;
@@ -591,37 +617,128 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
             }
         }
         } else {
-            if (ok) {
+            // An item split over several CTAs: each part stores its fp32 dK
+            // (unscaled) and dV in its own slot, then counts itself; the part
+            // that counts last sums the slots in part order (its own from
+            // TMEM), so the result does not depend on which part that is, and
+            // writes dK, dV.  Slot layout: float4 (c, key row) at c * 128 + row,
+            // c = 8 j + t for dK columns 32 j + 4 t .. + 3, 32 + 8 j + t for dV,
+            // so that a warp's store covers 512 contiguous bytes.  The stores
+            // are published by one thread (CTA barrier, release fence, count)
+            // and the counter read the same way (count, acquire fence, barrier);
+            // all 256 compute threads take both barriers on every path.
+            bool write = ok;
+            const float4 *slots = nullptr;           // part 0's slot of this item
+            int sidx = 0;
+            const int part = split_part(&sidx);
+            if constexpr (PLAIN) {
+                if (part >= 0) {
+                    slots = reinterpret_cast<const float4 *>(p.split_buf) + (size_t)sidx * p.split_f * 8192;
+                    if (ok) {
+                        float4 *mine = const_cast<float4 *>(slots) + (size_t)part * 8192 + r;
+    #pragma unroll 1
+                        for (int j = wg * 2; j < wg * 2 + 2; ++j) {
+                            uint32_t a[32], vv[32];
+                            tmem_ld32(tmem + lane_off + S::TM_DK + 32u * j, a);
+                            tmem_ld32(tmem + lane_off + S::TM_DV + 32u * j, vv);
+                            tmem_ld_wait(a);
+                            tmem_ld_wait(vv);
+    #pragma unroll
+                            for (int t = 0; t < 8; ++t) {
+                                mine[(8 * j + t) * 128] = make_float4(__uint_as_float(a[4 * t]), __uint_as_float(a[4 * t + 1]),
+                                                                      __uint_as_float(a[4 * t + 2]), __uint_as_float(a[4 * t + 3]));
+                                mine[(32 + 8 * j + t) * 128] =
+                                    make_float4(__uint_as_float(vv[4 * t]), __uint_as_float(vv[4 * t + 1]),
+                                                __uint_as_float(vv[4 * t + 2]), __uint_as_float(vv[4 * t + 3]));
+                            }
+                        }
+                    }
+                    named_bar_sync(1, 256);
+                    volatile int *last = reinterpret_cast<volatile int *>(sb + S::OFF_MISC + 8);
+                    if (threadIdx.x == 128) {
+                        // byte counter sidx % 4 of word sidx / 4 (it never exceeds split_f <= 4)
+                        unsigned *w = p.split_cnt + (sidx >> 2);
+                        const unsigned sh = 8u * (unsigned)(sidx & 3);
+                        fence_acq_rel_gpu();
+                        const unsigned n = ((atomicAdd(w, 1u << sh) >> sh) & 0xFFu) + 1u;
+                        const int l = n == (unsigned)p.split_f ? 1 : 0;
+                        if (l) {
+                            atomicAnd(w, ~(0xFFu << sh));   // every part has counted: zero for the next launch
+                            fence_acq_rel_gpu();
+                        }
+                        *last = l;
+                    }
+                    named_bar_sync(1, 256);
+                    write = ok && *last != 0;
+                }
+            }
+            if (write) {
                 const size_t krow = VARLEN ? (size_t)(k_start + key) * p.H + h : (size_t)bh * p.N + key;
                 __nv_bfloat16 *dkrow = reinterpret_cast<__nv_bfloat16 *>(p.dK) + krow * 128;
                 __nv_bfloat16 *dvrow = reinterpret_cast<__nv_bfloat16 *>(p.dV) + krow * 128;
-    #pragma unroll 1
-                for (int j = wg * 2; j < wg * 2 + 2; ++j) {
-                    uint32_t a[32], vv[32];
+                // one half (dK columns 32 j .. 32 j + 31, scaled, or dV's) of
+                // this thread's key row: TMEM, for a split item summed with the
+                // other parts' slots, to bf16 and global memory
+                auto write_half = [&](uint32_t tm_col, int grp0, float sc, __nv_bfloat16 *dst) {
+                    uint32_t a[32];
                     if (i > 0) {
-                        tmem_ld32(tmem + lane_off + S::TM_DK + 32u * j, a);
-                        tmem_ld32(tmem + lane_off + S::TM_DV + 32u * j, vv);
+                        tmem_ld32(tmem + lane_off + tm_col, a);
                         tmem_ld_wait(a);
-                        tmem_ld_wait(vv);
                     } else {
     #pragma unroll
-                        for (int t = 0; t < 32; ++t) a[t] = vv[t] = 0u;
+                        for (int t = 0; t < 32; ++t) a[t] = 0u;
                     }
-                    uint32_t wk[16], wv[16];
+                    if constexpr (PLAIN) {
+                        if (part >= 0) {
+                            // sum over the parts in order 0, 1, ...: slot o (its eight
+                            // float4 loads issued together) or, for o = part, own
+                            auto load_slot = [&](int o, float (&x)[32]) {
+                                const float4 *src = slots + (size_t)o * 8192 + (size_t)grp0 * 128 + r;
     #pragma unroll
-                    for (int t = 0; t < 16; ++t) {
-                        wk[t] = pack_bf16x2(__uint_as_float(a[2 * t]) * p.scale, __uint_as_float(a[2 * t + 1]) * p.scale);
-                        wv[t] = pack_bf16x2(__uint_as_float(vv[2 * t]), __uint_as_float(vv[2 * t + 1]));
-                    }
-                    if (key < Lk) {
-                        uint4 *dk4 = reinterpret_cast<uint4 *>(dkrow + 32 * j);
-                        uint4 *dv4 = reinterpret_cast<uint4 *>(dvrow + 32 * j);
+                                for (int t = 0; t < 8; ++t) {
+                                    const float4 q = __ldcg(src + t * 128);
+                                    x[4 * t] = q.x;
+                                    x[4 * t + 1] = q.y;
+                                    x[4 * t + 2] = q.z;
+                                    x[4 * t + 3] = q.w;
+                                }
+                            };
+                            float sum[32];
+                            if (part == 0) {
     #pragma unroll
-                        for (int t = 0; t < 4; ++t) {
-                            dk4[t] = make_uint4(wk[4 * t], wk[4 * t + 1], wk[4 * t + 2], wk[4 * t + 3]);
-                            dv4[t] = make_uint4(wv[4 * t], wv[4 * t + 1], wv[4 * t + 2], wv[4 * t + 3]);
+                                for (int t = 0; t < 32; ++t) sum[t] = __uint_as_float(a[t]);
+                            } else {
+                                load_slot(0, sum);
+                            }
+                            for (int o = 1; o < p.split_f; ++o) {
+                                if (o == part) {
+    #pragma unroll
+                                    for (int t = 0; t < 32; ++t) sum[t] += __uint_as_float(a[t]);
+                                } else {
+                                    float x[32];
+                                    load_slot(o, x);
+    #pragma unroll
+                                    for (int t = 0; t < 32; ++t) sum[t] += x[t];
+                                }
+                            }
+    #pragma unroll
+                            for (int t = 0; t < 32; ++t) a[t] = __float_as_uint(sum[t]);
                         }
                     }
+                    uint32_t w[16];
+    #pragma unroll
+                    for (int t = 0; t < 16; ++t)
+                        w[t] = pack_bf16x2(__uint_as_float(a[2 * t]) * sc, __uint_as_float(a[2 * t + 1]) * sc);
+                    if (key < Lk) {
+                        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+    #pragma unroll
+                        for (int t = 0; t < 4; ++t) d4[t] = make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
+                    }
+                };
+    #pragma unroll 1
+                for (int j = wg * 2; j < wg * 2 + 2; ++j) {
+                    write_half(S::TM_DK + 32u * j, 8 * j, p.scale, dkrow + 32 * j);
+                    write_half(S::TM_DV + 32u * j, 32 + 8 * j, 1.f, dvrow + 32 * j);
                 }
             }
         }
@@ -700,18 +817,51 @@ static cudaError_t launch_bwd128_t(const BwdParams &p, cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(fa_bwd128_kernel<VARLEN, STAGER, PLAIN>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    return launch_dep(fa_bwd128_kernel<VARLEN, STAGER, PLAIN>, (unsigned)p.Tk * (unsigned)p.BH, Bwd128::THREADS,
-                      smem, st, p);
+    const int64_t items = (int64_t)p.Tk * p.BH;
+    const int64_t grid = p.split_f > 1 ? p.split_from + (items - p.split_from) * p.split_f : items;
+    return launch_dep(fa_bwd128_kernel<VARLEN, STAGER, PLAIN>, (unsigned)grid, Bwd128::THREADS, smem, st, p);
+}
+
+// Split plan of the plain instantiation, whose items all take the same time:
+// one CTA per SM at a time, so the items past the last full wave (rem of
+// them) would run on rem SMs while the others idle.  Each of those runs as
+// f = SMs / rem parts instead (at most 4, at least two query blocks per part,
+// at most what the buffer holds), so that the last wave is about 1/f as long.
+// A part costs a few microseconds more than its share of the blocks (the
+// slots' stores and loads): with one query block per part that was more
+// than the split saved.
+static void plan_split(BwdParams &q) {
+    q.split_from = 0;
+    q.split_f = 0;
+    if (!q.split_buf || !q.split_cnt || q.split_cap < 2) return;
+    const int64_t items = (int64_t)q.Tk * q.BH;
+    const int64_t sms = device_sm_count();
+    const int64_t rem = items % sms;
+    if (rem == 0) return;
+    if (rem > kSplitMaxItems) return;
+    int64_t f = std::min<int64_t>(std::min<int64_t>(sms / rem, 4), q.Tqb / 2);
+    if (f * rem > q.split_cap) f = q.split_cap / rem;
+    if (f < 2) return;
+    q.split_from = (int)(items - rem);
+    q.split_f = (int)f;
 }
 
 cudaError_t launch_bwd128_main(const BwdParams &p, cudaStream_t st) {
-    if (p.causal) return launch_bwd128_t<false, false>(p, st);
-    const bool plain = !p.key_len && !p.block_mask && p.N % 128 == 0;
-    return plain ? launch_bwd128_t<false, true, true>(p, st) : launch_bwd128_t<false, true>(p, st);
+    BwdParams q = p;
+    q.split_from = 0;
+    q.split_f = 0;
+    if (q.causal) return launch_bwd128_t<false, false>(q, st);
+    const bool plain = !q.key_len && !q.block_mask && q.N % 128 == 0;
+    if (!plain) return launch_bwd128_t<false, true>(q, st);
+    plan_split(q);
+    return launch_bwd128_t<false, true, true>(q, st);
 }
 
 cudaError_t launch_bwd128_main_varlen(const BwdParams &p, cudaStream_t st) {
-    return p.causal ? launch_bwd128_t<true, false>(p, st) : launch_bwd128_t<true, true>(p, st);
+    BwdParams q = p;
+    q.split_from = 0;
+    q.split_f = 0;
+    return q.causal ? launch_bwd128_t<true, false>(q, st) : launch_bwd128_t<true, true>(q, st);
 }
 
 }  // namespace fa

@@ -57,6 +57,13 @@ cudaError_t launch_bwd_main_varlen(int d, const BwdParams &p, cudaStream_t st);
 cudaError_t launch_bwd_convert(int d, const float *dQacc, void *dQ, int64_t elems, float scale,
                                cudaStream_t st);
 int bwd_query_block(int d);
+// Workspace of the backward without the d = 128 split area: the status block,
+// D and the dQ accumulator (what fa_bwd requires).
+size_t bwd_base_workspace_bytes(int B, int H, int N, int d);
+// The d = 128 split: at most this many split items (byte counters in the
+// status block's words 8..63) and parts (fp32 slots of 128 x 256).
+constexpr int kSplitMaxItems = 224;
+constexpr int kSplitMaxParts = 256;
 // d = 64: the persistent kernel (fa_bwd64.cu); the workspace's words 2 and 3
 // hold its item counter.
 cudaError_t launch_bwd64_main(const BwdParams &p, cudaStream_t st);

@@ -112,7 +112,9 @@ extern "C" fa_status fa_bwd_noalloc(const void *Q, const void *K, const void *V,
     const void *ptrs[] = {Q, K, V, O, LSE, dO, dQ, dK, dV};
     for (const void *x : ptrs)
         if (!x || !aligned16(x)) return FA_ERR_INVALID_ARGUMENT;
-    const size_t need = fa_bwd_workspace_size(B, H, N, d);
+    // what fa_bwd requires (status block, D, accumulator); the d = 128 split
+    // area after it is used when the array holds that too
+    const size_t need = fa::bwd_base_workspace_bytes(B, H, N, d);
     if (need == 0 || need > kScratchBytes) return FA_ERR_WORKSPACE;
     void *ws = scratch_address();
     if (!ws) return FA_ERR_CUDA;
@@ -121,5 +123,5 @@ extern "C" fa_status fa_bwd_noalloc(const void *Q, const void *K, const void *V,
     // are rewritten by the preprocessing kernel inside fa_bwd)
     if (cudaMemsetAsync(ws, 0, 8, s) != cudaSuccess) return FA_ERR_CUDA;
     return fa_bwd(Q, K, V, O, LSE, dO, dQ, dK, dV, B, H, N, d, softmax_scale, causal, key_len, block_mask, ws,
-                  need, stream);
+                  kScratchBytes, stream);
 }

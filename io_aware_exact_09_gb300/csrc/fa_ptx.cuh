@@ -44,6 +44,17 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Acquire-release fence at GPU scope: with a relaxed atomic after it, a
+// release; after it, an acquire (one thread, behind or ahead of a CTA barrier
+// that orders the other threads' accesses).
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+// Named barrier `id` (1..15; 0 is __syncthreads) over `count` threads (a
+// multiple of 32), all of which must reach it on every path.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");

@@ -145,6 +145,21 @@ struct BwdParams {
     int spread;                      // d = 64 persistent grid: items (key tile, b*h) taken
                                      // key-tile-major across heads (key tile 0 of every head first),
                                      // else head-major; set when the items differ in length
+    // d = 128, every tile full: the items (key tile, b*h) from split_from on
+    // are each run as split_f CTAs over consecutive ranges of query blocks
+    // (split_f < 2: none).  Part j of item split_from + t writes its fp32 dK
+    // (unscaled) and dV to split_buf slot t * split_f + j (128 KiB: 64 column
+    // groups of 4, dK's then dV's, each 128 key rows of float4) and counts
+    // itself in byte t % 4 of
+    // split_cnt[t / 4] (workspace words 8..63: at most 224 split items); the
+    // part that counts last adds the others' slots to its own, writes dK, dV
+    // and sets its byte back to zero.  The host supplies split_buf, split_cnt
+    // and split_cap (slots the buffer holds; 0: no split); the launcher sets
+    // split_from and split_f.
+    float *split_buf;
+    unsigned *split_cnt;
+    int split_cap;
+    int split_from, split_f;
 };
 
 // The sequence a CTA of a ragged batch works on: query rows [q_start,

@@ -40,6 +40,16 @@ def test_status_strings_and_sizes(L):
     # status + D [B,H,N] fp32 + dQacc [B,H,N,d] fp32, 256-byte rounded
     assert fa.fa_bwd_workspace_size(1, 2, 128, 64) == 256 + 1024 + 65536
     assert fa.fa_bwd_workspace_size(1, 1, 3, 64) == 256 + 256 + 768
+    # d = 128: + 128 KiB per CTA of a split key tile, for N > 128 only:
+    # min(256, B * H * T * min(4, T)) of them, T = ceil(N / 128)
+    slot = 128 * 256 * 4
+    assert fa.fa_bwd_workspace_size(1, 2, 128, 128) == 256 + 1024 + 131072
+    assert fa.fa_bwd_workspace_size(1, 1, 256, 128) == 256 + 1024 + 131072 + 4 * slot
+    assert fa.fa_bwd_workspace_size(1, 2, 512, 128) == 256 + 4096 + 524288 + 32 * slot
+    rows = 16 * 16384
+    assert fa.fa_bwd_workspace_size(1, 16, 16384, 128) == 256 + rows * 4 + rows * 128 * 4 + 256 * slot
+    # the ragged backward does not split
+    assert fa.fa_bwd_varlen_workspace_size(16, 16384, 128) == 256 + rows * 4 + rows * 128 * 4
     assert fa.fa_host_workspace_size(1, 2, 128, 64, 1) > fa.fa_host_workspace_size(1, 2, 128, 64, 0)
 
 

@@ -1,0 +1,95 @@
+"""The d = 128 backward's split of the last wave's key tiles (every tile
+full: no mask, N a multiple of 128).  The items past the last full wave of
+one CTA per SM run as 2-4 CTAs each over consecutive query-block ranges; the
+CTA that finishes an item last sums the parts' fp32 dK, dV in part order and
+writes them.  Checked here: parity with the oracle at several split factors,
+agreement with the unsplit kernel (a workspace without the split area),
+bit-identical repeats (the sum's order does not depend on which part ends
+last), and the counters in the status block back at zero after every call."""
+import pytest
+import torch
+
+import oracle
+from synthetic import make_case
+from gpu_common import GRAD_REL_FRO, check_forward, check_grads, f64, oracle_args, rel_fro, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def base_bytes(B, H, N, d):
+    r256 = lambda x: (x + 255) // 256 * 256
+    rows = B * H * N
+    return 256 + r256(rows * 4) + r256(rows * d * 4)
+
+
+def split_factor(B, H, N, sms):
+    """The launcher's plan: items past the last full wave, parts per item."""
+    T = N // 128
+    items = B * H * T
+    rem = items % sms
+    if rem == 0 or rem > 224:
+        return 0
+    f = min(sms // rem, 4, T // 2)
+    cap = min(256, B * H * T * min(4, T))
+    if f * rem > cap:
+        f = cap // rem
+    return f if f >= 2 else 0
+
+
+# (B, H, N) on 152 SMs: every item split into 4 (8 items), 3 parts after one
+# full wave (192 items), 2 parts after one full wave (224 items), every item
+# split into 2 (at least two query blocks per part)
+SHAPES = [(1, 2, 1024), (1, 12, 2048), (1, 28, 1024), (1, 3, 512)]
+
+
+@pytest.mark.parametrize("B,H,N", SHAPES)
+def test_split_backward_matches_oracle_and_unsplit(B, H, N):
+    import io_aware_exact_09_gb300 as fa
+    d = 128
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    f = split_factor(B, H, N, sms)
+    c = make_case(B, H, N, d, seed=3 * H + N)
+    c["scale"] = 1.0 / d ** 0.5
+    g = to_dev(c, "cuda")
+    O, L = fa.attention_forward(g["Q"], g["K"], g["V"], c["scale"], False, check_status=True)
+    full = fa.fa_bwd_workspace_size(B, H, N, d)
+    assert full > base_bytes(B, H, N, d)
+    ws = fa.workspace(full, "cuda")
+    got = fa.attention_backward(g["Q"], g["K"], g["V"], O, L, g["dO"], c["scale"], False, ws=ws, check_status=True)
+    torch.cuda.synchronize()
+    # the status block's split counters (words 8..63) are back at zero, and
+    # the parts' slots (after D and the accumulator) were written: the split ran
+    assert int(ws[32:256].view(torch.int32).abs().sum()) == 0, f
+    if f >= 2:
+        assert int((ws[base_bytes(B, H, N, d):] != 0).sum()) > 0, f
+    # bit-identical repeats
+    for _ in range(3):
+        again = fa.attention_backward(g["Q"], g["K"], g["V"], O, L, g["dO"], c["scale"], False, ws=ws)
+        assert torch.equal(got[1], again[1]) and torch.equal(got[2], again[2]), f
+    assert fa.fa_get_device_status(ws) == 0
+    assert int(ws[32:256].view(torch.int32).abs().sum()) == 0
+    # the unsplit kernel: a workspace holding the status block, D and the accumulator only
+    ws0 = fa.workspace(base_bytes(B, H, N, d), "cuda")
+    ref0 = fa.attention_backward(g["Q"], g["K"], g["V"], O, L, g["dO"], c["scale"], False, ws=ws0,
+                                 check_status=True)
+    for k in (1, 2):
+        e = rel_fro(got[k].double().cpu().numpy(), ref0[k].double().cpu().numpy())
+        assert e <= 2e-3, ("split vs unsplit", f, k, e)
+    # the oracle
+    rO, rL, rdQ, rdK, rdV = oracle.attention_bwd(f64(c["Q"]), f64(c["K"]), f64(c["V"]), f64(c["dO"]), c["scale"],
+                                                 **oracle_args(c))
+    check_forward(O.double().cpu().numpy(), L.double().cpu().numpy(), rO, rL, "split fwd")
+    check_grads({k: t.double().cpu().numpy() for k, t in zip(("dQ", "dK", "dV"), got)},
+                dict(dQ=rdQ, dK=rdK, dV=rdV), "split f=%d" % f)
+
+
+def test_split_plan_covers_the_intended_factors():
+    """On this GPU the shapes above take the split factors they are meant to
+    (152 SMs: 4, 3, 2, 2); on another SM count the parity test still holds for
+    whatever plan the launcher makes."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    fs = [split_factor(B, H, N, sms) for B, H, N in SHAPES]
+    if sms == 152:
+        assert fs == [4, 3, 2, 2], fs
+    # the long-context shape: 2048 items, 72 past 13 full waves -> 2 parts each
+    assert split_factor(1, 16, 16384, 152) == 2
