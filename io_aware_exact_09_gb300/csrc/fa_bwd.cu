@@ -140,12 +140,18 @@ cudaError_t launch_bwd_pre(int d, const void *O, const void *dO, float *Dvec, fl
     const int64_t per_block = (int64_t)(256 / (d / 8)) * 4;
     const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>((rows + per_block - 1) / per_block,
                                                                            (int64_t)device_sm_count() * 16));
+    // A plain launch (the kernel's wait is then a no-op; its trigger still lets
+    // the main kernel be scheduled early).  Launched to overlap the forward's
+    // last CTAs, it made the step after it slower: long-context step 5.74 ->
+    // 5.81 ms (the main kernel's CTAs then also scheduled early; either
+    // plain launch alone removes the loss), GPT-2-medium shape unchanged.
     if (d == 64)
-        return launch_dep(fa_bwd_pre_kernel<64>, grid, 256, 0, st, (const __nv_bfloat16 *)O,
-                          (const __nv_bfloat16 *)dO, Dvec, dQacc, rows);
+        fa_bwd_pre_kernel<64><<<grid, 256, 0, st>>>((const __nv_bfloat16 *)O, (const __nv_bfloat16 *)dO, Dvec,
+                                                    dQacc, rows);
     else
-        return launch_dep(fa_bwd_pre_kernel<128>, grid, 256, 0, st, (const __nv_bfloat16 *)O,
-                          (const __nv_bfloat16 *)dO, Dvec, dQacc, rows);
+        fa_bwd_pre_kernel<128><<<grid, 256, 0, st>>>((const __nv_bfloat16 *)O, (const __nv_bfloat16 *)dO, Dvec,
+                                                     dQacc, rows);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_convert(int d, const float *dQacc, void *dQ, int64_t elems, float scale,

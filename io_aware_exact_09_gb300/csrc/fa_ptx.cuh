@@ -31,9 +31,10 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 }
 
 // ------------------------------------------------------------------ programmatic dependent launch
-// The library launches its kernels with programmatic stream serialisation, so
-// a kernel's CTAs may be scheduled while the previous kernel in the stream is
-// still draining.  Every kernel calls grid_dep_wait() in every thread as its
+// The library launches its kernels (all but the plan export, the self-test
+// and, by measurement, the backward preprocessing) with programmatic stream
+// serialisation, so a kernel's CTAs may be scheduled while the previous kernel
+// in the stream is still draining.  Every kernel calls grid_dep_wait() in every thread as its
 // first statement: it returns once the previous kernel has completed and its
 // memory operations are visible (at once outside such a launch).  Since no
 // grid completes before its own wait returned, all earlier work in the stream

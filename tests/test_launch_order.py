@@ -11,7 +11,9 @@ after it would then no longer be ordered behind the earlier ones.  This test
 finds every kernel passed to ``launch_dep`` and checks that the first
 statements of its body are the wait and then the trigger, and that the plain
 ``<<<>>>`` form (fully ordered, no overlap) is left to the two kernels that are
-not on any step's path: the plan export and the failure-path self-test."""
+not on any step's path (the plan export and the failure-path self-test) and to
+the backward preprocessing, launched plainly by measurement; a plain launch
+is always ordered behind everything before it."""
 import os
 import re
 
@@ -66,7 +68,7 @@ def test_every_dependent_launch_waits_first():
         if n == "fa_internal.h":
             continue
         launched |= dep_launched(s)
-    assert {"fa_fwd_kernel", "fa_bwd_pre_kernel", "fa_bwd64_kernel", "fa_bwd128_kernel",
+    assert {"fa_fwd_kernel", "fa_bwd64_kernel", "fa_bwd128_kernel",
             "fa_bwd_convert_kernel", "fa_decode_kernel", "fa_decode_merge_kernel", "fa_fwd_fp8_kernel",
             "fa_quant_fp8_kernel"} <= launched
     for k in sorted(launched):
@@ -80,7 +82,19 @@ def test_plain_launches_are_the_listed_ones():
     plain = set()
     for s in sources().values():
         plain |= set(re.findall(r"(\w+)(?:<[^<>;]*>)?<<<", s))
-    assert plain == {"fa_plan_kernel", "fa_selftest_wait_kernel"}, plain
+    # the plan export and the self-test are off every step's path; the
+    # backward preprocessing is launched plainly by measurement (launched to
+    # overlap the forward's tail it slowed the main kernel after it down) and
+    # still waits first and triggers its successor early
+    assert plain == {"fa_plan_kernel", "fa_selftest_wait_kernel", "fa_bwd_pre_kernel"}, plain
+
+
+def test_plainly_launched_step_kernels_keep_the_wait_and_trigger():
+    bodies = {}
+    for s in sources().values():
+        bodies.update(kernel_bodies(s))
+    stmts = [x.strip() for x in bodies["fa_bwd_pre_kernel"].split(";") if x.strip()]
+    assert stmts[:2] == ["grid_dep_wait()", "grid_dep_launch()"], stmts[:2]
 
 
 def test_the_wait_is_the_griddepcontrol_pair():
