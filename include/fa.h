@@ -79,8 +79,16 @@ typedef enum {
 /* Size of the 128 x 128 tile (and of a block_mask block). */
 int fa_tile_size(void);
 
-/* Bytes of device workspace fa_fwd needs (256): the status word and the
- * work-item counter of the persistent forward grid. */
+/* Bytes of device workspace for fa_fwd and fa_fwd_fp8: the 256-byte status
+ * block (status word, the persistent forward grid's work-item counter), and
+ * for d = 128 with at least 32 key tiles (N >= 4096) the FP8 forward's split
+ * area: 130 KiB per CTA of a split item, for min(512, B * H * ceil(T / 2) *
+ * min(4, T / 16)) of them (T = ceil(N / 128)).  With no mask and N a multiple
+ * of 128 every FP8 forward item (two query tiles) takes the same time; the
+ * items past the last full wave of one CTA per SM run as 2-4 CTAs each over
+ * parts of the key range, whose unnormalised O and running (max, sum) meet in
+ * that area, the last to finish merging them.  The calls accept the 256-byte
+ * status block alone and then do not split. */
 size_t fa_fwd_workspace_size(int B, int H, int N, int d);
 
 /* Bytes of device workspace fa_bwd uses: the 256-byte status block, the
@@ -215,7 +223,9 @@ fa_status fa_quantize_fp8_rotated(const void *X, void *X8, float *scales, const 
  * scale) with both products on the FP8 tensor cores; the probabilities are
  * rounded to e4m3 for the P.V product (this, not the inputs, sets the
  * accuracy: about 2^-5 relative per probability).  O (bf16), LSE (fp32,
- * natural log), masks and workspace as fa_fwd.  One kernel launch.
+ * natural log), masks and workspace as fa_fwd (the split of the last wave,
+ * fa_fwd_workspace_size, is this call's; each part rounds its probabilities
+ * against its own running maximum).  One kernel launch.
  */
 fa_status fa_fwd_fp8(const void *Q8, const void *K8, const void *Vt8, const float *sQ,
                      const float *sK, const float *sV, void *O, float *LSE, int B, int H, int N,

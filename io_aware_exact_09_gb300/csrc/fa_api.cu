@@ -166,6 +166,17 @@ size_t bwd_split_parts(int B, int H, int N, int d) {
     if (bh >= fa::kSplitMaxParts || per >= fa::kSplitMaxParts) return fa::kSplitMaxParts;
     return (size_t)std::min<int64_t>(fa::kSplitMaxParts, bh * per);
 }
+// d = 128, at least 32 key tiles: slots for the forward's split of its last
+// wave (fa_fwd_fp8.cu), at most four parts per item of two query tiles, 16
+// key tiles per part at least, kFwdSplitMaxParts in all.
+size_t fwd_split_parts(int B, int H, int N, int d) {
+    if (d != 128 || B <= 0 || H <= 0 || N < 32 * 128) return 0;
+    const int64_t T = (N + 127) / 128;
+    const int64_t bh = (int64_t)B * H;
+    const int64_t per = (T + 1) / 2 * std::min<int64_t>(4, T / 16);
+    if (bh >= fa::kFwdSplitMaxParts || per >= fa::kFwdSplitMaxParts) return fa::kFwdSplitMaxParts;
+    return (size_t)std::min<int64_t>(fa::kFwdSplitMaxParts, bh * per);
+}
 }  // namespace
 
 extern "C" {
@@ -173,8 +184,7 @@ extern "C" {
 int fa_tile_size(void) { return fa::kTile; }
 
 size_t fa_fwd_workspace_size(int B, int H, int N, int d) {
-    (void)B; (void)H; (void)N; (void)d;
-    return kStatusBytes;
+    return kStatusBytes + fwd_split_parts(B, H, N, d) * fa::kFwdSplitSlotBytes;
 }
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
@@ -228,8 +238,7 @@ fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LS
     if (!Q || !K || !V || !O || !LSE) return FA_ERR_INVALID_ARGUMENT;
     if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(LSE))
         return FA_ERR_INVALID_ARGUMENT;
-    if (!workspace || !aligned16(workspace) || workspace_bytes < fa_fwd_workspace_size(B, H, N, d))
-        return FA_ERR_WORKSPACE;
+    if (!workspace || !aligned16(workspace) || workspace_bytes < kStatusBytes) return FA_ERR_WORKSPACE;
     if (block_mask && (N + 127) / 128 > kFwdMaxMaskedKeyTiles) return FA_ERR_UNSUPPORTED;
 
     FwdParams p;
@@ -267,8 +276,7 @@ fa_status fa_fwd_tiles(const void *Q, const void *K, const void *V, void *O, flo
     if (!Q || !K || !V || !O || !LSE) return FA_ERR_INVALID_ARGUMENT;
     if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(LSE))
         return FA_ERR_INVALID_ARGUMENT;
-    if (!workspace || !aligned16(workspace) || workspace_bytes < fa_fwd_workspace_size(B, H, N, d))
-        return FA_ERR_WORKSPACE;
+    if (!workspace || !aligned16(workspace) || workspace_bytes < kStatusBytes) return FA_ERR_WORKSPACE;
     if (block_mask && (N + block_k - 1) / block_k > kFwdMaxMaskedKeyTiles) return FA_ERR_UNSUPPORTED;
     FwdParams p;
     std::memset(&p, 0, sizeof(p));
@@ -377,8 +385,7 @@ fa_status fa_fwd_fp8(const void *Q8, const void *K8, const void *Vt8, const floa
     if (!Q8 || !K8 || !Vt8 || !sQ || !sK || !sV || !O || !LSE) return FA_ERR_INVALID_ARGUMENT;
     if (!aligned16(Q8) || !aligned16(K8) || !aligned16(Vt8) || !aligned16(O) || !aligned16(LSE))
         return FA_ERR_INVALID_ARGUMENT;
-    if (!workspace || !aligned16(workspace) || workspace_bytes < fa_fwd_workspace_size(B, H, N, d))
-        return FA_ERR_WORKSPACE;
+    if (!workspace || !aligned16(workspace) || workspace_bytes < kStatusBytes) return FA_ERR_WORKSPACE;
     FwdParams p;
     std::memset(&p, 0, sizeof(p));
     const int BH = B * H;
@@ -401,6 +408,13 @@ fa_status fa_fwd_fp8(const void *Q8, const void *K8, const void *Vt8, const floa
     p.Tk = p.Tq;
     p.causal = causal ? 1 : 0;
     p.scale_log2 = softmax_scale * kLog2e;
+    // the split area, when the workspace holds it (the launcher decides whether to split)
+    const size_t parts = fwd_split_parts(B, H, N, d);
+    if (parts >= 2 && workspace_bytes >= kStatusBytes + parts * fa::kFwdSplitSlotBytes) {
+        p.split_cnt = p.status + 8;
+        p.split_buf = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + kStatusBytes);
+        p.split_cap = (int)parts;
+    }
     return fa::launch_fwd_fp8(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

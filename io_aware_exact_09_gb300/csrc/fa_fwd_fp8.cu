@@ -97,10 +97,31 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     const int Tp = (p.Tq + 1) / 2;
-    const int pq = Tp - 1 - (int)(blockIdx.x % Tp);
-    const int bh = (int)(blockIdx.x / Tp);
-    const int b = bh / p.H;
     const int nb = (p.N + kTile - 1) / kTile;
+    // the item (query-tile pair, b*h) of this CTA; from split_from on (every
+    // tile full), part `part` of an item run as split_f CTAs, each over its own
+    // range of key tiles (the last wave's items, so that it fills the SMs).
+    // split_part: -1 for a whole item, else the part; *sidx: the split item's
+    // index past split_from.  Recomputed where needed rather than kept live.
+    auto split_part = [&](int *sidx) -> int {
+        const int j = (int)blockIdx.x - p.split_from;
+        if (!PLAIN || p.split_f < 2 || j < 0) return -1;
+        *sidx = j / p.split_f;
+        return j - *sidx * p.split_f;
+    };
+    int item = (int)blockIdx.x;
+    int khi = 0;                                     // a part's key tiles end here (0: whole item)
+    {
+        int si = 0;
+        const int part = split_part(&si);
+        if (part >= 0) {
+            item = p.split_from + si;
+            khi = (part + 1) * nb / p.split_f;
+        }
+    }
+    const int pq = Tp - 1 - item % Tp;
+    const int bh = item / Tp;
+    const int b = bh / p.H;
     int q0[2], qn[2];
 #pragma unroll
     for (int x = 0; x < 2; ++x) {
@@ -123,6 +144,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
         int lim = kvis;
         if (p.causal) lim = min(lim, q0[x] + qn[x]);
         kend[x] = qn[x] > 0 ? (lim + kTile - 1) / kTile : 0;
+        if (PLAIN && khi > 0) kend[x] = khi;
     }
     const int kend_union = max(kend[0], kend[1]);
     // per-query-tile values by selection, so that the arrays stay in registers
@@ -152,6 +174,20 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
             if (v0 || v1) return k;
         }
         return p.Tk;
+    };
+    // the first tile of query tile x (x = 2: of either): a split part starts
+    // at its own first key tile (computed here, at the loops' entry, so that
+    // the per-tile next_tile keeps no extra value live)
+    auto first_tile = [&](int x) -> int {
+        if constexpr (PLAIN) {
+            int si = 0;
+            const int part = split_part(&si);
+            if (part >= 0) {
+                const int k = part * nb / p.split_f;
+                return k < (x == 2 ? kend_union : kend_of(x)) ? k : p.Tk;
+            }
+        }
+        return next_tile(x, -1);
     };
 
     if (threadIdx.x == 0) {
@@ -195,7 +231,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
             {
                 int u = 0;
                 bool ok = true;
-                int kt = next_tile(2, -1);
+                int kt = first_tile(2);
                 if (kt < p.Tk) {
                     const uint32_t nq = (qn[0] > 0 ? 1u : 0u) + (qn[1] > 0 ? 1u : 0u);
                     mbar_arrive_expect_tx_elect(bar(S::B_QFULL), nq * S::TILE_BYTES);
@@ -217,7 +253,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
                     tma_load_3d_elect(base + S::OFF_V + s * S::TILE_BYTES, &p.tmV, bar(S::B_VFULL + s), kt * kTile, 0, bh);
                 }
                 if (!ok) {
-                    if (next_tile(2, -1) < p.Tk) f8_drain_wait(bar(S::B_QFULL), 0);
+                    if (first_tile(2) < p.Tk) f8_drain_wait(bar(S::B_QFULL), 0);
                     for (int i = (u > S::STAGES ? u - S::STAGES : 0); i < u; ++i) {
                         const int s = i % S::STAGES;
                         const uint32_t ph = (uint32_t)(i / S::STAGES) & 1u;
@@ -248,7 +284,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
                     mma_commit_elect(bar(S::B_SFULL + x));
                     ++ns;
                 };
-                int kt = next_tile(2, -1);
+                int kt = first_tile(2);
                 if (kt < p.Tk) {
                     ok = mbar_wait_warp(bar(S::B_QFULL), 0, g, 0x211) && mbar_wait_warp(bar(S::B_KFULL + 0), 0, g, 0x212);
                     if (ok && !skip(x, kt)) {
@@ -336,7 +372,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
         // per-tile block scales, loaded one tile ahead so their latency hides
         // behind the previous tile's work
         const float *sKh = p.sK + (size_t)bh * p.Tk, *sVh = p.sV + (size_t)bh * p.Tk;
-        int kt = next_tile(x, -1);
+        int kt = first_tile(x);
         float sk_n = 0.f, sv_n = 0.f;
         if (kt < p.Tk) {
             sk_n = sKh[kt];
@@ -480,8 +516,93 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
             ok = mbar_wait_warp(bar(S::B_OFULL + x), 0u, g, 0x414);
             tc_fence_after();
         }
-        if (ok) {
-            const float inv_l = (l > 0.f) ? sv_max / l : 0.f;
+        // An item split over several CTAs: each part stores its row of O
+        // (unnormalised fp32, relative to its m_ref) and (m_ref, l) in its slot,
+        // then counts itself; the part that counts last merges the parts in part
+        // order (its own from TMEM and registers), O = sum_j w_j O_j * sv_max /
+        // sum_j w_j l_j with w_j = 2^(m_j - max m), so the result does not depend
+        // on which part that is.  O in the slot is [query tile][column group of
+        // 4][row] float4, so that a warp's store covers 512 contiguous bytes.
+        // The stores are published by one thread (CTA barrier, release fence,
+        // count) and the counter read the same way (count, acquire fence,
+        // barrier); all 256 softmax threads take both barriers on every path.
+        constexpr int kSlotF4 = (int)(kFwdSplitSlotBytes / 16);
+        bool write = ok;
+        const float4 *slots = nullptr;               // part 0's slot of this item
+        int sidx = 0;
+        const int part = split_part(&sidx);
+        if constexpr (PLAIN) {
+            if (part >= 0) {
+                slots = reinterpret_cast<const float4 *>(p.split_buf) + (size_t)sidx * p.split_f * kSlotF4;
+                if (ok) {
+                    float4 *mine = const_cast<float4 *>(slots) + (size_t)part * kSlotF4;
+#pragma unroll 1
+                    for (int j = 0; j < D / 32; ++j) {
+                        uint32_t o[32];
+                        tmem_ld32(o_tmem + 32u * j, o);
+                        tmem_ld_wait(o);
+#pragma unroll
+                        for (int t = 0; t < 8; ++t)
+                            mine[(x * 32 + 8 * j + t) * 128 + r] =
+                                make_float4(__uint_as_float(o[4 * t]), __uint_as_float(o[4 * t + 1]),
+                                            __uint_as_float(o[4 * t + 2]), __uint_as_float(o[4 * t + 3]));
+                    }
+                    reinterpret_cast<float2 *>(mine + 2 * 32 * 128)[x * 128 + r] = make_float2(m_ref, l);
+                }
+                named_bar_sync(1, 256);
+                volatile int *last = reinterpret_cast<volatile int *>(sb + S::OFF_MISC + 8);
+                if (threadIdx.x == 128) {
+                    // byte counter sidx % 4 of word sidx / 4 (it never exceeds split_f <= 4)
+                    unsigned *w = p.split_cnt + (sidx >> 2);
+                    const unsigned sh = 8u * (unsigned)(sidx & 3);
+                    fence_acq_rel_gpu();
+                    const unsigned n = ((atomicAdd(w, 1u << sh) >> sh) & 0xFFu) + 1u;
+                    const int lst = n == (unsigned)p.split_f ? 1 : 0;
+                    if (lst) {
+                        atomicAnd(w, ~(0xFFu << sh));    // every part has counted: zero for the next launch
+                        fence_acq_rel_gpu();
+                    }
+                    *last = lst;
+                }
+                named_bar_sync(1, 256);
+                write = ok && *last != 0;
+            }
+        }
+        if (write) {
+            float inv_l = (l > 0.f) ? sv_max / l : 0.f;
+            float lse2 = (l > 0.f) ? m_ref + log2f(l) : -INFINITY;     // log2 domain
+            float wgt[4] = {1.f, 1.f, 1.f, 1.f};                       // the parts' weights (split items)
+            if constexpr (PLAIN) {
+                if (part >= 0) {
+                    float mm[4], ll[4];
+                    float M = -INFINITY;
+#pragma unroll
+                    for (int o = 0; o < 4; ++o) {
+                        mm[o] = -INFINITY;
+                        ll[o] = 0.f;
+                        if (o < p.split_f) {
+                            if (o == part) {
+                                mm[o] = m_ref;
+                                ll[o] = l;
+                            } else {
+                                const float2 v = __ldcg(reinterpret_cast<const float2 *>(
+                                                            slots + (size_t)o * kSlotF4 + 2 * 32 * 128) + x * 128 + r);
+                                mm[o] = v.x;
+                                ll[o] = v.y;
+                            }
+                            M = fmaxf(M, mm[o]);
+                        }
+                    }
+                    float L = 0.f;
+#pragma unroll
+                    for (int o = 0; o < 4; ++o) {
+                        wgt[o] = (o < p.split_f && mm[o] != -INFINITY) ? ex2(mm[o] - M) : 0.f;
+                        L += wgt[o] * ll[o];
+                    }
+                    inv_l = (L > 0.f) ? sv_max / L : 0.f;
+                    lse2 = (L > 0.f) ? M + log2f(L) : -INFINITY;
+                }
+            }
             __nv_bfloat16 *orow = reinterpret_cast<__nv_bfloat16 *>(p.O) + ((size_t)bh * p.N + q) * D;
 #pragma unroll 1
             for (int j = 0; j < D / 32; ++j) {
@@ -493,6 +614,38 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
 #pragma unroll
                     for (int t = 0; t < 32; ++t) o[t] = 0u;
                 }
+                if constexpr (PLAIN) {
+                    if (part >= 0) {
+                        // sum over the parts in order 0, 1, ...: slot oo (its eight
+                        // float4 loads issued together) or, for oo = part, own
+                        float acc[32];
+#pragma unroll
+                        for (int t = 0; t < 32; ++t) acc[t] = 0.f;
+#pragma unroll
+                        for (int oo = 0; oo < 4; ++oo) {
+                            if (oo >= p.split_f) break;
+                            float xv[32];
+                            if (oo == part) {
+#pragma unroll
+                                for (int t = 0; t < 32; ++t) xv[t] = __uint_as_float(o[t]);
+                            } else {
+                                const float4 *src = slots + (size_t)oo * kSlotF4 + (size_t)(x * 32 + 8 * j) * 128 + r;
+#pragma unroll
+                                for (int t = 0; t < 8; ++t) {
+                                    const float4 v = __ldcg(src + t * 128);
+                                    xv[4 * t] = v.x;
+                                    xv[4 * t + 1] = v.y;
+                                    xv[4 * t + 2] = v.z;
+                                    xv[4 * t + 3] = v.w;
+                                }
+                            }
+#pragma unroll
+                            for (int t = 0; t < 32; ++t) acc[t] = fmaf(wgt[oo], xv[t], acc[t]);
+                        }
+#pragma unroll
+                        for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(acc[t]);
+                    }
+                }
                 uint32_t w[16];
 #pragma unroll
                 for (int t = 0; t < 16; ++t)
@@ -503,8 +656,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
                     for (int t = 0; t < 4; ++t) dst[t] = make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
                 }
             }
-            if (r < qnx)
-                p.LSE[(size_t)bh * p.N + q] = (l > 0.f) ? (m_ref + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+            if (r < qnx) p.LSE[(size_t)bh * p.N + q] = lse2 * 0.69314718055994530942f;
         }
         __syncwarp();
         setmaxnreg_dec<S::REGS_CTRL>();
@@ -518,17 +670,54 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
 
 }  // namespace
 
+// Split plan of the plain instantiation, whose items all take the same time:
+// one CTA per SM, so the items past the last full wave (rem of them) would run
+// on rem SMs while the others idle.  Each of those runs as f parts over
+// consecutive key-tile ranges instead, f in 2..4 chosen so that the parts'
+// waves, ceil(rem f / SMs) of them, each 1/f long, end soonest; none if no f
+// beats a whole wave.  A part costs ~5-10 us beyond its share of the tiles
+// (the slot's stores, the count, the last part's merge), paid once per wave of
+// parts, so a part gets 16 key tiles at least: with 8 (B4 H16 N4096, f = 4)
+// the split was 7 % slower.  Long-context shape: 1,024 items, 112 past six
+// waves of 152, f = 4 (1.158 -> 1.139 ms).
+static void plan_fwd_split(FwdParams &q) {
+    q.split_from = 0;
+    q.split_f = 0;
+    if (!q.split_buf || !q.split_cnt || q.split_cap < 2) return;
+    const int64_t items = (int64_t)((q.Tq + 1) / 2) * q.BH;
+    const int64_t sms = device_sm_count();
+    const int64_t rem = items % sms;
+    if (rem == 0 || rem > kSplitMaxItems) return;
+    int64_t best = 1, best_num = 1, best_den = 1;          // last wave's length best_num / best_den
+    for (int64_t f = 2; f <= 4 && f <= q.Tk / 16 && rem * f <= q.split_cap; ++f) {
+        const int64_t num = (rem * f + sms - 1) / sms;
+        if (num * best_den < best_num * f) {
+            best = f;
+            best_num = num;
+            best_den = f;
+        }
+    }
+    if (best < 2) return;
+    q.split_from = (int)(items - rem);
+    q.split_f = (int)best;
+}
+
 cudaError_t launch_fwd_fp8(const FwdParams &p, cudaStream_t st) {
     const int smem = F8Shape::SMEM_BYTES;
     const bool plain = !p.causal && !p.key_len && !p.block_mask && p.N % 128 == 0;
     cudaError_t e = cudaFuncSetAttribute(plain ? fa_fwd_fp8_kernel<true> : fa_fwd_fp8_kernel<false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    const unsigned grid = (unsigned)((p.Tq + 1) / 2) * (unsigned)p.BH;
+    FwdParams q = p;
+    q.split_from = 0;
+    q.split_f = 0;
+    if (plain) plan_fwd_split(q);
+    const int64_t items = (int64_t)((q.Tq + 1) / 2) * q.BH;
+    const int64_t grid = q.split_f > 1 ? q.split_from + (items - q.split_from) * q.split_f : items;
     if (plain)
-        return launch_dep(fa_fwd_fp8_kernel<true>, grid, F8Shape::THREADS, smem, st, p);
+        return launch_dep(fa_fwd_fp8_kernel<true>, (unsigned)grid, F8Shape::THREADS, smem, st, q);
     else
-        return launch_dep(fa_fwd_fp8_kernel<false>, grid, F8Shape::THREADS, smem, st, p);
+        return launch_dep(fa_fwd_fp8_kernel<false>, (unsigned)grid, F8Shape::THREADS, smem, st, q);
 }
 
 }  // namespace fa

@@ -43,6 +43,10 @@ cudaError_t launch_fwd_tiles(int d, int block_k, const FwdParams &p, cudaStream_
 cudaError_t launch_fwd_varlen(int d, const FwdParams &p, cudaStream_t st);
 // FP8 forward (d = 128): e4m3 Q, K, V^T with per-block scales.
 cudaError_t launch_fwd_fp8(const FwdParams &p, cudaStream_t st);
+// The forward's split of the last wave: at most this many parts, one slot of
+// kFwdSplitSlotBytes each (two query tiles x 128 rows: 128 fp32 of O, m, l).
+constexpr int kFwdSplitMaxParts = 512;
+constexpr size_t kFwdSplitSlotBytes = 2 * 128 * (128 + 2) * 4;
 // FP8 block quantisation of one bf16 tensor [BH][N][d] (V: transposed);
 // with signs (Q, K only), of the incoherently rotated rows (x * signs) H.
 cudaError_t launch_quant_fp8(int d, const void *X, void *Y, float *scales, int BH, int N, int transpose,

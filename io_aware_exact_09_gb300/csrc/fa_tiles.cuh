@@ -104,6 +104,20 @@ struct FwdParams {
     int spread;                      // persistent grid: items handed out query-tile-pair-major across
                                      // heads (heaviest pairs of every head first), else head-major;
                                      // set when the items differ in length
+    // FP8 forward, every tile full: the items (query-tile pair, b*h) from
+    // split_from on are each run as split_f CTAs over consecutive ranges of key
+    // tiles (split_f < 2: none).  Part j of item split_from + t writes its
+    // unnormalised fp32 O rows and (m, l) to split_buf slot t * split_f + j
+    // (kFwdSplitSlotBytes: O as [query tile 2][column group 32][row 128] float4,
+    // then (m, l) as [query tile 2][row 128] float2) and counts itself in byte
+    // t % 4 of split_cnt[t / 4] (workspace words 8..63); the part that counts
+    // last merges the slots, writes O and LSE and sets its byte back to zero.
+    // The host supplies split_buf, split_cnt and split_cap (slots the buffer
+    // holds; 0: no split); the launcher sets split_from and split_f.
+    float *split_buf;
+    unsigned *split_cnt;
+    int split_cap;
+    int split_from, split_f;
 };
 
 struct DecParams {

@@ -48,6 +48,14 @@ def test_status_strings_and_sizes(L):
     assert fa.fa_bwd_workspace_size(1, 2, 512, 128) == 256 + 4096 + 524288 + 32 * slot
     rows = 16 * 16384
     assert fa.fa_bwd_workspace_size(1, 16, 16384, 128) == 256 + rows * 4 + rows * 128 * 4 + 256 * slot
+    # the forward's split area (FP8 forward): d = 128 and at least 32 key tiles,
+    # min(512, B * H * ceil(T / 2) * min(4, T / 16)) slots of 2 x 128 x 130 fp32
+    fslot = 2 * 128 * 130 * 4
+    assert fa.fa_fwd_workspace_size(1, 2, 4095, 128) == 256
+    assert fa.fa_fwd_workspace_size(1, 2, 4096, 128) == 256 + 64 * fslot
+    assert fa.fa_fwd_workspace_size(1, 1, 8192, 128) == 256 + 128 * fslot
+    assert fa.fa_fwd_workspace_size(1, 16, 16384, 128) == 256 + 512 * fslot
+    assert fa.fa_fwd_workspace_size(4, 16, 16384, 64) == 256
     # the ragged backward does not split
     assert fa.fa_bwd_varlen_workspace_size(16, 16384, 128) == 256 + rows * 4 + rows * 128 * 4
     assert fa.fa_host_workspace_size(1, 2, 128, 64, 1) > fa.fa_host_workspace_size(1, 2, 128, 64, 0)

@@ -218,3 +218,80 @@ def test_incoherent_processing_lowers_fp8_error_with_outliers():
         O, _ = fa.attention_forward_fp8(dev(Q), dev(K), dev(V), scale, False, check_status=True, signs=s)
         err[name] = float(np.linalg.norm(O.double().cpu().numpy() - rO) / np.linalg.norm(rO))
     assert err["plain"] / err["rotated"] > 1.5, err
+
+
+def fp8_split_factor(B, H, N, sms):
+    """The launcher's plan for the plain FP8 forward: items (query-tile pairs
+    x B x H) past the last full wave, parts per item (2..4, 16 key tiles per
+    part at least), the f whose parts' waves end soonest."""
+    T = N // 128
+    items = B * H * ((T + 1) // 2)
+    rem = items % sms
+    if rem == 0 or rem > 224 or T < 32:
+        return 0
+    cap = min(512, B * H * ((T + 1) // 2) * min(4, T // 16))
+    best, best_len = 1, 1.0
+    for f in range(2, 5):
+        if f > T // 16 or rem * f > cap:
+            break
+        ln = -(-rem * f // sms) / f
+        if ln < best_len - 1e-12:
+            best, best_len = f, ln
+    return best if best >= 2 else 0
+
+
+# (B, H, N) on 152 SMs: f = 2 (64 items of 32 key tiles), f = 3 (96 items of
+# 64), f = 4 (32 items of 64)
+FP8_SPLIT_SHAPES = [(1, 4, 4096), (1, 3, 8192), (1, 1, 8192)]
+
+
+@pytest.mark.parametrize("B,H,N", FP8_SPLIT_SHAPES)
+def test_fwd_fp8_split_matches_oracle_and_unsplit(B, H, N):
+    """The plain FP8 forward's last wave split over 2-4 CTAs per item (each
+    over its own key tiles, the last to finish merging the parts' O and
+    (m, l)): parity with the oracle, agreement with the unsplit kernel (a
+    256-byte workspace, which has no room for the parts), bit-identical
+    repeats (the merge's order does not depend on which part ends last), and
+    the status block's counters back at zero."""
+    import io_aware_exact_09_gb300 as fa
+    d = 128
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    f = fp8_split_factor(B, H, N, sms)
+    case = make_case(B, H, N, d, seed=H * 7 + N)
+    dev = lambda t: t.cuda().contiguous()
+    Q, K, V = dev(case["Q"]), dev(case["K"]), dev(case["V"])
+    need = fa.fa_fwd_workspace_size(B, H, N, d)
+    assert need > 256
+    ws = fa.workspace(need, "cuda")
+    O, L = fa.attention_forward_fp8(Q, K, V, case["scale"], False, ws=ws, check_status=True)
+    torch.cuda.synchronize()
+    assert int(ws[32:256].view(torch.int32).abs().sum()) == 0, f
+    if f >= 2:
+        assert int((ws[256:] != 0).sum()) > 0, f              # the parts' slots were written: the split ran
+    for _ in range(3):
+        O2, L2 = fa.attention_forward_fp8(Q, K, V, case["scale"], False, ws=ws)
+        assert torch.equal(O, O2) and torch.equal(L, L2), f
+    assert fa.fa_get_device_status(ws) == 0
+    assert int(ws[32:256].view(torch.int32).abs().sum()) == 0
+    ws0 = fa.workspace(256, "cuda")
+    O0, L0 = fa.attention_forward_fp8(Q, K, V, case["scale"], False, ws=ws0, check_status=True)
+    On, Ln, O0n, L0n = (t.double().cpu().numpy() for t in (O, L, O0, L0))
+    # each part rounds its probabilities to e4m3 against its own running
+    # maximum, so O agrees with the unsplit kernel's within the FP8 bound (not
+    # bit for bit); LSE sums unrounded probabilities: fp32 rounding only
+    assert rel_fro(On, O0n) <= FP8_O_REL_FRO, ("split vs unsplit", f, rel_fro(On, O0n))
+    assert np.max(np.abs(Ln - L0n)) <= 1e-4, ("split vs unsplit LSE", f, np.max(np.abs(Ln - L0n)))
+    Qh, Kh, Vh = dequantized(case)
+    rO, rL = oracle.attention_fwd(Qh, Kh, Vh, case["scale"], causal=False)
+    check_fp8(On, Ln, rO, rL, Vh, ("split", f))
+
+
+def test_fwd_fp8_split_plan_covers_the_intended_factors():
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    fs = [fp8_split_factor(B, H, N, sms) for B, H, N in FP8_SPLIT_SHAPES]
+    if sms == 152:
+        assert fs == [2, 3, 4], fs
+    # 8 key tiles per part would be too short: B4 H16 N4096 does not split
+    assert fp8_split_factor(4, 16, 4096, 152) == 0
+    # the long-context shape: 1,024 items, 112 past six waves of 152 -> 4 parts each
+    assert fp8_split_factor(1, 16, 16384, 152) == 4
