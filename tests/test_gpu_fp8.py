@@ -295,3 +295,29 @@ def test_fwd_fp8_split_plan_covers_the_intended_factors():
     assert fp8_split_factor(4, 16, 4096, 152) == 0
     # the long-context shape: 1,024 items, 112 past six waves of 152 -> 4 parts each
     assert fp8_split_factor(1, 16, 16384, 152) == 4
+
+
+def test_fwd_fp8_full_size_sampled():
+    """The long-context workload at full size, as the benchmark runs it (its
+    last wave split four ways): sampled query rows of the first and last
+    head and of random heads against the oracle's rows of the dequantised
+    inputs."""
+    import io_aware_exact_09_gb300 as fa
+    from test_gpu_fullsize import sample_rows
+    w = WORKLOADS["longctx_b1h16n16384d128"]
+    case = make_inputs(w)
+    B, H, N, d = w.B, w.H, w.N, w.d
+    dev = lambda t: t.cuda().contiguous()
+    O, L = fa.attention_forward_fp8(dev(case["Q"]), dev(case["K"]), dev(case["V"]), case["scale"], False,
+                                    check_status=True)
+    torch.cuda.synchronize()
+    rows, _ = sample_rows(B, H, N, np.random.default_rng(99))
+    Qh, Kh, Vh = dequantized(case)
+    O_r, L_r, _ = oracle.query_rows(Qh, Kh, Vh, None, case["scale"], rows)
+    gO = O.double().cpu().numpy().reshape(B * H * N, d)[rows]
+    gL = L.double().cpu().numpy().reshape(-1)[rows]
+    assert np.all(np.isfinite(gO))
+    e = rel_fro(gO, O_r)
+    assert e <= FP8_O_REL_FRO, e
+    assert np.max(np.abs(gO - O_r)) <= fp8_max_abs(Vh), np.max(np.abs(gO - O_r))
+    assert np.max(np.abs(gL - L_r)) <= LSE_MAX_ABS, np.max(np.abs(gL - L_r))
