@@ -130,8 +130,15 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
         int si = 0;
         if (split_part(&si) >= 0) item = p.split_from + si;
     }
-    const int kt = item % p.Tk;
-    const int bh = item / p.Tk;
+    // head-major (every key tile of a head, then the next head), or, when the
+    // items differ in length and the host asks for it, spread: key tile 0 of
+    // every head first, then key tile 1, ..., so that the blocks the hardware
+    // dispatches last are the shortest of all (under the causal mask key tile
+    // kt sees T - kt query blocks; head-major puts the last head's longest at
+    // the end)
+    const bool spread = !VARLEN && !PLAIN && p.spread;
+    const int kt = spread ? item / p.BH : item % p.Tk;
+    const int bh = spread ? item % p.BH : item / p.Tk;
     const int b = bh / p.H, h = bh % p.H;
     const int k0 = kt * kTile;
     const int nb = (p.N + kTile - 1) / kTile;
