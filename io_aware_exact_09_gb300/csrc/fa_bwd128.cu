@@ -130,15 +130,23 @@ __global__ void __launch_bounds__(512, 1) fa_bwd128_kernel(const __grid_constant
         int si = 0;
         if (split_part(&si) >= 0) item = p.split_from + si;
     }
-    // head-major (every key tile of a head, then the next head), or, when the
-    // items differ in length and the host asks for it, spread: key tile 0 of
-    // every head first, then key tile 1, ..., so that the blocks the hardware
-    // dispatches last are the shortest of all (under the causal mask key tile
-    // kt sees T - kt query blocks; head-major puts the last head's longest at
-    // the end)
-    const bool spread = !VARLEN && !PLAIN && p.spread;
-    const int kt = spread ? item / p.BH : item % p.Tk;
-    const int bh = spread ? item % p.BH : item / p.Tk;
+    // Block order.  Every tile full (PLAIN): head-major, every key tile of a
+    // head, then the next head.  Under a mask the items differ in length (the
+    // causal mask gives key tile kt T - kt query blocks), and head-major would
+    // dispatch the last head's longest near the end; so the heads go in groups
+    // of kGroup, key-tile-major inside a group (key tile 0 of the group's heads,
+    // then key tile 1, ...): the last blocks dispatched are the last group's
+    // shortest, and the CTAs at work at one time touch about kGroup heads, so
+    // their Q, dO, LSE and D stay shared in L2 as in head-major order.
+    constexpr int kGroup = 8;
+    int kt = item % p.Tk, bh = item / p.Tk;
+    if (!VARLEN && !PLAIN) {
+        const int per = p.Tk * kGroup;
+        const int gi = item / per, i = item - gi * per;
+        const int gs = min(kGroup, p.BH - gi * kGroup);      // the last group may be smaller
+        kt = i / gs;
+        bh = gi * kGroup + (i - kt * gs);
+    }
     const int b = bh / p.H, h = bh % p.H;
     const int k0 = kt * kTile;
     const int nb = (p.N + kTile - 1) / kTile;

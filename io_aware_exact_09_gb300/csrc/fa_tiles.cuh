@@ -156,10 +156,9 @@ struct BwdParams {
     int causal;
     float scale_log2;                // softmax_scale * log2(e)
     float scale;                     // softmax_scale
-    int spread;                      // items (key tile, b*h) taken (d = 64, persistent grid) or
-                                     // numbered (d = 128) key-tile-major across heads (key tile 0 of
-                                     // every head first), else head-major; set when the items differ
-                                     // in length
+    int spread;                      // d = 64 persistent grid: items (key tile, b*h) taken
+                                     // key-tile-major across heads (key tile 0 of every head first),
+                                     // else head-major; set when the items differ in length
     // d = 128, every tile full: the items (key tile, b*h) from split_from on
     // are each run as split_f CTAs over consecutive ranges of query blocks
     // (split_f < 2: none).  Part j of item split_from + t writes its fp32 dK
