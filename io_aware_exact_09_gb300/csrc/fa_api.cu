@@ -691,7 +691,8 @@ fa_status fa_decode(const void *Q, const void *K, const void *V, void *O, float 
     DecParams p;
     std::memset(&p, 0, sizeof(p));
     if (!encode_bf16_3d(&p.tmQ, Q, d, Nq, (int)BH, 128) || !encode_bf16_3d(&p.tmK, K, d, Nk, (int)BH, 128) ||
-        !encode_bf16_3d(&p.tmV, V, d, Nk, (int)BH, 128))
+        !encode_bf16_3d(&p.tmV, V, d, Nk, (int)BH, 128) ||
+        (Nq <= 32 && !encode_bf16_3d(&p.tmQs, Q, d, Nq, (int)BH, 32)))
         return FA_ERR_CUDA;
     p.Opart = Opart;
     p.Lpart = Lpart;

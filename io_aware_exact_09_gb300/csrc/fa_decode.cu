@@ -68,7 +68,14 @@ __device__ __forceinline__ void dec_drain_wait(uint32_t bar, uint32_t parity) {
 
 }  // namespace
 
-template <int D>
+// QTR (2 <= Nq <= 32, one query tile): the query rows are loaded into all four
+// 32-row quarters of the tile, and softmax warp k takes key columns
+// [32 k, 32 k + 32) of every key tile for its copy, with running statistics
+// of its own; the epilogue merges the four partial rows of each query
+// (the block-merge identity of "FlashAttention: Mathematical Foundations
+// ...", "Incremental Online Updates").  One warp's softmax over whole
+// 128-key rows, four of them real, was the chain each key tile waited on.
+template <int D, bool QTR>
 __global__ void __launch_bounds__(256, 1) fa_decode_kernel(const __grid_constant__ DecParams p) {
     grid_dep_wait();                                 // the previous kernel in the stream is done
     grid_dep_launch();
@@ -148,8 +155,16 @@ __global__ void __launch_bounds__(256, 1) fa_decode_kernel(const __grid_constant
             int it = 0;
             bool ok = true;
             mbar_arrive_expect_tx_elect(bar(S::B_QFULL), S::TILE_BYTES);
-            for (int c = 0; c < S::CHUNKS; ++c)
-                tma_load_3d_elect(base + S::OFF_Q + c * S::CHUNK_BYTES, &p.tmQ, bar(S::B_QFULL), c * 64, q0, bh);
+            if constexpr (QTR) {
+                // rows 0..31 of the queries into each quarter (a 32-row offset keeps the 128-byte swizzle)
+                for (int cp = 0; cp < 4; ++cp)
+                    for (int c = 0; c < S::CHUNKS; ++c)
+                        tma_load_3d_elect(base + S::OFF_Q + c * S::CHUNK_BYTES + cp * 32 * 128, &p.tmQs,
+                                          bar(S::B_QFULL), c * 64, 0, bh);
+            } else {
+                for (int c = 0; c < S::CHUNKS; ++c)
+                    tma_load_3d_elect(base + S::OFF_Q + c * S::CHUNK_BYTES, &p.tmQ, bar(S::B_QFULL), c * 64, q0, bh);
+            }
             for (int kt = first; kt < kt_end; kt = next_tile(kt), ++it) {
                 const int s = it % S::STAGES;
                 const uint32_t ph = (uint32_t)(it / S::STAGES) & 1u;
@@ -235,8 +250,8 @@ __global__ void __launch_bounds__(256, 1) fa_decode_kernel(const __grid_constant
     } else if (warp >= 4) {
         // ---------------------------------------------------------- softmax
         const int wq = warp & 3;
-        const int r = wq * 32 + lane;
-        const int q = q0 + r;
+        const int r = wq * 32 + lane;                // TMEM lane / tile row
+        const int q = QTR ? lane : q0 + r;           // the query row (QTR: copy wq of query `lane`)
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const uint32_t o_tmem = tmem + lane_off + S::TM_O;
         const float c2 = p.scale_log2;
@@ -245,7 +260,7 @@ __global__ void __launch_bounds__(256, 1) fa_decode_kernel(const __grid_constant
         bool ok = true;
         // a warp whose 32 rows all lie past Nq has nothing to compute: its P
         // rows only feed output rows that are never stored
-        const bool active = q0 + wq * 32 < p.Nq;
+        const bool active = QTR || q0 + wq * 32 < p.Nq;
         for (int kt = first; kt < kt_end; kt = next_tile(kt), ++it) {
             if (!active) {
                 if (!mbar_wait_warp(bar(S::B_SFULL + (it & 1)), (uint32_t)(it >> 1) & 1u, g, 0x521)) {
@@ -263,77 +278,152 @@ __global__ void __launch_bounds__(256, 1) fa_decode_kernel(const __grid_constant
             }
             tc_fence_after();
             const uint32_t s_tmem = tmem + lane_off + S::TM_S + (uint32_t)(it & 1) * 128u;
-            uint32_t sr[4][32];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) tmem_ld32(s_tmem + 32u * j, sr[j]);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) tmem_ld_wait(sr[j]);
-            if (partial) {
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
+            if constexpr (QTR) {
+                // key columns [32 wq, 32 wq + 32) of this tile for query `lane`
+                uint32_t sr[32];
+                tmem_ld32(s_tmem + 32u * wq, sr);
+                tmem_ld_wait(sr);
+                if (partial) {
 #pragma unroll
                     for (int t = 0; t < 32; ++t) {
-                        const int key = k0 + 32 * j + t;
-                        if (key >= kvis || (p.causal && key > q + shift)) sr[j][t] = __float_as_uint(-INFINITY);
+                        const int key = k0 + 32 * wq + t;
+                        if (key >= kvis || (p.causal && key > q + shift)) sr[t] = __float_as_uint(-INFINITY);
                     }
-            }
-            float pm[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) pm[u] = -INFINITY;
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-#pragma unroll
-                for (int t = 0; t < 32; t += 4) {
-                    const int u = (j * 8 + t / 4) & 7;
-                    pm[u] = fmax3(pm[u], __uint_as_float(sr[j][t]), __uint_as_float(sr[j][t + 1]));
-                    pm[u] = fmax3(pm[u], __uint_as_float(sr[j][t + 2]), __uint_as_float(sr[j][t + 3]));
                 }
-            const float m_tile = c2 * fmaxf(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], fmax3(pm[5], pm[6], pm[7])));
-            const bool rescale = __any_sync(0xffffffffu, m_tile > m_ref + kDecRescaleLog2);
-            float alpha = 1.f;
-            if (rescale) {
-                const float m_new = fmaxf(m_ref, m_tile);
-                alpha = (m_new == -INFINITY) ? 1.f : ex2(m_ref - m_new);
-                l *= alpha;
-                m_ref = m_new;
-            }
-            const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-            float ps[8];
+                float pm[4];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) ps[u] = 0.f;
+                for (int u = 0; u < 4; ++u) pm[u] = -INFINITY;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                uint32_t pk[16];
+                for (int t = 0; t < 32; t += 8) {
+                    const int u = t / 8;
+                    pm[u] = fmax3(pm[u], __uint_as_float(sr[t]), __uint_as_float(sr[t + 1]));
+                    pm[u] = fmax3(pm[u], __uint_as_float(sr[t + 2]), __uint_as_float(sr[t + 3]));
+                    pm[u] = fmax3(pm[u], __uint_as_float(sr[t + 4]), __uint_as_float(sr[t + 5]));
+                    pm[u] = fmax3(pm[u], __uint_as_float(sr[t + 6]), __uint_as_float(sr[t + 7]));
+                }
+                const float m_tile = c2 * fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3]));
+                const bool rescale = __any_sync(0xffffffffu, m_tile > m_ref + kDecRescaleLog2);
+                float alpha = 1.f;
+                if (rescale) {
+                    const float m_new = fmaxf(m_ref, m_tile);
+                    alpha = (m_new == -INFINITY) ? 1.f : ex2(m_ref - m_new);
+                    l *= alpha;
+                    m_ref = m_new;
+                }
+                const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+                float ps[4] = {0.f, 0.f, 0.f, 0.f};
+                uint32_t pk[16], zero[16];
 #pragma unroll
                 for (int t = 0; t < 16; ++t) {
                     float a, bb;
-                    fma2(a, bb, __uint_as_float(sr[j][2 * t]), __uint_as_float(sr[j][2 * t + 1]), c2, c2, -m_use, -m_use);
+                    fma2(a, bb, __uint_as_float(sr[2 * t]), __uint_as_float(sr[2 * t + 1]), c2, c2, -m_use, -m_use);
                     a = ex2(a);
                     bb = ex2(bb);
-                    const int u = 2 * (t & 3);
+                    const int u = 2 * (t & 1);
                     add2(ps[u], ps[u + 1], a, bb);
                     pk[t] = pack_bf16x2(a, bb);
+                    zero[t] = 0u;
                 }
-                tmem_st16(s_tmem + 16u * j, pk);
-            }
-            l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-            tmem_st_wait();
-            if (rescale && it > 0) {
-                if (!mbar_wait_warp(bar(S::B_PVDONE + ((it - 1) & 1)), (uint32_t)((it - 1) >> 1) & 1u, g, 0x522)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-#pragma unroll 1
-                for (int j = 0; j < D / 32; ++j) {
-                    uint32_t o[32];
-                    tmem_ld32(o_tmem + 32u * j, o);
-                    tmem_ld_wait(o);
+                // this row's P: its own 32 keys, zero for the other quarters' keys
 #pragma unroll
-                    for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * alpha);
-                    tmem_st32(o_tmem + 32u * j, o);
+                for (int j = 0; j < 4; ++j) {
+                    if (j == wq)                     // warp-uniform
+                        tmem_st16(s_tmem + 16u * j, pk);
+                    else
+                        tmem_st16(s_tmem + 16u * j, zero);
                 }
+                l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
                 tmem_st_wait();
+                if (rescale && it > 0) {
+                    if (!mbar_wait_warp(bar(S::B_PVDONE + ((it - 1) & 1)), (uint32_t)((it - 1) >> 1) & 1u, g, 0x522)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int j = 0; j < D / 32; ++j) {
+                        uint32_t o[32];
+                        tmem_ld32(o_tmem + 32u * j, o);
+                        tmem_ld_wait(o);
+#pragma unroll
+                        for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * alpha);
+                        tmem_st32(o_tmem + 32u * j, o);
+                    }
+                    tmem_st_wait();
+                }
+            } else {
+                uint32_t sr[4][32];
+    #pragma unroll
+                for (int j = 0; j < 4; ++j) tmem_ld32(s_tmem + 32u * j, sr[j]);
+    #pragma unroll
+                for (int j = 0; j < 4; ++j) tmem_ld_wait(sr[j]);
+                if (partial) {
+    #pragma unroll
+                    for (int j = 0; j < 4; ++j)
+    #pragma unroll
+                        for (int t = 0; t < 32; ++t) {
+                            const int key = k0 + 32 * j + t;
+                            if (key >= kvis || (p.causal && key > q + shift)) sr[j][t] = __float_as_uint(-INFINITY);
+                        }
+                }
+                float pm[8];
+    #pragma unroll
+                for (int u = 0; u < 8; ++u) pm[u] = -INFINITY;
+    #pragma unroll
+                for (int j = 0; j < 4; ++j)
+    #pragma unroll
+                    for (int t = 0; t < 32; t += 4) {
+                        const int u = (j * 8 + t / 4) & 7;
+                        pm[u] = fmax3(pm[u], __uint_as_float(sr[j][t]), __uint_as_float(sr[j][t + 1]));
+                        pm[u] = fmax3(pm[u], __uint_as_float(sr[j][t + 2]), __uint_as_float(sr[j][t + 3]));
+                    }
+                const float m_tile = c2 * fmaxf(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], fmax3(pm[5], pm[6], pm[7])));
+                const bool rescale = __any_sync(0xffffffffu, m_tile > m_ref + kDecRescaleLog2);
+                float alpha = 1.f;
+                if (rescale) {
+                    const float m_new = fmaxf(m_ref, m_tile);
+                    alpha = (m_new == -INFINITY) ? 1.f : ex2(m_ref - m_new);
+                    l *= alpha;
+                    m_ref = m_new;
+                }
+                const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+                float ps[8];
+    #pragma unroll
+                for (int u = 0; u < 8; ++u) ps[u] = 0.f;
+    #pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    uint32_t pk[16];
+    #pragma unroll
+                    for (int t = 0; t < 16; ++t) {
+                        float a, bb;
+                        fma2(a, bb, __uint_as_float(sr[j][2 * t]), __uint_as_float(sr[j][2 * t + 1]), c2, c2, -m_use, -m_use);
+                        a = ex2(a);
+                        bb = ex2(bb);
+                        const int u = 2 * (t & 3);
+                        add2(ps[u], ps[u + 1], a, bb);
+                        pk[t] = pack_bf16x2(a, bb);
+                    }
+                    tmem_st16(s_tmem + 16u * j, pk);
+                }
+                l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+                tmem_st_wait();
+                if (rescale && it > 0) {
+                    if (!mbar_wait_warp(bar(S::B_PVDONE + ((it - 1) & 1)), (uint32_t)((it - 1) >> 1) & 1u, g, 0x522)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+    #pragma unroll 1
+                    for (int j = 0; j < D / 32; ++j) {
+                        uint32_t o[32];
+                        tmem_ld32(o_tmem + 32u * j, o);
+                        tmem_ld_wait(o);
+    #pragma unroll
+                        for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * alpha);
+                        tmem_st32(o_tmem + 32u * j, o);
+                    }
+                    tmem_st_wait();
+                }
             }
             tc_fence_before();
             mbar_arrive(bar(S::B_PFULL + (it & 1)));
@@ -344,7 +434,76 @@ __global__ void __launch_bounds__(256, 1) fa_decode_kernel(const __grid_constant
             ok = mbar_wait_warp(bar(S::B_PVDONE + ((it - 1) & 1)), (uint32_t)((it - 1) >> 1) & 1u, g, 0x523);
             tc_fence_after();
         }
-        if (ok && active) {
+        if constexpr (QTR) {
+            // merge the four copies of each query row: every softmax thread
+            // stages (m_ref, l) and its unnormalised O row in the K stages'
+            // shared memory (free: every product is done), O as [copy][column
+            // group of 4][row] float4 so that a warp's store covers 512
+            // contiguous bytes; the copy-0 warp then sums the copies in copy
+            // order with weights 2^(m_k - max m).  All 128 softmax threads take
+            // the barrier on every path.
+            float4 *ostg = reinterpret_cast<float4 *>(sb + S::OFF_K);
+            float2 *mstg = reinterpret_cast<float2 *>(sb + S::OFF_K + 4 * (D / 4) * 32 * 16);
+            if (ok) {
+#pragma unroll 1
+                for (int j = 0; j < D / 32; ++j) {
+                    uint32_t o[32];
+                    if (it > 0) {
+                        tmem_ld32(o_tmem + 32u * j, o);
+                        tmem_ld_wait(o);
+                    } else {
+#pragma unroll
+                        for (int t = 0; t < 32; ++t) o[t] = 0u;
+                    }
+#pragma unroll
+                    for (int t = 0; t < 8; ++t)
+                        ostg[(wq * (D / 4) + 8 * j + t) * 32 + lane] =
+                            make_float4(__uint_as_float(o[4 * t]), __uint_as_float(o[4 * t + 1]),
+                                        __uint_as_float(o[4 * t + 2]), __uint_as_float(o[4 * t + 3]));
+                }
+                mstg[wq * 32 + lane] = make_float2(m_ref, l);
+            }
+            named_bar_sync(1, 128);
+            if (ok && wq == 0 && lane < qn) {
+                float mm[4], ll[4], wk[4];
+                float M = -INFINITY;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float2 v = mstg[k * 32 + lane];
+                    mm[k] = v.x;
+                    ll[k] = v.y;
+                    M = fmaxf(M, mm[k]);
+                }
+                float L = 0.f;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    wk[k] = (mm[k] == -INFINITY) ? 0.f : ex2(mm[k] - M);
+                    L += wk[k] * ll[k];
+                }
+                const float inv_l = (L > 0.f) ? 1.f / L : 0.f;
+                const size_t row = ((size_t)sp * p.BH + bh) * p.Nq + q;
+#pragma unroll 1
+                for (int c = 0; c < D / 4; ++c) {
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float4 v = ostg[(k * (D / 4) + c) * 32 + lane];
+                        acc.x = fmaf(wk[k], v.x, acc.x);
+                        acc.y = fmaf(wk[k], v.y, acc.y);
+                        acc.z = fmaf(wk[k], v.z, acc.z);
+                        acc.w = fmaf(wk[k], v.w, acc.w);
+                    }
+                    if (p.O) {
+                        uint2 *dst = reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(p.O) + row * D + 4 * c);
+                        *dst = make_uint2(pack_bf16x2(acc.x * inv_l, acc.y * inv_l), pack_bf16x2(acc.z * inv_l, acc.w * inv_l));
+                    } else {
+                        reinterpret_cast<float4 *>(p.Opart + row * D)[c] =
+                            make_float4(acc.x * inv_l, acc.y * inv_l, acc.z * inv_l, acc.w * inv_l);
+                    }
+                }
+                (p.LSE ? p.LSE : p.Lpart)[row] = (L > 0.f) ? (M + log2f(L)) * 0.69314718055994530942f : -INFINITY;
+            }
+        } else if (ok && active) {
             const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
             const size_t row = ((size_t)sp * p.BH + bh) * p.Nq + q;
 #pragma unroll 1
@@ -433,17 +592,22 @@ __global__ void __launch_bounds__(256) fa_decode_merge_kernel(const float *__res
     if (lane == 0) LSE[row] = wsum > 0.f ? lmax + logf(wsum) : -INFINITY;
 }
 
-template <int D>
+template <int D, bool QTR>
 static cudaError_t launch_decode_t(const DecParams &p, cudaStream_t st) {
     const int smem = DecShape<D>::SMEM_BYTES;
-    cudaError_t e = cudaFuncSetAttribute(fa_decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = cudaFuncSetAttribute(fa_decode_kernel<D, QTR>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)p.Tq * (unsigned)p.BH * (unsigned)p.splits;
-    return launch_dep(fa_decode_kernel<D>, grid, 256, smem, st, p);
+    return launch_dep(fa_decode_kernel<D, QTR>, grid, 256, smem, st, p);
 }
 
 cudaError_t launch_decode(int d, const DecParams &p, cudaStream_t st) {
-    return d == 64 ? launch_decode_t<64>(p, st) : launch_decode_t<128>(p, st);
+    // 2..32 query rows: the quartered softmax (the host encoded tmQs).  One
+    // query row: the whole-row softmax of one warp, which keeps up with HBM
+    // there (the quartered form measured 0.7 % slower: four warps' TMEM traffic)
+    if (p.Nq >= 2 && p.Nq <= 32)
+        return d == 64 ? launch_decode_t<64, true>(p, st) : launch_decode_t<128, true>(p, st);
+    return d == 64 ? launch_decode_t<64, false>(p, st) : launch_decode_t<128, false>(p, st);
 }
 
 cudaError_t launch_decode_merge(int d, const float *Opart, const float *Lpart, void *O, float *LSE, int64_t rows,

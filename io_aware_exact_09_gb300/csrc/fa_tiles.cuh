@@ -122,6 +122,7 @@ struct FwdParams {
 
 struct DecParams {
     CUtensorMap tmQ;                 // [BH][Nq][d] bf16, box {64, 128, 1}
+    CUtensorMap tmQs;                // the same, box {64, 32, 1} (Nq <= 32: the query rows in each quarter)
     CUtensorMap tmK, tmV;            // [BH][Nk][d] bf16, box {64, 128, 1}
     float *Opart;                    // [splits][BH][Nq][d] fp32, each split's normalised output
     float *Lpart;                    // [splits][BH][Nq] fp32, each split's log-sum-exp (-inf: none visible)

@@ -44,6 +44,8 @@ CASES = [
     (1, 2, 130, 777, 64),
     (1, 1, 1, 1, 128),
     (2, 4, 8, 2048, 128),
+    (1, 2, 32, 1500, 64),       # the most query rows of the quartered softmax
+    (1, 1, 33, 600, 128),       # one past it: whole-row softmax, two warps with rows
 ]
 
 
