@@ -221,10 +221,16 @@ const char *fa_status_string(fa_status s) {
 // V); block-sparse B2 H16 N8192 d64 backward 0.315 -> 0.242 ms; a ragged
 // batch of 16 x 16 sequence-heads (329 MB of K and V) was slower spread,
 // 0.501 -> 0.549 ms.
+// When neither holds (non-ragged problems only) the heads go in groups of 8,
+// the items spread across a group's heads and the groups in order, so that
+// the last items handed out are the last group's lightest while the CTAs at
+// work touch about 8 heads.  The value is the group size the kernels map
+// item indices with: every head (spread), 8, or 0 (head-major).
 constexpr double kSpreadL2Bytes = 192.0 * (1 << 20);
-static int spread_items(bool lengths_vary, double bytes, int64_t heads) {
+static int spread_items(bool lengths_vary, double bytes, int64_t heads, bool ragged = false) {
     if (!lengths_vary) return 0;
-    return (bytes <= kSpreadL2Bytes || heads * 4 <= fa::device_sm_count()) ? 1 : 0;
+    if (bytes <= kSpreadL2Bytes || heads * 4 <= fa::device_sm_count()) return (int)heads;
+    return (ragged || heads <= 8) ? 0 : 8;
 }
 
 fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H, int N,
@@ -340,7 +346,7 @@ fa_status fa_fwd_varlen(const void *Q, const void *K, const void *V, void *O, fl
     p.Tk = 0;
     p.causal = causal ? 1 : 0;
     p.scale_log2 = softmax_scale * kLog2e;
-    p.spread = spread_items(true, 4.0 * total_k * H * d, (int64_t)B * H);
+    p.spread = spread_items(true, 4.0 * total_k * H * d, (int64_t)B * H, true);
     return fa::launch_fwd_varlen(d, p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -610,7 +616,7 @@ fa_status fa_bwd_varlen(const void *Q, const void *K, const void *V, const void 
         p.causal = causal ? 1 : 0;
         p.scale_log2 = softmax_scale * kLog2e;
         p.scale = softmax_scale;
-        p.spread = spread_items(true, 4.0 * total_k * H * d + 8.0 * total_q * H * d, (int64_t)B * H);
+        p.spread = spread_items(true, 4.0 * total_k * H * d + 8.0 * total_q * H * d, (int64_t)B * H, true);
         if (fa::launch_bwd_main_varlen(d, p, s) != cudaSuccess) return FA_ERR_CUDA;
     }
     if (total_q > 0 &&

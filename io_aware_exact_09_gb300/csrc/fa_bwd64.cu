@@ -225,8 +225,16 @@ __global__ void __launch_bounds__(512, 1) fa_bwd64_kernel(const __grid_constant_
                     j = __shfl_sync(0xffffffffu, j, 0);
                     if (j >= n_items) break;
                     // item j: head-major, the causally heaviest (lowest) key tile first;
-                    // spread: key tile 0 of every head first, then key tile 1
-                    const int kt = p.spread ? j / p.BH : j % p.Tk, bh = p.spread ? j % p.BH : j / p.Tk;
+                    // else groups of p.spread heads (every head: spread order), key
+                    // tile 0 of a group's heads first, then key tile 1, the groups in order
+                    int kt = j % p.Tk, bh = j / p.Tk;
+                    if (p.spread > 0) {
+                        const int per = p.Tk * p.spread;
+                        const int gi = j / per, i = j - gi * per;
+                        const int gs = min(p.spread, p.BH - gi * p.spread);
+                        kt = i / gs;
+                        bh = gi * p.spread + (i - kt * gs);
+                    }
                     const int b = bh / p.H, h = bh % p.H;
                     int q_start = 0, k_start = 0, Lq = p.N, Lk = p.N;
                     bool bad = false;

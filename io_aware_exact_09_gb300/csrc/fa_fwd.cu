@@ -255,8 +255,17 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                     if (j >= n_items) break;
                     // item j: head-major, the causally heaviest pair of the head first;
                     // spread: the heaviest pair of every head first, then the next
-                    const int pq = Tp - 1 - (p.spread ? j / p.BH : j % Tp);
-                    const int bh = p.spread ? j % p.BH : j / Tp;
+                    int pqi = j % Tp, bh = j / Tp;
+                    if (p.spread > 0) {
+                        // groups of p.spread heads (every head: spread order), items
+                        // spread across a group's heads, the groups in order
+                        const int per = Tp * p.spread;
+                        const int gi = j / per, i = j - gi * per;
+                        const int gs = min(p.spread, p.BH - gi * p.spread);
+                        pqi = i / gs;
+                        bh = gi * p.spread + (i - pqi * gs);
+                    }
+                    const int pq = Tp - 1 - pqi;
                     const int b = bh / p.H, h = bh % p.H;
                     int q_start = 0, k_start = 0, Lq = p.N, Lk = p.N;
                     bool bad = false;

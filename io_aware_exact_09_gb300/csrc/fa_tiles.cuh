@@ -101,9 +101,9 @@ struct FwdParams {
     int H, N, BH, Tq, Tk;
     int causal;
     float scale_log2;                // softmax_scale * log2(e)
-    int spread;                      // persistent grid: items handed out query-tile-pair-major across
-                                     // heads (heaviest pairs of every head first), else head-major;
-                                     // set when the items differ in length
+    int spread;                      // persistent grid: 0 head-major, else the items handed out in
+                                     // groups of `spread` heads (every head: the heaviest pairs of
+                                     // every head first), pair-major inside a group
     // FP8 forward, every tile full: the items (query-tile pair, b*h) from
     // split_from on are each run as split_f CTAs over consecutive ranges of key
     // tiles (split_f < 2: none).  Part j of item split_from + t writes its
@@ -157,9 +157,9 @@ struct BwdParams {
     int causal;
     float scale_log2;                // softmax_scale * log2(e)
     float scale;                     // softmax_scale
-    int spread;                      // d = 64 persistent grid: items (key tile, b*h) taken
-                                     // key-tile-major across heads (key tile 0 of every head first),
-                                     // else head-major; set when the items differ in length
+    int spread;                      // d = 64 persistent grid: 0 head-major, else items (key tile,
+                                     // b*h) taken in groups of `spread` heads, key-tile-major inside a
+                                     // group (every head: key tile 0 of every head first)
     // d = 128, every tile full: the items (key tile, b*h) from split_from on
     // are each run as split_f CTAs over consecutive ranges of query blocks
     // (split_f < 2: none).  Part j of item split_from + t writes its fp32 dK
