@@ -224,3 +224,34 @@ def test_decode_full_size_sampled(name):
         assert rel_fro(o, rO) <= O_REL_FRO, (name, b, h, rel_fro(o, rO))
         assert np.max(np.abs(o - rO)) <= O_MAX_ABS, (name, b, h)
         assert np.max(np.abs(l - rL)) <= LSE_MAX_ABS, (name, b, h)
+
+
+@pytest.mark.parametrize("B,H,N,d", [(8, 16, 4096, 128), (16, 16, 2048, 64)])
+def test_grouped_item_order_sampled(B, H, N, d):
+    """Masked shapes past the spread rule (working set beyond L2, many heads):
+    the persistent forward (8 x 16 x 4096 x 128) and the d = 64 backward
+    (16 x 16 x 2048 x 64) hand out their items in groups of 8 heads, and the
+    d = 128 backward numbers its blocks the same way.  Sampled query rows (O,
+    LSE, dQ) and key rows (dK, dV) of the first, the last and random heads
+    against the oracle."""
+    case = make_case(B, H, N, d, seed=B * H + N + d, causal=True)
+    case["scale"] = 1.0 / d ** 0.5
+    got = run_cuda(case)
+    rng = np.random.default_rng(11)
+    qrows, _ = sample_rows(B, H, N, rng, n_heads=3, per_head=16)
+    Q, K, V, dO = (f64(case[k]) for k in ("Q", "K", "V", "dO"))
+    oa = oracle_args(case)
+    O_r, L_r, dQ_r = oracle.query_rows(Q, K, V, dO, case["scale"], qrows, **oa)
+    flat = lambda X: X.reshape(B * H * N, -1)
+    gO, gL, gdQ = flat(got["O"])[qrows], got["LSE"].reshape(-1)[qrows], flat(got["dQ"])[qrows]
+    assert rel_fro(gO, O_r) <= O_REL_FRO, rel_fro(gO, O_r)
+    assert np.max(np.abs(gO - O_r)) <= O_MAX_ABS
+    assert np.max(np.abs(gL - L_r)) <= LSE_MAX_ABS
+    assert rel_fro(gdQ, dQ_r) <= GRAD_REL_FRO, rel_fro(gdQ, dQ_r)
+    krows, _ = sample_rows(B, H, N, np.random.default_rng(13), n_heads=3, per_head=8)
+    dK_r, dV_r = oracle.key_rows(Q, K, V, dO, case["scale"], krows, **oa)
+    gdK, gdV = flat(got["dK"])[krows], flat(got["dV"])[krows]
+    assert rel_fro(gdK, dK_r) <= GRAD_REL_FRO, rel_fro(gdK, dK_r)
+    assert rel_fro(gdV, dV_r) <= GRAD_REL_FRO, rel_fro(gdV, dV_r)
+    for k in ("O", "dQ", "dK", "dV"):
+        assert np.all(np.isfinite(got[k])), k
