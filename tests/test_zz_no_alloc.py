@@ -82,3 +82,32 @@ def test_noalloc_matches_workspace_backward_twice(d):
             assert orel(got, ref) <= GRAD_REL_FRO, (call, name, "oracle", orel(got, ref))
         # dK and dV are not accumulated across CTAs: identical to the workspace path
         assert torch.equal(dK, rK) and torch.equal(dV, rV), call
+
+
+@pytest.mark.gpu
+def test_noalloc_plain_d128_uses_the_split_and_matches():
+    """d = 128 with every tile full: the built-in array holds the split area
+    for this size (the last wave's key tiles run in parts), so fa_bwd_noalloc
+    takes the same plan as fa_bwd with a full workspace: dK and dV bit for
+    bit, dQ within the parity bound, every output against the oracle too;
+    twice, since the split's counters must be back at zero for the next
+    call."""
+    fa.build()
+    B, H, N, d = 1, 2, 1024, 128
+    c = make_case(B, H, N, d, seed=91)
+    scale = 1.0 / d ** 0.5
+    Q, K, V, dO = (c[k].cuda() for k in ("Q", "K", "V", "dO"))
+    O, LSE = fa.attention_forward(Q, K, V, scale, False, check_status=True)
+    rQ, rK, rV = fa.attention_backward(Q, K, V, O, LSE, dO, scale, False, check_status=True)
+    f64 = lambda t: t.to(torch.float64).numpy()
+    _, _, odQ, odK, odV = oracle.attention_bwd(f64(c["Q"]), f64(c["K"]), f64(c["V"]), f64(c["dO"]), scale)
+    orel = lambda got, ref: float(np.linalg.norm(got.double().cpu().numpy() - ref) / np.linalg.norm(ref))
+    for call in range(2):
+        dQ, dK, dV = (torch.full_like(Q, float("nan")) for _ in range(3))
+        st = fa.fa_bwd_noalloc(Q, K, V, O, LSE, dO, dQ, dK, dV, B, H, N, d, scale, False, None, None)
+        assert st == 0, fa.fa_status_string(st)
+        torch.cuda.synchronize()
+        assert torch.equal(dK, rK) and torch.equal(dV, rV), call
+        assert rel_fro(dQ, rQ) <= GRAD_REL_FRO, call
+        for got, ref, name in ((dQ, odQ, "dQ"), (dK, odK, "dK"), (dV, odV, "dV")):
+            assert orel(got, ref) <= GRAD_REL_FRO, (call, name, orel(got, ref))
