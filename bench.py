@@ -188,14 +188,43 @@ def pick_peak(peaks, clk):
     return sustained, "bf16_tflops_sustained (SM clock below its maximum or not recorded)"
 
 
+def strip_comments(src: str) -> str:
+    """C++ source without its comments (// to the end of the line, /* ... */),
+    string and character literals kept as they are; the line breaks stay."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            j = n if j < 0 else j + 2
+            out.append("\n" * src.count("\n", i, j))
+            i = j
+        else:
+            out.append(c)
+            i += 1
+    return "".join(out)
+
+
 def source_digest(fname) -> str:
     """Digest of a kernel's source file(s) (a name or a tuple of names) and the
-    shared device headers."""
+    shared device headers, over the code lines alone (comments, trailing blanks
+    and empty lines left out): a change to a comment leaves the compiled
+    kernel, and so its ncu record, as it was."""
     h = hashlib.sha256()
     files = {fname} if isinstance(fname, str) else set(fname)
     for f in sorted(files | {"fa_ptx.cuh", "fa_tiles.cuh"}):
-        with open(os.path.join(ROOT, "io_aware_exact_09_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "io_aware_exact_09_gb300", "csrc", f), encoding="utf-8") as fh:
+            code = [ln.rstrip() for ln in strip_comments(fh.read()).splitlines()]
+            h.update("\n".join(ln for ln in code if ln).encode())
     return h.hexdigest()[:16]
 
 

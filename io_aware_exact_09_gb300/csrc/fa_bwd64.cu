@@ -17,7 +17,8 @@
 //     the workspace (words 2 and 3, left at zero by every launch: the last
 //     CTA to stop taking items resets it), head-major with the causally
 //     heaviest key tile of a head first, or, when the items differ in length,
-//     spread across heads (key tile 0 of every head first) for a short tail;
+//     spread across the heads of a group (8 heads, or all of them: key tile 0
+//     of every head in the group first) for a short tail;
 //   - K and V double-buffered: the next item's tiles load while the current
 //     item computes;
 //   - a dQ-drain warpgroup of its own (TMEM -> swizzled staging -> TMA

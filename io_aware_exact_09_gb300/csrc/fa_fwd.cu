@@ -145,10 +145,11 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 // pair of each head first, and handed out in that order, so the CTAs at work
 // at one time share one head's K and V in L2 and the longest items start
 // first.  When the items differ in length (causal, key padding, block mask,
-// ragged) the host asks for the spread order instead: the heaviest pair of
-// every head, then the next, so that the last items handed out are the
-// shortest of all (head-major would start the last head's heaviest pair near
-// the end, where it runs alone).  The counter resets itself: the last CTA to finish taking items sets
+// ragged) the host asks for a spread order instead: the heads in groups (of
+// 8, or all of them), the heaviest pair of every head in a group, then the
+// next, so that the last items handed out are short (head-major would start
+// the last head's heaviest pair near the end, where it runs alone) while the
+// CTAs at work share the K and V of a few heads only.  The counter resets itself: the last CTA to finish taking items sets
 // it back to zero, so the next launch on the same workspace starts from 0.
 template <int D, bool VARLEN, int BC, int QPC, int MODE>
 __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
@@ -253,8 +254,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                     if (lane == 0) j = (int)atomicAdd(sched, 1u);
                     j = __shfl_sync(0xffffffffu, j, 0);
                     if (j >= n_items) break;
-                    // item j: head-major, the causally heaviest pair of the head first;
-                    // spread: the heaviest pair of every head first, then the next
+                    // item j: head-major, the causally heaviest pair of the head first
                     int pqi = j % Tp, bh = j / Tp;
                     if (p.spread > 0) {
                         // groups of p.spread heads (every head: spread order), items
