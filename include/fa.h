@@ -46,12 +46,13 @@
  *     the workspace and read back with fa_get_device_status().
  *   - The workspace must be zero-filled once before its first use.  Word 0
  *     is the status word, which the library only ever sets, never clears
- *     (fa_reset_device_status() clears it).  The forward kernels hand out
- *     their work items from a counter in words 2 and 3, which every launch
- *     leaves at zero again; the d = 128 backward keeps the counters of its
- *     split key tiles (fa_bwd_workspace_size) in words 8..63, also left at
- *     zero.  After a call that recorded a device-side timeout, zero-fill
- *     the workspace again before reusing it.  A workspace therefore serves one call at a
+ *     (fa_reset_device_status() clears it).  The persistent kernels (the
+ *     forward, the d = 64 backward) hand out their work items from a counter
+ *     in words 2 and 3, which every launch leaves at zero again; the d = 128 backward and the FP8 forward keep
+ *     the counters of their last-wave splits (fa_bwd_workspace_size,
+ *     fa_fwd_workspace_size) in words 8..63, also left at zero.  After a
+ *     call that recorded a device-side timeout, zero-fill the workspace
+ *     again before reusing it.  A workspace therefore serves one call at a
  *     time: calls that may run concurrently (different streams) need
  *     workspaces of their own.
  *   - No entry point throws or exits; there is no CPU fallback.
