@@ -144,7 +144,9 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
         int lim = kvis;
         if (p.causal) lim = min(lim, q0[x] + qn[x]);
         kend[x] = qn[x] > 0 ? (lim + kTile - 1) / kTile : 0;
-        if (PLAIN && khi > 0) kend[x] = khi;
+        // a split part's key tiles end at khi; an empty query tile (the
+        // second of the last pair when the tile count is odd) keeps none
+        if (PLAIN && khi > 0 && qn[x] > 0) kend[x] = khi;
     }
     const int kend_union = max(kend[0], kend[1]);
     // per-query-tile values by selection, so that the arrays stay in registers
