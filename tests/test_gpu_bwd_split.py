@@ -38,8 +38,9 @@ def split_factor(B, H, N, sms):
 
 # (B, H, N) on 152 SMs: every item split into 4 (8 items), 3 parts after one
 # full wave (192 items), 2 parts after one full wave (224 items), every item
-# split into 2 (at least two query blocks per part)
-SHAPES = [(1, 2, 1024), (1, 12, 2048), (1, 28, 1024), (1, 3, 512)]
+# split into 2 (at least two query blocks per part), every item of a two-batch
+# input split into 3 (48 items)
+SHAPES = [(1, 2, 1024), (1, 12, 2048), (1, 28, 1024), (1, 3, 512), (2, 3, 1024)]
 
 
 @pytest.mark.parametrize("B,H,N", SHAPES)
@@ -85,11 +86,11 @@ def test_split_backward_matches_oracle_and_unsplit(B, H, N):
 
 def test_split_plan_covers_the_intended_factors():
     """On this GPU the shapes above take the split factors they are meant to
-    (152 SMs: 4, 3, 2, 2); on another SM count the parity test still holds for
-    whatever plan the launcher makes."""
+    (152 SMs: 4, 3, 2, 2, 3); on another SM count the parity test still holds
+    for whatever plan the launcher makes."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     fs = [split_factor(B, H, N, sms) for B, H, N in SHAPES]
     if sms == 152:
-        assert fs == [4, 3, 2, 2], fs
+        assert fs == [4, 3, 2, 2, 3], fs
     # the long-context shape: 2048 items, 72 past 13 full waves -> 2 parts each
     assert split_factor(1, 16, 16384, 152) == 2

@@ -242,8 +242,9 @@ def fp8_split_factor(B, H, N, sms):
 
 # (B, H, N) on 152 SMs: f = 2 (64 items of 32 key tiles), f = 3 (96 items of
 # 64), f = 4 (32 items of 64), f = 2 with an odd tile count (68 items of 33 key
-# tiles; every head's last pair holds one query tile, and is split too)
-FP8_SPLIT_SHAPES = [(1, 4, 4096), (1, 3, 8192), (1, 1, 8192), (1, 4, 4224)]
+# tiles; every head's last pair holds one query tile, and is split too), f = 2
+# on a two-batch input (64 items of 32)
+FP8_SPLIT_SHAPES = [(1, 4, 4096), (1, 3, 8192), (1, 1, 8192), (1, 4, 4224), (2, 2, 4096)]
 
 
 @pytest.mark.parametrize("B,H,N", FP8_SPLIT_SHAPES)
@@ -291,7 +292,7 @@ def test_fwd_fp8_split_plan_covers_the_intended_factors():
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     fs = [fp8_split_factor(B, H, N, sms) for B, H, N in FP8_SPLIT_SHAPES]
     if sms == 152:
-        assert fs == [2, 3, 4, 2], fs
+        assert fs == [2, 3, 4, 2, 2], fs
     # 8 key tiles per part would be too short: B4 H16 N4096 does not split
     assert fp8_split_factor(4, 16, 4096, 152) == 0
     # the long-context shape: 1,024 items, 112 past six waves of 152 -> 4 parts each
