@@ -1,6 +1,5 @@
 """The C-ABI library loads without a GPU, exports every symbol include/fa.h
 declares, and rejects bad arguments on the host before anything is launched."""
-import ctypes
 import os
 import re
 

@@ -11,7 +11,7 @@ import torch
 
 import oracle
 from synthetic import make_case
-from gpu_common import GRAD_REL_FRO, check_forward, check_grads, f64, oracle_args, rel_fro, to_dev
+from gpu_common import check_forward, check_grads, f64, oracle_args, rel_fro, to_dev
 
 pytestmark = pytest.mark.gpu
 

@@ -5,7 +5,6 @@ the work of all ranks."""
 import os
 import socket
 
-import pytest
 import torch.multiprocessing as mp
 
 
