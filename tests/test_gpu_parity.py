@@ -54,6 +54,18 @@ def test_masks_ragged(d, kind):
 
 
 @pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("kind", ["causal_keylen", "sparse"])
+def test_masks_ten_heads(d, kind):
+    """B * H = 10 under a mask: the d = 128 backward hands out its blocks in
+    groups of 8 heads, so this input has one full group and one of 2."""
+    kw = dict(causal=True, key_len=[384, 200]) if kind == "causal_keylen" else \
+        dict(block_mask=[[1, 0, 1], [1, 1, 0], [0, 1, 1]])
+    c = make_case(2, 5, 384, d, seed=31 + d, **kw)
+    c["scale"] = 1.0 / d ** 0.5
+    compare(c, "B2 H5 %s d=%d" % (kind, d))
+
+
+@pytest.mark.parametrize("d", [64, 128])
 def test_every_mask_combination_n512(d):
     bm = np.ones((4, 4), np.uint8)
     bm[0, 1] = bm[2, 0] = bm[3, 1] = bm[1, 3] = 0
