@@ -226,14 +226,16 @@ def test_decode_full_size_sampled(name):
         assert np.max(np.abs(l - rL)) <= LSE_MAX_ABS, (name, b, h)
 
 
-@pytest.mark.parametrize("B,H,N,d", [(8, 16, 4096, 128), (16, 16, 2048, 64)])
+@pytest.mark.parametrize("B,H,N,d", [(8, 16, 4096, 128), (16, 16, 2048, 64), (5, 20, 4096, 128),
+                                     (7, 13, 4096, 64)])
 def test_grouped_item_order_sampled(B, H, N, d):
     """Masked shapes past the spread rule (working set beyond L2, many heads):
-    the persistent forward (8 x 16 x 4096 x 128) and the d = 64 backward
-    (16 x 16 x 2048 x 64) hand out their items in groups of 8 heads, and the
-    d = 128 backward numbers its blocks the same way.  Sampled query rows (O,
-    LSE, dQ) and key rows (dK, dV) of the first, the last and random heads
-    against the oracle."""
+    the persistent forward (8 x 16 x 4096 x 128, 5 x 20 x 4096 x 128) and the
+    d = 64 backward (16 x 16 x 2048 x 64, 7 x 13 x 4096 x 64) hand out their
+    items in groups of 8 heads, and the d = 128 backward numbers its blocks the
+    same way; with 100 and 91 heads the last group holds 4 and 3.  Sampled
+    query rows (O, LSE, dQ) and key rows (dK, dV) of the first, the last and
+    random heads against the oracle."""
     case = make_case(B, H, N, d, seed=B * H + N + d, causal=True)
     case["scale"] = 1.0 / d ** 0.5
     got = run_cuda(case)
