@@ -36,7 +36,11 @@
  *     shared by every (b, h): the 128 x 128 block (query block r, key block
  *     c) is kept iff block_mask[r * nb + c] != 0 ("Attention" chapter of
  *     learn-kernels.com, block-sparse paragraph: blocks the mask zeroes are
- *     skipped, never loaded).
+ *     skipped, never loaded).  With a block_mask nb may be at most 2048
+ *     (the forward lists a row's key tiles in shared memory; fa_fwd_tiles:
+ *     2048 key tiles of its width), else the call returns
+ *     FA_ERR_UNSUPPORTED, like every argument error before anything is
+ *     enqueued.
  *   - A query row with no visible key gets O = 0, LSE = -inf and contributes
  *     nothing to the gradients.
  *   - stream is a cudaStream_t (NULL = legacy default stream).  Calls are

@@ -136,9 +136,7 @@ fa_status check_sizes(int B, int H, int N, int d, bool *empty) {
 
 bool scale_ok(float s) { return std::isfinite(s) && s > 0.f; }
 
-// The forward lists an item's key tiles in shared memory under a block mask
-// (at most this many tiles per row).
-constexpr int kFwdMaxMaskedKeyTiles = 2048;
+using fa::kFwdMaxMaskedKeyTiles;
 
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -543,6 +541,8 @@ fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, con
     const void *ptrs[] = {Q, K, V, O, LSE, dO, dQ, dK, dV};
     for (const void *x : ptrs)
         if (!x || !aligned16(x)) return FA_ERR_INVALID_ARGUMENT;
+    // the main stage's own check, made here so that a rejected call enqueues nothing
+    if (block_mask && (N + 127) / 128 > kFwdMaxMaskedKeyTiles) return FA_ERR_UNSUPPORTED;
     st = fa_bwd_preprocess(O, dO, B, H, N, d, workspace, workspace_bytes, stream);
     if (st != FA_OK) return st;
     st = fa_bwd_main(Q, K, V, LSE, dO, dK, dV, B, H, N, d, softmax_scale, causal, key_len, block_mask, workspace,
@@ -898,6 +898,7 @@ fa_status fa_attention_host(const void *Q, const void *K, const void *V, const v
     if (!Q || !K || !V || !O || !LSE || (bwd && (!dQ || !dK || !dV))) return FA_ERR_INVALID_ARGUMENT;
     const HostLayout L = host_layout(B, H, N, d, bwd);
     if (!dev_workspace || !aligned16(dev_workspace) || dev_workspace_bytes < L.total) return FA_ERR_WORKSPACE;
+    if (block_mask && (N + 127) / 128 > kFwdMaxMaskedKeyTiles) return FA_ERR_UNSUPPORTED;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t *w = static_cast<uint8_t *>(dev_workspace);
     const size_t nb = ((size_t)N + 127) / 128;

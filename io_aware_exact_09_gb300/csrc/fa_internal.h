@@ -12,6 +12,11 @@ namespace fa {
 // Multiprocessor count of the current device (cached per device).
 int device_sm_count();
 
+// The forward lists an item's key tiles under a block mask in shared memory,
+// at most this many per row (its list capacity); a call with a block mask
+// over more key tiles returns FA_ERR_UNSUPPORTED before enqueuing anything.
+constexpr int kFwdMaxMaskedKeyTiles = 2048;
+
 // Launch with programmatic stream serialisation: the kernel may be scheduled
 // while the previous kernel in the stream drains, and waits for it on the
 // device (grid_dep_wait() in fa_ptx.cuh, the first statement of every kernel

@@ -112,6 +112,7 @@ extern "C" fa_status fa_bwd_noalloc(const void *Q, const void *K, const void *V,
     const void *ptrs[] = {Q, K, V, O, LSE, dO, dQ, dK, dV};
     for (const void *x : ptrs)
         if (!x || !aligned16(x)) return FA_ERR_INVALID_ARGUMENT;
+    if (block_mask && (N + 127) / 128 > fa::kFwdMaxMaskedKeyTiles) return FA_ERR_UNSUPPORTED;
     // what fa_bwd requires (status block, D, accumulator); the d = 128 split
     // area after it is used when the array holds that too
     const size_t need = fa::bwd_base_workspace_bytes(B, H, N, d);

@@ -79,6 +79,32 @@ def test_forward_argument_errors(L):
     assert _fwd(N=0) == 0
 
 
+def test_size_limits(L):
+    """The grids number (b*h) and (tile, b*h) items in 32-bit integers: past
+    INT_MAX the calls return FA_ERR_UNSUPPORTED before touching the GPU; one
+    tile short of it they go on to the next check (a missing workspace).  A
+    block mask is listed per row of at most 2048 key tiles."""
+    assert _fwd(B=1 << 16, H=1 << 16) == 2                       # B*H = 2^32
+    assert _fwd(B=1 << 13, H=1 << 13, N=128 * 32) == 2           # tiles * B*H = 2^31
+    assert _fwd(B=1 << 13, H=1 << 13, N=128 * 31, ws=None) == 3  # 31 * 2^26 < 2^31
+    f = fa.lib().fa_fwd
+    assert f(256, 256, 256, 256, 256, 1, 1, 128 * 2049, 64, 0.125, 0, None, 256, 256, 256, None) == 2
+    b = fa.lib().fa_bwd
+    ok_ws = fa.fa_bwd_workspace_size(1, 1, 128, 64)
+    assert b(256, 256, 256, 256, 256, 256, 256, 256, 256, 1 << 16, 1 << 16, 128, 64, 0.1, 0, None, None, 256,
+             ok_ws, None) == 2
+    assert b(256, 256, 256, 256, 256, 256, 256, 256, 256, 1, 1, 128 * 2049, 64, 0.1, 0, None, 256, 256,
+             1 << 40, None) == 2
+    # the host-buffer path and the no-alloc backward reject it before any CUDA
+    # call (here, without a GPU, any CUDA call would fail with FA_ERR_CUDA)
+    h = fa.lib().fa_attention_host
+    need = fa.fa_host_workspace_size(1, 1, 128 * 2049, 64, 0)
+    assert h(256, 256, 256, None, 256, 256, None, None, None, 1, 1, 128 * 2049, 64, 0.1, 0, None, 256, 256, need,
+             None) == 2
+    n = fa.lib().fa_bwd_noalloc
+    assert n(256, 256, 256, 256, 256, 256, 256, 256, 256, 1, 1, 128 * 2049, 64, 0.1, 0, None, 256, None) == 2
+
+
 def test_backward_and_plan_argument_errors(L):
     b = fa.lib().fa_bwd
     ok_ws = fa.fa_bwd_workspace_size(1, 1, 128, 64)
