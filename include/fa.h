@@ -74,7 +74,8 @@ extern "C" {
 typedef enum {
     FA_OK = 0,
     FA_ERR_INVALID_ARGUMENT = 1,   /* null/misaligned pointer, negative size, bad scale */
-    FA_ERR_UNSUPPORTED = 2,        /* d not in {64, 128}, sizes beyond the 32-bit grid limits */
+    FA_ERR_UNSUPPORTED = 2,        /* d not in {64, 128}, sizes beyond the 32-bit grid limits,
+                                      a block_mask over more than 2048 key tiles */
     FA_ERR_WORKSPACE = 3,          /* workspace NULL or smaller than the call needs (*_workspace_size) */
     FA_ERR_CUDA = 4,               /* a CUDA runtime call or kernel launch failed */
     FA_ERR_DEVICE_TIMEOUT = 5,     /* a device-side wait gave up (kernel returned early) */

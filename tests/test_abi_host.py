@@ -34,6 +34,10 @@ def test_every_declared_symbol_is_exported(L):
 def test_status_strings_and_sizes(L):
     assert fa.fa_status_string(0) == "ok"
     assert "timed out" in fa.fa_status_string(5)
+    # every code the header declares has its own string; anything else is unknown
+    strs = [fa.fa_status_string(c) for c in range(7)]
+    assert len(set(strs)) == 7 and all(x and x != "unknown status" for x in strs), strs
+    assert fa.fa_status_string(7) == fa.fa_status_string(-1) == "unknown status"
     assert fa.fa_tile_size() == 128
     assert fa.fa_fwd_workspace_size(1, 2, 128, 64) == 256
     # status + D [B,H,N] fp32 + dQacc [B,H,N,d] fp32, 256-byte rounded
